@@ -1,0 +1,480 @@
+#!/usr/bin/env python3
+"""Benchmark: split-K decode attention on one GB300 (replicas for N > 1).
+
+Default workload: Llama-3-8B-shaped GQA decode (batch 64, 32 q / 8 KV heads,
+head_dim 128, ragged kv_len uniform in [512, 8192], paged cache with page
+128 and a seeded random page permutation, bf16, auto split-K).  One step is
+one attn_decode call (partition kernel + split-K reduce) over that batch.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+                    [--workload llama3|long_context|mla|tiny]
+
+Prints one JSON line (rank 0).  The metric is achieved HBM bandwidth:
+algorithmic bytes per call (visible K + V, plus q, out and lse) over the
+device time per call, with the KV cache resident in HBM.  The KV cache
+(>= 1.1 GB) is larger than L2 (129 MB), so consecutive calls cannot hit in
+L2; no flush is needed between them.
+
+--impl reference times the fp64 CPU oracle (the only reference there is) on
+the host cores, on a bounded sample of the same workload.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = ("decode-attn achieved HBM GB/s (% of GB300 peak) and µs/call, "
+          "GQA 32q/8kv d128")
+FALLBACK_HBM_GBS = 6800.0
+PROFILE_TRAFFIC = os.path.join(ROOT, "profiles", "traffic.json")
+KERNEL_SOURCES = {
+    "gqa_decode": ["split_flash_decoding_gb300/csrc/gqa_decode.cu",
+                   "split_flash_decoding_gb300/csrc/ptx.cuh",
+                   "split_flash_decoding_gb300/csrc/launch.h"],
+}
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=4000)
+    ap.add_argument("--warmup", type=int, default=50)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default="llama3",
+                    choices=["llama3", "long_context", "mla", "tiny"])
+    ap.add_argument("--partitions", type=int, default=0, help="0 = planner's choice")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    return ap.parse_args()
+
+
+# ---------------------------------------------------------------------------
+# helpers
+# ---------------------------------------------------------------------------
+
+def measured_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), "measured", d
+    except Exception:
+        return FALLBACK_HBM_GBS, "fallback", {}
+
+
+def source_hash(kernel: str) -> str:
+    h = hashlib.sha256()
+    for rel in KERNEL_SOURCES[kernel]:
+        with open(os.path.join(ROOT, rel), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def profiled_traffic(kernel: str, workload: str):
+    """DRAM bytes per launch from a committed ncu capture, if it was taken on
+    the current kernel source; else None."""
+    try:
+        with open(PROFILE_TRAFFIC) as f:
+            d = json.load(f)
+        e = d[kernel][workload]
+        if e.get("source_hash") == source_hash(kernel):
+            return float(e["dram_bytes_per_launch"])
+    except Exception:
+        pass
+    return None
+
+
+class ClockSampler:
+    """nvidia-smi clocks and throttle reasons sampled every 200 ms."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, device_index: int):
+        self.idx = device_index
+        self.proc = None
+        self.lines = []
+        self.t_marks = []
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-i", str(self.idx), "-lms", "200"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.reader = threading.Thread(target=self._read, daemon=True)
+            self.reader.start()
+        except Exception:
+            self.proc = None
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append((time.time(), line.strip()))
+
+    def mark(self):
+        self.t_marks.append(time.time())
+
+    def stop(self):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except Exception:
+                self.proc.kill()
+
+    def summary(self):
+        rows = []
+        for t, line in self.lines:
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                rows.append((t, float(parts[1]), float(parts[2]), parts[5:9]))
+            except ValueError:
+                continue
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"], "samples": 0}
+        t0, t1 = (self.t_marks + [0, 0])[:2]
+        window = [r for r in rows if t0 <= r[0] <= t1 + 0.2] or rows
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in window for i, v in enumerate(r[3])
+                          if v.strip().lower() == "active"})
+        return {"sm_mhz": statistics.median(r[1] for r in window),
+                "sm_max_mhz": max(r[2] for r in window), "reasons": reasons,
+                "samples": len(window)}
+
+
+def build_workload(name: str, device):
+    from split_flash_decoding_gb300 import workloads as W
+    if name == "llama3":
+        return W.llama3_8b_decode(device=device)
+    if name == "long_context":
+        return W.long_context_decode(device=device)
+    if name == "mla":
+        return W.deepseek_v3_mla_decode(device=device)
+    if name == "tiny":
+        return W.tiny_decode(device=device)
+    raise ValueError(name)
+
+
+def algorithmic_bytes(w) -> int:
+    """Visible K + V bytes (each byte once per call), q, out and lse."""
+    hkv = w.num_kv_heads
+    total_keys = sum(w.kv_len_host)
+    if w.is_mla:
+        kv = total_keys * w.dim_qk * 2                 # V is a prefix of K
+    else:
+        kv = total_keys * hkv * (w.dim_qk + w.dim_v) * 2
+    q = w.q.numel() * 2
+    o = w.rows * w.num_q_heads * w.dim_v * 2
+    lse = w.rows * w.num_q_heads * 4
+    return kv + q + o + lse
+
+
+def algorithmic_flops(w) -> int:
+    total_keys = sum(w.kv_len_host)
+    return total_keys * w.num_q_heads * 2 * (w.dim_qk + w.dim_v)
+
+
+# ---------------------------------------------------------------------------
+# the reference arm: the fp64 CPU oracle on the host cores
+# ---------------------------------------------------------------------------
+
+def oracle_sample_time(w, k_host, v_host, seqs):
+    """Run the oracle on every (row, head) of the listed sequences; returns
+    (seconds, bytes those sequences account for, threads)."""
+    import numpy as np
+    import oracle
+    rows = []
+    heads = []
+    for b in seqs:
+        for h in range(w.num_q_heads):
+            rows.append(b)
+            heads.append(h)
+    threads = os.cpu_count() or 1
+    kk = (oracle.KV.paged(k_host, w.page_table.cpu()) if w.page_table is not None
+          else oracle.KV.contiguous(k_host))
+    vv = kk if v_host is None else (oracle.KV.paged(v_host, w.page_table.cpu())
+                                    if w.page_table is not None else oracle.KV.contiguous(v_host))
+    sink = None if w.sink is None else w.sink.cpu()
+    t0 = time.perf_counter()
+    oracle.attention(w.q.cpu(), kk, vv, w.kv_len.cpu(), group=w.group, scale=w.scale,
+                     dim_v=w.dim_v, sink=sink, sample=(np.array(rows), np.array(heads)),
+                     threads=threads)
+    dt = time.perf_counter() - t0
+    hkv = w.num_kv_heads
+    per_key = (w.dim_qk * 2) if w.is_mla else hkv * (w.dim_qk + w.dim_v) * 2
+    nbytes = sum(w.kv_len_host[b] * per_key for b in seqs)
+    nbytes += len(seqs) * w.num_q_heads * (w.dim_qk * 2 + w.dim_v * 2 + 4)
+    return dt, nbytes, threads
+
+
+def host_copies(w):
+    import torch
+    k_host = w.k_cache.cpu()
+    v_host = None if w.v_cache is None else w.v_cache.cpu()
+    torch.cuda.synchronize()
+    return k_host, v_host
+
+
+def choose_sample(w, k_host, v_host, budget_s):
+    """Sequences (in seed order) whose oracle time fits the budget."""
+    t1, _, _ = oracle_sample_time(w, k_host, v_host, [0])
+    per_key = t1 / max(1, w.kv_len_host[0])
+    seqs, est = [], 0.0
+    for b, L in enumerate(w.kv_len_host):
+        c = per_key * max(L, 1)
+        if seqs and est + c > budget_s:
+            break
+        seqs.append(b)
+        est += c
+    return seqs
+
+
+def run_reference(args, rank, world):
+    import torch
+    if rank != 0:
+        return
+    torch.cuda.set_device(0)
+    w = build_workload(args.workload, torch.device("cuda", 0))
+    k_host, v_host = host_copies(w)
+    total_budget = 150.0
+    per_step = total_budget / max(1, args.steps + args.warmup)
+    seqs = choose_sample(w, k_host, v_host, per_step)
+    for _ in range(args.warmup):
+        oracle_sample_time(w, k_host, v_host, seqs)
+    secs, nbytes, threads = 0.0, 0, 1
+    for _ in range(args.steps):
+        dt, nb, threads = oracle_sample_time(w, k_host, v_host, seqs)
+        secs += dt
+        nbytes += nb
+    value = nbytes / secs / 1e9
+    sample = (f"all (row, head) pairs of sequences {seqs[0]}..{seqs[-1]} "
+              f"({len(seqs)} of {w.batch}) per step")
+    line = {
+        "impl": "reference", "metric": METRIC, "value": round(value, 4), "unit": "GB/s",
+        "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": round(secs / max(1, args.steps) * 1e3, 3), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": w.name},
+        "cpu_baseline": {"value": round(value, 4), "unit": "GB/s", "cores": threads,
+                         "kind": "oracle", "sample": sample},
+        "e2e": {"value": round(value, 4), "unit": "GB/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+# ---------------------------------------------------------------------------
+# our arm
+# ---------------------------------------------------------------------------
+
+def run_ours(args, rank, world, dist):
+    import torch
+    from split_flash_decoding_gb300 import attn
+    local = int(os.environ.get("LOCAL_RANK", rank))
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    w = build_workload(args.workload, dev)
+    stream = torch.cuda.Stream(device=dev)
+
+    if w.is_mla:
+        P, ws_bytes = attn.attn_plan_partitions(w.batch, w.rows, w.num_q_heads, 1, w.dim_v,
+                                                w.max_kv_len, args.partitions)
+    else:
+        P, ws_bytes = attn.attn_plan_partitions(w.batch, w.rows, w.num_q_heads,
+                                                w.num_kv_heads, w.dim_v, w.max_kv_len,
+                                                args.partitions)
+    ws = torch.empty(max(ws_bytes, 1), dtype=torch.uint8, device=dev)
+    out = torch.empty((w.rows, w.num_q_heads, w.dim_v), dtype=torch.bfloat16, device=dev)
+    lse = torch.empty((w.rows, w.num_q_heads), dtype=torch.float32, device=dev)
+
+    def call(q=w.q, kv_len=w.kv_len, page_table=w.page_table, o=out, l=lse):
+        if w.is_mla:
+            attn.attn_mla_decode(q, w.k_cache, kv_len, scale=w.scale, max_kv_len=w.max_kv_len,
+                                 dim_v=w.dim_v, page_table=page_table, sink=w.sink,
+                                 num_partitions=P, workspace=ws, out=o, lse=l, stream=stream)
+        else:
+            attn.attn_decode(q, w.k_cache, w.v_cache, kv_len, group=w.group, scale=w.scale,
+                             max_kv_len=w.max_kv_len, page_table=page_table, sink=w.sink,
+                             num_partitions=P, workspace=ws, out=o, lse=l, stream=stream)
+
+    launches_per_call = 1 if P == 1 else 2
+    nbytes = algorithmic_bytes(w)
+    flops = algorithmic_flops(w)
+
+    clocks = ClockSampler(local)
+    if rank == 0:
+        clocks.start()
+    with torch.cuda.stream(stream):
+        for _ in range(max(3, args.warmup)):
+            call()
+    torch.cuda.synchronize(dev)
+    attn.attn_device_error_flags(clear=True)
+
+    # ---- device-timed region: inputs resident in HBM ----
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    if dist is not None:
+        dist.barrier()
+    torch.cuda.synchronize(dev)
+    clocks.mark()
+    t_begin = torch.cuda.Event(enable_timing=True)
+    t_end = torch.cuda.Event(enable_timing=True)
+    t_begin.record(stream)
+    for i in range(args.steps):
+        starts[i].record(stream)
+        call()
+        ends[i].record(stream)
+    t_end.record(stream)
+    torch.cuda.synchronize(dev)
+    clocks.mark()
+    if dist is not None:
+        dist.barrier()
+    total_ms = t_begin.elapsed_time(t_end)
+    per_call_ms = [s.elapsed_time(e) for s, e in zip(starts, ends)]
+    flags = attn.attn_device_error_flags(clear=True)
+    if flags:
+        raise RuntimeError(f"device error flags {flags:#x} during the timed region")
+
+    # ---- end to end through the public API, host buffers ----
+    e2e_steps = max(1, min(args.steps, 200))
+    q_host = w.q.cpu().pin_memory()
+    kvl_host = w.kv_len.cpu().pin_memory()
+    pt_host = None if w.page_table is None else w.page_table.cpu().pin_memory()
+    out_host = torch.empty(out.shape, dtype=out.dtype).pin_memory()
+    lse_host = torch.empty(lse.shape, dtype=lse.dtype).pin_memory()
+    q_dev = torch.empty_like(w.q)
+    kvl_dev = torch.empty_like(w.kv_len)
+    pt_dev = None if pt_host is None else torch.empty_like(w.page_table)
+    h2d = q_host.numel() * 2 + kvl_host.numel() * 4 + (0 if pt_host is None else pt_host.numel() * 4)
+    d2h = out_host.numel() * 2 + lse_host.numel() * 4
+
+    def e2e_step():
+        with torch.cuda.stream(stream):
+            q_dev.copy_(q_host, non_blocking=True)
+            kvl_dev.copy_(kvl_host, non_blocking=True)
+            if pt_dev is not None:
+                pt_dev.copy_(pt_host, non_blocking=True)
+            call(q=q_dev, kv_len=kvl_dev, page_table=pt_dev)
+            out_host.copy_(out, non_blocking=True)
+            lse_host.copy_(lse, non_blocking=True)
+        stream.synchronize()
+
+    for _ in range(3):
+        e2e_step()
+    if dist is not None:
+        dist.barrier()
+    t0 = time.perf_counter()
+    for _ in range(e2e_steps):
+        e2e_step()
+    e2e_s = (time.perf_counter() - t0) / e2e_steps
+    if dist is not None:
+        dist.barrier()
+    clocks.stop()
+
+    # ---- max over ranks ----
+    mean_call_ms = sum(per_call_ms) / len(per_call_ms)
+    vals = torch.tensor([total_ms, mean_call_ms, e2e_s], dtype=torch.float64)
+    if dist is not None:
+        t = vals.to(dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        vals = t.cpu()
+    total_ms, mean_call_ms, e2e_s = [float(x) for x in vals]
+    if rank != 0:
+        return
+
+    ms_per_step = total_ms / args.steps
+    value = world * nbytes / (ms_per_step * 1e-3) / 1e9
+    peak, peak_kind, _ = measured_peaks()
+    achieved = nbytes / (mean_call_ms * 1e-3) / 1e9
+    kernel_key = "gqa_decode" if not w.is_mla else "mla_decode"
+    traffic = profiled_traffic(kernel_key, w.name) if kernel_key in KERNEL_SOURCES else None
+    cpu = None
+    if not args.no_cpu_baseline:
+        k_host, v_host = host_copies(w)
+        seqs = choose_sample(w, k_host, v_host, 20.0)
+        dt, nb, threads = oracle_sample_time(w, k_host, v_host, seqs)
+        cpu = {"value": round(nb / dt / 1e9, 4), "unit": "GB/s", "cores": threads,
+               "kind": "oracle",
+               "sample": f"fp64 oracle over every (row, head) of sequences "
+                         f"{seqs[0]}..{seqs[-1]} ({len(seqs)} of {w.batch}), "
+                         f"{nb / 1e6:.1f} MB of the workload, {dt:.1f} s"}
+    line = {
+        "metric": METRIC,
+        "value": round(value, 2),
+        "unit": "GB/s",
+        "n_gpus": world,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": round(ms_per_step, 5),
+        "us_per_call": round(ms_per_step * 1e3, 2),
+        "hbm_frac": round(value / world / peak, 4),
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "bf16",
+        "data": "synthetic",
+        "config": {
+            "workload": w.name,
+            "batch": w.batch, "num_q_heads": w.num_q_heads, "num_kv_heads": w.num_kv_heads,
+            "head_dim": w.dim_qk, "dim_v": w.dim_v, "page_size": w.page_size,
+            "total_kv_tokens": sum(w.kv_len_host), "max_kv_len": w.max_kv_len,
+            "num_partitions": P, "algorithmic_bytes_per_call": nbytes,
+            "flops_per_call": flops,
+            "l2": "inputs larger than L2: the KV cache read every step exceeds 129 MB; no flush",
+            "parallelism": f"replicas x{world}",
+        },
+        "clocks": clocks.summary(),
+        "e2e": {"value": round(world * nbytes / e2e_s / 1e9, 2), "unit": "GB/s",
+                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+                "us_per_step": round(e2e_s * 1e6, 2),
+                "note": "public Python API per step: H2D of q, kv_len, page table from pinned "
+                        "memory, attn_decode, D2H of out and lse, stream sync; KV cache "
+                        "resident"},
+        "gpu_launches": launches_per_call * args.steps,
+        "roofline": {"bound": "hbm", "achieved": round(achieved, 2), "peak": peak,
+                     "unit": "GB/s", "frac": round(achieved / peak, 4), "traffic": traffic,
+                     "peak_source": f"{peak_kind} hbm_gbs",
+                     "kernel": "attn_decode call (partition kernel + split-K reduce), "
+                               "CUDA events per call on the launch stream"},
+        "cpu_baseline": cpu,
+    }
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    args = parse()
+    rank = int(os.environ.get("RANK", 0))
+    world = int(os.environ.get("WORLD_SIZE", 1))
+    if args.impl == "reference":
+        run_reference(args, rank, world)
+        return
+    dist = None
+    if world > 1:
+        import torch
+        import torch.distributed as tdist
+        torch.cuda.set_device(int(os.environ.get("LOCAL_RANK", rank)))
+        tdist.init_process_group("nccl")
+        dist = tdist
+    try:
+        run_ours(args, rank, world, dist)
+    finally:
+        if dist is not None:
+            dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,212 @@
+/*
+ * attn_decode.h -- C ABI of the GB300 split-K flash-decoding library
+ * (libattn.so).
+ *
+ * Scope: single- and few-token attention of query rows against a KV cache
+ * on one GPU.  The key dimension is split into partitions ("When
+ * num_partitions exceeds 1, each block processes a contiguous slice of the
+ * key dimension and writes partial exp_sum and qk_max statistics for a
+ * subsequent mha_splitk_reduce pass", mha_decoding_single_batch_pipelined,
+ * summary); the partials are merged by a log-sum-exp reduce.
+ *
+ * Conventions shared by every entry point
+ * ---------------------------------------
+ * - Pointers marked "device" are CUDA device (or managed) memory of the
+ *   current device.  The caller owns every buffer.  The library never
+ *   allocates device memory, never synchronises, and enqueues all work on
+ *   the given stream (NULL = legacy default stream).  Calls are
+ *   asynchronous: device-side results are ready once the stream reaches
+ *   them.
+ * - Arguments are validated on the host before anything is launched.  A
+ *   failed check returns a status and launches nothing.  A failed launch
+ *   returns ATTN_ERR_CUDA (the CUDA error is left for cudaGetLastError).
+ * - bf16 for q, K, V and out; fp32 for scale, sink logits, lse and the
+ *   split-K workspace.  All element strides are in elements.
+ * - lse is the natural-log log-sum-exp of the scaled scores, sink
+ *   included; it is -inf for a row with no visible key and no sink (its
+ *   output row is then 0).
+ * - Query head h reads KV head h / group (groups of consecutive query
+ *   heads share one KV head; "group: Number of query heads per KV head
+ *   (GQA group size)", mha_sm100_dispatch, Parameters).
+ * - The number of partitions comes only from host integers, never from
+ *   device data, so a call can be captured in a CUDA graph and replayed
+ *   while the per-sequence lengths change (capture-invariant partition
+ *   ceiling, mha_sm100_dispatch, Args: num_partitions_override).
+ */
+#ifndef ATTN_DECODE_H
+#define ATTN_DECODE_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef struct CUstream_st *attn_stream_t; /* identical to cudaStream_t */
+
+enum {
+    ATTN_OK = 0,
+    ATTN_ERR_INVALID_ARG = 1,  /* null pointer, bad size, inconsistent shape */
+    ATTN_ERR_UNSUPPORTED = 2,  /* valid but not implemented (head dim, page size, ...) */
+    ATTN_ERR_WORKSPACE = 3,    /* workspace missing, misaligned or too small */
+    ATTN_ERR_CUDA = 4,         /* a CUDA runtime/driver call failed */
+    ATTN_ERR_DEVICE = 5        /* a kernel reported a device-side error flag */
+};
+
+/* Largest split-K partition count accepted by every entry point. */
+#define ATTN_MAX_PARTITIONS 1024
+
+/*
+ * One K or V cache operand ("Key/value operand descriptor with dtype and
+ * page size", mha_sm100_dispatch, Parameters: KVType; paged KVCache operand
+ * or contiguous tensor operand, flare_mla_decoding_dispatch, Parameters: k_t).
+ *
+ * Token t of sequence b, KV head kh, channel c is the bf16 element
+ *   base[page * page_stride + (t % page_size) * token_stride
+ *        + kh * head_stride + c]
+ * with page = page_table[b * max_pages + t / page_size] when page_table is
+ * non-NULL (paged cache) and page = b when it is NULL (contiguous cache,
+ * one "page" of page_size >= every kv_len per sequence).
+ *
+ * Requirements: base 16-byte aligned; channels contiguous; page_stride,
+ * token_stride and head_stride multiples of 8 elements (16 bytes);
+ * num_pages = number of pages in the pool (= batch for a contiguous
+ * cache).  For a paged cache page_size must be a power of two >= 8.  Page
+ * table entries must lie in [0, num_pages); entries are read only for
+ * pages that hold tokens < kv_len[b].
+ */
+typedef struct attn_kv {
+    const void *base;          /* device, bf16 */
+    int64_t page_stride;
+    int64_t token_stride;
+    int64_t head_stride;
+    int32_t page_size;
+    int32_t num_pages;
+    const int32_t *page_table; /* device int32 [batch][max_pages], or NULL */
+    int32_t max_pages;         /* row length of page_table */
+    int32_t reserved;          /* must be 0 */
+} attn_kv_t;
+
+/*
+ * attn_plan_partitions -- choose the split-K partition count.
+ *
+ * Follows the automatic partition ladder with an exact override
+ * ("num_partitions_override: Exact split-K partition count to use, or 0 for
+ * the automatic ladder. A non-zero value is honored verbatim",
+ * mha_sm100_dispatch, Args; "num_partitions: Optional explicit split-K
+ * partition count; None selects via heuristic",
+ * flare_mla_decoding_dispatch, Args).
+ *
+ *   num_sms       SMs to plan for; <= 0 queries the current device.
+ *   batch         sequences; num_q_rows total query rows (= batch for
+ *                 single-token decode).
+ *   num_q_heads, num_kv_heads   heads (num_kv_heads = 1 for MLA).
+ *   head_dim_v    output channels (128 for GQA d128, 512 for MLA).
+ *   max_kv_len    host upper bound of every kv_len[b].
+ *   requested     0 = automatic; > 0 = use exactly this many partitions.
+ *   num_partitions  out: partitions P (1 <= P <= ATTN_MAX_PARTITIONS).
+ *   workspace_bytes out: workspace size attn_decode / attn_mla_decode need
+ *                 for this P (0 when P == 1).
+ *
+ * Key slice p of a sequence is [p*C, min((p+1)*C, kv_len)) with
+ * C = ceil(ceil(max_kv_len / P) / 32) * 32; slices past kv_len are empty.
+ * Returns ATTN_OK, ATTN_ERR_INVALID_ARG, or ATTN_ERR_CUDA if the SM count
+ * query fails.  Launches nothing.
+ */
+int attn_plan_partitions(int num_sms, int batch, int num_q_rows, int num_q_heads,
+                         int num_kv_heads, int head_dim_v, int max_kv_len, int requested,
+                         int *num_partitions, size_t *workspace_bytes);
+
+/*
+ * attn_decode -- GQA/MHA decode attention over a paged or contiguous cache
+ * with split-K (mha_decoding_single_batch_pipelined; mha_sm100_dispatch).
+ *
+ *   q          device bf16 [batch][num_q_heads][head_dim] (one query token
+ *              per sequence; "q_arg: Pointer to the query tensor data").
+ *   k, v       cache operands (host structs describing device memory); both
+ *              head_dim wide and sharing one page table layout.
+ *   kv_len     device uint32 [batch]: keys of sequence b ("valid_length:
+ *              Per-row valid KV length pointer").  The cache already holds
+ *              the current token's K/V.
+ *   batch, num_q_heads, group   num_q_heads % group == 0; group <= 8.
+ *   head_dim   64 or 128.
+ *   max_kv_len host upper bound of kv_len ("max_cache_valid_length_arg").
+ *   scale      multiplies Q.K' before the softmax.
+ *   sink       device fp32 [num_q_heads] attention-sink logits, or NULL.
+ *              A sink adds exp(sink[h]) to the softmax normaliser of head h
+ *              and carries no value; it is not multiplied by scale.
+ *   num_partitions  P from attn_plan_partitions (or any 1..MAX).
+ *   workspace  device, 256-byte aligned, >= the planner's workspace_bytes
+ *              for this P; may be NULL when P == 1.  Contents on entry are
+ *              ignored; it holds fp32 partial O, qk_max and exp_sum after.
+ *   out        device bf16 [batch][num_q_heads][head_dim].
+ *   lse        device fp32 [batch][num_q_heads], or NULL.
+ *
+ * Launches the partition kernel (grid: P x num_kv_heads x batch) and, for
+ * P > 1, the split-K reduce.  Returns ATTN_OK or an error status.
+ */
+int attn_decode(const void *q, const attn_kv_t *k, const attn_kv_t *v, const uint32_t *kv_len,
+                int batch, int num_q_heads, int group, int head_dim, int max_kv_len, float scale,
+                const float *sink, int num_partitions, void *workspace, size_t workspace_bytes,
+                void *out, float *lse, attn_stream_t stream);
+
+/*
+ * attn_mla_decode -- multi-head latent attention decode: one KV head whose
+ * rows are dim_qk = 576 wide (512 latent + 64 rope), V = K[:, :dim_v]
+ * with dim_v = 512 ("kv_num_heads: Must be 1 for MLA"; "V is derived as
+ * K[:, :, :depth_v], so V is not loaded separately",
+ * flare_mla_decoding_dispatch, Parameters and Args).
+ *
+ *   q          device bf16 [batch][num_q_heads][dim_qk]; num_q_heads = 128.
+ *   kv         the single cache operand (num_kv_heads = 1).
+ *   kv_len, max_kv_len, scale, sink, num_partitions, workspace,
+ *   workspace_bytes, lse    as for attn_decode.
+ *   out        device bf16 [batch][num_q_heads][dim_v].
+ */
+int attn_mla_decode(const void *q, const attn_kv_t *kv, const uint32_t *kv_len, int batch,
+                    int num_q_heads, int dim_qk, int dim_v, int max_kv_len, float scale,
+                    const float *sink, int num_partitions, void *workspace,
+                    size_t workspace_bytes, void *out, float *lse, attn_stream_t stream);
+
+/*
+ * attn_splitk_reduce -- merge split-K partials by log-sum-exp
+ * (mha_splitk_reduce / mla_splitk_reduce, named in
+ * mha_decoding_single_batch_pipelined, summary, and
+ * flare_mla_decoding_dispatch, summary).
+ *
+ * For each row r and head h, with m_p = ws_m[p][r][h], l_p = ws_l[p][r][h],
+ * O_p = ws_o[p][r][h][:], t = sink[h] (or -inf):
+ *   M = max(max_p m_p, t);  w_p = exp(m_p - M)  (0 when m_p = -inf)
+ *   Z = sum_p w_p l_p + exp(t - M)
+ *   out[r][h][:] = sum_p w_p O_p / Z   (bf16, 0 when Z = 0)
+ *   lse[r][h] = M + ln Z               (-inf when Z = 0)
+ *
+ *   ws_o       device fp32 [num_partitions][rows][num_q_heads][dim_v]
+ *              (unnormalised partial outputs).
+ *   ws_m, ws_l device fp32 [num_partitions][rows][num_q_heads]: partial
+ *              max score (natural-log units, -inf for an empty partition)
+ *              and partial exp-sum relative to it.
+ *   dim_v      a multiple of 4, <= 1024.
+ *   sink       device fp32 [num_q_heads] or NULL.
+ *   out        device bf16 [rows][num_q_heads][dim_v]; lse device fp32
+ *              [rows][num_q_heads] or NULL.
+ */
+int attn_splitk_reduce(const float *ws_o, const float *ws_m, const float *ws_l,
+                       int num_partitions, int rows, int num_q_heads, int dim_v,
+                       const float *sink, void *out, float *lse, attn_stream_t stream);
+
+/*
+ * attn_device_error_flags -- read (and optionally clear) the device-side
+ * error word that kernels set instead of hanging: bit 0 = a pipeline wait
+ * ran past its time limit, bit 1 = a page-table entry outside
+ * [0, num_pages) was seen (that tile was skipped).  Synchronises the
+ * current device.  Returns ATTN_OK or ATTN_ERR_CUDA.
+ */
+int attn_device_error_flags(unsigned int *flags, int clear);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* ATTN_DECODE_H */

@@ -1,0 +1,243 @@
+"""Python binding of libattn.so (argument marshalling only).
+
+Every step of the attention path runs in the library's CUDA kernels; this
+module converts torch tensors into the pointers, sizes and cache
+descriptors that the C ABI (include/attn_decode.h) takes, and turns
+non-zero status codes into exceptions.  PyTorch supplies device memory
+(including the split-K workspace) and the current stream.  There is no CPU
+fallback: if libattn.so has not been built, importing the library fails.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+from typing import Optional
+
+import torch
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "libattn.so")
+
+ATTN_OK = 0
+ATTN_ERR_INVALID_ARG = 1
+ATTN_ERR_UNSUPPORTED = 2
+ATTN_ERR_WORKSPACE = 3
+ATTN_ERR_CUDA = 4
+ATTN_ERR_DEVICE = 5
+ATTN_MAX_PARTITIONS = 1024
+
+_STATUS_NAMES = {
+    ATTN_ERR_INVALID_ARG: "ATTN_ERR_INVALID_ARG",
+    ATTN_ERR_UNSUPPORTED: "ATTN_ERR_UNSUPPORTED",
+    ATTN_ERR_WORKSPACE: "ATTN_ERR_WORKSPACE",
+    ATTN_ERR_CUDA: "ATTN_ERR_CUDA",
+    ATTN_ERR_DEVICE: "ATTN_ERR_DEVICE",
+}
+
+
+class AttnError(RuntimeError):
+    def __init__(self, fn: str, status: int):
+        super().__init__(f"{fn} returned {_STATUS_NAMES.get(status, status)}")
+        self.status = status
+
+
+class attn_kv_t(ctypes.Structure):
+    _fields_ = [
+        ("base", ctypes.c_void_p),
+        ("page_stride", ctypes.c_int64),
+        ("token_stride", ctypes.c_int64),
+        ("head_stride", ctypes.c_int64),
+        ("page_size", ctypes.c_int32),
+        ("num_pages", ctypes.c_int32),
+        ("page_table", ctypes.c_void_p),
+        ("max_pages", ctypes.c_int32),
+        ("reserved", ctypes.c_int32),
+    ]
+
+
+_c = ctypes
+_SIGNATURES = {
+    "attn_plan_partitions": [_c.c_int, _c.c_int, _c.c_int, _c.c_int, _c.c_int, _c.c_int,
+                             _c.c_int, _c.c_int, _c.POINTER(_c.c_int),
+                             _c.POINTER(_c.c_size_t)],
+    "attn_decode": [_c.c_void_p, _c.POINTER(attn_kv_t), _c.POINTER(attn_kv_t), _c.c_void_p,
+                    _c.c_int, _c.c_int, _c.c_int, _c.c_int, _c.c_int, _c.c_float, _c.c_void_p,
+                    _c.c_int, _c.c_void_p, _c.c_size_t, _c.c_void_p, _c.c_void_p, _c.c_void_p],
+    "attn_mla_decode": [_c.c_void_p, _c.POINTER(attn_kv_t), _c.c_void_p, _c.c_int, _c.c_int,
+                        _c.c_int, _c.c_int, _c.c_int, _c.c_float, _c.c_void_p, _c.c_int,
+                        _c.c_void_p, _c.c_size_t, _c.c_void_p, _c.c_void_p, _c.c_void_p],
+    "attn_splitk_reduce": [_c.c_void_p, _c.c_void_p, _c.c_void_p, _c.c_int, _c.c_int, _c.c_int,
+                           _c.c_int, _c.c_void_p, _c.c_void_p, _c.c_void_p, _c.c_void_p],
+    "attn_device_error_flags": [_c.POINTER(_c.c_uint), _c.c_int],
+}
+
+_lib = None
+
+
+def lib():
+    """The loaded libattn.so (raises if it has not been built)."""
+    global _lib
+    if _lib is None:
+        if not os.path.exists(LIB_PATH):
+            raise ImportError(f"{LIB_PATH} is missing: build it with "
+                              "split_flash_decoding_gb300.build.build()")
+        handle = ctypes.CDLL(LIB_PATH)
+        for name, argtypes in _SIGNATURES.items():
+            fn = getattr(handle, name)
+            fn.argtypes = argtypes
+            fn.restype = ctypes.c_int
+        _lib = handle
+    return _lib
+
+
+def _check(fn: str, status: int):
+    if status != ATTN_OK:
+        raise AttnError(fn, status)
+
+
+def _ptr(t: Optional[torch.Tensor]):
+    return None if t is None else t.data_ptr()
+
+
+def _stream_handle(stream) -> Optional[int]:
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return stream.cuda_stream
+
+
+# ---------------------------------------------------------------------------
+# cache descriptors
+# ---------------------------------------------------------------------------
+
+def kv_descriptor(cache: torch.Tensor, page_table: Optional[torch.Tensor] = None) -> attn_kv_t:
+    """Describe a bf16 cache tensor for the C ABI.
+
+    Paged: cache [num_pages, page_size, num_kv_heads, dim] with page_table
+    int32 [batch, max_pages].  Contiguous: cache [batch, capacity,
+    num_kv_heads, dim] and page_table None.  The last dimension must be
+    contiguous; other strides are taken from the tensor.
+    """
+    if cache.dtype != torch.bfloat16:
+        raise TypeError("cache must be bf16")
+    if cache.dim() != 4 or cache.stride(3) != 1:
+        raise ValueError("cache must be 4-D with contiguous channels")
+    d = attn_kv_t()
+    d.base = cache.data_ptr()
+    d.page_stride = cache.stride(0)
+    d.token_stride = cache.stride(1)
+    d.head_stride = cache.stride(2)
+    d.page_size = cache.shape[1]
+    d.num_pages = cache.shape[0]
+    if page_table is not None:
+        if page_table.dtype != torch.int32 or page_table.dim() != 2 or not page_table.is_contiguous():
+            raise ValueError("page_table must be a contiguous int32 [batch, max_pages] tensor")
+        d.page_table = page_table.data_ptr()
+        d.max_pages = page_table.shape[1]
+    else:
+        d.page_table = None
+        d.max_pages = 0
+    d.reserved = 0
+    return d
+
+
+# ---------------------------------------------------------------------------
+# entry points
+# ---------------------------------------------------------------------------
+
+def attn_plan_partitions(batch: int, num_q_rows: int, num_q_heads: int, num_kv_heads: int,
+                         head_dim_v: int, max_kv_len: int, requested: int = 0,
+                         num_sms: int = 0):
+    """Returns (num_partitions, workspace_bytes)."""
+    P = ctypes.c_int(0)
+    ws = ctypes.c_size_t(0)
+    _check("attn_plan_partitions",
+           lib().attn_plan_partitions(num_sms, batch, num_q_rows, num_q_heads, num_kv_heads,
+                                      head_dim_v, max_kv_len, requested, ctypes.byref(P),
+                                      ctypes.byref(ws)))
+    return P.value, ws.value
+
+
+def _workspace(nbytes: int, device, workspace: Optional[torch.Tensor]):
+    if nbytes == 0:
+        return None, 0
+    if workspace is None:
+        workspace = torch.empty(nbytes, dtype=torch.uint8, device=device)
+    return workspace, workspace.numel() * workspace.element_size()
+
+
+def attn_decode(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tensor,
+                kv_len: torch.Tensor, *, group: int, scale: float, max_kv_len: int,
+                page_table: Optional[torch.Tensor] = None, sink: Optional[torch.Tensor] = None,
+                num_partitions: int = 0, workspace: Optional[torch.Tensor] = None,
+                out: Optional[torch.Tensor] = None, lse: Optional[torch.Tensor] = None,
+                return_lse: bool = True, stream=None):
+    """Decode attention (one query token per sequence) through attn_decode.
+
+    q bf16 [batch, num_q_heads, head_dim]; caches as for kv_descriptor;
+    kv_len int32/uint32 [batch] on the device; sink fp32 [num_q_heads] or
+    None.  num_partitions 0 plans automatically.  Returns (out, lse).
+    """
+    batch, hq, d = q.shape
+    if out is None:
+        out = torch.empty((batch, hq, d), dtype=torch.bfloat16, device=q.device)
+    if lse is None and return_lse:
+        lse = torch.empty((batch, hq), dtype=torch.float32, device=q.device)
+    P, ws_bytes = attn_plan_partitions(batch, batch, hq, hq // group, d, max_kv_len,
+                                       num_partitions)
+    ws, ws_size = _workspace(ws_bytes, q.device, workspace)
+    kd = kv_descriptor(k_cache, page_table)
+    vd = kv_descriptor(v_cache, page_table)
+    _check("attn_decode",
+           lib().attn_decode(q.data_ptr(), ctypes.byref(kd), ctypes.byref(vd), kv_len.data_ptr(),
+                             batch, hq, group, d, max_kv_len, scale, _ptr(sink), P, _ptr(ws),
+                             ws_size, out.data_ptr(), _ptr(lse), _stream_handle(stream)))
+    return out, lse
+
+
+def attn_mla_decode(q: torch.Tensor, kv_cache: torch.Tensor, kv_len: torch.Tensor, *,
+                    scale: float, max_kv_len: int, dim_v: int = 512,
+                    page_table: Optional[torch.Tensor] = None,
+                    sink: Optional[torch.Tensor] = None, num_partitions: int = 0,
+                    workspace: Optional[torch.Tensor] = None, out: Optional[torch.Tensor] = None,
+                    lse: Optional[torch.Tensor] = None, return_lse: bool = True, stream=None):
+    """MLA decode through attn_mla_decode: q bf16 [batch, num_q_heads, 576],
+    one-head cache [pages, page_size, 1, 576]; V = K[..., :dim_v]."""
+    batch, hq, dqk = q.shape
+    if out is None:
+        out = torch.empty((batch, hq, dim_v), dtype=torch.bfloat16, device=q.device)
+    if lse is None and return_lse:
+        lse = torch.empty((batch, hq), dtype=torch.float32, device=q.device)
+    P, ws_bytes = attn_plan_partitions(batch, batch, hq, 1, dim_v, max_kv_len, num_partitions)
+    ws, ws_size = _workspace(ws_bytes, q.device, workspace)
+    kd = kv_descriptor(kv_cache, page_table)
+    _check("attn_mla_decode",
+           lib().attn_mla_decode(q.data_ptr(), ctypes.byref(kd), kv_len.data_ptr(), batch, hq, dqk,
+                                 dim_v, max_kv_len, scale, _ptr(sink), P, _ptr(ws), ws_size,
+                                 out.data_ptr(), _ptr(lse), _stream_handle(stream)))
+    return out, lse
+
+
+def attn_splitk_reduce(ws_o: torch.Tensor, ws_m: torch.Tensor, ws_l: torch.Tensor, *,
+                       sink: Optional[torch.Tensor] = None, out: Optional[torch.Tensor] = None,
+                       lse: Optional[torch.Tensor] = None, stream=None):
+    """Merge fp32 partials ws_o [P, rows, Hq, dv], ws_m / ws_l [P, rows, Hq]."""
+    P, rows, hq, dv = ws_o.shape
+    for t in (ws_o, ws_m, ws_l):
+        if t.dtype != torch.float32 or not t.is_contiguous():
+            raise ValueError("partials must be contiguous fp32")
+    if out is None:
+        out = torch.empty((rows, hq, dv), dtype=torch.bfloat16, device=ws_o.device)
+    if lse is None:
+        lse = torch.empty((rows, hq), dtype=torch.float32, device=ws_o.device)
+    _check("attn_splitk_reduce",
+           lib().attn_splitk_reduce(ws_o.data_ptr(), ws_m.data_ptr(), ws_l.data_ptr(), P, rows,
+                                    hq, dv, _ptr(sink), out.data_ptr(), _ptr(lse),
+                                    _stream_handle(stream)))
+    return out, lse
+
+
+def attn_device_error_flags(clear: bool = True) -> int:
+    flags = ctypes.c_uint(0)
+    _check("attn_device_error_flags", lib().attn_device_error_flags(ctypes.byref(flags),
+                                                                    1 if clear else 0))
+    return flags.value

@@ -1,0 +1,387 @@
+// api.cu -- the extern "C" entry points of libattn.so (declared in
+// include/attn_decode.h): host-side validation, the split-K partition
+// planner, TMA tensor-map encoding and kernel launches.
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include <cstdint>
+#include <cstring>
+#include <mutex>
+
+#include "attn_decode.h"
+#include "launch.h"
+
+namespace attn {
+namespace {
+
+// Device error word written by kernels instead of trapping or hanging.
+__device__ unsigned g_error_word;
+
+constexpr int kMaxDevices = 64;
+std::mutex g_mu;
+unsigned *g_err_ptr[kMaxDevices];
+
+// Address of g_error_word on the current device (looked up once per device).
+int error_word(unsigned **out) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices)
+        return ATTN_ERR_CUDA;
+    std::lock_guard<std::mutex> lk(g_mu);
+    if (!g_err_ptr[dev]) {
+        void *ptr = nullptr;
+        if (cudaGetSymbolAddress(&ptr, g_error_word) != cudaSuccess) return ATTN_ERR_CUDA;
+        g_err_ptr[dev] = static_cast<unsigned *>(ptr);
+    }
+    *out = g_err_ptr[dev];
+    return ATTN_OK;
+}
+
+using EncodeTiledFn = CUresult (*)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *,
+                                   const cuuint64_t *, const cuuint64_t *, const cuuint32_t *,
+                                   const cuuint32_t *, CUtensorMapInterleave,
+                                   CUtensorMapSwizzle, CUtensorMapL2promotion,
+                                   CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn() {
+    static EncodeTiledFn fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void *p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000,
+                                             cudaEnableDefault, &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<EncodeTiledFn>(p);
+    });
+    return fn;
+}
+
+// 4-D map over a cache operand: (channel, slot in page, kv head, page) with a
+// box of 64 channels (128 B, swizzled 128B) x box_rows slots x 1 x 1.
+int encode_kv_map(CUtensorMap *map, const attn_kv_t &kv, int dim, int num_kv_heads,
+                  int box_rows) {
+    EncodeTiledFn fn = encode_fn();
+    if (!fn) return ATTN_ERR_CUDA;
+    cuuint64_t gdim[4] = {cuuint64_t(dim), cuuint64_t(kv.page_size), cuuint64_t(num_kv_heads),
+                          cuuint64_t(kv.num_pages)};
+    cuuint64_t gstride[3] = {cuuint64_t(kv.token_stride) * 2, cuuint64_t(kv.head_stride) * 2,
+                             cuuint64_t(kv.page_stride) * 2};
+    cuuint32_t box[4] = {64, cuuint32_t(box_rows), 1, 1};
+    cuuint32_t estride[4] = {1, 1, 1, 1};
+    CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void *>(kv.base), gdim,
+                    gstride, box, estride, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                    CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                    CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS ? ATTN_OK : ATTN_ERR_UNSUPPORTED;
+}
+
+bool is_pow2(long long x) { return x > 0 && (x & (x - 1)) == 0; }
+
+size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
+
+// Workspace layout for P partitions: ws_o | ws_m | ws_l, each 256-B aligned.
+size_t workspace_layout(int P, long long rows, int hq, int dv, size_t *off_m, size_t *off_l) {
+    if (P <= 1) {
+        if (off_m) *off_m = 0;
+        if (off_l) *off_l = 0;
+        return 0;
+    }
+    const size_t n = size_t(P) * size_t(rows) * size_t(hq);
+    const size_t o_bytes = align256(n * size_t(dv) * sizeof(float));
+    const size_t m_bytes = align256(n * sizeof(float));
+    if (off_m) *off_m = o_bytes;
+    if (off_l) *off_l = o_bytes + m_bytes;
+    return o_bytes + 2 * m_bytes;
+}
+
+int chunk_for(int max_kv_len, int P, int tile) {
+    long long per = (static_cast<long long>(max_kv_len) + P - 1) / P;
+    if (per < 1) per = 1;
+    per = (per + tile - 1) / tile * tile;
+    return static_cast<int>(per);
+}
+
+// Validate one cache operand.  contiguous (no page table) means page b is
+// sequence b and page_size bounds every length.
+int check_kv(const attn_kv_t *kv, int batch, int dim, int max_kv_len) {
+    if (!kv || !kv->base) return ATTN_ERR_INVALID_ARG;
+    if (kv->reserved != 0) return ATTN_ERR_INVALID_ARG;
+    if (reinterpret_cast<uintptr_t>(kv->base) % 16) return ATTN_ERR_INVALID_ARG;
+    if (kv->page_size <= 0 || kv->num_pages <= 0) return ATTN_ERR_INVALID_ARG;
+    if (kv->token_stride <= 0 || kv->head_stride <= 0 || kv->page_stride <= 0)
+        return ATTN_ERR_INVALID_ARG;
+    if (kv->token_stride % 8 || kv->head_stride % 8 || kv->page_stride % 8)
+        return ATTN_ERR_INVALID_ARG;
+    if (kv->head_stride < dim && kv->token_stride < dim) return ATTN_ERR_INVALID_ARG;
+    if (kv->page_table) {
+        if (!is_pow2(kv->page_size) || kv->page_size < 8) return ATTN_ERR_UNSUPPORTED;
+        if (kv->max_pages <= 0) return ATTN_ERR_INVALID_ARG;
+        const long long need = (static_cast<long long>(max_kv_len) + kv->page_size - 1) /
+                               kv->page_size;
+        if (need > kv->max_pages) return ATTN_ERR_INVALID_ARG;
+    } else {
+        if (kv->page_size < max_kv_len) return ATTN_ERR_INVALID_ARG;
+        if (kv->num_pages < batch) return ATTN_ERR_INVALID_ARG;
+    }
+    return ATTN_OK;
+}
+
+int map_cuda(cudaError_t e) { return e == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA; }
+
+}  // namespace
+}  // namespace attn
+
+using namespace attn;
+
+extern "C" int attn_plan_partitions(int num_sms, int batch, int num_q_rows, int num_q_heads,
+                                    int num_kv_heads, int head_dim_v, int max_kv_len,
+                                    int requested, int *num_partitions,
+                                    size_t *workspace_bytes) {
+    if (!num_partitions || !workspace_bytes) return ATTN_ERR_INVALID_ARG;
+    if (batch < 0 || num_q_rows < 0 || num_q_heads <= 0 || num_kv_heads <= 0 ||
+        head_dim_v <= 0 || max_kv_len < 0 || requested < 0)
+        return ATTN_ERR_INVALID_ARG;
+    if (num_q_heads % num_kv_heads) return ATTN_ERR_INVALID_ARG;
+    if (requested > ATTN_MAX_PARTITIONS) return ATTN_ERR_INVALID_ARG;
+    int P = requested;
+    if (P == 0) {
+        if (num_sms <= 0) {
+            int dev = 0;
+            if (cudaGetDevice(&dev) != cudaSuccess ||
+                cudaDeviceGetAttribute(&num_sms, cudaDevAttrMultiProcessorCount, dev) !=
+                    cudaSuccess)
+                return ATTN_ERR_CUDA;
+        }
+        // Fill at least one wave of CTAs (two resident per SM) even if every
+        // sequence had max_kv_len keys, and keep slices near 512 keys so the
+        // last wave of a ragged batch is short.
+        const long long units = static_cast<long long>(batch > 0 ? batch : 1) * num_kv_heads;
+        const long long slots = 2LL * num_sms;
+        long long p_fill = (slots + units - 1) / units;
+        long long p_len = (static_cast<long long>(max_kv_len) + 511) / 512;
+        long long p = p_fill > p_len ? p_fill : p_len;
+        const long long p_max_useful = (static_cast<long long>(max_kv_len) + kGqaTileKeys - 1) /
+                                       kGqaTileKeys;
+        if (p > p_max_useful) p = p_max_useful;
+        if (p < 1) p = 1;
+        if (p > ATTN_MAX_PARTITIONS) p = ATTN_MAX_PARTITIONS;
+        P = static_cast<int>(p);
+    }
+    *num_partitions = P;
+    *workspace_bytes = workspace_layout(P, num_q_rows, num_q_heads, head_dim_v, nullptr, nullptr);
+    return ATTN_OK;
+}
+
+extern "C" int attn_decode(const void *q, const attn_kv_t *k, const attn_kv_t *v,
+                           const uint32_t *kv_len, int batch, int num_q_heads, int group,
+                           int head_dim, int max_kv_len, float scale, const float *sink,
+                           int num_partitions, void *workspace, size_t workspace_bytes,
+                           void *out, float *lse, attn_stream_t stream) {
+    if (batch < 0 || num_q_heads <= 0 || group <= 0 || max_kv_len < 0)
+        return ATTN_ERR_INVALID_ARG;
+    if (num_q_heads % group) return ATTN_ERR_INVALID_ARG;
+    if (num_partitions < 1 || num_partitions > ATTN_MAX_PARTITIONS) return ATTN_ERR_INVALID_ARG;
+    if (!(scale == scale)) return ATTN_ERR_INVALID_ARG;
+    if (batch == 0) return ATTN_OK;
+    if (!q || !kv_len || !out) return ATTN_ERR_INVALID_ARG;
+    if (group != 1 && group != 2 && group != 4 && group != 8) return ATTN_ERR_UNSUPPORTED;
+    if (head_dim != 64 && head_dim != 128) return ATTN_ERR_UNSUPPORTED;
+    if (reinterpret_cast<uintptr_t>(out) % 16 || reinterpret_cast<uintptr_t>(q) % 16)
+        return ATTN_ERR_INVALID_ARG;
+    const int hkv = num_q_heads / group;
+    int st = check_kv(k, batch, head_dim, max_kv_len);
+    if (st) return st;
+    st = check_kv(v, batch, head_dim, max_kv_len);
+    if (st) return st;
+    if (k->page_table != v->page_table || k->page_size != v->page_size ||
+        k->max_pages != v->max_pages || k->num_pages != v->num_pages)
+        return ATTN_ERR_UNSUPPORTED;
+
+    size_t off_m = 0, off_l = 0;
+    const size_t need = workspace_layout(num_partitions, batch, num_q_heads, head_dim, &off_m,
+                                         &off_l);
+    if (num_partitions > 1) {
+        if (!workspace || workspace_bytes < need) return ATTN_ERR_WORKSPACE;
+        if (reinterpret_cast<uintptr_t>(workspace) % 256) return ATTN_ERR_WORKSPACE;
+    }
+
+    GqaParams p;
+    std::memset(&p, 0, sizeof(p));
+    p.box_rows = k->page_table ? (k->page_size < kGqaTileKeys ? k->page_size : kGqaTileKeys)
+                               : kGqaTileKeys;
+    st = encode_kv_map(&p.k_map, *k, head_dim, hkv, p.box_rows);
+    if (st) return st;
+    st = encode_kv_map(&p.v_map, *v, head_dim, hkv, p.box_rows);
+    if (st) return st;
+    st = error_word(&p.err);
+    if (st) return st;
+
+    p.q = static_cast<const uint16_t *>(q);
+    p.kv_len = kv_len;
+    p.page_table = k->page_table;
+    p.sink = sink;
+    if (num_partitions > 1) {
+        uint8_t *ws = static_cast<uint8_t *>(workspace);
+        p.ws_o = reinterpret_cast<float *>(ws);
+        p.ws_m = reinterpret_cast<float *>(ws + off_m);
+        p.ws_l = reinterpret_cast<float *>(ws + off_l);
+    }
+    p.out = static_cast<uint16_t *>(out);
+    p.lse = lse;
+    p.batch = batch;
+    p.num_q_heads = num_q_heads;
+    p.group = group;
+    p.head_dim = head_dim;
+    p.max_pages = k->max_pages;
+    p.page_size = k->page_size;
+    p.num_pages = k->num_pages;
+    p.num_partitions = num_partitions;
+    p.chunk = chunk_for(max_kv_len, num_partitions, kGqaTileKeys);
+    p.qk_scale_log2 = scale * 1.4426950408889634f;
+
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    st = map_cuda(launch_gqa_decode(p, s));
+    if (st || num_partitions == 1) return st;
+
+    ReduceParams r;
+    std::memset(&r, 0, sizeof(r));
+    r.ws_o = p.ws_o;
+    r.ws_m = p.ws_m;
+    r.ws_l = p.ws_l;
+    r.sink = sink;
+    r.out = p.out;
+    r.lse = lse;
+    r.kv_len = kv_len;
+    r.num_partitions = num_partitions;
+    r.rows = batch;
+    r.num_q_heads = num_q_heads;
+    r.dim_v = head_dim;
+    r.chunk = p.chunk;
+    return map_cuda(launch_splitk_reduce(r, s, /*pdl=*/true));
+}
+
+extern "C" int attn_mla_decode(const void *q, const attn_kv_t *kv, const uint32_t *kv_len,
+                               int batch, int num_q_heads, int dim_qk, int dim_v, int max_kv_len,
+                               float scale, const float *sink, int num_partitions,
+                               void *workspace, size_t workspace_bytes, void *out, float *lse,
+                               attn_stream_t stream) {
+    if (batch < 0 || num_q_heads <= 0 || dim_qk <= 0 || dim_v <= 0 || max_kv_len < 0)
+        return ATTN_ERR_INVALID_ARG;
+    if (num_partitions < 1 || num_partitions > ATTN_MAX_PARTITIONS) return ATTN_ERR_INVALID_ARG;
+    if (!(scale == scale)) return ATTN_ERR_INVALID_ARG;
+    if (batch == 0) return ATTN_OK;
+    if (!q || !kv_len || !out) return ATTN_ERR_INVALID_ARG;
+    if (num_q_heads != kMlaHeads || dim_qk != kMlaDimQK || dim_v != kMlaDimV)
+        return ATTN_ERR_UNSUPPORTED;
+    if (reinterpret_cast<uintptr_t>(out) % 16 || reinterpret_cast<uintptr_t>(q) % 16)
+        return ATTN_ERR_INVALID_ARG;
+    int st = check_kv(kv, batch, dim_qk, max_kv_len);
+    if (st) return st;
+    if (static_cast<long long>(batch) * kMlaHeads > (1LL << 31)) return ATTN_ERR_UNSUPPORTED;
+
+    size_t off_m = 0, off_l = 0;
+    const size_t need = workspace_layout(num_partitions, batch, num_q_heads, dim_v, &off_m,
+                                         &off_l);
+    if (num_partitions > 1) {
+        if (!workspace || workspace_bytes < need) return ATTN_ERR_WORKSPACE;
+        if (reinterpret_cast<uintptr_t>(workspace) % 256) return ATTN_ERR_WORKSPACE;
+    }
+
+    MlaParams p;
+    std::memset(&p, 0, sizeof(p));
+    p.box_rows = kv->page_table ? (kv->page_size < kMlaTileKeys ? kv->page_size : kMlaTileKeys)
+                                : kMlaTileKeys;
+    st = encode_kv_map(&p.kv_map, *kv, dim_qk, 1, p.box_rows);
+    if (st) return st;
+    {
+        EncodeTiledFn fn = encode_fn();
+        if (!fn) return ATTN_ERR_CUDA;
+        cuuint64_t gdim[2] = {cuuint64_t(dim_qk), cuuint64_t(batch) * kMlaHeads};
+        cuuint64_t gstride[1] = {cuuint64_t(dim_qk) * 2};
+        cuuint32_t box[2] = {64, 128};
+        cuuint32_t estride[2] = {1, 1};
+        CUresult r = fn(&p.q_map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void *>(q),
+                        gdim, gstride, box, estride, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                        CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                        CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+        if (r != CUDA_SUCCESS) return ATTN_ERR_UNSUPPORTED;
+    }
+    st = error_word(&p.err);
+    if (st) return st;
+    p.kv_len = kv_len;
+    p.page_table = kv->page_table;
+    p.sink = sink;
+    if (num_partitions > 1) {
+        uint8_t *ws = static_cast<uint8_t *>(workspace);
+        p.ws_o = reinterpret_cast<float *>(ws);
+        p.ws_m = reinterpret_cast<float *>(ws + off_m);
+        p.ws_l = reinterpret_cast<float *>(ws + off_l);
+    }
+    p.out = static_cast<uint16_t *>(out);
+    p.lse = lse;
+    p.batch = batch;
+    p.max_pages = kv->max_pages;
+    p.page_size = kv->page_size;
+    p.num_pages = kv->num_pages;
+    p.num_partitions = num_partitions;
+    p.chunk = chunk_for(max_kv_len, num_partitions, kMlaTileKeys);
+    p.qk_scale_log2 = scale * 1.4426950408889634f;
+
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    st = map_cuda(launch_mla_decode(p, s));
+    if (st || num_partitions == 1) return st;
+
+    ReduceParams r;
+    std::memset(&r, 0, sizeof(r));
+    r.ws_o = p.ws_o;
+    r.ws_m = p.ws_m;
+    r.ws_l = p.ws_l;
+    r.sink = sink;
+    r.out = p.out;
+    r.lse = lse;
+    r.kv_len = kv_len;
+    r.num_partitions = num_partitions;
+    r.rows = batch;
+    r.num_q_heads = num_q_heads;
+    r.dim_v = dim_v;
+    r.chunk = p.chunk;
+    return map_cuda(launch_splitk_reduce(r, s, /*pdl=*/true));
+}
+
+extern "C" int attn_splitk_reduce(const float *ws_o, const float *ws_m, const float *ws_l,
+                                  int num_partitions, int rows, int num_q_heads, int dim_v,
+                                  const float *sink, void *out, float *lse,
+                                  attn_stream_t stream) {
+    if (num_partitions < 1 || num_partitions > ATTN_MAX_PARTITIONS || rows < 0 ||
+        num_q_heads <= 0 || dim_v <= 0 || dim_v % 4 || dim_v > 1024)
+        return ATTN_ERR_INVALID_ARG;
+    if (rows == 0) return ATTN_OK;
+    if (!ws_o || !ws_m || !ws_l || !out) return ATTN_ERR_INVALID_ARG;
+    if (reinterpret_cast<uintptr_t>(ws_o) % 16 || reinterpret_cast<uintptr_t>(out) % 8)
+        return ATTN_ERR_INVALID_ARG;
+    ReduceParams r;
+    std::memset(&r, 0, sizeof(r));
+    r.ws_o = ws_o;
+    r.ws_m = ws_m;
+    r.ws_l = ws_l;
+    r.sink = sink;
+    r.out = static_cast<uint16_t *>(out);
+    r.lse = lse;
+    r.num_partitions = num_partitions;
+    r.rows = rows;
+    r.num_q_heads = num_q_heads;
+    r.dim_v = dim_v;
+    return map_cuda(launch_splitk_reduce(r, reinterpret_cast<cudaStream_t>(stream), false));
+}
+
+extern "C" int attn_device_error_flags(unsigned int *flags, int clear) {
+    if (!flags) return ATTN_ERR_INVALID_ARG;
+    unsigned *ptr = nullptr;
+    int st = error_word(&ptr);
+    if (st) return st;
+    if (cudaDeviceSynchronize() != cudaSuccess) return ATTN_ERR_CUDA;
+    if (cudaMemcpy(flags, ptr, sizeof(unsigned), cudaMemcpyDeviceToHost) != cudaSuccess)
+        return ATTN_ERR_CUDA;
+    if (clear && cudaMemset(ptr, 0, sizeof(unsigned)) != cudaSuccess) return ATTN_ERR_CUDA;
+    return ATTN_OK;
+}

@@ -1,0 +1,74 @@
+// launch.h -- parameter blocks passed from the C-ABI layer (api.cu) to the
+// kernel launchers.  Everything here is already validated.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace attn {
+
+// Keys per pipeline stage and per consumer warp pass in the GQA kernel;
+// partition slices are multiples of it.
+constexpr int kGqaTileKeys = 32;
+
+struct GqaParams {
+    CUtensorMap k_map;            // 4-D: (channel, slot, kv head, page)
+    CUtensorMap v_map;
+    const uint16_t *q;            // bf16 [batch][Hq][D]
+    const uint32_t *kv_len;       // [batch]
+    const int32_t *page_table;    // [batch][max_pages] or nullptr
+    const float *sink;            // [Hq] or nullptr
+    float *ws_o;                  // [P][batch][Hq][D]
+    float *ws_m;                  // [P][batch][Hq]
+    float *ws_l;                  // [P][batch][Hq]
+    uint16_t *out;                // bf16 [batch][Hq][D]
+    float *lse;                   // [batch][Hq] or nullptr
+    unsigned *err;                // device error word
+    int batch, num_q_heads, group, head_dim;
+    int max_pages, page_size, num_pages;
+    int box_rows;                 // tokens per TMA box (min(tile, page size))
+    int num_partitions;           // P (grid.x)
+    int chunk;                    // keys per partition slice, multiple of kGqaTileKeys
+    float qk_scale_log2;          // scale * log2(e)
+};
+
+// Keys per tile in the MLA kernel; its partition slices are multiples of it.
+constexpr int kMlaTileKeys = 64;
+constexpr int kMlaHeads = 128;
+constexpr int kMlaDimQK = 576;
+constexpr int kMlaDimV = 512;
+
+struct MlaParams {
+    CUtensorMap kv_map;           // 4-D: (channel 576, slot, head 1, page)
+    CUtensorMap q_map;            // 2-D: (channel 576, row = b * 128 + h)
+    const uint32_t *kv_len;       // [batch]
+    const int32_t *page_table;    // [batch][max_pages] or nullptr
+    const float *sink;            // [128] or nullptr
+    float *ws_o;                  // [P][batch][128][512]
+    float *ws_m;                  // [P][batch][128]
+    float *ws_l;
+    uint16_t *out;                // bf16 [batch][128][512]
+    float *lse;                   // [batch][128] or nullptr
+    unsigned *err;
+    int batch, max_pages, page_size, num_pages;
+    int box_rows;                 // tokens per TMA box (min(64, page size))
+    int num_partitions, chunk;    // chunk: multiple of kMlaTileKeys
+    float qk_scale_log2;
+};
+
+struct ReduceParams {
+    const float *ws_o, *ws_m, *ws_l;
+    const float *sink;            // [Hq] or nullptr
+    uint16_t *out;                // bf16 [rows][Hq][dv]
+    float *lse;                   // [rows][Hq] or nullptr
+    const uint32_t *kv_len;       // optional: rows whose kv_len needs < 2 slices are skipped
+    int num_partitions, rows, num_q_heads, dim_v;
+    int chunk;                    // slice length when kv_len is given
+};
+
+cudaError_t launch_gqa_decode(const GqaParams &p, cudaStream_t stream);
+cudaError_t launch_mla_decode(const MlaParams &p, cudaStream_t stream);
+cudaError_t launch_splitk_reduce(const ReduceParams &p, cudaStream_t stream, bool pdl);
+
+}  // namespace attn

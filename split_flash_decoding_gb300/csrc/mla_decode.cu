@@ -1,0 +1,467 @@
+// mla_decode.cu -- split-K MLA decode on the 5th-generation tensor cores.
+//
+// Multi-head latent attention decode: 128 query heads attend to one KV head
+// whose rows are 576 channels (512 latent + 64 rope), and V is the first 512
+// channels of K ("kv_num_heads: Must be 1 for MLA"; "V is derived as
+// K[:, :, :depth_v], so V is not loaded separately",
+// flare_mla_decoding_dispatch, Parameters and Args).
+//
+// Work unit: a cluster of two CTAs per (key slice p, sequence b).  The 128
+// heads are the MMA's M dimension.  The two CTAs split the 576 channels:
+//
+//   rank 0 loads channels [0, 256)   = the first half of V (4 TMA boxes),
+//   rank 1 loads channels [256, 576) = the second half of V + rope (5 boxes),
+//
+// so every byte of a K row is fetched from HBM exactly once per cluster.
+// Per 64-key tile each CTA computes a partial score S_r = Q[:, ch_r] K[:, ch_r]^T
+// with tcgen05.mma into TMEM, the two CTAs swap partials through distributed
+// shared memory and add them (fp32 addition is commutative, so both hold the
+// identical full S), run the same online softmax, and each accumulates its
+// half of the output, O_r += P V[:, 256 r : 256 r + 256], in TMEM.
+//
+// Warp roles (192 threads per CTA):
+//   warps 0-3  softmax: thread h owns head row h (its TMEM lane)
+//   warp 4     TMA producer (Q once, then K tiles into a 2-stage ring)
+//   warp 5     TMEM allocation and MMA issue (one thread)
+//
+// TMEM columns: S double buffer [0, 128), O half [256, 512).
+// The running max is kept lazily: P = exp2(s - m_ref) with m_ref raised (and
+// O rescaled) only when a tile's max exceeds m_ref by more than 8 (base 2),
+// so P <= 256 and O/l stay finite in fp32.
+#include "launch.h"
+#include "ptx.cuh"
+#include "tc.cuh"
+
+namespace attn {
+namespace {
+
+constexpr int kBN = kMlaTileKeys;          // 64 keys per tile
+constexpr int kStages = 2;
+constexpr int kMaxBoxes = 5;               // 64-channel boxes per rank (4 or 5)
+constexpr int kQBoxBytes = 128 * 128;      // 128 rows x 128 B
+constexpr int kKBoxBytes = kBN * 128;      // 64 rows x 128 B
+constexpr int kStageBytes = kMaxBoxes * kKBoxBytes;
+constexpr int kThreads = 192;
+constexpr uint32_t kTmemCols = 512;
+constexpr uint32_t kTmemS = 0;             // two 64-column S buffers
+constexpr uint32_t kTmemO = 256;           // 256-column O half
+constexpr float kRescaleThreshold = 8.0f;  // base-2 units
+
+// V (B operand of O = P V) is MN-major: 4 boxes of 64 channels x 64 keys.
+constexpr uint32_t kVLbo = kKBoxBytes;     // stride between 64-channel blocks
+constexpr uint32_t kVSbo = 1024;           // stride between 8-key groups
+
+struct Smem {
+    static constexpr int q = 0;
+    static constexpr int kv = q + kMaxBoxes * kQBoxBytes;            // 80 KB
+    static constexpr int p = kv + kStages * kStageBytes;              // +80 KB
+    static constexpr int x = p + 128 * 128;                           // +16 KB
+    static constexpr int bars = x + 128 * kBN * 4;                    // +32 KB
+    static constexpr int total = bars + 256;
+};
+constexpr size_t kSmemBytes = Smem::total + 1024;
+
+enum Bar {
+    kKvFull = 0,                // [2]
+    kKvEmpty = 2,               // [2]
+    kQFull = 4,
+    kSFull = 5,                 // [2]
+    kSFree = 7,                 // [2]
+    kPFull = 9,
+    kODone = 10,
+    kXFull = 11,
+    kXFree = 12,
+    kNumBars = 13
+};
+
+__device__ __forceinline__ uint32_t p_swz(int row, int chunk) {
+    return uint32_t(row * 128 + ((chunk ^ (row & 7)) << 4));
+}
+
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
+mla_decode_kernel(const __grid_constant__ MlaParams p) {
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t *smem = reinterpret_cast<uint8_t *>(
+        (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    uint64_t *bar = reinterpret_cast<uint64_t *>(smem + Smem::bars);
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + Smem::bars + kNumBars * 8);
+
+    const uint32_t rank = cluster_ctarank();
+    const uint32_t peer = rank ^ 1u;
+    const int part = blockIdx.x >> 1;
+    const int b = blockIdx.y;
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+    const int nbox = rank == 0 ? 4 : 5;
+    const int col0 = rank == 0 ? 0 : 256;
+
+    const uint32_t cap = uint32_t(p.num_partitions) * uint32_t(p.chunk);
+    const uint32_t len_in = p.kv_len[b];
+    if (len_in > cap && part == 0 && threadIdx.x == 0 && rank == 0)
+        atomicOr(p.err, kErrBadLength);
+    const int L = static_cast<int>(min(len_in, cap));
+    const int start = part * p.chunk;
+    const int end = min(start + p.chunk, L);
+    const int nslices = (L + p.chunk - 1) / p.chunk;
+    const bool direct = nslices <= 1;
+    if (start >= L && !(direct && part == 0)) return;  // uniform over the cluster
+    const int ntiles = start < end ? (end - start + kBN - 1) / kBN : 0;
+
+    if (threadIdx.x == 0) {
+        mbar_init(&bar[kKvFull + 0], 1);
+        mbar_init(&bar[kKvFull + 1], 1);
+        mbar_init(&bar[kKvEmpty + 0], 1);
+        mbar_init(&bar[kKvEmpty + 1], 1);
+        mbar_init(&bar[kQFull], 1);
+        mbar_init(&bar[kSFull + 0], 1);
+        mbar_init(&bar[kSFull + 1], 1);
+        mbar_init(&bar[kSFree + 0], 4);
+        mbar_init(&bar[kSFree + 1], 4);
+        mbar_init(&bar[kPFull], 4);
+        mbar_init(&bar[kODone], 1);
+        mbar_init(&bar[kXFull], 4);   // the peer's four softmax warps
+        mbar_init(&bar[kXFree], 4);
+        fence_mbar_init();
+    }
+    if (warp == 5) {
+        tc::tmem_alloc(tmem_slot, kTmemCols);
+        tc::tmem_relinquish();
+    }
+    tc::fence_before_sync();
+    __syncthreads();
+    cluster_sync();  // both CTAs' barriers exist before any remote arrive
+    tc::fence_after_sync();
+    const uint32_t tmem = *tmem_slot;
+
+    if (warp == 4) {
+        // ------------------------------------------------------------ producer
+        if (ntiles > 0) {
+            if (lane == 0) {
+                prefetch_tensormap(&p.kv_map);
+                prefetch_tensormap(&p.q_map);
+                mbar_arrive_expect_tx(&bar[kQFull], uint32_t(nbox) * kQBoxBytes);
+                for (int cb = 0; cb < nbox; ++cb)
+                    tma_load_2d(smem + Smem::q + cb * kQBoxBytes, &p.q_map, &bar[kQFull],
+                                col0 + cb * 64, b * kMlaHeads);
+            }
+            const int box_rows = p.box_rows;
+            const int boxes_per_tile = kBN / box_rows;   // 1..8
+            bool aborted = false;
+            for (int base = 0; base < ntiles && !aborted; base += 32) {
+                // lane i resolves the pages of tile base + i (up to 8 row boxes)
+                int pg[8], sl[8];
+#pragma unroll
+                for (int r = 0; r < 8; ++r) { pg[r] = -1; sl[r] = 0; }
+                const int my_tile = base + lane;
+                if (my_tile < ntiles) {
+                    const int t0 = start + my_tile * kBN;
+#pragma unroll
+                    for (int r = 0; r < 8; ++r) {
+                        const int t = t0 + r * box_rows;
+                        if (r >= boxes_per_tile || t >= L) continue;
+                        if (p.page_table) {
+                            const int pidx = t / p.page_size;
+                            int e = pidx < p.max_pages
+                                        ? p.page_table[size_t(b) * p.max_pages + pidx] : -1;
+                            if (e < 0 || e >= p.num_pages) {
+                                atomicOr(p.err, kErrBadPage);
+                                e = -1;
+                            }
+                            pg[r] = e;
+                            sl[r] = t % p.page_size;
+                        } else {
+                            pg[r] = b;
+                            sl[r] = t;
+                        }
+                    }
+                }
+                const int lim = min(base + 32, ntiles);
+                for (int i = base; i < lim; ++i) {
+                    int pages[8], slots[8];
+#pragma unroll
+                    for (int r = 0; r < 8; ++r) {
+                        pages[r] = __shfl_sync(0xffffffffu, pg[r], i - base);
+                        slots[r] = __shfl_sync(0xffffffffu, sl[r], i - base);
+                    }
+                    if (lane == 0) {
+                        const int s = i % kStages;
+                        if (i >= kStages &&
+                            !mbar_wait(&bar[kKvEmpty + s], ((i / kStages) - 1) & 1, p.err)) {
+                            aborted = true;
+                        } else {
+                            uint32_t nrow = 0;
+#pragma unroll
+                            for (int r = 0; r < 8; ++r) nrow += pages[r] >= 0 ? 1u : 0u;
+                            mbar_arrive_expect_tx(&bar[kKvFull + s],
+                                                  nrow * uint32_t(nbox) * uint32_t(box_rows) * 128u);
+                            uint8_t *st = smem + Smem::kv + s * kStageBytes;
+#pragma unroll
+                            for (int r = 0; r < 8; ++r) {
+                                if (pages[r] < 0) continue;
+                                for (int cb = 0; cb < nbox; ++cb)
+                                    tma_load_4d(st + cb * kKBoxBytes + r * box_rows * 128,
+                                                &p.kv_map, &bar[kKvFull + s], col0 + cb * 64,
+                                                slots[r], 0, pages[r]);
+                            }
+                        }
+                    }
+                    aborted = __shfl_sync(0xffffffffu, aborted, 0);
+                    if (aborted) break;
+                }
+            }
+        }
+    } else if (warp == 5) {
+        // ------------------------------------------------------------ MMA issue
+        if (ntiles > 0 && lane == 0) {
+            constexpr uint32_t idesc_s = tc::idesc_bf16_f32(128, kBN, 0, 0);
+            constexpr uint32_t idesc_o = tc::idesc_bf16_f32(128, 256, 0, 1);
+            const uint32_t q_base = smem_addr(smem + Smem::q);
+            const uint32_t kv_base = smem_addr(smem + Smem::kv);
+            const uint32_t p_base = smem_addr(smem + Smem::p);
+            bool ok = mbar_wait(&bar[kQFull], 0, p.err);
+            for (int t = 0; ok && t <= ntiles; ++t) {
+                if (t < ntiles) {
+                    const int s = t % kStages;
+                    const int sb = t & 1;
+                    ok = mbar_wait(&bar[kKvFull + s], (t / kStages) & 1, p.err);
+                    if (ok && t >= 2) ok = mbar_wait(&bar[kSFree + sb], ((t >> 1) - 1) & 1, p.err);
+                    if (!ok) break;
+                    tc::fence_after_sync();
+                    const uint32_t st = kv_base + s * kStageBytes;
+                    const int ksteps = nbox * 4;
+                    for (int ks = 0; ks < ksteps; ++ks) {
+                        const uint32_t off = (ks >> 2) * 0 + (ks & 3) * 32;
+                        const uint64_t a = tc::smem_desc_sw128(
+                            q_base + (ks >> 2) * kQBoxBytes + off, 16, 1024);
+                        const uint64_t bd = tc::smem_desc_sw128(
+                            st + (ks >> 2) * kKBoxBytes + off, 16, 1024);
+                        tc::mma_bf16(tmem + kTmemS + sb * kBN, a, bd, idesc_s, ks > 0);
+                    }
+                    tc::mma_commit(&bar[kSFull + sb]);
+                }
+                if (t >= 1) {
+                    const int tp = t - 1;
+                    ok = mbar_wait(&bar[kPFull], tp & 1, p.err);
+                    if (!ok) break;
+                    tc::fence_after_sync();
+                    const uint32_t st = kv_base + (tp % kStages) * kStageBytes;
+                    for (int kk = 0; kk < kBN / 16; ++kk) {
+                        const uint64_t a = tc::smem_desc_sw128(p_base + kk * 32, 16, 1024);
+                        const uint64_t bd = tc::smem_desc_sw128(st + kk * 16 * 128, kVLbo, kVSbo);
+                        tc::mma_bf16(tmem + kTmemO, a, bd, idesc_o, tp > 0 || kk > 0);
+                    }
+                    tc::mma_commit(&bar[kODone]);
+                    tc::mma_commit(&bar[kKvEmpty + (tp % kStages)]);
+                }
+            }
+        }
+    } else {
+        // ------------------------------------------------------------ softmax
+        const int h = warp * 32 + lane;          // head row == TMEM lane
+        const uint32_t lane_base = uint32_t(warp * 32) << 16;
+        uint8_t *xbuf = smem + Smem::x;
+        const uint32_t peer_x = mapa_shared(smem_addr(xbuf), peer);
+        const uint32_t peer_xfull = mapa_shared(smem_addr(&bar[kXFull]), peer);
+        const uint32_t peer_xfree = mapa_shared(smem_addr(&bar[kXFree]), peer);
+        uint8_t *pbuf = smem + Smem::p;
+        float m_ref = -INFINITY;
+        float l = 0.f;
+        bool ok = true;
+        for (int t = 0; t < ntiles; ++t) {
+            const int sb = t & 1;
+            const int t0 = start + t * kBN;
+            const int nvalid = min(kBN, end - t0);
+            ok = mbar_wait(&bar[kSFull + sb], (t >> 1) & 1, p.err);
+            if (!ok) break;
+            tc::fence_after_sync();
+            float s[64];
+            {
+                float v[32];
+                tc::tmem_ld32(tmem + lane_base + kTmemS + sb * kBN, v);
+#pragma unroll
+                for (int j = 0; j < 32; ++j) s[j] = v[j];
+                tc::tmem_ld32(tmem + lane_base + kTmemS + sb * kBN + 32, v);
+#pragma unroll
+                for (int j = 0; j < 32; ++j) s[32 + j] = v[j];
+            }
+            tc::fence_before_sync();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&bar[kSFree + sb]);
+
+            // ---- swap partial scores with the peer CTA (skewed 16-B chunks) ----
+            if (t >= 1) {
+                ok = mbar_wait_cluster(&bar[kXFree], (t - 1) & 1, p.err);
+                if (!ok) break;
+            }
+#pragma unroll
+            for (int c = 0; c < 16; ++c) {
+                const int pc = (c + h) & 15;
+                st_cluster_f4(peer_x + h * 256 + pc * 16, s[4 * c], s[4 * c + 1], s[4 * c + 2],
+                              s[4 * c + 3]);
+            }
+            fence_cluster();
+            __syncwarp();
+            if (lane == 0) mbar_arrive_cluster(peer_xfull);
+            ok = mbar_wait_cluster(&bar[kXFull], t & 1, p.err);
+            if (!ok) break;
+#pragma unroll
+            for (int c = 0; c < 16; ++c) {
+                const int pc = (c + h) & 15;
+                const float4 o = *reinterpret_cast<const float4 *>(xbuf + h * 256 + pc * 16);
+                s[4 * c] += o.x;
+                s[4 * c + 1] += o.y;
+                s[4 * c + 2] += o.z;
+                s[4 * c + 3] += o.w;
+            }
+            fence_cluster();
+            __syncwarp();
+            if (lane == 0) mbar_arrive_cluster(peer_xfree);
+
+            // ---- online softmax in base 2, lazy max --------------------------
+            float mt = -INFINITY;
+#pragma unroll
+            for (int j = 0; j < 64; ++j) {
+                s[j] = j < nvalid ? s[j] * p.qk_scale_log2 : -INFINITY;
+                mt = fmaxf(mt, s[j]);
+            }
+            const bool raise = mt > m_ref + kRescaleThreshold;   // always on the first tile
+            float alpha = 1.f;
+            if (raise) {
+                alpha = fast_exp2(m_ref - mt);                  // 0 when m_ref = -inf
+                m_ref = mt;
+            }
+            float rowsum = 0.f;
+            uint32_t pk[32];
+#pragma unroll
+            for (int j = 0; j < 32; ++j) {
+                const float p0 = fast_exp2(s[2 * j] - m_ref);
+                const float p1 = fast_exp2(s[2 * j + 1] - m_ref);
+                rowsum += p0 + p1;
+                pk[j] = pack_bf16x2(p0, p1);
+            }
+            l = l * alpha + rowsum;
+
+            // P(t-1)'s MMA must be done before P is overwritten or O rescaled.
+            if (t >= 1) {
+                ok = mbar_wait(&bar[kODone], (t - 1) & 1, p.err);
+                if (!ok) break;
+                tc::fence_after_sync();
+                if (__any_sync(0xffffffffu, raise)) {
+#pragma unroll 1
+                    for (int c = 0; c < 256; c += 32) {
+                        float v[32];
+                        tc::tmem_ld32(tmem + lane_base + kTmemO + c, v);
+#pragma unroll
+                        for (int j = 0; j < 32; ++j) v[j] *= alpha;
+                        tc::tmem_st32(tmem + lane_base + kTmemO + c, v);
+                    }
+                    tc::tmem_wait_st();
+                }
+            }
+            // P row h: 64 bf16 keys = 128 B, K-major with 128-byte swizzle.
+#pragma unroll
+            for (int c = 0; c < 8; ++c) {
+                uint4 v;
+                v.x = pk[4 * c]; v.y = pk[4 * c + 1]; v.z = pk[4 * c + 2]; v.w = pk[4 * c + 3];
+                *reinterpret_cast<uint4 *>(pbuf + p_swz(h, c)) = v;
+            }
+            if (nvalid < kBN) {
+                // Rows past the sequence end may hold anything (even NaN):
+                // zero them in the V part of the stage so 0 * V stays 0.
+                uint8_t *st = smem + Smem::kv + (t % kStages) * kStageBytes;
+                const int nz = (kBN - nvalid) * 4 * 8;   // 16-B chunks in 4 boxes
+                for (int i = h; i < nz; i += 128) {
+                    const int box = i / ((kBN - nvalid) * 8);
+                    const int rem = i - box * ((kBN - nvalid) * 8);
+                    const int row = nvalid + rem / 8;
+                    const int ch = rem & 7;
+                    *reinterpret_cast<uint4 *>(st + box * kKBoxBytes + row * 128 + ch * 16) =
+                        make_uint4(0u, 0u, 0u, 0u);
+                }
+            }
+            tc::fence_async_smem();
+            tc::fence_before_sync();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&bar[kPFull]);   // one arrival per softmax warp
+        }
+
+        // ---- epilogue ---------------------------------------------------------
+        if (ok && ntiles > 0) {
+            ok = mbar_wait(&bar[kODone], (ntiles - 1) & 1, p.err);
+            tc::fence_after_sync();
+        }
+        float scale_o = 0.f, Mf = -INFINITY, Z = 0.f;
+        if (direct) {
+            const float t2 = p.sink ? p.sink[h] * kLog2e : -INFINITY;
+            Mf = fmaxf(m_ref, t2);
+            float so = 0.f;
+            if (Mf != -INFINITY) {
+                so = fast_exp2(m_ref - Mf);
+                Z = l * so + fast_exp2(t2 - Mf);
+            }
+            scale_o = Z > 0.f ? so / Z : 0.f;
+        }
+        const size_t row = size_t(b) * kMlaHeads + h;
+#pragma unroll 1
+        for (int c = 0; c < 256; c += 32) {
+            float v[32];
+            if (ntiles > 0 && ok) {
+                tc::tmem_ld32(tmem + lane_base + kTmemO + c, v);
+            } else {
+#pragma unroll
+                for (int j = 0; j < 32; ++j) v[j] = 0.f;
+            }
+            if (direct) {
+                uint16_t *dst = p.out + row * kMlaDimV + rank * 256 + c;
+#pragma unroll
+                for (int j = 0; j < 32; j += 8) {
+                    uint4 w;
+                    w.x = pack_bf16x2(v[j] * scale_o, v[j + 1] * scale_o);
+                    w.y = pack_bf16x2(v[j + 2] * scale_o, v[j + 3] * scale_o);
+                    w.z = pack_bf16x2(v[j + 4] * scale_o, v[j + 5] * scale_o);
+                    w.w = pack_bf16x2(v[j + 6] * scale_o, v[j + 7] * scale_o);
+                    *reinterpret_cast<uint4 *>(dst + j) = w;
+                }
+            } else {
+                float *dst = p.ws_o + (size_t(part) * p.batch * kMlaHeads + row) * kMlaDimV +
+                             rank * 256 + c;
+#pragma unroll
+                for (int j = 0; j < 32; j += 4)
+                    *reinterpret_cast<float4 *>(dst + j) =
+                        make_float4(v[j], v[j + 1], v[j + 2], v[j + 3]);
+            }
+        }
+        if (rank == 0) {
+            if (direct) {
+                if (p.lse) p.lse[row] = Z > 0.f ? (Mf + fast_log2(Z)) * kLn2 : -INFINITY;
+            } else {
+                const size_t idx = size_t(part) * p.batch * kMlaHeads + row;
+                p.ws_m[idx] = m_ref * kLn2;
+                p.ws_l[idx] = l;
+            }
+        }
+        pdl_launch_dependents();
+    }
+
+    tc::fence_before_sync();
+    __syncthreads();
+    cluster_sync();  // no CTA leaves while its peer may still touch its smem
+    if (warp == 5) {
+        tc::fence_after_sync();
+        tc::tmem_dealloc(tmem, kTmemCols);
+    }
+}
+
+}  // namespace
+
+cudaError_t launch_mla_decode(const MlaParams &p, cudaStream_t stream) {
+    cudaError_t e = cudaFuncSetAttribute(mla_decode_kernel,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         int(kSmemBytes));
+    if (e != cudaSuccess) return e;
+    dim3 grid(2 * p.num_partitions, p.batch);
+    mla_decode_kernel<<<grid, kThreads, kSmemBytes, stream>>>(p);
+    return cudaGetLastError();
+}
+
+}  // namespace attn

@@ -1,0 +1,163 @@
+"""The C-ABI library without a GPU: it loads, exports every entry point the
+header declares, validates arguments on the host (no launch), and the
+partition planner follows its stated formulas."""
+import ctypes
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER_DIR = os.path.join(ROOT, "include")
+
+
+@pytest.fixture(scope="module")
+def attn():
+    from split_flash_decoding_gb300 import build
+    build.build()
+    from split_flash_decoding_gb300 import attn as a
+    return a
+
+
+def declared_functions():
+    names = set()
+    for f in os.listdir(HEADER_DIR):
+        if f.endswith(".h"):
+            text = open(os.path.join(HEADER_DIR, f)).read()
+            text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+            names.update(re.findall(r"^\s*int\s+(attn_\w+)\s*\(", text, flags=re.M))
+    return sorted(names)
+
+
+def test_header_declares_the_entry_points():
+    names = declared_functions()
+    for required in ("attn_decode", "attn_mla_decode", "attn_splitk_reduce",
+                     "attn_plan_partitions"):
+        assert required in names
+
+
+def test_library_exports_every_declared_symbol(attn):
+    handle = ctypes.CDLL(attn.LIB_PATH)
+    for name in declared_functions():
+        assert hasattr(handle, name), name
+    assert set(declared_functions()) <= set(attn._SIGNATURES)
+
+
+def test_struct_layout_matches_header(attn):
+    # attn_kv_t: pointer, 3 x int64, 2 x int32, pointer, 2 x int32
+    assert ctypes.sizeof(attn.attn_kv_t) == 56
+    assert attn.attn_kv_t.page_table.offset == 40
+
+
+def kv(attn, **over):
+    d = attn.attn_kv_t()
+    d.base = 0x10000
+    d.page_stride = 128 * 8 * 128
+    d.token_stride = 8 * 128
+    d.head_stride = 128
+    d.page_size = 128
+    d.num_pages = 10
+    d.page_table = 0x20000
+    d.max_pages = 4
+    d.reserved = 0
+    for k, v in over.items():
+        setattr(d, k, v)
+    return d
+
+
+def call_decode(attn, k=None, v=None, **over):
+    args = dict(q=0x30000, kv_len=0x40000, batch=2, hq=32, group=4, d=128, max_kv_len=500,
+                scale=0.088, sink=None, P=1, ws=None, ws_bytes=0, out=0x50000, lse=None)
+    args.update(over)
+    k = k or kv(attn)
+    v = v or kv(attn)
+    return attn.lib().attn_decode(args["q"], ctypes.byref(k), ctypes.byref(v), args["kv_len"],
+                                  args["batch"], args["hq"], args["group"], args["d"],
+                                  args["max_kv_len"], args["scale"], args["sink"], args["P"],
+                                  args["ws"], args["ws_bytes"], args["out"], args["lse"], None)
+
+
+def test_decode_rejects_bad_arguments_before_launch(attn):
+    E = attn
+    assert call_decode(attn, q=None) == E.ATTN_ERR_INVALID_ARG
+    assert call_decode(attn, out=None) == E.ATTN_ERR_INVALID_ARG
+    assert call_decode(attn, kv_len=None) == E.ATTN_ERR_INVALID_ARG
+    assert call_decode(attn, hq=30, group=4) == E.ATTN_ERR_INVALID_ARG
+    assert call_decode(attn, group=0) == E.ATTN_ERR_INVALID_ARG
+    assert call_decode(attn, hq=48, group=16) == E.ATTN_ERR_UNSUPPORTED
+    assert call_decode(attn, d=96) == E.ATTN_ERR_UNSUPPORTED
+    assert call_decode(attn, P=0) == E.ATTN_ERR_INVALID_ARG
+    assert call_decode(attn, P=E.ATTN_MAX_PARTITIONS + 1) == E.ATTN_ERR_INVALID_ARG
+    assert call_decode(attn, scale=float("nan")) == E.ATTN_ERR_INVALID_ARG
+    assert call_decode(attn, max_kv_len=-1) == E.ATTN_ERR_INVALID_ARG
+    assert call_decode(attn, q=0x30008) == E.ATTN_ERR_INVALID_ARG          # misaligned
+    assert call_decode(attn, k=kv(attn, base=0)) == E.ATTN_ERR_INVALID_ARG
+    assert call_decode(attn, k=kv(attn, base=0x10008)) == E.ATTN_ERR_INVALID_ARG
+    assert call_decode(attn, k=kv(attn, reserved=1)) == E.ATTN_ERR_INVALID_ARG
+    assert call_decode(attn, k=kv(attn, token_stride=1020)) == E.ATTN_ERR_INVALID_ARG
+    assert call_decode(attn, k=kv(attn, page_size=96)) == E.ATTN_ERR_UNSUPPORTED
+    assert call_decode(attn, k=kv(attn, page_size=4)) == E.ATTN_ERR_UNSUPPORTED
+    assert call_decode(attn, k=kv(attn, max_pages=3)) == E.ATTN_ERR_INVALID_ARG  # 500 > 3*128
+    assert call_decode(attn, k=kv(attn, page_table=None, page_size=400, num_pages=2)) \
+        == E.ATTN_ERR_INVALID_ARG                                             # capacity < 500
+    assert call_decode(attn, k=kv(attn, page_table=None, page_size=512, num_pages=1)) \
+        == E.ATTN_ERR_INVALID_ARG                                             # fewer seqs
+    # K and V must share one page-table layout
+    assert call_decode(attn, v=kv(attn, page_table=0x20100)) == E.ATTN_ERR_UNSUPPORTED
+    # split-K needs a large enough, aligned workspace
+    assert call_decode(attn, P=4) == E.ATTN_ERR_WORKSPACE
+    assert call_decode(attn, P=4, ws=0x60000, ws_bytes=16) == E.ATTN_ERR_WORKSPACE
+    P, need = attn.attn_plan_partitions(2, 2, 32, 8, 128, 500, 4, num_sms=152)
+    assert call_decode(attn, P=4, ws=0x60010, ws_bytes=need) == E.ATTN_ERR_WORKSPACE
+    # an empty batch is a no-op
+    assert call_decode(attn, batch=0, q=None, out=None) == E.ATTN_OK
+
+
+def test_reduce_rejects_bad_arguments(attn):
+    L = attn.lib()
+    f = L.attn_splitk_reduce
+    assert f(0x1000, 0x2000, 0x3000, 0, 4, 8, 128, None, 0x4000, None, None) == attn.ATTN_ERR_INVALID_ARG
+    assert f(0x1000, 0x2000, 0x3000, 2, 4, 8, 130, None, 0x4000, None, None) == attn.ATTN_ERR_INVALID_ARG
+    assert f(None, 0x2000, 0x3000, 2, 4, 8, 128, None, 0x4000, None, None) == attn.ATTN_ERR_INVALID_ARG
+    assert f(0x1000, 0x2000, 0x3000, 2, 0, 8, 128, None, None, None, None) == attn.ATTN_OK
+
+
+def test_planner_formulas(attn):
+    # explicit request is honoured verbatim
+    for req in (1, 2, 7, 148, 1024):
+        P, ws = attn.attn_plan_partitions(64, 64, 32, 8, 128, 8192, req, num_sms=152)
+        assert P == req
+        n = req * 64 * 32
+        align = lambda x: (x + 255) // 256 * 256
+        expect = 0 if req == 1 else align(n * 128 * 4) + 2 * align(n * 4)
+        assert ws == expect
+    # automatic: at least one wave of CTAs, slices of about 512 keys
+    P, _ = attn.attn_plan_partitions(64, 64, 32, 8, 128, 8192, 0, num_sms=152)
+    assert P == 16
+    P, _ = attn.attn_plan_partitions(1, 1, 32, 8, 128, 131072, 0, num_sms=152)
+    assert 8 * P >= 2 * 152
+    P, _ = attn.attn_plan_partitions(1, 1, 32, 8, 128, 20, 0, num_sms=152)
+    assert P == 1                                     # one tile of keys cannot split
+    P, _ = attn.attn_plan_partitions(4, 4, 32, 8, 128, 0, 0, num_sms=152)
+    assert P == 1
+    # more SMs never means fewer partitions
+    prev = 0
+    for sms in (16, 64, 132, 152, 304):
+        P, _ = attn.attn_plan_partitions(2, 2, 32, 8, 128, 65536, 0, num_sms=sms)
+        assert P >= prev
+        prev = P
+    with pytest.raises(attn.AttnError):
+        attn.attn_plan_partitions(2, 2, 30, 8, 128, 100, 0, num_sms=152)
+    with pytest.raises(attn.AttnError):
+        attn.attn_plan_partitions(2, 2, 32, 8, 128, 100, attn.ATTN_MAX_PARTITIONS + 1,
+                                  num_sms=152)
+
+
+def test_product_package_does_not_import_the_oracle():
+    pkg = os.path.join(ROOT, "split_flash_decoding_gb300")
+    for dirpath, _, files in os.walk(pkg):
+        for f in files:
+            if f.endswith((".py", ".cu", ".cuh", ".h", ".cpp")):
+                text = open(os.path.join(dirpath, f)).read()
+                assert not re.search(r"^\s*(import|from)\s+oracle", text, flags=re.M), f
+                assert "attn_oracle" not in text, f
