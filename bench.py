@@ -53,7 +53,7 @@ def parse():
     ap.add_argument("--warmup", type=int, default=50)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default="llama3",
-                    choices=["llama3", "long_context", "mla", "tiny"])
+                    choices=["llama3", "long_context", "mla", "mixed", "tiny"])
     ap.add_argument("--partitions", type=int, default=0, help="0 = planner's choice")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     return ap.parse_args()
@@ -164,6 +164,8 @@ def build_workload(name: str, device):
         return W.long_context_decode(device=device)
     if name == "mla":
         return W.deepseek_v3_mla_decode(device=device)
+    if name == "mixed":
+        return W.mixed_prefill_decode(device=device)
     if name == "tiny":
         return W.tiny_decode(device=device)
     raise ValueError(name)
@@ -183,9 +185,25 @@ def algorithmic_bytes(w) -> int:
     return kv + q + o + lse
 
 
+def visible_pairs(w) -> int:
+    """(row, key) pairs the mask lets through, summed over sequences."""
+    if w.q_row_offsets_host is None:
+        return sum(w.kv_len_host)
+    total = 0
+    o = w.q_row_offsets_host
+    for b, L in enumerate(w.kv_len_host):
+        n = o[b + 1] - o[b]
+        if not w.causal:
+            total += n * L
+        else:
+            # row i sees min(L, L - n + i + 1) keys (at least 0)
+            for i in range(n):
+                total += max(0, min(L, L - n + i + 1))
+    return total
+
+
 def algorithmic_flops(w) -> int:
-    total_keys = sum(w.kv_len_host)
-    return total_keys * w.num_q_heads * 2 * (w.dim_qk + w.dim_v)
+    return visible_pairs(w) * w.num_q_heads * 2 * (w.dim_qk + w.dim_v)
 
 
 # ---------------------------------------------------------------------------
@@ -293,6 +311,8 @@ def run_ours(args, rank, world, dist):
     if w.is_mla:
         P, ws_bytes = attn.attn_plan_partitions(w.batch, w.rows, w.num_q_heads, 1, w.dim_v,
                                                 w.max_kv_len, args.partitions)
+    elif w.max_q_len > 1:
+        P, ws_bytes = 1, 0
     else:
         P, ws_bytes = attn.attn_plan_partitions(w.batch, w.rows, w.num_q_heads,
                                                 w.num_kv_heads, w.dim_v, w.max_kv_len,
@@ -309,7 +329,9 @@ def run_ours(args, rank, world, dist):
         else:
             attn.attn_decode(q, w.k_cache, w.v_cache, kv_len, group=w.group, scale=w.scale,
                              max_kv_len=w.max_kv_len, page_table=page_table, sink=w.sink,
-                             num_partitions=P, workspace=ws, out=o, lse=l, stream=stream)
+                             q_row_offsets=w.q_row_offsets, max_q_len=w.max_q_len,
+                             causal=w.causal, num_partitions=P, workspace=ws, out=o, lse=l,
+                             stream=stream)
 
     launches_per_call = 1 if P == 1 else 2
     nbytes = algorithmic_bytes(w)
@@ -398,8 +420,10 @@ def run_ours(args, rank, world, dist):
 
     ms_per_step = total_ms / args.steps
     value = world * nbytes / (ms_per_step * 1e-3) / 1e9
-    peak, peak_kind, _ = measured_peaks()
+    peak, peak_kind, peaks = measured_peaks()
     achieved = nbytes / (mean_call_ms * 1e-3) / 1e9
+    tflops = flops / (mean_call_ms * 1e-3) / 1e12
+    tensor_peak = float(peaks.get("bf16_tflops", 1900.0))
     kernel_key = "gqa_decode" if not w.is_mla else "mla_decode"
     traffic = profiled_traffic(kernel_key, w.name) if kernel_key in KERNEL_SOURCES else None
     cpu = None
@@ -451,6 +475,10 @@ def run_ours(args, rank, world, dist):
                      "kernel": "attn_decode call (partition kernel + split-K reduce), "
                                "CUDA events per call on the launch stream"},
         "cpu_baseline": cpu,
+        "tensor": {"achieved_tflops": round(tflops, 2), "peak_tflops": tensor_peak,
+                   "frac": round(tflops / tensor_peak, 4),
+                   "note": "algorithmic FLOPs (visible pairs x 2 x (d_qk + d_v) per head) "
+                           "over the per-call time; only meaningful for the tensor-core paths"},
     }
     print(json.dumps(line), flush=True)
 

@@ -110,7 +110,10 @@ typedef struct attn_kv {
  *                 for this P (0 when P == 1).
  *
  * Key slice p of a sequence is [p*C, min((p+1)*C, kv_len)) with
- * C = ceil(ceil(max_kv_len / P) / 32) * 32; slices past kv_len are empty.
+ * C = ceil(ceil(max_kv_len / P) / T) * T, T = 32 for attn_decode and 64 for
+ * attn_mla_decode; slices past kv_len are empty.  The automatic choice
+ * treats num_kv_heads == 1 with head_dim_v == 512 as the MLA shape (longer
+ * slices, one two-CTA cluster per SM pair) and everything else as GQA.
  * Returns ATTN_OK, ATTN_ERR_INVALID_ARG, or ATTN_ERR_CUDA if the SM count
  * query fails.  Launches nothing.
  */
@@ -119,37 +122,54 @@ int attn_plan_partitions(int num_sms, int batch, int num_q_rows, int num_q_heads
                          int *num_partitions, size_t *workspace_bytes);
 
 /*
- * attn_decode -- GQA/MHA decode attention over a paged or contiguous cache
- * with split-K (mha_decoding_single_batch_pipelined; mha_sm100_dispatch).
+ * attn_decode -- GQA/MHA attention of few query rows per sequence against a
+ * paged or contiguous cache, with split-K for single-token decode
+ * (mha_decoding_single_batch_pipelined; mha_sm100_dispatch).
  *
- *   q          device bf16 [batch][num_q_heads][head_dim] (one query token
- *              per sequence; "q_arg: Pointer to the query tensor data").
+ *   q          device bf16 [num_q_rows][num_q_heads][head_dim]
+ *              ("q_arg: Pointer to the query tensor data").
  *   k, v       cache operands (host structs describing device memory); both
  *              head_dim wide and sharing one page table layout.
- *   kv_len     device uint32 [batch]: keys of sequence b ("valid_length:
- *              Per-row valid KV length pointer").  The cache already holds
- *              the current token's K/V.
- *   batch, num_q_heads, group   num_q_heads % group == 0; group <= 8.
- *   head_dim   64 or 128.
+ *   kv_len     device uint32 [batch]: keys of sequence b, including its own
+ *              query tokens ("valid_length: Per-row valid KV length
+ *              pointer").  The cache already holds the current tokens' K/V.
+ *   q_row_offsets  device uint32 [batch + 1] (rows of sequence b are
+ *              [off[b], off[b+1])), or NULL for one row per sequence.
+ *   batch, num_q_rows   sequences and total query rows (num_q_rows = batch
+ *              when q_row_offsets is NULL; otherwise = off[batch]).
+ *   num_q_heads, group  num_q_heads % group == 0; group in {1, 2, 4, 8}.
+ *   head_dim   64 or 128 (128 when max_q_len > 1).
+ *   max_q_len  host upper bound of the rows of any sequence ("max_prompt_len
+ *              ... optionally static").  1 selects the split-K decode
+ *              kernel; > 1 selects the tensor-core tile kernel, which takes
+ *              every sequence of the batch, single-token ones included
+ *              ("a single-token prompt is just the shortest prefill",
+ *              mha_sm100_dispatch, summary).
  *   max_kv_len host upper bound of kv_len ("max_cache_valid_length_arg").
  *   scale      multiplies Q.K' before the softmax.
  *   sink       device fp32 [num_q_heads] attention-sink logits, or NULL.
  *              A sink adds exp(sink[h]) to the softmax normaliser of head h
  *              and carries no value; it is not multiplied by scale.
- *   num_partitions  P from attn_plan_partitions (or any 1..MAX).
+ *   causal     non-zero: row i of a sequence with n rows and L keys sees
+ *              keys j <= L - n + i (bottom-right aligned).  A no-op for
+ *              single-row sequences.
+ *   num_partitions  P from attn_plan_partitions (or any 1..MAX); must be 1
+ *              when max_q_len > 1.
  *   workspace  device, 256-byte aligned, >= the planner's workspace_bytes
  *              for this P; may be NULL when P == 1.  Contents on entry are
  *              ignored; it holds fp32 partial O, qk_max and exp_sum after.
- *   out        device bf16 [batch][num_q_heads][head_dim].
- *   lse        device fp32 [batch][num_q_heads], or NULL.
+ *   out        device bf16 [num_q_rows][num_q_heads][head_dim].
+ *   lse        device fp32 [num_q_rows][num_q_heads], or NULL.
  *
- * Launches the partition kernel (grid: P x num_kv_heads x batch) and, for
- * P > 1, the split-K reduce.  Returns ATTN_OK or an error status.
+ * Single-token decode launches the partition kernel (grid: P x num_kv_heads
+ * x batch) and, for P > 1, the split-K reduce.  Returns ATTN_OK or an error
+ * status.
  */
 int attn_decode(const void *q, const attn_kv_t *k, const attn_kv_t *v, const uint32_t *kv_len,
-                int batch, int num_q_heads, int group, int head_dim, int max_kv_len, float scale,
-                const float *sink, int num_partitions, void *workspace, size_t workspace_bytes,
-                void *out, float *lse, attn_stream_t stream);
+                const uint32_t *q_row_offsets, int batch, int num_q_rows, int num_q_heads,
+                int group, int head_dim, int max_q_len, int max_kv_len, float scale,
+                const float *sink, int causal, int num_partitions, void *workspace,
+                size_t workspace_bytes, void *out, float *lse, attn_stream_t stream);
 
 /*
  * attn_mla_decode -- multi-head latent attention decode: one KV head whose

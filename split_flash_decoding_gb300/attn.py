@@ -61,8 +61,9 @@ _SIGNATURES = {
                              _c.c_int, _c.c_int, _c.POINTER(_c.c_int),
                              _c.POINTER(_c.c_size_t)],
     "attn_decode": [_c.c_void_p, _c.POINTER(attn_kv_t), _c.POINTER(attn_kv_t), _c.c_void_p,
-                    _c.c_int, _c.c_int, _c.c_int, _c.c_int, _c.c_int, _c.c_float, _c.c_void_p,
-                    _c.c_int, _c.c_void_p, _c.c_size_t, _c.c_void_p, _c.c_void_p, _c.c_void_p],
+                    _c.c_void_p, _c.c_int, _c.c_int, _c.c_int, _c.c_int, _c.c_int, _c.c_int,
+                    _c.c_int, _c.c_float, _c.c_void_p, _c.c_int, _c.c_int, _c.c_void_p,
+                    _c.c_size_t, _c.c_void_p, _c.c_void_p, _c.c_void_p],
     "attn_mla_decode": [_c.c_void_p, _c.POINTER(attn_kv_t), _c.c_void_p, _c.c_int, _c.c_int,
                         _c.c_int, _c.c_int, _c.c_int, _c.c_float, _c.c_void_p, _c.c_int,
                         _c.c_void_p, _c.c_size_t, _c.c_void_p, _c.c_void_p, _c.c_void_p],
@@ -168,28 +169,36 @@ def _workspace(nbytes: int, device, workspace: Optional[torch.Tensor]):
 def attn_decode(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tensor,
                 kv_len: torch.Tensor, *, group: int, scale: float, max_kv_len: int,
                 page_table: Optional[torch.Tensor] = None, sink: Optional[torch.Tensor] = None,
-                num_partitions: int = 0, workspace: Optional[torch.Tensor] = None,
-                out: Optional[torch.Tensor] = None, lse: Optional[torch.Tensor] = None,
-                return_lse: bool = True, stream=None):
-    """Decode attention (one query token per sequence) through attn_decode.
+                q_row_offsets: Optional[torch.Tensor] = None, max_q_len: int = 1,
+                causal: bool = False, num_partitions: int = 0,
+                workspace: Optional[torch.Tensor] = None, out: Optional[torch.Tensor] = None,
+                lse: Optional[torch.Tensor] = None, return_lse: bool = True, stream=None):
+    """Attention of q rows against a KV cache through attn_decode.
 
-    q bf16 [batch, num_q_heads, head_dim]; caches as for kv_descriptor;
-    kv_len int32/uint32 [batch] on the device; sink fp32 [num_q_heads] or
-    None.  num_partitions 0 plans automatically.  Returns (out, lse).
+    q bf16 [rows, num_q_heads, head_dim] (rows = batch for single-token
+    decode, else q_row_offsets[-1]); caches as for kv_descriptor; kv_len
+    int32/uint32 [batch] on the device; q_row_offsets int32 [batch + 1] on
+    the device or None; sink fp32 [num_q_heads] or None.  num_partitions 0
+    plans automatically (always 1 when max_q_len > 1).  Returns (out, lse).
     """
-    batch, hq, d = q.shape
+    rows, hq, d = q.shape
+    batch = kv_len.shape[0]
     if out is None:
-        out = torch.empty((batch, hq, d), dtype=torch.bfloat16, device=q.device)
+        out = torch.empty((rows, hq, d), dtype=torch.bfloat16, device=q.device)
     if lse is None and return_lse:
-        lse = torch.empty((batch, hq), dtype=torch.float32, device=q.device)
-    P, ws_bytes = attn_plan_partitions(batch, batch, hq, hq // group, d, max_kv_len,
-                                       num_partitions)
+        lse = torch.empty((rows, hq), dtype=torch.float32, device=q.device)
+    if max_q_len > 1:
+        P, ws_bytes = 1, 0
+    else:
+        P, ws_bytes = attn_plan_partitions(batch, rows, hq, hq // group, d, max_kv_len,
+                                           num_partitions)
     ws, ws_size = _workspace(ws_bytes, q.device, workspace)
     kd = kv_descriptor(k_cache, page_table)
     vd = kv_descriptor(v_cache, page_table)
     _check("attn_decode",
            lib().attn_decode(q.data_ptr(), ctypes.byref(kd), ctypes.byref(vd), kv_len.data_ptr(),
-                             batch, hq, group, d, max_kv_len, scale, _ptr(sink), P, _ptr(ws),
+                             _ptr(q_row_offsets), batch, rows, hq, group, d, max_q_len,
+                             max_kv_len, scale, _ptr(sink), 1 if causal else 0, P, _ptr(ws),
                              ws_size, out.data_ptr(), _ptr(lse), _stream_handle(stream)))
     return out, lse
 

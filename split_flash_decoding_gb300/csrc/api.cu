@@ -128,6 +128,79 @@ int check_kv(const attn_kv_t *kv, int batch, int dim, int max_kv_len) {
 
 int map_cuda(cudaError_t e) { return e == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA; }
 
+int prefill_path(const void *q, const attn_kv_t *k, const attn_kv_t *v, const uint32_t *kv_len,
+                 const uint32_t *q_row_offsets, int batch, int num_q_rows, int num_q_heads,
+                 int group, int head_dim, int max_q_len, int max_kv_len, float scale,
+                 const float *sink, int causal, void *out, float *lse, attn_stream_t stream);
+
+}  // namespace
+}  // namespace attn
+
+
+namespace attn {
+namespace {
+
+int prefill_path(const void *q, const attn_kv_t *k, const attn_kv_t *v, const uint32_t *kv_len,
+                 const uint32_t *q_row_offsets, int batch, int num_q_rows, int num_q_heads,
+                 int group, int head_dim, int max_q_len, int max_kv_len, float scale,
+                 const float *sink, int causal, void *out, float *lse, attn_stream_t stream) {
+    if (head_dim != 128) return ATTN_ERR_UNSUPPORTED;
+    if (group != 1 && group != 2 && group != 4 && group != 8) return ATTN_ERR_UNSUPPORTED;
+    if (reinterpret_cast<uintptr_t>(out) % 16 || reinterpret_cast<uintptr_t>(q) % 16)
+        return ATTN_ERR_INVALID_ARG;
+    const int hkv = num_q_heads / group;
+    int st = check_kv(k, batch, head_dim, max_kv_len);
+    if (st) return st;
+    st = check_kv(v, batch, head_dim, max_kv_len);
+    if (st) return st;
+    if (k->page_table != v->page_table || k->page_size != v->page_size ||
+        k->max_pages != v->max_pages || k->num_pages != v->num_pages)
+        return ATTN_ERR_UNSUPPORTED;
+
+    TileParams p;
+    std::memset(&p, 0, sizeof(p));
+    p.box_rows = k->page_table ? (k->page_size < kTileKeys ? k->page_size : kTileKeys)
+                               : kTileKeys;
+    st = encode_kv_map(&p.k_map, *k, head_dim, hkv, p.box_rows);
+    if (st) return st;
+    st = encode_kv_map(&p.v_map, *v, head_dim, hkv, p.box_rows);
+    if (st) return st;
+    const int tokens = kTileRows / group;
+    {
+        EncodeTiledFn fn = encode_fn();
+        if (!fn) return ATTN_ERR_CUDA;
+        cuuint64_t gdim[4] = {128, cuuint64_t(group), cuuint64_t(hkv), cuuint64_t(num_q_rows)};
+        cuuint64_t gstride[3] = {128 * 2, cuuint64_t(group) * 128 * 2,
+                                 cuuint64_t(num_q_heads) * 128 * 2};
+        cuuint32_t box[4] = {64, cuuint32_t(group), 1, cuuint32_t(tokens)};
+        cuuint32_t estride[4] = {1, 1, 1, 1};
+        CUresult r = fn(&p.q_map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void *>(q),
+                        gdim, gstride, box, estride, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                        CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                        CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+        if (r != CUDA_SUCCESS) return ATTN_ERR_UNSUPPORTED;
+    }
+    st = error_word(&p.err);
+    if (st) return st;
+    p.kv_len = kv_len;
+    p.q_row_offsets = q_row_offsets;
+    p.page_table = k->page_table;
+    p.sink = sink;
+    p.out = static_cast<uint16_t *>(out);
+    p.lse = lse;
+    p.batch = batch;
+    p.num_q_rows = num_q_rows;
+    p.num_q_heads = num_q_heads;
+    p.group = group;
+    p.max_pages = k->max_pages;
+    p.page_size = k->page_size;
+    p.num_pages = k->num_pages;
+    p.causal = causal ? 1 : 0;
+    p.tiles_per_seq = (max_q_len + tokens - 1) / tokens;
+    p.qk_scale_log2 = scale * 1.4426950408889634f;
+    return map_cuda(launch_tile_attention(p, reinterpret_cast<cudaStream_t>(stream)));
+}
+
 }  // namespace
 }  // namespace attn
 
@@ -152,16 +225,21 @@ extern "C" int attn_plan_partitions(int num_sms, int batch, int num_q_rows, int 
                     cudaSuccess)
                 return ATTN_ERR_CUDA;
         }
-        // Fill at least one wave of CTAs (two resident per SM) even if every
-        // sequence had max_kv_len keys, and keep slices near 512 keys so the
-        // last wave of a ragged batch is short.
+        // MLA shapes (one KV head, 512 output channels) run one two-CTA
+        // cluster per SM pair and write 256 KB of fp32 partials per slice, so
+        // their slices are long (~4096 keys); GQA runs two CTAs per SM and
+        // uses ~512-key slices so the last wave of a ragged batch is short.
+        // Either way, at least one full wave of CTAs is planned as if every
+        // sequence had max_kv_len keys.
+        const bool mla = num_kv_heads == 1 && head_dim_v == kMlaDimV;
         const long long units = static_cast<long long>(batch > 0 ? batch : 1) * num_kv_heads;
-        const long long slots = 2LL * num_sms;
+        const long long slots = mla ? num_sms / 2 : 2LL * num_sms;
+        const long long target = mla ? 4096 : 512;
+        const long long tile = mla ? kMlaTileKeys : kGqaTileKeys;
         long long p_fill = (slots + units - 1) / units;
-        long long p_len = (static_cast<long long>(max_kv_len) + 511) / 512;
+        long long p_len = (static_cast<long long>(max_kv_len) + target - 1) / target;
         long long p = p_fill > p_len ? p_fill : p_len;
-        const long long p_max_useful = (static_cast<long long>(max_kv_len) + kGqaTileKeys - 1) /
-                                       kGqaTileKeys;
+        const long long p_max_useful = (static_cast<long long>(max_kv_len) + tile - 1) / tile;
         if (p > p_max_useful) p = p_max_useful;
         if (p < 1) p = 1;
         if (p > ATTN_MAX_PARTITIONS) p = ATTN_MAX_PARTITIONS;
@@ -173,17 +251,28 @@ extern "C" int attn_plan_partitions(int num_sms, int batch, int num_q_rows, int 
 }
 
 extern "C" int attn_decode(const void *q, const attn_kv_t *k, const attn_kv_t *v,
-                           const uint32_t *kv_len, int batch, int num_q_heads, int group,
-                           int head_dim, int max_kv_len, float scale, const float *sink,
-                           int num_partitions, void *workspace, size_t workspace_bytes,
-                           void *out, float *lse, attn_stream_t stream) {
-    if (batch < 0 || num_q_heads <= 0 || group <= 0 || max_kv_len < 0)
+                           const uint32_t *kv_len, const uint32_t *q_row_offsets, int batch,
+                           int num_q_rows, int num_q_heads, int group, int head_dim,
+                           int max_q_len, int max_kv_len, float scale, const float *sink,
+                           int causal, int num_partitions, void *workspace,
+                           size_t workspace_bytes, void *out, float *lse, attn_stream_t stream) {
+    if (batch < 0 || num_q_rows < 0 || num_q_heads <= 0 || group <= 0 || max_kv_len < 0 ||
+        max_q_len < 1)
         return ATTN_ERR_INVALID_ARG;
     if (num_q_heads % group) return ATTN_ERR_INVALID_ARG;
     if (num_partitions < 1 || num_partitions > ATTN_MAX_PARTITIONS) return ATTN_ERR_INVALID_ARG;
     if (!(scale == scale)) return ATTN_ERR_INVALID_ARG;
-    if (batch == 0) return ATTN_OK;
+    if (!q_row_offsets && (num_q_rows != batch || max_q_len != 1)) return ATTN_ERR_INVALID_ARG;
+    if (batch == 0 || num_q_rows == 0) return ATTN_OK;
     if (!q || !kv_len || !out) return ATTN_ERR_INVALID_ARG;
+    if (max_q_len > 1) {
+        // Tensor-core tile path for multi-row sequences (not split).
+        if (num_partitions != 1) return ATTN_ERR_UNSUPPORTED;
+        return prefill_path(q, k, v, kv_len, q_row_offsets, batch, num_q_rows, num_q_heads,
+                            group, head_dim, max_q_len, max_kv_len, scale, sink, causal, out,
+                            lse, stream);
+    }
+    if (q_row_offsets && num_q_rows != batch) return ATTN_ERR_INVALID_ARG;
     if (group != 1 && group != 2 && group != 4 && group != 8) return ATTN_ERR_UNSUPPORTED;
     if (head_dim != 64 && head_dim != 128) return ATTN_ERR_UNSUPPORTED;
     if (reinterpret_cast<uintptr_t>(out) % 16 || reinterpret_cast<uintptr_t>(q) % 16)

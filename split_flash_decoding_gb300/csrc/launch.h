@@ -57,6 +57,29 @@ struct MlaParams {
     float qk_scale_log2;
 };
 
+// Multi-row (prefill-shaped) tile kernel: 128 MMA rows = (128 / group)
+// tokens x group heads of one KV head; 128-key tiles.
+constexpr int kTileRows = 128;
+constexpr int kTileKeys = 128;
+
+struct TileParams {
+    CUtensorMap q_map;            // 4-D: (channel, head in group, kv head, row)
+    CUtensorMap k_map;            // 4-D: (channel, slot, kv head, page)
+    CUtensorMap v_map;
+    const uint32_t *kv_len;       // [batch]
+    const uint32_t *q_row_offsets;  // [batch + 1]
+    const int32_t *page_table;    // [batch][max_pages] or nullptr
+    const float *sink;            // [Hq] or nullptr
+    uint16_t *out;                // bf16 [rows][Hq][128]
+    float *lse;                   // [rows][Hq] or nullptr
+    unsigned *err;
+    int batch, num_q_rows, num_q_heads, group;
+    int max_pages, page_size, num_pages, box_rows;
+    int causal;
+    int tiles_per_seq;            // grid.x = ceil(max_q_len / (128 / group))
+    float qk_scale_log2;
+};
+
 struct ReduceParams {
     const float *ws_o, *ws_m, *ws_l;
     const float *sink;            // [Hq] or nullptr
@@ -69,6 +92,7 @@ struct ReduceParams {
 
 cudaError_t launch_gqa_decode(const GqaParams &p, cudaStream_t stream);
 cudaError_t launch_mla_decode(const MlaParams &p, cudaStream_t stream);
+cudaError_t launch_tile_attention(const TileParams &p, cudaStream_t stream);
 cudaError_t launch_splitk_reduce(const ReduceParams &p, cudaStream_t stream, bool pdl);
 
 }  // namespace attn

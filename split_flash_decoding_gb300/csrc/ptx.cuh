@@ -15,7 +15,7 @@ constexpr unsigned kErrBadPage = 2u;
 constexpr unsigned kErrBadLength = 4u;
 
 // A pipeline wait gives up after this many nanoseconds of global time.
-constexpr unsigned long long kWaitLimitNs = 2000000000ull;  // 2 s
+constexpr unsigned long long kWaitLimitNs = 250000000ull;  // 250 ms
 
 __device__ __forceinline__ uint32_t smem_addr(const void *p) {
     return static_cast<uint32_t>(__cvta_generic_to_shared(p));
@@ -39,6 +39,13 @@ __device__ __forceinline__ void fence_mbar_init() {
 __device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t *bar, uint32_t bytes) {
     asm volatile("mbarrier.arrive.expect_tx.release.cta.shared::cta.b64 _, [%0], %1;" ::"r"(
                      smem_addr(bar)),
+                 "r"(bytes)
+                 : "memory");
+}
+
+// Retire `bytes` of an mbarrier's expected transaction count without an arrival.
+__device__ __forceinline__ void mbar_complete_tx(uint64_t *bar, uint32_t bytes) {
+    asm volatile("mbarrier.complete_tx.shared::cta.b64 [%0], %1;" ::"r"(smem_addr(bar)),
                  "r"(bytes)
                  : "memory");
 }

@@ -1,0 +1,387 @@
+// tile_attention.cu -- tensor-core (tcgen05) attention tiles for batches
+// whose sequences carry several query rows (ragged prefill mixed with
+// decode), with a causal mask aligned to the end of the cache.
+//
+// "Decode is not a separate route: a single-token prompt is just the
+// shortest prefill" (mha_sm100_dispatch, summary): every sequence of the
+// batch, single-row ones included, is cut into tiles of 128 MMA rows.  A tile
+// holds T = 128 / group consecutive tokens x the group's query heads of one
+// KV head, so each K/V tile fetched serves all heads of the group.  Row r is
+// token r / group, head r % group -- exactly the memory order of q, so one
+// 4-D TMA box (64 channels x group heads x 1 KV head x T tokens) loads it.
+//
+// Per 128-key tile: S = Q K^T (M=128, N=128, K=128) into a double-buffered
+// TMEM accumulator, online softmax by four warps (thread = row, causal and
+// length masks applied per element), P (bf16) to shared memory, then
+// O += P V (M=128, N=128, K=128) in TMEM.  The running max is lazy: it is
+// raised, and O rescaled, only when a tile's max exceeds it by more than 8
+// (base 2).  No split-K: each CTA covers all keys its rows can see.
+//
+// Warp roles (192 threads): 0-3 softmax/epilogue, 4 TMA producer, 5 TMEM
+// allocation + MMA issue.
+#include "launch.h"
+#include "ptx.cuh"
+#include "tc.cuh"
+
+namespace attn {
+namespace {
+
+constexpr int kD = 128;
+constexpr int kBN = kTileKeys;               // keys per tile
+constexpr int kStages = 2;
+constexpr int kBoxBytes = 128 * 128;         // 128 rows x 128 B (64 channels)
+constexpr int kTileBytes = 2 * kBoxBytes;    // 128 rows x 128 channels
+constexpr int kStageBytes = 2 * kTileBytes;  // K + V
+constexpr int kThreads = 192;
+constexpr uint32_t kTmemCols = 512;
+constexpr uint32_t kTmemS = 0;               // S buffers at 0 and 128
+constexpr uint32_t kTmemO = 256;
+constexpr float kRescaleThreshold = 8.0f;
+
+// V as the MN-major B operand: two 64-channel blocks 16 KB apart, 8-key
+// groups 1 KB apart.
+constexpr uint32_t kVLbo = kBoxBytes;
+constexpr uint32_t kVSbo = 1024;
+
+struct Smem {
+    static constexpr int q = 0;                                  // 32 KB
+    static constexpr int kv = q + kTileBytes;                    // 128 KB
+    static constexpr int p = kv + kStages * kStageBytes;         // 32 KB
+    static constexpr int bars = p + kTileBytes;
+    static constexpr int total = bars + 256;
+};
+constexpr size_t kSmemBytes = Smem::total + 1024;
+
+enum Bar {
+    kKvFull = 0,   // [2]
+    kKvEmpty = 2,  // [2]
+    kQFull = 4,
+    kSFull = 5,    // [2]
+    kSFree = 7,    // [2]
+    kPFull = 9,
+    kODone = 10,
+    kNumBars = 11
+};
+
+__global__ void __launch_bounds__(kThreads, 1)
+tile_attention_kernel(const __grid_constant__ TileParams p) {
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t *smem = reinterpret_cast<uint8_t *>(
+        (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    uint64_t *bar = reinterpret_cast<uint64_t *>(smem + Smem::bars);
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + Smem::bars + kNumBars * 8);
+
+    const int G = p.group;
+    const int T = kTileRows / G;                 // tokens per tile
+    // Longest tiles first: blockIdx.x counts down the tiles of a sequence.
+    const int tile = p.tiles_per_seq - 1 - static_cast<int>(blockIdx.x);
+    const int kvh = blockIdx.y;
+    const int b = blockIdx.z;
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+
+    const int q_off = static_cast<int>(p.q_row_offsets[b]);
+    const int n = static_cast<int>(p.q_row_offsets[b + 1]) - q_off;
+    const int L = static_cast<int>(p.kv_len[b]);
+    const int t0 = tile * T;
+    if (t0 >= n) return;                         // uniform over the CTA
+    const int t_end = min(t0 + T, n);
+    // Keys any row of this tile can see.
+    int kmax = p.causal ? L - n + t_end : L;
+    kmax = max(0, min(kmax, L));
+    const int ntiles = (kmax + kBN - 1) / kBN;
+
+    if (threadIdx.x == 0) {
+        for (int i = 0; i < kNumBars; ++i) {
+            const uint32_t cnt = (i == kSFree || i == kSFree + 1 || i == kPFull) ? 4u : 1u;
+            mbar_init(&bar[i], cnt);
+        }
+        fence_mbar_init();
+    }
+    if (warp == 5) {
+        tc::tmem_alloc(tmem_slot, kTmemCols);
+        tc::tmem_relinquish();
+    }
+    tc::fence_before_sync();
+    __syncthreads();
+    tc::fence_after_sync();
+    const uint32_t tmem = *tmem_slot;
+
+    if (warp == 4) {
+        // ------------------------------------------------------------ producer
+        if (ntiles > 0) {
+            if (lane == 0) {
+                prefetch_tensormap(&p.q_map);
+                prefetch_tensormap(&p.k_map);
+                prefetch_tensormap(&p.v_map);
+                mbar_arrive_expect_tx(&bar[kQFull], kTileBytes);
+                for (int cb = 0; cb < 2; ++cb)
+                    tma_load_4d(smem + Smem::q + cb * kBoxBytes, &p.q_map, &bar[kQFull], cb * 64,
+                                0, kvh, q_off + t0);
+            }
+            const int box_rows = p.box_rows;       // 128, 64, 32, 16 or 8
+            const int nb = kBN / box_rows;         // row boxes per key tile
+            int cached = -1, my_page = -1, my_slot = 0;
+            bool aborted = false;
+            for (int i = 0; i < ntiles && !aborted; ++i) {
+                const int key0 = i * kBN;
+                const int live = min(nb, (L - key0 + box_rows - 1) / box_rows);
+                const int s = i % kStages;
+                if (lane == 0) {
+                    if (i >= kStages &&
+                        !mbar_wait(&bar[kKvEmpty + s], ((i / kStages) - 1) & 1, p.err))
+                        aborted = true;
+                    else
+                        mbar_arrive_expect_tx(&bar[kKvFull + s],
+                                              uint32_t(live) * 2u * 2u * uint32_t(box_rows) * 128u);
+                }
+                aborted = __shfl_sync(0xffffffffu, aborted, 0);
+                if (aborted) break;
+                uint8_t *ks = smem + Smem::kv + s * kStageBytes;
+                uint8_t *vs = ks + kTileBytes;
+                for (int r = 0; r < live; ++r) {
+                    const int g = i * nb + r;      // box index within the sequence
+                    if ((g >> 5) != cached) {      // warp-uniform refill of 32 lookups
+                        cached = g >> 5;
+                        const int t = ((cached << 5) + lane) * box_rows;
+                        my_page = -1;
+                        my_slot = 0;
+                        if (t < L) {
+                            if (p.page_table) {
+                                const int pidx = t / p.page_size;
+                                int e = pidx < p.max_pages
+                                            ? p.page_table[size_t(b) * p.max_pages + pidx] : -1;
+                                if (e < 0 || e >= p.num_pages) {
+                                    atomicOr(p.err, kErrBadPage);
+                                    e = -1;
+                                }
+                                my_page = e;
+                                my_slot = t % p.page_size;
+                            } else {
+                                my_page = b;
+                                my_slot = t;
+                            }
+                        }
+                    }
+                    const int page = __shfl_sync(0xffffffffu, my_page, g & 31);
+                    const int slot = __shfl_sync(0xffffffffu, my_slot, g & 31);
+                    if (lane == 0) {
+                        if (page < 0) {
+                            // a skipped (bad-page) box: retire its expected bytes
+                            mbar_complete_tx(&bar[kKvFull + s], 2u * 2u * uint32_t(box_rows) * 128u);
+                        } else {
+#pragma unroll
+                            for (int cb = 0; cb < 2; ++cb) {
+                                const int off = cb * kBoxBytes + r * box_rows * 128;
+                                tma_load_4d(ks + off, &p.k_map, &bar[kKvFull + s], cb * 64, slot,
+                                            kvh, page);
+                                tma_load_4d(vs + off, &p.v_map, &bar[kKvFull + s], cb * 64, slot,
+                                            kvh, page);
+                            }
+                        }
+                    }
+                }
+            }
+        }
+    } else if (warp == 5) {
+        // ------------------------------------------------------------ MMA issue
+        if (ntiles > 0 && lane == 0) {
+            constexpr uint32_t idesc_s = tc::idesc_bf16_f32(128, kBN, 0, 0);
+            constexpr uint32_t idesc_o = tc::idesc_bf16_f32(128, kD, 0, 1);
+            const uint32_t q_base = smem_addr(smem + Smem::q);
+            const uint32_t kv_base = smem_addr(smem + Smem::kv);
+            const uint32_t p_base = smem_addr(smem + Smem::p);
+            bool ok = mbar_wait(&bar[kQFull], 0, p.err);
+            for (int t = 0; ok && t <= ntiles; ++t) {
+                if (t < ntiles) {
+                    const int s = t % kStages;
+                    const int sb = t & 1;
+                    ok = mbar_wait(&bar[kKvFull + s], (t / kStages) & 1, p.err);
+                    if (ok && t >= 2) ok = mbar_wait(&bar[kSFree + sb], ((t >> 1) - 1) & 1, p.err);
+                    if (!ok) break;
+                    tc::fence_after_sync();
+                    const uint32_t ks = kv_base + s * kStageBytes;
+                    for (int kk = 0; kk < kD / 16; ++kk) {
+                        const uint32_t off = (kk >> 2) * kBoxBytes + (kk & 3) * 32;
+                        tc::mma_bf16(tmem + kTmemS + sb * kBN,
+                                     tc::smem_desc_sw128(q_base + off, 16, 1024),
+                                     tc::smem_desc_sw128(ks + off, 16, 1024), idesc_s, kk > 0);
+                    }
+                    tc::mma_commit(&bar[kSFull + sb]);
+                }
+                if (t >= 1) {
+                    const int tp = t - 1;
+                    ok = mbar_wait(&bar[kPFull], tp & 1, p.err);
+                    if (!ok) break;
+                    tc::fence_after_sync();
+                    const uint32_t vs = kv_base + (tp % kStages) * kStageBytes + kTileBytes;
+                    for (int kk = 0; kk < kBN / 16; ++kk) {
+                        const uint32_t poff = (kk >> 2) * kBoxBytes + (kk & 3) * 32;
+                        tc::mma_bf16(tmem + kTmemO, tc::smem_desc_sw128(p_base + poff, 16, 1024),
+                                     tc::smem_desc_sw128(vs + kk * 16 * 128, kVLbo, kVSbo),
+                                     idesc_o, tp > 0 || kk > 0);
+                    }
+                    tc::mma_commit(&bar[kODone]);
+                    tc::mma_commit(&bar[kKvEmpty + (tp % kStages)]);
+                }
+            }
+        }
+    } else {
+        // ------------------------------------------------------------ softmax
+        const int r = warp * 32 + lane;          // MMA row == TMEM lane
+        const int tok = t0 + r / G;              // token index inside the sequence
+        const bool row_valid = tok < n;
+        const int lim = p.causal ? min(L, L - n + tok + 1) : L;   // keys [0, lim)
+        const uint32_t lane_base = uint32_t(warp * 32) << 16;
+        uint8_t *pbuf = smem + Smem::p;
+        float m_ref = -INFINITY;
+        float l = 0.f;
+        bool ok = true;
+        for (int t = 0; t < ntiles; ++t) {
+            const int sb = t & 1;
+            const int key0 = t * kBN;
+            ok = mbar_wait(&bar[kSFull + sb], (t >> 1) & 1, p.err);
+            if (!ok) break;
+            tc::fence_after_sync();
+            float sc[kBN];
+#pragma unroll
+            for (int c = 0; c < kBN; c += 32) {
+                float v[32];
+                tc::tmem_ld32(tmem + lane_base + kTmemS + sb * kBN + c, v);
+#pragma unroll
+                for (int j = 0; j < 32; ++j) sc[c + j] = v[j];
+            }
+            tc::fence_before_sync();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&bar[kSFree + sb]);
+
+            const int nvis = lim - key0;         // keys of this tile the row sees
+            float mt = -INFINITY;
+#pragma unroll
+            for (int j = 0; j < kBN; ++j) {
+                sc[j] = j < nvis ? sc[j] * p.qk_scale_log2 : -INFINITY;
+                mt = fmaxf(mt, sc[j]);
+            }
+            const bool raise = mt > m_ref + kRescaleThreshold;
+            float alpha = 1.f;
+            if (raise) {
+                alpha = fast_exp2(m_ref - mt);
+                m_ref = mt;
+            }
+            const bool live = m_ref != -INFINITY;
+            float rowsum = 0.f;
+            uint32_t pk[kBN / 2];
+#pragma unroll
+            for (int j = 0; j < kBN / 2; ++j) {
+                const float p0 = live ? fast_exp2(sc[2 * j] - m_ref) : 0.f;
+                const float p1 = live ? fast_exp2(sc[2 * j + 1] - m_ref) : 0.f;
+                rowsum += p0 + p1;
+                pk[j] = pack_bf16x2(p0, p1);
+            }
+            l = l * alpha + rowsum;
+
+            if (t >= 1) {
+                ok = mbar_wait(&bar[kODone], (t - 1) & 1, p.err);
+                if (!ok) break;
+                tc::fence_after_sync();
+                if (__any_sync(0xffffffffu, raise)) {
+#pragma unroll 1
+                    for (int c = 0; c < kD; c += 32) {
+                        float v[32];
+                        tc::tmem_ld32(tmem + lane_base + kTmemO + c, v);
+#pragma unroll
+                        for (int j = 0; j < 32; ++j) v[j] *= alpha;
+                        tc::tmem_st32(tmem + lane_base + kTmemO + c, v);
+                    }
+                    tc::tmem_wait_st();
+                }
+            }
+            // P row r: keys 0-63 in box 0, 64-127 in box 1 (128-byte swizzle).
+#pragma unroll
+            for (int c = 0; c < 16; ++c) {
+                uint4 v;
+                v.x = pk[4 * c]; v.y = pk[4 * c + 1]; v.z = pk[4 * c + 2]; v.w = pk[4 * c + 3];
+                const int box = c >> 3, ch = c & 7;
+                *reinterpret_cast<uint4 *>(pbuf + box * kBoxBytes + r * 128 +
+                                           ((ch ^ (r & 7)) << 4)) = v;
+            }
+            const int nkeys = min(kBN, L - key0);
+            if (nkeys < kBN) {
+                // Slots past the sequence end may hold anything: zero them in V.
+                uint8_t *vs = smem + Smem::kv + (t % kStages) * kStageBytes + kTileBytes;
+                const int per_box = (kBN - nkeys) * 8;          // 16-B chunks
+                for (int i = r; i < 2 * per_box; i += 128) {
+                    const int box = i / per_box;
+                    const int rem = i - box * per_box;
+                    *reinterpret_cast<uint4 *>(vs + box * kBoxBytes + (nkeys + rem / 8) * 128 +
+                                               (rem & 7) * 16) = make_uint4(0u, 0u, 0u, 0u);
+                }
+            }
+            tc::fence_async_smem();
+            tc::fence_before_sync();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&bar[kPFull]);
+        }
+
+        // ---- epilogue ---------------------------------------------------------
+        if (ok && ntiles > 0) {
+            ok = mbar_wait(&bar[kODone], (ntiles - 1) & 1, p.err);
+            tc::fence_after_sync();
+        }
+        const int h = kvh * G + (r % G);
+        const float t2 = p.sink ? p.sink[h] * kLog2e : -INFINITY;
+        const float Mf = fmaxf(m_ref, t2);
+        float so = 0.f, Z = 0.f;
+        if (Mf != -INFINITY) {
+            so = fast_exp2(m_ref - Mf);
+            Z = l * so + fast_exp2(t2 - Mf);
+        }
+        const float scale_o = Z > 0.f ? so / Z : 0.f;
+        const size_t row = size_t(q_off) + tok;
+        uint16_t *dst = p.out + (row * p.num_q_heads + h) * kD;
+#pragma unroll 1
+        for (int c = 0; c < kD; c += 32) {
+            float v[32];
+            if (ntiles > 0 && ok) {
+                tc::tmem_ld32(tmem + lane_base + kTmemO + c, v);
+            } else {
+#pragma unroll
+                for (int j = 0; j < 32; ++j) v[j] = 0.f;
+            }
+            if (row_valid) {
+#pragma unroll
+                for (int j = 0; j < 32; j += 8) {
+                    uint4 w;
+                    w.x = pack_bf16x2(v[j] * scale_o, v[j + 1] * scale_o);
+                    w.y = pack_bf16x2(v[j + 2] * scale_o, v[j + 3] * scale_o);
+                    w.z = pack_bf16x2(v[j + 4] * scale_o, v[j + 5] * scale_o);
+                    w.w = pack_bf16x2(v[j + 6] * scale_o, v[j + 7] * scale_o);
+                    *reinterpret_cast<uint4 *>(dst + c + j) = w;
+                }
+            }
+        }
+        if (row_valid && p.lse)
+            p.lse[row * p.num_q_heads + h] = Z > 0.f ? (Mf + fast_log2(Z)) * kLn2 : -INFINITY;
+    }
+
+    tc::fence_before_sync();
+    __syncthreads();
+    if (warp == 5) {
+        tc::fence_after_sync();
+        tc::tmem_dealloc(tmem, kTmemCols);
+    }
+}
+
+}  // namespace
+
+cudaError_t launch_tile_attention(const TileParams &p, cudaStream_t stream) {
+    cudaError_t e = cudaFuncSetAttribute(tile_attention_kernel,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         int(kSmemBytes));
+    if (e != cudaSuccess) return e;
+    dim3 grid(p.tiles_per_seq, p.num_q_heads / p.group, p.batch);
+    tile_attention_kernel<<<grid, kThreads, kSmemBytes, stream>>>(p);
+    return cudaGetLastError();
+}
+
+}  // namespace attn

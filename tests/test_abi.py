@@ -66,15 +66,20 @@ def kv(attn, **over):
 
 
 def call_decode(attn, k=None, v=None, **over):
-    args = dict(q=0x30000, kv_len=0x40000, batch=2, hq=32, group=4, d=128, max_kv_len=500,
-                scale=0.088, sink=None, P=1, ws=None, ws_bytes=0, out=0x50000, lse=None)
+    args = dict(q=0x30000, kv_len=0x40000, offs=None, batch=2, rows=None, hq=32, group=4,
+                d=128, max_q_len=1, max_kv_len=500, scale=0.088, sink=None, causal=0, P=1,
+                ws=None, ws_bytes=0, out=0x50000, lse=None)
     args.update(over)
+    if args["rows"] is None:
+        args["rows"] = args["batch"]
     k = k or kv(attn)
     v = v or kv(attn)
     return attn.lib().attn_decode(args["q"], ctypes.byref(k), ctypes.byref(v), args["kv_len"],
-                                  args["batch"], args["hq"], args["group"], args["d"],
-                                  args["max_kv_len"], args["scale"], args["sink"], args["P"],
-                                  args["ws"], args["ws_bytes"], args["out"], args["lse"], None)
+                                  args["offs"], args["batch"], args["rows"], args["hq"],
+                                  args["group"], args["d"], args["max_q_len"],
+                                  args["max_kv_len"], args["scale"], args["sink"],
+                                  args["causal"], args["P"], args["ws"], args["ws_bytes"],
+                                  args["out"], args["lse"], None)
 
 
 def test_decode_rejects_bad_arguments_before_launch(attn):
@@ -109,6 +114,12 @@ def test_decode_rejects_bad_arguments_before_launch(attn):
     assert call_decode(attn, P=4, ws=0x60000, ws_bytes=16) == E.ATTN_ERR_WORKSPACE
     P, need = attn.attn_plan_partitions(2, 2, 32, 8, 128, 500, 4, num_sms=152)
     assert call_decode(attn, P=4, ws=0x60010, ws_bytes=need) == E.ATTN_ERR_WORKSPACE
+    # rows must match the batch without row offsets; multi-row needs offsets
+    assert call_decode(attn, rows=3) == E.ATTN_ERR_INVALID_ARG
+    assert call_decode(attn, max_q_len=4) == E.ATTN_ERR_INVALID_ARG
+    assert call_decode(attn, max_q_len=0) == E.ATTN_ERR_INVALID_ARG
+    # the multi-row tile path does not split K
+    assert call_decode(attn, offs=0x70000, rows=40, max_q_len=30, P=2) == E.ATTN_ERR_UNSUPPORTED
     # an empty batch is a no-op
     assert call_decode(attn, batch=0, q=None, out=None) == E.ATTN_OK
 

@@ -1,0 +1,101 @@
+"""GPU parity of the tensor-core tile path (attn_decode with several query
+rows per sequence: ragged prefill mixed with decode, causal) against the
+fp64 oracle."""
+import math
+
+import numpy as np
+import pytest
+import torch
+
+from split_flash_decoding_gb300 import workloads as W
+from tests.helpers import assert_close, bits_equal, oracle_result
+
+pytestmark = pytest.mark.gpu
+DEV = "cuda:0"
+
+
+@pytest.fixture(scope="module")
+def attn():
+    from split_flash_decoding_gb300 import build
+    build.build()
+    from split_flash_decoding_gb300 import attn as a
+    a.attn_device_error_flags(clear=True)
+    yield a
+    assert a.attn_device_error_flags(clear=True) == 0
+
+
+def tile_workload(q_lens, prefix, hq=8, hkv=2, page_size=16, seed=0, causal=True, sink=False):
+    kv_lens = [p + n for p, n in zip(prefix, q_lens)]
+    return W.make_workload("tile", batch=len(q_lens), num_q_heads=hq, num_kv_heads=hkv,
+                           dim_qk=128, kv_lens=kv_lens, page_size=page_size, seed=seed,
+                           device=DEV, q_lens=q_lens, causal=causal, sink=sink)
+
+
+def run(attn, w, sink="workload"):
+    s = w.sink if sink == "workload" else sink
+    out, lse = attn.attn_decode(w.q, w.k_cache, w.v_cache, w.kv_len, group=w.group,
+                                scale=w.scale, max_kv_len=w.max_kv_len,
+                                page_table=w.page_table, sink=s,
+                                q_row_offsets=w.q_row_offsets, max_q_len=w.max_q_len,
+                                causal=w.causal, num_partitions=1)
+    torch.cuda.synchronize()
+    return out, lse
+
+
+@pytest.mark.parametrize("causal", [True, False])
+def test_mixed_rows_match_oracle(attn, causal):
+    w = tile_workload([1, 5, 40, 130, 1], [0, 20, 100, 7, 300], seed=31, causal=causal)
+    out, lse = run(attn, w)
+    ref_o, ref_l = oracle_result(w)
+    assert_close(out, lse, ref_o, ref_l, f"tile causal={causal}")
+
+
+@pytest.mark.parametrize("hq,hkv", [(8, 8), (8, 4), (16, 4), (32, 4)])
+def test_groups(attn, hq, hkv):
+    w = tile_workload([3, 70, 129], [10, 0, 200], hq=hq, hkv=hkv, seed=32)
+    out, lse = run(attn, w)
+    ref_o, ref_l = oracle_result(w)
+    assert_close(out, lse, ref_o, ref_l, f"tile hq={hq} hkv={hkv}")
+
+
+@pytest.mark.parametrize("page_size", [16, 64, 128, 256])
+def test_tile_paged_equals_contiguous_bitwise(attn, page_size):
+    w = tile_workload([33, 1, 300], [90, 500, 0], page_size=page_size, seed=33)
+    c = W.contiguous_copy(w)
+    o1, l1 = run(attn, w)
+    o2, l2 = run(attn, c)
+    assert bits_equal(o1, o2) and bits_equal(l1, l2)
+    ref_o, ref_l = oracle_result(w)
+    assert_close(o1, l1, ref_o, ref_l, f"tile page {page_size}")
+
+
+def test_tile_sinks(attn):
+    w = tile_workload([17, 1, 64], [5, 40, 0], seed=34, sink=True)
+    out, lse = run(attn, w)
+    ref_o, ref_l = oracle_result(w)
+    assert_close(out, lse, ref_o, ref_l, "tile sinks")
+    no_sink = torch.full((w.num_q_heads,), -math.inf, dtype=torch.float32, device=DEV)
+    o1, l1 = run(attn, w, sink=no_sink)
+    o2, l2 = run(attn, w, sink=None)
+    assert bits_equal(o1, o2) and bits_equal(l1, l2)
+
+
+def test_mixed_prefill_decode_full_size_sampled(attn):
+    """The 16-sequence mixed batch at full size; the oracle checks 1024
+    sampled (row, head) pairs covering every sequence, first and last rows
+    included."""
+    w = W.mixed_prefill_decode(device=DEV)
+    out, lse = run(attn, w)
+    offs = w.q_row_offsets_host
+    rng = np.random.default_rng(5)
+    rows, heads = [], []
+    for b in range(w.batch):
+        lo, hi = offs[b], offs[b + 1]
+        pick = {lo, hi - 1} | set(rng.integers(lo, hi, size=min(62, hi - lo)).tolist())
+        for r in sorted(pick):
+            rows.append(r)
+            heads.append(int(rng.integers(0, w.num_q_heads)))
+    rows, heads = np.array(rows), np.array(heads)
+    ref_o, ref_l = oracle_result(w, sample=(rows, heads))
+    ri, hi_ = torch.as_tensor(rows, device=DEV), torch.as_tensor(heads, device=DEV)
+    assert_close(out[ri, hi_], lse[ri, hi_], ref_o, ref_l, "mixed full size sampled")
