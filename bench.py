@@ -55,6 +55,8 @@ def parse():
     ap.add_argument("--workload", default="llama3",
                     choices=["llama3", "long_context", "mla", "mixed", "tiny"])
     ap.add_argument("--partitions", type=int, default=0, help="0 = planner's choice")
+    ap.add_argument("--batch", type=int, default=0,
+                    help="override the batch of the llama3 / mla workloads (profiling captures)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     return ap.parse_args()
 
@@ -156,14 +158,14 @@ class ClockSampler:
                 "samples": len(window)}
 
 
-def build_workload(name: str, device):
+def build_workload(name: str, device, batch: int = 0):
     from split_flash_decoding_gb300 import workloads as W
     if name == "llama3":
-        return W.llama3_8b_decode(device=device)
+        return W.llama3_8b_decode(device=device, **({"batch": batch} if batch else {}))
     if name == "long_context":
         return W.long_context_decode(device=device)
     if name == "mla":
-        return W.deepseek_v3_mla_decode(device=device)
+        return W.deepseek_v3_mla_decode(device=device, **({"batch": batch} if batch else {}))
     if name == "mixed":
         return W.mixed_prefill_decode(device=device)
     if name == "tiny":
@@ -204,6 +206,24 @@ def visible_pairs(w) -> int:
 
 def algorithmic_flops(w) -> int:
     return visible_pairs(w) * w.num_q_heads * 2 * (w.dim_qk + w.dim_v)
+
+
+def max_over_ranks(values, dist, device=None):
+    """Element-wise max of per-rank timings (host-side bookkeeping only; the
+    attention path itself has no collective)."""
+    import torch
+    vals = torch.tensor([float(v) for v in values], dtype=torch.float64)
+    if dist is not None:
+        t = vals.to(device) if device is not None else vals
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        vals = t.cpu()
+    return [float(x) for x in vals]
+
+
+def whole_job_value(world: int, bytes_per_rank: int, ms_per_step: float) -> float:
+    """Weak scaling: every rank processes its own copy of the workload, so
+    the job moves world * bytes per step in the slowest rank's time."""
+    return world * bytes_per_rank / (ms_per_step * 1e-3) / 1e9
 
 
 # ---------------------------------------------------------------------------
@@ -266,7 +286,7 @@ def run_reference(args, rank, world):
     if rank != 0:
         return
     torch.cuda.set_device(0)
-    w = build_workload(args.workload, torch.device("cuda", 0))
+    w = build_workload(args.workload, torch.device("cuda", 0), args.batch)
     k_host, v_host = host_copies(w)
     total_budget = 150.0
     per_step = total_budget / max(1, args.steps + args.warmup)
@@ -305,7 +325,7 @@ def run_ours(args, rank, world, dist):
     local = int(os.environ.get("LOCAL_RANK", rank))
     torch.cuda.set_device(local)
     dev = torch.device("cuda", local)
-    w = build_workload(args.workload, dev)
+    w = build_workload(args.workload, dev, args.batch)
     stream = torch.cuda.Stream(device=dev)
 
     if w.is_mla:
@@ -409,17 +429,12 @@ def run_ours(args, rank, world, dist):
 
     # ---- max over ranks ----
     mean_call_ms = sum(per_call_ms) / len(per_call_ms)
-    vals = torch.tensor([total_ms, mean_call_ms, e2e_s], dtype=torch.float64)
-    if dist is not None:
-        t = vals.to(dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        vals = t.cpu()
-    total_ms, mean_call_ms, e2e_s = [float(x) for x in vals]
+    total_ms, mean_call_ms, e2e_s = max_over_ranks([total_ms, mean_call_ms, e2e_s], dist, dev)
     if rank != 0:
         return
 
     ms_per_step = total_ms / args.steps
-    value = world * nbytes / (ms_per_step * 1e-3) / 1e9
+    value = whole_job_value(world, nbytes, ms_per_step)
     peak, peak_kind, peaks = measured_peaks()
     achieved = nbytes / (mean_call_ms * 1e-3) / 1e9
     tflops = flops / (mean_call_ms * 1e-3) / 1e12

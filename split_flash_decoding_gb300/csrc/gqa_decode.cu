@@ -114,6 +114,7 @@ gqa_decode_kernel(const __grid_constant__ GqaParams p) {
         const int boxes_per_tile = kTile / box_rows;
         const uint32_t box_bytes = uint32_t(box_rows) * 128u;
         bool aborted = false;
+        int issued = 0;
         for (int base = 0; base < ntiles && !aborted; base += 32) {
             int pg[4] = {-1, -1, -1, -1};
             int sl[4] = {0, 0, 0, 0};
@@ -173,8 +174,14 @@ gqa_decode_kernel(const __grid_constant__ GqaParams p) {
                 }
                 aborted = __shfl_sync(0xffffffffu, aborted, 0);
                 if (aborted) break;
+                issued = i + 1;
             }
         }
+        // Before the warp leaves, every copy it issued must have landed
+        // (normally the consumers already saw these phases complete).
+        if (lane == 0)
+            for (int i = max(0, issued - kStages); i < issued; ++i)
+                mbar_wait(&full[i % kStages], (i / kStages) & 1, p.err);
         return;
     }
 

@@ -147,6 +147,7 @@ mla_decode_kernel(const __grid_constant__ MlaParams p) {
             const int box_rows = p.box_rows;
             const int boxes_per_tile = kBN / box_rows;   // 1..8
             bool aborted = false;
+            int issued = 0;
             for (int base = 0; base < ntiles && !aborted; base += 32) {
                 // lane i resolves the pages of tile base + i (up to 8 row boxes)
                 int pg[8], sl[8];
@@ -207,7 +208,14 @@ mla_decode_kernel(const __grid_constant__ MlaParams p) {
                     }
                     aborted = __shfl_sync(0xffffffffu, aborted, 0);
                     if (aborted) break;
+                    issued = i + 1;
                 }
+            }
+            // every copy this warp issued must land before the CTA may leave
+            if (lane == 0) {
+                mbar_wait(&bar[kQFull], 0, p.err);
+                for (int i = max(0, issued - kStages); i < issued; ++i)
+                    mbar_wait(&bar[kKvFull + i % kStages], (i / kStages) & 1, p.err);
             }
         }
     } else if (warp == 5) {

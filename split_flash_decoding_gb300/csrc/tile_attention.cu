@@ -123,6 +123,7 @@ tile_attention_kernel(const __grid_constant__ TileParams p) {
             const int nb = kBN / box_rows;         // row boxes per key tile
             int cached = -1, my_page = -1, my_slot = 0;
             bool aborted = false;
+            int issued = 0;
             for (int i = 0; i < ntiles && !aborted; ++i) {
                 const int key0 = i * kBN;
                 const int live = min(nb, (L - key0 + box_rows - 1) / box_rows);
@@ -181,6 +182,13 @@ tile_attention_kernel(const __grid_constant__ TileParams p) {
                         }
                     }
                 }
+                issued = i + 1;
+            }
+            // every copy this warp issued must land before the CTA may leave
+            if (lane == 0) {
+                mbar_wait(&bar[kQFull], 0, p.err);
+                for (int i = max(0, issued - kStages); i < issued; ++i)
+                    mbar_wait(&bar[kKvFull + i % kStages], (i / kStages) & 1, p.err);
             }
         }
     } else if (warp == 5) {
