@@ -1,24 +1,27 @@
-// gqa_decode.cu -- split-K flash-decoding partition kernel for grouped-query
-// attention over a paged (or contiguous) bf16 KV cache.
+// gqa_decode.cu -- split-K flash-decoding kernel for grouped-query attention
+// over a paged (or contiguous) bf16 KV cache.
 //
-// One CTA handles one (key slice p, KV head, sequence b).  The `group` query
-// heads that share the KV head are folded into the CTA's rows, so every K/V
-// byte is read from HBM once per call.  Inside the CTA:
+// Work item: one (sequence b, KV head, key slice p).  The `group` query heads
+// that share the KV head are folded into the item's rows, so every K/V byte
+// is read from HBM once per call.  The kernel is persistent: a grid of two
+// CTAs per SM walks the list of non-empty items in a fixed round-robin order
+// (item j goes to CTA j mod grid), so the TMA pipeline never drains between
+// items and slices past a sequence's end cost nothing.  Inside a CTA:
 //
 //   * one producer warp streams 32-key K and V tiles with TMA
 //     (cp.async.bulk.tensor, 128-byte swizzle) into a ring of shared-memory
 //     stages, translating logical token -> (page, slot) through the page
-//     table for every tile;
-//   * four consumer warps take the tiles round-robin.  Each keeps its own
-//     online-softmax state (running max m, exp-sum l, unnormalised O) --
+//     table; it runs ahead across item boundaries;
+//   * four consumer warps take an item's tiles round-robin.  Each keeps its
+//     own online-softmax state (running max m, exp-sum l, unnormalised O) --
 //     a warp-level split of the slice ("decoding_warp_split_k",
-//     mha_decoding_single_batch_pipelined, Parameters) -- and the four are
-//     merged at the end;
+//     mha_decoding_single_batch_pipelined, Parameters) -- merged at the end of
+//     the item;
 //   * scores: lane j owns key j of the tile and dots it with all group rows
 //     of q (fp32, packed FFMA2); softmax statistics use warp-shuffle max;
 //     P.V: lane owns head_dim/32 channels of every row.
 //
-// The slice's result is either the final output (the sequence needs at most
+// An item's result is either the final output (its sequence needs at most
 // one slice) or the partial (O, m, l) for the split-K reduce ("writes partial
 // exp_sum and qk_max statistics for a subsequent mha_splitk_reduce pass",
 // mha_decoding_single_batch_pipelined, summary).  Scores are kept in base-2
@@ -38,62 +41,117 @@ constexpr int kTile = kGqaTileKeys;  // keys per stage
 constexpr int kConsumers = 4;        // consumer warps
 constexpr int kThreads = (kConsumers + 1) * 32;
 
-template <int D>
+// Stage counts keep two CTAs (~104 KB each) resident per SM.
+template <int D, int G>
 struct GqaShape {
     static constexpr int kBoxes = D / 64;                 // 64-channel (128 B) column boxes
     static constexpr int kTileBytes = kTile * D * 2;      // one K or V tile
     static constexpr int kStageBytes = 2 * kTileBytes;
-    static constexpr int kStages = D == 128 ? 6 : 10;
+    static constexpr int kStages = D == 128 ? (G >= 8 ? 3 : 5) : 10;
     static constexpr int kDpl = D / 32;                   // P.V channels per lane
 };
 
+// Shared-memory layout (byte offsets from the 1024-aligned base).
 template <int D, int G>
-constexpr size_t gqa_smem_bytes() {
-    using S = GqaShape<D>;
-    return 1024 /* alignment slack */ + size_t(S::kStages) * S::kStageBytes +
-           sizeof(float) * (G * D + kConsumers * kTile * G + 2 * kConsumers * G +
-                            kConsumers * G * D) +
-           sizeof(uint64_t) * 2 * S::kStages;
+struct GqaSmem {
+    using S = GqaShape<D, G>;
+    static constexpr int stages = 0;
+    static constexpr int q = stages + S::kStages * S::kStageBytes;      // fp32 [2][G][D]
+    static constexpr int p = q + 2 * G * D * 4;                          // fp32 [4][32][G]
+    static constexpr int mrg = p + kConsumers * kTile * G * 4;           // [2] merge buffers
+    static constexpr int mrg_bytes = (2 * kConsumers * G + kConsumers * G * D) * 4;
+    static constexpr int bars = mrg + 2 * mrg_bytes;                     // full[], empty[]
+    static constexpr int items = bars + 2 * S::kStages * 8;              // int [batch + 1]
+    static constexpr int fixed = items;
+};
+
+template <int D, int G>
+size_t gqa_smem_bytes(int batch) {
+    return 1024 + size_t(GqaSmem<D, G>::fixed) + sizeof(int) * size_t(batch + 1);
+}
+
+// Item j -> (b, kvh, p) through the prefix sums cum[b] = number of items of
+// sequences < b (each sequence has num_kv_heads * n_b items, n_b >= 1).
+struct Item {
+    int b, kvh, part, L, start, end, ntiles;
+    bool direct;
+};
+
+__device__ __forceinline__ Item decode_item(const GqaParams &p, const int *cum, int j, int hkv) {
+    int lo = 0, hi = p.batch;  // find b: cum[b] <= j < cum[b+1]
+    while (hi - lo > 1) {
+        const int mid = (lo + hi) >> 1;
+        if (cum[mid] <= j) lo = mid; else hi = mid;
+    }
+    Item it;
+    it.b = lo;
+    const int per_head = (cum[lo + 1] - cum[lo]) / hkv;   // n_b
+    const int r = j - cum[lo];
+    it.kvh = r / per_head;
+    it.part = r - it.kvh * per_head;
+    const uint32_t cap = uint32_t(p.num_partitions) * uint32_t(p.chunk);
+    it.L = static_cast<int>(min(p.kv_len[lo], cap));
+    it.start = it.part * p.chunk;
+    it.end = min(it.start + p.chunk, it.L);
+    it.ntiles = it.start < it.end ? (it.end - it.start + kTile - 1) / kTile : 0;
+    it.direct = per_head <= 1 && (it.L + p.chunk - 1) / p.chunk <= 1;
+    return it;
 }
 
 template <int D, int G>
 __global__ void __launch_bounds__(kThreads, 2)
 gqa_decode_kernel(const __grid_constant__ GqaParams p) {
-    using S = GqaShape<D>;
+    using S = GqaShape<D, G>;
+    using M = GqaSmem<D, G>;
     constexpr int kStages = S::kStages;
     constexpr int kDpl = S::kDpl;
 
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-    float *q_s = reinterpret_cast<float *>(smem + kStages * S::kStageBytes);
-    float *p_s = q_s + G * D;                  // [consumer][key][row]
-    float *m_s = p_s + kConsumers * kTile * G;  // [consumer][row]
-    float *l_s = m_s + kConsumers * G;
-    float *o_s = l_s + kConsumers * G;         // [consumer][row][D]
-    uint64_t *full = reinterpret_cast<uint64_t *>(o_s + kConsumers * G * D);
+    uint64_t *full = reinterpret_cast<uint64_t *>(smem + M::bars);
     uint64_t *empty = full + kStages;
+    int *cum = reinterpret_cast<int *>(smem + M::items);
 
-    const int part = blockIdx.x;
-    const int kvh = blockIdx.y;
-    const int b = blockIdx.z;
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
-
-    // A length above the planned capacity P * chunk is a caller error: flag
-    // it and attend to the first P * chunk keys only.
+    const int hkv = p.num_q_heads / G;
     const uint32_t cap = uint32_t(p.num_partitions) * uint32_t(p.chunk);
-    const uint32_t len_in = p.kv_len[b];
-    if (len_in > cap && part == 0 && threadIdx.x == 0) atomicOr(p.err, kErrBadLength);
-    const int L = static_cast<int>(min(len_in, cap));
-    const int start = part * p.chunk;
-    const int end = min(start + p.chunk, L);
-    const int nslices = (L + p.chunk - 1) / p.chunk;
-    const bool direct = nslices <= 1;  // this CTA (part 0) writes the final rows
-    if (start >= L && !(direct && part == 0)) return;
-    const int ntiles = start < end ? (end - start + kTile - 1) / kTile : 0;
 
-    if (threadIdx.x == 0) {
+    // ---- item table: n_b = max(1, slices of b); cum = prefix sums * hkv ----
+    if (warp == 0) {
+        const int per_lane = (p.batch + 31) / 32;
+        const int b0 = lane * per_lane;
+        int local = 0;
+        for (int i = 0; i < per_lane; ++i) {
+            const int b = b0 + i;
+            if (b < p.batch) {
+                const uint32_t len_in = p.kv_len[b];
+                if (len_in > cap && blockIdx.x == 0) atomicOr(p.err, kErrBadLength);
+                const uint32_t L = min(len_in, cap);
+                const int ns = static_cast<int>((L + p.chunk - 1) / p.chunk);
+                local += max(ns, 1) * hkv;
+            }
+        }
+        int incl = local;  // inclusive warp scan of the per-lane sums
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const int v = __shfl_up_sync(0xffffffffu, incl, o);
+            if (lane >= o) incl += v;
+        }
+        int run = incl - local;
+        for (int i = 0; i < per_lane; ++i) {
+            const int b = b0 + i;
+            if (b < p.batch) {
+                cum[b] = run;
+                const uint32_t L = min(p.kv_len[b], cap);
+                const int ns = static_cast<int>((L + p.chunk - 1) / p.chunk);
+                run += max(ns, 1) * hkv;
+            }
+        }
+        if (lane == 31) cum[p.batch] = incl;
+    }
+    if (threadIdx.x == 32) {
         for (int s = 0; s < kStages; ++s) {
             mbar_init(&full[s], 1);
             mbar_init(&empty[s], 1);
@@ -101,6 +159,7 @@ gqa_decode_kernel(const __grid_constant__ GqaParams p) {
         fence_mbar_init();
     }
     __syncthreads();
+    const int num_items = cum[p.batch];
 
     if (warp == kConsumers) {
         // ------------------------------------------------------------------
@@ -110,280 +169,340 @@ gqa_decode_kernel(const __grid_constant__ GqaParams p) {
             prefetch_tensormap(&p.k_map);
             prefetch_tensormap(&p.v_map);
         }
-        const int box_rows = p.box_rows;            // 32, 16 or 8
+        const int box_rows = p.box_rows;  // 32, 16 or 8
         const int boxes_per_tile = kTile / box_rows;
         const uint32_t box_bytes = uint32_t(box_rows) * 128u;
         bool aborted = false;
-        int issued = 0;
-        for (int base = 0; base < ntiles && !aborted; base += 32) {
-            int pg[4] = {-1, -1, -1, -1};
-            int sl[4] = {0, 0, 0, 0};
-            const int my_tile = base + lane;
-            if (my_tile < ntiles) {
-                const int t0 = start + my_tile * kTile;
-                for (int r = 0; r < boxes_per_tile; ++r) {
-                    const int t = t0 + r * box_rows;
-                    if (t >= L) break;
-                    if (p.page_table) {
-                        const int pidx = t / p.page_size;
-                        int e = pidx < p.max_pages
-                                    ? p.page_table[size_t(b) * p.max_pages + pidx] : -1;
-                        if (e < 0 || e >= p.num_pages) {
-                            atomicOr(p.err, kErrBadPage);
-                            e = -1;
+        int g = 0;  // tiles issued by this CTA so far
+        for (int j = blockIdx.x; j < num_items && !aborted; j += gridDim.x) {
+            const Item it = decode_item(p, cum, j, hkv);
+            for (int base = 0; base < it.ntiles && !aborted; base += 32) {
+                int pg[4] = {-1, -1, -1, -1};
+                int sl[4] = {0, 0, 0, 0};
+                const int my_tile = base + lane;
+                if (my_tile < it.ntiles) {
+                    const int t0 = it.start + my_tile * kTile;
+#pragma unroll
+                    for (int r = 0; r < 4; ++r) {
+                        const int t = t0 + r * box_rows;
+                        if (r >= boxes_per_tile || t >= it.L) continue;
+                        if (p.page_table) {
+                            const int pidx = t / p.page_size;
+                            int e = pidx < p.max_pages
+                                        ? p.page_table[size_t(it.b) * p.max_pages + pidx] : -1;
+                            if (e < 0 || e >= p.num_pages) {
+                                atomicOr(p.err, kErrBadPage);
+                                e = -1;
+                            }
+                            pg[r] = e;
+                            sl[r] = t % p.page_size;
+                        } else {
+                            pg[r] = it.b;
+                            sl[r] = t;
                         }
-                        pg[r] = e;
-                        sl[r] = t % p.page_size;
-                    } else {
-                        pg[r] = b;
-                        sl[r] = t;
                     }
                 }
-            }
-            const int lim = min(base + 32, ntiles);
-            for (int i = base; i < lim; ++i) {
-                int pages[4], slots[4];
+                const int lim = min(base + 32, it.ntiles);
+                for (int i = base; i < lim; ++i) {
+                    int pages[4], slots[4];
 #pragma unroll
-                for (int r = 0; r < 4; ++r) {
-                    pages[r] = __shfl_sync(0xffffffffu, pg[r], i - base);
-                    slots[r] = __shfl_sync(0xffffffffu, sl[r], i - base);
-                }
-                if (lane == 0) {
-                    const int s = i % kStages;
-                    if (i >= kStages && !mbar_wait(&empty[s], ((i / kStages) - 1) & 1, p.err)) {
-                        aborted = true;
-                    } else {
-                        uint32_t nbox = 0;
-                        for (int r = 0; r < boxes_per_tile; ++r) nbox += pages[r] >= 0 ? 1u : 0u;
-                        // every box is loaded for K and V, in kBoxes column blocks
-                        mbar_arrive_expect_tx(&full[s], 2u * S::kBoxes * nbox * box_bytes);
-                        uint8_t *ks = smem + s * S::kStageBytes;
-                        uint8_t *vs = ks + S::kTileBytes;
-                        for (int r = 0; r < boxes_per_tile; ++r) {
-                            if (pages[r] < 0) continue;
+                    for (int r = 0; r < 4; ++r) {
+                        pages[r] = __shfl_sync(0xffffffffu, pg[r], i - base);
+                        slots[r] = __shfl_sync(0xffffffffu, sl[r], i - base);
+                    }
+                    if (lane == 0) {
+                        const int s = g % kStages;
+                        if (g >= kStages &&
+                            !mbar_wait(&empty[s], ((g / kStages) - 1) & 1, p.err)) {
+                            aborted = true;
+                        } else {
+                            uint32_t nbox = 0;
 #pragma unroll
-                            for (int cb = 0; cb < S::kBoxes; ++cb) {
-                                const int off = cb * kTile * 128 + r * box_rows * 128;
-                                tma_load_4d(ks + off, &p.k_map, &full[s], cb * 64, slots[r], kvh,
-                                            pages[r]);
-                                tma_load_4d(vs + off, &p.v_map, &full[s], cb * 64, slots[r], kvh,
-                                            pages[r]);
+                            for (int r = 0; r < 4; ++r) nbox += pages[r] >= 0 ? 1u : 0u;
+                            // every box is loaded for K and V, in kBoxes column blocks
+                            mbar_arrive_expect_tx(&full[s], 2u * S::kBoxes * nbox * box_bytes);
+                            uint8_t *ks = smem + M::stages + s * S::kStageBytes;
+                            uint8_t *vs = ks + S::kTileBytes;
+#pragma unroll
+                            for (int r = 0; r < 4; ++r) {
+                                if (pages[r] < 0) continue;
+#pragma unroll
+                                for (int cb = 0; cb < S::kBoxes; ++cb) {
+                                    const int off = cb * kTile * 128 + r * box_rows * 128;
+                                    tma_load_4d(ks + off, &p.k_map, &full[s], cb * 64, slots[r],
+                                                it.kvh, pages[r]);
+                                    tma_load_4d(vs + off, &p.v_map, &full[s], cb * 64, slots[r],
+                                                it.kvh, pages[r]);
+                                }
                             }
                         }
                     }
+                    aborted = __shfl_sync(0xffffffffu, aborted, 0);
+                    if (aborted) break;
+                    ++g;
                 }
-                aborted = __shfl_sync(0xffffffffu, aborted, 0);
-                if (aborted) break;
-                issued = i + 1;
             }
         }
         // Before the warp leaves, every copy it issued must have landed
         // (normally the consumers already saw these phases complete).
         if (lane == 0)
-            for (int i = max(0, issued - kStages); i < issued; ++i)
+            for (int i = max(0, g - kStages); i < g; ++i)
                 mbar_wait(&full[i % kStages], (i / kStages) & 1, p.err);
         return;
     }
 
     // ----------------------------------------------------------------------
-    // Consumer warps.
+    // Consumer warps (threads 0..127).
     // ----------------------------------------------------------------------
-    const int h0 = kvh * G;  // first query head of this KV head's group
-    for (int i = threadIdx.x; i < G * D; i += kConsumers * 32) {
-        const int r = i / D, c = i - (i / D) * D;
-        const uint16_t bits = p.q[(size_t(b) * p.num_q_heads + h0 + r) * D + c];
-        q_s[i] = __uint_as_float(uint32_t(bits) << 16) * p.qk_scale_log2;
-    }
-    named_sync(1, kConsumers * 32);
-
-    float m_run[G], l_lane[G], o_acc[G][kDpl];
-#pragma unroll
-    for (int r = 0; r < G; ++r) {
-        m_run[r] = -INFINITY;
-        l_lane[r] = 0.f;
-#pragma unroll
-        for (int d = 0; d < kDpl; ++d) o_acc[r][d] = 0.f;
-    }
-
+    const int tid = threadIdx.x;
     // P.V addressing: this lane's kDpl channels inside the swizzled V rows.
     const int pv_col = lane * kDpl;
     const int pv_box = pv_col / 64;
     const int pv_byte = (pv_col % 64) * 2;
     const int pv_chunk = pv_byte >> 4;
     const int pv_inner = pv_byte & 15;
-    float *p_w = p_s + warp * kTile * G;
+    float *p_w = reinterpret_cast<float *>(smem + M::p) + warp * kTile * G;
 
-    for (int i = warp; i < ntiles; i += kConsumers) {
-        const int s = i % kStages;
-        if (!mbar_wait(&full[s], (i / kStages) & 1, p.err)) break;
-        const uint8_t *ks = smem + s * S::kStageBytes;
-        const uint8_t *vs = ks + S::kTileBytes;
-        const int t0 = start + i * kTile;
-        const int nvalid = min(kTile, end - t0);
-
-        // ---- scores: lane j <-> key j --------------------------------------
-        float2 acc[G];
+    // q of the next item, prefetched into registers: G*D/128 values per thread.
+    constexpr int kQPer = (G * D + kConsumers * 32 - 1) / (kConsumers * 32);
+    uint16_t q_next[kQPer];
+    auto load_q = [&](int j) {
+        if (j < num_items) {
+            const Item it = decode_item(p, cum, j, hkv);
+            const uint16_t *src = p.q + (size_t(it.b) * p.num_q_heads + it.kvh * G) * D;
 #pragma unroll
-        for (int r = 0; r < G; ++r) acc[r] = make_float2(0.f, 0.f);
-#pragma unroll
-        for (int cb = 0; cb < S::kBoxes; ++cb) {
-            const uint8_t *krow = ks + cb * kTile * 128 + lane * 128;
-#pragma unroll
-            for (int ch = 0; ch < 8; ++ch) {
-                const uint4 kw =
-                    *reinterpret_cast<const uint4 *>(krow + ((ch ^ (lane & 7)) << 4));
-                const float2 k01 = bf16x2_to_float2(kw.x);
-                const float2 k23 = bf16x2_to_float2(kw.y);
-                const float2 k45 = bf16x2_to_float2(kw.z);
-                const float2 k67 = bf16x2_to_float2(kw.w);
-                const float *qc = q_s + cb * 64 + ch * 8;
-#pragma unroll
-                for (int r = 0; r < G; ++r) {
-                    const float4 qa = *reinterpret_cast<const float4 *>(qc + r * D);
-                    const float4 qb = *reinterpret_cast<const float4 *>(qc + r * D + 4);
-                    acc[r] = __ffma2_rn(make_float2(qa.x, qa.y), k01, acc[r]);
-                    acc[r] = __ffma2_rn(make_float2(qa.z, qa.w), k23, acc[r]);
-                    acc[r] = __ffma2_rn(make_float2(qb.x, qb.y), k45, acc[r]);
-                    acc[r] = __ffma2_rn(make_float2(qb.z, qb.w), k67, acc[r]);
-                }
+            for (int k = 0; k < kQPer; ++k) {
+                const int idx = tid + k * kConsumers * 32;
+                q_next[k] = idx < G * D ? src[idx] : uint16_t(0);
             }
         }
+    };
+    load_q(blockIdx.x);
 
-        // ---- online softmax (base 2) ---------------------------------------
-        const bool valid = lane < nvalid;
-        float pr[G], alpha[G];
+    bool ok = true;
+    int g_base = 0;  // tiles of this CTA before the current item
+    int iter = 0;
+    for (int j = blockIdx.x; j < num_items; j += gridDim.x, ++iter) {
+        const Item it = decode_item(p, cum, j, hkv);
+        float *q_s = reinterpret_cast<float *>(smem + M::q) + (iter & 1) * G * D;
+#pragma unroll
+        for (int k = 0; k < kQPer; ++k) {
+            const int idx = tid + k * kConsumers * 32;
+            if (idx < G * D)
+                q_s[idx] = __uint_as_float(uint32_t(q_next[k]) << 16) * p.qk_scale_log2;
+        }
+        load_q(j + gridDim.x);
+        named_sync(1, kConsumers * 32);
+
+        float m_run[G], l_lane[G], o_acc[G][kDpl];
 #pragma unroll
         for (int r = 0; r < G; ++r) {
-            const float sc = valid ? acc[r].x + acc[r].y : -INFINITY;
-            const float mt = warp_max(sc);          // finite: key 0 of the tile is valid
-            const float mn = fmaxf(m_run[r], mt);
-            alpha[r] = fast_exp2(m_run[r] - mn);    // 0 on the first tile
-            pr[r] = fast_exp2(sc - mn);             // 0 for masked keys
-            m_run[r] = mn;
-            l_lane[r] = l_lane[r] * alpha[r] + pr[r];
+            m_run[r] = -INFINITY;
+            l_lane[r] = 0.f;
+#pragma unroll
+            for (int d = 0; d < kDpl; ++d) o_acc[r][d] = 0.f;
         }
-        if constexpr (G == 4) {
-            *reinterpret_cast<float4 *>(p_w + lane * 4) = make_float4(pr[0], pr[1], pr[2], pr[3]);
-        } else if constexpr (G == 2) {
-            *reinterpret_cast<float2 *>(p_w + lane * 2) = make_float2(pr[0], pr[1]);
-        } else {
-#pragma unroll
-            for (int r = 0; r < G; ++r) p_w[lane * G + r] = pr[r];
-        }
-        __syncwarp();
-#pragma unroll
-        for (int r = 0; r < G; ++r)
-#pragma unroll
-            for (int d = 0; d < kDpl; ++d) o_acc[r][d] *= alpha[r];
 
-        // ---- P.V: lane owns kDpl channels of every row ---------------------
-        const uint8_t *vbase = vs + pv_box * kTile * 128 + pv_inner;
-        for (int j = 0; j < nvalid; ++j) {
-            const uint8_t *vr = vbase + j * 128 + ((pv_chunk ^ (j & 7)) << 4);
-            float2 v01, v23;
-            if constexpr (kDpl == 4) {
-                const uint2 vw = *reinterpret_cast<const uint2 *>(vr);
-                v01 = bf16x2_to_float2(vw.x);
-                v23 = bf16x2_to_float2(vw.y);
-            } else {
-                v01 = bf16x2_to_float2(*reinterpret_cast<const uint32_t *>(vr));
+        for (int t = warp; ok && t < it.ntiles; t += kConsumers) {
+            const int g = g_base + t;
+            const int s = g % kStages;
+            if (!mbar_wait(&full[s], (g / kStages) & 1, p.err)) {
+                ok = false;
+                break;
             }
-            float pj[G];
-            if constexpr (G == 4) {
-                const float4 t = *reinterpret_cast<const float4 *>(p_w + j * 4);
-                pj[0] = t.x; pj[1] = t.y; pj[2] = t.z; pj[3] = t.w;
-            } else {
+            const uint8_t *ks = smem + M::stages + s * S::kStageBytes;
+            const uint8_t *vs = ks + S::kTileBytes;
+            const int t0 = it.start + t * kTile;
+            const int nvalid = min(kTile, it.end - t0);
+
+            // ---- scores: lane j <-> key j ----------------------------------
+            float2 acc[G];
 #pragma unroll
-                for (int r = 0; r < G; ++r) pj[r] = p_w[j * G + r];
+            for (int r = 0; r < G; ++r) acc[r] = make_float2(0.f, 0.f);
+#pragma unroll
+            for (int cb = 0; cb < S::kBoxes; ++cb) {
+                const uint8_t *krow = ks + cb * kTile * 128 + lane * 128;
+#pragma unroll
+                for (int ch = 0; ch < 8; ++ch) {
+                    const uint4 kw =
+                        *reinterpret_cast<const uint4 *>(krow + ((ch ^ (lane & 7)) << 4));
+                    const float2 k01 = bf16x2_to_float2(kw.x);
+                    const float2 k23 = bf16x2_to_float2(kw.y);
+                    const float2 k45 = bf16x2_to_float2(kw.z);
+                    const float2 k67 = bf16x2_to_float2(kw.w);
+                    const float *qc = q_s + cb * 64 + ch * 8;
+#pragma unroll
+                    for (int r = 0; r < G; ++r) {
+                        const float4 qa = *reinterpret_cast<const float4 *>(qc + r * D);
+                        const float4 qb = *reinterpret_cast<const float4 *>(qc + r * D + 4);
+                        acc[r] = __ffma2_rn(make_float2(qa.x, qa.y), k01, acc[r]);
+                        acc[r] = __ffma2_rn(make_float2(qa.z, qa.w), k23, acc[r]);
+                        acc[r] = __ffma2_rn(make_float2(qb.x, qb.y), k45, acc[r]);
+                        acc[r] = __ffma2_rn(make_float2(qb.z, qb.w), k67, acc[r]);
+                    }
+                }
             }
+
+            // ---- online softmax (base 2) -----------------------------------
+            const bool valid = lane < nvalid;
+            float pr[G], alpha[G];
 #pragma unroll
             for (int r = 0; r < G; ++r) {
-                float2 o01 = make_float2(o_acc[r][0], o_acc[r][1]);
-                o01 = __ffma2_rn(make_float2(pj[r], pj[r]), v01, o01);
-                o_acc[r][0] = o01.x;
-                o_acc[r][1] = o01.y;
+                const float sc = valid ? acc[r].x + acc[r].y : -INFINITY;
+                const float mt = warp_max(sc);          // finite: key 0 of the tile is valid
+                const float mn = fmaxf(m_run[r], mt);
+                alpha[r] = fast_exp2(m_run[r] - mn);    // 0 on the first tile
+                pr[r] = fast_exp2(sc - mn);             // 0 for masked keys
+                m_run[r] = mn;
+                l_lane[r] = l_lane[r] * alpha[r] + pr[r];
+            }
+            if constexpr (G == 4) {
+                *reinterpret_cast<float4 *>(p_w + lane * 4) =
+                    make_float4(pr[0], pr[1], pr[2], pr[3]);
+            } else if constexpr (G == 2) {
+                *reinterpret_cast<float2 *>(p_w + lane * 2) = make_float2(pr[0], pr[1]);
+            } else {
+#pragma unroll
+                for (int r = 0; r < G; ++r) p_w[lane * G + r] = pr[r];
+            }
+            __syncwarp();
+#pragma unroll
+            for (int r = 0; r < G; ++r)
+#pragma unroll
+                for (int d = 0; d < kDpl; ++d) o_acc[r][d] *= alpha[r];
+
+            // ---- P.V: lane owns kDpl channels of every row -----------------
+            const uint8_t *vbase = vs + pv_box * kTile * 128 + pv_inner;
+            for (int jj = 0; jj < nvalid; ++jj) {
+                const uint8_t *vr = vbase + jj * 128 + ((pv_chunk ^ (jj & 7)) << 4);
+                float2 v01, v23;
                 if constexpr (kDpl == 4) {
-                    float2 o23 = make_float2(o_acc[r][2], o_acc[r][3]);
-                    o23 = __ffma2_rn(make_float2(pj[r], pj[r]), v23, o23);
-                    o_acc[r][2] = o23.x;
-                    o_acc[r][3] = o23.y;
+                    const uint2 vw = *reinterpret_cast<const uint2 *>(vr);
+                    v01 = bf16x2_to_float2(vw.x);
+                    v23 = bf16x2_to_float2(vw.y);
+                } else {
+                    v01 = bf16x2_to_float2(*reinterpret_cast<const uint32_t *>(vr));
+                }
+                float pj[G];
+                if constexpr (G == 4) {
+                    const float4 tq = *reinterpret_cast<const float4 *>(p_w + jj * 4);
+                    pj[0] = tq.x; pj[1] = tq.y; pj[2] = tq.z; pj[3] = tq.w;
+                } else {
+#pragma unroll
+                    for (int r = 0; r < G; ++r) pj[r] = p_w[jj * G + r];
+                }
+#pragma unroll
+                for (int r = 0; r < G; ++r) {
+                    float2 o01 = make_float2(o_acc[r][0], o_acc[r][1]);
+                    o01 = __ffma2_rn(make_float2(pj[r], pj[r]), v01, o01);
+                    o_acc[r][0] = o01.x;
+                    o_acc[r][1] = o01.y;
+                    if constexpr (kDpl == 4) {
+                        float2 o23 = make_float2(o_acc[r][2], o_acc[r][3]);
+                        o23 = __ffma2_rn(make_float2(pj[r], pj[r]), v23, o23);
+                        o_acc[r][2] = o23.x;
+                        o_acc[r][3] = o23.y;
+                    }
+                }
+            }
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&empty[s]);
+        }
+        g_base += it.ntiles;
+
+        // ---- merge the consumer warps' states and write the item --------------
+        float *mb = reinterpret_cast<float *>(smem + M::mrg + (iter & 1) * M::mrg_bytes);
+        float *m_s = mb;                          // [consumer][row]
+        float *l_s = mb + kConsumers * G;
+        float *o_s = mb + 2 * kConsumers * G;     // [consumer][row][D]
+#pragma unroll
+        for (int r = 0; r < G; ++r) {
+            const float l = warp_sum(l_lane[r]);
+            if (lane == 0) {
+                m_s[warp * G + r] = m_run[r];
+                l_s[warp * G + r] = l;
+            }
+#pragma unroll
+            for (int d = 0; d < kDpl; ++d) o_s[(warp * G + r) * D + pv_col + d] = o_acc[r][d];
+        }
+        named_sync(1, kConsumers * 32);
+
+        const int h0 = it.kvh * G;
+        constexpr int kVec = 4;
+        for (int idx = tid; idx < G * D / kVec; idx += kConsumers * 32) {
+            const int r = idx / (D / kVec);
+            const int c0 = (idx - r * (D / kVec)) * kVec;
+            float Mx = -INFINITY;
+#pragma unroll
+            for (int w = 0; w < kConsumers; ++w) Mx = fmaxf(Mx, m_s[w * G + r]);
+            float l = 0.f;
+            float4 o = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+            for (int w = 0; w < kConsumers; ++w) {
+                const float mw = m_s[w * G + r];
+                if (mw == -INFINITY) continue;
+                const float sc = fast_exp2(mw - Mx);
+                l += sc * l_s[w * G + r];
+                const float4 ow = *reinterpret_cast<const float4 *>(o_s + (w * G + r) * D + c0);
+                o.x += sc * ow.x; o.y += sc * ow.y; o.z += sc * ow.z; o.w += sc * ow.w;
+            }
+            const int h = h0 + r;
+            if (it.direct) {
+                const float t2 = p.sink ? p.sink[h] * kLog2e : -INFINITY;
+                const float Mf = fmaxf(Mx, t2);
+                float Z = 0.f, so = 0.f;
+                if (Mf != -INFINITY) {
+                    so = fast_exp2(Mx - Mf);
+                    Z = l * so + fast_exp2(t2 - Mf);
+                }
+                const float inv = Z > 0.f ? so / Z : 0.f;
+                uint2 packed;
+                packed.x = pack_bf16x2(o.x * inv, o.y * inv);
+                packed.y = pack_bf16x2(o.z * inv, o.w * inv);
+                *reinterpret_cast<uint2 *>(p.out + (size_t(it.b) * p.num_q_heads + h) * D + c0) =
+                    packed;
+                if (c0 == 0 && p.lse)
+                    p.lse[size_t(it.b) * p.num_q_heads + h] =
+                        Z > 0.f ? (Mf + fast_log2(Z)) * kLn2 : -INFINITY;
+            } else {
+                const size_t base = (size_t(it.part) * p.batch + it.b) * p.num_q_heads + h;
+                *reinterpret_cast<float4 *>(p.ws_o + base * D + c0) = o;
+                if (c0 == 0) {
+                    p.ws_m[base] = Mx * kLn2;
+                    p.ws_l[base] = l;
                 }
             }
         }
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&empty[s]);
     }
-
     pdl_launch_dependents();
-
-    // ---- merge the consumer warps' states ---------------------------------
-#pragma unroll
-    for (int r = 0; r < G; ++r) {
-        const float l = warp_sum(l_lane[r]);
-        if (lane == 0) {
-            m_s[warp * G + r] = m_run[r];
-            l_s[warp * G + r] = l;
-        }
-#pragma unroll
-        for (int d = 0; d < kDpl; ++d) o_s[(warp * G + r) * D + pv_col + d] = o_acc[r][d];
-    }
-    named_sync(1, kConsumers * 32);
-
-    constexpr int kVec = 4;
-    for (int idx = threadIdx.x; idx < G * D / kVec; idx += kConsumers * 32) {
-        const int r = idx / (D / kVec);
-        const int c0 = (idx - r * (D / kVec)) * kVec;
-        float M = -INFINITY;
-#pragma unroll
-        for (int w = 0; w < kConsumers; ++w) M = fmaxf(M, m_s[w * G + r]);
-        float l = 0.f;
-        float4 o = make_float4(0.f, 0.f, 0.f, 0.f);
-#pragma unroll
-        for (int w = 0; w < kConsumers; ++w) {
-            const float mw = m_s[w * G + r];
-            if (mw == -INFINITY) continue;
-            const float sc = fast_exp2(mw - M);
-            l += sc * l_s[w * G + r];
-            const float4 ow = *reinterpret_cast<const float4 *>(o_s + (w * G + r) * D + c0);
-            o.x += sc * ow.x; o.y += sc * ow.y; o.z += sc * ow.z; o.w += sc * ow.w;
-        }
-        const int h = h0 + r;
-        if (direct) {
-            const float t2 = p.sink ? p.sink[h] * kLog2e : -INFINITY;
-            const float Mf = fmaxf(M, t2);
-            float Z = 0.f, so = 0.f;
-            if (Mf != -INFINITY) {
-                so = fast_exp2(M - Mf);
-                Z = l * so + fast_exp2(t2 - Mf);
-            }
-            const float inv = Z > 0.f ? so / Z : 0.f;
-            uint2 packed;
-            packed.x = pack_bf16x2(o.x * inv, o.y * inv);
-            packed.y = pack_bf16x2(o.z * inv, o.w * inv);
-            *reinterpret_cast<uint2 *>(p.out + (size_t(b) * p.num_q_heads + h) * D + c0) = packed;
-            if (c0 == 0 && p.lse)
-                p.lse[size_t(b) * p.num_q_heads + h] =
-                    Z > 0.f ? (Mf + fast_log2(Z)) * kLn2 : -INFINITY;
-        } else {
-            const size_t base = (size_t(part) * p.batch + b) * p.num_q_heads + h;
-            *reinterpret_cast<float4 *>(p.ws_o + base * D + c0) = o;
-            if (c0 == 0) {
-                p.ws_m[base] = M * kLn2;
-                p.ws_l[base] = l;
-            }
-        }
-    }
 }
+
+int g_num_sms[64];
 
 template <int D, int G>
 cudaError_t launch_t(const GqaParams &p, cudaStream_t stream) {
-    constexpr size_t smem = gqa_smem_bytes<D, G>();
+    const size_t smem = gqa_smem_bytes<D, G>(p.batch);
     auto kern = gqa_decode_kernel<D, G>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          int(smem));
     if (e != cudaSuccess) return e;
-    dim3 grid(p.num_partitions, p.num_q_heads / G, p.batch);
-    kern<<<grid, kThreads, smem, stream>>>(p);
+    int dev = 0;
+    e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+    if (g_num_sms[dev] == 0) {
+        int n = 0;
+        e = cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
+        if (e != cudaSuccess) return e;
+        g_num_sms[dev] = n;
+    }
+    // Two resident CTAs per SM; never more CTAs than the largest item count.
+    long long grid = 2LL * g_num_sms[dev];
+    const long long max_items = static_cast<long long>(p.batch) * (p.num_q_heads / G) *
+                                p.num_partitions;
+    if (grid > max_items) grid = max_items;
+    if (grid < 1) grid = 1;
+    kern<<<dim3(static_cast<unsigned>(grid)), kThreads, smem, stream>>>(p);
     return cudaGetLastError();
 }
 
