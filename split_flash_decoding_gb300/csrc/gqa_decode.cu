@@ -8,15 +8,20 @@
 // (item j goes to CTA j mod grid), so the TMA pipeline never drains between
 // items and slices past a sequence's end cost nothing.  Inside a CTA:
 //
-//   * one producer warp streams 32-key K and V tiles with TMA
-//     (cp.async.bulk.tensor, 128-byte swizzle) into a ring of shared-memory
-//     stages, translating logical token -> (page, slot) through the page
-//     table; it runs ahead across item boundaries;
-//   * four consumer warps take an item's tiles round-robin.  Each keeps its
-//     own online-softmax state (running max m, exp-sum l, unnormalised O) --
-//     a warp-level split of the slice ("decoding_warp_split_k",
-//     mha_decoding_single_batch_pipelined, Parameters) -- merged at the end of
-//     the item;
+//   * two producer warps stream 32-key K tiles and V tiles with TMA
+//     (cp.async.bulk.tensor, 128-byte swizzle) into two rings of shared-
+//     memory stages, translating logical token -> (page, slot) through the
+//     page table; they run ahead across item boundaries, K and V each at
+//     their own pace, so the K of a warp's next tile lands while it is still
+//     busy with the V of the current one;
+//   * four consumer warps take the tiles round-robin (tile g -> warp g % 4).
+//     Both ring sizes are multiples of 4, so every stage is always consumed
+//     by the same warp, in order: a waiter is never more than one phase
+//     behind its barrier and the parity wait cannot alias an older phase.
+//     Each warp keeps its own online-softmax state (running max m, exp-sum l,
+//     unnormalised O) -- a warp-level split of the slice
+//     ("decoding_warp_split_k", mha_decoding_single_batch_pipelined,
+//     Parameters) -- merged at the end of the item;
 //   * scores: lane j owns key j of the tile and dots it with all group rows
 //     of q (fp32, packed FFMA2); softmax statistics use warp-shuffle max;
 //     P.V: lane owns head_dim/32 channels of every row.
@@ -41,27 +46,33 @@ constexpr int kTile = kGqaTileKeys;  // keys per stage
 constexpr int kConsumers = 4;        // consumer warps
 constexpr int kThreads = (kConsumers + 1) * 32;
 
-// Stage counts keep two CTAs (~104 KB each) resident per SM.
+constexpr int kThreadsAll = kThreads + 32;  // + the V producer warp
+
+// Ring sizes are multiples of kConsumers (stage ownership, see above) and keep
+// two CTAs (<= ~112 KB each) resident per SM.
 template <int D, int G>
 struct GqaShape {
     static constexpr int kBoxes = D / 64;                 // 64-channel (128 B) column boxes
     static constexpr int kTileBytes = kTile * D * 2;      // one K or V tile
-    static constexpr int kStageBytes = 2 * kTileBytes;
-    static constexpr int kStages = D == 128 ? (G >= 8 ? 3 : 5) : 10;
+    static constexpr int kKStages = D == 128 ? (G >= 8 ? 4 : 8) : 8;
+    static constexpr int kVStages = 4;
     static constexpr int kDpl = D / 32;                   // P.V channels per lane
+    static_assert(kKStages % kConsumers == 0 && kVStages % kConsumers == 0,
+                  "every stage must have a single consumer warp");
 };
 
 // Shared-memory layout (byte offsets from the 1024-aligned base).
 template <int D, int G>
 struct GqaSmem {
     using S = GqaShape<D, G>;
-    static constexpr int stages = 0;
-    static constexpr int q = stages + S::kStages * S::kStageBytes;      // fp32 [2][G][D]
+    static constexpr int kring = 0;
+    static constexpr int vring = kring + S::kKStages * S::kTileBytes;
+    static constexpr int q = vring + S::kVStages * S::kTileBytes;        // fp32 [2][G][D]
     static constexpr int p = q + 2 * G * D * 4;                          // fp32 [4][32][G]
-    static constexpr int mrg = p + kConsumers * kTile * G * 4;           // [2] merge buffers
+    static constexpr int mrg = p + kConsumers * kTile * G * 4;           // merge buffer
     static constexpr int mrg_bytes = (2 * kConsumers * G + kConsumers * G * D) * 4;
-    static constexpr int bars = mrg + 2 * mrg_bytes;                     // full[], empty[]
-    static constexpr int items = bars + 2 * S::kStages * 8;              // int [batch + 1]
+    static constexpr int bars = mrg + mrg_bytes;                         // kfull, kempty, vfull, vempty
+    static constexpr int items = bars + 2 * (S::kKStages + S::kVStages) * 8;  // int [batch + 1]
     static constexpr int fixed = items;
 };
 
@@ -99,18 +110,21 @@ __device__ __forceinline__ Item decode_item(const GqaParams &p, const int *cum, 
 }
 
 template <int D, int G>
-__global__ void __launch_bounds__(kThreads, 2)
+__global__ void __launch_bounds__(kThreadsAll, 2)
 gqa_decode_kernel(const __grid_constant__ GqaParams p) {
     using S = GqaShape<D, G>;
     using M = GqaSmem<D, G>;
-    constexpr int kStages = S::kStages;
+    constexpr int kKStages = S::kKStages;
+    constexpr int kVStages = S::kVStages;
     constexpr int kDpl = S::kDpl;
 
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-    uint64_t *full = reinterpret_cast<uint64_t *>(smem + M::bars);
-    uint64_t *empty = full + kStages;
+    uint64_t *kfull = reinterpret_cast<uint64_t *>(smem + M::bars);
+    uint64_t *kempty = kfull + kKStages;
+    uint64_t *vfull = kempty + kKStages;
+    uint64_t *vempty = vfull + kVStages;
     int *cum = reinterpret_cast<int *>(smem + M::items);
 
     const int warp = threadIdx.x >> 5;
@@ -152,28 +166,36 @@ gqa_decode_kernel(const __grid_constant__ GqaParams p) {
         if (lane == 31) cum[p.batch] = incl;
     }
     if (threadIdx.x == 32) {
-        for (int s = 0; s < kStages; ++s) {
-            mbar_init(&full[s], 1);
-            mbar_init(&empty[s], 1);
+        for (int s = 0; s < kKStages; ++s) {
+            mbar_init(&kfull[s], 1);
+            mbar_init(&kempty[s], 1);
+        }
+        for (int s = 0; s < kVStages; ++s) {
+            mbar_init(&vfull[s], 1);
+            mbar_init(&vempty[s], 1);
         }
         fence_mbar_init();
     }
     __syncthreads();
     const int num_items = cum[p.batch];
 
-    if (warp == kConsumers) {
+    if (warp >= kConsumers) {
         // ------------------------------------------------------------------
-        // Producer warp: page-table lookups by all lanes, TMA issue by lane 0.
+        // Producer warps: warp 4 streams K, warp 5 streams V.  Page-table
+        // lookups by all lanes, TMA issue by lane 0.
         // ------------------------------------------------------------------
-        if (lane == 0) {
-            prefetch_tensormap(&p.k_map);
-            prefetch_tensormap(&p.v_map);
-        }
+        const bool is_k = warp == kConsumers;
+        const CUtensorMap *map = is_k ? &p.k_map : &p.v_map;
+        const int nst = is_k ? kKStages : kVStages;
+        uint64_t *full = is_k ? kfull : vfull;
+        uint64_t *empty = is_k ? kempty : vempty;
+        uint8_t *ring = smem + (is_k ? M::kring : M::vring);
+        if (lane == 0) prefetch_tensormap(map);
         const int box_rows = p.box_rows;  // 32, 16 or 8
         const int boxes_per_tile = kTile / box_rows;
         const uint32_t box_bytes = uint32_t(box_rows) * 128u;
         bool aborted = false;
-        int g = 0;  // tiles issued by this CTA so far
+        int g = 0;  // tiles issued by this warp so far
         for (int j = blockIdx.x; j < num_items && !aborted; j += gridDim.x) {
             const Item it = decode_item(p, cum, j, hkv);
             for (int base = 0; base < it.ntiles && !aborted; base += 32) {
@@ -191,7 +213,7 @@ gqa_decode_kernel(const __grid_constant__ GqaParams p) {
                             int e = pidx < p.max_pages
                                         ? p.page_table[size_t(it.b) * p.max_pages + pidx] : -1;
                             if (e < 0 || e >= p.num_pages) {
-                                atomicOr(p.err, kErrBadPage);
+                                if (is_k) atomicOr(p.err, kErrBadPage);
                                 e = -1;
                             }
                             pg[r] = e;
@@ -211,29 +233,22 @@ gqa_decode_kernel(const __grid_constant__ GqaParams p) {
                         slots[r] = __shfl_sync(0xffffffffu, sl[r], i - base);
                     }
                     if (lane == 0) {
-                        const int s = g % kStages;
-                        if (g >= kStages &&
-                            !mbar_wait(&empty[s], ((g / kStages) - 1) & 1, p.err)) {
+                        const int s = g % nst;
+                        if (g >= nst && !mbar_wait(&empty[s], ((g / nst) - 1) & 1, p.err)) {
                             aborted = true;
                         } else {
                             uint32_t nbox = 0;
 #pragma unroll
                             for (int r = 0; r < 4; ++r) nbox += pages[r] >= 0 ? 1u : 0u;
-                            // every box is loaded for K and V, in kBoxes column blocks
-                            mbar_arrive_expect_tx(&full[s], 2u * S::kBoxes * nbox * box_bytes);
-                            uint8_t *ks = smem + M::stages + s * S::kStageBytes;
-                            uint8_t *vs = ks + S::kTileBytes;
+                            mbar_arrive_expect_tx(&full[s], S::kBoxes * nbox * box_bytes);
+                            uint8_t *dst = ring + s * S::kTileBytes;
 #pragma unroll
                             for (int r = 0; r < 4; ++r) {
                                 if (pages[r] < 0) continue;
 #pragma unroll
-                                for (int cb = 0; cb < S::kBoxes; ++cb) {
-                                    const int off = cb * kTile * 128 + r * box_rows * 128;
-                                    tma_load_4d(ks + off, &p.k_map, &full[s], cb * 64, slots[r],
-                                                it.kvh, pages[r]);
-                                    tma_load_4d(vs + off, &p.v_map, &full[s], cb * 64, slots[r],
-                                                it.kvh, pages[r]);
-                                }
+                                for (int cb = 0; cb < S::kBoxes; ++cb)
+                                    tma_load_4d(dst + cb * kTile * 128 + r * box_rows * 128, map,
+                                                &full[s], cb * 64, slots[r], it.kvh, pages[r]);
                             }
                         }
                     }
@@ -246,8 +261,8 @@ gqa_decode_kernel(const __grid_constant__ GqaParams p) {
         // Before the warp leaves, every copy it issued must have landed
         // (normally the consumers already saw these phases complete).
         if (lane == 0)
-            for (int i = max(0, g - kStages); i < g; ++i)
-                mbar_wait(&full[i % kStages], (i / kStages) & 1, p.err);
+            for (int i = max(0, g - nst); i < g; ++i)
+                mbar_wait(&full[i % nst], (i / nst) & 1, p.err);
         return;
     }
 
@@ -263,7 +278,7 @@ gqa_decode_kernel(const __grid_constant__ GqaParams p) {
     const int pv_inner = pv_byte & 15;
     float *p_w = reinterpret_cast<float *>(smem + M::p) + warp * kTile * G;
 
-    // q of the next item, prefetched into registers: G*D/128 values per thread.
+    // q of the next item, prefetched into registers.
     constexpr int kQPer = (G * D + kConsumers * 32 - 1) / (kConsumers * 32);
     uint16_t q_next[kQPer];
     auto load_q = [&](int j) {
@@ -292,6 +307,8 @@ gqa_decode_kernel(const __grid_constant__ GqaParams p) {
                 q_s[idx] = __uint_as_float(uint32_t(q_next[k]) << 16) * p.qk_scale_log2;
         }
         load_q(j + gridDim.x);
+        // q_s ready; every consumer has also finished reading the merge
+        // buffer of the previous item.
         named_sync(1, kConsumers * 32);
 
         float m_run[G], l_lane[G], o_acc[G][kDpl];
@@ -303,15 +320,18 @@ gqa_decode_kernel(const __grid_constant__ GqaParams p) {
             for (int d = 0; d < kDpl; ++d) o_acc[r][d] = 0.f;
         }
 
-        for (int t = warp; ok && t < it.ntiles; t += kConsumers) {
+        // This warp's tiles of the item: item-local t with (g_base + t) % 4 == warp.
+        const int t_first = (warp - g_base % kConsumers + kConsumers) % kConsumers;
+        for (int t = t_first; ok && t < it.ntiles; t += kConsumers) {
             const int g = g_base + t;
-            const int s = g % kStages;
-            if (!mbar_wait(&full[s], (g / kStages) & 1, p.err)) {
+            const int sk = g % kKStages;
+            const int sv = g % kVStages;
+            if (!mbar_wait(&kfull[sk], (g / kKStages) & 1, p.err)) {
                 ok = false;
                 break;
             }
-            const uint8_t *ks = smem + M::stages + s * S::kStageBytes;
-            const uint8_t *vs = ks + S::kTileBytes;
+            const uint8_t *ks = smem + M::kring + sk * S::kTileBytes;
+            const uint8_t *vs = smem + M::vring + sv * S::kTileBytes;
             const int t0 = it.start + t * kTile;
             const int nvalid = min(kTile, it.end - t0);
 
@@ -342,6 +362,8 @@ gqa_decode_kernel(const __grid_constant__ GqaParams p) {
                     }
                 }
             }
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&kempty[sk]);   // K tile no longer needed
 
             // ---- online softmax (base 2) -----------------------------------
             const bool valid = lane < nvalid;
@@ -372,6 +394,10 @@ gqa_decode_kernel(const __grid_constant__ GqaParams p) {
                 for (int d = 0; d < kDpl; ++d) o_acc[r][d] *= alpha[r];
 
             // ---- P.V: lane owns kDpl channels of every row -----------------
+            if (!mbar_wait(&vfull[sv], (g / kVStages) & 1, p.err)) {
+                ok = false;
+                break;
+            }
             const uint8_t *vbase = vs + pv_box * kTile * 128 + pv_inner;
             for (int jj = 0; jj < nvalid; ++jj) {
                 const uint8_t *vr = vbase + jj * 128 + ((pv_chunk ^ (jj & 7)) << 4);
@@ -406,12 +432,12 @@ gqa_decode_kernel(const __grid_constant__ GqaParams p) {
                 }
             }
             __syncwarp();
-            if (lane == 0) mbar_arrive(&empty[s]);
+            if (lane == 0) mbar_arrive(&vempty[sv]);
         }
         g_base += it.ntiles;
 
         // ---- merge the consumer warps' states and write the item --------------
-        float *mb = reinterpret_cast<float *>(smem + M::mrg + (iter & 1) * M::mrg_bytes);
+        float *mb = reinterpret_cast<float *>(smem + M::mrg);
         float *m_s = mb;                          // [consumer][row]
         float *l_s = mb + kConsumers * G;
         float *o_s = mb + 2 * kConsumers * G;     // [consumer][row][D]
@@ -502,7 +528,7 @@ cudaError_t launch_t(const GqaParams &p, cudaStream_t stream) {
                                 p.num_partitions;
     if (grid > max_items) grid = max_items;
     if (grid < 1) grid = 1;
-    kern<<<dim3(static_cast<unsigned>(grid)), kThreads, smem, stream>>>(p);
+    kern<<<dim3(static_cast<unsigned>(grid)), kThreadsAll, smem, stream>>>(p);
     return cudaGetLastError();
 }
 
