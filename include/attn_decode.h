@@ -217,6 +217,33 @@ int attn_splitk_reduce(const float *ws_o, const float *ws_m, const float *ws_l,
                        const float *sink, void *out, float *lse, attn_stream_t stream);
 
 /*
+ * attn_decode_noalloc -- attn_decode for callers that cannot allocate device
+ * memory: an engine plugin bound to a memory plan fixed at start-up, or a
+ * plain C program with no allocator at hand.  The source pages have no
+ * counterpart; it exists only because split-K needs scratch space.
+ *
+ * Arguments are those of attn_decode without workspace / workspace_bytes;
+ * num_partitions 0 plans automatically (attn_plan_partitions).  The split-K
+ * scratch is a fixed 32 MiB array inside the library (a file-scope device
+ * array that every GPU loading the library keeps until the process exits);
+ * a partition count whose workspace would exceed it returns
+ * ATTN_ERR_WORKSPACE and launches nothing.  The call itself allocates
+ * nothing (no cudaMalloc/cudaFree, no allocating library routine).
+ *
+ * The first call on a device looks up the array's device address
+ * (cudaGetSymbolAddress, with that device current); make that first call
+ * before any stream capture.  Every call shares the one array and leaves its
+ * partials there: calls that can overlap on the GPU (other streams, other
+ * host threads) race on it and must be serialised by the caller.  Nothing in
+ * it needs to start at zero.
+ */
+int attn_decode_noalloc(const void *q, const attn_kv_t *k, const attn_kv_t *v,
+                        const uint32_t *kv_len, const uint32_t *q_row_offsets, int batch,
+                        int num_q_rows, int num_q_heads, int group, int head_dim, int max_q_len,
+                        int max_kv_len, float scale, const float *sink, int causal,
+                        int num_partitions, void *out, float *lse, attn_stream_t stream);
+
+/*
  * attn_device_error_flags -- read (and optionally clear) the device-side
  * error word that kernels set instead of hanging: bit 0 = a pipeline wait
  * ran past its time limit, bit 1 = a page-table entry outside

@@ -70,6 +70,10 @@ _SIGNATURES = {
     "attn_splitk_reduce": [_c.c_void_p, _c.c_void_p, _c.c_void_p, _c.c_int, _c.c_int, _c.c_int,
                            _c.c_int, _c.c_void_p, _c.c_void_p, _c.c_void_p, _c.c_void_p],
     "attn_device_error_flags": [_c.POINTER(_c.c_uint), _c.c_int],
+    "attn_decode_noalloc": [_c.c_void_p, _c.POINTER(attn_kv_t), _c.POINTER(attn_kv_t),
+                            _c.c_void_p, _c.c_void_p, _c.c_int, _c.c_int, _c.c_int, _c.c_int,
+                            _c.c_int, _c.c_int, _c.c_int, _c.c_float, _c.c_void_p, _c.c_int,
+                            _c.c_int, _c.c_void_p, _c.c_void_p, _c.c_void_p],
 }
 
 _lib = None
@@ -242,6 +246,29 @@ def attn_splitk_reduce(ws_o: torch.Tensor, ws_m: torch.Tensor, ws_l: torch.Tenso
            lib().attn_splitk_reduce(ws_o.data_ptr(), ws_m.data_ptr(), ws_l.data_ptr(), P, rows,
                                     hq, dv, _ptr(sink), out.data_ptr(), _ptr(lse),
                                     _stream_handle(stream)))
+    return out, lse
+
+
+def attn_decode_noalloc(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tensor,
+                        kv_len: torch.Tensor, *, group: int, scale: float, max_kv_len: int,
+                        page_table: Optional[torch.Tensor] = None,
+                        sink: Optional[torch.Tensor] = None,
+                        q_row_offsets: Optional[torch.Tensor] = None, max_q_len: int = 1,
+                        causal: bool = False, num_partitions: int = 0,
+                        out: torch.Tensor, lse: Optional[torch.Tensor] = None, stream=None):
+    """attn_decode whose split-K scratch is the library's fixed device array,
+    for callers that cannot allocate: the caller passes only inputs and
+    outputs (out must be preallocated), and the call allocates nothing."""
+    rows, hq, d = q.shape
+    batch = kv_len.shape[0]
+    kd = kv_descriptor(k_cache, page_table)
+    vd = kv_descriptor(v_cache, page_table)
+    _check("attn_decode_noalloc",
+           lib().attn_decode_noalloc(q.data_ptr(), ctypes.byref(kd), ctypes.byref(vd),
+                                     kv_len.data_ptr(), _ptr(q_row_offsets), batch, rows, hq,
+                                     group, d, max_q_len, max_kv_len, scale, _ptr(sink),
+                                     1 if causal else 0, num_partitions, out.data_ptr(),
+                                     _ptr(lse), _stream_handle(stream)))
     return out, lse
 
 
