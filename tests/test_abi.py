@@ -142,11 +142,16 @@ def test_planner_formulas(attn):
         align = lambda x: (x + 255) // 256 * 256
         expect = 0 if req == 1 else align(n * 128 * 4) + 2 * align(n * 4)
         assert ws == expect
-    # automatic: at least one wave of CTAs, slices of about 512 keys
+    # automatic GQA (two CTAs per SM): fewer units than CTAs -> one wave of
+    # slices; otherwise >= 4 items per CTA at full length and slices of
+    # <= ~1024 keys
     P, _ = attn.attn_plan_partitions(64, 64, 32, 8, 128, 8192, 0, num_sms=152)
-    assert P == 16
+    assert P == 8
     P, _ = attn.attn_plan_partitions(1, 1, 32, 8, 128, 131072, 0, num_sms=152)
-    assert 8 * P >= 2 * 152
+    assert P == 38 and 8 * P == 2 * 152
+    # automatic MLA (one KV head, 512 output channels): one cluster per SM pair
+    P, _ = attn.attn_plan_partitions(32, 32, 128, 1, 512, 32768, 0, num_sms=152)
+    assert P == 19 and 32 * P >= 4 * 76 and (32 * P) % 76 == 0
     P, _ = attn.attn_plan_partitions(1, 1, 32, 8, 128, 20, 0, num_sms=152)
     assert P == 1                                     # one tile of keys cannot split
     P, _ = attn.attn_plan_partitions(4, 4, 32, 8, 128, 0, 0, num_sms=152)
