@@ -110,10 +110,11 @@ typedef struct attn_kv {
  *                 for this P (0 when P == 1).
  *
  * Key slice p of a sequence is [p*C, min((p+1)*C, kv_len)) with
- * C = ceil(ceil(max_kv_len / P) / T) * T, T = 32 for attn_decode and 64 for
- * attn_mla_decode; slices past kv_len are empty.  The automatic choice
- * treats num_kv_heads == 1 with head_dim_v == 512 as the MLA shape (longer
- * slices, one two-CTA cluster per SM pair) and everything else as GQA.
+ * C = ceil(ceil(max_kv_len / P) / T) * T, T = 128 for attn_decode with
+ * head_dim 128, 32 for head_dim 64, and 64 for attn_mla_decode; slices past
+ * kv_len are empty.  The automatic choice treats num_kv_heads == 1 with
+ * head_dim_v == 512 as the MLA shape (longer slices, one two-CTA cluster per
+ * SM pair) and everything else as GQA.
  * Returns ATTN_OK, ATTN_ERR_INVALID_ARG, or ATTN_ERR_CUDA if the SM count
  * query fails.  Launches nothing.
  */
@@ -136,7 +137,8 @@ int attn_plan_partitions(int num_sms, int batch, int num_q_rows, int num_q_heads
  *   q_row_offsets  device uint32 [batch + 1] (rows of sequence b are
  *              [off[b], off[b+1])), or NULL for one row per sequence.
  *   batch, num_q_rows   sequences and total query rows (num_q_rows = batch
- *              when q_row_offsets is NULL; otherwise = off[batch]).
+ *              when q_row_offsets is NULL; otherwise = off[batch]).  Single-
+ *              token decode accepts batch <= 2048.
  *   num_q_heads, group  num_q_heads % group == 0; group in {1, 2, 4, 8}.
  *   head_dim   64 or 128 (128 when max_q_len > 1).
  *   max_q_len  host upper bound of the rows of any sequence ("max_prompt_len

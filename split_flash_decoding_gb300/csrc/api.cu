@@ -225,8 +225,9 @@ extern "C" int attn_plan_partitions(int num_sms, int batch, int num_q_rows, int 
                     cudaSuccess)
                 return ATTN_ERR_CUDA;
         }
-        // GQA runs a persistent grid of two CTAs per SM over (sequence, KV
-        // head, slice) items; MLA runs one two-CTA cluster per SM pair per
+        // GQA runs a persistent grid over (sequence, KV head, slice) items,
+        // one CTA per SM for head_dim 128 (tensor cores) and two for
+        // head_dim 64; MLA runs one two-CTA cluster per SM pair per
         // item and writes 256 KB of fp32 partials per slice, so its slices
         // are longer.  GQA with fewer (sequence, KV head) units than CTAs gets
         // one slice per CTA (one wave), as if every sequence had max_kv_len
@@ -236,8 +237,10 @@ extern "C" int attn_plan_partitions(int num_sms, int batch, int num_q_rows, int 
         // balanced; when it does not cost more than doubling P, P is rounded
         // up so that units * P is a multiple of the CTA count.
         const bool mla = num_kv_heads == 1 && head_dim_v == kMlaDimV;
+        const bool tc = !mla && head_dim_v == 128;   // tensor-core decode: one CTA per SM
         const long long units = static_cast<long long>(batch > 0 ? batch : 1) * num_kv_heads;
-        const long long ctas = mla ? (num_sms / 2 > 0 ? num_sms / 2 : 1) : 2LL * num_sms;
+        const long long ctas = mla ? (num_sms / 2 > 0 ? num_sms / 2 : 1)
+                                   : (tc ? num_sms : 2LL * num_sms);
         const long long target = mla ? 4096 : 1024;
         long long p;
         if (!mla && units < ctas) {
@@ -252,7 +255,7 @@ extern "C" int attn_plan_partitions(int num_sms, int batch, int num_q_rows, int 
             const long long aligned = (p + q - 1) / q * q;
             if (aligned <= 2 * p) p = aligned;
         }
-        const long long tile = mla ? kMlaTileKeys : kGqaTileKeys;
+        const long long tile = mla ? kMlaTileKeys : (tc ? kGqaTcTileKeys : kGqaTileKeys);
         const long long p_max_useful = (static_cast<long long>(max_kv_len) + tile - 1) / tile;
         if (p > p_max_useful) p = p_max_useful;
         if (p < 1) p = 1;
@@ -309,14 +312,30 @@ extern "C" int attn_decode(const void *q, const attn_kv_t *k, const attn_kv_t *v
         if (reinterpret_cast<uintptr_t>(workspace) % 256) return ATTN_ERR_WORKSPACE;
     }
 
+    // head_dim 128 runs on the tensor cores (128-key tiles), head_dim 64 on
+    // the CUDA cores (32-key tiles).
+    const bool tc = head_dim == 128;
+    const int tile = tc ? kGqaTcTileKeys : kGqaTileKeys;
     GqaParams p;
     std::memset(&p, 0, sizeof(p));
-    p.box_rows = k->page_table ? (k->page_size < kGqaTileKeys ? k->page_size : kGqaTileKeys)
-                               : kGqaTileKeys;
+    p.box_rows = k->page_table ? (k->page_size < tile ? k->page_size : tile) : tile;
     st = encode_kv_map(&p.k_map, *k, head_dim, hkv, p.box_rows);
     if (st) return st;
     st = encode_kv_map(&p.v_map, *v, head_dim, hkv, p.box_rows);
     if (st) return st;
+    if (tc) {
+        EncodeTiledFn fn = encode_fn();
+        if (!fn) return ATTN_ERR_CUDA;
+        cuuint64_t gdim[2] = {128, cuuint64_t(batch) * cuuint64_t(num_q_heads)};
+        cuuint64_t gstride[1] = {128 * 2};
+        cuuint32_t box[2] = {64, cuuint32_t(group)};
+        cuuint32_t estride[2] = {1, 1};
+        CUresult r = fn(&p.q_map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void *>(q),
+                        gdim, gstride, box, estride, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                        CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                        CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+        if (r != CUDA_SUCCESS) return ATTN_ERR_UNSUPPORTED;
+    }
     st = error_word(&p.err);
     if (st) return st;
 
@@ -340,11 +359,11 @@ extern "C" int attn_decode(const void *q, const attn_kv_t *k, const attn_kv_t *v
     p.page_size = k->page_size;
     p.num_pages = k->num_pages;
     p.num_partitions = num_partitions;
-    p.chunk = chunk_for(max_kv_len, num_partitions, kGqaTileKeys);
+    p.chunk = chunk_for(max_kv_len, num_partitions, tile);
     p.qk_scale_log2 = scale * 1.4426950408889634f;
 
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-    st = map_cuda(launch_gqa_decode(p, s));
+    st = map_cuda(tc ? launch_gqa_decode_tc(p, s) : launch_gqa_decode(p, s));
     if (st || num_partitions == 1) return st;
 
     ReduceParams r;

@@ -1,0 +1,507 @@
+// gqa_decode_tc.cu -- split-K flash-decoding for grouped-query attention with
+// head_dim 128 on the 5th-generation tensor cores.
+//
+// Same work list as the CUDA-core kernel (gqa_items.cuh: one item = one
+// (sequence, KV head, key slice), persistent grid, one CTA per SM), but the
+// two contractions of a 128-key tile run as tcgen05 MMAs with the keys / the
+// channels on the 128-row M dimension and the folded query heads of the group
+// on N (padded to 16):
+//
+//   S^T [128 keys x 16]  = K_tile [128 keys x 128 ch] . Q^T    (K-major A, B)
+//   O^T [128 ch x 16]   += V_tile^T [128 ch x 128 keys] . P^T  (MN-major A)
+//
+// so the per-key work left to the SIMT threads is the softmax only (thread =
+// key of the tile = TMEM lane), and the kernel stays bound by HBM.  The group
+// makes Q.K' and P.V dense contractions of depth 128 over 128 keys; only the
+// N side is padded.
+//
+// Warp roles (224 threads): warps 0-3 softmax and epilogue, warp 4 streams
+// K tiles and the item's Q (TMA), warp 5 streams V tiles (TMA), warp 6 owns
+// TMEM and issues the MMAs.  Rings: 3 K stages and 3 V stages of 32 KB, each
+// consumed in order by the single MMA thread, so parity waits never alias.
+//
+// Per tile: the MMA thread issues S(t) into one of two TMEM score buffers as
+// soon as K(t) has landed; the softmax warps take the tile max per head
+// across the four warps (shared memory), update the running max m and sums
+// l, rescale O^T in TMEM when m moved, and write P^T (bf16) to shared memory;
+// the MMA thread then accumulates O^T += V(t)^T P(t)^T.  Scores are scaled
+// in fp32 after the MMA (q enters the MMA unscaled and exact).  Two sums are
+// kept: of the fp32 weights (lse) and of the bf16 weights the MMA used
+// (normalisation of O).  Keys past the sequence end are masked in S and
+// zeroed in the V stage before the P.V MMA reads it.
+#include "gqa_items.cuh"
+#include "launch.h"
+#include "ptx.cuh"
+#include "tc.cuh"
+
+namespace attn {
+namespace {
+
+constexpr int kD = 128;
+constexpr int kBK = kGqaTcTileKeys;          // 128 keys per tile
+constexpr int kStages = 3;
+constexpr int kBox = 128 * 128;              // 128 rows x 128 B
+constexpr int kTileBytes = 2 * kBox;         // 128 keys x 128 channels, bf16
+constexpr int kNRows = 16;                   // N of both MMAs (query heads, padded)
+constexpr int kNBox = kNRows * 128;          // 16 rows x 128 B
+constexpr int kNBytes = 2 * kNBox;           // 16 rows x 128 channels / keys
+constexpr int kThreads = 224;
+constexpr uint32_t kTmemCols = 64;
+constexpr uint32_t kTmemS = 0;               // two 16-column score buffers
+constexpr uint32_t kTmemO = 32;              // 16-column output accumulator
+
+struct Smem {
+    static constexpr int kring = 0;
+    static constexpr int vring = kring + kStages * kTileBytes;
+    static constexpr int q = vring + kStages * kTileBytes;     // [2] Q^T buffers
+    static constexpr int p = q + 2 * kNBytes;                   // P^T
+    static constexpr int red = p + kNBytes;                     // float [2][4][16] tile max
+    static constexpr int lred = red + 2 * 4 * 16 * 4;           // float [2][4][16] row sums
+    static constexpr int bars = lred + 2 * 4 * 16 * 4;
+    static constexpr int items = bars + 256;
+};
+
+enum Bar {
+    kKFull = 0, kKEmpty = 3, kVFull = 6, kVEmpty = 9,   // [3] each
+    kQFull = 12, kQEmpty = 14,                          // [2] each
+    kSFull = 16, kSFree = 18,                           // [2] each
+    kPFull = 20, kODone = 21,
+    kNumBars = 22
+};
+
+size_t tc_smem_bytes(int batch) {
+    return 1024 + size_t(Smem::items) + sizeof(int) * size_t(batch + 1);
+}
+
+// Position of element (row r, column c) of a 16-row operand stored as two
+// 128-byte-swizzled column boxes of 64 bf16 each.
+__device__ __forceinline__ uint32_t n_operand_offset(int r, int c) {
+    const int box = c >> 6, chunk = (c & 63) >> 3;
+    return uint32_t(box * kNBox + r * 128 + ((chunk ^ (r & 7)) << 4) + (c & 7) * 2);
+}
+
+// Producer loop shared by the K (+Q) and V warps: walks this CTA's items and
+// tiles, resolves pages lane-parallel (32 row boxes at a time) and lets lane
+// 0 issue the boxes of each tile into the ring.
+template <bool kIsK>
+__device__ __forceinline__ void produce(const GqaParams &p, const int *cum, int num_items, int hkv,
+                                        uint8_t *smem, uint64_t *bar, int lane) {
+    const CUtensorMap *map = kIsK ? &p.k_map : &p.v_map;
+    uint64_t *full = bar + (kIsK ? kKFull : kVFull);
+    uint64_t *empty = bar + (kIsK ? kKEmpty : kVEmpty);
+    uint8_t *ring = smem + (kIsK ? Smem::kring : Smem::vring);
+    if (lane == 0) {
+        prefetch_tensormap(map);
+        if (kIsK) prefetch_tensormap(&p.q_map);
+    }
+    const int G = p.group;
+    const int box_rows = p.box_rows;        // 128, 64, 32, 16 or 8
+    const int nb = kBK / box_rows;          // row boxes per tile
+    const uint32_t box_bytes = uint32_t(box_rows) * 128u;
+    int g = 0, itq = 0;
+    bool aborted = false;
+    for (int j = blockIdx.x; j < num_items && !aborted; j += gridDim.x) {
+        const GqaItem it = gqa_item<kBK>(p, cum, j, hkv);
+        if (it.ntiles == 0) continue;
+        if (kIsK && lane == 0) {
+            const int qb = itq & 1;
+            if (itq >= 2 && !mbar_wait(&bar[kQEmpty + qb], ((itq >> 1) - 1) & 1, p.err)) {
+                aborted = true;
+            } else {
+                mbar_arrive_expect_tx(&bar[kQFull + qb], 2u * uint32_t(G) * 128u);
+                uint8_t *qs = smem + Smem::q + qb * kNBytes;
+                for (int cb = 0; cb < 2; ++cb)
+                    tma_load_2d(qs + cb * kNBox, &p.q_map, &bar[kQFull + qb], cb * 64,
+                                it.b * p.num_q_heads + it.kvh * G);
+            }
+        }
+        aborted = __shfl_sync(0xffffffffu, aborted, 0);
+        int cached = -1, my_page = -1, my_slot = 0;
+        for (int t = 0; t < it.ntiles && !aborted; ++t) {
+            const int gg = g + t;
+            const int s = gg % kStages;
+            const int key0 = it.start + t * kBK;
+            const int live = min(nb, (it.L - key0 + box_rows - 1) / box_rows);
+            if (lane == 0) {
+                if (gg >= kStages && !mbar_wait(&empty[s], ((gg / kStages) - 1) & 1, p.err))
+                    aborted = true;
+                else
+                    mbar_arrive_expect_tx(&full[s], uint32_t(live) * 2u * box_bytes);
+            }
+            aborted = __shfl_sync(0xffffffffu, aborted, 0);
+            if (aborted) break;
+            uint8_t *dst = ring + s * kTileBytes;
+            for (int r = 0; r < live; ++r) {
+                const int gb = (key0 - it.start) / box_rows + r;   // box index in the item
+                if ((gb >> 5) != cached) {                          // warp-uniform refill
+                    cached = gb >> 5;
+                    const int tk = it.start + ((cached << 5) + lane) * box_rows;
+                    my_page = -1;
+                    my_slot = 0;
+                    if (tk < it.L) {
+                        if (p.page_table) {
+                            const int pidx = tk / p.page_size;
+                            int e = pidx < p.max_pages
+                                        ? p.page_table[size_t(it.b) * p.max_pages + pidx] : -1;
+                            if (e < 0 || e >= p.num_pages) {
+                                if (kIsK) atomicOr(p.err, kErrBadPage);
+                                e = -1;
+                            }
+                            my_page = e;
+                            my_slot = tk % p.page_size;
+                        } else {
+                            my_page = it.b;
+                            my_slot = tk;
+                        }
+                    }
+                }
+                const int page = __shfl_sync(0xffffffffu, my_page, gb & 31);
+                const int slot = __shfl_sync(0xffffffffu, my_slot, gb & 31);
+                if (lane == 0) {
+                    if (page < 0) {
+                        mbar_complete_tx(&full[s], 2u * box_bytes);   // skipped bad page
+                    } else {
+#pragma unroll
+                        for (int cb = 0; cb < 2; ++cb)
+                            tma_load_4d(dst + cb * kBox + r * box_rows * 128, map, &full[s],
+                                        cb * 64, slot, it.kvh, page);
+                    }
+                }
+            }
+        }
+        g += it.ntiles;
+        ++itq;
+    }
+    // Every copy this warp issued must land before the CTA may leave.
+    if (lane == 0) {
+        for (int i = max(0, g - kStages); i < g; ++i)
+            mbar_wait(&full[i % kStages], (i / kStages) & 1, p.err);
+        if (kIsK)
+            for (int i = max(0, itq - 2); i < itq; ++i)
+                mbar_wait(&bar[kQFull + (i & 1)], (i >> 1) & 1, p.err);
+    }
+}
+
+template <int G>
+__global__ void __launch_bounds__(kThreads, 1)
+gqa_decode_tc_kernel(const __grid_constant__ GqaParams p) {
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t *smem = reinterpret_cast<uint8_t *>(
+        (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    uint64_t *bar = reinterpret_cast<uint64_t *>(smem + Smem::bars);
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + Smem::bars + kNumBars * 8);
+    int *cum = reinterpret_cast<int *>(smem + Smem::items);
+
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+    const int hkv = p.num_q_heads / G;
+
+    if (warp == 0) gqa_build_items(p, hkv, cum, lane);
+    if (threadIdx.x == 32) {
+        for (int i = 0; i < kNumBars; ++i) {
+            const bool per_warp = (i == kSFree || i == kSFree + 1 || i == kPFull);
+            mbar_init(&bar[i], per_warp ? 4u : 1u);
+        }
+        fence_mbar_init();
+    }
+    if (warp == 6) {
+        tc::tmem_alloc(tmem_slot, kTmemCols);
+        tc::tmem_relinquish();
+    }
+    // Padding rows of the Q^T and P^T operands (heads G..15) stay zero.
+    for (int i = threadIdx.x; i < (3 * kNBytes) / 16; i += kThreads)
+        reinterpret_cast<uint4 *>(smem + Smem::q)[i] = make_uint4(0u, 0u, 0u, 0u);
+    tc::fence_async_smem();
+    tc::fence_before_sync();
+    __syncthreads();
+    tc::fence_after_sync();
+    const uint32_t tmem = *tmem_slot;
+    const int num_items = cum[p.batch];
+
+    if (warp == 4) {
+        produce<true>(p, cum, num_items, hkv, smem, bar, lane);
+    } else if (warp == 5) {
+        produce<false>(p, cum, num_items, hkv, smem, bar, lane);
+    } else if (warp == 6) {
+        // ---------------------------------------------------------- MMA issue
+        if (lane == 0) {
+            constexpr uint32_t idesc_s = tc::idesc_bf16_f32(128, kNRows, 0, 0);
+            constexpr uint32_t idesc_o = tc::idesc_bf16_f32(128, kNRows, 1, 0);
+            const uint32_t k_base = smem_addr(smem + Smem::kring);
+            const uint32_t v_base = smem_addr(smem + Smem::vring);
+            const uint32_t q_base = smem_addr(smem + Smem::q);
+            const uint32_t p_base = smem_addr(smem + Smem::p);
+            int g = 0, itq = 0;
+            bool ok = true;
+            for (int j = blockIdx.x; ok && j < num_items; j += gridDim.x) {
+                const GqaItem it = gqa_item<kBK>(p, cum, j, hkv);
+                if (it.ntiles == 0) continue;
+                const int qb = itq & 1;
+                ok = mbar_wait(&bar[kQFull + qb], (itq >> 1) & 1, p.err);
+                for (int t = 0; ok && t <= it.ntiles; ++t) {
+                    if (t < it.ntiles) {
+                        const int gg = g + t;
+                        const int ks = gg % kStages;
+                        const int sb = gg & 1;
+                        ok = mbar_wait(&bar[kKFull + ks], (gg / kStages) & 1, p.err);
+                        if (ok && gg >= 2)
+                            ok = mbar_wait(&bar[kSFree + sb], ((gg >> 1) - 1) & 1, p.err);
+                        if (!ok) break;
+                        tc::fence_after_sync();
+                        const uint32_t kst = k_base + ks * kTileBytes;
+                        const uint32_t qst = q_base + qb * kNBytes;
+#pragma unroll
+                        for (int kk = 0; kk < kD / 16; ++kk) {
+                            const uint32_t ka = kst + (kk >> 2) * kBox + (kk & 3) * 32;
+                            const uint32_t qa = qst + (kk >> 2) * kNBox + (kk & 3) * 32;
+                            tc::mma_bf16(tmem + kTmemS + sb * kNRows,
+                                         tc::smem_desc_sw128(ka, 16, 1024),
+                                         tc::smem_desc_sw128(qa, 16, 1024), idesc_s, kk > 0);
+                        }
+                        tc::mma_commit(&bar[kSFull + sb]);
+                        tc::mma_commit(&bar[kKEmpty + ks]);
+                    }
+                    if (t >= 1) {
+                        const int gp = g + t - 1;
+                        const int vs = gp % kStages;
+                        ok = mbar_wait(&bar[kPFull], gp & 1, p.err);
+                        if (ok) ok = mbar_wait(&bar[kVFull + vs], (gp / kStages) & 1, p.err);
+                        if (!ok) break;
+                        tc::fence_after_sync();
+                        const uint32_t vst = v_base + vs * kTileBytes;
+#pragma unroll
+                        for (int kk = 0; kk < kBK / 16; ++kk) {
+                            const uint32_t pa = p_base + (kk >> 2) * kNBox + (kk & 3) * 32;
+                            // V^T as the MN-major A operand: channel blocks of 64
+                            // are the two 16 KB column boxes, 8-key groups 1 KB apart.
+                            tc::mma_bf16(tmem + kTmemO,
+                                         tc::smem_desc_sw128(vst + kk * 16 * 128, kBox, 1024),
+                                         tc::smem_desc_sw128(pa, 16, 1024), idesc_o,
+                                         t > 1 || kk > 0);
+                        }
+                        tc::mma_commit(&bar[kODone]);
+                        tc::mma_commit(&bar[kVEmpty + vs]);
+                    }
+                }
+                tc::mma_commit(&bar[kQEmpty + qb]);
+                g += it.ntiles;
+                ++itq;
+            }
+        }
+    } else {
+        // ---------------------------------------------------- softmax + epilogue
+        const int k = warp * 32 + lane;              // key of the tile == TMEM lane
+        const uint32_t lane_base = uint32_t(warp * 32) << 16;
+        float *red = reinterpret_cast<float *>(smem + Smem::red);     // [2][4][16]
+        float *lred = reinterpret_cast<float *>(smem + Smem::lred);   // [2][4][16]
+        uint8_t *pbuf = smem + Smem::p;
+        int g = 0;
+        bool ok = true;
+        for (int j = blockIdx.x; j < num_items; j += gridDim.x) {
+            const GqaItem it = gqa_item<kBK>(p, cum, j, hkv);
+            float m[G], l[G], lr[G];
+#pragma unroll
+            for (int h = 0; h < G; ++h) {
+                m[h] = -INFINITY;
+                l[h] = 0.f;
+                lr[h] = 0.f;
+            }
+            // Every warp runs every named barrier of every tile, even after a
+            // wait gave up (ok == false), so no warp can strand the others.
+            for (int t = 0; t < it.ntiles; ++t) {
+                const int gg = g + t;
+                const int sb = gg & 1;
+                const int t0 = it.start + t * kBK;
+                const int nvalid = min(kBK, it.end - t0);
+                ok = ok && mbar_wait(&bar[kSFull + sb], (gg >> 1) & 1, p.err);
+                tc::fence_after_sync();
+                float s[G];
+                tc::tmem_ld_n<G>(tmem + lane_base + kTmemS + sb * kNRows, s);
+                tc::fence_before_sync();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&bar[kSFree + sb]);
+
+                // ---- tile max per head across the four warps -----------------
+                const bool valid = k < nvalid;
+                float *rb = red + (gg & 1) * 64;
+#pragma unroll
+                for (int h = 0; h < G; ++h) {
+                    s[h] = valid ? s[h] * p.qk_scale_log2 : -INFINITY;
+                    const float wm = warp_max(s[h]);
+                    if (lane == 0) rb[warp * 16 + h] = wm;
+                }
+                named_sync(1, 128);
+                float alpha[G];
+                bool moved = false;
+#pragma unroll
+                for (int h = 0; h < G; ++h) {
+                    const float tmax = fmaxf(fmaxf(rb[h], rb[16 + h]), fmaxf(rb[32 + h], rb[48 + h]));
+                    const float mn = fmaxf(m[h], tmax);   // finite: key 0 of the tile is valid
+                    alpha[h] = fast_exp2(m[h] - mn);      // 0 on the first tile
+                    moved |= mn != m[h];
+                    m[h] = mn;
+                }
+                uint16_t pb[G];
+#pragma unroll
+                for (int h = 0; h < G; ++h) {
+                    const float pv = valid ? fast_exp2(s[h] - m[h]) : 0.f;
+                    const uint32_t packed = pack_bf16x2(pv, 0.f);
+                    pb[h] = static_cast<uint16_t>(packed & 0xffffu);
+                    l[h] = l[h] * alpha[h] + pv;
+                    lr[h] = lr[h] * alpha[h] + bf16_lo(packed);
+                }
+                if (t >= 1) {
+                    // O^T(t-1) is complete: P^T may be overwritten and O^T
+                    // rescaled (thread = channel lane, columns = heads).
+                    ok = ok && mbar_wait(&bar[kODone], (gg - 1) & 1, p.err);
+                    tc::fence_after_sync();
+                    if (moved) {   // identical in every thread
+                        float o[G];
+                        tc::tmem_ld_n<G>(tmem + lane_base + kTmemO, o);
+#pragma unroll
+                        for (int h = 0; h < G; ++h) o[h] *= alpha[h];
+                        tc::tmem_st_n<G>(tmem + lane_base + kTmemO, o);
+                        tc::tmem_wait_st();
+                    }
+                }
+#pragma unroll
+                for (int h = 0; h < G; ++h)
+                    *reinterpret_cast<uint16_t *>(pbuf + n_operand_offset(h, k)) = pb[h];
+                if (t0 + kBK > it.L) {
+                    // Slots past the sequence end may hold anything (even NaN):
+                    // zero them in the V stage before P.V reads it.
+                    const int vs = gg % kStages;
+                    ok = ok && mbar_wait(&bar[kVFull + vs], (gg / kStages) & 1, p.err);
+                    uint8_t *vst = smem + Smem::vring + vs * kTileBytes;
+                    const int first = it.L - t0;               // first invalid key
+                    const int nz = (kBK - first) * 8;          // 16-B chunks per box
+                    for (int i = k; i < 2 * nz; i += 128) {
+                        const int box = i / nz, rem = i - (i / nz) * nz;
+                        *reinterpret_cast<uint4 *>(vst + box * kBox + (first + rem / 8) * 128 +
+                                                   (rem & 7) * 16) = make_uint4(0u, 0u, 0u, 0u);
+                    }
+                }
+                tc::fence_async_smem();
+                tc::fence_before_sync();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&bar[kPFull]);
+            }
+
+            // ---- item epilogue ----------------------------------------------------
+            if (ok && it.ntiles > 0) {
+                ok = mbar_wait(&bar[kODone], (g + it.ntiles - 1) & 1, p.err);
+                tc::fence_after_sync();
+            }
+            float lsum[G], lrsum[G];
+            {
+                float *lb = lred + (j / gridDim.x & 1) * 64;
+#pragma unroll
+                for (int h = 0; h < G; ++h) {
+                    const float a = warp_sum(l[h]);
+                    const float b = warp_sum(lr[h]);
+                    if (lane == 0) {
+                        lb[warp * 16 + h] = a;
+                        lb[warp * 16 + 8 + h] = b;
+                    }
+                }
+                named_sync(1, 128);
+#pragma unroll
+                for (int h = 0; h < G; ++h) {
+                    lsum[h] = (lb[h] + lb[16 + h]) + (lb[32 + h] + lb[48 + h]);
+                    lrsum[h] = (lb[8 + h] + lb[24 + h]) + (lb[40 + h] + lb[56 + h]);
+                }
+            }
+            float o[G];
+            if (ok && it.ntiles > 0) {
+                tc::tmem_ld_n<G>(tmem + lane_base + kTmemO, o);
+            } else {
+#pragma unroll
+                for (int h = 0; h < G; ++h) o[h] = 0.f;
+            }
+            tc::fence_before_sync();
+            const int c = k;   // output channel of this thread
+#pragma unroll
+            for (int h = 0; h < G; ++h) {
+                const int hq = it.kvh * G + h;
+                if (it.direct) {
+                    const float t2 = p.sink ? p.sink[hq] * kLog2e : -INFINITY;
+                    const float Mf = fmaxf(m[h], t2);
+                    float Z = 0.f, Zr = 0.f, so = 0.f;
+                    if (Mf != -INFINITY) {
+                        so = fast_exp2(m[h] - Mf);
+                        const float st = fast_exp2(t2 - Mf);
+                        Z = lsum[h] * so + st;
+                        Zr = lrsum[h] * so + st;
+                    }
+                    const float scale_o = Zr > 0.f ? so / Zr : 0.f;
+                    const uint32_t packed = pack_bf16x2(o[h] * scale_o, 0.f);
+                    p.out[(size_t(it.b) * p.num_q_heads + hq) * kD + c] =
+                        static_cast<uint16_t>(packed & 0xffffu);
+                    if (c == 0 && p.lse)
+                        p.lse[size_t(it.b) * p.num_q_heads + hq] =
+                            Z > 0.f ? (Mf + fast_log2(Z)) * kLn2 : -INFINITY;
+                } else {
+                    const size_t base = (size_t(it.part) * p.batch + it.b) * p.num_q_heads + hq;
+                    const float scale_o = lrsum[h] > 0.f ? lsum[h] / lrsum[h] : 0.f;
+                    p.ws_o[base * kD + c] = o[h] * scale_o;
+                    if (c == 0) {
+                        p.ws_m[base] = m[h] * kLn2;
+                        p.ws_l[base] = lsum[h];
+                    }
+                }
+            }
+            g += it.ntiles;
+        }
+        pdl_launch_dependents();
+    }
+
+    tc::fence_before_sync();
+    __syncthreads();
+    if (warp == 6) {
+        tc::fence_after_sync();
+        tc::tmem_dealloc(tmem, kTmemCols);
+    }
+}
+
+int g_num_sms_tc[64];
+
+template <int G>
+cudaError_t launch_g(const GqaParams &p, cudaStream_t stream) {
+    const size_t smem = tc_smem_bytes(p.batch);
+    auto kern = gqa_decode_tc_kernel<G>;
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         int(smem));
+    if (e != cudaSuccess) return e;
+    int dev = 0;
+    e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+    if (g_num_sms_tc[dev] == 0) {
+        int n = 0;
+        e = cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
+        if (e != cudaSuccess) return e;
+        g_num_sms_tc[dev] = n;
+    }
+    long long grid = g_num_sms_tc[dev];   // one resident CTA per SM
+    const long long max_items = static_cast<long long>(p.batch) * (p.num_q_heads / G) *
+                                p.num_partitions;
+    if (grid > max_items) grid = max_items;
+    if (grid < 1) grid = 1;
+    kern<<<dim3(static_cast<unsigned>(grid)), kThreads, smem, stream>>>(p);
+    return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_gqa_decode_tc(const GqaParams &p, cudaStream_t stream) {
+    if (p.head_dim != kD) return cudaErrorInvalidValue;
+    switch (p.group) {
+        case 1: return launch_g<1>(p, stream);
+        case 2: return launch_g<2>(p, stream);
+        case 4: return launch_g<4>(p, stream);
+        case 8: return launch_g<8>(p, stream);
+        default: return cudaErrorInvalidValue;
+    }
+}
+
+}  // namespace attn

@@ -11,6 +11,9 @@ namespace attn {
 // Keys per pipeline stage and per consumer warp pass in the GQA kernel;
 // partition slices are multiples of it.
 constexpr int kGqaTileKeys = 32;
+// Keys per tile of the tensor-core GQA decode kernel (head_dim 128); its
+// partition slices are multiples of it.
+constexpr int kGqaTcTileKeys = 128;
 // The single-token decode kernel keeps a per-sequence item table in shared
 // memory; batches above this size are rejected.
 constexpr int kGqaMaxBatch = 2048;
@@ -18,6 +21,7 @@ constexpr int kGqaMaxBatch = 2048;
 struct GqaParams {
     CUtensorMap k_map;            // 4-D: (channel, slot, kv head, page)
     CUtensorMap v_map;
+    CUtensorMap q_map;            // 2-D: (channel, row = b * Hq + h); tensor-core kernel only
     const uint16_t *q;            // bf16 [batch][Hq][D]
     const uint32_t *kv_len;       // [batch]
     const int32_t *page_table;    // [batch][max_pages] or nullptr
@@ -94,6 +98,7 @@ struct ReduceParams {
 };
 
 cudaError_t launch_gqa_decode(const GqaParams &p, cudaStream_t stream);
+cudaError_t launch_gqa_decode_tc(const GqaParams &p, cudaStream_t stream);
 cudaError_t launch_mla_decode(const MlaParams &p, cudaStream_t stream);
 cudaError_t launch_tile_attention(const TileParams &p, cudaStream_t stream);
 cudaError_t launch_splitk_reduce(const ReduceParams &p, cudaStream_t stream, bool pdl);

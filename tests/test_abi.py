@@ -142,12 +142,14 @@ def test_planner_formulas(attn):
         align = lambda x: (x + 255) // 256 * 256
         expect = 0 if req == 1 else align(n * 128 * 4) + 2 * align(n * 4)
         assert ws == expect
-    # automatic GQA (two CTAs per SM): fewer units than CTAs -> one wave of
-    # slices; otherwise >= 4 items per CTA at full length and slices of
-    # <= ~1024 keys
+    # automatic GQA (head_dim 128: one CTA per SM; head_dim 64: two): fewer
+    # units than CTAs -> one wave of slices; otherwise >= 4 items per CTA at
+    # full length and slices of <= ~1024 keys
     P, _ = attn.attn_plan_partitions(64, 64, 32, 8, 128, 8192, 0, num_sms=152)
     assert P == 8
     P, _ = attn.attn_plan_partitions(1, 1, 32, 8, 128, 131072, 0, num_sms=152)
+    assert P == 19 and 8 * P == 152
+    P, _ = attn.attn_plan_partitions(1, 1, 16, 8, 64, 131072, 0, num_sms=152)
     assert P == 38 and 8 * P == 2 * 152
     # automatic MLA (one KV head, 512 output channels): one cluster per SM pair
     P, _ = attn.attn_plan_partitions(32, 32, 128, 1, 512, 32768, 0, num_sms=152)
@@ -156,12 +158,10 @@ def test_planner_formulas(attn):
     assert P == 1                                     # one tile of keys cannot split
     P, _ = attn.attn_plan_partitions(4, 4, 32, 8, 128, 0, 0, num_sms=152)
     assert P == 1
-    # more SMs never means fewer partitions
-    prev = 0
+    # every CTA gets at least one slice of a full-length batch
     for sms in (16, 64, 132, 152, 304):
         P, _ = attn.attn_plan_partitions(2, 2, 32, 8, 128, 65536, 0, num_sms=sms)
-        assert P >= prev
-        prev = P
+        assert 2 * 8 * P >= sms
     with pytest.raises(attn.AttnError):
         attn.attn_plan_partitions(2, 2, 30, 8, 128, 100, 0, num_sms=152)
     with pytest.raises(attn.AttnError):
