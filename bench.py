@@ -39,11 +39,23 @@ METRIC = ("decode-attn achieved HBM GB/s (% of GB300 peak) and µs/call, "
           "GQA 32q/8kv d128")
 FALLBACK_HBM_GBS = 6800.0
 PROFILE_TRAFFIC = os.path.join(ROOT, "profiles", "traffic.json")
+_CSRC = "split_flash_decoding_gb300/csrc/"
 KERNEL_SOURCES = {
-    "gqa_decode": ["split_flash_decoding_gb300/csrc/gqa_decode.cu",
-                   "split_flash_decoding_gb300/csrc/ptx.cuh",
-                   "split_flash_decoding_gb300/csrc/launch.h"],
+    "gqa_decode_tc": [_CSRC + f for f in ("gqa_decode_tc.cu", "gqa_items.cuh", "tc.cuh",
+                                          "ptx.cuh", "launch.h")],
+    "gqa_decode": [_CSRC + f for f in ("gqa_decode.cu", "ptx.cuh", "launch.h")],
+    "mla_decode": [_CSRC + f for f in ("mla_decode.cu", "tc.cuh", "ptx.cuh", "launch.h")],
+    "tile_attention": [_CSRC + f for f in ("tile_attention.cu", "tc.cuh", "ptx.cuh",
+                                           "launch.h")],
 }
+
+
+def dominant_kernel(w) -> str:
+    if w.is_mla:
+        return "mla_decode"
+    if w.max_q_len > 1:
+        return "tile_attention"
+    return "gqa_decode_tc" if w.dim_qk == 128 else "gqa_decode"
 
 
 def parse():
@@ -439,8 +451,8 @@ def run_ours(args, rank, world, dist):
     achieved = nbytes / (mean_call_ms * 1e-3) / 1e9
     tflops = flops / (mean_call_ms * 1e-3) / 1e12
     tensor_peak = float(peaks.get("bf16_tflops", 1900.0))
-    kernel_key = "gqa_decode" if not w.is_mla else "mla_decode"
-    traffic = profiled_traffic(kernel_key, w.name) if kernel_key in KERNEL_SOURCES else None
+    kernel_key = dominant_kernel(w)
+    traffic = profiled_traffic(kernel_key, w.name)
     cpu = None
     if not args.no_cpu_baseline:
         # About 10-20 s of host work: a prefix of the batch sized to ~10 s,
@@ -494,7 +506,7 @@ def run_ours(args, rank, world, dist):
         "roofline": {"bound": "hbm", "achieved": round(achieved, 2), "peak": peak,
                      "unit": "GB/s", "frac": round(achieved / peak, 4), "traffic": traffic,
                      "peak_source": f"{peak_kind} hbm_gbs",
-                     "kernel": "attn_decode call (partition kernel + split-K reduce), "
+                     "kernel": f"{kernel_key} + split-K reduce (one attn_decode call), "
                                "CUDA events per call on the launch stream"},
         "cpu_baseline": cpu,
         "tensor": {"achieved_tflops": round(tflops, 2), "peak_tflops": tensor_peak,
