@@ -416,19 +416,7 @@ extern "C" int attn_mla_decode(const void *q, const attn_kv_t *kv, const uint32_
                                 : kMlaTileKeys;
     st = encode_kv_map(&p.kv_map, *kv, dim_qk, 1, p.box_rows);
     if (st) return st;
-    {
-        EncodeTiledFn fn = encode_fn();
-        if (!fn) return ATTN_ERR_CUDA;
-        cuuint64_t gdim[2] = {cuuint64_t(dim_qk), cuuint64_t(batch) * kMlaHeads};
-        cuuint64_t gstride[1] = {cuuint64_t(dim_qk) * 2};
-        cuuint32_t box[2] = {64, 128};
-        cuuint32_t estride[2] = {1, 1};
-        CUresult r = fn(&p.q_map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void *>(q),
-                        gdim, gstride, box, estride, CU_TENSOR_MAP_INTERLEAVE_NONE,
-                        CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-                        CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-        if (r != CUDA_SUCCESS) return ATTN_ERR_UNSUPPORTED;
-    }
+    p.q = static_cast<const uint16_t *>(q);
     st = error_word(&p.err);
     if (st) return st;
     p.kv_len = kv_len;

@@ -48,7 +48,7 @@ constexpr int kMlaDimV = 512;
 
 struct MlaParams {
     CUtensorMap kv_map;           // 4-D: (channel 576, slot, head 1, page)
-    CUtensorMap q_map;            // 2-D: (channel 576, row = b * 128 + h)
+    const uint16_t *q;            // bf16 [batch][128][576]
     const uint32_t *kv_len;       // [batch]
     const int32_t *page_table;    // [batch][max_pages] or nullptr
     const float *sink;            // [128] or nullptr

@@ -19,12 +19,19 @@
 // identical full S), run the same online softmax, and each accumulates its
 // half of the output, O_r += P V[:, 256 r : 256 r + 256], in TMEM.
 //
-// Warp roles (192 threads per CTA):
-//   warps 0-3  softmax: thread h owns head row h (its TMEM lane)
-//   warp 4     TMA producer (Q once, then K tiles into a 2-stage ring)
+// Warp roles (224 threads per CTA):
+//   warps 0-3  softmax: thread h owns head row h (its TMEM lane); they also
+//              copy the CTA's Q channels into TMEM at the start
+//   warp 4     TMA producer (K tiles into a 3-stage ring)
 //   warp 5     TMEM allocation and MMA issue (one thread)
+//   warp 6     score exchange: one bulk copy (cp.async.bulk, shared::cta to
+//              the peer's shared::cluster, complete-tx on the peer's barrier)
+//              moves the CTA's 32 KB of partial scores per tile
 //
-// TMEM columns: S double buffer [0, 128), O half [256, 512).
+// Q is the A operand of the score MMA straight from TMEM, so shared memory
+// holds only the K ring, P and the exchange buffer, and the score MMA reads
+// only K from shared memory.  TMEM columns: Q [0, 160) (bf16 pairs), S
+// [192, 256), O half [256, 512).
 // The running max is kept lazily: P = exp2(s - m_ref) with m_ref raised (and
 // O rescaled) only when a tile's max exceeds m_ref by more than 8 (base 2),
 // so P <= 256 and O/l stay finite in fp32.
@@ -36,14 +43,15 @@ namespace attn {
 namespace {
 
 constexpr int kBN = kMlaTileKeys;          // 64 keys per tile
-constexpr int kStages = 2;
+constexpr int kStages = 3;
 constexpr int kMaxBoxes = 5;               // 64-channel boxes per rank (4 or 5)
-constexpr int kQBoxBytes = 128 * 128;      // 128 rows x 128 B
 constexpr int kKBoxBytes = kBN * 128;      // 64 rows x 128 B
 constexpr int kStageBytes = kMaxBoxes * kKBoxBytes;
-constexpr int kThreads = 192;
+constexpr int kThreads = 224;
+constexpr uint32_t kXBytes = 128u * kMlaTileKeys * 4u;   // one tile of fp32 partial scores
 constexpr uint32_t kTmemCols = 512;
-constexpr uint32_t kTmemS = 0;             // two 64-column S buffers
+constexpr uint32_t kTmemQ = 0;             // up to 160 columns of packed bf16 pairs
+constexpr uint32_t kTmemS = 192;           // 64-column S buffer
 constexpr uint32_t kTmemO = 256;           // 256-column O half
 constexpr float kRescaleThreshold = 8.0f;  // base-2 units
 
@@ -52,26 +60,28 @@ constexpr uint32_t kVLbo = kKBoxBytes;     // stride between 64-channel blocks
 constexpr uint32_t kVSbo = 1024;           // stride between 8-key groups
 
 struct Smem {
-    static constexpr int q = 0;
-    static constexpr int kv = q + kMaxBoxes * kQBoxBytes;            // 80 KB
-    static constexpr int p = kv + kStages * kStageBytes;              // +80 KB
-    static constexpr int x = p + 128 * 128;                           // +16 KB
-    static constexpr int bars = x + 128 * kBN * 4;                    // +32 KB
+    static constexpr int kv = 0;
+    static constexpr int p = kv + kStages * kStageBytes;              // 160 KB
+    static constexpr int x_in = p + 128 * 128;                        // +16 KB (peer's partial)
+    static constexpr int x_out = x_in + 128 * kBN * 4;                // +32 KB (own partial)
+    static constexpr int bars = x_out + 128 * kBN * 4;                // +32 KB
     static constexpr int total = bars + 256;
 };
 constexpr size_t kSmemBytes = Smem::total + 1024;
 
 enum Bar {
-    kKvFull = 0,                // [2]
-    kKvEmpty = 2,               // [2]
-    kQFull = 4,
-    kSFull = 5,                 // [2]
-    kSFree = 7,                 // [2]
-    kPFull = 9,
-    kODone = 10,
-    kXFull = 11,
-    kXFree = 12,
-    kNumBars = 13
+    kKvFull = 0,                // [kStages]
+    kKvEmpty = kStages,         // [kStages]
+    kQFull = 2 * kStages,
+    kSFull,
+    kSFree,
+    kPFull,
+    kODone,
+    kXFull,       // peer's partial landed in x_in (own expect_tx + peer's copy bytes)
+    kXPeerFree,   // the peer has read its x_in (remote arrivals from its 4 softmax warps)
+    kXoReady,     // own 4 softmax warps wrote x_out
+    kXoFree,      // the bulk copy finished reading x_out
+    kNumBars
 };
 
 __device__ __forceinline__ uint32_t p_swz(int row, int chunk) {
@@ -108,19 +118,19 @@ mla_decode_kernel(const __grid_constant__ MlaParams p) {
     const int ntiles = start < end ? (end - start + kBN - 1) / kBN : 0;
 
     if (threadIdx.x == 0) {
-        mbar_init(&bar[kKvFull + 0], 1);
-        mbar_init(&bar[kKvFull + 1], 1);
-        mbar_init(&bar[kKvEmpty + 0], 1);
-        mbar_init(&bar[kKvEmpty + 1], 1);
-        mbar_init(&bar[kQFull], 1);
-        mbar_init(&bar[kSFull + 0], 1);
-        mbar_init(&bar[kSFull + 1], 1);
-        mbar_init(&bar[kSFree + 0], 4);
-        mbar_init(&bar[kSFree + 1], 4);
+        for (int i = 0; i < kStages; ++i) {
+            mbar_init(&bar[kKvFull + i], 1);
+            mbar_init(&bar[kKvEmpty + i], 1);
+        }
+        mbar_init(&bar[kQFull], 4);   // the four softmax warps, after Q is in TMEM
+        mbar_init(&bar[kSFull], 1);
+        mbar_init(&bar[kSFree], 4);
         mbar_init(&bar[kPFull], 4);
         mbar_init(&bar[kODone], 1);
-        mbar_init(&bar[kXFull], 1);   // own expect_tx arrival + the peer's st.async bytes
-        mbar_init(&bar[kXFree], 4);
+        mbar_init(&bar[kXFull], 1);
+        mbar_init(&bar[kXPeerFree], 4);
+        mbar_init(&bar[kXoReady], 4);
+        mbar_init(&bar[kXoFree], 1);
         fence_mbar_init();
     }
     if (warp == 5) {
@@ -136,14 +146,7 @@ mla_decode_kernel(const __grid_constant__ MlaParams p) {
     if (warp == 4) {
         // ------------------------------------------------------------ producer
         if (ntiles > 0) {
-            if (lane == 0) {
-                prefetch_tensormap(&p.kv_map);
-                prefetch_tensormap(&p.q_map);
-                mbar_arrive_expect_tx(&bar[kQFull], uint32_t(nbox) * kQBoxBytes);
-                for (int cb = 0; cb < nbox; ++cb)
-                    tma_load_2d(smem + Smem::q + cb * kQBoxBytes, &p.q_map, &bar[kQFull],
-                                col0 + cb * 64, b * kMlaHeads);
-            }
+            if (lane == 0) prefetch_tensormap(&p.kv_map);
             const int box_rows = p.box_rows;
             const int boxes_per_tile = kBN / box_rows;   // 1..8
             bool aborted = false;
@@ -213,7 +216,6 @@ mla_decode_kernel(const __grid_constant__ MlaParams p) {
             }
             // every copy this warp issued must land before the CTA may leave
             if (lane == 0) {
-                mbar_wait(&bar[kQFull], 0, p.err);
                 for (int i = max(0, issued - kStages); i < issued; ++i)
                     mbar_wait(&bar[kKvFull + i % kStages], (i / kStages) & 1, p.err);
             }
@@ -223,29 +225,26 @@ mla_decode_kernel(const __grid_constant__ MlaParams p) {
         if (ntiles > 0 && lane == 0) {
             constexpr uint32_t idesc_s = tc::idesc_bf16_f32(128, kBN, 0, 0);
             constexpr uint32_t idesc_o = tc::idesc_bf16_f32(128, 256, 0, 1);
-            const uint32_t q_base = smem_addr(smem + Smem::q);
             const uint32_t kv_base = smem_addr(smem + Smem::kv);
             const uint32_t p_base = smem_addr(smem + Smem::p);
             bool ok = mbar_wait(&bar[kQFull], 0, p.err);
             for (int t = 0; ok && t <= ntiles; ++t) {
                 if (t < ntiles) {
                     const int s = t % kStages;
-                    const int sb = t & 1;
                     ok = mbar_wait(&bar[kKvFull + s], (t / kStages) & 1, p.err);
-                    if (ok && t >= 2) ok = mbar_wait(&bar[kSFree + sb], ((t >> 1) - 1) & 1, p.err);
+                    if (ok && t >= 1) ok = mbar_wait(&bar[kSFree], (t - 1) & 1, p.err);
                     if (!ok) break;
                     tc::fence_after_sync();
                     const uint32_t st = kv_base + s * kStageBytes;
                     const int ksteps = nbox * 4;
                     for (int ks = 0; ks < ksteps; ++ks) {
-                        const uint32_t off = (ks >> 2) * 0 + (ks & 3) * 32;
-                        const uint64_t a = tc::smem_desc_sw128(
-                            q_base + (ks >> 2) * kQBoxBytes + off, 16, 1024);
                         const uint64_t bd = tc::smem_desc_sw128(
-                            st + (ks >> 2) * kKBoxBytes + off, 16, 1024);
-                        tc::mma_bf16(tmem + kTmemS + sb * kBN, a, bd, idesc_s, ks > 0);
+                            st + (ks >> 2) * kKBoxBytes + (ks & 3) * 32, 16, 1024);
+                        // A = Q from TMEM: 16 channels = 8 columns of bf16 pairs per step
+                        tc::mma_bf16_tmem_a(tmem + kTmemS, tmem + kTmemQ + ks * 8, bd, idesc_s,
+                                            ks > 0);
                     }
-                    tc::mma_commit(&bar[kSFull + sb]);
+                    tc::mma_commit(&bar[kSFull]);
                 }
                 if (t >= 1) {
                     const int tp = t - 1;
@@ -263,65 +262,102 @@ mla_decode_kernel(const __grid_constant__ MlaParams p) {
                 }
             }
         }
+    } else if (warp == 6) {
+        // ------------------------------------------------------------ exchange
+        if (ntiles > 0 && lane == 0) {
+            const uint32_t dst = mapa_shared(smem_addr(smem + Smem::x_in), peer);
+            const uint32_t dst_bar = mapa_shared(smem_addr(&bar[kXFull]), peer);
+            const uint32_t src = smem_addr(smem + Smem::x_out);
+            for (int t = 0; t < ntiles; ++t) {
+                if (!mbar_wait(&bar[kXoReady], t & 1, p.err)) break;
+                if (t >= 1 && !mbar_wait_cluster(&bar[kXPeerFree], (t - 1) & 1, p.err)) break;
+                bulk_copy_to_peer(dst, src, kXBytes, dst_bar);
+                bulk_wait_read();
+                mbar_arrive(&bar[kXoFree]);
+            }
+        }
     } else {
         // ------------------------------------------------------------ softmax
         const int h = warp * 32 + lane;          // head row == TMEM lane
         const uint32_t lane_base = uint32_t(warp * 32) << 16;
-        uint8_t *xbuf = smem + Smem::x;
-        const uint32_t peer_x = mapa_shared(smem_addr(xbuf), peer);
-        const uint32_t peer_xfull = mapa_shared(smem_addr(&bar[kXFull]), peer);
-        const uint32_t peer_xfree = mapa_shared(smem_addr(&bar[kXFree]), peer);
+        uint8_t *x_in = smem + Smem::x_in;
+        uint8_t *x_out = smem + Smem::x_out;
+        const uint32_t peer_xfree = mapa_shared(smem_addr(&bar[kXPeerFree]), peer);
         uint8_t *pbuf = smem + Smem::p;
+        if (ntiles > 0) {
+            // This CTA's Q channels of head row h into TMEM lane h: 64 channels
+            // (32 columns of bf16 pairs) per store.
+            const uint4 *src = reinterpret_cast<const uint4 *>(
+                p.q + (size_t(b) * kMlaHeads + h) * kMlaDimQK + col0);
+            for (int cb = 0; cb < nbox; ++cb) {
+                float v[32];
+#pragma unroll
+                for (int i = 0; i < 8; ++i) {
+                    const uint4 w = src[cb * 8 + i];
+                    v[4 * i] = __uint_as_float(w.x);
+                    v[4 * i + 1] = __uint_as_float(w.y);
+                    v[4 * i + 2] = __uint_as_float(w.z);
+                    v[4 * i + 3] = __uint_as_float(w.w);
+                }
+                tc::tmem_st32(tmem + lane_base + kTmemQ + cb * 32, v);
+            }
+            tc::tmem_wait_st();
+            tc::fence_before_sync();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&bar[kQFull]);
+        }
         float m_ref = -INFINITY;
         float l = 0.f, l_r = 0.f;
         bool ok = true;
         for (int t = 0; t < ntiles; ++t) {
-            const int sb = t & 1;
             const int t0 = start + t * kBN;
             const int nvalid = min(kBN, end - t0);
-            ok = mbar_wait(&bar[kSFull + sb], (t >> 1) & 1, p.err);
+            ok = mbar_wait(&bar[kSFull], t & 1, p.err);
             if (!ok) break;
             tc::fence_after_sync();
             float s[64];
             {
                 float v[32];
-                tc::tmem_ld32(tmem + lane_base + kTmemS + sb * kBN, v);
+                tc::tmem_ld32(tmem + lane_base + kTmemS, v);
 #pragma unroll
                 for (int j = 0; j < 32; ++j) s[j] = v[j];
-                tc::tmem_ld32(tmem + lane_base + kTmemS + sb * kBN + 32, v);
+                tc::tmem_ld32(tmem + lane_base + kTmemS + 32, v);
 #pragma unroll
                 for (int j = 0; j < 32; ++j) s[32 + j] = v[j];
             }
             tc::fence_before_sync();
             __syncwarp();
-            if (lane == 0) mbar_arrive(&bar[kSFree + sb]);
+            if (lane == 0) mbar_arrive(&bar[kSFree]);
 
             // ---- swap partial scores with the peer CTA (skewed 16-B chunks) ----
-            // st.async reports each store's bytes to the peer's x_full
-            // barrier, which expects 128 rows x 256 B per tile.
-            if (h == 0) mbar_arrive_expect_tx(&bar[kXFull], 128u * kBN * 4u);
+            // Own partial to x_out; warp 6 copies it in bulk into the peer's
+            // x_in, whose x_full barrier expects 128 rows x 256 B per tile.
+            if (h == 0) mbar_arrive_expect_tx(&bar[kXFull], kXBytes);
             if (t >= 1) {
-                ok = mbar_wait_cluster(&bar[kXFree], (t - 1) & 1, p.err);
+                ok = mbar_wait(&bar[kXoFree], (t - 1) & 1, p.err);
                 if (!ok) break;
             }
 #pragma unroll
             for (int c = 0; c < 16; ++c) {
                 const int pc = (c + h) & 15;
-                st_async_f4(peer_x + h * 256 + pc * 16, s[4 * c], s[4 * c + 1], s[4 * c + 2],
-                            s[4 * c + 3], peer_xfull);
+                *reinterpret_cast<float4 *>(x_out + h * 256 + pc * 16) =
+                    make_float4(s[4 * c], s[4 * c + 1], s[4 * c + 2], s[4 * c + 3]);
             }
+            tc::fence_async_smem();   // generic writes -> the bulk copy engine
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&bar[kXoReady]);
             ok = mbar_wait_cluster(&bar[kXFull], t & 1, p.err);
             if (!ok) break;
 #pragma unroll
             for (int c = 0; c < 16; ++c) {
                 const int pc = (c + h) & 15;
-                const float4 o = *reinterpret_cast<const float4 *>(xbuf + h * 256 + pc * 16);
+                const float4 o = *reinterpret_cast<const float4 *>(x_in + h * 256 + pc * 16);
                 s[4 * c] += o.x;
                 s[4 * c + 1] += o.y;
                 s[4 * c + 2] += o.z;
                 s[4 * c + 3] += o.w;
             }
-            __syncwarp();   // the warp's reads of x_buf happen before the release
+            __syncwarp();   // the warp's reads of x_in happen before the release
             if (lane == 0) mbar_arrive_cluster(peer_xfree);
 
             // ---- online softmax in base 2, lazy max --------------------------

@@ -187,6 +187,22 @@ __device__ __forceinline__ void st_async_f4(uint32_t addr, float a, float b, flo
         : "memory");
 }
 
+// Bulk copy of `bytes` (multiple of 16) from this CTA's shared memory to a
+// peer CTA's shared memory (cluster address), completing on the peer's
+// mbarrier; then wait until the source has been read.
+__device__ __forceinline__ void bulk_copy_to_peer(uint32_t dst, uint32_t src, uint32_t bytes,
+                                                  uint32_t dst_mbar) {
+    asm volatile(
+        "cp.async.bulk.shared::cluster.shared::cta.mbarrier::complete_tx::bytes [%0], [%1], %2, "
+        "[%3];\n\t"
+        "cp.async.bulk.commit_group;" ::"r"(dst),
+        "r"(src), "r"(bytes), "r"(dst_mbar)
+        : "memory");
+}
+__device__ __forceinline__ void bulk_wait_read() {
+    asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
+}
+
 // Arrive (release at cluster scope) on an mbarrier given by its cluster address.
 __device__ __forceinline__ void mbar_arrive_cluster(uint32_t cluster_addr) {
     asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(
