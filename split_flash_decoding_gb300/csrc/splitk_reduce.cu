@@ -2,61 +2,41 @@
 // (mha_splitk_reduce / mla_splitk_reduce, mha_decoding_single_batch_pipelined
 // summary and flare_mla_decoding_dispatch summary).
 //
-// One CTA of 256 threads per (row, head).  For partials (O_p unnormalised,
+// Two shapes: for many (row, head) items, one warp per item (eight per CTA);
+// for few items (a long-context batch of one), one CTA of eight warps per
+// item with the partitions split across the warps.  For partials (O_p unnormalised,
 // m_p natural-log max, l_p exp-sum relative to m_p) and an optional sink
 // logit t:
 //   M = max(max_p m_p, t), w_p = exp(m_p - M), Z = sum_p w_p l_p + exp(t - M),
 //   out = sum_p w_p O_p / Z,  lse = M + ln Z.
-// The weights are computed once into shared memory; then thread t owns
-// channel vector t % V (V = dv / 4 vectors, at most 256) of the partitions
-// congruent to t / V, and the 256 / V partial sums are added in shared
-// memory.  Partitions with m_p = -inf (empty slices) get weight 0 and their
-// O_p is never read.
+// Lanes read the partition statistics in parallel, the weights go to the
+// warp's slice of shared memory, and then each lane accumulates 4 channels
+// per 128-channel stripe over all partitions with independent, unrolled
+// loads.  Partitions with m_p = -inf (empty slices) get weight 0 and their
+// O_p is never read.  The kernel is latency-bound (a few dependent rounds of
+// global loads), so it issues everything it can at once.
 #include "launch.h"
 #include "ptx.cuh"
 
 namespace attn {
 namespace {
 
-constexpr int kThreads = 256;
-constexpr int kWarps = kThreads / 32;
+constexpr int kWarps = 8;
 constexpr int kMaxP = 1024;   // ATTN_MAX_PARTITIONS
 
-__device__ __forceinline__ float block_max(float v, float *red) {
-    v = warp_max(v);
-    if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = v;
-    __syncthreads();
-    v = red[0];
-#pragma unroll
-    for (int i = 1; i < kWarps; ++i) v = fmaxf(v, red[i]);
-    __syncthreads();
-    return v;
-}
-
-__device__ __forceinline__ float block_sum(float v, float *red) {
-    v = warp_sum(v);
-    if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = v;
-    __syncthreads();
-    v = red[0];
-#pragma unroll
-    for (int i = 1; i < kWarps; ++i) v += red[i];
-    __syncthreads();
-    return v;
-}
-
-__global__ void __launch_bounds__(kThreads)
+__global__ void __launch_bounds__(kWarps * 32)
 splitk_reduce_kernel(const __grid_constant__ ReduceParams p) {
     // With programmatic dependent launch this grid may start while the
     // partition kernel is still running: wait for its writes first.
     pdl_wait_primary();
 
-    __shared__ float w_s[kMaxP];
-    __shared__ float red[kWarps];
-    __shared__ float4 part[kThreads];
-
-    const int row = blockIdx.x / p.num_q_heads;
-    const int h = blockIdx.x - row * p.num_q_heads;
-    const int tid = threadIdx.x;
+    __shared__ float w_s[kWarps][kMaxP / 4];   // weights, up to 256 partitions per warp
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+    const long long item = static_cast<long long>(blockIdx.x) * kWarps + warp;
+    if (item >= static_cast<long long>(p.rows) * p.num_q_heads) return;
+    const int row = static_cast<int>(item / p.num_q_heads);
+    const int h = static_cast<int>(item - static_cast<long long>(row) * p.num_q_heads);
 
     int P = p.num_partitions;
     if (p.kv_len) {
@@ -64,20 +44,99 @@ splitk_reduce_kernel(const __grid_constant__ ReduceParams p) {
         const uint32_t cap = uint32_t(p.num_partitions) * uint32_t(p.chunk);
         const uint32_t L = min(p.kv_len[row], cap);
         const int ns = static_cast<int>((L + p.chunk - 1) / p.chunk);
-        if (ns < 2) return;  // uniform over the CTA
+        if (ns < 2) return;  // uniform over the warp
         P = ns;
     }
     const size_t stride_p = static_cast<size_t>(p.rows) * p.num_q_heads;  // per partition
     const size_t idx0 = static_cast<size_t>(row) * p.num_q_heads + h;
 
     float mloc = -INFINITY;
-    for (int q = tid; q < P; q += kThreads) mloc = fmaxf(mloc, p.ws_m[q * stride_p + idx0]);
-    const float M = block_max(mloc, red);
+    for (int q = lane; q < P; q += 32) mloc = fmaxf(mloc, p.ws_m[q * stride_p + idx0]);
+    const float M = warp_max(mloc);
+    const float t = p.sink ? p.sink[h] : -INFINITY;
+    const float Mf = fmaxf(M, t);
+
+    // Weights: kept in shared memory when P fits the warp's slice, otherwise
+    // recomputed in the channel loop.
+    const bool cached = P <= kMaxP / 4;
+    float zloc = 0.f;
+    for (int q = lane; q < P; q += 32) {
+        const float m = p.ws_m[q * stride_p + idx0];
+        float w = 0.f;
+        if (m != -INFINITY) {
+            w = fast_exp2((m - Mf) * kLog2e);
+            zloc += w * p.ws_l[q * stride_p + idx0];
+        }
+        if (cached) w_s[warp][q] = w;
+    }
+    __syncwarp();
+    float Z = warp_sum(zloc);
+    if (Mf != -INFINITY) Z += fast_exp2((t - Mf) * kLog2e);
+    const float inv = Z > 0.f ? 1.f / Z : 0.f;
+
+    for (int c = lane * 4; c < p.dim_v; c += 128) {
+        float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+        const float *src = p.ws_o + idx0 * p.dim_v + c;
+#pragma unroll 8
+        for (int q = 0; q < P; ++q) {
+            float w;
+            if (cached) {
+                w = w_s[warp][q];
+            } else {
+                const float m = p.ws_m[q * stride_p + idx0];
+                w = m == -INFINITY ? 0.f : fast_exp2((m - Mf) * kLog2e);
+            }
+            if (w == 0.f) continue;
+            const float4 o = *reinterpret_cast<const float4 *>(src + q * stride_p * p.dim_v);
+            acc.x += w * o.x; acc.y += w * o.y; acc.z += w * o.z; acc.w += w * o.w;
+        }
+        uint2 packed;
+        packed.x = pack_bf16x2(acc.x * inv, acc.y * inv);
+        packed.y = pack_bf16x2(acc.z * inv, acc.w * inv);
+        *reinterpret_cast<uint2 *>(p.out + idx0 * p.dim_v + c) = packed;
+    }
+    if (lane == 0 && p.lse) p.lse[idx0] = Z > 0.f ? Mf + fast_log2(Z) * kLn2 : -INFINITY;
+}
+
+// Few items: CTA per (row, head); warp w takes partitions q = w, w + 8, ...
+__global__ void __launch_bounds__(kWarps * 32)
+splitk_reduce_wide_kernel(const __grid_constant__ ReduceParams p) {
+    pdl_wait_primary();
+
+    __shared__ float w_s[kMaxP];
+    __shared__ float red[kWarps];
+    __shared__ float4 part[kWarps][32];
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+    const int tid = threadIdx.x;
+    const int row = blockIdx.x / p.num_q_heads;
+    const int h = blockIdx.x - row * p.num_q_heads;
+
+    int P = p.num_partitions;
+    if (p.kv_len) {
+        const uint32_t cap = uint32_t(p.num_partitions) * uint32_t(p.chunk);
+        const uint32_t L = min(p.kv_len[row], cap);
+        const int ns = static_cast<int>((L + p.chunk - 1) / p.chunk);
+        if (ns < 2) return;  // uniform over the CTA
+        P = ns;
+    }
+    const size_t stride_p = static_cast<size_t>(p.rows) * p.num_q_heads;
+    const size_t idx0 = static_cast<size_t>(row) * p.num_q_heads + h;
+
+    float mloc = -INFINITY;
+    for (int q = tid; q < P; q += kWarps * 32) mloc = fmaxf(mloc, p.ws_m[q * stride_p + idx0]);
+    mloc = warp_max(mloc);
+    if (lane == 0) red[warp] = mloc;
+    __syncthreads();
+    float M = red[0];
+#pragma unroll
+    for (int i = 1; i < kWarps; ++i) M = fmaxf(M, red[i]);
+    __syncthreads();
     const float t = p.sink ? p.sink[h] : -INFINITY;
     const float Mf = fmaxf(M, t);
 
     float zloc = 0.f;
-    for (int q = tid; q < P; q += kThreads) {
+    for (int q = tid; q < P; q += kWarps * 32) {
         const float m = p.ws_m[q * stride_p + idx0];
         float w = 0.f;
         if (m != -INFINITY) {
@@ -86,32 +145,33 @@ splitk_reduce_kernel(const __grid_constant__ ReduceParams p) {
         }
         w_s[q] = w;
     }
-    float Z = block_sum(zloc, red);   // also publishes w_s
+    zloc = warp_sum(zloc);
+    if (lane == 0) red[warp] = zloc;
+    __syncthreads();   // also publishes w_s
+    float Z = 0.f;
+#pragma unroll
+    for (int i = 0; i < kWarps; ++i) Z += red[i];
     if (Mf != -INFINITY) Z += fast_exp2((t - Mf) * kLog2e);
     const float inv = Z > 0.f ? 1.f / Z : 0.f;
 
-    const int V = min(p.dim_v / 4, kThreads);   // channel vectors handled at once
-    const int lanes = kThreads / V;             // partition lanes
-    const int v = tid % V;
-    const int pl = tid / V;
-    for (int c0 = 0; c0 < p.dim_v; c0 += V * 4) {
-        const int c = c0 + v * 4;
+    for (int c0 = 0; c0 < p.dim_v; c0 += 128) {
+        const int c = c0 + lane * 4;
         float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-        if (pl < lanes && c < p.dim_v) {
+        if (c < p.dim_v) {
+            const float *src = p.ws_o + idx0 * p.dim_v + c;
 #pragma unroll 4
-            for (int q = pl; q < P; q += lanes) {
+            for (int q = warp; q < P; q += kWarps) {
                 const float w = w_s[q];
                 if (w == 0.f) continue;
-                const float4 o = *reinterpret_cast<const float4 *>(
-                    p.ws_o + (q * stride_p + idx0) * p.dim_v + c);
+                const float4 o = *reinterpret_cast<const float4 *>(src + q * stride_p * p.dim_v);
                 acc.x += w * o.x; acc.y += w * o.y; acc.z += w * o.z; acc.w += w * o.w;
             }
         }
-        part[tid] = acc;
+        part[warp][lane] = acc;
         __syncthreads();
-        if (pl == 0 && c < p.dim_v) {
-            for (int k = 1; k < lanes; ++k) {
-                const float4 o = part[k * V + v];
+        if (warp == 0 && c < p.dim_v) {
+            for (int k = 1; k < kWarps; ++k) {
+                const float4 o = part[k][lane];
                 acc.x += o.x; acc.y += o.y; acc.z += o.z; acc.w += o.w;
             }
             uint2 packed;
@@ -129,10 +189,14 @@ splitk_reduce_kernel(const __grid_constant__ ReduceParams p) {
 cudaError_t launch_splitk_reduce(const ReduceParams &p, cudaStream_t stream, bool pdl) {
     const long long items = static_cast<long long>(p.rows) * p.num_q_heads;
     if (items == 0) return cudaSuccess;
-    if (p.num_partitions > kMaxP || items > 0x7fffffffLL) return cudaErrorInvalidValue;
+    if (p.num_partitions > kMaxP) return cudaErrorInvalidValue;
+    // Fewer items than about two warps per SM: spread each item over a CTA.
+    const bool wide = items <= 256;
+    const long long blocks = wide ? items : (items + kWarps - 1) / kWarps;
+    if (blocks > 0x7fffffffLL) return cudaErrorInvalidValue;
     cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(static_cast<unsigned>(items));
-    cfg.blockDim = dim3(kThreads);
+    cfg.gridDim = dim3(static_cast<unsigned>(blocks));
+    cfg.blockDim = dim3(kWarps * 32);
     cfg.dynamicSmemBytes = 0;
     cfg.stream = stream;
     cudaLaunchAttribute attr[1];
@@ -140,7 +204,8 @@ cudaError_t launch_splitk_reduce(const ReduceParams &p, cudaStream_t stream, boo
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = pdl ? 1 : 0;
-    return cudaLaunchKernelEx(&cfg, splitk_reduce_kernel, p);
+    return wide ? cudaLaunchKernelEx(&cfg, splitk_reduce_wide_kernel, p)
+                : cudaLaunchKernelEx(&cfg, splitk_reduce_kernel, p);
 }
 
 }  // namespace attn
