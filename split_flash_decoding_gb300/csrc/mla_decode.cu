@@ -19,19 +19,32 @@
 // identical full S), run the same online softmax, and each accumulates its
 // half of the output, O_r += P V[:, 256 r : 256 r + 256], in TMEM.
 //
-// Warp roles (224 threads per CTA):
-//   warps 0-3  softmax: thread h owns head row h (its TMEM lane); they also
-//              copy the CTA's Q channels into TMEM at the start
-//   warp 4     TMA producer (K tiles into a 3-stage ring)
-//   warp 5     TMEM allocation and MMA issue (one thread)
-//   warp 6     score exchange: one bulk copy (cp.async.bulk, shared::cta to
-//              the peer's shared::cluster, complete-tx on the peer's barrier)
-//              moves the CTA's 32 KB of partial scores per tile
+// The partial-score exchange is the critical resource (32 KB each way per
+// tile over the SM-to-SM network), so it is kept busy: the softmax warps
+// work one tile ahead, staging tile t+1's partial scores for the copy
+// before they run the softmax of tile t, which then overlaps the copy of
+// tile t+1.
+//
+// Warp roles (352 threads per CTA):
+//   warps 0-7  softmax: warps w and w+4 share head rows 32(w%4).. (their
+//              TMEM lanes); warp half w/4 owns keys [32 half, 32 half + 32)
+//              of every tile.  Per tile t: read the partial S(t+1) from TMEM
+//              and stage it for the copy, add the peer's partial of S(t),
+//              online softmax (row maxima of the two halves combined through
+//              shared memory), P(t) (bf16 pairs) into TMEM, where the P.V MMA
+//              takes it as the A operand.  They also copy this CTA's Q
+//              channels into TMEM.
+//   warp 8     TMA producer (K tiles into a 4-stage ring)
+//   warp 9     TMEM allocation and MMA issue (one thread), order
+//              S0 S1 S2 O0 S3 O1 ...: the score MMA of tile t+2 is issued
+//              as soon as S(t+1) has been read, ahead of O(t)
+//   warp 10    exchange: one bulk copy per tile (cp.async.bulk, shared::cta
+//              to the peer's shared::cluster, complete-tx on the peer's
+//              barrier) of the staged 32 KB of partial scores
 //
 // Q is the A operand of the score MMA straight from TMEM, so shared memory
-// holds only the K ring, P and the exchange buffer, and the score MMA reads
-// only K from shared memory.  TMEM columns: Q [0, 160) (bf16 pairs), S
-// [192, 256), O half [256, 512).
+// holds only the K ring and the two exchange buffers.  TMEM columns: Q
+// [0, 160) (bf16 pairs), P [160, 192), S [192, 256), O half [256, 512).
 // The running max is kept lazily: P = exp2(s - m_ref) with m_ref raised (and
 // O rescaled) only when a tile's max exceeds m_ref by more than 8 (base 2),
 // so P <= 256 and O/l stay finite in fp32.
@@ -43,14 +56,17 @@ namespace attn {
 namespace {
 
 constexpr int kBN = kMlaTileKeys;          // 64 keys per tile
-constexpr int kStages = 3;
+constexpr int kStages = 4;
 constexpr int kMaxBoxes = 5;               // 64-channel boxes per rank (4 or 5)
 constexpr int kKBoxBytes = kBN * 128;      // 64 rows x 128 B
 constexpr int kStageBytes = kMaxBoxes * kKBoxBytes;
-constexpr int kThreads = 224;
+constexpr int kThreads = 352;
+constexpr int kSoftmaxThreads = 256;   // warps 0-7
+constexpr int kBarSoftmax = 1;         // named barrier of the softmax warps
 constexpr uint32_t kXBytes = 128u * kMlaTileKeys * 4u;   // one tile of fp32 partial scores
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kTmemQ = 0;             // up to 160 columns of packed bf16 pairs
+constexpr uint32_t kTmemP = 160;           // 32 columns: P of one tile as bf16 pairs
 constexpr uint32_t kTmemS = 192;           // 64-column S buffer
 constexpr uint32_t kTmemO = 256;           // 256-column O half
 constexpr float kRescaleThreshold = 8.0f;  // base-2 units
@@ -61,11 +77,11 @@ constexpr uint32_t kVSbo = 1024;           // stride between 8-key groups
 
 struct Smem {
     static constexpr int kv = 0;
-    static constexpr int p = kv + kStages * kStageBytes;              // 160 KB
-    static constexpr int x_in = p + 128 * 128;                        // +16 KB (peer's partial)
-    static constexpr int x_out = x_in + 128 * kBN * 4;                // +32 KB (own partial)
-    static constexpr int bars = x_out + 128 * kBN * 4;                // +32 KB
-    static constexpr int total = bars + 256;
+    static constexpr int x_in = kv + kStages * kStageBytes;           // 160 KB
+    static constexpr int x_out = x_in + int(kXBytes);                 // +32 KB (peer's partial)
+    static constexpr int red = x_out + int(kXBytes);                  // +32 KB (own partial)
+    static constexpr int bars = red + 2 * 128 * 4;                    // +1 KB (row maxima)
+    static constexpr int total = bars + 160;
 };
 constexpr size_t kSmemBytes = Smem::total + 1024;
 
@@ -73,19 +89,21 @@ enum Bar {
     kKvFull = 0,                // [kStages]
     kKvEmpty = kStages,         // [kStages]
     kQFull = 2 * kStages,
-    kSFull,
-    kSFree,
-    kPFull,
-    kODone,
+    kSFull,       // partial S of a tile in TMEM (MMA commit)
+    kSFree,       // the softmax warps have read it (4 arrivals)
+    kPFull,       // P of a tile in TMEM, V tail cleared (4 arrivals)
+    kODone,       // O MMA of a tile finished (commit)
     kXFull,       // peer's partial landed in x_in (own expect_tx + peer's copy bytes)
     kXPeerFree,   // the peer has read its x_in (remote arrivals from its 4 softmax warps)
-    kXoReady,     // own 4 softmax warps wrote x_out
+    kXoReady,     // own 4 softmax warps staged x_out
     kXoFree,      // the bulk copy finished reading x_out
     kNumBars
 };
 
-__device__ __forceinline__ uint32_t p_swz(int row, int chunk) {
-    return uint32_t(row * 128 + ((chunk ^ (row & 7)) << 4));
+// Partial score row h of one tile in an exchange buffer: 16-B chunk c at a
+// row-dependent rotation, so a warp's 32 rows hit different banks.
+__device__ __forceinline__ uint32_t x_off(int h, int c) {
+    return uint32_t(h * 256 + (((c + h) & 15) << 4));
 }
 
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
@@ -122,18 +140,18 @@ mla_decode_kernel(const __grid_constant__ MlaParams p) {
             mbar_init(&bar[kKvFull + i], 1);
             mbar_init(&bar[kKvEmpty + i], 1);
         }
-        mbar_init(&bar[kQFull], 4);   // the four softmax warps, after Q is in TMEM
+        mbar_init(&bar[kQFull], 8);   // the eight softmax warps, after Q is in TMEM
         mbar_init(&bar[kSFull], 1);
-        mbar_init(&bar[kSFree], 4);
-        mbar_init(&bar[kPFull], 4);
+        mbar_init(&bar[kSFree], 8);
+        mbar_init(&bar[kPFull], 8);
         mbar_init(&bar[kODone], 1);
         mbar_init(&bar[kXFull], 1);
-        mbar_init(&bar[kXPeerFree], 4);
-        mbar_init(&bar[kXoReady], 4);
+        mbar_init(&bar[kXPeerFree], 8);
+        mbar_init(&bar[kXoReady], 8);
         mbar_init(&bar[kXoFree], 1);
         fence_mbar_init();
     }
-    if (warp == 5) {
+    if (warp == 9) {
         tc::tmem_alloc(tmem_slot, kTmemCols);
         tc::tmem_relinquish();
     }
@@ -143,7 +161,7 @@ mla_decode_kernel(const __grid_constant__ MlaParams p) {
     tc::fence_after_sync();
     const uint32_t tmem = *tmem_slot;
 
-    if (warp == 4) {
+    if (warp == 8) {
         // ------------------------------------------------------------ producer
         if (ntiles > 0) {
             if (lane == 0) prefetch_tensormap(&p.kv_map);
@@ -220,49 +238,58 @@ mla_decode_kernel(const __grid_constant__ MlaParams p) {
                     mbar_wait(&bar[kKvFull + i % kStages], (i / kStages) & 1, p.err);
             }
         }
-    } else if (warp == 5) {
+    } else if (warp == 9) {
         // ------------------------------------------------------------ MMA issue
         if (ntiles > 0 && lane == 0) {
             constexpr uint32_t idesc_s = tc::idesc_bf16_f32(128, kBN, 0, 0);
             constexpr uint32_t idesc_o = tc::idesc_bf16_f32(128, 256, 0, 1);
             const uint32_t kv_base = smem_addr(smem + Smem::kv);
-            const uint32_t p_base = smem_addr(smem + Smem::p);
+            // S(t) = Q K^T over this CTA's channels.  Descriptors advance by
+            // byte offset / 16 in their start field; the loops are unrolled so
+            // issue is not bound by descriptor arithmetic.
+            auto issue_s = [&](int t) -> bool {
+                const int s = t % kStages;
+                if (!mbar_wait(&bar[kKvFull + s], (t / kStages) & 1, p.err)) return false;
+                if (t >= 1 && !mbar_wait(&bar[kSFree], (t - 1) & 1, p.err)) return false;
+                tc::fence_after_sync();
+                const uint64_t b0 = tc::smem_desc_sw128(kv_base + s * kStageBytes, 16, 1024);
+#pragma unroll
+                for (int ks = 0; ks < 16; ++ks)
+                    // A = Q from TMEM: 16 channels = 8 columns of bf16 pairs per step
+                    tc::mma_bf16_tmem_a(tmem + kTmemS, tmem + kTmemQ + ks * 8,
+                                        b0 + uint64_t(((ks >> 2) * kKBoxBytes + (ks & 3) * 32) >> 4),
+                                        idesc_s, ks > 0);
+                if (nbox == 5) {
+#pragma unroll
+                    for (int ks = 16; ks < 20; ++ks)
+                        tc::mma_bf16_tmem_a(tmem + kTmemS, tmem + kTmemQ + ks * 8,
+                                            b0 + uint64_t((4 * kKBoxBytes + (ks & 3) * 32) >> 4),
+                                            idesc_s, true);
+                }
+                tc::mma_commit(&bar[kSFull]);
+                return true;
+            };
             bool ok = mbar_wait(&bar[kQFull], 0, p.err);
-            for (int t = 0; ok && t <= ntiles; ++t) {
-                if (t < ntiles) {
-                    const int s = t % kStages;
-                    ok = mbar_wait(&bar[kKvFull + s], (t / kStages) & 1, p.err);
-                    if (ok && t >= 1) ok = mbar_wait(&bar[kSFree], (t - 1) & 1, p.err);
-                    if (!ok) break;
-                    tc::fence_after_sync();
-                    const uint32_t st = kv_base + s * kStageBytes;
-                    const int ksteps = nbox * 4;
-                    for (int ks = 0; ks < ksteps; ++ks) {
-                        const uint64_t bd = tc::smem_desc_sw128(
-                            st + (ks >> 2) * kKBoxBytes + (ks & 3) * 32, 16, 1024);
-                        // A = Q from TMEM: 16 channels = 8 columns of bf16 pairs per step
-                        tc::mma_bf16_tmem_a(tmem + kTmemS, tmem + kTmemQ + ks * 8, bd, idesc_s,
-                                            ks > 0);
-                    }
-                    tc::mma_commit(&bar[kSFull]);
-                }
-                if (t >= 1) {
-                    const int tp = t - 1;
-                    ok = mbar_wait(&bar[kPFull], tp & 1, p.err);
-                    if (!ok) break;
-                    tc::fence_after_sync();
-                    const uint32_t st = kv_base + (tp % kStages) * kStageBytes;
-                    for (int kk = 0; kk < kBN / 16; ++kk) {
-                        const uint64_t a = tc::smem_desc_sw128(p_base + kk * 32, 16, 1024);
-                        const uint64_t bd = tc::smem_desc_sw128(st + kk * 16 * 128, kVLbo, kVSbo);
-                        tc::mma_bf16(tmem + kTmemO, a, bd, idesc_o, tp > 0 || kk > 0);
-                    }
-                    tc::mma_commit(&bar[kODone]);
-                    tc::mma_commit(&bar[kKvEmpty + (tp % kStages)]);
-                }
+            if (ok) ok = issue_s(0);
+            if (ok && ntiles > 1) ok = issue_s(1);
+            for (int t = 0; ok && t < ntiles; ++t) {
+                if (t + 2 < ntiles && !(ok = issue_s(t + 2))) break;
+                ok = mbar_wait(&bar[kPFull], t & 1, p.err);
+                if (!ok) break;
+                tc::fence_after_sync();
+                const uint64_t v0 = tc::smem_desc_sw128(kv_base + (t % kStages) * kStageBytes,
+                                                        kVLbo, kVSbo);
+#pragma unroll
+                for (int kk = 0; kk < kBN / 16; ++kk)
+                    // A = P from TMEM: 16 keys = 8 columns of bf16 pairs per step
+                    tc::mma_bf16_tmem_a(tmem + kTmemO, tmem + kTmemP + kk * 8,
+                                        v0 + uint64_t((kk * 16 * 128) >> 4), idesc_o,
+                                        t > 0 || kk > 0);
+                tc::mma_commit(&bar[kODone]);
+                tc::mma_commit(&bar[kKvEmpty + (t % kStages)]);
             }
         }
-    } else if (warp == 6) {
+    } else if (warp == 10) {
         // ------------------------------------------------------------ exchange
         if (ntiles > 0 && lane == 0) {
             const uint32_t dst = mapa_shared(smem_addr(smem + Smem::x_in), peer);
@@ -278,18 +305,24 @@ mla_decode_kernel(const __grid_constant__ MlaParams p) {
         }
     } else {
         // ------------------------------------------------------------ softmax
-        const int h = warp * 32 + lane;          // head row == TMEM lane
-        const uint32_t lane_base = uint32_t(warp * 32) << 16;
+        const int h = (warp & 3) * 32 + lane;    // head row == TMEM lane
+        const int half = warp >> 2;              // keys [32 half, 32 half + 32)
+        const uint32_t lane_base = uint32_t((warp & 3) * 32) << 16;
         uint8_t *x_in = smem + Smem::x_in;
         uint8_t *x_out = smem + Smem::x_out;
+        float *red = reinterpret_cast<float *>(smem + Smem::red);
         const uint32_t peer_xfree = mapa_shared(smem_addr(&bar[kXPeerFree]), peer);
-        uint8_t *pbuf = smem + Smem::p;
-        if (ntiles > 0) {
+        const uint32_t s_col = kTmemS + 32u * half;
+        float m_ref = -INFINITY;
+        float l = 0.f, l_r = 0.f;   // this half's share of the row sums
+        bool ok = ntiles > 0;
+        float s_own[32];
+        if (ok) {
             // This CTA's Q channels of head row h into TMEM lane h: 64 channels
-            // (32 columns of bf16 pairs) per store.
+            // (32 columns of bf16 pairs) per store, boxes split over the halves.
             const uint4 *src = reinterpret_cast<const uint4 *>(
                 p.q + (size_t(b) * kMlaHeads + h) * kMlaDimQK + col0);
-            for (int cb = 0; cb < nbox; ++cb) {
+            for (int cb = half; cb < nbox; cb += 2) {
                 float v[32];
 #pragma unroll
                 for (int i = 0; i < 8; ++i) {
@@ -305,138 +338,187 @@ mla_decode_kernel(const __grid_constant__ MlaParams p) {
             tc::fence_before_sync();
             __syncwarp();
             if (lane == 0) mbar_arrive(&bar[kQFull]);
+
+            // Tile 0's partial: read this half and stage it for the copy.
+            ok = __all_sync(0xffffffffu, mbar_wait(&bar[kSFull], 0, p.err));
+            if (ok) {
+                tc::fence_after_sync();
+                tc::tmem_ld32(tmem + lane_base + s_col, s_own);
+                tc::fence_before_sync();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&bar[kSFree]);
+#pragma unroll
+                for (int c = 0; c < 8; ++c)
+                    *reinterpret_cast<float4 *>(x_out + x_off(h, 8 * half + c)) =
+                        make_float4(s_own[4 * c], s_own[4 * c + 1], s_own[4 * c + 2],
+                                    s_own[4 * c + 3]);
+                tc::fence_async_smem();   // generic writes -> the bulk copy engine
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&bar[kXoReady]);
+            }
         }
-        float m_ref = -INFINITY;
-        float l = 0.f, l_r = 0.f;
-        bool ok = true;
+        // The loop never breaks: every softmax warp reaches the named barriers
+        // of every tile; after a failed wait the remaining work is skipped.
         for (int t = 0; t < ntiles; ++t) {
             const int t0 = start + t * kBN;
-            const int nvalid = min(kBN, end - t0);
-            ok = mbar_wait(&bar[kSFull], t & 1, p.err);
-            if (!ok) break;
-            tc::fence_after_sync();
-            float s[64];
-            {
-                float v[32];
-                tc::tmem_ld32(tmem + lane_base + kTmemS, v);
-#pragma unroll
-                for (int j = 0; j < 32; ++j) s[j] = v[j];
-                tc::tmem_ld32(tmem + lane_base + kTmemS + 32, v);
-#pragma unroll
-                for (int j = 0; j < 32; ++j) s[32 + j] = v[j];
-            }
-            tc::fence_before_sync();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(&bar[kSFree]);
+            const int nvalid = min(kBN, end - t0) - 32 * half;   // this half's valid keys
+            if (ok && threadIdx.x == 0) mbar_arrive_expect_tx(&bar[kXFull], kXBytes);
 
-            // ---- swap partial scores with the peer CTA (skewed 16-B chunks) ----
-            // Own partial to x_out; warp 6 copies it in bulk into the peer's
-            // x_in, whose x_full barrier expects 128 rows x 256 B per tile.
-            if (h == 0) mbar_arrive_expect_tx(&bar[kXFull], kXBytes);
-            if (t >= 1) {
-                ok = mbar_wait(&bar[kXoFree], (t - 1) & 1, p.err);
-                if (!ok) break;
-            }
+            // ---- one tile ahead: partial S(t+1) out of TMEM, staged for the copy
+            float s_next[32];
+            const bool more = t + 1 < ntiles;
+            if (ok && more) {
+                ok = __all_sync(0xffffffffu, mbar_wait(&bar[kSFull], (t + 1) & 1, p.err));
+                if (ok) {
+                    tc::fence_after_sync();
+                    tc::tmem_ld32(tmem + lane_base + s_col, s_next);
+                    tc::fence_before_sync();
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(&bar[kSFree]);
+                    // copy(t) has read x_out
+                    ok = __all_sync(0xffffffffu, mbar_wait(&bar[kXoFree], t & 1, p.err));
+                }
+                if (ok) {
 #pragma unroll
-            for (int c = 0; c < 16; ++c) {
-                const int pc = (c + h) & 15;
-                *reinterpret_cast<float4 *>(x_out + h * 256 + pc * 16) =
-                    make_float4(s[4 * c], s[4 * c + 1], s[4 * c + 2], s[4 * c + 3]);
+                    for (int c = 0; c < 8; ++c)
+                        *reinterpret_cast<float4 *>(x_out + x_off(h, 8 * half + c)) =
+                            make_float4(s_next[4 * c], s_next[4 * c + 1], s_next[4 * c + 2],
+                                        s_next[4 * c + 3]);
+                    tc::fence_async_smem();
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(&bar[kXoReady]);
+                }
             }
-            tc::fence_async_smem();   // generic writes -> the bulk copy engine
-            __syncwarp();
-            if (lane == 0) mbar_arrive(&bar[kXoReady]);
-            ok = mbar_wait_cluster(&bar[kXFull], t & 1, p.err);
-            if (!ok) break;
-#pragma unroll
-            for (int c = 0; c < 16; ++c) {
-                const int pc = (c + h) & 15;
-                const float4 o = *reinterpret_cast<const float4 *>(x_in + h * 256 + pc * 16);
-                s[4 * c] += o.x;
-                s[4 * c + 1] += o.y;
-                s[4 * c + 2] += o.z;
-                s[4 * c + 3] += o.w;
-            }
-            __syncwarp();   // the warp's reads of x_in happen before the release
-            if (lane == 0) mbar_arrive_cluster(peer_xfree);
 
-            // ---- online softmax in base 2, lazy max --------------------------
-            float mt = -INFINITY;
+            // ---- full S(t) = own partial + the peer's --------------------------
+            if (ok) ok = __all_sync(0xffffffffu, mbar_wait_cluster(&bar[kXFull], t & 1, p.err));
+            float mloc = -INFINITY;
+            if (ok) {
 #pragma unroll
-            for (int j = 0; j < 64; ++j) {
-                s[j] = j < nvalid ? s[j] * p.qk_scale_log2 : -INFINITY;
-                mt = fmaxf(mt, s[j]);
-            }
-            const bool raise = mt > m_ref + kRescaleThreshold;   // always on the first tile
-            float alpha = 1.f;
-            if (raise) {
-                alpha = fast_exp2(m_ref - mt);                  // 0 when m_ref = -inf
-                m_ref = mt;
-            }
-            // Two row sums: of the fp32 weights (for lse) and of the bf16-
-            // rounded weights the MMA multiplies V by (to normalise O).
-            float rowsum = 0.f, rowsum_r = 0.f;
-            uint32_t pk[32];
+                for (int c = 0; c < 8; ++c) {
+                    const float4 o =
+                        *reinterpret_cast<const float4 *>(x_in + x_off(h, 8 * half + c));
+                    s_own[4 * c] += o.x;
+                    s_own[4 * c + 1] += o.y;
+                    s_own[4 * c + 2] += o.z;
+                    s_own[4 * c + 3] += o.w;
+                }
+                __syncwarp();   // the warp's reads of x_in happen before the release
+                // The values read from x_in are already consumed (added into
+                // s_own) when the arrive issues, so a relaxed arrive suffices.
+                if (lane == 0)
+                    asm volatile("mbarrier.arrive.relaxed.cluster.shared::cluster.b64 _, [%0];"
+                                 ::"r"(peer_xfree) : "memory");
+                if (nvalid >= 32) {
 #pragma unroll
-            for (int j = 0; j < 32; ++j) {
-                const float p0 = fast_exp2(s[2 * j] - m_ref);
-                const float p1 = fast_exp2(s[2 * j + 1] - m_ref);
-                pk[j] = pack_bf16x2(p0, p1);
-                rowsum += p0 + p1;
-                rowsum_r += bf16_lo(pk[j]) + bf16_hi(pk[j]);
+                    for (int j = 0; j < 32; ++j) {
+                        s_own[j] *= p.qk_scale_log2;
+                        mloc = fmaxf(mloc, s_own[j]);
+                    }
+                } else {
+#pragma unroll
+                    for (int j = 0; j < 32; ++j) {
+                        s_own[j] = j < nvalid ? s_own[j] * p.qk_scale_log2 : -INFINITY;
+                        mloc = fmaxf(mloc, s_own[j]);
+                    }
+                }
             }
-            l = l * alpha + rowsum;
-            l_r = l_r * alpha + rowsum_r;
+            // ---- row max over both halves ------------------------------------
+            named_sync(kBarSoftmax, kSoftmaxThreads);   // the last tile's reads are done
+            red[half * 128 + h] = mloc;
+            named_sync(kBarSoftmax, kSoftmaxThreads);
+            const float mt = fmaxf(mloc, red[(half ^ 1) * 128 + h]);
 
-            // P(t-1)'s MMA must be done before P is overwritten or O rescaled.
-            if (t >= 1) {
-                ok = mbar_wait(&bar[kODone], (t - 1) & 1, p.err);
-                if (!ok) break;
-                tc::fence_after_sync();
-                if (__any_sync(0xffffffffu, raise)) {
+            if (ok) {
+                // ---- online softmax in base 2, lazy max --------------------------
+                const bool raise = mt > m_ref + kRescaleThreshold;   // always on the first tile
+                float alpha = 1.f;
+                if (raise) {
+                    alpha = fast_exp2(m_ref - mt);                  // 0 when m_ref = -inf
+                    m_ref = mt;
+                }
+                // Two row sums: of the fp32 weights (for lse) and of the bf16-
+                // rounded weights the MMA multiplies V by (to normalise O).
+                float rowsum = 0.f, rowsum_r = 0.f;
+                float pk[16];
+#pragma unroll
+                for (int j = 0; j < 16; ++j) {
+                    const float p0 = fast_exp2(s_own[2 * j] - m_ref);
+                    const float p1 = fast_exp2(s_own[2 * j + 1] - m_ref);
+                    const uint32_t w = pack_bf16x2(p0, p1);
+                    pk[j] = __uint_as_float(w);
+                    rowsum += p0 + p1;
+                    rowsum_r += bf16_lo(w) + bf16_hi(w);
+                }
+                l = l * alpha + rowsum;
+                l_r = l_r * alpha + rowsum_r;
+
+                // O(t-1) has read P(t-1) and must be finished before O is rescaled.
+                if (t >= 1) {
+                    ok = __all_sync(0xffffffffu, mbar_wait(&bar[kODone], (t - 1) & 1, p.err));
+                    tc::fence_after_sync();
+                    if (ok && __any_sync(0xffffffffu, raise)) {
 #pragma unroll 1
-                    for (int c = 0; c < 256; c += 32) {
-                        float v[32];
-                        tc::tmem_ld32(tmem + lane_base + kTmemO + c, v);
+                        for (int c = 0; c < 128; c += 32) {
+                            float v[32];
+                            const uint32_t oc = kTmemO + 128u * half + c;
+                            tc::tmem_ld32(tmem + lane_base + oc, v);
 #pragma unroll
-                        for (int j = 0; j < 32; ++j) v[j] *= alpha;
-                        tc::tmem_st32(tmem + lane_base + kTmemO + c, v);
+                            for (int j = 0; j < 32; ++j) v[j] *= alpha;
+                            tc::tmem_st32(tmem + lane_base + oc, v);
+                        }
+                    }
+                }
+                if (ok) {
+                    float p8[8];
+#pragma unroll
+                    for (int j = 0; j < 8; ++j) p8[j] = pk[j];
+                    tc::tmem_st_n<8>(tmem + lane_base + kTmemP + 16u * half, p8);
+#pragma unroll
+                    for (int j = 0; j < 8; ++j) p8[j] = pk[8 + j];
+                    tc::tmem_st_n<8>(tmem + lane_base + kTmemP + 16u * half + 8, p8);
+                    const int nv = min(kBN, end - t0);
+                    if (nv < kBN) {
+                        // Rows past the sequence end may hold anything (even NaN):
+                        // zero them in the V part of the stage so 0 * V stays 0.
+                        uint8_t *st = smem + Smem::kv + (t % kStages) * kStageBytes;
+                        const int nz = (kBN - nv) * 4 * 8;   // 16-B chunks in 4 boxes
+                        for (int i = threadIdx.x; i < nz; i += kSoftmaxThreads) {
+                            const int box = i / ((kBN - nv) * 8);
+                            const int rem = i - box * ((kBN - nv) * 8);
+                            const int row = nv + rem / 8;
+                            const int ch = rem & 7;
+                            *reinterpret_cast<uint4 *>(st + box * kKBoxBytes + row * 128 +
+                                                       ch * 16) = make_uint4(0u, 0u, 0u, 0u);
+                        }
+                        tc::fence_async_smem();
                     }
                     tc::tmem_wait_st();
+                    tc::fence_before_sync();
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(&bar[kPFull]);   // one arrival per softmax warp
                 }
             }
-            // P row h: 64 bf16 keys = 128 B, K-major with 128-byte swizzle.
+            if (more) {
 #pragma unroll
-            for (int c = 0; c < 8; ++c) {
-                uint4 v;
-                v.x = pk[4 * c]; v.y = pk[4 * c + 1]; v.z = pk[4 * c + 2]; v.w = pk[4 * c + 3];
-                *reinterpret_cast<uint4 *>(pbuf + p_swz(h, c)) = v;
+                for (int j = 0; j < 32; ++j) s_own[j] = s_next[j];
             }
-            if (nvalid < kBN) {
-                // Rows past the sequence end may hold anything (even NaN):
-                // zero them in the V part of the stage so 0 * V stays 0.
-                uint8_t *st = smem + Smem::kv + (t % kStages) * kStageBytes;
-                const int nz = (kBN - nvalid) * 4 * 8;   // 16-B chunks in 4 boxes
-                for (int i = h; i < nz; i += 128) {
-                    const int box = i / ((kBN - nvalid) * 8);
-                    const int rem = i - box * ((kBN - nvalid) * 8);
-                    const int row = nvalid + rem / 8;
-                    const int ch = rem & 7;
-                    *reinterpret_cast<uint4 *>(st + box * kKBoxBytes + row * 128 + ch * 16) =
-                        make_uint4(0u, 0u, 0u, 0u);
-                }
-            }
-            tc::fence_async_smem();
-            tc::fence_before_sync();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(&bar[kPFull]);   // one arrival per softmax warp
         }
 
         // ---- epilogue ---------------------------------------------------------
         if (ok && ntiles > 0) {
-            ok = mbar_wait(&bar[kODone], (ntiles - 1) & 1, p.err);
+            ok = __all_sync(0xffffffffu, mbar_wait(&bar[kODone], (ntiles - 1) & 1, p.err));
             tc::fence_after_sync();
         }
+        // Row sums of the two halves (same m_ref): through shared memory in the
+        // K ring, which no MMA or copy touches any more.
+        float *sums = reinterpret_cast<float *>(smem + Smem::kv);
+        named_sync(kBarSoftmax, kSoftmaxThreads);
+        sums[half * 256 + h] = l;
+        sums[half * 256 + 128 + h] = l_r;
+        named_sync(kBarSoftmax, kSoftmaxThreads);
+        l += sums[(half ^ 1) * 256 + h];
+        l_r += sums[(half ^ 1) * 256 + 128 + h];
         // O was accumulated with the rounded weights: normalise it by their
         // sum (direct), or rescale it to the fp32 sum l kept for the merge.
         float scale_o = 0.f, Mf = -INFINITY, Z = 0.f;
@@ -455,17 +537,18 @@ mla_decode_kernel(const __grid_constant__ MlaParams p) {
             scale_o = l_r > 0.f ? l / l_r : 0.f;
         }
         const size_t row = size_t(b) * kMlaHeads + h;
+        const int ch0 = rank * 256 + half * 128;   // this warp's output channels
 #pragma unroll 1
-        for (int c = 0; c < 256; c += 32) {
+        for (int c = 0; c < 128; c += 32) {
             float v[32];
             if (ntiles > 0 && ok) {
-                tc::tmem_ld32(tmem + lane_base + kTmemO + c, v);
+                tc::tmem_ld32(tmem + lane_base + kTmemO + 128u * half + c, v);
             } else {
 #pragma unroll
                 for (int j = 0; j < 32; ++j) v[j] = 0.f;
             }
             if (direct) {
-                uint16_t *dst = p.out + row * kMlaDimV + rank * 256 + c;
+                uint16_t *dst = p.out + row * kMlaDimV + ch0 + c;
 #pragma unroll
                 for (int j = 0; j < 32; j += 8) {
                     uint4 w;
@@ -477,7 +560,7 @@ mla_decode_kernel(const __grid_constant__ MlaParams p) {
                 }
             } else {
                 float *dst = p.ws_o + (size_t(part) * p.batch * kMlaHeads + row) * kMlaDimV +
-                             rank * 256 + c;
+                             ch0 + c;
 #pragma unroll
                 for (int j = 0; j < 32; j += 4)
                     *reinterpret_cast<float4 *>(dst + j) =
@@ -485,7 +568,7 @@ mla_decode_kernel(const __grid_constant__ MlaParams p) {
                                     v[j + 3] * scale_o);
             }
         }
-        if (rank == 0) {
+        if (rank == 0 && half == 0) {
             if (direct) {
                 if (p.lse) p.lse[row] = Z > 0.f ? (Mf + fast_log2(Z)) * kLn2 : -INFINITY;
             } else {
@@ -500,7 +583,7 @@ mla_decode_kernel(const __grid_constant__ MlaParams p) {
     tc::fence_before_sync();
     __syncthreads();
     cluster_sync();  // no CTA leaves while its peer may still touch its smem
-    if (warp == 5) {
+    if (warp == 9) {
         tc::fence_after_sync();
         tc::tmem_dealloc(tmem, kTmemCols);
     }
