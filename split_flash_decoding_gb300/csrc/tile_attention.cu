@@ -11,13 +11,15 @@
 // 4-D TMA box (64 channels x group heads x 1 KV head x T tokens) loads it.
 //
 // Per 128-key tile: S = Q K^T (M=128, N=128, K=128) into a double-buffered
-// TMEM accumulator, online softmax by four warps (thread = row, causal and
-// length masks applied per element), P (bf16) to shared memory, then
-// O += P V (M=128, N=128, K=128) in TMEM.  The running max is lazy: it is
+// TMEM accumulator, online softmax by eight warps (two per row: warps w and
+// w+4 share TMEM lanes 32(w%4).. and split the 128 keys; causal and length
+// masks applied per element; the two halves' row maxima combined through
+// shared memory), P (bf16 pairs) into TMEM, then O += P V (M=128, N=128,
+// K=128) with P as the A operand from TMEM.  The running max is lazy: it is
 // raised, and O rescaled, only when a tile's max exceeds it by more than 8
 // (base 2).  No split-K: each CTA covers all keys its rows can see.
 //
-// Warp roles (192 threads): 0-3 softmax/epilogue, 4 TMA producer, 5 TMEM
+// Warp roles (320 threads): 0-7 softmax/epilogue, 8 TMA producer, 9 TMEM
 // allocation + MMA issue.
 #include "launch.h"
 #include "ptx.cuh"
@@ -28,14 +30,17 @@ namespace {
 
 constexpr int kD = 128;
 constexpr int kBN = kTileKeys;               // keys per tile
-constexpr int kStages = 2;
+constexpr int kStages = 3;
 constexpr int kBoxBytes = 128 * 128;         // 128 rows x 128 B (64 channels)
 constexpr int kTileBytes = 2 * kBoxBytes;    // 128 rows x 128 channels
 constexpr int kStageBytes = 2 * kTileBytes;  // K + V
-constexpr int kThreads = 192;
+constexpr int kThreads = 320;
+constexpr int kSoftmaxThreads = 256;         // warps 0-7
+constexpr int kBarSoftmax = 1;               // named barrier of the softmax warps
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kTmemS = 0;               // S buffers at 0 and 128
 constexpr uint32_t kTmemO = 256;
+constexpr uint32_t kTmemP = 384;             // 64 columns: P of one tile as bf16 pairs
 constexpr float kRescaleThreshold = 8.0f;
 
 // V as the MN-major B operand: two 64-channel blocks 16 KB apart, 8-key
@@ -46,21 +51,21 @@ constexpr uint32_t kVSbo = 1024;
 struct Smem {
     static constexpr int q = 0;                                  // 32 KB
     static constexpr int kv = q + kTileBytes;                    // 128 KB
-    static constexpr int p = kv + kStages * kStageBytes;         // 32 KB
-    static constexpr int bars = p + kTileBytes;
+    static constexpr int red = kv + kStages * kStageBytes;       // 192 KB
+    static constexpr int bars = red + 2 * 128 * 4;               // +1 KB (row maxima)
     static constexpr int total = bars + 256;
 };
 constexpr size_t kSmemBytes = Smem::total + 1024;
 
 enum Bar {
-    kKvFull = 0,   // [2]
-    kKvEmpty = 2,  // [2]
-    kQFull = 4,
-    kSFull = 5,    // [2]
-    kSFree = 7,    // [2]
-    kPFull = 9,
-    kODone = 10,
-    kNumBars = 11
+    kKvFull = 0,                  // [kStages]
+    kKvEmpty = kStages,           // [kStages]
+    kQFull = 2 * kStages,
+    kSFull = kQFull + 1,          // [2]
+    kSFree = kSFull + 2,          // [2]
+    kPFull = kSFree + 2,
+    kODone = kPFull + 1,
+    kNumBars = kODone + 1
 };
 
 __global__ void __launch_bounds__(kThreads, 1)
@@ -93,12 +98,12 @@ tile_attention_kernel(const __grid_constant__ TileParams p) {
 
     if (threadIdx.x == 0) {
         for (int i = 0; i < kNumBars; ++i) {
-            const uint32_t cnt = (i == kSFree || i == kSFree + 1 || i == kPFull) ? 4u : 1u;
+            const uint32_t cnt = (i == kSFree || i == kSFree + 1 || i == kPFull) ? 8u : 1u;
             mbar_init(&bar[i], cnt);
         }
         fence_mbar_init();
     }
-    if (warp == 5) {
+    if (warp == 9) {
         tc::tmem_alloc(tmem_slot, kTmemCols);
         tc::tmem_relinquish();
     }
@@ -107,7 +112,7 @@ tile_attention_kernel(const __grid_constant__ TileParams p) {
     tc::fence_after_sync();
     const uint32_t tmem = *tmem_slot;
 
-    if (warp == 4) {
+    if (warp == 8) {
         // ------------------------------------------------------------ producer
         if (ntiles > 0) {
             if (lane == 0) {
@@ -191,14 +196,13 @@ tile_attention_kernel(const __grid_constant__ TileParams p) {
                     mbar_wait(&bar[kKvFull + i % kStages], (i / kStages) & 1, p.err);
             }
         }
-    } else if (warp == 5) {
+    } else if (warp == 9) {
         // ------------------------------------------------------------ MMA issue
         if (ntiles > 0 && lane == 0) {
             constexpr uint32_t idesc_s = tc::idesc_bf16_f32(128, kBN, 0, 0);
             constexpr uint32_t idesc_o = tc::idesc_bf16_f32(128, kD, 0, 1);
             const uint32_t q_base = smem_addr(smem + Smem::q);
             const uint32_t kv_base = smem_addr(smem + Smem::kv);
-            const uint32_t p_base = smem_addr(smem + Smem::p);
             bool ok = mbar_wait(&bar[kQFull], 0, p.err);
             for (int t = 0; ok && t <= ntiles; ++t) {
                 if (t < ntiles) {
@@ -208,12 +212,14 @@ tile_attention_kernel(const __grid_constant__ TileParams p) {
                     if (ok && t >= 2) ok = mbar_wait(&bar[kSFree + sb], ((t >> 1) - 1) & 1, p.err);
                     if (!ok) break;
                     tc::fence_after_sync();
-                    const uint32_t ks = kv_base + s * kStageBytes;
+                    // Descriptors advance by byte offset / 16 in their start
+                    // field; unrolled so issue is not bound by descriptor math.
+                    const uint64_t qd = tc::smem_desc_sw128(q_base, 16, 1024);
+                    const uint64_t kd = tc::smem_desc_sw128(kv_base + s * kStageBytes, 16, 1024);
+#pragma unroll
                     for (int kk = 0; kk < kD / 16; ++kk) {
-                        const uint32_t off = (kk >> 2) * kBoxBytes + (kk & 3) * 32;
-                        tc::mma_bf16(tmem + kTmemS + sb * kBN,
-                                     tc::smem_desc_sw128(q_base + off, 16, 1024),
-                                     tc::smem_desc_sw128(ks + off, 16, 1024), idesc_s, kk > 0);
+                        const uint64_t off = uint64_t(((kk >> 2) * kBoxBytes + (kk & 3) * 32) >> 4);
+                        tc::mma_bf16(tmem + kTmemS + sb * kBN, qd + off, kd + off, idesc_s, kk > 0);
                     }
                     tc::mma_commit(&bar[kSFull + sb]);
                 }
@@ -222,13 +228,14 @@ tile_attention_kernel(const __grid_constant__ TileParams p) {
                     ok = mbar_wait(&bar[kPFull], tp & 1, p.err);
                     if (!ok) break;
                     tc::fence_after_sync();
-                    const uint32_t vs = kv_base + (tp % kStages) * kStageBytes + kTileBytes;
-                    for (int kk = 0; kk < kBN / 16; ++kk) {
-                        const uint32_t poff = (kk >> 2) * kBoxBytes + (kk & 3) * 32;
-                        tc::mma_bf16(tmem + kTmemO, tc::smem_desc_sw128(p_base + poff, 16, 1024),
-                                     tc::smem_desc_sw128(vs + kk * 16 * 128, kVLbo, kVSbo),
-                                     idesc_o, tp > 0 || kk > 0);
-                    }
+                    const uint64_t vd = tc::smem_desc_sw128(
+                        kv_base + (tp % kStages) * kStageBytes + kTileBytes, kVLbo, kVSbo);
+#pragma unroll
+                    for (int kk = 0; kk < kBN / 16; ++kk)
+                        // A = P from TMEM: 16 keys = 8 columns of bf16 pairs per step
+                        tc::mma_bf16_tmem_a(tmem + kTmemO, tmem + kTmemP + kk * 8,
+                                            vd + uint64_t((kk * 16 * 128) >> 4), idesc_o,
+                                            tp > 0 || kk > 0);
                     tc::mma_commit(&bar[kODone]);
                     tc::mma_commit(&bar[kKvEmpty + (tp % kStages)]);
                 }
@@ -236,40 +243,50 @@ tile_attention_kernel(const __grid_constant__ TileParams p) {
         }
     } else {
         // ------------------------------------------------------------ softmax
-        const int r = warp * 32 + lane;          // MMA row == TMEM lane
+        const int r = (warp & 3) * 32 + lane;    // MMA row == TMEM lane
+        const int half = warp >> 2;              // keys [64 half, 64 half + 64) of a tile
         const int tok = t0 + r / G;              // token index inside the sequence
         const bool row_valid = tok < n;
         const int lim = p.causal ? min(L, L - n + tok + 1) : L;   // keys [0, lim)
-        const uint32_t lane_base = uint32_t(warp * 32) << 16;
-        uint8_t *pbuf = smem + Smem::p;
+        const uint32_t lane_base = uint32_t((warp & 3) * 32) << 16;
+        float *red = reinterpret_cast<float *>(smem + Smem::red);
         float m_ref = -INFINITY;
-        float l = 0.f, l_r = 0.f;
+        float l = 0.f, l_r = 0.f;   // this half's share of the row sums
         bool ok = true;
+        // The loop never breaks: every softmax warp reaches the named barriers
+        // of every tile; after a failed wait the remaining work is skipped.
         for (int t = 0; t < ntiles; ++t) {
             const int sb = t & 1;
-            const int key0 = t * kBN;
-            ok = mbar_wait(&bar[kSFull + sb], (t >> 1) & 1, p.err);
-            if (!ok) break;
-            tc::fence_after_sync();
-            float sc[kBN];
+            const int key0 = t * kBN + 64 * half;
+            float sc[64];
+            float mloc = -INFINITY;
+            if (ok) ok = __all_sync(0xffffffffu, mbar_wait(&bar[kSFull + sb], (t >> 1) & 1, p.err));
+            if (ok) {
+                tc::fence_after_sync();
 #pragma unroll
-            for (int c = 0; c < kBN; c += 32) {
-                float v[32];
-                tc::tmem_ld32(tmem + lane_base + kTmemS + sb * kBN + c, v);
+                for (int c = 0; c < 64; c += 32) {
+                    float v[32];
+                    tc::tmem_ld32(tmem + lane_base + kTmemS + sb * kBN + 64 * half + c, v);
 #pragma unroll
-                for (int j = 0; j < 32; ++j) sc[c + j] = v[j];
+                    for (int j = 0; j < 32; ++j) sc[c + j] = v[j];
+                }
+                tc::fence_before_sync();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&bar[kSFree + sb]);
+                const int nvis = lim - key0;         // keys of this half the row sees
+#pragma unroll
+                for (int j = 0; j < 64; ++j) {
+                    sc[j] = j < nvis ? sc[j] * p.qk_scale_log2 : -INFINITY;
+                    mloc = fmaxf(mloc, sc[j]);
+                }
             }
-            tc::fence_before_sync();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(&bar[kSFree + sb]);
+            // ---- row max over both halves ------------------------------------
+            named_sync(kBarSoftmax, kSoftmaxThreads);   // the last tile's reads are done
+            red[half * 128 + r] = mloc;
+            named_sync(kBarSoftmax, kSoftmaxThreads);
+            const float mt = fmaxf(mloc, red[(half ^ 1) * 128 + r]);
+            if (!ok) continue;
 
-            const int nvis = lim - key0;         // keys of this tile the row sees
-            float mt = -INFINITY;
-#pragma unroll
-            for (int j = 0; j < kBN; ++j) {
-                sc[j] = j < nvis ? sc[j] * p.qk_scale_log2 : -INFINITY;
-                mt = fmaxf(mt, sc[j]);
-            }
             const bool raise = mt > m_ref + kRescaleThreshold;
             float alpha = 1.f;
             if (raise) {
@@ -280,56 +297,53 @@ tile_attention_kernel(const __grid_constant__ TileParams p) {
             // Two row sums: of the fp32 weights (for lse) and of the bf16-
             // rounded weights the MMA multiplies V by (to normalise O).
             float rowsum = 0.f, rowsum_r = 0.f;
-            uint32_t pk[kBN / 2];
+            float pk[32];
 #pragma unroll
-            for (int j = 0; j < kBN / 2; ++j) {
+            for (int j = 0; j < 32; ++j) {
                 const float p0 = live ? fast_exp2(sc[2 * j] - m_ref) : 0.f;
                 const float p1 = live ? fast_exp2(sc[2 * j + 1] - m_ref) : 0.f;
-                pk[j] = pack_bf16x2(p0, p1);
+                const uint32_t w = pack_bf16x2(p0, p1);
+                pk[j] = __uint_as_float(w);
                 rowsum += p0 + p1;
-                rowsum_r += bf16_lo(pk[j]) + bf16_hi(pk[j]);
+                rowsum_r += bf16_lo(w) + bf16_hi(w);
             }
             l = l * alpha + rowsum;
             l_r = l_r * alpha + rowsum_r;
 
+            // O(t-1) has read P(t-1) and must be finished before P is
+            // overwritten or O rescaled.
             if (t >= 1) {
-                ok = mbar_wait(&bar[kODone], (t - 1) & 1, p.err);
-                if (!ok) break;
+                ok = __all_sync(0xffffffffu, mbar_wait(&bar[kODone], (t - 1) & 1, p.err));
+                if (!ok) continue;
                 tc::fence_after_sync();
                 if (__any_sync(0xffffffffu, raise)) {
 #pragma unroll 1
-                    for (int c = 0; c < kD; c += 32) {
+                    for (int c = 0; c < 64; c += 32) {
                         float v[32];
-                        tc::tmem_ld32(tmem + lane_base + kTmemO + c, v);
+                        const uint32_t oc = kTmemO + 64u * half + c;
+                        tc::tmem_ld32(tmem + lane_base + oc, v);
 #pragma unroll
                         for (int j = 0; j < 32; ++j) v[j] *= alpha;
-                        tc::tmem_st32(tmem + lane_base + kTmemO + c, v);
+                        tc::tmem_st32(tmem + lane_base + oc, v);
                     }
-                    tc::tmem_wait_st();
                 }
             }
-            // P row r: keys 0-63 in box 0, 64-127 in box 1 (128-byte swizzle).
-#pragma unroll
-            for (int c = 0; c < 16; ++c) {
-                uint4 v;
-                v.x = pk[4 * c]; v.y = pk[4 * c + 1]; v.z = pk[4 * c + 2]; v.w = pk[4 * c + 3];
-                const int box = c >> 3, ch = c & 7;
-                *reinterpret_cast<uint4 *>(pbuf + box * kBoxBytes + r * 128 +
-                                           ((ch ^ (r & 7)) << 4)) = v;
-            }
-            const int nkeys = min(kBN, L - key0);
+            // P row r, keys of this half: 32 columns of bf16 pairs.
+            tc::tmem_st32(tmem + lane_base + kTmemP + 32u * half, pk);
+            const int nkeys = min(kBN, L - t * kBN);
             if (nkeys < kBN) {
                 // Slots past the sequence end may hold anything: zero them in V.
                 uint8_t *vs = smem + Smem::kv + (t % kStages) * kStageBytes + kTileBytes;
                 const int per_box = (kBN - nkeys) * 8;          // 16-B chunks
-                for (int i = r; i < 2 * per_box; i += 128) {
+                for (int i = threadIdx.x; i < 2 * per_box; i += kSoftmaxThreads) {
                     const int box = i / per_box;
                     const int rem = i - box * per_box;
                     *reinterpret_cast<uint4 *>(vs + box * kBoxBytes + (nkeys + rem / 8) * 128 +
                                                (rem & 7) * 16) = make_uint4(0u, 0u, 0u, 0u);
                 }
+                tc::fence_async_smem();
             }
-            tc::fence_async_smem();
+            tc::tmem_wait_st();
             tc::fence_before_sync();
             __syncwarp();
             if (lane == 0) mbar_arrive(&bar[kPFull]);
@@ -337,9 +351,18 @@ tile_attention_kernel(const __grid_constant__ TileParams p) {
 
         // ---- epilogue ---------------------------------------------------------
         if (ok && ntiles > 0) {
-            ok = mbar_wait(&bar[kODone], (ntiles - 1) & 1, p.err);
+            ok = __all_sync(0xffffffffu, mbar_wait(&bar[kODone], (ntiles - 1) & 1, p.err));
             tc::fence_after_sync();
         }
+        // Row sums of the two halves (same m_ref), through the Q buffer, which
+        // no MMA reads any more.
+        float *sums = reinterpret_cast<float *>(smem + Smem::q);
+        named_sync(kBarSoftmax, kSoftmaxThreads);
+        sums[half * 256 + r] = l;
+        sums[half * 256 + 128 + r] = l_r;
+        named_sync(kBarSoftmax, kSoftmaxThreads);
+        l += sums[(half ^ 1) * 256 + r];
+        l_r += sums[(half ^ 1) * 256 + 128 + r];
         const int h = kvh * G + (r % G);
         const float t2 = p.sink ? p.sink[h] * kLog2e : -INFINITY;
         const float Mf = fmaxf(m_ref, t2);
@@ -352,12 +375,12 @@ tile_attention_kernel(const __grid_constant__ TileParams p) {
         }
         const float scale_o = Zr > 0.f ? so / Zr : 0.f;
         const size_t row = size_t(q_off) + tok;
-        uint16_t *dst = p.out + (row * p.num_q_heads + h) * kD;
+        uint16_t *dst = p.out + (row * p.num_q_heads + h) * kD + 64 * half;
 #pragma unroll 1
-        for (int c = 0; c < kD; c += 32) {
+        for (int c = 0; c < 64; c += 32) {
             float v[32];
             if (ntiles > 0 && ok) {
-                tc::tmem_ld32(tmem + lane_base + kTmemO + c, v);
+                tc::tmem_ld32(tmem + lane_base + kTmemO + 64u * half + c, v);
             } else {
 #pragma unroll
                 for (int j = 0; j < 32; ++j) v[j] = 0.f;
@@ -374,13 +397,13 @@ tile_attention_kernel(const __grid_constant__ TileParams p) {
                 }
             }
         }
-        if (row_valid && p.lse)
+        if (row_valid && p.lse && half == 0)
             p.lse[row * p.num_q_heads + h] = Z > 0.f ? (Mf + fast_log2(Z)) * kLn2 : -INFINITY;
     }
 
     tc::fence_before_sync();
     __syncthreads();
-    if (warp == 5) {
+    if (warp == 9) {
         tc::fence_after_sync();
         tc::tmem_dealloc(tmem, kTmemCols);
     }
