@@ -227,15 +227,16 @@ extern "C" int attn_plan_partitions(int num_sms, int batch, int num_q_rows, int 
         }
         // GQA runs a persistent grid over (sequence, KV head, slice) items,
         // one CTA per SM for head_dim 128 (tensor cores) and two for
-        // head_dim 64; MLA runs one two-CTA cluster per SM pair per
-        // item and writes 256 KB of fp32 partials per slice, so its slices
-        // are longer.  GQA with fewer (sequence, KV head) units than CTAs gets
-        // one slice per CTA (one wave), as if every sequence had max_kv_len
-        // keys.  Otherwise P is at least what gives every CTA four
-        // items at full length and at least max_kv_len / target (slices of
-        // ~1024 keys for GQA, ~4096 for MLA), which keeps a ragged batch
-        // balanced; when it does not cost more than doubling P, P is rounded
-        // up so that units * P is a multiple of the CTA count.
+        // head_dim 64.  GQA with fewer (sequence, KV head) units than CTAs
+        // gets one slice per CTA (one wave), as if every sequence had
+        // max_kv_len keys.  Otherwise P is at least what gives every CTA four
+        // items at full length and at least max_kv_len / 1024, which keeps a
+        // ragged batch balanced; when it does not cost more than doubling P,
+        // P is rounded up so that units * P is a multiple of the CTA count.
+        // MLA runs one two-CTA cluster per SM pair per (slice, sequence) and
+        // writes 256 KB of fp32 partials per slice, which the reduce reads
+        // back: slices of ~4096 keys, and at least one per cluster when the
+        // batch is smaller than the cluster count.
         const bool mla = num_kv_heads == 1 && head_dim_v == kMlaDimV;
         const bool tc = !mla && head_dim_v == 128;   // tensor-core decode: one CTA per SM
         const long long units = static_cast<long long>(batch > 0 ? batch : 1) * num_kv_heads;
@@ -243,7 +244,11 @@ extern "C" int attn_plan_partitions(int num_sms, int batch, int num_q_rows, int 
                                    : (tc ? num_sms : 2LL * num_sms);
         const long long target = mla ? 4096 : 1024;
         long long p;
-        if (!mla && units < ctas) {
+        if (mla) {
+            const long long p_fill = (ctas + units - 1) / units;
+            const long long p_len = (static_cast<long long>(max_kv_len) + target - 1) / target;
+            p = p_fill > p_len ? p_fill : p_len;
+        } else if (units < ctas) {
             p = (ctas + units - 1) / units;
         } else {
             const long long p_fill = (4 * ctas + units - 1) / units;

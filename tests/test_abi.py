@@ -151,9 +151,13 @@ def test_planner_formulas(attn):
     assert P == 19 and 8 * P == 152
     P, _ = attn.attn_plan_partitions(1, 1, 16, 8, 64, 131072, 0, num_sms=152)
     assert P == 38 and 8 * P == 2 * 152
-    # automatic MLA (one KV head, 512 output channels): one cluster per SM pair
+    # automatic MLA (one KV head, 512 output channels): one cluster per SM
+    # pair; slices of ~4096 keys, at least one cluster's worth when the
+    # batch is small
     P, _ = attn.attn_plan_partitions(32, 32, 128, 1, 512, 32768, 0, num_sms=152)
-    assert P == 19 and 32 * P >= 4 * 76 and (32 * P) % 76 == 0
+    assert P == 8
+    P, _ = attn.attn_plan_partitions(1, 1, 128, 1, 512, 131072, 0, num_sms=152)
+    assert P == 76
     P, _ = attn.attn_plan_partitions(1, 1, 32, 8, 128, 20, 0, num_sms=152)
     assert P == 1                                     # one tile of keys cannot split
     P, _ = attn.attn_plan_partitions(4, 4, 32, 8, 128, 0, 0, num_sms=152)
