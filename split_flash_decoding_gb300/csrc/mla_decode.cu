@@ -38,9 +38,10 @@
 //   warp 9     TMEM allocation and MMA issue (one thread), order
 //              S0 S1 S2 O0 S3 O1 ...: the score MMA of tile t+2 is issued
 //              as soon as S(t+1) has been read, ahead of O(t)
-//   warp 10    exchange: one bulk copy per tile (cp.async.bulk, shared::cta
-//              to the peer's shared::cluster, complete-tx on the peer's
-//              barrier) of the staged 32 KB of partial scores
+//   warp 10    exchange: two bulk copies per tile, one per key half
+//              (cp.async.bulk, shared::cta to the peer's shared::cluster,
+//              complete-tx on the peer's barrier of that half), 16 KB each;
+//              a half is staged while the other half is on the wire
 //
 // Q is the A operand of the score MMA straight from TMEM, so shared memory
 // holds only the K ring and the two exchange buffers.  TMEM columns: Q
@@ -64,6 +65,7 @@ constexpr int kThreads = 352;
 constexpr int kSoftmaxThreads = 256;   // warps 0-7
 constexpr int kBarSoftmax = 1;         // named barrier of the softmax warps
 constexpr uint32_t kXBytes = 128u * kMlaTileKeys * 4u;   // one tile of fp32 partial scores
+constexpr uint32_t kXHalfBytes = kXBytes / 2;            // one key half (32 keys)
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kTmemQ = 0;             // up to 160 columns of packed bf16 pairs
 constexpr uint32_t kTmemP = 160;           // 32 columns: P of one tile as bf16 pairs
@@ -81,7 +83,7 @@ struct Smem {
     static constexpr int x_out = x_in + int(kXBytes);                 // +32 KB (peer's partial)
     static constexpr int red = x_out + int(kXBytes);                  // +32 KB (own partial)
     static constexpr int bars = red + 2 * 128 * 4;                    // +1 KB (row maxima)
-    static constexpr int total = bars + 160;
+    static constexpr int total = bars + 192;
 };
 constexpr size_t kSmemBytes = Smem::total + 1024;
 
@@ -93,17 +95,20 @@ enum Bar {
     kSFree,       // the softmax warps have read it (4 arrivals)
     kPFull,       // P of a tile in TMEM, V tail cleared (4 arrivals)
     kODone,       // O MMA of a tile finished (commit)
-    kXFull,       // peer's partial landed in x_in (own expect_tx + peer's copy bytes)
-    kXPeerFree,   // the peer has read its x_in (remote arrivals from its 4 softmax warps)
-    kXoReady,     // own 4 softmax warps staged x_out
-    kXoFree,      // the bulk copy finished reading x_out
-    kNumBars
+    // [2] each: one per key half of the exchange buffers
+    kXFull,                     // peer's half landed in x_in (own expect_tx + peer's copy bytes)
+    kXPeerFree = kXFull + 2,    // the peer has read its half of x_in (its 4 warps of that half)
+    kXoReady = kXPeerFree + 2,  // own 4 softmax warps of the half staged x_out
+    kXoFree = kXoReady + 2,     // the bulk copy finished reading the half of x_out
+    kXEnd = kXoFree + 2,
+    kNumBars = kXEnd
 };
 
-// Partial score row h of one tile in an exchange buffer: 16-B chunk c at a
-// row-dependent rotation, so a warp's 32 rows hit different banks.
-__device__ __forceinline__ uint32_t x_off(int h, int c) {
-    return uint32_t(h * 256 + (((c + h) & 15) << 4));
+// Partial score row h of one key half (32 keys, 128 B) in an exchange
+// buffer: 16-B chunk c at a row-dependent rotation, so the 8 rows of a
+// quarter-warp access hit all 32 banks.
+__device__ __forceinline__ uint32_t x_half_off(int hf, int h, int c) {
+    return uint32_t(hf) * kXHalfBytes + uint32_t(h * 128 + (((c + h) & 7) << 4));
 }
 
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
@@ -145,10 +150,12 @@ mla_decode_kernel(const __grid_constant__ MlaParams p) {
         mbar_init(&bar[kSFree], 8);
         mbar_init(&bar[kPFull], 8);
         mbar_init(&bar[kODone], 1);
-        mbar_init(&bar[kXFull], 1);
-        mbar_init(&bar[kXPeerFree], 8);
-        mbar_init(&bar[kXoReady], 8);
-        mbar_init(&bar[kXoFree], 1);
+        for (int i = 0; i < 2; ++i) {
+            mbar_init(&bar[kXFull + i], 1);
+            mbar_init(&bar[kXPeerFree + i], 4);
+            mbar_init(&bar[kXoReady + i], 4);
+            mbar_init(&bar[kXoFree + i], 1);
+        }
         fence_mbar_init();
     }
     if (warp == 9) {
@@ -295,12 +302,22 @@ mla_decode_kernel(const __grid_constant__ MlaParams p) {
             const uint32_t dst = mapa_shared(smem_addr(smem + Smem::x_in), peer);
             const uint32_t dst_bar = mapa_shared(smem_addr(&bar[kXFull]), peer);
             const uint32_t src = smem_addr(smem + Smem::x_out);
-            for (int t = 0; t < ntiles; ++t) {
-                if (!mbar_wait(&bar[kXoReady], t & 1, p.err)) break;
-                if (t >= 1 && !mbar_wait_cluster(&bar[kXPeerFree], (t - 1) & 1, p.err)) break;
-                bulk_copy_to_peer(dst, src, kXBytes, dst_bar);
-                bulk_wait_read();
-                mbar_arrive(&bar[kXoFree]);
+            // The two key halves go one after the other, so one half is
+            // staged while the other is on the wire.
+            bool run = true;
+            for (int t = 0; run && t < ntiles; ++t) {
+                for (int hf = 0; hf < 2; ++hf) {
+                    if (!mbar_wait(&bar[kXoReady + hf], t & 1, p.err) ||
+                        (t >= 1 &&
+                         !mbar_wait_cluster(&bar[kXPeerFree + hf], (t - 1) & 1, p.err))) {
+                        run = false;
+                        break;
+                    }
+                    bulk_copy_to_peer(dst + hf * kXHalfBytes, src + hf * kXHalfBytes,
+                                      kXHalfBytes, dst_bar + 8u * hf);
+                    bulk_wait_read();
+                    mbar_arrive(&bar[kXoFree + hf]);
+                }
             }
         }
     } else {
@@ -311,7 +328,7 @@ mla_decode_kernel(const __grid_constant__ MlaParams p) {
         uint8_t *x_in = smem + Smem::x_in;
         uint8_t *x_out = smem + Smem::x_out;
         float *red = reinterpret_cast<float *>(smem + Smem::red);
-        const uint32_t peer_xfree = mapa_shared(smem_addr(&bar[kXPeerFree]), peer);
+        const uint32_t peer_xfree = mapa_shared(smem_addr(&bar[kXPeerFree + half]), peer);
         const uint32_t s_col = kTmemS + 32u * half;
         float m_ref = -INFINITY;
         float l = 0.f, l_r = 0.f;   // this half's share of the row sums
@@ -349,12 +366,12 @@ mla_decode_kernel(const __grid_constant__ MlaParams p) {
                 if (lane == 0) mbar_arrive(&bar[kSFree]);
 #pragma unroll
                 for (int c = 0; c < 8; ++c)
-                    *reinterpret_cast<float4 *>(x_out + x_off(h, 8 * half + c)) =
+                    *reinterpret_cast<float4 *>(x_out + x_half_off(half, h, c)) =
                         make_float4(s_own[4 * c], s_own[4 * c + 1], s_own[4 * c + 2],
                                     s_own[4 * c + 3]);
                 tc::fence_async_smem();   // generic writes -> the bulk copy engine
                 __syncwarp();
-                if (lane == 0) mbar_arrive(&bar[kXoReady]);
+                if (lane == 0) mbar_arrive(&bar[kXoReady + half]);
             }
         }
         // The loop never breaks: every softmax warp reaches the named barriers
@@ -362,7 +379,7 @@ mla_decode_kernel(const __grid_constant__ MlaParams p) {
         for (int t = 0; t < ntiles; ++t) {
             const int t0 = start + t * kBN;
             const int nvalid = min(kBN, end - t0) - 32 * half;   // this half's valid keys
-            if (ok && threadIdx.x == 0) mbar_arrive_expect_tx(&bar[kXFull], kXBytes);
+            if (ok && h == 0) mbar_arrive_expect_tx(&bar[kXFull + half], kXHalfBytes);
 
             // ---- one tile ahead: partial S(t+1) out of TMEM, staged for the copy
             float s_next[32];
@@ -376,28 +393,28 @@ mla_decode_kernel(const __grid_constant__ MlaParams p) {
                     __syncwarp();
                     if (lane == 0) mbar_arrive(&bar[kSFree]);
                     // copy(t) has read x_out
-                    ok = __all_sync(0xffffffffu, mbar_wait(&bar[kXoFree], t & 1, p.err));
+                    ok = __all_sync(0xffffffffu, mbar_wait(&bar[kXoFree + half], t & 1, p.err));
                 }
                 if (ok) {
 #pragma unroll
                     for (int c = 0; c < 8; ++c)
-                        *reinterpret_cast<float4 *>(x_out + x_off(h, 8 * half + c)) =
+                        *reinterpret_cast<float4 *>(x_out + x_half_off(half, h, c)) =
                             make_float4(s_next[4 * c], s_next[4 * c + 1], s_next[4 * c + 2],
                                         s_next[4 * c + 3]);
                     tc::fence_async_smem();
                     __syncwarp();
-                    if (lane == 0) mbar_arrive(&bar[kXoReady]);
+                    if (lane == 0) mbar_arrive(&bar[kXoReady + half]);
                 }
             }
 
             // ---- full S(t) = own partial + the peer's --------------------------
-            if (ok) ok = __all_sync(0xffffffffu, mbar_wait_cluster(&bar[kXFull], t & 1, p.err));
+            if (ok) ok = __all_sync(0xffffffffu, mbar_wait_cluster(&bar[kXFull + half], t & 1, p.err));
             float mloc = -INFINITY;
             if (ok) {
 #pragma unroll
                 for (int c = 0; c < 8; ++c) {
                     const float4 o =
-                        *reinterpret_cast<const float4 *>(x_in + x_off(h, 8 * half + c));
+                        *reinterpret_cast<const float4 *>(x_in + x_half_off(half, h, c));
                     s_own[4 * c] += o.x;
                     s_own[4 * c + 1] += o.y;
                     s_own[4 * c + 2] += o.z;
