@@ -274,10 +274,24 @@ tile_attention_kernel(const __grid_constant__ TileParams p) {
                 __syncwarp();
                 if (lane == 0) mbar_arrive(&bar[kSFree + sb]);
                 const int nvis = lim - key0;         // keys of this half the row sees
+                if (p.qk_scale_log2 > 0.f) {
+                    // Raw scores stay in sc (masked keys -inf); the scale goes
+                    // into the exponent's FMA and, being positive, commutes
+                    // with the max.  Only tiles some row sees partly are masked.
+                    if (!__all_sync(0xffffffffu, nvis >= 64)) {
 #pragma unroll
-                for (int j = 0; j < 64; ++j) {
-                    sc[j] = j < nvis ? sc[j] * p.qk_scale_log2 : -INFINITY;
-                    mloc = fmaxf(mloc, sc[j]);
+                        for (int j = 0; j < 64; ++j) sc[j] = j < nvis ? sc[j] : -INFINITY;
+                    }
+                    float m4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+#pragma unroll
+                    for (int j = 0; j < 64; ++j) m4[j & 3] = fmaxf(m4[j & 3], sc[j]);
+                    mloc = fmaxf(fmaxf(m4[0], m4[1]), fmaxf(m4[2], m4[3])) * p.qk_scale_log2;
+                } else {
+#pragma unroll
+                    for (int j = 0; j < 64; ++j) {
+                        sc[j] = j < nvis ? sc[j] * p.qk_scale_log2 : -INFINITY;
+                        mloc = fmaxf(mloc, sc[j]);
+                    }
                 }
             }
             // ---- row max over both halves ------------------------------------
@@ -293,20 +307,27 @@ tile_attention_kernel(const __grid_constant__ TileParams p) {
                 alpha = fast_exp2(m_ref - mt);
                 m_ref = mt;
             }
-            const bool live = m_ref != -INFINITY;
+            // A row that has seen no key yet has m_ref = -inf and only -inf
+            // scores: exp2 of them against 0 gives the weights 0.
+            const float m_use = m_ref != -INFINITY ? m_ref : 0.f;
+            // Folded scale: raw scores times scale (positive) minus m_ref;
+            // otherwise sc already holds the scaled scores.
+            const bool folded = p.qk_scale_log2 > 0.f;
+            const float sc_mul = folded ? p.qk_scale_log2 : 1.f;
             // Two row sums: of the fp32 weights (for lse) and of the bf16-
             // rounded weights the MMA multiplies V by (to normalise O).
-            float rowsum = 0.f, rowsum_r = 0.f;
+            float rs[2] = {0.f, 0.f}, rr[2] = {0.f, 0.f};
             float pk[32];
 #pragma unroll
             for (int j = 0; j < 32; ++j) {
-                const float p0 = live ? fast_exp2(sc[2 * j] - m_ref) : 0.f;
-                const float p1 = live ? fast_exp2(sc[2 * j + 1] - m_ref) : 0.f;
+                const float p0 = fast_exp2(fmaf(sc[2 * j], sc_mul, -m_use));
+                const float p1 = fast_exp2(fmaf(sc[2 * j + 1], sc_mul, -m_use));
                 const uint32_t w = pack_bf16x2(p0, p1);
                 pk[j] = __uint_as_float(w);
-                rowsum += p0 + p1;
-                rowsum_r += bf16_lo(w) + bf16_hi(w);
+                rs[j & 1] += p0 + p1;
+                rr[j & 1] += bf16_lo(w) + bf16_hi(w);
             }
+            const float rowsum = rs[0] + rs[1], rowsum_r = rr[0] + rr[1];
             l = l * alpha + rowsum;
             l_r = l_r * alpha + rowsum_r;
 
