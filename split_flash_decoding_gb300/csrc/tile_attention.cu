@@ -68,6 +68,13 @@ enum Bar {
     kNumBars = kODone + 1
 };
 
+// max of three (one instruction on this architecture)
+__device__ __forceinline__ float fmax3(float a, float b, float c) {
+    float r;
+    asm("max.f32 %0, %1, %2, %3;" : "=f"(r) : "f"(a), "f"(b), "f"(c));
+    return r;
+}
+
 __global__ void __launch_bounds__(kThreads, 1)
 tile_attention_kernel(const __grid_constant__ TileParams p) {
     extern __shared__ uint8_t smem_raw[];
@@ -284,7 +291,8 @@ tile_attention_kernel(const __grid_constant__ TileParams p) {
                     }
                     float m4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
 #pragma unroll
-                    for (int j = 0; j < 64; ++j) m4[j & 3] = fmaxf(m4[j & 3], sc[j]);
+                    for (int j = 0; j < 64; j += 2)
+                        m4[(j >> 1) & 3] = fmax3(m4[(j >> 1) & 3], sc[j], sc[j + 1]);
                     mloc = fmaxf(fmaxf(m4[0], m4[1]), fmaxf(m4[2], m4[3])) * p.qk_scale_log2;
                 } else {
 #pragma unroll
@@ -316,18 +324,24 @@ tile_attention_kernel(const __grid_constant__ TileParams p) {
             const float sc_mul = folded ? p.qk_scale_log2 : 1.f;
             // Two row sums: of the fp32 weights (for lse) and of the bf16-
             // rounded weights the MMA multiplies V by (to normalise O).
-            float rs[2] = {0.f, 0.f}, rr[2] = {0.f, 0.f};
+            // Pairs of keys go through the packed fp32x2 FMA and adds.
+            const float2 mul2 = make_float2(sc_mul, sc_mul);
+            const float2 neg2 = make_float2(-m_use, -m_use);
+            float2 rs[2] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
+            float2 rr[2] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
             float pk[32];
 #pragma unroll
             for (int j = 0; j < 32; ++j) {
-                const float p0 = fast_exp2(fmaf(sc[2 * j], sc_mul, -m_use));
-                const float p1 = fast_exp2(fmaf(sc[2 * j + 1], sc_mul, -m_use));
+                const float2 e = __ffma2_rn(make_float2(sc[2 * j], sc[2 * j + 1]), mul2, neg2);
+                const float p0 = fast_exp2(e.x);
+                const float p1 = fast_exp2(e.y);
                 const uint32_t w = pack_bf16x2(p0, p1);
                 pk[j] = __uint_as_float(w);
-                rs[j & 1] += p0 + p1;
-                rr[j & 1] += bf16_lo(w) + bf16_hi(w);
+                rs[j & 1] = __fadd2_rn(rs[j & 1], make_float2(p0, p1));
+                rr[j & 1] = __fadd2_rn(rr[j & 1], make_float2(bf16_lo(w), bf16_hi(w)));
             }
-            const float rowsum = rs[0] + rs[1], rowsum_r = rr[0] + rr[1];
+            const float rowsum = (rs[0].x + rs[1].x) + (rs[0].y + rs[1].y);
+            const float rowsum_r = (rr[0].x + rr[1].x) + (rr[0].y + rr[1].y);
             l = l * alpha + rowsum;
             l_r = l_r * alpha + rowsum_r;
 
