@@ -19,8 +19,13 @@
 // raised, and O rescaled, only when a tile's max exceeds it by more than 8
 // (base 2).  No split-K: each CTA covers all keys its rows can see.
 //
-// Warp roles (320 threads): 0-7 softmax/epilogue, 8 TMA producer, 9 TMEM
-// allocation + MMA issue.
+// K and V have rings of their own (three 32 KB stages each): a K stage is
+// free again as soon as its score MMA is done, so the next K tiles load
+// while the softmax and P.V of earlier tiles run, and V tiles arrive for the
+// P.V MMA later.
+//
+// Warp roles (352 threads): 0-7 softmax/epilogue, 8 TMA producer of Q and K,
+// 9 TMA producer of V, 10 TMEM allocation + MMA issue.
 #include "launch.h"
 #include "ptx.cuh"
 #include "tc.cuh"
@@ -33,8 +38,7 @@ constexpr int kBN = kTileKeys;               // keys per tile
 constexpr int kStages = 3;
 constexpr int kBoxBytes = 128 * 128;         // 128 rows x 128 B (64 channels)
 constexpr int kTileBytes = 2 * kBoxBytes;    // 128 rows x 128 channels
-constexpr int kStageBytes = 2 * kTileBytes;  // K + V
-constexpr int kThreads = 320;
+constexpr int kThreads = 352;
 constexpr int kSoftmaxThreads = 256;         // warps 0-7
 constexpr int kBarSoftmax = 1;               // named barrier of the softmax warps
 constexpr uint32_t kTmemCols = 512;
@@ -50,17 +54,20 @@ constexpr uint32_t kVSbo = 1024;
 
 struct Smem {
     static constexpr int q = 0;                                  // 32 KB
-    static constexpr int kv = q + kTileBytes;                    // 128 KB
-    static constexpr int red = kv + kStages * kStageBytes;       // 192 KB
+    static constexpr int k = q + kTileBytes;                     // K ring, 96 KB
+    static constexpr int v = k + kStages * kTileBytes;           // V ring, 96 KB
+    static constexpr int red = v + kStages * kTileBytes;
     static constexpr int bars = red + 2 * 128 * 4;               // +1 KB (row maxima)
     static constexpr int total = bars + 256;
 };
 constexpr size_t kSmemBytes = Smem::total + 1024;
 
 enum Bar {
-    kKvFull = 0,                  // [kStages]
-    kKvEmpty = kStages,           // [kStages]
-    kQFull = 2 * kStages,
+    kKFull = 0,                   // [kStages]
+    kKEmpty = kStages,            // [kStages]
+    kVFull = 2 * kStages,         // [kStages]
+    kVEmpty = 3 * kStages,        // [kStages]
+    kQFull = 4 * kStages,
     kSFull = kQFull + 1,          // [2]
     kSFree = kSFull + 2,          // [2]
     kPFull = kSFree + 2,
@@ -110,7 +117,7 @@ tile_attention_kernel(const __grid_constant__ TileParams p) {
         }
         fence_mbar_init();
     }
-    if (warp == 9) {
+    if (warp == 10) {
         tc::tmem_alloc(tmem_slot, kTmemCols);
         tc::tmem_relinquish();
     }
@@ -119,17 +126,24 @@ tile_attention_kernel(const __grid_constant__ TileParams p) {
     tc::fence_after_sync();
     const uint32_t tmem = *tmem_slot;
 
-    if (warp == 8) {
-        // ------------------------------------------------------------ producer
+    if (warp == 8 || warp == 9) {
+        // ------------------------------------------------------------ producers
+        // warp 8: Q, then the K ring; warp 9: the V ring.
+        const bool is_k = warp == 8;
+        const CUtensorMap *map = is_k ? &p.k_map : &p.v_map;
+        uint8_t *ring = smem + (is_k ? Smem::k : Smem::v);
+        uint64_t *full = &bar[is_k ? kKFull : kVFull];
+        uint64_t *empty = &bar[is_k ? kKEmpty : kVEmpty];
         if (ntiles > 0) {
             if (lane == 0) {
-                prefetch_tensormap(&p.q_map);
-                prefetch_tensormap(&p.k_map);
-                prefetch_tensormap(&p.v_map);
-                mbar_arrive_expect_tx(&bar[kQFull], kTileBytes);
-                for (int cb = 0; cb < 2; ++cb)
-                    tma_load_4d(smem + Smem::q + cb * kBoxBytes, &p.q_map, &bar[kQFull], cb * 64,
-                                0, kvh, q_off + t0);
+                prefetch_tensormap(map);
+                if (is_k) {
+                    prefetch_tensormap(&p.q_map);
+                    mbar_arrive_expect_tx(&bar[kQFull], kTileBytes);
+                    for (int cb = 0; cb < 2; ++cb)
+                        tma_load_4d(smem + Smem::q + cb * kBoxBytes, &p.q_map, &bar[kQFull],
+                                    cb * 64, 0, kvh, q_off + t0);
+                }
             }
             const int box_rows = p.box_rows;       // 128, 64, 32, 16 or 8
             const int nb = kBN / box_rows;         // row boxes per key tile
@@ -141,17 +155,15 @@ tile_attention_kernel(const __grid_constant__ TileParams p) {
                 const int live = min(nb, (L - key0 + box_rows - 1) / box_rows);
                 const int s = i % kStages;
                 if (lane == 0) {
-                    if (i >= kStages &&
-                        !mbar_wait(&bar[kKvEmpty + s], ((i / kStages) - 1) & 1, p.err))
+                    if (i >= kStages && !mbar_wait(&empty[s], ((i / kStages) - 1) & 1, p.err))
                         aborted = true;
                     else
-                        mbar_arrive_expect_tx(&bar[kKvFull + s],
-                                              uint32_t(live) * 2u * 2u * uint32_t(box_rows) * 128u);
+                        mbar_arrive_expect_tx(&full[s],
+                                              uint32_t(live) * 2u * uint32_t(box_rows) * 128u);
                 }
                 aborted = __shfl_sync(0xffffffffu, aborted, 0);
                 if (aborted) break;
-                uint8_t *ks = smem + Smem::kv + s * kStageBytes;
-                uint8_t *vs = ks + kTileBytes;
+                uint8_t *st = ring + s * kTileBytes;
                 for (int r = 0; r < live; ++r) {
                     const int g = i * nb + r;      // box index within the sequence
                     if ((g >> 5) != cached) {      // warp-uniform refill of 32 lookups
@@ -181,16 +193,12 @@ tile_attention_kernel(const __grid_constant__ TileParams p) {
                     if (lane == 0) {
                         if (page < 0) {
                             // a skipped (bad-page) box: retire its expected bytes
-                            mbar_complete_tx(&bar[kKvFull + s], 2u * 2u * uint32_t(box_rows) * 128u);
+                            mbar_complete_tx(&full[s], 2u * uint32_t(box_rows) * 128u);
                         } else {
 #pragma unroll
-                            for (int cb = 0; cb < 2; ++cb) {
-                                const int off = cb * kBoxBytes + r * box_rows * 128;
-                                tma_load_4d(ks + off, &p.k_map, &bar[kKvFull + s], cb * 64, slot,
-                                            kvh, page);
-                                tma_load_4d(vs + off, &p.v_map, &bar[kKvFull + s], cb * 64, slot,
-                                            kvh, page);
-                            }
+                            for (int cb = 0; cb < 2; ++cb)
+                                tma_load_4d(st + cb * kBoxBytes + r * box_rows * 128, map, &full[s],
+                                            cb * 64, slot, kvh, page);
                         }
                     }
                 }
@@ -198,45 +206,48 @@ tile_attention_kernel(const __grid_constant__ TileParams p) {
             }
             // every copy this warp issued must land before the CTA may leave
             if (lane == 0) {
-                mbar_wait(&bar[kQFull], 0, p.err);
+                if (is_k) mbar_wait(&bar[kQFull], 0, p.err);
                 for (int i = max(0, issued - kStages); i < issued; ++i)
-                    mbar_wait(&bar[kKvFull + i % kStages], (i / kStages) & 1, p.err);
+                    mbar_wait(&full[i % kStages], (i / kStages) & 1, p.err);
             }
         }
-    } else if (warp == 9) {
+    } else if (warp == 10) {
         // ------------------------------------------------------------ MMA issue
         if (ntiles > 0 && lane == 0) {
             constexpr uint32_t idesc_s = tc::idesc_bf16_f32(128, kBN, 0, 0);
             constexpr uint32_t idesc_o = tc::idesc_bf16_f32(128, kD, 0, 1);
             const uint32_t q_base = smem_addr(smem + Smem::q);
-            const uint32_t kv_base = smem_addr(smem + Smem::kv);
+            const uint32_t k_base = smem_addr(smem + Smem::k);
+            const uint32_t v_base = smem_addr(smem + Smem::v);
             bool ok = mbar_wait(&bar[kQFull], 0, p.err);
             for (int t = 0; ok && t <= ntiles; ++t) {
                 if (t < ntiles) {
                     const int s = t % kStages;
                     const int sb = t & 1;
-                    ok = mbar_wait(&bar[kKvFull + s], (t / kStages) & 1, p.err);
+                    ok = mbar_wait(&bar[kKFull + s], (t / kStages) & 1, p.err);
                     if (ok && t >= 2) ok = mbar_wait(&bar[kSFree + sb], ((t >> 1) - 1) & 1, p.err);
                     if (!ok) break;
                     tc::fence_after_sync();
                     // Descriptors advance by byte offset / 16 in their start
                     // field; unrolled so issue is not bound by descriptor math.
                     const uint64_t qd = tc::smem_desc_sw128(q_base, 16, 1024);
-                    const uint64_t kd = tc::smem_desc_sw128(kv_base + s * kStageBytes, 16, 1024);
+                    const uint64_t kd = tc::smem_desc_sw128(k_base + s * kTileBytes, 16, 1024);
 #pragma unroll
                     for (int kk = 0; kk < kD / 16; ++kk) {
                         const uint64_t off = uint64_t(((kk >> 2) * kBoxBytes + (kk & 3) * 32) >> 4);
                         tc::mma_bf16(tmem + kTmemS + sb * kBN, qd + off, kd + off, idesc_s, kk > 0);
                     }
                     tc::mma_commit(&bar[kSFull + sb]);
+                    tc::mma_commit(&bar[kKEmpty + s]);
                 }
                 if (t >= 1) {
                     const int tp = t - 1;
                     ok = mbar_wait(&bar[kPFull], tp & 1, p.err);
+                    if (ok) ok = mbar_wait(&bar[kVFull + tp % kStages], (tp / kStages) & 1, p.err);
                     if (!ok) break;
                     tc::fence_after_sync();
-                    const uint64_t vd = tc::smem_desc_sw128(
-                        kv_base + (tp % kStages) * kStageBytes + kTileBytes, kVLbo, kVSbo);
+                    const uint64_t vd = tc::smem_desc_sw128(v_base + (tp % kStages) * kTileBytes,
+                                                            kVLbo, kVSbo);
 #pragma unroll
                     for (int kk = 0; kk < kBN / 16; ++kk)
                         // A = P from TMEM: 16 keys = 8 columns of bf16 pairs per step
@@ -244,7 +255,7 @@ tile_attention_kernel(const __grid_constant__ TileParams p) {
                                             vd + uint64_t((kk * 16 * 128) >> 4), idesc_o,
                                             tp > 0 || kk > 0);
                     tc::mma_commit(&bar[kODone]);
-                    tc::mma_commit(&bar[kKvEmpty + (tp % kStages)]);
+                    tc::mma_commit(&bar[kVEmpty + (tp % kStages)]);
                 }
             }
         }
@@ -367,8 +378,12 @@ tile_attention_kernel(const __grid_constant__ TileParams p) {
             tc::tmem_st32(tmem + lane_base + kTmemP + 32u * half, pk);
             const int nkeys = min(kBN, L - t * kBN);
             if (nkeys < kBN) {
-                // Slots past the sequence end may hold anything: zero them in V.
-                uint8_t *vs = smem + Smem::kv + (t % kStages) * kStageBytes + kTileBytes;
+                // Slots past the sequence end may hold anything: zero them in V,
+                // once the V tile has landed.
+                ok = __all_sync(0xffffffffu,
+                                mbar_wait(&bar[kVFull + t % kStages], (t / kStages) & 1, p.err));
+                if (!ok) continue;
+                uint8_t *vs = smem + Smem::v + (t % kStages) * kTileBytes;
                 const int per_box = (kBN - nkeys) * 8;          // 16-B chunks
                 for (int i = threadIdx.x; i < 2 * per_box; i += kSoftmaxThreads) {
                     const int box = i / per_box;
@@ -438,7 +453,7 @@ tile_attention_kernel(const __grid_constant__ TileParams p) {
 
     tc::fence_before_sync();
     __syncthreads();
-    if (warp == 9) {
+    if (warp == 10) {
         tc::fence_after_sync();
         tc::tmem_dealloc(tmem, kTmemCols);
     }
