@@ -50,10 +50,16 @@ KERNEL_SOURCES = {
 }
 
 
+def few_token(w) -> bool:
+    """A few rows per sequence run split-K on the decode kernel."""
+    return (w.max_q_len > 1 and w.dim_qk == 128 and w.max_q_len * w.group <= 16
+            and w.batch <= 2048)
+
+
 def dominant_kernel(w) -> str:
     if w.is_mla:
         return "mla_decode"
-    if w.max_q_len > 1:
+    if w.max_q_len > 1 and not few_token(w):
         return "tile_attention"
     return "gqa_decode_tc" if w.dim_qk == 128 else "gqa_decode"
 
@@ -65,7 +71,7 @@ def parse():
     ap.add_argument("--warmup", type=int, default=50)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default="llama3",
-                    choices=["llama3", "long_context", "mla", "mixed", "tiny"])
+                    choices=["llama3", "long_context", "mla", "mixed", "few_token", "tiny"])
     ap.add_argument("--partitions", type=int, default=0, help="0 = planner's choice")
     ap.add_argument("--batch", type=int, default=0,
                     help="override the batch of the llama3 / mla workloads (profiling captures)")
@@ -180,6 +186,8 @@ def build_workload(name: str, device, batch: int = 0):
         return W.deepseek_v3_mla_decode(device=device, **({"batch": batch} if batch else {}))
     if name == "mixed":
         return W.mixed_prefill_decode(device=device)
+    if name == "few_token":
+        return W.few_token_decode(device=device, **({"batch": batch} if batch else {}))
     if name == "tiny":
         return W.tiny_decode(device=device)
     raise ValueError(name)
@@ -343,7 +351,7 @@ def run_ours(args, rank, world, dist):
     if w.is_mla:
         P, ws_bytes = attn.attn_plan_partitions(w.batch, w.rows, w.num_q_heads, 1, w.dim_v,
                                                 w.max_kv_len, args.partitions)
-    elif w.max_q_len > 1:
+    elif w.max_q_len > 1 and not few_token(w):
         P, ws_bytes = 1, 0
     else:
         P, ws_bytes = attn.attn_plan_partitions(w.batch, w.rows, w.num_q_heads,

@@ -170,6 +170,13 @@ def _workspace(nbytes: int, device, workspace: Optional[torch.Tensor]):
     return workspace, workspace.numel() * workspace.element_size()
 
 
+def few_token_split(max_q_len: int, group: int, head_dim: int, batch: int) -> bool:
+    """True when attn_decode folds the rows of each sequence onto the decode
+    kernel (and may split K): head_dim 128, max_q_len * group <= 16, batch
+    within the decode kernel's limit.  Mirrors the library's routing."""
+    return max_q_len > 1 and head_dim == 128 and max_q_len * group <= 16 and batch <= 2048
+
+
 def attn_decode(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tensor,
                 kv_len: torch.Tensor, *, group: int, scale: float, max_kv_len: int,
                 page_table: Optional[torch.Tensor] = None, sink: Optional[torch.Tensor] = None,
@@ -183,7 +190,9 @@ def attn_decode(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tensor,
     decode, else q_row_offsets[-1]); caches as for kv_descriptor; kv_len
     int32/uint32 [batch] on the device; q_row_offsets int32 [batch + 1] on
     the device or None; sink fp32 [num_q_heads] or None.  num_partitions 0
-    plans automatically (always 1 when max_q_len > 1).  Returns (out, lse).
+    plans automatically.  A few rows per sequence (max_q_len * group <= 16,
+    head_dim 128) run split-K on the decode kernel; longer row runs take the
+    tile kernel, which is not split (P = 1).  Returns (out, lse).
     """
     rows, hq, d = q.shape
     batch = kv_len.shape[0]
@@ -191,7 +200,7 @@ def attn_decode(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tensor,
         out = torch.empty((rows, hq, d), dtype=torch.bfloat16, device=q.device)
     if lse is None and return_lse:
         lse = torch.empty((rows, hq), dtype=torch.float32, device=q.device)
-    if max_q_len > 1:
+    if max_q_len > 1 and not few_token_split(max_q_len, group, d, batch):
         P, ws_bytes = 1, 0
     else:
         P, ws_bytes = attn_plan_partitions(batch, rows, hq, hq // group, d, max_kv_len,

@@ -287,14 +287,18 @@ extern "C" int attn_decode(const void *q, const attn_kv_t *k, const attn_kv_t *v
     if (!q_row_offsets && (num_q_rows != batch || max_q_len != 1)) return ATTN_ERR_INVALID_ARG;
     if (batch == 0 || num_q_rows == 0) return ATTN_OK;
     if (!q || !kv_len || !out) return ATTN_ERR_INVALID_ARG;
-    if (max_q_len > 1) {
-        // Tensor-core tile path for multi-row sequences (not split).
+    // A few rows per sequence (max_q_len * group <= 16, head_dim 128) fold
+    // onto the N side of the tensor-core decode kernel, split-K included;
+    // longer row runs take the tensor-core tile path (not split).
+    const bool fold = max_q_len > 1 && head_dim == 128 && max_q_len * group <= 16 &&
+                      batch <= kGqaMaxBatch;
+    if (max_q_len > 1 && !fold) {
         if (num_partitions != 1) return ATTN_ERR_UNSUPPORTED;
         return prefill_path(q, k, v, kv_len, q_row_offsets, batch, num_q_rows, num_q_heads,
                             group, head_dim, max_q_len, max_kv_len, scale, sink, causal, out,
                             lse, stream);
     }
-    if (q_row_offsets && num_q_rows != batch) return ATTN_ERR_INVALID_ARG;
+    if (!fold && q_row_offsets && num_q_rows != batch) return ATTN_ERR_INVALID_ARG;
     if (batch > kGqaMaxBatch) return ATTN_ERR_UNSUPPORTED;
     if (group != 1 && group != 2 && group != 4 && group != 8) return ATTN_ERR_UNSUPPORTED;
     if (head_dim != 64 && head_dim != 128) return ATTN_ERR_UNSUPPORTED;
@@ -310,8 +314,8 @@ extern "C" int attn_decode(const void *q, const attn_kv_t *k, const attn_kv_t *v
         return ATTN_ERR_UNSUPPORTED;
 
     size_t off_m = 0, off_l = 0;
-    const size_t need = workspace_layout(num_partitions, batch, num_q_heads, head_dim, &off_m,
-                                         &off_l);
+    const size_t need = workspace_layout(num_partitions, num_q_rows, num_q_heads, head_dim,
+                                         &off_m, &off_l);
     if (num_partitions > 1) {
         if (!workspace || workspace_bytes < need) return ATTN_ERR_WORKSPACE;
         if (reinterpret_cast<uintptr_t>(workspace) % 256) return ATTN_ERR_WORKSPACE;
@@ -329,13 +333,15 @@ extern "C" int attn_decode(const void *q, const attn_kv_t *k, const attn_kv_t *v
     st = encode_kv_map(&p.v_map, *v, head_dim, hkv, p.box_rows);
     if (st) return st;
     if (tc) {
+        // Q as (channel, head, query row); one box = the group's heads of
+        // max_q_len consecutive rows (rows past the tensor read as zero).
         EncodeTiledFn fn = encode_fn();
         if (!fn) return ATTN_ERR_CUDA;
-        cuuint64_t gdim[2] = {128, cuuint64_t(batch) * cuuint64_t(num_q_heads)};
-        cuuint64_t gstride[1] = {128 * 2};
-        cuuint32_t box[2] = {64, cuuint32_t(group)};
-        cuuint32_t estride[2] = {1, 1};
-        CUresult r = fn(&p.q_map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void *>(q),
+        cuuint64_t gdim[3] = {128, cuuint64_t(num_q_heads), cuuint64_t(num_q_rows)};
+        cuuint64_t gstride[2] = {128 * 2, cuuint64_t(num_q_heads) * 128 * 2};
+        cuuint32_t box[3] = {64, cuuint32_t(group), cuuint32_t(max_q_len)};
+        cuuint32_t estride[3] = {1, 1, 1};
+        CUresult r = fn(&p.q_map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void *>(q),
                         gdim, gstride, box, estride, CU_TENSOR_MAP_INTERLEAVE_NONE,
                         CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                         CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
@@ -346,6 +352,7 @@ extern "C" int attn_decode(const void *q, const attn_kv_t *k, const attn_kv_t *v
 
     p.q = static_cast<const uint16_t *>(q);
     p.kv_len = kv_len;
+    p.q_row_offsets = fold ? q_row_offsets : nullptr;
     p.page_table = k->page_table;
     p.sink = sink;
     if (num_partitions > 1) {
@@ -357,6 +364,9 @@ extern "C" int attn_decode(const void *q, const attn_kv_t *k, const attn_kv_t *v
     p.out = static_cast<uint16_t *>(out);
     p.lse = lse;
     p.batch = batch;
+    p.num_q_rows = fold ? num_q_rows : batch;
+    p.max_q_len = fold ? max_q_len : 1;
+    p.causal = causal ? 1 : 0;
     p.num_q_heads = num_q_heads;
     p.group = group;
     p.head_dim = head_dim;
@@ -380,8 +390,10 @@ extern "C" int attn_decode(const void *q, const attn_kv_t *k, const attn_kv_t *v
     r.out = p.out;
     r.lse = lse;
     r.kv_len = kv_len;
+    r.q_row_offsets = p.q_row_offsets;
+    r.batch = batch;
     r.num_partitions = num_partitions;
-    r.rows = batch;
+    r.rows = p.num_q_rows;
     r.num_q_heads = num_q_heads;
     r.dim_v = head_dim;
     r.chunk = p.chunk;

@@ -15,6 +15,12 @@
 // makes Q.K' and P.V dense contractions of depth 128 over 128 keys; only the
 // N side is padded.
 //
+// Few-token decode (n <= 16 / group query rows per sequence, e.g. draft
+// tokens) folds the rows onto N as well: column c = (row i = c / group, head
+// h = c % group), one TMA box of (64 channels x group heads x n rows) per Q
+// half, and a per-column causal limit (row i of n sees keys j <= L - n + i).
+// An item still covers all keys of a slice once for all the rows.
+//
 // Warp roles (224 threads): warps 0-3 softmax and epilogue, warp 4 streams
 // K tiles and the item's Q (TMA), warp 5 streams V tiles (TMA), warp 6 owns
 // TMEM and issues the MMAs.  Rings: 3 K stages and 3 V stages of 32 KB, each
@@ -50,14 +56,61 @@ constexpr uint32_t kTmemCols = 64;
 constexpr uint32_t kTmemS = 0;               // two 16-column score buffers
 constexpr uint32_t kTmemO = 32;              // 16-column output accumulator
 
+// 3-D tiled TMA load (Q: channel, head, query row).
+__device__ __forceinline__ void tma_load_3d(void *dst, const CUtensorMap *map, uint64_t *bar,
+                                            int c0, int c1, int c2) {
+    asm volatile(
+        "cp.async.bulk.tensor.3d.shared::cta.global.tile.mbarrier::complete_tx::bytes"
+        " [%0], [%1, {%2, %3, %4}], [%5];" ::"r"(smem_addr(dst)),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(c2), "r"(smem_addr(bar))
+        : "memory");
+}
+
+// N consecutive TMEM columns of the thread's lane (N = 1, 2, 4, 8 or 16).
+template <int N>
+__device__ __forceinline__ void tmem_ld_cols(uint32_t taddr, float (&v)[N]) {
+    if constexpr (N == 16) {
+        float a[8], b[8];
+        tc::tmem_ld_n<8>(taddr, a);
+        tc::tmem_ld_n<8>(taddr + 8, b);
+#pragma unroll
+        for (int i = 0; i < 8; ++i) { v[i] = a[i]; v[8 + i] = b[i]; }
+    } else {
+        tc::tmem_ld_n<N>(taddr, v);
+    }
+}
+template <int N>
+__device__ __forceinline__ void tmem_st_cols(uint32_t taddr, const float (&v)[N]) {
+    if constexpr (N == 16) {
+        float a[8], b[8];
+#pragma unroll
+        for (int i = 0; i < 8; ++i) { a[i] = v[i]; b[i] = v[8 + i]; }
+        tc::tmem_st_n<8>(taddr, a);
+        tc::tmem_st_n<8>(taddr + 8, b);
+    } else {
+        tc::tmem_st_n<N>(taddr, v);
+    }
+}
+
+// First query row and row count of sequence b.
+__device__ __forceinline__ void seq_rows(const GqaParams &p, int b, int &row0, int &nrows) {
+    if (p.q_row_offsets) {
+        row0 = int(p.q_row_offsets[b]);
+        nrows = int(p.q_row_offsets[b + 1]) - row0;
+    } else {
+        row0 = b;
+        nrows = 1;
+    }
+}
+
 struct Smem {
     static constexpr int kring = 0;
     static constexpr int vring = kring + kStages * kTileBytes;
     static constexpr int q = vring + kStages * kTileBytes;     // [2] Q^T buffers
     static constexpr int p = q + 2 * kNBytes;                   // P^T
     static constexpr int red = p + kNBytes;                     // float [2][4][16] tile max
-    static constexpr int lred = red + 2 * 4 * 16 * 4;           // float [2][4][16] row sums
-    static constexpr int bars = lred + 2 * 4 * 16 * 4;
+    static constexpr int lred = red + 2 * 4 * 16 * 4;           // float [2][4][2][16] row sums
+    static constexpr int bars = lred + 2 * 4 * 2 * 16 * 4;
     static constexpr int items = bars + 256;
 };
 
@@ -108,11 +161,15 @@ __device__ __forceinline__ void produce(const GqaParams &p, const int *cum, int 
             if (itq >= 2 && !mbar_wait(&bar[kQEmpty + qb], ((itq >> 1) - 1) & 1, p.err)) {
                 aborted = true;
             } else {
-                mbar_arrive_expect_tx(&bar[kQFull + qb], 2u * uint32_t(G) * 128u);
+                // rows past the sequence (or the tensor) are masked columns
+                int row0, nrows;
+                seq_rows(p, it.b, row0, nrows);
+                mbar_arrive_expect_tx(&bar[kQFull + qb],
+                                      2u * uint32_t(G) * uint32_t(p.max_q_len) * 128u);
                 uint8_t *qs = smem + Smem::q + qb * kNBytes;
                 for (int cb = 0; cb < 2; ++cb)
-                    tma_load_2d(qs + cb * kNBox, &p.q_map, &bar[kQFull + qb], cb * 64,
-                                it.b * p.num_q_heads + it.kvh * G);
+                    tma_load_3d(qs + cb * kNBox, &p.q_map, &bar[kQFull + qb], cb * 64,
+                                it.kvh * G, row0);
             }
         }
         aborted = __shfl_sync(0xffffffffu, aborted, 0);
@@ -182,7 +239,9 @@ __device__ __forceinline__ void produce(const GqaParams &p, const int *cum, int 
     }
 }
 
-template <int G>
+// G: query heads per KV head; NC: score columns (G for one row per sequence,
+// 16 for the few-token fold).
+template <int G, int NC>
 __global__ void __launch_bounds__(kThreads, 1)
 gqa_decode_tc_kernel(const __grid_constant__ GqaParams p) {
     extern __shared__ uint8_t smem_raw[];
@@ -208,7 +267,8 @@ gqa_decode_tc_kernel(const __grid_constant__ GqaParams p) {
         tc::tmem_alloc(tmem_slot, kTmemCols);
         tc::tmem_relinquish();
     }
-    // Padding rows of the Q^T and P^T operands (heads G..15) stay zero.
+    // Padding rows of the Q^T and P^T operands (columns past the loaded
+    // rows) stay zero.
     for (int i = threadIdx.x; i < (3 * kNBytes) / 16; i += kThreads)
         reinterpret_cast<uint4 *>(smem + Smem::q)[i] = make_uint4(0u, 0u, 0u, 0u);
     tc::fence_async_smem();
@@ -299,12 +359,21 @@ gqa_decode_tc_kernel(const __grid_constant__ GqaParams p) {
         bool ok = true;
         for (int j = blockIdx.x; j < num_items; j += gridDim.x) {
             const GqaItem it = gqa_item<kBK>(p, cum, j, hkv);
-            float m[G], l[G], lr[G];
+            int row0, nrows;
+            seq_rows(p, it.b, row0, nrows);
+            // Column c = (row c / G, head c % G): keys j < lim[c] are visible.
+            int lim[NC];
 #pragma unroll
-            for (int h = 0; h < G; ++h) {
-                m[h] = -INFINITY;
-                l[h] = 0.f;
-                lr[h] = 0.f;
+            for (int c = 0; c < NC; ++c) {
+                const int i = c / G;
+                lim[c] = i >= nrows ? 0 : (p.causal ? it.L - nrows + i + 1 : it.L);
+            }
+            float m[NC], l[NC], lr[NC];
+#pragma unroll
+            for (int c = 0; c < NC; ++c) {
+                m[c] = -INFINITY;
+                l[c] = 0.f;
+                lr[c] = 0.f;
             }
             // Every warp runs every named barrier of every tile, even after a
             // wait gave up (ok == false), so no warp can strand the others.
@@ -315,40 +384,42 @@ gqa_decode_tc_kernel(const __grid_constant__ GqaParams p) {
                 const int nvalid = min(kBK, it.end - t0);
                 ok = ok && mbar_wait(&bar[kSFull + sb], (gg >> 1) & 1, p.err);
                 tc::fence_after_sync();
-                float s[G];
-                tc::tmem_ld_n<G>(tmem + lane_base + kTmemS + sb * kNRows, s);
+                float s[NC];
+                tmem_ld_cols<NC>(tmem + lane_base + kTmemS + sb * kNRows, s);
                 tc::fence_before_sync();
                 __syncwarp();
                 if (lane == 0) mbar_arrive(&bar[kSFree + sb]);
 
-                // ---- tile max per head across the four warps -----------------
+                // ---- tile max per column across the four warps ---------------
                 const bool valid = k < nvalid;
                 float *rb = red + (gg & 1) * 64;
 #pragma unroll
-                for (int h = 0; h < G; ++h) {
-                    s[h] = valid ? s[h] * p.qk_scale_log2 : -INFINITY;
-                    const float wm = warp_max(s[h]);
-                    if (lane == 0) rb[warp * 16 + h] = wm;
+                for (int c = 0; c < NC; ++c) {
+                    s[c] = valid && t0 + k < lim[c] ? s[c] * p.qk_scale_log2 : -INFINITY;
+                    const float wm = warp_max(s[c]);
+                    if (lane == 0) rb[warp * 16 + c] = wm;
                 }
                 named_sync(1, 128);
-                float alpha[G];
+                float alpha[NC];
                 bool moved = false;
 #pragma unroll
-                for (int h = 0; h < G; ++h) {
-                    const float tmax = fmaxf(fmaxf(rb[h], rb[16 + h]), fmaxf(rb[32 + h], rb[48 + h]));
-                    const float mn = fmaxf(m[h], tmax);   // finite: key 0 of the tile is valid
-                    alpha[h] = fast_exp2(m[h] - mn);      // 0 on the first tile
-                    moved |= mn != m[h];
-                    m[h] = mn;
+                for (int c = 0; c < NC; ++c) {
+                    const float tmax = fmaxf(fmaxf(rb[c], rb[16 + c]), fmaxf(rb[32 + c], rb[48 + c]));
+                    const float mn = fmaxf(m[c], tmax);
+                    // A column with no visible key so far keeps m = -inf and
+                    // weights 0 (its alpha is irrelevant: l and O are 0).
+                    alpha[c] = mn == -INFINITY ? 1.f : fast_exp2(m[c] - mn);   // 0 on the first
+                    moved |= mn != m[c];
+                    m[c] = mn;
                 }
-                uint16_t pb[G];
+                uint16_t pb[NC];
 #pragma unroll
-                for (int h = 0; h < G; ++h) {
-                    const float pv = valid ? fast_exp2(s[h] - m[h]) : 0.f;
+                for (int c = 0; c < NC; ++c) {
+                    const float pv = s[c] != -INFINITY ? fast_exp2(s[c] - m[c]) : 0.f;
                     const uint32_t packed = pack_bf16x2(pv, 0.f);
-                    pb[h] = static_cast<uint16_t>(packed & 0xffffu);
-                    l[h] = l[h] * alpha[h] + pv;
-                    lr[h] = lr[h] * alpha[h] + bf16_lo(packed);
+                    pb[c] = static_cast<uint16_t>(packed & 0xffffu);
+                    l[c] = l[c] * alpha[c] + pv;
+                    lr[c] = lr[c] * alpha[c] + bf16_lo(packed);
                 }
                 if (t >= 1) {
                     // O^T(t-1) is complete: P^T may be overwritten and O^T
@@ -356,17 +427,17 @@ gqa_decode_tc_kernel(const __grid_constant__ GqaParams p) {
                     ok = ok && mbar_wait(&bar[kODone], (gg - 1) & 1, p.err);
                     tc::fence_after_sync();
                     if (moved) {   // identical in every thread
-                        float o[G];
-                        tc::tmem_ld_n<G>(tmem + lane_base + kTmemO, o);
+                        float o[NC];
+                        tmem_ld_cols<NC>(tmem + lane_base + kTmemO, o);
 #pragma unroll
-                        for (int h = 0; h < G; ++h) o[h] *= alpha[h];
-                        tc::tmem_st_n<G>(tmem + lane_base + kTmemO, o);
+                        for (int c = 0; c < NC; ++c) o[c] *= alpha[c];
+                        tmem_st_cols<NC>(tmem + lane_base + kTmemO, o);
                         tc::tmem_wait_st();
                     }
                 }
 #pragma unroll
-                for (int h = 0; h < G; ++h)
-                    *reinterpret_cast<uint16_t *>(pbuf + n_operand_offset(h, k)) = pb[h];
+                for (int c = 0; c < NC; ++c)
+                    *reinterpret_cast<uint16_t *>(pbuf + n_operand_offset(c, k)) = pb[c];
                 if (t0 + kBK > it.L) {
                     // Slots past the sequence end may hold anything (even NaN):
                     // zero them in the V stage before P.V reads it.
@@ -392,61 +463,65 @@ gqa_decode_tc_kernel(const __grid_constant__ GqaParams p) {
                 ok = mbar_wait(&bar[kODone], (g + it.ntiles - 1) & 1, p.err);
                 tc::fence_after_sync();
             }
-            float lsum[G], lrsum[G];
+            float lsum[NC], lrsum[NC];
             {
-                float *lb = lred + (j / gridDim.x & 1) * 64;
+                float *lb = lred + (j / gridDim.x & 1) * 128;   // [4 warps][2][16]
 #pragma unroll
-                for (int h = 0; h < G; ++h) {
-                    const float a = warp_sum(l[h]);
-                    const float b = warp_sum(lr[h]);
+                for (int c = 0; c < NC; ++c) {
+                    const float a = warp_sum(l[c]);
+                    const float b2 = warp_sum(lr[c]);
                     if (lane == 0) {
-                        lb[warp * 16 + h] = a;
-                        lb[warp * 16 + 8 + h] = b;
+                        lb[warp * 32 + c] = a;
+                        lb[warp * 32 + 16 + c] = b2;
                     }
                 }
                 named_sync(1, 128);
 #pragma unroll
-                for (int h = 0; h < G; ++h) {
-                    lsum[h] = (lb[h] + lb[16 + h]) + (lb[32 + h] + lb[48 + h]);
-                    lrsum[h] = (lb[8 + h] + lb[24 + h]) + (lb[40 + h] + lb[56 + h]);
+                for (int c = 0; c < NC; ++c) {
+                    lsum[c] = (lb[c] + lb[32 + c]) + (lb[64 + c] + lb[96 + c]);
+                    lrsum[c] = (lb[16 + c] + lb[48 + c]) + (lb[80 + c] + lb[112 + c]);
                 }
             }
-            float o[G];
+            float o[NC];
             if (ok && it.ntiles > 0) {
-                tc::tmem_ld_n<G>(tmem + lane_base + kTmemO, o);
+                tmem_ld_cols<NC>(tmem + lane_base + kTmemO, o);
             } else {
 #pragma unroll
-                for (int h = 0; h < G; ++h) o[h] = 0.f;
+                for (int c = 0; c < NC; ++c) o[c] = 0.f;
             }
             tc::fence_before_sync();
-            const int c = k;   // output channel of this thread
+            const int ch = k;   // output channel of this thread
 #pragma unroll
-            for (int h = 0; h < G; ++h) {
+            for (int c = 0; c < NC; ++c) {
+                const int i = c / G, h = c % G;
+                if (i >= nrows) continue;
                 const int hq = it.kvh * G + h;
+                const size_t row = size_t(row0 + i);
                 if (it.direct) {
                     const float t2 = p.sink ? p.sink[hq] * kLog2e : -INFINITY;
-                    const float Mf = fmaxf(m[h], t2);
+                    const float Mf = fmaxf(m[c], t2);
                     float Z = 0.f, Zr = 0.f, so = 0.f;
                     if (Mf != -INFINITY) {
-                        so = fast_exp2(m[h] - Mf);
+                        so = fast_exp2(m[c] - Mf);     // 0 when m = -inf
                         const float st = fast_exp2(t2 - Mf);
-                        Z = lsum[h] * so + st;
-                        Zr = lrsum[h] * so + st;
+                        Z = lsum[c] * so + st;
+                        Zr = lrsum[c] * so + st;
                     }
                     const float scale_o = Zr > 0.f ? so / Zr : 0.f;
-                    const uint32_t packed = pack_bf16x2(o[h] * scale_o, 0.f);
-                    p.out[(size_t(it.b) * p.num_q_heads + hq) * kD + c] =
+                    const uint32_t packed = pack_bf16x2(o[c] * scale_o, 0.f);
+                    p.out[(row * p.num_q_heads + hq) * kD + ch] =
                         static_cast<uint16_t>(packed & 0xffffu);
-                    if (c == 0 && p.lse)
-                        p.lse[size_t(it.b) * p.num_q_heads + hq] =
+                    if (ch == 0 && p.lse)
+                        p.lse[row * p.num_q_heads + hq] =
                             Z > 0.f ? (Mf + fast_log2(Z)) * kLn2 : -INFINITY;
                 } else {
-                    const size_t base = (size_t(it.part) * p.batch + it.b) * p.num_q_heads + hq;
-                    const float scale_o = lrsum[h] > 0.f ? lsum[h] / lrsum[h] : 0.f;
-                    p.ws_o[base * kD + c] = o[h] * scale_o;
-                    if (c == 0) {
-                        p.ws_m[base] = m[h] * kLn2;
-                        p.ws_l[base] = lsum[h];
+                    const size_t base =
+                        (size_t(it.part) * p.num_q_rows + row) * p.num_q_heads + hq;
+                    const float scale_o = lrsum[c] > 0.f ? lsum[c] / lrsum[c] : 0.f;
+                    p.ws_o[base * kD + ch] = o[c] * scale_o;
+                    if (ch == 0) {
+                        p.ws_m[base] = m[c] * kLn2;
+                        p.ws_l[base] = lsum[c];
                     }
                 }
             }
@@ -465,10 +540,10 @@ gqa_decode_tc_kernel(const __grid_constant__ GqaParams p) {
 
 int g_num_sms_tc[64];
 
-template <int G>
+template <int G, int NC>
 cudaError_t launch_g(const GqaParams &p, cudaStream_t stream) {
     const size_t smem = tc_smem_bytes(p.batch);
-    auto kern = gqa_decode_tc_kernel<G>;
+    auto kern = gqa_decode_tc_kernel<G, NC>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          int(smem));
     if (e != cudaSuccess) return e;
@@ -494,12 +569,14 @@ cudaError_t launch_g(const GqaParams &p, cudaStream_t stream) {
 }  // namespace
 
 cudaError_t launch_gqa_decode_tc(const GqaParams &p, cudaStream_t stream) {
-    if (p.head_dim != kD) return cudaErrorInvalidValue;
+    if (p.head_dim != kD || p.max_q_len < 1 || p.max_q_len * p.group > kNRows)
+        return cudaErrorInvalidValue;
+    const bool fold = p.max_q_len > 1;
     switch (p.group) {
-        case 1: return launch_g<1>(p, stream);
-        case 2: return launch_g<2>(p, stream);
-        case 4: return launch_g<4>(p, stream);
-        case 8: return launch_g<8>(p, stream);
+        case 1: return fold ? launch_g<1, 16>(p, stream) : launch_g<1, 1>(p, stream);
+        case 2: return fold ? launch_g<2, 16>(p, stream) : launch_g<2, 2>(p, stream);
+        case 4: return fold ? launch_g<4, 16>(p, stream) : launch_g<4, 4>(p, stream);
+        case 8: return fold ? launch_g<8, 16>(p, stream) : launch_g<8, 8>(p, stream);
         default: return cudaErrorInvalidValue;
     }
 }

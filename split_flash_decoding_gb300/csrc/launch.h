@@ -21,18 +21,22 @@ constexpr int kGqaMaxBatch = 2048;
 struct GqaParams {
     CUtensorMap k_map;            // 4-D: (channel, slot, kv head, page)
     CUtensorMap v_map;
-    CUtensorMap q_map;            // 2-D: (channel, row = b * Hq + h); tensor-core kernel only
-    const uint16_t *q;            // bf16 [batch][Hq][D]
+    CUtensorMap q_map;            // 3-D: (channel, head, query row), box (64, group,
+                                  // max_q_len); tensor-core kernel only
+    const uint16_t *q;            // bf16 [rows][Hq][D]
     const uint32_t *kv_len;       // [batch]
+    const uint32_t *q_row_offsets;  // [batch + 1], or nullptr: row b is sequence b
     const int32_t *page_table;    // [batch][max_pages] or nullptr
     const float *sink;            // [Hq] or nullptr
-    float *ws_o;                  // [P][batch][Hq][D]
-    float *ws_m;                  // [P][batch][Hq]
-    float *ws_l;                  // [P][batch][Hq]
-    uint16_t *out;                // bf16 [batch][Hq][D]
-    float *lse;                   // [batch][Hq] or nullptr
+    float *ws_o;                  // [P][rows][Hq][D]
+    float *ws_m;                  // [P][rows][Hq]
+    float *ws_l;                  // [P][rows][Hq]
+    uint16_t *out;                // bf16 [rows][Hq][D]
+    float *lse;                   // [rows][Hq] or nullptr
     unsigned *err;                // device error word
-    int batch, num_q_heads, group, head_dim;
+    int batch, num_q_rows, num_q_heads, group, head_dim;
+    int max_q_len;                // rows of any sequence (tensor-core kernel: * group <= 16)
+    int causal;                   // rows of a sequence see keys j <= L - n + i
     int max_pages, page_size, num_pages;
     int box_rows;                 // tokens per TMA box (min(tile, page size))
     int num_partitions;           // P (grid.x)
@@ -93,6 +97,9 @@ struct ReduceParams {
     uint16_t *out;                // bf16 [rows][Hq][dv]
     float *lse;                   // [rows][Hq] or nullptr
     const uint32_t *kv_len;       // optional: rows whose kv_len needs < 2 slices are skipped
+    const uint32_t *q_row_offsets;  // optional: kv_len is per sequence, row r of sequence b
+                                    // has off[b] <= r < off[b+1]
+    int batch;
     int num_partitions, rows, num_q_heads, dim_v;
     int chunk;                    // slice length when kv_len is given
 };

@@ -24,6 +24,17 @@ namespace {
 constexpr int kWarps = 8;
 constexpr int kMaxP = 1024;   // ATTN_MAX_PARTITIONS
 
+// Sequence of query row `row`: the row itself, or found in the row offsets.
+__device__ __forceinline__ int row_sequence(const ReduceParams &p, int row) {
+    if (!p.q_row_offsets) return row;
+    int lo = 0, hi = p.batch;   // off[lo] <= row < off[hi]
+    while (hi - lo > 1) {
+        const int mid = (lo + hi) >> 1;
+        if (int(p.q_row_offsets[mid]) <= row) lo = mid; else hi = mid;
+    }
+    return lo;
+}
+
 __global__ void __launch_bounds__(kWarps * 32)
 splitk_reduce_kernel(const __grid_constant__ ReduceParams p) {
     // With programmatic dependent launch this grid may start while the
@@ -42,7 +53,7 @@ splitk_reduce_kernel(const __grid_constant__ ReduceParams p) {
     if (p.kv_len) {
         // Rows that fit in one slice were finished by the partition kernel.
         const uint32_t cap = uint32_t(p.num_partitions) * uint32_t(p.chunk);
-        const uint32_t L = min(p.kv_len[row], cap);
+        const uint32_t L = min(p.kv_len[row_sequence(p, row)], cap);
         const int ns = static_cast<int>((L + p.chunk - 1) / p.chunk);
         if (ns < 2) return;  // uniform over the warp
         P = ns;
@@ -115,7 +126,7 @@ splitk_reduce_wide_kernel(const __grid_constant__ ReduceParams p) {
     int P = p.num_partitions;
     if (p.kv_len) {
         const uint32_t cap = uint32_t(p.num_partitions) * uint32_t(p.chunk);
-        const uint32_t L = min(p.kv_len[row], cap);
+        const uint32_t L = min(p.kv_len[row_sequence(p, row)], cap);
         const int ns = static_cast<int>((L + p.chunk - 1) / p.chunk);
         if (ns < 2) return;  // uniform over the CTA
         P = ns;

@@ -240,6 +240,21 @@ def deepseek_v3_mla_decode(device="cpu", seed: int = 4, batch: int = 32) -> Work
                          scale=1.0 / math.sqrt(192.0))
 
 
+def few_token_decode(device="cpu", seed: int = 6, batch: int = 64, max_q_len: int = 4) -> Workload:
+    """Few-token decode on the Llama-3-8B shapes: batch 64, 32 q / 8 KV heads,
+    head_dim 128, paged (page 128), cache lengths uniform in [512, 8192], and
+    1..max_q_len query rows per sequence (draft tokens being verified),
+    causal (row i of n sees keys j <= L - n + i)."""
+    g = torch.Generator()
+    g.manual_seed(seed)
+    q_lens = [int(x) for x in torch.randint(1, max_q_len + 1, (batch,), generator=g)]
+    kv_lens = _uniform_ints(512, 8192, batch, seed)
+    return make_workload(f"few_token_decode_b{batch}_q{max_q_len}_h32kv8_d128_paged128",
+                         batch=batch, num_q_heads=32, num_kv_heads=8, dim_qk=128,
+                         kv_lens=kv_lens, page_size=128, seed=seed, device=device,
+                         q_lens=q_lens, causal=True)
+
+
 def mixed_prefill_decode(device="cpu", seed: int = 5) -> Workload:
     """Ragged mixed prefill + decode: 16 sequences, eight with one query row
     and eight with q_len uniform in [512, 4096]; cached prefix uniform in
