@@ -124,7 +124,7 @@ int attn_plan_partitions(int num_sms, int batch, int num_q_rows, int num_q_heads
 
 /*
  * attn_decode -- GQA/MHA attention of few query rows per sequence against a
- * paged or contiguous cache, with split-K for single-token decode
+ * paged or contiguous cache, with split-K for single- and few-token decode
  * (mha_decoding_single_batch_pipelined; mha_sm100_dispatch).
  *
  *   q          device bf16 [num_q_rows][num_q_heads][head_dim]
@@ -137,16 +137,21 @@ int attn_plan_partitions(int num_sms, int batch, int num_q_rows, int num_q_heads
  *   q_row_offsets  device uint32 [batch + 1] (rows of sequence b are
  *              [off[b], off[b+1])), or NULL for one row per sequence.
  *   batch, num_q_rows   sequences and total query rows (num_q_rows = batch
- *              when q_row_offsets is NULL; otherwise = off[batch]).  Single-
- *              token decode accepts batch <= 2048.
+ *              when q_row_offsets is NULL; otherwise = off[batch]).  The
+ *              split-K decode kernel accepts batch <= 2048.
  *   num_q_heads, group  num_q_heads % group == 0; group in {1, 2, 4, 8}.
  *   head_dim   64 or 128 (128 when max_q_len > 1).
  *   max_q_len  host upper bound of the rows of any sequence ("max_prompt_len
- *              ... optionally static").  1 selects the split-K decode
- *              kernel; > 1 selects the tensor-core tile kernel, which takes
- *              every sequence of the batch, single-token ones included
- *              ("a single-token prompt is just the shortest prefill",
- *              mha_sm100_dispatch, summary).
+ *              ... optionally static"); no sequence may have more rows.
+ *              1 selects the split-K decode kernel.  A few rows (head_dim
+ *              128, max_q_len * group <= 16, batch <= 2048: e.g. draft
+ *              tokens being verified) stay on that kernel: the rows of a
+ *              sequence fold onto the tensor-core N side next to the group's
+ *              heads and share every K/V tile, split-K included.  More rows
+ *              select the tensor-core tile kernel, which takes every sequence
+ *              of the batch, single-token ones included ("a single-token
+ *              prompt is just the shortest prefill", mha_sm100_dispatch,
+ *              summary), and does not split.
  *   max_kv_len host upper bound of kv_len ("max_cache_valid_length_arg").
  *   scale      multiplies Q.K' before the softmax.
  *   sink       device fp32 [num_q_heads] attention-sink logits, or NULL.
@@ -156,16 +161,16 @@ int attn_plan_partitions(int num_sms, int batch, int num_q_rows, int num_q_heads
  *              keys j <= L - n + i (bottom-right aligned).  A no-op for
  *              single-row sequences.
  *   num_partitions  P from attn_plan_partitions (or any 1..MAX); must be 1
- *              when max_q_len > 1.
+ *              on the tile kernel (max_q_len > 1 beyond the few-row fold).
  *   workspace  device, 256-byte aligned, >= the planner's workspace_bytes
  *              for this P; may be NULL when P == 1.  Contents on entry are
  *              ignored; it holds fp32 partial O, qk_max and exp_sum after.
  *   out        device bf16 [num_q_rows][num_q_heads][head_dim].
  *   lse        device fp32 [num_q_rows][num_q_heads], or NULL.
  *
- * Single-token decode launches the partition kernel (grid: P x num_kv_heads
- * x batch) and, for P > 1, the split-K reduce.  Returns ATTN_OK or an error
- * status.
+ * Decode launches the partition kernel (a persistent grid over (sequence,
+ * KV head, key slice) items) and, for P > 1, the split-K reduce.  Returns
+ * ATTN_OK or an error status.
  */
 int attn_decode(const void *q, const attn_kv_t *k, const attn_kv_t *v, const uint32_t *kv_len,
                 const uint32_t *q_row_offsets, int batch, int num_q_rows, int num_q_heads,
