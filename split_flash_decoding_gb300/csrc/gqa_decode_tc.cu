@@ -92,6 +92,14 @@ __device__ __forceinline__ void tmem_st_cols(uint32_t taddr, const float (&v)[N]
     }
 }
 
+// Maximum over the 32 lanes of the warp in one instruction (-inf is the
+// identity; every lane gets the result).
+__device__ __forceinline__ float warp_max_redux(float v) {
+    float r;
+    asm volatile("redux.sync.max.f32 %0, %1, 0xffffffff;" : "=f"(r) : "f"(v));
+    return r;
+}
+
 // First query row and row count of sequence b.
 __device__ __forceinline__ void seq_rows(const GqaParams &p, int b, int &row0, int &nrows) {
     if (p.q_row_offsets) {
@@ -396,7 +404,7 @@ gqa_decode_tc_kernel(const __grid_constant__ GqaParams p) {
 #pragma unroll
                 for (int c = 0; c < NC; ++c) {
                     s[c] = valid && t0 + k < lim[c] ? s[c] * p.qk_scale_log2 : -INFINITY;
-                    const float wm = warp_max(s[c]);
+                    const float wm = warp_max_redux(s[c]);
                     if (lane == 0) rb[warp * 16 + c] = wm;
                 }
                 named_sync(1, 128);
