@@ -253,11 +253,23 @@ int attn_decode_noalloc(const void *q, const attn_kv_t *k, const attn_kv_t *v,
 /*
  * attn_device_error_flags -- read (and optionally clear) the device-side
  * error word that kernels set instead of hanging: bit 0 = a pipeline wait
- * ran past its time limit, bit 1 = a page-table entry outside
- * [0, num_pages) was seen (that tile was skipped).  Synchronises the
+ * ran past its time limit (250 ms), bit 1 = a page-table entry outside
+ * [0, num_pages) was seen (that tile was skipped), bit 2 = a kv_len above
+ * num_partitions x slice length was seen (it was clamped).  Synchronises the
  * current device.  Returns ATTN_OK or ATTN_ERR_CUDA.
  */
 int attn_device_error_flags(unsigned int *flags, int clear);
+
+/*
+ * attn_selftest_wait_timeout -- the pages have no counterpart: a check of
+ * the failure path for deployments (and this library's tests).  Launches one
+ * kernel that waits, with the kernels' own bounded mbarrier wait, on a
+ * barrier nothing arrives on; after the time limit the wait gives up, sets
+ * bit 0 of the error word and the kernel returns, leaving the context
+ * usable.  Asynchronous on `stream`; read the result with
+ * attn_device_error_flags.  Returns ATTN_OK or ATTN_ERR_CUDA.
+ */
+int attn_selftest_wait_timeout(attn_stream_t stream);
 
 #ifdef __cplusplus
 }

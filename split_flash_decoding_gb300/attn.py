@@ -70,6 +70,7 @@ _SIGNATURES = {
     "attn_splitk_reduce": [_c.c_void_p, _c.c_void_p, _c.c_void_p, _c.c_int, _c.c_int, _c.c_int,
                            _c.c_int, _c.c_void_p, _c.c_void_p, _c.c_void_p, _c.c_void_p],
     "attn_device_error_flags": [_c.POINTER(_c.c_uint), _c.c_int],
+    "attn_selftest_wait_timeout": [_c.c_void_p],
     "attn_decode_noalloc": [_c.c_void_p, _c.POINTER(attn_kv_t), _c.POINTER(attn_kv_t),
                             _c.c_void_p, _c.c_void_p, _c.c_int, _c.c_int, _c.c_int, _c.c_int,
                             _c.c_int, _c.c_int, _c.c_int, _c.c_float, _c.c_void_p, _c.c_int,
@@ -279,6 +280,13 @@ def attn_decode_noalloc(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.T
                                      1 if causal else 0, num_partitions, out.data_ptr(),
                                      _ptr(lse), _stream_handle(stream)))
     return out, lse
+
+
+def attn_selftest_wait_timeout(stream=None) -> None:
+    """Failure-path check: one kernel whose bounded wait on a barrier nothing
+    arrives on gives up after its time limit and sets bit 0 of the device
+    error word (read it with attn_device_error_flags)."""
+    _check("attn_selftest_wait_timeout", lib().attn_selftest_wait_timeout(_stream_handle(stream)))
 
 
 def attn_device_error_flags(clear: bool = True) -> int:

@@ -10,6 +10,7 @@
 
 #include "attn_decode.h"
 #include "launch.h"
+#include "ptx.cuh"
 
 namespace attn {
 namespace {
@@ -127,6 +128,20 @@ int check_kv(const attn_kv_t *kv, int batch, int dim, int max_kv_len) {
 }
 
 int map_cuda(cudaError_t e) { return e == cudaSuccess ? ATTN_OK : ATTN_ERR_CUDA; }
+
+// Failure-path self-test: an mbarrier that nothing ever arrives on, waited on
+// with the same bounded wait the kernels use.  The wait gives up after its
+// time limit and sets the timeout bit of the error word; the kernel then
+// returns normally.
+__global__ void selftest_wait_kernel(unsigned *err) {
+    __shared__ uint64_t bar;
+    if (threadIdx.x == 0) {
+        mbar_init(&bar, 1);
+        fence_mbar_init();
+    }
+    __syncthreads();
+    if (threadIdx.x == 0) mbar_wait(&bar, 0, err);
+}
 
 int prefill_path(const void *q, const attn_kv_t *k, const attn_kv_t *v, const uint32_t *kv_len,
                  const uint32_t *q_row_offsets, int batch, int num_q_rows, int num_q_heads,
@@ -500,6 +515,14 @@ extern "C" int attn_splitk_reduce(const float *ws_o, const float *ws_m, const fl
     r.num_q_heads = num_q_heads;
     r.dim_v = dim_v;
     return map_cuda(launch_splitk_reduce(r, reinterpret_cast<cudaStream_t>(stream), false));
+}
+
+extern "C" int attn_selftest_wait_timeout(attn_stream_t stream) {
+    unsigned *err = nullptr;
+    const int st = error_word(&err);
+    if (st) return st;
+    selftest_wait_kernel<<<1, 32, 0, reinterpret_cast<cudaStream_t>(stream)>>>(err);
+    return map_cuda(cudaGetLastError());
 }
 
 extern "C" int attn_device_error_flags(unsigned int *flags, int clear) {
