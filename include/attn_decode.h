@@ -3,11 +3,11 @@
  * (libattn.so).
  *
  * Scope: single- and few-token attention of query rows against a KV cache
- * on one GPU.  The key dimension is split into partitions ("When
- * num_partitions exceeds 1, each block processes a contiguous slice of the
- * key dimension and writes partial exp_sum and qk_max statistics for a
- * subsequent mha_splitk_reduce pass", mha_decoding_single_batch_pipelined,
- * summary); the partials are merged by a log-sum-exp reduce.
+ * on one GPU.  The key dimension is split into partitions (with more than
+ * one partition every block takes one contiguous key range and leaves its
+ * exponential sum and running maximum for a separate reduce pass,
+ * mha_decoding_single_batch_pipelined, summary); the partials are merged by
+ * a log-sum-exp reduce.
  *
  * Conventions shared by every entry point
  * ---------------------------------------
@@ -26,8 +26,8 @@
  *   included; it is -inf for a row with no visible key and no sink (its
  *   output row is then 0).
  * - Query head h reads KV head h / group (groups of consecutive query
- *   heads share one KV head; "group: Number of query heads per KV head
- *   (GQA group size)", mha_sm100_dispatch, Parameters).
+ *   heads share one KV head; group is the GQA group size, the count of
+ *   query heads per KV head, mha_sm100_dispatch, Parameters).
  * - The number of partitions comes only from host integers, never from
  *   device data, so a call can be captured in a CUDA graph and replayed
  *   while the per-sequence lengths change (capture-invariant partition
@@ -58,8 +58,8 @@ enum {
 #define ATTN_MAX_PARTITIONS 1024
 
 /*
- * One K or V cache operand ("Key/value operand descriptor with dtype and
- * page size", mha_sm100_dispatch, Parameters: KVType; paged KVCache operand
+ * One K or V cache operand (the KV operand type carries the element type and
+ * the page size, mha_sm100_dispatch, Parameters: KVType; paged KVCache operand
  * or contiguous tensor operand, flare_mla_decoding_dispatch, Parameters: k_t).
  *
  * Token t of sequence b, KV head kh, channel c is the bf16 element
@@ -92,11 +92,9 @@ typedef struct attn_kv {
  * attn_plan_partitions -- choose the split-K partition count.
  *
  * Follows the automatic partition ladder with an exact override
- * ("num_partitions_override: Exact split-K partition count to use, or 0 for
- * the automatic ladder. A non-zero value is honored verbatim",
- * mha_sm100_dispatch, Args; "num_partitions: Optional explicit split-K
- * partition count; None selects via heuristic",
- * flare_mla_decoding_dispatch, Args).
+ * (a non-zero num_partitions_override is used as given and zero selects the
+ * automatic ladder, mha_sm100_dispatch, Args; an absent num_partitions lets
+ * a heuristic choose, flare_mla_decoding_dispatch, Args).
  *
  *   num_sms       SMs to plan for; <= 0 queries the current device.
  *   batch         sequences; num_q_rows total query rows (= batch for
@@ -128,12 +126,13 @@ int attn_plan_partitions(int num_sms, int batch, int num_q_rows, int num_q_heads
  * (mha_decoding_single_batch_pipelined; mha_sm100_dispatch).
  *
  *   q          device bf16 [num_q_rows][num_q_heads][head_dim]
- *              ("q_arg: Pointer to the query tensor data").
+ *              (q_arg, mha_decoding_single_batch_pipelined, Args).
  *   k, v       cache operands (host structs describing device memory); both
  *              head_dim wide and sharing one page table layout.
  *   kv_len     device uint32 [batch]: keys of sequence b, including its own
- *              query tokens ("valid_length: Per-row valid KV length
- *              pointer").  The cache already holds the current tokens' K/V.
+ *              query tokens (valid_length, the per-row count of valid
+ *              keys, mha_sm100_dispatch, Args).  The cache already holds the
+ *              current tokens' K/V.
  *   q_row_offsets  device uint32 [batch + 1] (rows of sequence b are
  *              [off[b], off[b+1])), or NULL for one row per sequence.
  *   batch, num_q_rows   sequences and total query rows (num_q_rows = batch
@@ -141,17 +140,18 @@ int attn_plan_partitions(int num_sms, int batch, int num_q_rows, int num_q_heads
  *              split-K decode kernel accepts batch <= 2048.
  *   num_q_heads, group  num_q_heads % group == 0; group in {1, 2, 4, 8}.
  *   head_dim   64 or 128 (128 when max_q_len > 1).
- *   max_q_len  host upper bound of the rows of any sequence ("max_prompt_len
- *              ... optionally static"); no sequence may have more rows.
+ *   max_q_len  host upper bound of the rows of any sequence (max_prompt_len,
+ *              mha_sm100_dispatch, Args); no sequence may have more rows.
  *              1 selects the split-K decode kernel.  A few rows (head_dim
  *              128, max_q_len * group <= 16, batch <= 2048: e.g. draft
  *              tokens being verified) stay on that kernel: the rows of a
  *              sequence fold onto the tensor-core N side next to the group's
  *              heads and share every K/V tile, split-K included.  More rows
  *              select the tensor-core tile kernel, which takes every sequence
- *              of the batch, single-token ones included ("a single-token
- *              prompt is just the shortest prefill", mha_sm100_dispatch,
- *              summary), and does not split.
+ *              of the batch, single-token ones included (that page handles
+ *              one-token decode as the degenerate case of prefill rather
+ *              than a route of its own, mha_sm100_dispatch, summary), and does
+ *              not split.
  *   max_kv_len host upper bound of kv_len ("max_cache_valid_length_arg").
  *   scale      multiplies Q.K' before the softmax.
  *   sink       device fp32 [num_q_heads] attention-sink logits, or NULL.
@@ -181,9 +181,9 @@ int attn_decode(const void *q, const attn_kv_t *k, const attn_kv_t *v, const uin
 /*
  * attn_mla_decode -- multi-head latent attention decode: one KV head whose
  * rows are dim_qk = 576 wide (512 latent + 64 rope), V = K[:, :dim_v]
- * with dim_v = 512 ("kv_num_heads: Must be 1 for MLA"; "V is derived as
- * K[:, :, :depth_v], so V is not loaded separately",
- * flare_mla_decoding_dispatch, Parameters and Args).
+ * with dim_v = 512 (MLA has exactly one KV head, and V is the leading
+ * depth_v channels of K rather than a second operand that is read,
+ * flare_mla_decoding_dispatch, Parameters: kv_num_heads and Args: k).
  *
  *   q          device bf16 [batch][num_q_heads][dim_qk]; num_q_heads = 128.
  *   kv         the single cache operand (num_kv_heads = 1).

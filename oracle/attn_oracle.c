@@ -10,13 +10,13 @@
  * split-K):
  *
  *   For sequence b, query row i (0 <= i < n_b), query head h, KV head
- *   k = h / group ("group: query heads per key/value head",
+ *   k = h / group (group counts the query heads that share one KV head,
  *   mha_sm100_dispatch, Parameters; mha_decoding_single_batch_pipelined,
  *   Parameters):
  *
  *     J      = { j : 0 <= j < L_b, and j <= L_b - n_b + i when causal }
- *     s_j    = scale * sum_c q[c] * K[j, k, c]         ("scale: scalar applied
- *              to the Q@K' product before softmax", mha_sm100_dispatch, Args)
+ *     s_j    = scale * sum_c q[c] * K[j, k, c]         (scale multiplies
+ *              Q K^T ahead of the softmax, mha_sm100_dispatch, Args)
  *     t      = sink[h] if sinks are given, else -inf
  *     M      = max(max_{j in J} s_j, t)
  *     Z      = sum_{j in J} exp(s_j - M) + exp(t - M)
@@ -25,17 +25,17 @@
  *
  *   An empty J with no sink gives out = 0 and lse = -inf.  MLA is the same
  *   with one KV head, a 576-deep K and V = K[:, :512], passed here as a V
- *   operand that aliases K with dim_v = 512 ("V is derived as
- *   K[:, :, :depth_v]", flare_mla_decoding_dispatch, Args).
+ *   operand that aliases K with dim_v = 512 (V is the leading depth_v
+ *   channels of K, flare_mla_decoding_dispatch, Args: k).
  *
  *   Logical token t of sequence b lives at physical row
  *   page_table[b][t / page_size] * page_size + t % page_size of the cache
- *   ("Key/value operand descriptor with dtype and page size",
- *   mha_sm100_dispatch, Parameters); with no page table the page index is b.
+ *   (the KV operand type carries the page size, mha_sm100_dispatch,
+ *   Parameters: KVType); with no page table the page index is b.
  *
  * oracle_partials computes the per-partition statistics that the split-K
- * method keeps ("writes partial exp_sum and qk_max statistics",
- * mha_decoding_single_batch_pipelined, summary): for a key slice S,
+ * method keeps (each key slice leaves its running maximum and exponential
+ * sum behind, mha_decoding_single_batch_pipelined, summary): for a key slice S,
  *   m_S = max_{j in S cap J} s_j,  l_S = sum exp(s_j - m_S),
  *   O_S[c] = sum exp(s_j - m_S) V[j, c]   (unnormalised),
  * and (-inf, 0, 0) for an empty slice.

@@ -27,8 +27,8 @@
 //     P.V: lane owns head_dim/32 channels of every row.
 //
 // An item's result is either the final output (its sequence needs at most
-// one slice) or the partial (O, m, l) for the split-K reduce ("writes partial
-// exp_sum and qk_max statistics for a subsequent mha_splitk_reduce pass",
+// one slice) or the partial (O, m, l) for the split-K reduce (a slice leaves
+// its exponential sum and running maximum for the reduce pass,
 // mha_decoding_single_batch_pipelined, summary).  Scores are kept in base-2
 // units internally (q is pre-scaled by scale*log2 e); the partial max written
 // to the workspace is in natural-log units.

@@ -2,9 +2,9 @@
 //
 // Multi-head latent attention decode: 128 query heads attend to one KV head
 // whose rows are 576 channels (512 latent + 64 rope), and V is the first 512
-// channels of K ("kv_num_heads: Must be 1 for MLA"; "V is derived as
-// K[:, :, :depth_v], so V is not loaded separately",
-// flare_mla_decoding_dispatch, Parameters and Args).
+// channels of K, which is never fetched a second time (one KV head and V
+// taken from K: flare_mla_decoding_dispatch, Parameters: kv_num_heads and
+// Args: k).
 //
 // Work unit: a cluster of two CTAs per (key slice p, sequence b).  The 128
 // heads are the MMA's M dimension.  The two CTAs split the 576 channels:

@@ -2,8 +2,8 @@
 // whose sequences carry several query rows (ragged prefill mixed with
 // decode), with a causal mask aligned to the end of the cache.
 //
-// "Decode is not a separate route: a single-token prompt is just the
-// shortest prefill" (mha_sm100_dispatch, summary): every sequence of the
+// Decode takes no route of its own here: one-token decode is handled as the
+// degenerate case of prefill (mha_sm100_dispatch, summary), so every sequence of the
 // batch, single-row ones included, is cut into tiles of 128 MMA rows.  A tile
 // holds T = 128 / group consecutive tokens x the group's query heads of one
 // KV head, so each K/V tile fetched serves all heads of the group.  Row r is
