@@ -55,6 +55,8 @@ class _KV(ctypes.Structure):
         ("_pad", ctypes.c_int32),
         ("page_table", ctypes.c_void_p),
         ("max_pages", ctypes.c_int64),
+        ("indices", ctypes.c_void_p),
+        ("indices_stride", ctypes.c_int64),
     ]
 
 
@@ -162,10 +164,13 @@ class KV:
     ``page * page_stride + slot * token_stride + head * head_stride + c`` is
     channel c of the token in slot ``slot`` of page ``page``.  With
     ``page_table`` None, page = sequence index and slot = token index.
+    With ``indices`` [batch, indices_stride] (sparse top-k), token t of
+    sequence b is physical row r = indices[b, t], slot r % page_size of page
+    r // page_size; ``num_rows`` bounds r.
     """
 
     def __init__(self, data, page_stride, token_stride, head_stride, page_size,
-                 page_table=None, channel_offset=0):
+                 page_table=None, channel_offset=0, indices=None, num_rows=None):
         self.data = _bits(data).reshape(-1)
         self.page_stride = int(page_stride)
         self.token_stride = int(token_stride)
@@ -173,12 +178,40 @@ class KV:
         self.page_size = int(page_size)
         self.page_table = _i32(page_table)
         self.channel_offset = int(channel_offset)
+        self.indices = _i32(indices)
+        if self.indices is not None:
+            if self.page_table is not None:
+                raise ValueError("a sparse operand has indices instead of a page table")
+            if self.indices.ndim != 2:
+                raise ValueError("indices must be [batch, indices_stride]")
+            if num_rows is None:
+                raise ValueError("a sparse operand needs num_rows")
+        self.num_rows = None if num_rows is None else int(num_rows)
 
     @classmethod
     def paged(cls, cache, page_table):
         """cache [num_pages, page_size, num_kv_heads, dim], page_table [B, max_pages]."""
         n, ps, hk, d = cache.shape
         return cls(cache, ps * hk * d, hk * d, d, ps, page_table)
+
+    @classmethod
+    def sparse(cls, cache, indices):
+        """cache [num_pages, page_size, num_kv_heads, dim] read as
+        num_pages * page_size physical rows; indices int [batch, stride]."""
+        n, ps, hk, d = cache.shape
+        return cls(cache, ps * hk * d, hk * d, d, ps, None, indices=indices, num_rows=n * ps)
+
+    def check_rows(self, kv_len):
+        """Every index a sequence uses (the first kv_len[b]) names a row."""
+        if self.indices is None:
+            return
+        for b, L in enumerate(kv_len):
+            if L > self.indices.shape[1]:
+                raise ValueError(f"sequence {b}: {L} keys but indices_stride "
+                                 f"{self.indices.shape[1]}")
+            r = self.indices[b, :L]
+            if L and (r.min() < 0 or r.max() >= self.num_rows):
+                raise ValueError(f"sequence {b}: index outside [0, {self.num_rows})")
 
     @classmethod
     def contiguous(cls, cache):
@@ -196,6 +229,8 @@ class KV:
         s.page_size = self.page_size
         s.page_table = pt.ctypes.data if pt is not None else None
         s.max_pages = pt.shape[1] if pt is not None else 0
+        s.indices = self.indices.ctypes.data if self.indices is not None else None
+        s.indices_stride = self.indices.shape[1] if self.indices is not None else 0
         return s
 
 
@@ -214,6 +249,8 @@ def _problem(q, k: KV, v: KV, kv_len, q_row_offsets, group, scale, sink, causal,
         raise ValueError("q_row_offsets must be [batch+1] ending at the row count")
     if hq % group:
         raise ValueError("num_q_heads must be a multiple of group")
+    k.check_rows(kvl)
+    v.check_rows(kvl)
     ks, vs = k._struct(), v._struct()
     pr = _Problem()
     pr.q = qb.ctypes.data

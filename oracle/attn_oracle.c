@@ -33,6 +33,14 @@
  *   (the KV operand type carries the page size, mha_sm100_dispatch,
  *   Parameters: KVType); with no page table the page index is b.
  *
+ *   Sparse top-k (flare_mla_decoding_dispatch, Parameters: sparse; Args:
+ *   d_indices, indices_stride, topk_lengths): sequence b attends only to the
+ *   L_b = topk_lengths[b] cache rows that its index list names.  Its logical
+ *   token t (t < L_b) is physical row r = indices[b * indices_stride + t],
+ *   which sits in slot r % page_size of page r / page_size; entries past L_b
+ *   are never read.  With that mapping the definition above applies as it
+ *   stands (kv_len = topk_lengths, no causal mask for a single query row).
+ *
  * oracle_partials computes the per-partition statistics that the split-K
  * method keeps (each key slice leaves its running maximum and exponential
  * sum behind, mha_decoding_single_batch_pipelined, summary): for a key slice S,
@@ -58,6 +66,8 @@ typedef struct {
     int32_t _pad;
     const int32_t *page_table; /* [batch][max_pages] or NULL: page = b */
     int64_t max_pages;
+    const int32_t *indices;    /* sparse: [batch][indices_stride] physical rows, or NULL */
+    int64_t indices_stride;
 } oracle_kv;
 
 typedef struct {
@@ -80,7 +90,11 @@ static double bf16_to_double(uint16_t bits) {
 
 static const uint16_t *kv_row(const oracle_kv *kv, int b, int64_t t, int head) {
     int64_t page, slot;
-    if (kv->page_table) {
+    if (kv->indices) {
+        int64_t r = kv->indices[(int64_t)b * kv->indices_stride + t];
+        page = r / kv->page_size;
+        slot = r % kv->page_size;
+    } else if (kv->page_table) {
         page = kv->page_table[(int64_t)b * kv->max_pages + t / kv->page_size];
         slot = t % kv->page_size;
     } else {

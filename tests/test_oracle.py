@@ -364,6 +364,91 @@ def test_partials_merge_to_the_unsplit_result():
 
 
 # --------------------------------------------------------------------------
+# sparse top-k (indices name the physical rows each sequence attends to)
+# --------------------------------------------------------------------------
+
+def sparse_problem(seed, batch, hq, d, num_pages, page_size, topk, replace=False):
+    """q [batch, hq, d], a one-head row pool [num_pages, page_size, 1, d] and
+    index lists int32 [batch, max(topk)]; entries past topk[b] are -1."""
+    g = torch.Generator().manual_seed(seed)
+    q = torch.randn(batch, hq, d, generator=g).to(torch.bfloat16)
+    pool = torch.randn(num_pages, page_size, 1, d, generator=g).to(torch.bfloat16)
+    rng = np.random.default_rng(seed)
+    idx = np.full((batch, max(max(topk), 1)), -1, dtype=np.int32)
+    for b, L in enumerate(topk):
+        idx[b, :L] = rng.choice(num_pages * page_size, L, replace=replace)
+    return q, pool, idx
+
+
+def gather_rows(pool, idx, topk):
+    """Logical cache [batch, max(topk), 1, d] holding the named rows in
+    order, copied with explicit loops from (page, slot) = divmod(row, page_size)."""
+    ps = pool.shape[1]
+    out = torch.zeros((idx.shape[0], max(max(topk), 1), 1, pool.shape[-1]), dtype=pool.dtype)
+    for b, L in enumerate(topk):
+        for t in range(L):
+            page, slot = divmod(int(idx[b, t]), ps)
+            out[b, t] = pool[page, slot]
+    return out
+
+
+@pytest.mark.parametrize("replace", [False, True])
+def test_sparse_equals_sdpa_over_gathered_rows(replace):
+    topk = [37, 0, 64, 5]
+    q, pool, idx = sparse_problem(61, 4, 8, 40, num_pages=12, page_size=16, topk=topk,
+                                  replace=replace)
+    kv = oracle.KV.sparse(pool, idx)
+    out, lse = oracle.attention(q, kv, kv, topk, group=8, scale=0.15, dim_v=32)
+    k = gather_rows(pool, idx, topk)
+    ref_o, ref_l = sdpa_reference(q, k, k[..., :32], topk, 8, 0.15)
+    np.testing.assert_allclose(out, ref_o, rtol=0, atol=1e-12)
+    np.testing.assert_allclose(lse, ref_l, rtol=1e-12, atol=1e-12)
+
+
+def test_sparse_identity_indices_equal_paged_bitwise():
+    lens = [70, 3, 33]
+    q, k, _ = logical_problem(62, 3, 4, 1, 24, lens)
+    pool, table = to_paged(k, lens, 8, seed=4)
+    idx = np.full((3, 70), -1, dtype=np.int32)
+    for b, L in enumerate(lens):
+        for t in range(L):
+            idx[b, t] = table[b, t // 8] * 8 + t % 8
+    kp = oracle.KV.paged(pool, table)
+    ks = oracle.KV.sparse(pool, idx)
+    o1, l1 = oracle.attention(q, kp, kp, lens, group=4, scale=0.3, dim_v=16)
+    o2, l2 = oracle.attention(q, ks, ks, lens, group=4, scale=0.3, dim_v=16)
+    assert np.array_equal(o1, o2) and np.array_equal(l1, l2)
+
+
+def test_sparse_ignores_indices_past_topk():
+    topk = [10, 25]
+    q, pool, idx = sparse_problem(63, 2, 4, 16, num_pages=4, page_size=32, topk=topk)
+    kv = oracle.KV.sparse(pool, idx)
+    o1, l1 = oracle.attention(q, kv, kv, topk, group=4, scale=0.5)
+    idx2 = idx.copy()
+    idx2[0, 10:] = np.arange(15) + 3          # valid rows, but past topk[0]
+    kv2 = oracle.KV.sparse(pool, idx2)
+    o2, l2 = oracle.attention(q, kv2, kv2, topk, group=4, scale=0.5)
+    assert np.array_equal(o1, o2) and np.array_equal(l1, l2)
+
+
+def test_sparse_identical_selected_rows_closed_form():
+    # every selected row equals x: uniform weights, out = x[:dv], lse = s + ln L
+    topk = [9]
+    q, pool, idx = sparse_problem(64, 1, 2, 16, num_pages=3, page_size=8, topk=topk)
+    x = torch.randn(16, generator=torch.Generator().manual_seed(5)).to(torch.bfloat16)
+    for r in idx[0, :9]:
+        pool[int(r) // 8, int(r) % 8, 0] = x
+    kv = oracle.KV.sparse(pool, idx)
+    out, lse = oracle.attention(q, kv, kv, topk, group=2, scale=0.25, dim_v=12)
+    xd = x.double().numpy()
+    for h in range(2):
+        assert np.array_equal(out[0, h], xd[:12])
+        s = 0.25 * float(np.dot(q[0, h].double().numpy(), xd))
+        np.testing.assert_allclose(lse[0, h], s + math.log(9), rtol=1e-13, atol=1e-13)
+
+
+# --------------------------------------------------------------------------
 # the standard workload generators
 # --------------------------------------------------------------------------
 

@@ -29,6 +29,10 @@ MUTATIONS = {
     "v_read_from_k": ("const uint16_t *vp = kv_row(pr->v, b, j, kh);\n        Z += 0;",
                       None),
     "partial_max_unscaled": ("double w = exp(s[j] - m);", "double w = exp(s[j]);"),
+    "sparse_batch_offset_dropped": ("int64_t r = kv->indices[(int64_t)b * kv->indices_stride + t];",
+                                    "int64_t r = kv->indices[t];"),
+    "sparse_slot_page_swapped": ("slot = r % kv->page_size;\n    } else if",
+                                 "slot = r / kv->page_size;\n    } else if"),
     "last_key_dropped": ("for (int64_t j = 0; j < nvis; ++j) {\n        double w",
                          "for (int64_t j = 0; j + 1 < nvis; ++j) {\n        double w"),
 }
