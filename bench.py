@@ -7,7 +7,7 @@ head_dim 128, ragged kv_len uniform in [512, 8192], paged cache with page
 one attn_decode call (partition kernel + split-K reduce) over that batch.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
-                    [--workload llama3|long_context|mla|tiny]
+                    [--workload llama3|long_context|mla|sparse_mla|mixed|few_token|tiny]
 
 Prints one JSON line (rank 0).  The metric is achieved HBM bandwidth:
 algorithmic bytes per call (visible K + V, plus q, out and lse) over the
@@ -71,7 +71,8 @@ def parse():
     ap.add_argument("--warmup", type=int, default=50)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default="llama3",
-                    choices=["llama3", "long_context", "mla", "mixed", "few_token", "tiny"])
+                    choices=["llama3", "long_context", "mla", "sparse_mla", "mixed", "few_token",
+                             "tiny"])
     ap.add_argument("--partitions", type=int, default=0, help="0 = planner's choice")
     ap.add_argument("--batch", type=int, default=0,
                     help="override the batch of the llama3 / mla workloads (profiling captures)")
@@ -184,6 +185,9 @@ def build_workload(name: str, device, batch: int = 0):
         return W.long_context_decode(device=device)
     if name == "mla":
         return W.deepseek_v3_mla_decode(device=device, **({"batch": batch} if batch else {}))
+    if name == "sparse_mla":
+        return W.deepseek_v32_sparse_mla_decode(device=device,
+                                                **({"batch": batch} if batch else {}))
     if name == "mixed":
         return W.mixed_prefill_decode(device=device)
     if name == "few_token":
@@ -194,13 +198,16 @@ def build_workload(name: str, device, batch: int = 0):
 
 
 def algorithmic_bytes(w) -> int:
-    """Visible K + V bytes (each byte once per call), q, out and lse."""
+    """Visible K + V bytes (each byte once per call), q, out and lse; for
+    sparse top-k also the 4-byte index of every key read."""
     hkv = w.num_kv_heads
     total_keys = sum(w.kv_len_host)
     if w.is_mla:
         kv = total_keys * w.dim_qk * 2                 # V is a prefix of K
     else:
         kv = total_keys * hkv * (w.dim_qk + w.dim_v) * 2
+    if w.indices is not None:
+        kv += total_keys * 4
     q = w.q.numel() * 2
     o = w.rows * w.num_q_heads * w.dim_v * 2
     lse = w.rows * w.num_q_heads * 4
@@ -262,8 +269,12 @@ def oracle_sample_time(w, k_host, v_host, seqs):
             rows.append(b)
             heads.append(h)
     threads = os.cpu_count() or 1
-    kk = (oracle.KV.paged(k_host, w.page_table.cpu()) if w.page_table is not None
-          else oracle.KV.contiguous(k_host))
+    if w.indices is not None:
+        kk = oracle.KV.sparse(k_host, w.indices.cpu())
+    elif w.page_table is not None:
+        kk = oracle.KV.paged(k_host, w.page_table.cpu())
+    else:
+        kk = oracle.KV.contiguous(k_host)
     vv = kk if v_host is None else (oracle.KV.paged(v_host, w.page_table.cpu())
                                     if w.page_table is not None else oracle.KV.contiguous(v_host))
     sink = None if w.sink is None else w.sink.cpu()
@@ -348,9 +359,11 @@ def run_ours(args, rank, world, dist):
     w = build_workload(args.workload, dev, args.batch)
     stream = torch.cuda.Stream(device=dev)
 
+    sparse = w.indices is not None
     if w.is_mla:
+        span = w.indices.shape[1] if sparse else w.max_kv_len
         P, ws_bytes = attn.attn_plan_partitions(w.batch, w.rows, w.num_q_heads, 1, w.dim_v,
-                                                w.max_kv_len, args.partitions)
+                                                span, args.partitions)
     elif w.max_q_len > 1 and not few_token(w):
         P, ws_bytes = 1, 0
     else:
@@ -361,8 +374,12 @@ def run_ours(args, rank, world, dist):
     out = torch.empty((w.rows, w.num_q_heads, w.dim_v), dtype=torch.bfloat16, device=dev)
     lse = torch.empty((w.rows, w.num_q_heads), dtype=torch.float32, device=dev)
 
-    def call(q=w.q, kv_len=w.kv_len, page_table=w.page_table, o=out, l=lse):
-        if w.is_mla:
+    def call(q=w.q, kv_len=w.kv_len, page_table=w.page_table, o=out, l=lse, indices=w.indices):
+        if sparse:
+            attn.attn_mla_decode_sparse(q, w.k_cache, indices, kv_len, scale=w.scale,
+                                        dim_v=w.dim_v, sink=w.sink, num_partitions=P,
+                                        workspace=ws, out=o, lse=l, stream=stream)
+        elif w.is_mla:
             attn.attn_mla_decode(q, w.k_cache, kv_len, scale=w.scale, max_kv_len=w.max_kv_len,
                                  dim_v=w.dim_v, page_table=page_table, sink=w.sink,
                                  num_partitions=P, workspace=ws, out=o, lse=l, stream=stream)
@@ -421,7 +438,10 @@ def run_ours(args, rank, world, dist):
     q_dev = torch.empty_like(w.q)
     kvl_dev = torch.empty_like(w.kv_len)
     pt_dev = None if pt_host is None else torch.empty_like(w.page_table)
+    idx_host = None if w.indices is None else w.indices.cpu().pin_memory()
+    idx_dev = None if idx_host is None else torch.empty_like(w.indices)
     h2d = q_host.numel() * 2 + kvl_host.numel() * 4 + (0 if pt_host is None else pt_host.numel() * 4)
+    h2d += 0 if idx_host is None else idx_host.numel() * 4
     d2h = out_host.numel() * 2 + lse_host.numel() * 4
 
     def e2e_step():
@@ -430,7 +450,9 @@ def run_ours(args, rank, world, dist):
             kvl_dev.copy_(kvl_host, non_blocking=True)
             if pt_dev is not None:
                 pt_dev.copy_(pt_host, non_blocking=True)
-            call(q=q_dev, kv_len=kvl_dev, page_table=pt_dev)
+            if idx_dev is not None:
+                idx_dev.copy_(idx_host, non_blocking=True)
+            call(q=q_dev, kv_len=kvl_dev, page_table=pt_dev, indices=idx_dev)
             out_host.copy_(out, non_blocking=True)
             lse_host.copy_(lse, non_blocking=True)
         stream.synchronize()
@@ -520,9 +542,9 @@ def run_ours(args, rank, world, dist):
         "e2e": {"value": round(world * nbytes / e2e_s / 1e9, 2), "unit": "GB/s",
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                 "us_per_step": round(e2e_s * 1e6, 2),
-                "note": "public Python API per step: H2D of q, kv_len, page table from pinned "
-                        "memory, attn_decode, D2H of out and lse, stream sync; KV cache "
-                        "resident"},
+                "note": "public Python API per step: H2D of q, kv_len and the page table "
+                        "(or the top-k indices) from pinned memory, the decode call, D2H of "
+                        "out and lse, stream sync; KV cache resident"},
         "gpu_launches": launches_per_call * args.steps,
         "roofline": roofline,
         "cpu_baseline": cpu,

@@ -111,8 +111,11 @@ typedef struct attn_kv {
  * C = ceil(ceil(max_kv_len / P) / T) * T, T = 128 for attn_decode with
  * head_dim 128, 32 for head_dim 64, and 64 for attn_mla_decode; slices past
  * kv_len are empty.  The automatic choice treats num_kv_heads == 1 with
- * head_dim_v == 512 as the MLA shape (longer slices, one two-CTA cluster per
- * SM pair) and everything else as GQA.
+ * head_dim_v == 512 as the MLA shape and everything else as GQA.  MLA:
+ * P = max(floor(num_sms / 2 / batch), ceil(max_kv_len / 4096)), at least 1
+ * (one two-CTA cluster per SM pair; slices of about 4096 keys, or as many
+ * as one wave of clusters holds).  For attn_mla_decode_sparse pass
+ * max_kv_len = indices_stride.
  * Returns ATTN_OK, ATTN_ERR_INVALID_ARG, or ATTN_ERR_CUDA if the SM count
  * query fails.  Launches nothing.
  */
@@ -197,6 +200,48 @@ int attn_mla_decode(const void *q, const attn_kv_t *kv, const uint32_t *kv_len, 
                     size_t workspace_bytes, void *out, float *lse, attn_stream_t stream);
 
 /*
+ * attn_mla_decode_sparse -- MLA decode in which every sequence attends only
+ * to the cache rows that a top-k index list names (flare_mla_decoding_dispatch,
+ * Parameters: sparse; Args: d_indices, indices_stride, topk_lengths).
+ *
+ *   q          device bf16 [batch][num_q_heads][dim_qk]; num_q_heads = 128,
+ *              dim_qk = 576, dim_v = 512 as for attn_mla_decode.
+ *   kv         the cache read as num_pages * page_size rows at one stride:
+ *              row r is slot r % page_size of page r / page_size, and
+ *              page_stride must equal page_size * token_stride (a contiguous
+ *              pool; otherwise ATTN_ERR_UNSUPPORTED).  page_table must be
+ *              NULL (the indices take its place); any page_size >= 1; the
+ *              other requirements of attn_kv_t hold.
+ *   indices    device int32 [batch][indices_stride]: key t of sequence b is
+ *              row indices[b * indices_stride + t].  Entries at t >=
+ *              topk_lengths[b] are never read.  A row may appear more than
+ *              once (it then counts once per appearance).  May be NULL when
+ *              indices_stride is 0.
+ *   indices_stride  row length of indices (the largest top-k of the batch);
+ *              it plays the part of max_kv_len for partition planning
+ *              (attn_plan_partitions with num_kv_heads 1, head_dim_v 512,
+ *              max_kv_len = indices_stride gives num_partitions and the
+ *              workspace size).
+ *   topk_lengths  device int32 [batch]: valid keys of sequence b,
+ *              0 <= topk_lengths[b] <= indices_stride.  0 gives out = 0 and
+ *              lse = -inf (or the sink alone).
+ *   scale, sink, num_partitions, workspace, workspace_bytes, out, lse
+ *              as for attn_mla_decode.  extra_k (an always-attended second
+ *              cache) is not supported.
+ *
+ * An index outside [0, num_pages * page_size) sets bit 1 of the device
+ * error word and that key is not read.  Returns ATTN_OK, ATTN_ERR_INVALID_ARG,
+ * ATTN_ERR_UNSUPPORTED, ATTN_ERR_WORKSPACE or ATTN_ERR_CUDA; launches nothing
+ * on an error return.
+ */
+int attn_mla_decode_sparse(const void *q, const attn_kv_t *kv, const int32_t *indices,
+                           int indices_stride, const int32_t *topk_lengths, int batch,
+                           int num_q_heads, int dim_qk, int dim_v, float scale,
+                           const float *sink, int num_partitions, void *workspace,
+                           size_t workspace_bytes, void *out, float *lse,
+                           attn_stream_t stream);
+
+/*
  * attn_splitk_reduce -- merge split-K partials by log-sum-exp
  * (mha_splitk_reduce / mla_splitk_reduce, named in
  * mha_decoding_single_batch_pipelined, summary, and
@@ -254,9 +299,11 @@ int attn_decode_noalloc(const void *q, const attn_kv_t *k, const attn_kv_t *v,
  * attn_device_error_flags -- read (and optionally clear) the device-side
  * error word that kernels set instead of hanging: bit 0 = a pipeline wait
  * ran past its time limit (250 ms), bit 1 = a page-table entry outside
- * [0, num_pages) was seen (that tile was skipped), bit 2 = a kv_len above
- * num_partitions x slice length was seen (it was clamped).  Synchronises the
- * current device.  Returns ATTN_OK or ATTN_ERR_CUDA.
+ * [0, num_pages) or a sparse index outside [0, num_pages * page_size) was
+ * seen (that page or row was not read; the output is then undefined),
+ * bit 2 = a kv_len above num_partitions x slice length, or a top-k count
+ * above indices_stride or below 0, was seen (it was clamped).  Synchronises
+ * the current device.  Returns ATTN_OK or ATTN_ERR_CUDA.
  */
 int attn_device_error_flags(unsigned int *flags, int clear);
 

@@ -67,6 +67,10 @@ _SIGNATURES = {
     "attn_mla_decode": [_c.c_void_p, _c.POINTER(attn_kv_t), _c.c_void_p, _c.c_int, _c.c_int,
                         _c.c_int, _c.c_int, _c.c_int, _c.c_float, _c.c_void_p, _c.c_int,
                         _c.c_void_p, _c.c_size_t, _c.c_void_p, _c.c_void_p, _c.c_void_p],
+    "attn_mla_decode_sparse": [_c.c_void_p, _c.POINTER(attn_kv_t), _c.c_void_p, _c.c_int,
+                               _c.c_void_p, _c.c_int, _c.c_int, _c.c_int, _c.c_int, _c.c_float,
+                               _c.c_void_p, _c.c_int, _c.c_void_p, _c.c_size_t, _c.c_void_p,
+                               _c.c_void_p, _c.c_void_p],
     "attn_splitk_reduce": [_c.c_void_p, _c.c_void_p, _c.c_void_p, _c.c_int, _c.c_int, _c.c_int,
                            _c.c_int, _c.c_void_p, _c.c_void_p, _c.c_void_p, _c.c_void_p],
     "attn_device_error_flags": [_c.POINTER(_c.c_uint), _c.c_int],
@@ -237,6 +241,38 @@ def attn_mla_decode(q: torch.Tensor, kv_cache: torch.Tensor, kv_len: torch.Tenso
            lib().attn_mla_decode(q.data_ptr(), ctypes.byref(kd), kv_len.data_ptr(), batch, hq, dqk,
                                  dim_v, max_kv_len, scale, _ptr(sink), P, _ptr(ws), ws_size,
                                  out.data_ptr(), _ptr(lse), _stream_handle(stream)))
+    return out, lse
+
+
+def attn_mla_decode_sparse(q: torch.Tensor, kv_cache: torch.Tensor, indices: torch.Tensor,
+                           topk_lengths: torch.Tensor, *, scale: float, dim_v: int = 512,
+                           sink: Optional[torch.Tensor] = None, num_partitions: int = 0,
+                           workspace: Optional[torch.Tensor] = None,
+                           out: Optional[torch.Tensor] = None, lse: Optional[torch.Tensor] = None,
+                           return_lse: bool = True, stream=None):
+    """Sparse top-k MLA decode through attn_mla_decode_sparse: q bf16
+    [batch, num_q_heads, 576]; kv_cache [num_pages, page_size, 1, 576] read as
+    rows (row r = slot r % page_size of page r // page_size); indices int32
+    [batch, indices_stride] naming each sequence's rows; topk_lengths int32
+    [batch] valid entries per row of indices."""
+    batch, hq, dqk = q.shape
+    if indices.dtype != torch.int32 or indices.dim() != 2 or not indices.is_contiguous():
+        raise ValueError("indices must be a contiguous int32 [batch, indices_stride] tensor")
+    if indices.shape[0] != batch or topk_lengths.shape[0] != batch:
+        raise ValueError("indices and topk_lengths need one row per sequence")
+    stride = indices.shape[1]
+    if out is None:
+        out = torch.empty((batch, hq, dim_v), dtype=torch.bfloat16, device=q.device)
+    if lse is None and return_lse:
+        lse = torch.empty((batch, hq), dtype=torch.float32, device=q.device)
+    P, ws_bytes = attn_plan_partitions(batch, batch, hq, 1, dim_v, stride, num_partitions)
+    ws, ws_size = _workspace(ws_bytes, q.device, workspace)
+    kd = kv_descriptor(kv_cache)
+    _check("attn_mla_decode_sparse",
+           lib().attn_mla_decode_sparse(q.data_ptr(), ctypes.byref(kd), indices.data_ptr(), stride,
+                                        topk_lengths.data_ptr(), batch, hq, dqk, dim_v, scale,
+                                        _ptr(sink), P, _ptr(ws), ws_size, out.data_ptr(),
+                                        _ptr(lse), _stream_handle(stream)))
     return out, lse
 
 

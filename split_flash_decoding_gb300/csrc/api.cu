@@ -250,8 +250,9 @@ extern "C" int attn_plan_partitions(int num_sms, int batch, int num_q_rows, int 
         // P is rounded up so that units * P is a multiple of the CTA count.
         // MLA runs one two-CTA cluster per SM pair per (slice, sequence) and
         // writes 256 KB of fp32 partials per slice, which the reduce reads
-        // back: slices of ~4096 keys, and at least one per cluster when the
-        // batch is smaller than the cluster count.
+        // back: slices of ~4096 keys, and as many slices per sequence as fit
+        // in one wave of clusters when that is more (a wave that spills over
+        // by a few clusters costs a whole extra round of tiles).
         const bool mla = num_kv_heads == 1 && head_dim_v == kMlaDimV;
         const bool tc = !mla && head_dim_v == 128;   // tensor-core decode: one CTA per SM
         const long long units = static_cast<long long>(batch > 0 ? batch : 1) * num_kv_heads;
@@ -260,7 +261,7 @@ extern "C" int attn_plan_partitions(int num_sms, int batch, int num_q_rows, int 
         const long long target = mla ? 4096 : 1024;
         long long p;
         if (mla) {
-            const long long p_fill = (ctas + units - 1) / units;
+            const long long p_fill = ctas / units > 0 ? ctas / units : 1;
             const long long p_len = (static_cast<long long>(max_kv_len) + target - 1) / target;
             p = p_fill > p_len ? p_fill : p_len;
         } else if (units < ctas) {
@@ -415,11 +416,50 @@ extern "C" int attn_decode(const void *q, const attn_kv_t *k, const attn_kv_t *v
     return map_cuda(launch_splitk_reduce(r, s, /*pdl=*/true));
 }
 
-extern "C" int attn_mla_decode(const void *q, const attn_kv_t *kv, const uint32_t *kv_len,
-                               int batch, int num_q_heads, int dim_qk, int dim_v, int max_kv_len,
-                               float scale, const float *sink, int num_partitions,
-                               void *workspace, size_t workspace_bytes, void *out, float *lse,
-                               attn_stream_t stream) {
+namespace {
+
+// A cache read as rows for sparse top-k: row r is slot r % page_size of page
+// r / page_size, so any page size (1 included) and any page order work.
+int check_kv_rows(const attn_kv_t *kv, int dim) {
+    if (!kv || !kv->base) return ATTN_ERR_INVALID_ARG;
+    if (kv->reserved != 0 || kv->page_table) return ATTN_ERR_INVALID_ARG;
+    if (reinterpret_cast<uintptr_t>(kv->base) % 16) return ATTN_ERR_INVALID_ARG;
+    if (kv->page_size <= 0 || kv->num_pages <= 0) return ATTN_ERR_INVALID_ARG;
+    if (kv->token_stride <= 0 || kv->head_stride <= 0 || kv->page_stride <= 0)
+        return ATTN_ERR_INVALID_ARG;
+    if (kv->token_stride % 8 || kv->head_stride % 8 || kv->page_stride % 8)
+        return ATTN_ERR_INVALID_ARG;
+    if (kv->head_stride < dim && kv->token_stride < dim) return ATTN_ERR_INVALID_ARG;
+    // rows at one uniform stride (a contiguous pool of pages)
+    if (kv->page_stride != static_cast<int64_t>(kv->page_size) * kv->token_stride)
+        return ATTN_ERR_UNSUPPORTED;
+    if (kv->token_stride < dim) return ATTN_ERR_INVALID_ARG;
+    return ATTN_OK;
+}
+
+// The cache as a 2-D row array (channel, row) for gather4: box 64 channels x
+// one row, 128-byte swizzle.
+int encode_rows_map(CUtensorMap *map, const attn_kv_t &kv, int dim) {
+    EncodeTiledFn fn = encode_fn();
+    if (!fn) return ATTN_ERR_CUDA;
+    const long long rows = static_cast<long long>(kv.num_pages) * kv.page_size;
+    cuuint64_t gdim[2] = {cuuint64_t(dim), cuuint64_t(rows)};
+    cuuint64_t gstride[1] = {cuuint64_t(kv.token_stride) * 2};
+    cuuint32_t box[2] = {64, 1};
+    cuuint32_t estride[2] = {1, 1};
+    CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void *>(kv.base), gdim,
+                    gstride, box, estride, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                    CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                    CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS ? ATTN_OK : ATTN_ERR_UNSUPPORTED;
+}
+
+// Shared body of the dense (paged or contiguous) and sparse MLA entry points.
+int mla_decode_impl(const void *q, const attn_kv_t *kv, const uint32_t *kv_len, bool sparse,
+                    const int32_t *indices, int indices_stride, int batch, int num_q_heads,
+                    int dim_qk, int dim_v, int max_kv_len, float scale, const float *sink,
+                    int num_partitions, void *workspace, size_t workspace_bytes, void *out,
+                    float *lse, attn_stream_t stream) {
     if (batch < 0 || num_q_heads <= 0 || dim_qk <= 0 || dim_v <= 0 || max_kv_len < 0)
         return ATTN_ERR_INVALID_ARG;
     if (num_partitions < 1 || num_partitions > ATTN_MAX_PARTITIONS) return ATTN_ERR_INVALID_ARG;
@@ -430,7 +470,8 @@ extern "C" int attn_mla_decode(const void *q, const attn_kv_t *kv, const uint32_
         return ATTN_ERR_UNSUPPORTED;
     if (reinterpret_cast<uintptr_t>(out) % 16 || reinterpret_cast<uintptr_t>(q) % 16)
         return ATTN_ERR_INVALID_ARG;
-    int st = check_kv(kv, batch, dim_qk, max_kv_len);
+    if (reinterpret_cast<uintptr_t>(indices) % 4) return ATTN_ERR_INVALID_ARG;
+    int st = sparse ? check_kv_rows(kv, dim_qk) : check_kv(kv, batch, dim_qk, max_kv_len);
     if (st) return st;
     if (static_cast<long long>(batch) * kMlaHeads > (1LL << 31)) return ATTN_ERR_UNSUPPORTED;
 
@@ -444,15 +485,21 @@ extern "C" int attn_mla_decode(const void *q, const attn_kv_t *kv, const uint32_
 
     MlaParams p;
     std::memset(&p, 0, sizeof(p));
-    p.box_rows = kv->page_table ? (kv->page_size < kMlaTileKeys ? kv->page_size : kMlaTileKeys)
-                                : kMlaTileKeys;
-    st = encode_kv_map(&p.kv_map, *kv, dim_qk, 1, p.box_rows);
+    p.box_rows = sparse ? 1
+                 : kv->page_table ? (kv->page_size < kMlaTileKeys ? kv->page_size : kMlaTileKeys)
+                                  : kMlaTileKeys;
+    st = sparse ? encode_rows_map(&p.kv_map, *kv, dim_qk)
+                : encode_kv_map(&p.kv_map, *kv, dim_qk, 1, p.box_rows);
     if (st) return st;
     p.q = static_cast<const uint16_t *>(q);
     st = error_word(&p.err);
     if (st) return st;
     p.kv_len = kv_len;
     p.page_table = kv->page_table;
+    p.sparse = sparse ? 1 : 0;
+    p.indices = indices;
+    p.indices_stride = indices_stride;
+    p.num_rows = static_cast<long long>(kv->num_pages) * kv->page_size;
     p.sink = sink;
     if (num_partitions > 1) {
         uint8_t *ws = static_cast<uint8_t *>(workspace);
@@ -488,7 +535,38 @@ extern "C" int attn_mla_decode(const void *q, const attn_kv_t *kv, const uint32_
     r.num_q_heads = num_q_heads;
     r.dim_v = dim_v;
     r.chunk = p.chunk;
+    r.len_cap = sparse ? indices_stride : 0;
     return map_cuda(launch_splitk_reduce(r, s, /*pdl=*/true));
+}
+
+}  // namespace
+
+extern "C" int attn_mla_decode(const void *q, const attn_kv_t *kv, const uint32_t *kv_len,
+                               int batch, int num_q_heads, int dim_qk, int dim_v, int max_kv_len,
+                               float scale, const float *sink, int num_partitions,
+                               void *workspace, size_t workspace_bytes, void *out, float *lse,
+                               attn_stream_t stream) {
+    return mla_decode_impl(q, kv, kv_len, false, nullptr, 0, batch, num_q_heads, dim_qk, dim_v,
+                           max_kv_len, scale, sink, num_partitions, workspace, workspace_bytes,
+                           out, lse, stream);
+}
+
+extern "C" int attn_mla_decode_sparse(const void *q, const attn_kv_t *kv,
+                                      const int32_t *indices, int indices_stride,
+                                      const int32_t *topk_lengths, int batch, int num_q_heads,
+                                      int dim_qk, int dim_v, float scale, const float *sink,
+                                      int num_partitions, void *workspace,
+                                      size_t workspace_bytes, void *out, float *lse,
+                                      attn_stream_t stream) {
+    if (indices_stride < 0) return ATTN_ERR_INVALID_ARG;
+    if (batch > 0 && indices_stride > 0 && !indices) return ATTN_ERR_INVALID_ARG;
+    if (batch > 0 && !topk_lengths) return ATTN_ERR_INVALID_ARG;
+    // topk_lengths is read as unsigned: a negative count is above any cap and
+    // is reported as a length error.
+    return mla_decode_impl(q, kv, reinterpret_cast<const uint32_t *>(topk_lengths), true,
+                           indices, indices_stride, batch, num_q_heads, dim_qk, dim_v, indices_stride,
+                           scale, sink, num_partitions, workspace, workspace_bytes, out, lse,
+                           stream);
 }
 
 extern "C" int attn_splitk_reduce(const float *ws_o, const float *ws_m, const float *ws_l,

@@ -51,10 +51,15 @@ constexpr int kMlaDimQK = 576;
 constexpr int kMlaDimV = 512;
 
 struct MlaParams {
-    CUtensorMap kv_map;           // 4-D: (channel 576, slot, head 1, page)
+    CUtensorMap kv_map;           // 4-D: (channel 576, slot, head 1, page); sparse:
+                                  // 2-D (channel 576, row), box height 1
     const uint16_t *q;            // bf16 [batch][128][576]
     const uint32_t *kv_len;       // [batch]
     const int32_t *page_table;    // [batch][max_pages] or nullptr
+    const int32_t *indices;       // sparse: [batch][indices_stride] cache rows
+    long long num_rows;           // sparse: rows in the cache (num_pages * page_size)
+    int sparse;                   // 1: keys are named by indices, kv_len = top-k counts
+    int indices_stride;
     const float *sink;            // [128] or nullptr
     float *ws_o;                  // [P][batch][128][512]
     float *ws_m;                  // [P][batch][128]
@@ -102,6 +107,7 @@ struct ReduceParams {
     int batch;
     int num_partitions, rows, num_q_heads, dim_v;
     int chunk;                    // slice length when kv_len is given
+    int len_cap;                  // > 0: kv_len is clamped to it as well as to P * chunk
 };
 
 cudaError_t launch_gqa_decode(const GqaParams &p, cudaStream_t stream);

@@ -61,8 +61,26 @@ constexpr int kStages = 4;
 constexpr int kMaxBoxes = 5;               // 64-channel boxes per rank (4 or 5)
 constexpr int kKBoxBytes = kBN * 128;      // 64 rows x 128 B
 constexpr int kStageBytes = kMaxBoxes * kKBoxBytes;
-constexpr int kThreads = 352;
 constexpr int kSoftmaxThreads = 256;   // warps 0-7
+
+// Warp roles.  Dense (paged or contiguous) caches: 352 threads, one TMA
+// producer warp (8), MMA warp 9, exchange warp 10.  Sparse top-k: 512 threads,
+// six cp.async producer warps (8-11, 14, 15), MMA warp 12, exchange warp 13;
+// the softmax warpgroups raise their register budget to 168 and the other
+// two lower theirs to 80 (256 x 168 + 256 x 80 <= 512 x 128 launched).
+template <bool kSparse>
+struct Layout {
+    static constexpr int kThreads = kSparse ? 512 : 352;
+    static constexpr int kMmaWarp = kSparse ? 12 : 9;
+    static constexpr int kXchgWarp = kSparse ? 13 : 10;
+    static constexpr int kProducers = kSparse ? 6 : 1;
+    // producer index of a warp, or -1
+    static __device__ __forceinline__ int producer(int warp) {
+        if (!kSparse) return warp == 8 ? 0 : -1;
+        if (warp >= 8 && warp < 12) return warp - 8;
+        return warp >= 14 ? warp - 10 : -1;
+    }
+};
 constexpr int kBarSoftmax = 1;         // named barrier of the softmax warps
 constexpr uint32_t kXBytes = 128u * kMlaTileKeys * 4u;   // one tile of fp32 partial scores
 constexpr uint32_t kXHalfBytes = kXBytes / 2;            // one key half (32 keys)
@@ -111,8 +129,10 @@ __device__ __forceinline__ uint32_t x_half_off(int hf, int h, int c) {
     return uint32_t(hf) * kXHalfBytes + uint32_t(h * 128 + (((c + h) & 7) << 4));
 }
 
-__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
+template <bool kSparse>
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Layout<kSparse>::kThreads, 1)
 mla_decode_kernel(const __grid_constant__ MlaParams p) {
+    using Roles = Layout<kSparse>;
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -128,7 +148,8 @@ mla_decode_kernel(const __grid_constant__ MlaParams p) {
     const int nbox = rank == 0 ? 4 : 5;
     const int col0 = rank == 0 ? 0 : 256;
 
-    const uint32_t cap = uint32_t(p.num_partitions) * uint32_t(p.chunk);
+    uint32_t cap = uint32_t(p.num_partitions) * uint32_t(p.chunk);
+    if (kSparse) cap = min(cap, uint32_t(p.indices_stride));   // keys a sequence can name
     const uint32_t len_in = p.kv_len[b];
     if (len_in > cap && part == 0 && threadIdx.x == 0 && rank == 0)
         atomicOr(p.err, kErrBadLength);
@@ -142,7 +163,7 @@ mla_decode_kernel(const __grid_constant__ MlaParams p) {
 
     if (threadIdx.x == 0) {
         for (int i = 0; i < kStages; ++i) {
-            mbar_init(&bar[kKvFull + i], 1);
+            mbar_init(&bar[kKvFull + i], Roles::kProducers);
             mbar_init(&bar[kKvEmpty + i], 1);
         }
         mbar_init(&bar[kQFull], 8);   // the eight softmax warps, after Q is in TMEM
@@ -158,7 +179,7 @@ mla_decode_kernel(const __grid_constant__ MlaParams p) {
         }
         fence_mbar_init();
     }
-    if (warp == 9) {
+    if (warp == Roles::kMmaWarp) {
         tc::tmem_alloc(tmem_slot, kTmemCols);
         tc::tmem_relinquish();
     }
@@ -168,159 +189,233 @@ mla_decode_kernel(const __grid_constant__ MlaParams p) {
     tc::fence_after_sync();
     const uint32_t tmem = *tmem_slot;
 
-    if (warp == 8) {
-        // ------------------------------------------------------------ producer
-        if (ntiles > 0) {
-            if (lane == 0) prefetch_tensormap(&p.kv_map);
-            const int box_rows = p.box_rows;
-            const int boxes_per_tile = kBN / box_rows;   // 1..8
-            bool aborted = false;
-            int issued = 0;
-            for (int base = 0; base < ntiles && !aborted; base += 32) {
-                // lane i resolves the pages of tile base + i (up to 8 row boxes)
-                int pg[8], sl[8];
+    const int pidx = Roles::producer(warp);
+    if (warp >= 8) {
+        if constexpr (kSparse) setmaxnreg_dec<80>();   // same instruction for both warpgroups
+        if (pidx >= 0) {
+            // ------------------------------------------------------------ producer
+            if constexpr (kSparse) {
+                if (ntiles > 0) {
+                    // Sparse top-k: key j of the sequence is cache row indices[b][j]
+                    // (rows at a uniform stride).  Rows are scattered, so a tile
+                    // arrives as gather4 copies (four rows x one 64-channel box,
+                    // 512 bytes, swizzled like a tiled load): 16 row groups x
+                    // nbox boxes per tile, spread over the six producer warps, one
+                    // copy per lane (warp w, lane l takes copy w + 6 l).  Each warp
+                    // posts the bytes of its own copies on the stage barrier, so
+                    // the stage is full when all six warps' copies have landed and
+                    // the producers run up to kStages tiles ahead, as for a dense
+                    // cache.  A key past the slice end, or an index outside the
+                    // cache (reported), reads row 0 in its place; the softmax
+                    // masks the former and the error word reports the latter.
+                    // The indices of tile i + 1 are loaded while tile i waits for
+                    // its stage.
+                    const int nq = 16 * nbox;
+                    const int q = pidx + Roles::kProducers * lane;
+                    const bool mine = q < nq;
+                    const int g = mine ? q / nbox : 0;        // rows 4g .. 4g + 3 of the tile
+                    const int cb = mine ? q - g * nbox : 0;   // 64-channel box
+                    const int32_t *idx = p.indices + size_t(b) * size_t(p.indices_stride);
+                    auto load4 = [&](int tile, int (&r)[4]) {
 #pragma unroll
-                for (int r = 0; r < 8; ++r) { pg[r] = -1; sl[r] = 0; }
-                const int my_tile = base + lane;
-                if (my_tile < ntiles) {
-                    const int t0 = start + my_tile * kBN;
-#pragma unroll
-                    for (int r = 0; r < 8; ++r) {
-                        const int t = t0 + r * box_rows;
-                        if (r >= boxes_per_tile || t >= L) continue;
-                        if (p.page_table) {
-                            const int pidx = t / p.page_size;
-                            int e = pidx < p.max_pages
-                                        ? p.page_table[size_t(b) * p.max_pages + pidx] : -1;
-                            if (e < 0 || e >= p.num_pages) {
-                                atomicOr(p.err, kErrBadPage);
-                                e = -1;
-                            }
-                            pg[r] = e;
-                            sl[r] = t % p.page_size;
-                        } else {
-                            pg[r] = b;
-                            sl[r] = t;
+                        for (int u = 0; u < 4; ++u) {
+                            const int t = start + tile * kBN + 4 * g + u;
+                            r[u] = (mine && tile < ntiles && t < end) ? __ldg(idx + t) : 0;
                         }
-                    }
-                }
-                const int lim = min(base + 32, ntiles);
-                for (int i = base; i < lim; ++i) {
-                    int pages[8], slots[8];
-#pragma unroll
-                    for (int r = 0; r < 8; ++r) {
-                        pages[r] = __shfl_sync(0xffffffffu, pg[r], i - base);
-                        slots[r] = __shfl_sync(0xffffffffu, sl[r], i - base);
-                    }
-                    if (lane == 0) {
+                    };
+                    if (lane == 0) prefetch_tensormap(&p.kv_map);
+                    int cur[4], nxt[4];
+                    load4(0, cur);
+                    int issued = 0;
+                    for (int i = 0; i < ntiles; ++i) {
+                        load4(i + 1, nxt);
                         const int s = i % kStages;
-                        if (i >= kStages &&
-                            !mbar_wait(&bar[kKvEmpty + s], ((i / kStages) - 1) & 1, p.err)) {
-                            aborted = true;
-                        } else {
-                            uint32_t nrow = 0;
+                        bool ok = true;
+                        if (lane == 0 && i >= kStages)
+                            ok = mbar_wait(&bar[kKvEmpty + s], ((i / kStages) - 1) & 1, p.err);
+                        if (!__shfl_sync(0xffffffffu, ok, 0)) break;
+                        const int t_g = start + i * kBN + 4 * g;
+                        const bool live = mine && t_g < end;
+                        bool bad = false;
 #pragma unroll
-                            for (int r = 0; r < 8; ++r) nrow += pages[r] >= 0 ? 1u : 0u;
-                            mbar_arrive_expect_tx(&bar[kKvFull + s],
-                                                  nrow * uint32_t(nbox) * uint32_t(box_rows) * 128u);
-                            uint8_t *st = smem + Smem::kv + s * kStageBytes;
+                        for (int u = 0; u < 4; ++u) {
+                            if (cur[u] < 0 || static_cast<long long>(cur[u]) >= p.num_rows) {
+                                bad = true;
+                                cur[u] = 0;
+                            }
+                        }
+                        if (live && bad) atomicOr(p.err, kErrBadPage);
+                        const uint32_t n = __popc(__ballot_sync(0xffffffffu, live));
+                        if (lane == 0) mbar_arrive_expect_tx(&bar[kKvFull + s], n * 512u);
+                        __syncwarp();   // the expected bytes are posted before any copy lands
+                        if (live)
+                            tma_gather4(smem + Smem::kv + s * kStageBytes + cb * kKBoxBytes +
+                                            g * 512,
+                                        &p.kv_map, &bar[kKvFull + s], col0 + cb * 64, cur[0],
+                                        cur[1], cur[2], cur[3]);
+                        issued = i + 1;
 #pragma unroll
-                            for (int r = 0; r < 8; ++r) {
-                                if (pages[r] < 0) continue;
-                                for (int cb = 0; cb < nbox; ++cb)
-                                    tma_load_4d(st + cb * kKBoxBytes + r * box_rows * 128,
-                                                &p.kv_map, &bar[kKvFull + s], col0 + cb * 64,
-                                                slots[r], 0, pages[r]);
+                        for (int u = 0; u < 4; ++u) cur[u] = nxt[u];
+                    }
+                    // every copy this warp issued must land before the CTA may leave
+                    if (lane == 0) {
+                        for (int i = max(0, issued - kStages); i < issued; ++i)
+                            mbar_wait(&bar[kKvFull + i % kStages], (i / kStages) & 1, p.err);
+                    }
+                }
+            } else if (ntiles > 0) {
+                if (lane == 0) prefetch_tensormap(&p.kv_map);
+                const int box_rows = p.box_rows;
+                const int boxes_per_tile = kBN / box_rows;   // 1..8
+                bool aborted = false;
+                int issued = 0;
+                for (int base = 0; base < ntiles && !aborted; base += 32) {
+                    // lane i resolves the pages of tile base + i (up to 8 row boxes)
+                    int pg[8], sl[8];
+    #pragma unroll
+                    for (int r = 0; r < 8; ++r) { pg[r] = -1; sl[r] = 0; }
+                    const int my_tile = base + lane;
+                    if (my_tile < ntiles) {
+                        const int t0 = start + my_tile * kBN;
+    #pragma unroll
+                        for (int r = 0; r < 8; ++r) {
+                            const int t = t0 + r * box_rows;
+                            if (r >= boxes_per_tile || t >= L) continue;
+                            if (p.page_table) {
+                                const int pidx = t / p.page_size;
+                                int e = pidx < p.max_pages
+                                            ? p.page_table[size_t(b) * p.max_pages + pidx] : -1;
+                                if (e < 0 || e >= p.num_pages) {
+                                    atomicOr(p.err, kErrBadPage);
+                                    e = -1;
+                                }
+                                pg[r] = e;
+                                sl[r] = t % p.page_size;
+                            } else {
+                                pg[r] = b;
+                                sl[r] = t;
                             }
                         }
                     }
-                    aborted = __shfl_sync(0xffffffffu, aborted, 0);
-                    if (aborted) break;
-                    issued = i + 1;
-                }
-            }
-            // every copy this warp issued must land before the CTA may leave
-            if (lane == 0) {
-                for (int i = max(0, issued - kStages); i < issued; ++i)
-                    mbar_wait(&bar[kKvFull + i % kStages], (i / kStages) & 1, p.err);
-            }
-        }
-    } else if (warp == 9) {
-        // ------------------------------------------------------------ MMA issue
-        if (ntiles > 0 && lane == 0) {
-            constexpr uint32_t idesc_s = tc::idesc_bf16_f32(128, kBN, 0, 0);
-            constexpr uint32_t idesc_o = tc::idesc_bf16_f32(128, 256, 0, 1);
-            const uint32_t kv_base = smem_addr(smem + Smem::kv);
-            // S(t) = Q K^T over this CTA's channels.  Descriptors advance by
-            // byte offset / 16 in their start field; the loops are unrolled so
-            // issue is not bound by descriptor arithmetic.
-            auto issue_s = [&](int t) -> bool {
-                const int s = t % kStages;
-                if (!mbar_wait(&bar[kKvFull + s], (t / kStages) & 1, p.err)) return false;
-                if (t >= 1 && !mbar_wait(&bar[kSFree], (t - 1) & 1, p.err)) return false;
-                tc::fence_after_sync();
-                const uint64_t b0 = tc::smem_desc_sw128(kv_base + s * kStageBytes, 16, 1024);
-#pragma unroll
-                for (int ks = 0; ks < 16; ++ks)
-                    // A = Q from TMEM: 16 channels = 8 columns of bf16 pairs per step
-                    tc::mma_bf16_tmem_a(tmem + kTmemS, tmem + kTmemQ + ks * 8,
-                                        b0 + uint64_t(((ks >> 2) * kKBoxBytes + (ks & 3) * 32) >> 4),
-                                        idesc_s, ks > 0);
-                if (nbox == 5) {
-#pragma unroll
-                    for (int ks = 16; ks < 20; ++ks)
-                        tc::mma_bf16_tmem_a(tmem + kTmemS, tmem + kTmemQ + ks * 8,
-                                            b0 + uint64_t((4 * kKBoxBytes + (ks & 3) * 32) >> 4),
-                                            idesc_s, true);
-                }
-                tc::mma_commit(&bar[kSFull]);
-                return true;
-            };
-            bool ok = mbar_wait(&bar[kQFull], 0, p.err);
-            if (ok) ok = issue_s(0);
-            if (ok && ntiles > 1) ok = issue_s(1);
-            for (int t = 0; ok && t < ntiles; ++t) {
-                if (t + 2 < ntiles && !(ok = issue_s(t + 2))) break;
-                ok = mbar_wait(&bar[kPFull], t & 1, p.err);
-                if (!ok) break;
-                tc::fence_after_sync();
-                const uint64_t v0 = tc::smem_desc_sw128(kv_base + (t % kStages) * kStageBytes,
-                                                        kVLbo, kVSbo);
-#pragma unroll
-                for (int kk = 0; kk < kBN / 16; ++kk)
-                    // A = P from TMEM: 16 keys = 8 columns of bf16 pairs per step
-                    tc::mma_bf16_tmem_a(tmem + kTmemO, tmem + kTmemP + kk * 8,
-                                        v0 + uint64_t((kk * 16 * 128) >> 4), idesc_o,
-                                        t > 0 || kk > 0);
-                tc::mma_commit(&bar[kODone]);
-                tc::mma_commit(&bar[kKvEmpty + (t % kStages)]);
-            }
-        }
-    } else if (warp == 10) {
-        // ------------------------------------------------------------ exchange
-        if (ntiles > 0 && lane == 0) {
-            const uint32_t dst = mapa_shared(smem_addr(smem + Smem::x_in), peer);
-            const uint32_t dst_bar = mapa_shared(smem_addr(&bar[kXFull]), peer);
-            const uint32_t src = smem_addr(smem + Smem::x_out);
-            // The two key halves go one after the other, so one half is
-            // staged while the other is on the wire.
-            bool run = true;
-            for (int t = 0; run && t < ntiles; ++t) {
-                for (int hf = 0; hf < 2; ++hf) {
-                    if (!mbar_wait(&bar[kXoReady + hf], t & 1, p.err) ||
-                        (t >= 1 &&
-                         !mbar_wait_cluster(&bar[kXPeerFree + hf], (t - 1) & 1, p.err))) {
-                        run = false;
-                        break;
+                    const int lim = min(base + 32, ntiles);
+                    for (int i = base; i < lim; ++i) {
+                        int pages[8], slots[8];
+    #pragma unroll
+                        for (int r = 0; r < 8; ++r) {
+                            pages[r] = __shfl_sync(0xffffffffu, pg[r], i - base);
+                            slots[r] = __shfl_sync(0xffffffffu, sl[r], i - base);
+                        }
+                        if (lane == 0) {
+                            const int s = i % kStages;
+                            if (i >= kStages &&
+                                !mbar_wait(&bar[kKvEmpty + s], ((i / kStages) - 1) & 1, p.err)) {
+                                aborted = true;
+                            } else {
+                                uint32_t nrow = 0;
+    #pragma unroll
+                                for (int r = 0; r < 8; ++r) nrow += pages[r] >= 0 ? 1u : 0u;
+                                mbar_arrive_expect_tx(&bar[kKvFull + s],
+                                                      nrow * uint32_t(nbox) * uint32_t(box_rows) * 128u);
+                                uint8_t *st = smem + Smem::kv + s * kStageBytes;
+    #pragma unroll
+                                for (int r = 0; r < 8; ++r) {
+                                    if (pages[r] < 0) continue;
+                                    for (int cb = 0; cb < nbox; ++cb)
+                                        tma_load_4d(st + cb * kKBoxBytes + r * box_rows * 128,
+                                                    &p.kv_map, &bar[kKvFull + s], col0 + cb * 64,
+                                                    slots[r], 0, pages[r]);
+                                }
+                            }
+                        }
+                        aborted = __shfl_sync(0xffffffffu, aborted, 0);
+                        if (aborted) break;
+                        issued = i + 1;
                     }
-                    bulk_copy_to_peer(dst + hf * kXHalfBytes, src + hf * kXHalfBytes,
-                                      kXHalfBytes, dst_bar + 8u * hf);
-                    bulk_wait_read();
-                    mbar_arrive(&bar[kXoFree + hf]);
+                }
+                // every copy this warp issued must land before the CTA may leave
+                if (lane == 0) {
+                    for (int i = max(0, issued - kStages); i < issued; ++i)
+                        mbar_wait(&bar[kKvFull + i % kStages], (i / kStages) & 1, p.err);
+                }
+            }
+        } else if (warp == Roles::kMmaWarp) {
+            // ------------------------------------------------------------ MMA issue
+            if (ntiles > 0 && lane == 0) {
+                constexpr uint32_t idesc_s = tc::idesc_bf16_f32(128, kBN, 0, 0);
+                constexpr uint32_t idesc_o = tc::idesc_bf16_f32(128, 256, 0, 1);
+                const uint32_t kv_base = smem_addr(smem + Smem::kv);
+                // S(t) = Q K^T over this CTA's channels.  Descriptors advance by
+                // byte offset / 16 in their start field; the loops are unrolled so
+                // issue is not bound by descriptor arithmetic.
+                auto issue_s = [&](int t) -> bool {
+                    const int s = t % kStages;
+                    if (!mbar_wait(&bar[kKvFull + s], (t / kStages) & 1, p.err)) return false;
+                    if (t >= 1 && !mbar_wait(&bar[kSFree], (t - 1) & 1, p.err)) return false;
+                    tc::fence_after_sync();
+                    const uint64_t b0 = tc::smem_desc_sw128(kv_base + s * kStageBytes, 16, 1024);
+    #pragma unroll
+                    for (int ks = 0; ks < 16; ++ks)
+                        // A = Q from TMEM: 16 channels = 8 columns of bf16 pairs per step
+                        tc::mma_bf16_tmem_a(tmem + kTmemS, tmem + kTmemQ + ks * 8,
+                                            b0 + uint64_t(((ks >> 2) * kKBoxBytes + (ks & 3) * 32) >> 4),
+                                            idesc_s, ks > 0);
+                    if (nbox == 5) {
+    #pragma unroll
+                        for (int ks = 16; ks < 20; ++ks)
+                            tc::mma_bf16_tmem_a(tmem + kTmemS, tmem + kTmemQ + ks * 8,
+                                                b0 + uint64_t((4 * kKBoxBytes + (ks & 3) * 32) >> 4),
+                                                idesc_s, true);
+                    }
+                    tc::mma_commit(&bar[kSFull]);
+                    return true;
+                };
+                bool ok = mbar_wait(&bar[kQFull], 0, p.err);
+                if (ok) ok = issue_s(0);
+                if (ok && ntiles > 1) ok = issue_s(1);
+                for (int t = 0; ok && t < ntiles; ++t) {
+                    if (t + 2 < ntiles && !(ok = issue_s(t + 2))) break;
+                    ok = mbar_wait(&bar[kPFull], t & 1, p.err);
+                    if (!ok) break;
+                    tc::fence_after_sync();
+                    const uint64_t v0 = tc::smem_desc_sw128(kv_base + (t % kStages) * kStageBytes,
+                                                            kVLbo, kVSbo);
+    #pragma unroll
+                    for (int kk = 0; kk < kBN / 16; ++kk)
+                        // A = P from TMEM: 16 keys = 8 columns of bf16 pairs per step
+                        tc::mma_bf16_tmem_a(tmem + kTmemO, tmem + kTmemP + kk * 8,
+                                            v0 + uint64_t((kk * 16 * 128) >> 4), idesc_o,
+                                            t > 0 || kk > 0);
+                    tc::mma_commit(&bar[kODone]);
+                    tc::mma_commit(&bar[kKvEmpty + (t % kStages)]);
+                }
+            }
+        } else if (warp == Roles::kXchgWarp) {
+            // ------------------------------------------------------------ exchange
+            if (ntiles > 0 && lane == 0) {
+                const uint32_t dst = mapa_shared(smem_addr(smem + Smem::x_in), peer);
+                const uint32_t dst_bar = mapa_shared(smem_addr(&bar[kXFull]), peer);
+                const uint32_t src = smem_addr(smem + Smem::x_out);
+                // The two key halves go one after the other, so one half is
+                // staged while the other is on the wire.
+                bool run = true;
+                for (int t = 0; run && t < ntiles; ++t) {
+                    for (int hf = 0; hf < 2; ++hf) {
+                        if (!mbar_wait(&bar[kXoReady + hf], t & 1, p.err) ||
+                            (t >= 1 &&
+                             !mbar_wait_cluster(&bar[kXPeerFree + hf], (t - 1) & 1, p.err))) {
+                            run = false;
+                            break;
+                        }
+                        bulk_copy_to_peer(dst + hf * kXHalfBytes, src + hf * kXHalfBytes,
+                                          kXHalfBytes, dst_bar + 8u * hf);
+                        bulk_wait_read();
+                        mbar_arrive(&bar[kXoFree + hf]);
+                    }
                 }
             }
         }
     } else {
+        if constexpr (kSparse) setmaxnreg_inc<168>();
         // ------------------------------------------------------------ softmax
         const int h = (warp & 3) * 32 + lane;    // head row == TMEM lane
         const int half = warp >> 2;              // keys [32 half, 32 half + 32)
@@ -600,22 +695,27 @@ mla_decode_kernel(const __grid_constant__ MlaParams p) {
     tc::fence_before_sync();
     __syncthreads();
     cluster_sync();  // no CTA leaves while its peer may still touch its smem
-    if (warp == 9) {
+    if (warp == Roles::kMmaWarp) {
         tc::fence_after_sync();
         tc::tmem_dealloc(tmem, kTmemCols);
     }
 }
 
-}  // namespace
-
-cudaError_t launch_mla_decode(const MlaParams &p, cudaStream_t stream) {
-    cudaError_t e = cudaFuncSetAttribute(mla_decode_kernel,
+template <bool kSparse>
+cudaError_t launch_layout(const MlaParams &p, cudaStream_t stream) {
+    cudaError_t e = cudaFuncSetAttribute(mla_decode_kernel<kSparse>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          int(kSmemBytes));
     if (e != cudaSuccess) return e;
     dim3 grid(2 * p.num_partitions, p.batch);
-    mla_decode_kernel<<<grid, kThreads, kSmemBytes, stream>>>(p);
+    mla_decode_kernel<kSparse><<<grid, Layout<kSparse>::kThreads, kSmemBytes, stream>>>(p);
     return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_mla_decode(const MlaParams &p, cudaStream_t stream) {
+    return p.sparse ? launch_layout<true>(p, stream) : launch_layout<false>(p, stream);
 }
 
 }  // namespace attn

@@ -52,7 +52,8 @@ splitk_reduce_kernel(const __grid_constant__ ReduceParams p) {
     int P = p.num_partitions;
     if (p.kv_len) {
         // Rows that fit in one slice were finished by the partition kernel.
-        const uint32_t cap = uint32_t(p.num_partitions) * uint32_t(p.chunk);
+        uint32_t cap = uint32_t(p.num_partitions) * uint32_t(p.chunk);
+        if (p.len_cap > 0) cap = min(cap, uint32_t(p.len_cap));
         const uint32_t L = min(p.kv_len[row_sequence(p, row)], cap);
         const int ns = static_cast<int>((L + p.chunk - 1) / p.chunk);
         if (ns < 2) return;  // uniform over the warp
@@ -125,7 +126,8 @@ splitk_reduce_wide_kernel(const __grid_constant__ ReduceParams p) {
 
     int P = p.num_partitions;
     if (p.kv_len) {
-        const uint32_t cap = uint32_t(p.num_partitions) * uint32_t(p.chunk);
+        uint32_t cap = uint32_t(p.num_partitions) * uint32_t(p.chunk);
+        if (p.len_cap > 0) cap = min(cap, uint32_t(p.len_cap));
         const uint32_t L = min(p.kv_len[row_sequence(p, row)], cap);
         const int ns = static_cast<int>((L + p.chunk - 1) / p.chunk);
         if (ns < 2) return;  // uniform over the CTA

@@ -16,6 +16,11 @@ Layouts produced (all bf16 unless noted):
 * contiguous   [batch, capacity, num_kv_heads, dim]: sequence b is "page" b.
 * kv_len       int32 [batch], q_row_offsets int32 [batch + 1] or None,
                sink fp32 [num_q_heads] or None.
+* sparse top-k a one-head row pool [num_pages, page_size, 1, dim] read as
+               rows (row r = slot r % page_size of page r // page_size), an
+               index list int32 [batch, indices_stride] of the rows each
+               sequence attends to (-1 past its count) and kv_len = the
+               per-sequence counts.
 
 Values are N(0, 1) drawn in fp32 from a torch.Generator seeded per workload,
 then rounded to bf16; lengths and the page permutation come from a CPU
@@ -47,6 +52,7 @@ class Workload:
     scale: float                         # exactly representable in fp32
     sink: Optional[torch.Tensor]
     causal: bool
+    indices: Optional[torch.Tensor] = None   # sparse top-k rows [batch, stride], else None
 
     @property
     def batch(self) -> int:
@@ -87,7 +93,8 @@ class Workload:
         mv = lambda t: None if t is None else t.to(device)
         return replace(self, q=mv(self.q), k_cache=mv(self.k_cache), v_cache=mv(self.v_cache),
                        page_table=mv(self.page_table), kv_len=mv(self.kv_len),
-                       q_row_offsets=mv(self.q_row_offsets), sink=mv(self.sink))
+                       q_row_offsets=mv(self.q_row_offsets), sink=mv(self.sink),
+                       indices=mv(self.indices))
 
 
 def fp32(x: float) -> float:
@@ -161,6 +168,54 @@ def make_workload(name: str, *, batch: int, num_q_heads: int, num_kv_heads: int,
                     page_size=ps, kv_len=kv_len, kv_len_host=kv_lens, q_row_offsets=offs,
                     q_row_offsets_host=offs_host, group=num_q_heads // num_kv_heads,
                     dim_v=dim_v, scale=scale, sink=sk, causal=causal)
+
+
+def make_sparse_mla_workload(name: str, *, ctx_lens, topk: int, page_size: int, seed: int,
+                             device="cpu", num_q_heads: int = 128, dim_qk: int = 576,
+                             dim_v: int = 512, sink: bool = False,
+                             scale: Optional[float] = None,
+                             replace_rows: bool = False) -> Workload:
+    """Sparse top-k MLA decode: sequence b has a context of ctx_lens[b] tokens
+    in a paged one-head pool (random page permutation, as make_workload) and
+    attends to min(topk, ctx_lens[b]) of them, a seeded random choice in
+    random order (replace_rows: drawn with repetition).  Each chosen token t
+    is named by its physical row page_table[b, t // page_size] * page_size +
+    t % page_size; the page table itself is not part of the workload."""
+    ctx = [int(x) for x in ctx_lens]
+    batch = len(ctx)
+    base = make_workload(name, batch=batch, num_q_heads=num_q_heads, num_kv_heads=1,
+                         dim_qk=dim_qk, dim_v=dim_v, mla=True, kv_lens=ctx,
+                         page_size=page_size, seed=seed, device=device, sink=sink, scale=scale)
+    g = torch.Generator()
+    g.manual_seed(seed + 104729)
+    counts = [min(int(topk), c) for c in ctx]
+    stride = max(max(counts, default=0), 1)
+    idx = torch.full((batch, stride), -1, dtype=torch.int64)
+    pt = base.page_table.cpu().long()
+    for b, (c, n) in enumerate(zip(ctx, counts)):
+        if n == 0:
+            continue
+        if replace_rows:
+            t = torch.randint(0, c, (n,), generator=g)
+        else:
+            t = torch.randperm(c, generator=g)[:n]
+        idx[b, :n] = pt[b, t // page_size] * page_size + t % page_size
+    dev = torch.device(device)
+    return replace(base, page_table=None, kv_len=torch.tensor(counts, dtype=torch.int32,
+                                                                 device=dev),
+                   kv_len_host=counts, indices=idx.to(torch.int32).to(dev))
+
+
+def deepseek_v32_sparse_mla_decode(device="cpu", seed: int = 7, batch: int = 128,
+                                   topk: int = 2048) -> Workload:
+    """DeepSeek-V3.2-shaped sparse MLA decode: batch 128, 128 q heads, one KV
+    head of depth 576, V = K[:, :512], contexts uniform in [1024, 32768] in a
+    page-64 pool, top-2048 rows per sequence (all rows when the context is
+    shorter), scale 1/sqrt(192)."""
+    ctx = _uniform_ints(1024, 32768, batch, seed)
+    return make_sparse_mla_workload(f"deepseek_v32_sparse_mla_decode_b{batch}_top{topk}_h128_d576",
+                                    ctx_lens=ctx, topk=topk, page_size=64, seed=seed,
+                                    device=device, scale=1.0 / math.sqrt(192.0))
 
 
 def contiguous_copy(w: Workload, capacity: Optional[int] = None) -> Workload:

@@ -22,6 +22,8 @@ LSE_REL = 1e-4
 
 def oracle_kv(w, cache):
     cache = cache.cpu()
+    if w.indices is not None:
+        return oracle.KV.sparse(cache, w.indices.cpu())
     if w.page_table is not None:
         return oracle.KV.paged(cache, w.page_table.cpu())
     return oracle.KV.contiguous(cache)

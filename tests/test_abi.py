@@ -124,6 +124,49 @@ def test_decode_rejects_bad_arguments_before_launch(attn):
     assert call_decode(attn, batch=0, q=None, out=None) == E.ATTN_OK
 
 
+def call_sparse(attn, k=None, **over):
+    args = dict(q=0x30000, idx=0x80000, stride=2048, topk=0x40000, batch=2, hq=128, dqk=576,
+                dv=512, scale=0.07, sink=None, P=1, ws=None, ws_bytes=0, out=0x50000, lse=None)
+    args.update(over)
+    k = k or kv(attn, page_table=None, page_stride=64 * 576, token_stride=576, head_stride=576,
+                page_size=64, num_pages=100)
+    return attn.lib().attn_mla_decode_sparse(args["q"], ctypes.byref(k), args["idx"],
+                                             args["stride"], args["topk"], args["batch"],
+                                             args["hq"], args["dqk"], args["dv"], args["scale"],
+                                             args["sink"], args["P"], args["ws"],
+                                             args["ws_bytes"], args["out"], args["lse"], None)
+
+
+def test_sparse_mla_rejects_bad_arguments_before_launch(attn):
+    E = attn
+    rows = dict(page_table=None, page_stride=64 * 576, token_stride=576, head_stride=576,
+                page_size=64, num_pages=100)
+    assert call_sparse(attn, q=None) == E.ATTN_ERR_INVALID_ARG
+    assert call_sparse(attn, out=None) == E.ATTN_ERR_INVALID_ARG
+    assert call_sparse(attn, topk=None) == E.ATTN_ERR_INVALID_ARG
+    assert call_sparse(attn, idx=None) == E.ATTN_ERR_INVALID_ARG       # stride > 0 needs indices
+    assert call_sparse(attn, idx=0x80002) == E.ATTN_ERR_INVALID_ARG    # misaligned int32
+    assert call_sparse(attn, stride=-1) == E.ATTN_ERR_INVALID_ARG
+    assert call_sparse(attn, hq=64) == E.ATTN_ERR_UNSUPPORTED
+    assert call_sparse(attn, dqk=512) == E.ATTN_ERR_UNSUPPORTED
+    assert call_sparse(attn, P=0) == E.ATTN_ERR_INVALID_ARG
+    assert call_sparse(attn, scale=float("nan")) == E.ATTN_ERR_INVALID_ARG
+    # the indices replace the page table; row strides keep the 16-byte rule
+    assert call_sparse(attn, k=kv(attn, **dict(rows, page_table=0x20000))) \
+        == E.ATTN_ERR_INVALID_ARG
+    assert call_sparse(attn, k=kv(attn, **dict(rows, token_stride=580))) \
+        == E.ATTN_ERR_INVALID_ARG
+    assert call_sparse(attn, k=kv(attn, **dict(rows, page_size=0))) == E.ATTN_ERR_INVALID_ARG
+    # rows must sit at one stride: padded pages are not a row array
+    assert call_sparse(attn, k=kv(attn, **dict(rows, page_stride=65 * 576))) \
+        == E.ATTN_ERR_UNSUPPORTED
+    assert call_sparse(attn, k=kv(attn, **dict(rows, base=0x10008))) == E.ATTN_ERR_INVALID_ARG
+    # split-K needs a large enough workspace
+    assert call_sparse(attn, P=4) == E.ATTN_ERR_WORKSPACE
+    # an empty batch is a no-op
+    assert call_sparse(attn, batch=0, q=None, out=None, topk=None) == E.ATTN_OK
+
+
 def test_reduce_rejects_bad_arguments(attn):
     L = attn.lib()
     f = L.attn_splitk_reduce
@@ -158,6 +201,11 @@ def test_planner_formulas(attn):
     assert P == 8
     P, _ = attn.attn_plan_partitions(1, 1, 128, 1, 512, 131072, 0, num_sms=152)
     assert P == 76
+    # short (sparse top-k) spans: as many slices as one wave of 76 clusters holds
+    P, _ = attn.attn_plan_partitions(32, 32, 128, 1, 512, 2048, 0, num_sms=152)
+    assert P == 2
+    P, _ = attn.attn_plan_partitions(128, 128, 128, 1, 512, 2048, 0, num_sms=152)
+    assert P == 1
     P, _ = attn.attn_plan_partitions(1, 1, 32, 8, 128, 20, 0, num_sms=152)
     assert P == 1                                     # one tile of keys cannot split
     P, _ = attn.attn_plan_partitions(4, 4, 32, 8, 128, 0, 0, num_sms=152)

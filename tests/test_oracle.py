@@ -481,3 +481,19 @@ def test_workload_generators_are_seeded():
     assert torch.equal(a.page_table, b.page_table)
     assert torch.equal(a.q.view(torch.int16), b.q.view(torch.int16))
     assert all(512 <= L <= 8192 for L in a.kv_len_host)
+
+
+def test_sparse_workload_names_rows_of_the_pool():
+    w = W.make_sparse_mla_workload("s", ctx_lens=[0, 5, 300, 1000], topk=256, page_size=16,
+                                   seed=3, dim_qk=32, dim_v=16, num_q_heads=4)
+    rows = w.k_cache.shape[0] * w.k_cache.shape[1]
+    assert w.kv_len_host == [0, 5, 256, 256]
+    assert w.indices.shape == (4, 256) and w.page_table is None
+    for b, n in enumerate(w.kv_len_host):
+        r = w.indices[b, :n]
+        assert bool(((r >= 0) & (r < rows)).all())
+        assert len(set(r.tolist())) == n                  # drawn without repetition
+        assert bool((w.indices[b, n:] == -1).all())
+    again = W.make_sparse_mla_workload("s", ctx_lens=[0, 5, 300, 1000], topk=256, page_size=16,
+                                       seed=3, dim_qk=32, dim_v=16, num_q_heads=4)
+    assert torch.equal(w.indices, again.indices)
