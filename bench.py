@@ -7,7 +7,7 @@ head_dim 128, ragged kv_len uniform in [512, 8192], paged cache with page
 one attn_decode call (partition kernel + split-K reduce) over that batch.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
-                    [--workload llama3|long_context|mla|sparse_mla|mixed|few_token|tiny]
+                    [--workload llama3|long_context|mla|mla_mtp|sparse_mla|mixed|few_token|tiny]
 
 Prints one JSON line (rank 0).  The metric is achieved HBM bandwidth:
 algorithmic bytes per call (visible K + V, plus q, out and lse) over the
@@ -71,8 +71,8 @@ def parse():
     ap.add_argument("--warmup", type=int, default=50)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default="llama3",
-                    choices=["llama3", "long_context", "mla", "sparse_mla", "mixed", "few_token",
-                             "tiny"])
+                    choices=["llama3", "long_context", "mla", "mla_mtp", "sparse_mla", "mixed",
+                             "few_token", "tiny"])
     ap.add_argument("--partitions", type=int, default=0, help="0 = planner's choice")
     ap.add_argument("--batch", type=int, default=0,
                     help="override the batch of the llama3 / mla workloads (profiling captures)")
@@ -185,6 +185,8 @@ def build_workload(name: str, device, batch: int = 0):
         return W.long_context_decode(device=device)
     if name == "mla":
         return W.deepseek_v3_mla_decode(device=device, **({"batch": batch} if batch else {}))
+    if name == "mla_mtp":
+        return W.deepseek_v3_mtp_decode(device=device, **({"batch": batch} if batch else {}))
     if name == "sparse_mla":
         return W.deepseek_v32_sparse_mla_decode(device=device,
                                                 **({"batch": batch} if batch else {}))
@@ -374,11 +376,17 @@ def run_ours(args, rank, world, dist):
     out = torch.empty((w.rows, w.num_q_heads, w.dim_v), dtype=torch.bfloat16, device=dev)
     lse = torch.empty((w.rows, w.num_q_heads), dtype=torch.float32, device=dev)
 
-    def call(q=w.q, kv_len=w.kv_len, page_table=w.page_table, o=out, l=lse, indices=w.indices):
+    def call(q=w.q, kv_len=w.kv_len, page_table=w.page_table, o=out, l=lse, indices=w.indices,
+             offs=w.q_row_offsets):
         if sparse:
             attn.attn_mla_decode_sparse(q, w.k_cache, indices, kv_len, scale=w.scale,
                                         dim_v=w.dim_v, sink=w.sink, num_partitions=P,
                                         workspace=ws, out=o, lse=l, stream=stream)
+        elif w.is_mla and offs is not None:
+            attn.attn_mla_decode_rows(q, w.k_cache, kv_len, offs, scale=w.scale,
+                                      max_kv_len=w.max_kv_len, causal=w.causal, dim_v=w.dim_v,
+                                      page_table=page_table, sink=w.sink, num_partitions=P,
+                                      workspace=ws, out=o, lse=l, stream=stream)
         elif w.is_mla:
             attn.attn_mla_decode(q, w.k_cache, kv_len, scale=w.scale, max_kv_len=w.max_kv_len,
                                  dim_v=w.dim_v, page_table=page_table, sink=w.sink,
@@ -386,7 +394,7 @@ def run_ours(args, rank, world, dist):
         else:
             attn.attn_decode(q, w.k_cache, w.v_cache, kv_len, group=w.group, scale=w.scale,
                              max_kv_len=w.max_kv_len, page_table=page_table, sink=w.sink,
-                             q_row_offsets=w.q_row_offsets, max_q_len=w.max_q_len,
+                             q_row_offsets=offs, max_q_len=w.max_q_len,
                              causal=w.causal, num_partitions=P, workspace=ws, out=o, lse=l,
                              stream=stream)
 
@@ -442,6 +450,9 @@ def run_ours(args, rank, world, dist):
     idx_dev = None if idx_host is None else torch.empty_like(w.indices)
     h2d = q_host.numel() * 2 + kvl_host.numel() * 4 + (0 if pt_host is None else pt_host.numel() * 4)
     h2d += 0 if idx_host is None else idx_host.numel() * 4
+    offs_host = None if w.q_row_offsets is None else w.q_row_offsets.cpu().pin_memory()
+    offs_dev = None if offs_host is None else torch.empty_like(w.q_row_offsets)
+    h2d += 0 if offs_host is None else offs_host.numel() * 4
     d2h = out_host.numel() * 2 + lse_host.numel() * 4
 
     def e2e_step():
@@ -452,7 +463,9 @@ def run_ours(args, rank, world, dist):
                 pt_dev.copy_(pt_host, non_blocking=True)
             if idx_dev is not None:
                 idx_dev.copy_(idx_host, non_blocking=True)
-            call(q=q_dev, kv_len=kvl_dev, page_table=pt_dev, indices=idx_dev)
+            if offs_dev is not None:
+                offs_dev.copy_(offs_host, non_blocking=True)
+            call(q=q_dev, kv_len=kvl_dev, page_table=pt_dev, indices=idx_dev, offs=offs_dev)
             out_host.copy_(out, non_blocking=True)
             lse_host.copy_(lse, non_blocking=True)
         stream.synchronize()
@@ -500,19 +513,24 @@ def run_ours(args, rank, world, dist):
                "sample": f"fp64 oracle over every (row, head) of sequences "
                          f"{seqs[0]}..{seqs[-1]} ({len(seqs)} of {w.batch}) x {reps} "
                          f"repetitions, {nb / 1e6:.1f} MB of K/V/q/out, {dt:.1f} s"}
-    if kernel_key == "tile_attention":
-        # causal prefill tiles: FLOPs, not bytes, bind (about 9x past the ridge)
+    # The bound is whichever roof the algorithmic intensity reaches first:
+    # FLOP per byte above the ridge (tensor peak / HBM peak) is tensor-bound.
+    ridge = tensor_peak * 1e12 / (peak * 1e9)
+    if flops / nbytes > ridge:
+        # e.g. causal prefill tiles (about 9x past the ridge), MLA with draft rows
         roofline = {"bound": "tensor", "achieved": round(tflops, 2), "peak": tensor_peak,
                     "unit": "TFLOP/s", "frac": round(tflops / tensor_peak, 4),
                     "traffic": traffic, "peak_source": "measured bf16_tflops (burst)",
-                    "kernel": f"{kernel_key} (one attn_decode call), CUDA events per call "
-                              "on the launch stream"}
+                    "kernel": f"{kernel_key} (+ split-K reduce when P > 1, one call), CUDA "
+                              "events per call on the launch stream",
+                    "intensity_flop_per_byte": round(flops / nbytes, 1), "ridge": round(ridge, 1)}
     else:
         roofline = {"bound": "hbm", "achieved": round(achieved, 2), "peak": peak,
                     "unit": "GB/s", "frac": round(achieved / peak, 4), "traffic": traffic,
                     "peak_source": f"{peak_kind} hbm_gbs",
-                    "kernel": f"{kernel_key} + split-K reduce (one attn_decode call), "
-                              "CUDA events per call on the launch stream"}
+                    "kernel": f"{kernel_key} (+ split-K reduce when P > 1, one call), CUDA "
+                              "events per call on the launch stream",
+                    "intensity_flop_per_byte": round(flops / nbytes, 1), "ridge": round(ridge, 1)}
     line = {
         "metric": METRIC,
         "value": round(value, 2),

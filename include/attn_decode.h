@@ -112,9 +112,10 @@ typedef struct attn_kv {
  * head_dim 128, 32 for head_dim 64, and 64 for attn_mla_decode; slices past
  * kv_len are empty.  The automatic choice treats num_kv_heads == 1 with
  * head_dim_v == 512 as the MLA shape and everything else as GQA.  MLA:
- * P = max(floor(num_sms / 2 / batch), ceil(max_kv_len / 4096)), at least 1
- * (one two-CTA cluster per SM pair; slices of about 4096 keys, or as many
- * as one wave of clusters holds).  For attn_mla_decode_sparse pass
+ * P = max(floor(num_sms / 2 / num_q_rows), ceil(max_kv_len / (4096 n))), at
+ * least 1, with n = ceil(num_q_rows / batch) query rows per sequence (one
+ * two-CTA cluster per SM pair and per row; slices of about 4096 keys per
+ * row, or as many as one wave of clusters holds).  For attn_mla_decode_sparse pass
  * max_kv_len = indices_stride.
  * Returns ATTN_OK, ATTN_ERR_INVALID_ARG, or ATTN_ERR_CUDA if the SM count
  * query fails.  Launches nothing.
@@ -198,6 +199,35 @@ int attn_mla_decode(const void *q, const attn_kv_t *kv, const uint32_t *kv_len, 
                     int num_q_heads, int dim_qk, int dim_v, int max_kv_len, float scale,
                     const float *sink, int num_partitions, void *workspace,
                     size_t workspace_bytes, void *out, float *lse, attn_stream_t stream);
+
+/*
+ * attn_mla_decode_rows -- MLA decode of several query rows per sequence, for
+ * draft tokens being verified (the multi-token-prediction rows that
+ * max_prompt_len bounds, flare_mla_decoding_dispatch, Args).
+ *
+ *   q          device bf16 [num_q_rows][num_q_heads][dim_qk] (128, 576).
+ *   kv, kv_len, max_kv_len, scale, sink, num_partitions, workspace,
+ *   workspace_bytes   as for attn_mla_decode; kv_len counts every key of the
+ *              sequence, its own query tokens included.
+ *   q_row_offsets  device uint32 [batch + 1]: rows of sequence b are
+ *              [off[b], off[b+1]); num_q_rows = off[batch].  Required.
+ *   causal     nonzero: row i of a sequence with n rows and L keys sees keys
+ *              j <= L - n + i (the rows are the last n tokens); zero: every
+ *              row sees all L keys.
+ *   out, lse   device bf16 [num_q_rows][num_q_heads][dim_v] / fp32
+ *              [num_q_rows][num_q_heads] (lse may be NULL).
+ *
+ * Every row of a sequence runs over the same key slices (P and the
+ * workspace come from attn_plan_partitions with num_q_rows rows), one
+ * two-CTA cluster per (slice, row); clusters of the rows of a sequence are
+ * launched next to each other so the second and later reads of a key tile
+ * are served from L2.  num_q_rows <= 65535.  Returns as attn_mla_decode.
+ */
+int attn_mla_decode_rows(const void *q, const attn_kv_t *kv, const uint32_t *kv_len,
+                         const uint32_t *q_row_offsets, int batch, int num_q_rows,
+                         int num_q_heads, int dim_qk, int dim_v, int max_kv_len, float scale,
+                         const float *sink, int causal, int num_partitions, void *workspace,
+                         size_t workspace_bytes, void *out, float *lse, attn_stream_t stream);
 
 /*
  * attn_mla_decode_sparse -- MLA decode in which every sequence attends only

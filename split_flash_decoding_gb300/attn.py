@@ -67,6 +67,10 @@ _SIGNATURES = {
     "attn_mla_decode": [_c.c_void_p, _c.POINTER(attn_kv_t), _c.c_void_p, _c.c_int, _c.c_int,
                         _c.c_int, _c.c_int, _c.c_int, _c.c_float, _c.c_void_p, _c.c_int,
                         _c.c_void_p, _c.c_size_t, _c.c_void_p, _c.c_void_p, _c.c_void_p],
+    "attn_mla_decode_rows": [_c.c_void_p, _c.POINTER(attn_kv_t), _c.c_void_p, _c.c_void_p,
+                             _c.c_int, _c.c_int, _c.c_int, _c.c_int, _c.c_int, _c.c_int,
+                             _c.c_float, _c.c_void_p, _c.c_int, _c.c_int, _c.c_void_p,
+                             _c.c_size_t, _c.c_void_p, _c.c_void_p, _c.c_void_p],
     "attn_mla_decode_sparse": [_c.c_void_p, _c.POINTER(attn_kv_t), _c.c_void_p, _c.c_int,
                                _c.c_void_p, _c.c_int, _c.c_int, _c.c_int, _c.c_int, _c.c_float,
                                _c.c_void_p, _c.c_int, _c.c_void_p, _c.c_size_t, _c.c_void_p,
@@ -241,6 +245,38 @@ def attn_mla_decode(q: torch.Tensor, kv_cache: torch.Tensor, kv_len: torch.Tenso
            lib().attn_mla_decode(q.data_ptr(), ctypes.byref(kd), kv_len.data_ptr(), batch, hq, dqk,
                                  dim_v, max_kv_len, scale, _ptr(sink), P, _ptr(ws), ws_size,
                                  out.data_ptr(), _ptr(lse), _stream_handle(stream)))
+    return out, lse
+
+
+def attn_mla_decode_rows(q: torch.Tensor, kv_cache: torch.Tensor, kv_len: torch.Tensor,
+                         q_row_offsets: torch.Tensor, *, scale: float, max_kv_len: int,
+                         causal: bool = True, dim_v: int = 512,
+                         page_table: Optional[torch.Tensor] = None,
+                         sink: Optional[torch.Tensor] = None, num_partitions: int = 0,
+                         workspace: Optional[torch.Tensor] = None,
+                         out: Optional[torch.Tensor] = None, lse: Optional[torch.Tensor] = None,
+                         return_lse: bool = True, stream=None):
+    """MLA decode of several query rows per sequence (draft tokens) through
+    attn_mla_decode_rows: q bf16 [rows, 128, 576]; q_row_offsets int32
+    [batch + 1] on the device; row i of n sees keys j <= L - n + i when
+    causal."""
+    rows, hq, dqk = q.shape
+    batch = kv_len.shape[0]
+    if q_row_offsets.shape[0] != batch + 1:
+        raise ValueError("q_row_offsets must have batch + 1 entries")
+    if out is None:
+        out = torch.empty((rows, hq, dim_v), dtype=torch.bfloat16, device=q.device)
+    if lse is None and return_lse:
+        lse = torch.empty((rows, hq), dtype=torch.float32, device=q.device)
+    P, ws_bytes = attn_plan_partitions(batch, rows, hq, 1, dim_v, max_kv_len, num_partitions)
+    ws, ws_size = _workspace(ws_bytes, q.device, workspace)
+    kd = kv_descriptor(kv_cache, page_table)
+    _check("attn_mla_decode_rows",
+           lib().attn_mla_decode_rows(q.data_ptr(), ctypes.byref(kd), kv_len.data_ptr(),
+                                      q_row_offsets.data_ptr(), batch, rows, hq, dqk, dim_v,
+                                      max_kv_len, scale, _ptr(sink), 1 if causal else 0, P,
+                                      _ptr(ws), ws_size, out.data_ptr(), _ptr(lse),
+                                      _stream_handle(stream)))
     return out, lse
 
 

@@ -255,10 +255,17 @@ extern "C" int attn_plan_partitions(int num_sms, int batch, int num_q_rows, int 
         // by a few clusters costs a whole extra round of tiles).
         const bool mla = num_kv_heads == 1 && head_dim_v == kMlaDimV;
         const bool tc = !mla && head_dim_v == 128;   // tensor-core decode: one CTA per SM
-        const long long units = static_cast<long long>(batch > 0 ? batch : 1) * num_kv_heads;
+        // MLA runs a cluster per query row; GQA folds a sequence's rows
+        const long long units =
+            mla ? (num_q_rows > 0 ? num_q_rows : 1)
+                : static_cast<long long>(batch > 0 ? batch : 1) * num_kv_heads;
         const long long ctas = mla ? (num_sms / 2 > 0 ? num_sms / 2 : 1)
                                    : (tc ? num_sms : 2LL * num_sms);
-        const long long target = mla ? 4096 : 1024;
+        // MLA: ~4096 keys per slice and query row, so a sequence with n rows
+        // (n clusters per slice) gets n times longer slices
+        const long long rows_per_seq =
+            batch > 0 && num_q_rows > batch ? (num_q_rows + batch - 1) / batch : 1;
+        const long long target = mla ? 4096 * rows_per_seq : 1024;
         long long p;
         if (mla) {
             const long long p_fill = ctas / units > 0 ? ctas / units : 1;
@@ -455,28 +462,30 @@ int encode_rows_map(CUtensorMap *map, const attn_kv_t &kv, int dim) {
 }
 
 // Shared body of the dense (paged or contiguous) and sparse MLA entry points.
-int mla_decode_impl(const void *q, const attn_kv_t *kv, const uint32_t *kv_len, bool sparse,
+int mla_decode_impl(const void *q, const attn_kv_t *kv, const uint32_t *kv_len,
+                    const uint32_t *q_row_offsets, int num_q_rows, int causal, bool sparse,
                     const int32_t *indices, int indices_stride, int batch, int num_q_heads,
                     int dim_qk, int dim_v, int max_kv_len, float scale, const float *sink,
                     int num_partitions, void *workspace, size_t workspace_bytes, void *out,
                     float *lse, attn_stream_t stream) {
-    if (batch < 0 || num_q_heads <= 0 || dim_qk <= 0 || dim_v <= 0 || max_kv_len < 0)
+    if (batch < 0 || num_q_rows < 0 || num_q_heads <= 0 || dim_qk <= 0 || dim_v <= 0 ||
+        max_kv_len < 0)
         return ATTN_ERR_INVALID_ARG;
+    if (!q_row_offsets && num_q_rows != batch) return ATTN_ERR_INVALID_ARG;
     if (num_partitions < 1 || num_partitions > ATTN_MAX_PARTITIONS) return ATTN_ERR_INVALID_ARG;
     if (!(scale == scale)) return ATTN_ERR_INVALID_ARG;
-    if (batch == 0) return ATTN_OK;
+    if (batch == 0 || num_q_rows == 0) return ATTN_OK;
     if (!q || !kv_len || !out) return ATTN_ERR_INVALID_ARG;
     if (num_q_heads != kMlaHeads || dim_qk != kMlaDimQK || dim_v != kMlaDimV)
         return ATTN_ERR_UNSUPPORTED;
+    if (num_q_rows > 65535) return ATTN_ERR_UNSUPPORTED;   // grid rows
     if (reinterpret_cast<uintptr_t>(out) % 16 || reinterpret_cast<uintptr_t>(q) % 16)
         return ATTN_ERR_INVALID_ARG;
     if (reinterpret_cast<uintptr_t>(indices) % 4) return ATTN_ERR_INVALID_ARG;
     int st = sparse ? check_kv_rows(kv, dim_qk) : check_kv(kv, batch, dim_qk, max_kv_len);
     if (st) return st;
-    if (static_cast<long long>(batch) * kMlaHeads > (1LL << 31)) return ATTN_ERR_UNSUPPORTED;
-
     size_t off_m = 0, off_l = 0;
-    const size_t need = workspace_layout(num_partitions, batch, num_q_heads, dim_v, &off_m,
+    const size_t need = workspace_layout(num_partitions, num_q_rows, num_q_heads, dim_v, &off_m,
                                          &off_l);
     if (num_partitions > 1) {
         if (!workspace || workspace_bytes < need) return ATTN_ERR_WORKSPACE;
@@ -495,6 +504,9 @@ int mla_decode_impl(const void *q, const attn_kv_t *kv, const uint32_t *kv_len, 
     st = error_word(&p.err);
     if (st) return st;
     p.kv_len = kv_len;
+    p.q_row_offsets = q_row_offsets;
+    p.num_q_rows = num_q_rows;
+    p.causal = causal ? 1 : 0;
     p.page_table = kv->page_table;
     p.sparse = sparse ? 1 : 0;
     p.indices = indices;
@@ -530,8 +542,10 @@ int mla_decode_impl(const void *q, const attn_kv_t *kv, const uint32_t *kv_len, 
     r.out = p.out;
     r.lse = lse;
     r.kv_len = kv_len;
+    r.q_row_offsets = q_row_offsets;
+    r.batch = batch;
     r.num_partitions = num_partitions;
-    r.rows = batch;
+    r.rows = num_q_rows;
     r.num_q_heads = num_q_heads;
     r.dim_v = dim_v;
     r.chunk = p.chunk;
@@ -546,9 +560,22 @@ extern "C" int attn_mla_decode(const void *q, const attn_kv_t *kv, const uint32_
                                float scale, const float *sink, int num_partitions,
                                void *workspace, size_t workspace_bytes, void *out, float *lse,
                                attn_stream_t stream) {
-    return mla_decode_impl(q, kv, kv_len, false, nullptr, 0, batch, num_q_heads, dim_qk, dim_v,
-                           max_kv_len, scale, sink, num_partitions, workspace, workspace_bytes,
-                           out, lse, stream);
+    return mla_decode_impl(q, kv, kv_len, nullptr, batch, 0, false, nullptr, 0, batch,
+                           num_q_heads, dim_qk, dim_v, max_kv_len, scale, sink, num_partitions,
+                           workspace, workspace_bytes, out, lse, stream);
+}
+
+extern "C" int attn_mla_decode_rows(const void *q, const attn_kv_t *kv, const uint32_t *kv_len,
+                                    const uint32_t *q_row_offsets, int batch, int num_q_rows,
+                                    int num_q_heads, int dim_qk, int dim_v, int max_kv_len,
+                                    float scale, const float *sink, int causal,
+                                    int num_partitions, void *workspace, size_t workspace_bytes,
+                                    void *out, float *lse, attn_stream_t stream) {
+    if (batch > 0 && num_q_rows > 0 && !q_row_offsets) return ATTN_ERR_INVALID_ARG;
+    if (num_q_rows < 0 || batch < 0) return ATTN_ERR_INVALID_ARG;
+    return mla_decode_impl(q, kv, kv_len, q_row_offsets, num_q_rows, causal, false, nullptr, 0,
+                           batch, num_q_heads, dim_qk, dim_v, max_kv_len, scale, sink,
+                           num_partitions, workspace, workspace_bytes, out, lse, stream);
 }
 
 extern "C" int attn_mla_decode_sparse(const void *q, const attn_kv_t *kv,
@@ -563,8 +590,8 @@ extern "C" int attn_mla_decode_sparse(const void *q, const attn_kv_t *kv,
     if (batch > 0 && !topk_lengths) return ATTN_ERR_INVALID_ARG;
     // topk_lengths is read as unsigned: a negative count is above any cap and
     // is reported as a length error.
-    return mla_decode_impl(q, kv, reinterpret_cast<const uint32_t *>(topk_lengths), true,
-                           indices, indices_stride, batch, num_q_heads, dim_qk, dim_v, indices_stride,
+    return mla_decode_impl(q, kv, reinterpret_cast<const uint32_t *>(topk_lengths), nullptr,
+                           batch, 0, true, indices, indices_stride, batch, num_q_heads, dim_qk, dim_v, indices_stride,
                            scale, sink, num_partitions, workspace, workspace_bytes, out, lse,
                            stream);
 }

@@ -53,19 +53,22 @@ constexpr int kMlaDimV = 512;
 struct MlaParams {
     CUtensorMap kv_map;           // 4-D: (channel 576, slot, head 1, page); sparse:
                                   // 2-D (channel 576, row), box height 1
-    const uint16_t *q;            // bf16 [batch][128][576]
+    const uint16_t *q;            // bf16 [rows][128][576]
     const uint32_t *kv_len;       // [batch]
     const int32_t *page_table;    // [batch][max_pages] or nullptr
     const int32_t *indices;       // sparse: [batch][indices_stride] cache rows
     long long num_rows;           // sparse: rows in the cache (num_pages * page_size)
     int sparse;                   // 1: keys are named by indices, kv_len = top-k counts
     int indices_stride;
+    const uint32_t *q_row_offsets;  // [batch + 1] or nullptr (one query row per sequence)
+    int num_q_rows;               // rows of q / out (= batch without row offsets)
+    int causal;                   // rows of a sequence end at its last key (row offsets only)
     const float *sink;            // [128] or nullptr
-    float *ws_o;                  // [P][batch][128][512]
-    float *ws_m;                  // [P][batch][128]
+    float *ws_o;                  // [P][rows][128][512]
+    float *ws_m;                  // [P][rows][128]
     float *ws_l;
-    uint16_t *out;                // bf16 [batch][128][512]
-    float *lse;                   // [batch][128] or nullptr
+    uint16_t *out;                // bf16 [rows][128][512]
+    float *lse;                   // [rows][128] or nullptr
     unsigned *err;
     int batch, max_pages, page_size, num_pages;
     int box_rows;                 // tokens per TMA box (min(64, page size))

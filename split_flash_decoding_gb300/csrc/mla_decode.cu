@@ -142,7 +142,23 @@ mla_decode_kernel(const __grid_constant__ MlaParams p) {
     const uint32_t rank = cluster_ctarank();
     const uint32_t peer = rank ^ 1u;
     const int part = blockIdx.x >> 1;
-    const int b = blockIdx.y;
+    // Query row qrow of sequence b: one row per sequence, or several (draft
+    // tokens) given by row offsets, each with its own causal limit.  Every
+    // row of a sequence uses the same key slices; a row that sees none of a
+    // slice leaves an empty partial.
+    const int qrow = blockIdx.y;
+    int b = qrow, n_rows = 1, i_row = 0;
+    if (p.q_row_offsets) {
+        int lo = 0, hi = p.batch;   // off[lo] <= qrow < off[hi]
+        while (hi - lo > 1) {
+            const int mid = (lo + hi) >> 1;
+            if (static_cast<int>(p.q_row_offsets[mid]) <= qrow) lo = mid;
+            else hi = mid;
+        }
+        b = lo;
+        i_row = qrow - static_cast<int>(p.q_row_offsets[b]);
+        n_rows = static_cast<int>(p.q_row_offsets[b + 1]) - static_cast<int>(p.q_row_offsets[b]);
+    }
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
     const int nbox = rank == 0 ? 4 : 5;
@@ -155,10 +171,12 @@ mla_decode_kernel(const __grid_constant__ MlaParams p) {
         atomicOr(p.err, kErrBadLength);
     const int L = static_cast<int>(min(len_in, cap));
     const int start = part * p.chunk;
-    const int end = min(start + p.chunk, L);
     const int nslices = (L + p.chunk - 1) / p.chunk;
     const bool direct = nslices <= 1;
     if (start >= L && !(direct && part == 0)) return;  // uniform over the cluster
+    // keys j <= L - n + i for row i of n when causal
+    const int L_vis = p.causal ? max(0, min(L, L - n_rows + i_row + 1)) : L;
+    const int end = min(min(start + p.chunk, L), L_vis);
     const int ntiles = start < end ? (end - start + kBN - 1) / kBN : 0;
 
     if (threadIdx.x == 0) {
@@ -433,7 +451,7 @@ mla_decode_kernel(const __grid_constant__ MlaParams p) {
             // This CTA's Q channels of head row h into TMEM lane h: 64 channels
             // (32 columns of bf16 pairs) per store, boxes split over the halves.
             const uint4 *src = reinterpret_cast<const uint4 *>(
-                p.q + (size_t(b) * kMlaHeads + h) * kMlaDimQK + col0);
+                p.q + (size_t(qrow) * kMlaHeads + h) * kMlaDimQK + col0);
             for (int cb = half; cb < nbox; cb += 2) {
                 float v[32];
 #pragma unroll
@@ -648,7 +666,7 @@ mla_decode_kernel(const __grid_constant__ MlaParams p) {
         } else {
             scale_o = l_r > 0.f ? l / l_r : 0.f;
         }
-        const size_t row = size_t(b) * kMlaHeads + h;
+        const size_t row = size_t(qrow) * kMlaHeads + h;
         const int ch0 = rank * 256 + half * 128;   // this warp's output channels
 #pragma unroll 1
         for (int c = 0; c < 128; c += 32) {
@@ -671,7 +689,7 @@ mla_decode_kernel(const __grid_constant__ MlaParams p) {
                     *reinterpret_cast<uint4 *>(dst + j) = w;
                 }
             } else {
-                float *dst = p.ws_o + (size_t(part) * p.batch * kMlaHeads + row) * kMlaDimV +
+                float *dst = p.ws_o + (size_t(part) * p.num_q_rows * kMlaHeads + row) * kMlaDimV +
                              ch0 + c;
 #pragma unroll
                 for (int j = 0; j < 32; j += 4)
@@ -684,7 +702,7 @@ mla_decode_kernel(const __grid_constant__ MlaParams p) {
             if (direct) {
                 if (p.lse) p.lse[row] = Z > 0.f ? (Mf + fast_log2(Z)) * kLn2 : -INFINITY;
             } else {
-                const size_t idx = size_t(part) * p.batch * kMlaHeads + row;
+                const size_t idx = size_t(part) * p.num_q_rows * kMlaHeads + row;
                 p.ws_m[idx] = m_ref * kLn2;
                 p.ws_l[idx] = l;
             }
@@ -707,7 +725,7 @@ cudaError_t launch_layout(const MlaParams &p, cudaStream_t stream) {
                                          cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          int(kSmemBytes));
     if (e != cudaSuccess) return e;
-    dim3 grid(2 * p.num_partitions, p.batch);
+    dim3 grid(2 * p.num_partitions, p.num_q_rows);
     mla_decode_kernel<kSparse><<<grid, Layout<kSparse>::kThreads, kSmemBytes, stream>>>(p);
     return cudaGetLastError();
 }

@@ -295,6 +295,20 @@ def deepseek_v3_mla_decode(device="cpu", seed: int = 4, batch: int = 32) -> Work
                          scale=1.0 / math.sqrt(192.0))
 
 
+def deepseek_v3_mtp_decode(device="cpu", seed: int = 8, batch: int = 32,
+                           q_len: int = 2) -> Workload:
+    """DeepSeek-V3-shaped MLA decode with multi-token prediction: every
+    sequence carries q_len query rows (the current token and q_len - 1 draft
+    tokens), causal (row i of n sees keys j <= L - n + i); batch 32, 128 q
+    heads, one KV head of depth 576, V = K[:, :512], lengths uniform in
+    [1024, 32768], paged (page 64), scale 1/sqrt(192)."""
+    lens = _uniform_ints(1024, 32768, batch, seed)
+    return make_workload(f"deepseek_v3_mtp{q_len}_mla_decode_b{batch}_h128_d576_paged64",
+                         batch=batch, num_q_heads=128, num_kv_heads=1, dim_qk=576, dim_v=512,
+                         mla=True, kv_lens=lens, page_size=64, seed=seed, device=device,
+                         q_lens=[q_len] * batch, causal=True, scale=1.0 / math.sqrt(192.0))
+
+
 def few_token_decode(device="cpu", seed: int = 6, batch: int = 64, max_q_len: int = 4) -> Workload:
     """Few-token decode on the Llama-3-8B shapes: batch 64, 32 q / 8 KV heads,
     head_dim 128, paged (page 128), cache lengths uniform in [512, 8192], and

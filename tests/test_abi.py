@@ -167,6 +167,30 @@ def test_sparse_mla_rejects_bad_arguments_before_launch(attn):
     assert call_sparse(attn, batch=0, q=None, out=None, topk=None) == E.ATTN_OK
 
 
+def test_mla_rows_rejects_bad_arguments_before_launch(attn):
+    E = attn
+    k = kv(attn, page_stride=64 * 576, token_stride=576, head_stride=576, page_size=64,
+           num_pages=100, max_pages=40)
+
+    def call(**over):
+        a = dict(q=0x30000, kvl=0x40000, offs=0x48000, batch=2, rows=5, hq=128, dqk=576, dv=512,
+                 maxkv=2000, scale=0.07, sink=None, causal=1, P=1, ws=None, ws_bytes=0,
+                 out=0x50000, lse=None)
+        a.update(over)
+        return attn.lib().attn_mla_decode_rows(a["q"], ctypes.byref(k), a["kvl"], a["offs"],
+                                               a["batch"], a["rows"], a["hq"], a["dqk"], a["dv"],
+                                               a["maxkv"], a["scale"], a["sink"], a["causal"],
+                                               a["P"], a["ws"], a["ws_bytes"], a["out"],
+                                               a["lse"], None)
+    assert call(offs=None) == E.ATTN_ERR_INVALID_ARG
+    assert call(rows=-1) == E.ATTN_ERR_INVALID_ARG
+    assert call(q=None) == E.ATTN_ERR_INVALID_ARG
+    assert call(hq=64) == E.ATTN_ERR_UNSUPPORTED
+    assert call(rows=70000) == E.ATTN_ERR_UNSUPPORTED
+    assert call(P=3) == E.ATTN_ERR_WORKSPACE
+    assert call(rows=0, q=None, out=None) == E.ATTN_OK
+
+
 def test_reduce_rejects_bad_arguments(attn):
     L = attn.lib()
     f = L.attn_splitk_reduce
@@ -206,6 +230,11 @@ def test_planner_formulas(attn):
     assert P == 2
     P, _ = attn.attn_plan_partitions(128, 128, 128, 1, 512, 2048, 0, num_sms=152)
     assert P == 1
+    # MLA with several query rows per sequence: one cluster per (slice, row)
+    P, _ = attn.attn_plan_partitions(4, 8, 128, 1, 512, 2048, 0, num_sms=152)
+    assert P == 9
+    P, _ = attn.attn_plan_partitions(32, 64, 128, 1, 512, 32768, 0, num_sms=152)
+    assert P == 4                                     # slices of 8192 keys for 2 rows
     P, _ = attn.attn_plan_partitions(1, 1, 32, 8, 128, 20, 0, num_sms=152)
     assert P == 1                                     # one tile of keys cannot split
     P, _ = attn.attn_plan_partitions(4, 4, 32, 8, 128, 0, 0, num_sms=152)
