@@ -259,18 +259,21 @@ def whole_job_value(world: int, bytes_per_rank: int, ms_per_step: float) -> floa
 # the reference arm: the fp64 CPU oracle on the host cores
 # ---------------------------------------------------------------------------
 
-def oracle_sample_time(w, k_host, v_host, seqs):
-    """Run the oracle on every (row, head) of the listed sequences; returns
-    (seconds, bytes those sequences account for, threads)."""
+def oracle_sample_time(w, k_host, v_host, seqs, threads=None):
+    """Run the oracle on every (query row, head) of the listed sequences;
+    returns (seconds, bytes those sequences account for, threads)."""
     import numpy as np
     import oracle
-    rows = []
-    heads = []
+    offs = w.q_row_offsets_host
+    rows, heads = [], []
+    n_rows = 0
     for b in seqs:
-        for h in range(w.num_q_heads):
-            rows.append(b)
-            heads.append(h)
-    threads = os.cpu_count() or 1
+        for r in (range(offs[b], offs[b + 1]) if offs is not None else (b,)):
+            n_rows += 1
+            for h in range(w.num_q_heads):
+                rows.append(r)
+                heads.append(h)
+    threads = threads or os.cpu_count() or 1
     if w.indices is not None:
         kk = oracle.KV.sparse(k_host, w.indices.cpu())
     elif w.page_table is not None:
@@ -281,14 +284,18 @@ def oracle_sample_time(w, k_host, v_host, seqs):
                                     if w.page_table is not None else oracle.KV.contiguous(v_host))
     sink = None if w.sink is None else w.sink.cpu()
     t0 = time.perf_counter()
-    oracle.attention(w.q.cpu(), kk, vv, w.kv_len.cpu(), group=w.group, scale=w.scale,
-                     dim_v=w.dim_v, sink=sink, sample=(np.array(rows), np.array(heads)),
-                     threads=threads)
+    if rows:
+        oracle.attention(w.q.cpu(), kk, vv, w.kv_len.cpu(), group=w.group, scale=w.scale,
+                         dim_v=w.dim_v, sink=sink, causal=w.causal,
+                         q_row_offsets=None if w.q_row_offsets is None else w.q_row_offsets.cpu(),
+                         sample=(np.array(rows), np.array(heads)), threads=threads)
     dt = time.perf_counter() - t0
     hkv = w.num_kv_heads
     per_key = (w.dim_qk * 2) if w.is_mla else hkv * (w.dim_qk + w.dim_v) * 2
+    if w.indices is not None:
+        per_key += 4
     nbytes = sum(w.kv_len_host[b] * per_key for b in seqs)
-    nbytes += len(seqs) * w.num_q_heads * (w.dim_qk * 2 + w.dim_v * 2 + 4)
+    nbytes += n_rows * w.num_q_heads * (w.dim_qk * 2 + w.dim_v * 2 + 4)
     return dt, nbytes, threads
 
 
@@ -508,11 +515,14 @@ def run_ours(args, rank, world, dist):
             dt += d1
             nb += n1
             reps += 1
+        d1, n1, _ = oracle_sample_time(w, k_host, v_host, seqs[:1], threads=1)
         cpu = {"value": round(nb / dt / 1e9, 4), "unit": "GB/s", "cores": threads,
                "kind": "oracle",
                "sample": f"fp64 oracle over every (row, head) of sequences "
                          f"{seqs[0]}..{seqs[-1]} ({len(seqs)} of {w.batch}) x {reps} "
-                         f"repetitions, {nb / 1e6:.1f} MB of K/V/q/out, {dt:.1f} s"}
+                         f"repetitions, {nb / 1e6:.1f} MB of K/V/q/out, {dt:.1f} s",
+               "single_thread": {"value": round(n1 / d1 / 1e9, 4), "unit": "GB/s",
+                                 "sample": f"sequence {seqs[0]}, one thread, {d1:.2f} s"}}
     # The bound is whichever roof the algorithmic intensity reaches first:
     # FLOP per byte above the ridge (tensor peak / HBM peak) is tensor-bound.
     ridge = tensor_peak * 1e12 / (peak * 1e9)
@@ -540,6 +550,7 @@ def run_ours(args, rank, world, dist):
         "warmup": args.warmup,
         "ms_per_step": round(ms_per_step, 5),
         "us_per_call": round(ms_per_step * 1e3, 2),
+        "us_per_call_median": round(statistics.median(per_call_ms) * 1e3, 2),
         "hbm_frac": round(value / world / peak, 4),
         "higher_is_better": True,
         "scaling": "weak",
