@@ -110,8 +110,14 @@ typedef struct attn_kv {
  * Key slice p of a sequence is [p*C, min((p+1)*C, kv_len)) with
  * C = ceil(ceil(max_kv_len / P) / T) * T, T = 128 for attn_decode with
  * head_dim 128, 32 for head_dim 64, and 64 for attn_mla_decode; slices past
- * kv_len are empty.  The automatic choice treats num_kv_heads == 1 with
- * head_dim_v == 512 as the MLA shape and everything else as GQA.  MLA:
+ * kv_len are empty.  With head_dim 128, P = 2 or 4 needs no workspace
+ * (workspace_bytes 0): a cluster of P CTAs splits each (sequence, KV head)
+ * into P equal key slices of that sequence and merges them on chip.  The
+ * automatic choice treats num_kv_heads == 1 with head_dim_v == 512 as the
+ * MLA shape and everything else as GQA.  GQA with head_dim 128 and more
+ * query rows than sequences (the few-row fold): P = 1 when there are at
+ * least 2 (sequence, KV head) units per SM, P = 2 when there are at least
+ * num_sms / 2.  MLA:
  * P = max(floor(num_sms / 2 / num_q_rows), ceil(max_kv_len / (4096 n))), at
  * least 1, with n = ceil(num_q_rows / batch) query rows per sequence (one
  * two-CTA cluster per SM pair and per row; slices of about 4096 keys per
@@ -167,8 +173,10 @@ int attn_plan_partitions(int num_sms, int batch, int num_q_rows, int num_q_heads
  *   num_partitions  P from attn_plan_partitions (or any 1..MAX); must be 1
  *              on the tile kernel (max_q_len > 1 beyond the few-row fold).
  *   workspace  device, 256-byte aligned, >= the planner's workspace_bytes
- *              for this P; may be NULL when P == 1.  Contents on entry are
- *              ignored; it holds fp32 partial O, qk_max and exp_sum after.
+ *              for this P; may be NULL when P == 1, and with head_dim 128
+ *              when P is 2 or 4 (those merge on chip).  Contents on entry
+ *              are ignored; it holds fp32 partial O, qk_max and exp_sum
+ *              after.
  *   out        device bf16 [num_q_rows][num_q_heads][head_dim].
  *   lse        device fp32 [num_q_rows][num_q_heads], or NULL.
  *

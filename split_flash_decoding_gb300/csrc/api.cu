@@ -80,6 +80,10 @@ bool is_pow2(long long x) { return x > 0 && (x & (x - 1)) == 0; }
 
 size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
 
+// GQA decode on the tensor cores (head_dim 128) with 2 or 4 partitions
+// merges them on chip (a cluster of P CTAs) and needs no workspace.
+bool merges_on_chip(int P, int head_dim) { return head_dim == 128 && (P == 2 || P == 4); }
+
 // Workspace layout for P partitions: ws_o | ws_m | ws_l, each 256-B aligned.
 size_t workspace_layout(int P, long long rows, int hq, int dv, size_t *off_m, size_t *off_l) {
     if (P <= 1) {
@@ -271,6 +275,12 @@ extern "C" int attn_plan_partitions(int num_sms, int batch, int num_q_rows, int 
             const long long p_fill = ctas / units > 0 ? ctas / units : 1;
             const long long p_len = (static_cast<long long>(max_kv_len) + target - 1) / target;
             p = p_fill > p_len ? p_fill : p_len;
+        } else if (tc && num_q_rows > batch && units >= ctas / 2) {
+            // A few query rows per sequence fold onto 16 score columns, and
+            // every item then pays a 16-column epilogue and partial: long
+            // items win.  One slice per unit when there are two units per
+            // CTA or more, else two slices merged on chip by a CTA pair.
+            p = units >= 2 * ctas ? 1 : 2;
         } else if (units < ctas) {
             p = (ctas + units - 1) / units;
         } else {
@@ -291,7 +301,11 @@ extern "C" int attn_plan_partitions(int num_sms, int batch, int num_q_rows, int 
         P = static_cast<int>(p);
     }
     *num_partitions = P;
-    *workspace_bytes = workspace_layout(P, num_q_rows, num_q_heads, head_dim_v, nullptr, nullptr);
+    const bool gqa = !(num_kv_heads == 1 && head_dim_v == kMlaDimV);
+    *workspace_bytes = gqa && merges_on_chip(P, head_dim_v)
+                           ? 0
+                           : workspace_layout(P, num_q_rows, num_q_heads, head_dim_v, nullptr,
+                                              nullptr);
     return ATTN_OK;
 }
 
@@ -336,17 +350,18 @@ extern "C" int attn_decode(const void *q, const attn_kv_t *k, const attn_kv_t *v
         k->max_pages != v->max_pages || k->num_pages != v->num_pages)
         return ATTN_ERR_UNSUPPORTED;
 
+    // head_dim 128 runs on the tensor cores (128-key tiles), head_dim 64 on
+    // the CUDA cores (32-key tiles).  On the tensor cores a split into 2 or 4
+    // partitions is merged on chip by a cluster of that many CTAs.
+    const bool tc = head_dim == 128;
+    const bool on_chip = merges_on_chip(num_partitions, head_dim);
     size_t off_m = 0, off_l = 0;
     const size_t need = workspace_layout(num_partitions, num_q_rows, num_q_heads, head_dim,
                                          &off_m, &off_l);
-    if (num_partitions > 1) {
+    if (num_partitions > 1 && !on_chip) {
         if (!workspace || workspace_bytes < need) return ATTN_ERR_WORKSPACE;
         if (reinterpret_cast<uintptr_t>(workspace) % 256) return ATTN_ERR_WORKSPACE;
     }
-
-    // head_dim 128 runs on the tensor cores (128-key tiles), head_dim 64 on
-    // the CUDA cores (32-key tiles).
-    const bool tc = head_dim == 128;
     const int tile = tc ? kGqaTcTileKeys : kGqaTileKeys;
     GqaParams p;
     std::memset(&p, 0, sizeof(p));
@@ -378,12 +393,13 @@ extern "C" int attn_decode(const void *q, const attn_kv_t *k, const attn_kv_t *v
     p.q_row_offsets = fold ? q_row_offsets : nullptr;
     p.page_table = k->page_table;
     p.sink = sink;
-    if (num_partitions > 1) {
+    if (num_partitions > 1 && !on_chip) {
         uint8_t *ws = static_cast<uint8_t *>(workspace);
         p.ws_o = reinterpret_cast<float *>(ws);
         p.ws_m = reinterpret_cast<float *>(ws + off_m);
         p.ws_l = reinterpret_cast<float *>(ws + off_l);
     }
+    p.cluster = on_chip ? num_partitions : 0;
     p.out = static_cast<uint16_t *>(out);
     p.lse = lse;
     p.batch = batch;
@@ -402,7 +418,7 @@ extern "C" int attn_decode(const void *q, const attn_kv_t *k, const attn_kv_t *v
 
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
     st = map_cuda(tc ? launch_gqa_decode_tc(p, s) : launch_gqa_decode(p, s));
-    if (st || num_partitions == 1) return st;
+    if (st || num_partitions == 1 || on_chip) return st;
 
     ReduceParams r;
     std::memset(&r, 0, sizeof(r));

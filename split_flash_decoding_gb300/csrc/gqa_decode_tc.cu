@@ -26,6 +26,17 @@
 // TMEM and issues the MMAs.  Rings: 3 K stages and 3 V stages of 32 KB, each
 // consumed in order by the single MMA thread, so parity waits never alias.
 //
+// Small P, merged on chip: with 2 or 4 partitions the kernel can run as
+// clusters of that many CTAs instead.  A cluster takes one (sequence, KV
+// head) unit at a time and CTA r of the cluster covers the r-th of equal key
+// slices of it; at the end of the unit every CTA leaves its partial (O^T, m,
+// l per column) in its own shared memory, signals every CTA of the cluster
+// through a cluster-scope mbarrier arrive, and then merges its share of the
+// output channels by reading the partials of all CTAs over distributed
+// shared memory -- no workspace and no reduce launch.  The merge buffers are
+// double-buffered by unit parity: a CTA writes a buffer again only after the
+// next unit's signal from every peer, which follows the peers' reads.
+//
 // Per tile: the MMA thread issues S(t) into one of two TMEM score buffers as
 // soon as K(t) has landed; the softmax warps take the tile max per head
 // across the four warps (shared memory), update the running max m and sums
@@ -118,7 +129,14 @@ struct Smem {
     static constexpr int p = q + 2 * kNBytes;                   // P^T
     static constexpr int red = p + kNBytes;                     // float [2][4][16] tile max
     static constexpr int lred = red + 2 * 4 * 16 * 4;           // float [2][4][2][16] row sums
-    static constexpr int bars = lred + 2 * 4 * 2 * 16 * 4;
+    static constexpr int mrg = lred + 2 * 4 * 2 * 16 * 4;       // [2] merge buffers (clusters)
+};
+// One merge buffer: O^T partial [16 columns][128 channels] fp32, then m[16], l[16].
+constexpr int kMrgO = 16 * 128 * 4;
+constexpr int kMrgBytes = kMrgO + 2 * 16 * 4;
+template <int C>
+struct Tail {
+    static constexpr int bars = Smem::mrg + (C > 1 ? 2 * kMrgBytes : 0);
     static constexpr int items = bars + 256;
 };
 
@@ -127,11 +145,48 @@ enum Bar {
     kQFull = 12, kQEmpty = 14,                          // [2] each
     kSFull = 16, kSFree = 18,                           // [2] each
     kPFull = 20, kODone = 21,
-    kNumBars = 22
+    kMrgFull = 22,                                      // [2] clusters: partials in place
+    kNumBars = 24
 };
 
+// Dynamic shared memory: the item table (one int per sequence) only without
+// clusters.
+template <int C>
 size_t tc_smem_bytes(int batch) {
-    return 1024 + size_t(Smem::items) + sizeof(int) * size_t(batch + 1);
+    return 1024 + size_t(Tail<C>::items) + (C > 1 ? 0 : sizeof(int) * size_t(batch + 1));
+}
+
+// Work walk of one CTA.  Without clusters: items (sequence, KV head, slice)
+// j = blockIdx.x, blockIdx.x + gridDim.x, ...  With clusters of C: units
+// (sequence, KV head) j = cluster, cluster + clusters, ..., this CTA taking
+// the slice of its rank.
+template <int C>
+__device__ __forceinline__ int walk_first() { return C > 1 ? int(blockIdx.x) / C : int(blockIdx.x); }
+template <int C>
+__device__ __forceinline__ int walk_stride() { return C > 1 ? int(gridDim.x) / C : int(gridDim.x); }
+
+template <int C>
+__device__ __forceinline__ GqaItem walk_item(const GqaParams &p, const int *cum, int j, int hkv) {
+    if constexpr (C == 1) {
+        return gqa_item<kBK>(p, cum, j, hkv);
+    } else {
+        GqaItem it;
+        it.b = j / hkv;
+        it.kvh = j - it.b * hkv;
+        it.part = static_cast<int>(cluster_ctarank());
+        const uint32_t cap = uint32_t(C) * uint32_t(p.chunk);
+        const uint32_t len_in = p.kv_len[it.b];
+        if (len_in > cap && it.kvh == 0 && it.part == 0 && threadIdx.x == 0)
+            atomicOr(p.err, kErrBadLength);
+        it.L = static_cast<int>(min(len_in, cap));
+        // equal slices of this sequence, whole tiles
+        const int cs = ((it.L + C - 1) / C + kBK - 1) / kBK * kBK;
+        it.start = min(it.part * cs, it.L);
+        it.end = min(it.start + cs, it.L);
+        it.ntiles = it.start < it.end ? (it.end - it.start + kBK - 1) / kBK : 0;
+        it.direct = false;
+        return it;
+    }
 }
 
 // Position of element (row r, column c) of a 16-row operand stored as two
@@ -144,7 +199,7 @@ __device__ __forceinline__ uint32_t n_operand_offset(int r, int c) {
 // Producer loop shared by the K (+Q) and V warps: walks this CTA's items and
 // tiles, resolves pages lane-parallel (32 row boxes at a time) and lets lane
 // 0 issue the boxes of each tile into the ring.
-template <bool kIsK>
+template <bool kIsK, int C>
 __device__ __forceinline__ void produce(const GqaParams &p, const int *cum, int num_items, int hkv,
                                         uint8_t *smem, uint64_t *bar, int lane) {
     const CUtensorMap *map = kIsK ? &p.k_map : &p.v_map;
@@ -161,8 +216,8 @@ __device__ __forceinline__ void produce(const GqaParams &p, const int *cum, int 
     const uint32_t box_bytes = uint32_t(box_rows) * 128u;
     int g = 0, itq = 0;
     bool aborted = false;
-    for (int j = blockIdx.x; j < num_items && !aborted; j += gridDim.x) {
-        const GqaItem it = gqa_item<kBK>(p, cum, j, hkv);
+    for (int j = walk_first<C>(); j < num_items && !aborted; j += walk_stride<C>()) {
+        const GqaItem it = walk_item<C>(p, cum, j, hkv);
         if (it.ntiles == 0) continue;
         if (kIsK && lane == 0) {
             const int qb = itq & 1;
@@ -249,25 +304,26 @@ __device__ __forceinline__ void produce(const GqaParams &p, const int *cum, int 
 
 // G: query heads per KV head; NC: score columns (G for one row per sequence,
 // 16 for the few-token fold).
-template <int G, int NC>
+template <int G, int NC, int C>
 __global__ void __launch_bounds__(kThreads, 1)
 gqa_decode_tc_kernel(const __grid_constant__ GqaParams p) {
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-    uint64_t *bar = reinterpret_cast<uint64_t *>(smem + Smem::bars);
-    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + Smem::bars + kNumBars * 8);
-    int *cum = reinterpret_cast<int *>(smem + Smem::items);
+    uint64_t *bar = reinterpret_cast<uint64_t *>(smem + Tail<C>::bars);
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + Tail<C>::bars + kNumBars * 8);
+    int *cum = reinterpret_cast<int *>(smem + Tail<C>::items);
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
     const int hkv = p.num_q_heads / G;
 
-    if (warp == 0) gqa_build_items(p, hkv, cum, lane);
+    if (C == 1 && warp == 0) gqa_build_items(p, hkv, cum, lane);
     if (threadIdx.x == 32) {
         for (int i = 0; i < kNumBars; ++i) {
             const bool per_warp = (i == kSFree || i == kSFree + 1 || i == kPFull);
-            mbar_init(&bar[i], per_warp ? 4u : 1u);
+            const bool merge = i == kMrgFull || i == kMrgFull + 1;
+            mbar_init(&bar[i], merge ? 4u * C : (per_warp ? 4u : 1u));
         }
         fence_mbar_init();
     }
@@ -282,14 +338,15 @@ gqa_decode_tc_kernel(const __grid_constant__ GqaParams p) {
     tc::fence_async_smem();
     tc::fence_before_sync();
     __syncthreads();
+    if constexpr (C > 1) cluster_sync();   // every CTA's barriers exist before a remote arrive
     tc::fence_after_sync();
     const uint32_t tmem = *tmem_slot;
-    const int num_items = cum[p.batch];
+    const int num_items = C > 1 ? p.batch * hkv : cum[p.batch];
 
     if (warp == 4) {
-        produce<true>(p, cum, num_items, hkv, smem, bar, lane);
+        produce<true, C>(p, cum, num_items, hkv, smem, bar, lane);
     } else if (warp == 5) {
-        produce<false>(p, cum, num_items, hkv, smem, bar, lane);
+        produce<false, C>(p, cum, num_items, hkv, smem, bar, lane);
     } else if (warp == 6) {
         // ---------------------------------------------------------- MMA issue
         if (lane == 0) {
@@ -301,8 +358,8 @@ gqa_decode_tc_kernel(const __grid_constant__ GqaParams p) {
             const uint32_t p_base = smem_addr(smem + Smem::p);
             int g = 0, itq = 0;
             bool ok = true;
-            for (int j = blockIdx.x; ok && j < num_items; j += gridDim.x) {
-                const GqaItem it = gqa_item<kBK>(p, cum, j, hkv);
+            for (int j = walk_first<C>(); ok && j < num_items; j += walk_stride<C>()) {
+                const GqaItem it = walk_item<C>(p, cum, j, hkv);
                 if (it.ntiles == 0) continue;
                 const int qb = itq & 1;
                 ok = mbar_wait(&bar[kQFull + qb], (itq >> 1) & 1, p.err);
@@ -363,10 +420,10 @@ gqa_decode_tc_kernel(const __grid_constant__ GqaParams p) {
         float *red = reinterpret_cast<float *>(smem + Smem::red);     // [2][4][16]
         float *lred = reinterpret_cast<float *>(smem + Smem::lred);   // [2][4][16]
         uint8_t *pbuf = smem + Smem::p;
-        int g = 0;
+        int g = 0, iter = 0;
         bool ok = true;
-        for (int j = blockIdx.x; j < num_items; j += gridDim.x) {
-            const GqaItem it = gqa_item<kBK>(p, cum, j, hkv);
+        for (int j = walk_first<C>(); j < num_items; j += walk_stride<C>(), ++iter) {
+            const GqaItem it = walk_item<C>(p, cum, j, hkv);
             int row0, nrows;
             seq_rows(p, it.b, row0, nrows);
             // Column c = (row c / G, head c % G): keys j < lim[c] are visible.
@@ -473,7 +530,7 @@ gqa_decode_tc_kernel(const __grid_constant__ GqaParams p) {
             }
             float lsum[NC], lrsum[NC];
             {
-                float *lb = lred + (j / gridDim.x & 1) * 128;   // [4 warps][2][16]
+                float *lb = lred + (iter & 1) * 128;   // [4 warps][2][16]
 #pragma unroll
                 for (int c = 0; c < NC; ++c) {
                     const float a = warp_sum(l[c]);
@@ -498,39 +555,107 @@ gqa_decode_tc_kernel(const __grid_constant__ GqaParams p) {
                 for (int c = 0; c < NC; ++c) o[c] = 0.f;
             }
             tc::fence_before_sync();
-            const int ch = k;   // output channel of this thread
-#pragma unroll
-            for (int c = 0; c < NC; ++c) {
-                const int i = c / G, h = c % G;
-                if (i >= nrows) continue;
-                const int hq = it.kvh * G + h;
-                const size_t row = size_t(row0 + i);
-                if (it.direct) {
-                    const float t2 = p.sink ? p.sink[hq] * kLog2e : -INFINITY;
-                    const float Mf = fmaxf(m[c], t2);
-                    float Z = 0.f, Zr = 0.f, so = 0.f;
-                    if (Mf != -INFINITY) {
-                        so = fast_exp2(m[c] - Mf);     // 0 when m = -inf
-                        const float st = fast_exp2(t2 - Mf);
-                        Z = lsum[c] * so + st;
-                        Zr = lrsum[c] * so + st;
+            if constexpr (C == 1) {
+                const int ch = k;   // output channel of this thread
+    #pragma unroll
+                for (int c = 0; c < NC; ++c) {
+                    const int i = c / G, h = c % G;
+                    if (i >= nrows) continue;
+                    const int hq = it.kvh * G + h;
+                    const size_t row = size_t(row0 + i);
+                    if (it.direct) {
+                        const float t2 = p.sink ? p.sink[hq] * kLog2e : -INFINITY;
+                        const float Mf = fmaxf(m[c], t2);
+                        float Z = 0.f, Zr = 0.f, so = 0.f;
+                        if (Mf != -INFINITY) {
+                            so = fast_exp2(m[c] - Mf);     // 0 when m = -inf
+                            const float st = fast_exp2(t2 - Mf);
+                            Z = lsum[c] * so + st;
+                            Zr = lrsum[c] * so + st;
+                        }
+                        const float scale_o = Zr > 0.f ? so / Zr : 0.f;
+                        const uint32_t packed = pack_bf16x2(o[c] * scale_o, 0.f);
+                        p.out[(row * p.num_q_heads + hq) * kD + ch] =
+                            static_cast<uint16_t>(packed & 0xffffu);
+                        if (ch == 0 && p.lse)
+                            p.lse[row * p.num_q_heads + hq] =
+                                Z > 0.f ? (Mf + fast_log2(Z)) * kLn2 : -INFINITY;
+                    } else {
+                        const size_t base =
+                            (size_t(it.part) * p.num_q_rows + row) * p.num_q_heads + hq;
+                        const float scale_o = lrsum[c] > 0.f ? lsum[c] / lrsum[c] : 0.f;
+                        p.ws_o[base * kD + ch] = o[c] * scale_o;
+                        if (ch == 0) {
+                            p.ws_m[base] = m[c] * kLn2;
+                            p.ws_l[base] = lsum[c];
+                        }
                     }
-                    const float scale_o = Zr > 0.f ? so / Zr : 0.f;
-                    const uint32_t packed = pack_bf16x2(o[c] * scale_o, 0.f);
-                    p.out[(row * p.num_q_heads + hq) * kD + ch] =
+                }
+            } else {
+                // ---- on-chip merge of the cluster's partials -----------------
+                const int buf = iter & 1;
+                const int rank = it.part;
+                uint8_t *mb = smem + Smem::mrg + buf * kMrgBytes;
+                float *mo = reinterpret_cast<float *>(mb);                 // [16][128]
+                float *mml = reinterpret_cast<float *>(mb + kMrgO);        // m[16], l[16]
+#pragma unroll
+                for (int c = 0; c < NC; ++c) {
+                    // normalised to the fp32 weight sum, as a workspace partial
+                    const float scale_o = lrsum[c] > 0.f ? lsum[c] / lrsum[c] : 0.f;
+                    mo[c * 128 + k] = o[c] * scale_o;
+                }
+                if (k == 0) {
+#pragma unroll
+                    for (int c = 0; c < NC; ++c) {
+                        mml[c] = m[c];        // base 2
+                        mml[16 + c] = lsum[c];
+                    }
+                }
+                __syncwarp();
+                if (lane == 0) {
+                    const uint32_t local = smem_addr(&bar[kMrgFull + buf]);
+#pragma unroll
+                    for (int q = 0; q < C; ++q) mbar_arrive_cluster(mapa_shared(local, q));
+                }
+                ok = mbar_wait_cluster(&bar[kMrgFull + buf], (iter >> 1) & 1, p.err) && ok;
+                // this CTA's output channels [rank * 128 / C, (rank + 1) * 128 / C)
+                constexpr int kChs = 128 / C;
+                const uint32_t mb_local = smem_addr(mb);
+                for (int idx = k; idx < NC * kChs; idx += 128) {
+                    const int c = idx / kChs;
+                    const int chl = rank * kChs + (idx - c * kChs);
+                    const int i = c / G, h = c % G;
+                    if (i >= nrows) continue;
+                    const int hq = it.kvh * G + h;
+                    const size_t row = size_t(row0 + i);
+                    float mq[C], lq[C], oq[C];
+#pragma unroll
+                    for (int q = 0; q < C; ++q) {
+                        const uint32_t base = mapa_shared(mb_local, q);
+                        mq[q] = ld_cluster_f32(base + uint32_t(kMrgO + 4 * c));
+                        lq[q] = ld_cluster_f32(base + uint32_t(kMrgO + 64 + 4 * c));
+                        oq[q] = ld_cluster_f32(base + uint32_t(4 * (c * 128 + chl)));
+                    }
+                    const float t2 = p.sink ? p.sink[hq] * kLog2e : -INFINITY;
+                    float Mf = t2;
+#pragma unroll
+                    for (int q = 0; q < C; ++q) Mf = fmaxf(Mf, mq[q]);
+                    float Z = 0.f, acc = 0.f;
+                    if (Mf != -INFINITY) {
+                        Z = fast_exp2(t2 - Mf);
+#pragma unroll
+                        for (int q = 0; q < C; ++q) {
+                            const float w = mq[q] == -INFINITY ? 0.f : fast_exp2(mq[q] - Mf);
+                            Z += w * lq[q];
+                            acc += w * oq[q];
+                        }
+                    }
+                    const uint32_t packed = pack_bf16x2(Z > 0.f ? acc / Z : 0.f, 0.f);
+                    p.out[(row * p.num_q_heads + hq) * kD + chl] =
                         static_cast<uint16_t>(packed & 0xffffu);
-                    if (ch == 0 && p.lse)
+                    if (chl == 0 && p.lse)
                         p.lse[row * p.num_q_heads + hq] =
                             Z > 0.f ? (Mf + fast_log2(Z)) * kLn2 : -INFINITY;
-                } else {
-                    const size_t base =
-                        (size_t(it.part) * p.num_q_rows + row) * p.num_q_heads + hq;
-                    const float scale_o = lrsum[c] > 0.f ? lsum[c] / lrsum[c] : 0.f;
-                    p.ws_o[base * kD + ch] = o[c] * scale_o;
-                    if (ch == 0) {
-                        p.ws_m[base] = m[c] * kLn2;
-                        p.ws_l[base] = lsum[c];
-                    }
                 }
             }
             g += it.ntiles;
@@ -540,6 +665,7 @@ gqa_decode_tc_kernel(const __grid_constant__ GqaParams p) {
 
     tc::fence_before_sync();
     __syncthreads();
+    if constexpr (C > 1) cluster_sync();   // no CTA leaves while a peer may read its partials
     if (warp == 6) {
         tc::fence_after_sync();
         tc::tmem_dealloc(tmem, kTmemCols);
@@ -547,11 +673,12 @@ gqa_decode_tc_kernel(const __grid_constant__ GqaParams p) {
 }
 
 int g_num_sms_tc[64];
+int g_max_clusters_tc[64][2];   // clusters of 2 / 4 that fit at once, per device
 
-template <int G, int NC>
+template <int G, int NC, int C>
 cudaError_t launch_g(const GqaParams &p, cudaStream_t stream) {
-    const size_t smem = tc_smem_bytes(p.batch);
-    auto kern = gqa_decode_tc_kernel<G, NC>;
+    const size_t smem = tc_smem_bytes<C>(p.batch);
+    auto kern = gqa_decode_tc_kernel<G, NC, C>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          int(smem));
     if (e != cudaSuccess) return e;
@@ -565,13 +692,53 @@ cudaError_t launch_g(const GqaParams &p, cudaStream_t stream) {
         if (e != cudaSuccess) return e;
         g_num_sms_tc[dev] = n;
     }
-    long long grid = g_num_sms_tc[dev];   // one resident CTA per SM
-    const long long max_items = static_cast<long long>(p.batch) * (p.num_q_heads / G) *
-                                p.num_partitions;
-    if (grid > max_items) grid = max_items;
-    if (grid < 1) grid = 1;
-    kern<<<dim3(static_cast<unsigned>(grid)), kThreads, smem, stream>>>(p);
-    return cudaGetLastError();
+    const long long units = static_cast<long long>(p.batch) * (p.num_q_heads / G);
+    if constexpr (C == 1) {
+        long long grid = g_num_sms_tc[dev];   // one resident CTA per SM
+        const long long max_items = units * p.num_partitions;
+        if (grid > max_items) grid = max_items;
+        if (grid < 1) grid = 1;
+        kern<<<dim3(static_cast<unsigned>(grid)), kThreads, smem, stream>>>(p);
+        return cudaGetLastError();
+    } else {
+        cudaLaunchAttribute attr[1];
+        attr[0].id = cudaLaunchAttributeClusterDimension;
+        attr[0].val.clusterDim.x = C;
+        attr[0].val.clusterDim.y = 1;
+        attr[0].val.clusterDim.z = 1;
+        cudaLaunchConfig_t cfg = {};
+        cfg.blockDim = dim3(kThreads);
+        cfg.dynamicSmemBytes = smem;
+        cfg.stream = stream;
+        cfg.attrs = attr;
+        cfg.numAttrs = 1;
+        int &max_clusters = g_max_clusters_tc[dev][C == 2 ? 0 : 1];
+        if (max_clusters == 0) {
+            cfg.gridDim = dim3(static_cast<unsigned>(g_num_sms_tc[dev] / C * C));
+            int n = 0;
+            e = cudaOccupancyMaxActiveClusters(&n, kern, &cfg);
+            if (e != cudaSuccess) return e;
+            max_clusters = n > 0 ? n : 1;
+        }
+        long long clusters = max_clusters;   // persistent: one wave of clusters
+        if (clusters > units) clusters = units;
+        if (clusters < 1) clusters = 1;
+        cfg.gridDim = dim3(static_cast<unsigned>(clusters * C));
+        e = cudaLaunchKernelEx(&cfg, kern, p);
+        if (e != cudaSuccess) return e;
+        return cudaGetLastError();
+    }
+}
+
+template <int G, int NC>
+cudaError_t launch_c(const GqaParams &p, cudaStream_t stream) {
+    switch (p.cluster) {
+        case 0:
+        case 1: return launch_g<G, NC, 1>(p, stream);
+        case 2: return launch_g<G, NC, 2>(p, stream);
+        case 4: return launch_g<G, NC, 4>(p, stream);
+        default: return cudaErrorInvalidValue;
+    }
 }
 
 }  // namespace
@@ -581,10 +748,10 @@ cudaError_t launch_gqa_decode_tc(const GqaParams &p, cudaStream_t stream) {
         return cudaErrorInvalidValue;
     const bool fold = p.max_q_len > 1;
     switch (p.group) {
-        case 1: return fold ? launch_g<1, 16>(p, stream) : launch_g<1, 1>(p, stream);
-        case 2: return fold ? launch_g<2, 16>(p, stream) : launch_g<2, 2>(p, stream);
-        case 4: return fold ? launch_g<4, 16>(p, stream) : launch_g<4, 4>(p, stream);
-        case 8: return fold ? launch_g<8, 16>(p, stream) : launch_g<8, 8>(p, stream);
+        case 1: return fold ? launch_c<1, 16>(p, stream) : launch_c<1, 1>(p, stream);
+        case 2: return fold ? launch_c<2, 16>(p, stream) : launch_c<2, 2>(p, stream);
+        case 4: return fold ? launch_c<4, 16>(p, stream) : launch_c<4, 4>(p, stream);
+        case 8: return fold ? launch_c<8, 16>(p, stream) : launch_c<8, 8>(p, stream);
         default: return cudaErrorInvalidValue;
     }
 }

@@ -41,6 +41,8 @@ struct GqaParams {
     int box_rows;                 // tokens per TMA box (min(tile, page size))
     int num_partitions;           // P (grid.x)
     int chunk;                    // keys per partition slice, multiple of kGqaTileKeys
+    int cluster;                  // tensor-core kernel: 2 or 4 = P CTAs of a cluster split a
+                                  // unit and merge on chip (no workspace); 0 = off
     float qk_scale_log2;          // scale * log2(e)
 };
 

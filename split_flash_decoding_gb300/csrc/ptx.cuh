@@ -198,6 +198,13 @@ __device__ __forceinline__ void st_cluster_f4(uint32_t addr, float a, float b, f
                  : "memory");
 }
 
+// Load from a peer CTA's shared memory (cluster address).
+__device__ __forceinline__ float ld_cluster_f32(uint32_t addr) {
+    float v;
+    asm volatile("ld.shared::cluster.f32 %0, [%1];" : "=f"(v) : "r"(addr) : "memory");
+    return v;
+}
+
 // Asynchronous 16-byte store into a peer CTA's shared memory that reports its
 // bytes to the peer's mbarrier (complete_tx), so the peer needs no fence.
 __device__ __forceinline__ void st_async_f4(uint32_t addr, float a, float b, float c, float d,

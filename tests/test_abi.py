@@ -109,11 +109,11 @@ def test_decode_rejects_bad_arguments_before_launch(attn):
         == E.ATTN_ERR_INVALID_ARG                                             # fewer seqs
     # K and V must share one page-table layout
     assert call_decode(attn, v=kv(attn, page_table=0x20100)) == E.ATTN_ERR_UNSUPPORTED
-    # split-K needs a large enough, aligned workspace
-    assert call_decode(attn, P=4) == E.ATTN_ERR_WORKSPACE
-    assert call_decode(attn, P=4, ws=0x60000, ws_bytes=16) == E.ATTN_ERR_WORKSPACE
-    P, need = attn.attn_plan_partitions(2, 2, 32, 8, 128, 500, 4, num_sms=152)
-    assert call_decode(attn, P=4, ws=0x60010, ws_bytes=need) == E.ATTN_ERR_WORKSPACE
+    # split-K through the workspace needs a large enough, aligned one
+    assert call_decode(attn, P=3) == E.ATTN_ERR_WORKSPACE
+    assert call_decode(attn, P=3, ws=0x60000, ws_bytes=16) == E.ATTN_ERR_WORKSPACE
+    P, need = attn.attn_plan_partitions(2, 2, 32, 8, 128, 500, 3, num_sms=152)
+    assert call_decode(attn, P=3, ws=0x60010, ws_bytes=need) == E.ATTN_ERR_WORKSPACE
     # rows must match the batch without row offsets; multi-row needs offsets
     assert call_decode(attn, rows=3) == E.ATTN_ERR_INVALID_ARG
     assert call_decode(attn, max_q_len=4) == E.ATTN_ERR_INVALID_ARG
@@ -202,13 +202,18 @@ def test_reduce_rejects_bad_arguments(attn):
 
 def test_planner_formulas(attn):
     # explicit request is honoured verbatim
-    for req in (1, 2, 7, 148, 1024):
+    for req in (1, 3, 7, 148, 1024):
         P, ws = attn.attn_plan_partitions(64, 64, 32, 8, 128, 8192, req, num_sms=152)
         assert P == req
         n = req * 64 * 32
         align = lambda x: (x + 255) // 256 * 256
         expect = 0 if req == 1 else align(n * 128 * 4) + 2 * align(n * 4)
         assert ws == expect
+    # 2 or 4 partitions on the tensor-core path merge on chip: no workspace
+    for req in (2, 4):
+        assert attn.attn_plan_partitions(64, 64, 32, 8, 128, 8192, req, num_sms=152)[1] == 0
+        P, ws = attn.attn_plan_partitions(64, 64, 32, 16, 64, 8192, req, num_sms=152)
+        assert ws > 0                                 # head_dim 64 keeps the workspace
     # automatic GQA (head_dim 128: one CTA per SM; head_dim 64: two): fewer
     # units than CTAs -> one wave of slices; otherwise >= 4 items per CTA at
     # full length and slices of <= ~1024 keys
@@ -237,6 +242,11 @@ def test_planner_formulas(attn):
     assert P == 4                                     # slices of 8192 keys for 2 rows
     P, _ = attn.attn_plan_partitions(1, 1, 32, 8, 128, 20, 0, num_sms=152)
     assert P == 1                                     # one tile of keys cannot split
+    # a few query rows per sequence (the 16-column fold): long items
+    P, _ = attn.attn_plan_partitions(64, 160, 32, 8, 128, 8192, 0, num_sms=152)
+    assert P == 1                                     # 512 units, >= 2 per CTA
+    P, ws = attn.attn_plan_partitions(16, 40, 32, 8, 128, 8192, 0, num_sms=152)
+    assert P == 2 and ws == 0                         # 128 units: a pair merged on chip
     P, _ = attn.attn_plan_partitions(4, 4, 32, 8, 128, 0, 0, num_sms=152)
     assert P == 1
     # every CTA gets at least one slice of a full-length batch

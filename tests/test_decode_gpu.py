@@ -156,6 +156,31 @@ def test_graph_capture_replays_with_new_lengths(attn):
         assert_close(out, lse, ref_o, ref_l, f"graph replay {new}")
 
 
+@pytest.mark.parametrize("P", [2, 4])
+def test_small_split_merged_on_chip(attn, P):
+    """2 or 4 partitions on the tensor cores: a cluster of P CTAs splits each
+    (sequence, KV head) and merges on chip.  Lengths below one tile per CTA
+    leave some CTAs of a cluster without keys; sinks; every group size."""
+    for hq, hkv, seed in ((32, 8, 61), (16, 16, 62), (64, 8, 63)):
+        w = W.make_workload("t", batch=6, num_q_heads=hq, num_kv_heads=hkv, dim_qk=128,
+                            kv_lens=[1, 100, 129, 513, 5000, 0], page_size=64, seed=seed,
+                            device=DEV, sink=True)
+        out, lse = run(attn, w, P)
+        ref_o, ref_l = oracle_result(w)
+        assert_close(out, lse, ref_o, ref_l, f"on-chip merge P={P} hq={hq} hkv={hkv}")
+        o1, l1 = run(attn, w, 1)
+        assert_close(out, lse, o1.float().cpu().numpy(), l1.cpu().double().numpy(),
+                     f"on-chip merge P={P} vs P=1")
+
+
+def test_llama3_8b_full_size_merged_on_chip(attn):
+    w = W.llama3_8b_decode(device=DEV)
+    ref_o, ref_l = oracle_result(w)
+    for P in (2, 4):
+        out, lse = run(attn, w, P)
+        assert_close(out, lse, ref_o, ref_l, f"llama3-8b on-chip P={P}")
+
+
 def test_llama3_8b_decode_full_size(attn):
     """The Llama-3-8B-shaped decode batch at full size, auto split-K, against
     the oracle on every (sequence, head)."""

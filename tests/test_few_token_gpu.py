@@ -86,7 +86,7 @@ def test_sinks(attn):
 def test_split_matches_unsplit(attn):
     w = few_workload([4, 3, 2, 1, 4], [3000, 1500, 7000, 200, 5000], seed=65)
     o1, l1 = run(attn, w, 1)
-    for P in (2, 7, 16):
+    for P in (2, 4, 7, 16):
         o, l = run(attn, w, P)
         assert_close(o, l, o1.float().cpu().numpy().astype("float64"),
                      l1.cpu().numpy().astype("float64"), f"few P={P} vs P=1")
