@@ -120,6 +120,8 @@ def test_decode_rejects_bad_arguments_before_launch(attn):
     assert call_decode(attn, max_q_len=0) == E.ATTN_ERR_INVALID_ARG
     # the multi-row tile path does not split K
     assert call_decode(attn, offs=0x70000, rows=40, max_q_len=30, P=2) == E.ATTN_ERR_UNSUPPORTED
+    # the decode kernel's item table holds at most 2048 sequences
+    assert call_decode(attn, batch=2049) == E.ATTN_ERR_UNSUPPORTED
     # an empty batch is a no-op
     assert call_decode(attn, batch=0, q=None, out=None) == E.ATTN_OK
 

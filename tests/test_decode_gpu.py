@@ -181,6 +181,29 @@ def test_llama3_8b_full_size_merged_on_chip(attn):
         assert_close(out, lse, ref_o, ref_l, f"llama3-8b on-chip P={P}")
 
 
+def test_maximum_batch(attn):
+    """The decode kernel's largest batch (2048 sequences, one item table entry
+    each) with ragged short lengths, empty sequences included."""
+    g = torch.Generator().manual_seed(71)
+    lens = [int(x) for x in torch.randint(0, 300, (2048,), generator=g)]
+    w = W.make_workload("t", batch=2048, num_q_heads=32, num_kv_heads=8, dim_qk=128,
+                        kv_lens=lens, page_size=32, seed=71, device=DEV)
+    ref_o, ref_l = oracle_result(w)
+    for P in (0, 3):
+        out, lse = run(attn, w, P)
+        assert_close(out, lse, ref_o, ref_l, f"batch 2048 P={P}")
+
+
+def test_maximum_partitions(attn):
+    """ATTN_MAX_PARTITIONS slices of one tile each over one long sequence:
+    the wide reduce merges 1024 partials per (row, head)."""
+    w = W.make_workload("t", batch=1, num_q_heads=32, num_kv_heads=8, dim_qk=128,
+                        kv_lens=[131072], page_size=128, seed=72, device=DEV, sink=True)
+    out, lse = run(attn, w, attn.ATTN_MAX_PARTITIONS)
+    ref_o, ref_l = oracle_result(w)
+    assert_close(out, lse, ref_o, ref_l, "P=1024")
+
+
 def test_llama3_8b_decode_full_size(attn):
     """The Llama-3-8B-shaped decode batch at full size, auto split-K, against
     the oracle on every (sequence, head)."""

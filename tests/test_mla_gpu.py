@@ -46,7 +46,7 @@ def test_mla_small_matches_oracle(attn, P):
     assert_close(out, lse, ref_o, ref_l, f"mla P={P}")
 
 
-@pytest.mark.parametrize("page_size", [16, 64, 128])
+@pytest.mark.parametrize("page_size", [8, 16, 64, 128])
 def test_mla_paged_equals_contiguous_bitwise(attn, page_size):
     w = mla_workload([5, 130, 1000], page_size=page_size, seed=22)
     c = W.contiguous_copy(w)
@@ -78,6 +78,15 @@ def test_mla_split_k_matches_single_partition(attn):
     for P in (2, 9, 64):
         oP, lP = run(attn, w, P)
         assert_close(oP, lP, ref_o, ref_l, f"mla P={P}")
+
+
+def test_mla_many_one_tile_slices(attn):
+    """Slices of one 64-key tile each (P = 1024 over 65536 keys): the
+    partials of every slice go through the wide reduce."""
+    w = mla_workload([65536], seed=25)
+    out, lse = run(attn, w, attn.ATTN_MAX_PARTITIONS)
+    ref_o, ref_l = oracle_result(w)
+    assert_close(out, lse, ref_o, ref_l, "mla P=1024")
 
 
 def test_deepseek_v3_mla_full_size_sampled(attn):

@@ -123,6 +123,17 @@ def test_sparse_split_k_matches_single_partition(attn):
         assert_close(oP, lP, ref_o, ref_l, f"sparse P={P}")
 
 
+def test_sparse_single_key_and_unit_stride(attn):
+    """indices_stride 1, one key per sequence: out is that row's V exactly up
+    to bf16 rounding and lse is its score."""
+    w = sparse_workload([40, 1, 900], topk=1, seed=39)
+    assert w.indices.shape[1] == 1
+    for P in (1, 2):
+        out, lse = run(attn, w, P)
+        ref_o, ref_l = oracle_result(w)
+        assert_close(out, lse, ref_o, ref_l, f"sparse top-1 P={P}")
+
+
 def test_sparse_entries_past_topk_are_not_read(attn):
     """Entries past topk_lengths[b] may hold anything, out-of-range rows
     included: they are never read and set no error bit."""
