@@ -23,6 +23,7 @@ namespace {
 
 constexpr int kWarps = 8;
 constexpr int kMaxP = 1024;   // ATTN_MAX_PARTITIONS
+constexpr int kFastP = 8;     // partitions merged in one round trip
 
 // Sequence of query row `row`: the row itself, or found in the row offsets.
 __device__ __forceinline__ int row_sequence(const ReduceParams &p, int row) {
@@ -61,6 +62,49 @@ splitk_reduce_kernel(const __grid_constant__ ReduceParams p) {
     }
     const size_t stride_p = static_cast<size_t>(p.rows) * p.num_q_heads;  // per partition
     const size_t idx0 = static_cast<size_t>(row) * p.num_q_heads + h;
+
+    if (P <= kFastP) {
+        // Few partitions: the O partials of the first channel block, m and l
+        // are all requested at once (one round trip), and lane q's weight
+        // reaches the other lanes by shuffle.
+        const float m_lane = lane < P ? p.ws_m[lane * stride_p + idx0] : -INFINITY;
+        const float l_lane = lane < P ? p.ws_l[lane * stride_p + idx0] : 0.f;
+        const float *src0 = p.ws_o + idx0 * p.dim_v + lane * 4;
+        const size_t step = stride_p * p.dim_v;
+        float4 o[kFastP];
+#pragma unroll
+        for (int q = 0; q < kFastP; ++q)
+            if (q < P && lane * 4 < p.dim_v)
+                o[q] = *reinterpret_cast<const float4 *>(src0 + q * step);
+        const float t = p.sink ? p.sink[h] : -INFINITY;
+        const float Mf = fmaxf(warp_max(m_lane), t);
+        const float w_lane = m_lane == -INFINITY ? 0.f : fast_exp2((m_lane - Mf) * kLog2e);
+        float Z = warp_sum(w_lane * l_lane);
+        if (Mf != -INFINITY) Z += fast_exp2((t - Mf) * kLog2e);
+        const float inv = Z > 0.f ? 1.f / Z : 0.f;
+        for (int c = lane * 4; c < p.dim_v; c += 128) {
+            if (c != lane * 4) {
+#pragma unroll
+                for (int q = 0; q < kFastP; ++q)
+                    if (q < P) o[q] = *reinterpret_cast<const float4 *>(src0 + (c - lane * 4) + q * step);
+            }
+            float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+            for (int q = 0; q < kFastP; ++q) {
+                const float w = __shfl_sync(0xffffffffu, w_lane, q);
+                if (q < P && w != 0.f) {
+                    acc.x += w * o[q].x; acc.y += w * o[q].y;
+                    acc.z += w * o[q].z; acc.w += w * o[q].w;
+                }
+            }
+            uint2 packed;
+            packed.x = pack_bf16x2(acc.x * inv, acc.y * inv);
+            packed.y = pack_bf16x2(acc.z * inv, acc.w * inv);
+            *reinterpret_cast<uint2 *>(p.out + idx0 * p.dim_v + c) = packed;
+        }
+        if (lane == 0 && p.lse) p.lse[idx0] = Z > 0.f ? Mf + fast_log2(Z) * kLn2 : -INFINITY;
+        return;
+    }
 
     float mloc = -INFINITY;
     for (int q = lane; q < P; q += 32) mloc = fmaxf(mloc, p.ws_m[q * stride_p + idx0]);
