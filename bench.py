@@ -237,6 +237,13 @@ def algorithmic_flops(w) -> int:
     return visible_pairs(w) * w.num_q_heads * 2 * (w.dim_qk + w.dim_v)
 
 
+def roofline_bound(flops: float, nbytes: float, tensor_tflops: float, hbm_gbs: float) -> str:
+    """Whichever roof the algorithmic intensity reaches first: FLOP per byte
+    above the ridge (tensor peak / HBM peak) is tensor-bound."""
+    ridge = tensor_tflops * 1e12 / (hbm_gbs * 1e9)
+    return "tensor" if flops / nbytes > ridge else "hbm"
+
+
 def max_over_ranks(values, dist, device=None):
     """Element-wise max of per-rank timings (host-side bookkeeping only; the
     attention path itself has no collective)."""
@@ -526,7 +533,7 @@ def run_ours(args, rank, world, dist):
     # The bound is whichever roof the algorithmic intensity reaches first:
     # FLOP per byte above the ridge (tensor peak / HBM peak) is tensor-bound.
     ridge = tensor_peak * 1e12 / (peak * 1e9)
-    if flops / nbytes > ridge:
+    if roofline_bound(flops, nbytes, tensor_peak, peak) == "tensor":
         # e.g. causal prefill tiles (about 9x past the ridge), MLA with draft rows
         roofline = {"bound": "tensor", "achieved": round(tflops, 2), "peak": tensor_peak,
                     "unit": "TFLOP/s", "frac": round(tflops / tensor_peak, 4),
