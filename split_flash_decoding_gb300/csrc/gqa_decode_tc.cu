@@ -62,7 +62,11 @@ constexpr int kTileBytes = 2 * kBox;         // 128 keys x 128 channels, bf16
 constexpr int kNRows = 16;                   // N of both MMAs (query heads, padded)
 constexpr int kNBox = kNRows * 128;          // 16 rows x 128 B
 constexpr int kNBytes = 2 * kNBox;           // 16 rows x 128 channels / keys
-constexpr int kThreads = 224;
+// Threads: softmax warps (4, or 8 for the 16-column fold: two groups of four
+// sharing the TMEM lanes, each taking 8 of the 16 columns) + K producer + V
+// producer + MMA.
+__host__ __device__ constexpr int softmax_groups(int nc) { return nc > 8 ? 2 : 1; }
+__host__ __device__ constexpr int threads_for(int nc) { return 32 * (4 * softmax_groups(nc) + 3); }
 constexpr uint32_t kTmemCols = 64;
 constexpr uint32_t kTmemS = 0;               // two 16-column score buffers
 constexpr uint32_t kTmemO = 32;              // 16-column output accumulator
@@ -305,8 +309,12 @@ __device__ __forceinline__ void produce(const GqaParams &p, const int *cum, int 
 // G: query heads per KV head; NC: score columns (G for one row per sequence,
 // 16 for the few-token fold).
 template <int G, int NC, int C>
-__global__ void __launch_bounds__(kThreads, 1)
+__global__ void __launch_bounds__(threads_for(NC), 1)
 gqa_decode_tc_kernel(const __grid_constant__ GqaParams p) {
+    constexpr int kGroups = softmax_groups(NC);   // softmax warp groups
+    constexpr int NW = NC / kGroups;              // score columns per group
+    constexpr int kWarpK = 4 * kGroups, kWarpV = kWarpK + 1, kWarpMma = kWarpK + 2;
+    constexpr int kThreads = threads_for(NC);
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -323,11 +331,11 @@ gqa_decode_tc_kernel(const __grid_constant__ GqaParams p) {
         for (int i = 0; i < kNumBars; ++i) {
             const bool per_warp = (i == kSFree || i == kSFree + 1 || i == kPFull);
             const bool merge = i == kMrgFull || i == kMrgFull + 1;
-            mbar_init(&bar[i], merge ? 4u * C : (per_warp ? 4u : 1u));
+            mbar_init(&bar[i], merge ? 4u * kGroups * C : (per_warp ? 4u * kGroups : 1u));
         }
         fence_mbar_init();
     }
-    if (warp == 6) {
+    if (warp == kWarpMma) {
         tc::tmem_alloc(tmem_slot, kTmemCols);
         tc::tmem_relinquish();
     }
@@ -343,11 +351,11 @@ gqa_decode_tc_kernel(const __grid_constant__ GqaParams p) {
     const uint32_t tmem = *tmem_slot;
     const int num_items = C > 1 ? p.batch * hkv : cum[p.batch];
 
-    if (warp == 4) {
+    if (warp == kWarpK) {
         produce<true, C>(p, cum, num_items, hkv, smem, bar, lane);
-    } else if (warp == 5) {
+    } else if (warp == kWarpV) {
         produce<false, C>(p, cum, num_items, hkv, smem, bar, lane);
-    } else if (warp == 6) {
+    } else if (warp == kWarpMma) {
         // ---------------------------------------------------------- MMA issue
         if (lane == 0) {
             constexpr uint32_t idesc_s = tc::idesc_bf16_f32(128, kNRows, 0, 0);
@@ -415,8 +423,11 @@ gqa_decode_tc_kernel(const __grid_constant__ GqaParams p) {
         }
     } else {
         // ---------------------------------------------------- softmax + epilogue
-        const int k = warp * 32 + lane;              // key of the tile == TMEM lane
-        const uint32_t lane_base = uint32_t(warp * 32) << 16;
+        const int kw = warp & 3;                     // key warp: TMEM lanes 32 kw ..
+        const int grp = warp >> 2;                   // column group: columns grp * NW ..
+        const int cg0 = grp * NW;
+        const int k = kw * 32 + lane;                // key of the tile == TMEM lane
+        const uint32_t lane_base = uint32_t(kw * 32) << 16;
         float *red = reinterpret_cast<float *>(smem + Smem::red);     // [2][4][16]
         float *lred = reinterpret_cast<float *>(smem + Smem::lred);   // [2][4][16]
         uint8_t *pbuf = smem + Smem::p;
@@ -426,16 +437,17 @@ gqa_decode_tc_kernel(const __grid_constant__ GqaParams p) {
             const GqaItem it = walk_item<C>(p, cum, j, hkv);
             int row0, nrows;
             seq_rows(p, it.b, row0, nrows);
-            // Column c = (row c / G, head c % G): keys j < lim[c] are visible.
-            int lim[NC];
+            // Column cg = (row cg / G, head cg % G): keys j < lim visible.
+            // This group's columns: cg = cg0 + c, c < NW.
+            int lim[NW];
 #pragma unroll
-            for (int c = 0; c < NC; ++c) {
-                const int i = c / G;
+            for (int c = 0; c < NW; ++c) {
+                const int i = (cg0 + c) / G;
                 lim[c] = i >= nrows ? 0 : (p.causal ? it.L - nrows + i + 1 : it.L);
             }
-            float m[NC], l[NC], lr[NC];
+            float m[NW], l[NW], lr[NW];
 #pragma unroll
-            for (int c = 0; c < NC; ++c) {
+            for (int c = 0; c < NW; ++c) {
                 m[c] = -INFINITY;
                 l[c] = 0.f;
                 lr[c] = 0.f;
@@ -449,8 +461,8 @@ gqa_decode_tc_kernel(const __grid_constant__ GqaParams p) {
                 const int nvalid = min(kBK, it.end - t0);
                 ok = ok && mbar_wait(&bar[kSFull + sb], (gg >> 1) & 1, p.err);
                 tc::fence_after_sync();
-                float s[NC];
-                tmem_ld_cols<NC>(tmem + lane_base + kTmemS + sb * kNRows, s);
+                float s[NW];
+                tmem_ld_cols<NW>(tmem + lane_base + kTmemS + sb * kNRows + cg0, s);
                 tc::fence_before_sync();
                 __syncwarp();
                 if (lane == 0) mbar_arrive(&bar[kSFree + sb]);
@@ -459,17 +471,19 @@ gqa_decode_tc_kernel(const __grid_constant__ GqaParams p) {
                 const bool valid = k < nvalid;
                 float *rb = red + (gg & 1) * 64;
 #pragma unroll
-                for (int c = 0; c < NC; ++c) {
+                for (int c = 0; c < NW; ++c) {
                     s[c] = valid && t0 + k < lim[c] ? s[c] * p.qk_scale_log2 : -INFINITY;
                     const float wm = warp_max_redux(s[c]);
-                    if (lane == 0) rb[warp * 16 + c] = wm;
+                    if (lane == 0) rb[kw * 16 + cg0 + c] = wm;
                 }
-                named_sync(1, 128);
-                float alpha[NC];
+                named_sync(1 + grp, 128);
+                float alpha[NW];
                 bool moved = false;
 #pragma unroll
-                for (int c = 0; c < NC; ++c) {
-                    const float tmax = fmaxf(fmaxf(rb[c], rb[16 + c]), fmaxf(rb[32 + c], rb[48 + c]));
+                for (int c = 0; c < NW; ++c) {
+                    const int cg = cg0 + c;
+                    const float tmax =
+                        fmaxf(fmaxf(rb[cg], rb[16 + cg]), fmaxf(rb[32 + cg], rb[48 + cg]));
                     const float mn = fmaxf(m[c], tmax);
                     // A column with no visible key so far keeps m = -inf and
                     // weights 0 (its alpha is irrelevant: l and O are 0).
@@ -477,9 +491,9 @@ gqa_decode_tc_kernel(const __grid_constant__ GqaParams p) {
                     moved |= mn != m[c];
                     m[c] = mn;
                 }
-                uint16_t pb[NC];
+                uint16_t pb[NW];
 #pragma unroll
-                for (int c = 0; c < NC; ++c) {
+                for (int c = 0; c < NW; ++c) {
                     const float pv = s[c] != -INFINITY ? fast_exp2(s[c] - m[c]) : 0.f;
                     const uint32_t packed = pack_bf16x2(pv, 0.f);
                     pb[c] = static_cast<uint16_t>(packed & 0xffffu);
@@ -491,19 +505,19 @@ gqa_decode_tc_kernel(const __grid_constant__ GqaParams p) {
                     // rescaled (thread = channel lane, columns = heads).
                     ok = ok && mbar_wait(&bar[kODone], (gg - 1) & 1, p.err);
                     tc::fence_after_sync();
-                    if (moved) {   // identical in every thread
-                        float o[NC];
-                        tmem_ld_cols<NC>(tmem + lane_base + kTmemO, o);
+                    if (moved) {   // identical in every thread of the group
+                        float o[NW];
+                        tmem_ld_cols<NW>(tmem + lane_base + kTmemO + cg0, o);
 #pragma unroll
-                        for (int c = 0; c < NC; ++c) o[c] *= alpha[c];
-                        tmem_st_cols<NC>(tmem + lane_base + kTmemO, o);
+                        for (int c = 0; c < NW; ++c) o[c] *= alpha[c];
+                        tmem_st_cols<NW>(tmem + lane_base + kTmemO + cg0, o);
                         tc::tmem_wait_st();
                     }
                 }
 #pragma unroll
-                for (int c = 0; c < NC; ++c)
-                    *reinterpret_cast<uint16_t *>(pbuf + n_operand_offset(c, k)) = pb[c];
-                if (t0 + kBK > it.L) {
+                for (int c = 0; c < NW; ++c)
+                    *reinterpret_cast<uint16_t *>(pbuf + n_operand_offset(cg0 + c, k)) = pb[c];
+                if (grp == 0 && t0 + kBK > it.L) {
                     // Slots past the sequence end may hold anything (even NaN):
                     // zero them in the V stage before P.V reads it.
                     const int vs = gg % kStages;
@@ -528,38 +542,39 @@ gqa_decode_tc_kernel(const __grid_constant__ GqaParams p) {
                 ok = mbar_wait(&bar[kODone], (g + it.ntiles - 1) & 1, p.err);
                 tc::fence_after_sync();
             }
-            float lsum[NC], lrsum[NC];
+            float lsum[NW], lrsum[NW];
             {
-                float *lb = lred + (iter & 1) * 128;   // [4 warps][2][16]
+                float *lb = lred + (iter & 1) * 128;   // [4 key warps][2][16 columns]
 #pragma unroll
-                for (int c = 0; c < NC; ++c) {
+                for (int c = 0; c < NW; ++c) {
                     const float a = warp_sum(l[c]);
                     const float b2 = warp_sum(lr[c]);
                     if (lane == 0) {
-                        lb[warp * 32 + c] = a;
-                        lb[warp * 32 + 16 + c] = b2;
+                        lb[kw * 32 + cg0 + c] = a;
+                        lb[kw * 32 + 16 + cg0 + c] = b2;
                     }
                 }
-                named_sync(1, 128);
+                named_sync(1 + grp, 128);
 #pragma unroll
-                for (int c = 0; c < NC; ++c) {
-                    lsum[c] = (lb[c] + lb[32 + c]) + (lb[64 + c] + lb[96 + c]);
-                    lrsum[c] = (lb[16 + c] + lb[48 + c]) + (lb[80 + c] + lb[112 + c]);
+                for (int c = 0; c < NW; ++c) {
+                    const int cg = cg0 + c;
+                    lsum[c] = (lb[cg] + lb[32 + cg]) + (lb[64 + cg] + lb[96 + cg]);
+                    lrsum[c] = (lb[16 + cg] + lb[48 + cg]) + (lb[80 + cg] + lb[112 + cg]);
                 }
             }
-            float o[NC];
+            float o[NW];
             if (ok && it.ntiles > 0) {
-                tmem_ld_cols<NC>(tmem + lane_base + kTmemO, o);
+                tmem_ld_cols<NW>(tmem + lane_base + kTmemO + cg0, o);
             } else {
 #pragma unroll
-                for (int c = 0; c < NC; ++c) o[c] = 0.f;
+                for (int c = 0; c < NW; ++c) o[c] = 0.f;
             }
             tc::fence_before_sync();
             if constexpr (C == 1) {
                 const int ch = k;   // output channel of this thread
-    #pragma unroll
-                for (int c = 0; c < NC; ++c) {
-                    const int i = c / G, h = c % G;
+#pragma unroll
+                for (int c = 0; c < NW; ++c) {
+                    const int i = (cg0 + c) / G, h = (cg0 + c) % G;
                     if (i >= nrows) continue;
                     const int hq = it.kvh * G + h;
                     const size_t row = size_t(row0 + i);
@@ -599,16 +614,16 @@ gqa_decode_tc_kernel(const __grid_constant__ GqaParams p) {
                 float *mo = reinterpret_cast<float *>(mb);                 // [16][128]
                 float *mml = reinterpret_cast<float *>(mb + kMrgO);        // m[16], l[16]
 #pragma unroll
-                for (int c = 0; c < NC; ++c) {
+                for (int c = 0; c < NW; ++c) {
                     // normalised to the fp32 weight sum, as a workspace partial
                     const float scale_o = lrsum[c] > 0.f ? lsum[c] / lrsum[c] : 0.f;
-                    mo[c * 128 + k] = o[c] * scale_o;
+                    mo[(cg0 + c) * 128 + k] = o[c] * scale_o;
                 }
                 if (k == 0) {
 #pragma unroll
-                    for (int c = 0; c < NC; ++c) {
-                        mml[c] = m[c];        // base 2
-                        mml[16 + c] = lsum[c];
+                    for (int c = 0; c < NW; ++c) {
+                        mml[cg0 + c] = m[c];        // base 2
+                        mml[16 + cg0 + c] = lsum[c];
                     }
                 }
                 __syncwarp();
@@ -621,7 +636,7 @@ gqa_decode_tc_kernel(const __grid_constant__ GqaParams p) {
                 // this CTA's output channels [rank * 128 / C, (rank + 1) * 128 / C)
                 constexpr int kChs = 128 / C;
                 const uint32_t mb_local = smem_addr(mb);
-                for (int idx = k; idx < NC * kChs; idx += 128) {
+                for (int idx = grp * 128 + k; idx < NC * kChs; idx += 128 * kGroups) {
                     const int c = idx / kChs;
                     const int chl = rank * kChs + (idx - c * kChs);
                     const int i = c / G, h = c % G;
@@ -666,7 +681,7 @@ gqa_decode_tc_kernel(const __grid_constant__ GqaParams p) {
     tc::fence_before_sync();
     __syncthreads();
     if constexpr (C > 1) cluster_sync();   // no CTA leaves while a peer may read its partials
-    if (warp == 6) {
+    if (warp == kWarpMma) {
         tc::fence_after_sync();
         tc::tmem_dealloc(tmem, kTmemCols);
     }
@@ -698,7 +713,7 @@ cudaError_t launch_g(const GqaParams &p, cudaStream_t stream) {
         const long long max_items = units * p.num_partitions;
         if (grid > max_items) grid = max_items;
         if (grid < 1) grid = 1;
-        kern<<<dim3(static_cast<unsigned>(grid)), kThreads, smem, stream>>>(p);
+        kern<<<dim3(static_cast<unsigned>(grid)), threads_for(NC), smem, stream>>>(p);
         return cudaGetLastError();
     } else {
         cudaLaunchAttribute attr[1];
@@ -707,7 +722,7 @@ cudaError_t launch_g(const GqaParams &p, cudaStream_t stream) {
         attr[0].val.clusterDim.y = 1;
         attr[0].val.clusterDim.z = 1;
         cudaLaunchConfig_t cfg = {};
-        cfg.blockDim = dim3(kThreads);
+        cfg.blockDim = dim3(threads_for(NC));
         cfg.dynamicSmemBytes = smem;
         cfg.stream = stream;
         cfg.attrs = attr;
