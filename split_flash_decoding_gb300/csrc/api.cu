@@ -276,10 +276,11 @@ extern "C" int attn_plan_partitions(int num_sms, int batch, int num_q_rows, int 
             const long long p_len = (static_cast<long long>(max_kv_len) + target - 1) / target;
             p = p_fill > p_len ? p_fill : p_len;
         } else if (tc && num_q_rows > batch && units >= ctas / 2) {
-            // A few query rows per sequence fold onto 16 score columns, and
-            // every item then pays a 16-column epilogue and partial: long
-            // items win.  One slice per unit when there are two units per
-            // CTA or more, else two slices merged on chip by a CTA pair.
+            // A few query rows per sequence fold onto 16 score columns.  With
+            // enough units the split buys little (the memory streams are
+            // already spread over every SM) and costs a workspace and a
+            // reduce: one slice per unit when there are two units per CTA
+            // or more, else two slices merged on chip by a CTA pair.
             p = units >= 2 * ctas ? 1 : 2;
         } else if (units < ctas) {
             p = (ctas + units - 1) / units;
