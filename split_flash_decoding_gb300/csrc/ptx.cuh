@@ -192,28 +192,11 @@ __device__ __forceinline__ uint32_t mapa_shared(uint32_t addr, uint32_t rank) {
     return r;
 }
 
-__device__ __forceinline__ void st_cluster_f4(uint32_t addr, float a, float b, float c, float d) {
-    asm volatile("st.shared::cluster.v4.f32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "f"(a), "f"(b),
-                 "f"(c), "f"(d)
-                 : "memory");
-}
-
 // Load from a peer CTA's shared memory (cluster address).
 __device__ __forceinline__ float ld_cluster_f32(uint32_t addr) {
     float v;
     asm volatile("ld.shared::cluster.f32 %0, [%1];" : "=f"(v) : "r"(addr) : "memory");
     return v;
-}
-
-// Asynchronous 16-byte store into a peer CTA's shared memory that reports its
-// bytes to the peer's mbarrier (complete_tx), so the peer needs no fence.
-__device__ __forceinline__ void st_async_f4(uint32_t addr, float a, float b, float c, float d,
-                                            uint32_t mbar) {
-    asm volatile(
-        "st.async.shared::cluster.mbarrier::complete_tx::bytes.v4.f32 [%0], {%1, %2, %3, %4}, "
-        "[%5];" ::"r"(addr),
-        "f"(a), "f"(b), "f"(c), "f"(d), "r"(mbar)
-        : "memory");
 }
 
 // Bulk copy of `bytes` (multiple of 16) from this CTA's shared memory to a
@@ -264,23 +247,9 @@ __device__ __forceinline__ bool mbar_wait_cluster(uint64_t *bar, uint32_t parity
     }
 }
 
-__device__ __forceinline__ void fence_cluster() {
-    asm volatile("fence.acq_rel.cluster;" ::: "memory");
-}
-
 __device__ __forceinline__ void cluster_sync() {
     asm volatile("barrier.cluster.arrive.release.aligned;\n\t"
                  "barrier.cluster.wait.acquire.aligned;" ::: "memory");
-}
-
-// 2-D tiled TMA load.
-__device__ __forceinline__ void tma_load_2d(void *dst, const CUtensorMap *map, uint64_t *bar,
-                                            int c0, int c1) {
-    asm volatile(
-        "cp.async.bulk.tensor.2d.shared::cta.global.tile.mbarrier::complete_tx::bytes"
-        " [%0], [%1, {%2, %3}], [%4];" ::"r"(smem_addr(dst)),
-        "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(smem_addr(bar))
-        : "memory");
 }
 
 }  // namespace attn

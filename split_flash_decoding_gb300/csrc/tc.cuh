@@ -179,9 +179,6 @@ __device__ __forceinline__ void tmem_st_n(uint32_t taddr, const float (&v)[N]) {
     }
 }
 
-__device__ __forceinline__ void tmem_wait_ld() {
-    asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
-}
 __device__ __forceinline__ void tmem_wait_st() {
     asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
 }
