@@ -117,12 +117,17 @@ typedef struct attn_kv {
  * MLA shape and everything else as GQA.  GQA with head_dim 128 and more
  * query rows than sequences (the few-row fold): P = 1 when there are at
  * least 2 (sequence, KV head) units per SM, P = 2 when there are at least
- * num_sms / 2.  MLA:
- * P = max(floor(num_sms / 2 / num_q_rows), ceil(max_kv_len / (4096 n))), at
- * least 1, with n = ceil(num_q_rows / batch) query rows per sequence (one
- * two-CTA cluster per SM pair and per row; slices of about 4096 keys per
- * row, or as many as one wave of clusters holds).  For attn_mla_decode_sparse pass
- * max_kv_len = indices_stride.
+ * num_sms / 2.  MLA: with
+ * P' = max(floor(num_sms / 2 / num_q_rows), ceil(max_kv_len / (4096 n))),
+ * n = ceil(num_q_rows / batch) query rows per sequence, capped at
+ * ceil(max_kv_len / 64), the plan is P = 1 (no split) when P' <= 1 and
+ * otherwise P = 0, the balanced split: the 64-key tiles of every query row,
+ * concatenated, are dealt out in equal contiguous ranges to
+ * min(num_sms / 2, tiles) two-CTA clusters (one wave), with workspace_bytes
+ * = (num_sms / 2 + num_q_rows) slots of fp32 partials (128 x 512 O, m, l,
+ * each array 256-byte aligned) plus 16 (num_sms / 2) + 24 num_q_rows bytes
+ * of plan tables (each 256-byte aligned); it does not depend on max_kv_len.
+ * For attn_mla_decode_sparse pass max_kv_len = indices_stride.
  * Returns ATTN_OK, ATTN_ERR_INVALID_ARG, or ATTN_ERR_CUDA if the SM count
  * query fails.  Launches nothing.
  */
@@ -199,9 +204,23 @@ int attn_decode(const void *q, const attn_kv_t *k, const attn_kv_t *v, const uin
  *
  *   q          device bf16 [batch][num_q_heads][dim_qk]; num_q_heads = 128.
  *   kv         the single cache operand (num_kv_heads = 1).
- *   kv_len, max_kv_len, scale, sink, num_partitions, workspace,
- *   workspace_bytes, lse    as for attn_decode.
+ *   kv_len, max_kv_len, scale, sink, workspace_bytes, lse
+ *              as for attn_decode.
+ *   num_partitions  0 (the balanced split) or 1..MAX (P key slices per row),
+ *              from attn_plan_partitions or chosen.
+ *   workspace  as for attn_decode, sized by attn_plan_partitions for this P;
+ *              needed unless P == 1.
  *   out        device bf16 [batch][num_q_heads][dim_v].
+ *
+ * P >= 1: one two-CTA cluster per (key slice, row); slice p of a row is
+ * [p C, (p+1) C) as attn_plan_partitions states, then the split-K reduce.
+ * P == 0: a plan kernel (one CTA) writes the tile ranges of the clusters
+ * into the workspace, the decode grid (one wave of clusters, a dependent
+ * launch of the plan) walks them, a cluster writing the final rows of the
+ * rows its range holds whole and fp32 partials of the rows a range end
+ * cuts, and the reduce merges the latter (three launches).  kv_len above
+ * max_kv_len is then clamped to it and sets error bit 2, as a length above
+ * P C does for P >= 1.
  */
 int attn_mla_decode(const void *q, const attn_kv_t *kv, const uint32_t *kv_len, int batch,
                     int num_q_heads, int dim_qk, int dim_v, int max_kv_len, float scale,
@@ -225,11 +244,13 @@ int attn_mla_decode(const void *q, const attn_kv_t *kv, const uint32_t *kv_len, 
  *   out, lse   device bf16 [num_q_rows][num_q_heads][dim_v] / fp32
  *              [num_q_rows][num_q_heads] (lse may be NULL).
  *
- * Every row of a sequence runs over the same key slices (P and the
- * workspace come from attn_plan_partitions with num_q_rows rows), one
- * two-CTA cluster per (slice, row); clusters of the rows of a sequence are
- * launched next to each other so the second and later reads of a key tile
- * are served from L2.  num_q_rows <= 65535.  Returns as attn_mla_decode.
+ * P and the workspace come from attn_plan_partitions with num_q_rows rows.
+ * P >= 1: every row of a sequence runs over the same key slices, one
+ * two-CTA cluster per (slice, row), and clusters of the rows of a sequence
+ * are launched next to each other so the second and later reads of a key
+ * tile are served from L2.  P == 0: the balanced split over all rows' tiles
+ * (each row with its own causal length) as for attn_mla_decode.
+ * num_q_rows <= 65535.  Returns as attn_mla_decode.
  */
 int attn_mla_decode_rows(const void *q, const attn_kv_t *kv, const uint32_t *kv_len,
                          const uint32_t *q_row_offsets, int batch, int num_q_rows,

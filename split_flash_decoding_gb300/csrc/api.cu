@@ -99,6 +99,20 @@ size_t workspace_layout(int P, long long rows, int hq, int dv, size_t *off_m, si
     return o_bytes + 2 * m_bytes;
 }
 
+// Balanced MLA split: fp32 partials for clusters + rows slots, then the
+// plan tables (per cluster, per row, per row for the reduce).
+size_t mla_balanced_layout(int clusters, long long rows, size_t *off_m, size_t *off_l,
+                           size_t *off_plan) {
+    const size_t n = (size_t(clusters) + size_t(rows)) * size_t(kMlaHeads);
+    const size_t o_bytes = align256(n * size_t(kMlaDimV) * sizeof(float));
+    const size_t m_bytes = align256(n * sizeof(float));
+    if (off_m) *off_m = o_bytes;
+    if (off_l) *off_l = o_bytes + m_bytes;
+    if (off_plan) *off_plan = o_bytes + 2 * m_bytes;
+    return o_bytes + 2 * m_bytes + align256(size_t(clusters) * 16) + align256(size_t(rows) * 16) +
+           align256(size_t(rows) * 8);
+}
+
 int chunk_for(int max_kv_len, int P, int tile) {
     long long per = (static_cast<long long>(max_kv_len) + P - 1) / P;
     if (per < 1) per = 1;
@@ -300,6 +314,15 @@ extern "C" int attn_plan_partitions(int num_sms, int batch, int num_q_rows, int 
         if (p < 1) p = 1;
         if (p > ATTN_MAX_PARTITIONS) p = ATTN_MAX_PARTITIONS;
         P = static_cast<int>(p);
+        if (mla && P > 1) {
+            // MLA keys that need splitting at all take the balanced split over
+            // one wave of two-CTA clusters instead of P slices per row.
+            *num_partitions = 0;
+            *workspace_bytes = mla_balanced_layout(num_sms / 2 > 0 ? num_sms / 2 : 1,
+                                                   num_q_rows > 0 ? num_q_rows : 1, nullptr,
+                                                   nullptr, nullptr);
+            return ATTN_OK;
+        }
     }
     *num_partitions = P;
     const bool gqa = !(num_kv_heads == 1 && head_dim_v == kMlaDimV);
@@ -489,11 +512,18 @@ int mla_decode_impl(const void *q, const attn_kv_t *kv, const uint32_t *kv_len,
         max_kv_len < 0)
         return ATTN_ERR_INVALID_ARG;
     if (!q_row_offsets && num_q_rows != batch) return ATTN_ERR_INVALID_ARG;
-    if (num_partitions < 1 || num_partitions > ATTN_MAX_PARTITIONS) return ATTN_ERR_INVALID_ARG;
+    if (num_partitions < 0 || num_partitions > ATTN_MAX_PARTITIONS) return ATTN_ERR_INVALID_ARG;
     if (!(scale == scale)) return ATTN_ERR_INVALID_ARG;
     if (batch == 0 || num_q_rows == 0) return ATTN_OK;
     if (!q || !kv_len || !out) return ATTN_ERR_INVALID_ARG;
     if (num_q_heads != kMlaHeads || dim_qk != kMlaDimQK || dim_v != kMlaDimV)
+        return ATTN_ERR_UNSUPPORTED;
+    const bool balanced = num_partitions == 0;
+    if (num_partitions != 1 && !workspace) return ATTN_ERR_WORKSPACE;
+    // Balanced split: tile counts and starts are int (rows x tiles per row).
+    if (balanced &&
+        static_cast<long long>(num_q_rows) * ((static_cast<long long>(max_kv_len) + kMlaTileKeys - 1) /
+                                              kMlaTileKeys) >= (1LL << 31))
         return ATTN_ERR_UNSUPPORTED;
     if (num_q_rows > 65535) return ATTN_ERR_UNSUPPORTED;   // grid rows
     if (reinterpret_cast<uintptr_t>(out) % 16 || reinterpret_cast<uintptr_t>(q) % 16)
@@ -501,10 +531,20 @@ int mla_decode_impl(const void *q, const attn_kv_t *kv, const uint32_t *kv_len,
     if (reinterpret_cast<uintptr_t>(indices) % 4) return ATTN_ERR_INVALID_ARG;
     int st = sparse ? check_kv_rows(kv, dim_qk) : check_kv(kv, batch, dim_qk, max_kv_len);
     if (st) return st;
-    size_t off_m = 0, off_l = 0;
-    const size_t need = workspace_layout(num_partitions, num_q_rows, num_q_heads, dim_v, &off_m,
-                                         &off_l);
-    if (num_partitions > 1) {
+    size_t off_m = 0, off_l = 0, off_plan = 0;
+    int clusters = 0;
+    size_t need;
+    if (balanced) {
+        int dev = 0, sms = 0;
+        if (cudaGetDevice(&dev) != cudaSuccess ||
+            cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+            return ATTN_ERR_CUDA;
+        clusters = mla_cluster_slots(sms, sparse);
+        need = mla_balanced_layout(clusters, num_q_rows, &off_m, &off_l, &off_plan);
+    } else {
+        need = workspace_layout(num_partitions, num_q_rows, num_q_heads, dim_v, &off_m, &off_l);
+    }
+    if (num_partitions != 1) {
         if (!workspace || workspace_bytes < need) return ATTN_ERR_WORKSPACE;
         if (reinterpret_cast<uintptr_t>(workspace) % 256) return ATTN_ERR_WORKSPACE;
     }
@@ -530,11 +570,22 @@ int mla_decode_impl(const void *q, const attn_kv_t *kv, const uint32_t *kv_len,
     p.indices_stride = indices_stride;
     p.num_rows = static_cast<long long>(kv->num_pages) * kv->page_size;
     p.sink = sink;
-    if (num_partitions > 1) {
+    if (num_partitions != 1) {
         uint8_t *ws = static_cast<uint8_t *>(workspace);
         p.ws_o = reinterpret_cast<float *>(ws);
         p.ws_m = reinterpret_cast<float *>(ws + off_m);
         p.ws_l = reinterpret_cast<float *>(ws + off_l);
+    }
+    if (balanced) {
+        uint8_t *plan = static_cast<uint8_t *>(workspace) + off_plan;
+        p.plan_cluster = reinterpret_cast<int4 *>(plan);
+        plan += align256(size_t(clusters) * 16);
+        p.plan_rows = reinterpret_cast<int4 *>(plan);
+        plan += align256(size_t(num_q_rows) * 16);
+        p.plan_slots = reinterpret_cast<int2 *>(plan);
+        p.balanced = 1;
+        p.num_clusters = clusters;
+        p.len_cap = max_kv_len;
     }
     p.out = static_cast<uint16_t *>(out);
     p.lse = lse;
@@ -543,10 +594,14 @@ int mla_decode_impl(const void *q, const attn_kv_t *kv, const uint32_t *kv_len,
     p.page_size = kv->page_size;
     p.num_pages = kv->num_pages;
     p.num_partitions = num_partitions;
-    p.chunk = chunk_for(max_kv_len, num_partitions, kMlaTileKeys);
+    p.chunk = balanced ? kMlaTileKeys : chunk_for(max_kv_len, num_partitions, kMlaTileKeys);
     p.qk_scale_log2 = scale * 1.4426950408889634f;
 
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    if (balanced) {
+        st = map_cuda(launch_mla_plan(p, s));
+        if (st) return st;
+    }
     st = map_cuda(launch_mla_decode(p, s));
     if (st || num_partitions == 1) return st;
 
@@ -567,6 +622,12 @@ int mla_decode_impl(const void *q, const attn_kv_t *kv, const uint32_t *kv_len,
     r.dim_v = dim_v;
     r.chunk = p.chunk;
     r.len_cap = sparse ? indices_stride : 0;
+    if (balanced) {
+        r.slots = p.plan_slots;
+        r.kv_len = nullptr;
+        r.q_row_offsets = nullptr;
+        r.num_partitions = clusters;   // the most partials a row can have
+    }
     return map_cuda(launch_splitk_reduce(r, s, /*pdl=*/true));
 }
 

@@ -76,6 +76,15 @@ struct MlaParams {
     int box_rows;                 // tokens per TMA box (min(64, page size))
     int num_partitions, chunk;    // chunk: multiple of kMlaTileKeys
     float qk_scale_log2;
+    // Balanced split (num_partitions 0): cluster c takes tiles [x0, x1) of the
+    // concatenation of every query row's key tiles; the plan kernel writes
+    // the tables below into the workspace.  Partials go to slot c + row.
+    int balanced;
+    int num_clusters;
+    int len_cap;                  // kv_len above it is clamped (error bit 2)
+    int4 *plan_cluster;           // [num_clusters] {x0, x1, first row, 0}
+    int4 *plan_rows;              // [num_q_rows] {first tile, tiles, sequence, visible keys}
+    int2 *plan_slots;             // [num_q_rows] {first slot, partials} for the reduce
 };
 
 // Multi-row (prefill-shaped) tile kernel: 128 MMA rows = (128 / group)
@@ -113,11 +122,18 @@ struct ReduceParams {
     int num_partitions, rows, num_q_heads, dim_v;
     int chunk;                    // slice length when kv_len is given
     int len_cap;                  // > 0: kv_len is clamped to it as well as to P * chunk
+    // Balanced MLA split: row r's partials are slots e.x .. e.x + e.y - 1 of
+    // the workspace (e = slots[r]); e.y == 1 rows were finished by the
+    // decode kernel, e.y == 0 rows are empty.
+    const int2 *slots;
 };
 
 cudaError_t launch_gqa_decode(const GqaParams &p, cudaStream_t stream);
 cudaError_t launch_gqa_decode_tc(const GqaParams &p, cudaStream_t stream);
 cudaError_t launch_mla_decode(const MlaParams &p, cudaStream_t stream);
+cudaError_t launch_mla_plan(const MlaParams &p, cudaStream_t stream);
+// Two-CTA MLA clusters that run at once on num_sms SMs (at most num_sms / 2).
+int mla_cluster_slots(int num_sms, bool sparse);
 cudaError_t launch_tile_attention(const TileParams &p, cudaStream_t stream);
 cudaError_t launch_splitk_reduce(const ReduceParams &p, cudaStream_t stream, bool pdl);
 

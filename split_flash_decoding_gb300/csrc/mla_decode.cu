@@ -65,9 +65,9 @@ constexpr int kSoftmaxThreads = 256;   // warps 0-7
 
 // Warp roles.  Dense (paged or contiguous) caches: 352 threads, one TMA
 // producer warp (8), MMA warp 9, exchange warp 10.  Sparse top-k: 512 threads,
-// six cp.async producer warps (8-11, 14, 15), MMA warp 12, exchange warp 13;
-// the softmax warpgroups raise their register budget to 168 and the other
-// two lower theirs to 80 (256 x 168 + 256 x 80 <= 512 x 128 launched).
+// six TMA gather4 producer warps (8-11, 14, 15), MMA warp 12, exchange warp 13;
+// the softmax warpgroups raise their register budget to 152 and the other
+// two lower theirs to 104 (256 x 152 + 256 x 104 = 512 x 128 launched).
 template <bool kSparse>
 struct Layout {
     static constexpr int kThreads = kSparse ? 512 : 352;
@@ -129,23 +129,22 @@ __device__ __forceinline__ uint32_t x_half_off(int hf, int h, int c) {
     return uint32_t(hf) * kXHalfBytes + uint32_t(h * 128 + (((c + h) & 7) << 4));
 }
 
-template <bool kSparse>
-__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Layout<kSparse>::kThreads, 1)
-mla_decode_kernel(const __grid_constant__ MlaParams p) {
-    using Roles = Layout<kSparse>;
-    extern __shared__ uint8_t smem_raw[];
-    uint8_t *smem = reinterpret_cast<uint8_t *>(
-        (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-    uint64_t *bar = reinterpret_cast<uint64_t *>(smem + Smem::bars);
-    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + Smem::bars + kNumBars * 8);
+// One run of consecutive key tiles of one query row: keys [start, end) of
+// row qrow (sequence b).  direct: the run is the whole row, so the final
+// output is written; otherwise the partial goes to workspace slot ws.
+struct MlaSeg {
+    int qrow, b, start, end, ntiles, ws;
+    bool direct;
+};
 
-    const uint32_t rank = cluster_ctarank();
-    const uint32_t peer = rank ^ 1u;
+// Fixed split: key slice `part` of query row qrow of sequence b (one row per
+// sequence, or several given by row offsets, each with its own causal
+// limit).  Every row of a sequence uses the same key slices; a row that sees
+// none of a slice leaves an empty partial.  Returns false for a slice past
+// the sequence end (no work at all).
+template <bool kSparse>
+__device__ __forceinline__ bool fixed_slice(const MlaParams &p, MlaSeg &s, bool report) {
     const int part = blockIdx.x >> 1;
-    // Query row qrow of sequence b: one row per sequence, or several (draft
-    // tokens) given by row offsets, each with its own causal limit.  Every
-    // row of a sequence uses the same key slices; a row that sees none of a
-    // slice leaves an empty partial.
     const int qrow = blockIdx.y;
     int b = qrow, n_rows = 1, i_row = 0;
     if (p.q_row_offsets) {
@@ -159,25 +158,90 @@ mla_decode_kernel(const __grid_constant__ MlaParams p) {
         i_row = qrow - static_cast<int>(p.q_row_offsets[b]);
         n_rows = static_cast<int>(p.q_row_offsets[b + 1]) - static_cast<int>(p.q_row_offsets[b]);
     }
+    uint32_t cap = uint32_t(p.num_partitions) * uint32_t(p.chunk);
+    if (kSparse) cap = min(cap, uint32_t(p.indices_stride));   // keys a sequence can name
+    const uint32_t len_in = p.kv_len[b];
+    if (report && len_in > cap && part == 0) atomicOr(p.err, kErrBadLength);
+    const int L = static_cast<int>(min(len_in, cap));
+    const int start = part * p.chunk;
+    const int nslices = (L + p.chunk - 1) / p.chunk;
+    s.direct = nslices <= 1;
+    if (start >= L && !(s.direct && part == 0)) return false;
+    // keys j <= L - n + i for row i of n when causal
+    const int L_vis = p.causal ? max(0, min(L, L - n_rows + i_row + 1)) : L;
+    const int end = min(min(start + p.chunk, L), L_vis);
+    s.qrow = qrow;
+    s.b = b;
+    s.start = start;
+    s.end = end;
+    s.ntiles = start < end ? (end - start + kBN - 1) / kBN : 0;
+    s.ws = part * p.num_q_rows + qrow;
+    return true;
+}
+
+// The runs a cluster processes, in order.  Fixed split: the one key slice of
+// the cluster's grid position.  Balanced split: the rows that meet the
+// cluster's tile range [x0, x1) of the concatenated row tiles, read from the
+// plan one row ahead.  Every role walks the same list on its own.
+template <bool kSparse>
+struct SegWalk {
+    int r, x0, x1;   // fixed split: r = 1 while the slice is still to come
+    int4 nxt;        // plan entry of row r: {first tile, tiles, sequence, visible keys}
+
+    __device__ __forceinline__ bool next(const MlaParams &p, MlaSeg &s) {
+        if (!p.balanced) {
+            if (r == 0) return false;
+            r = 0;
+            return fixed_slice<kSparse>(p, s, false);
+        }
+        while (r < p.num_q_rows) {
+            const int4 e = nxt;
+            const int row = r++;
+            if (e.x >= x1) break;
+            if (r < p.num_q_rows) nxt = __ldcg(p.plan_rows + r);
+            const int tb = max(x0 - e.x, 0);
+            const int te = min(x1 - e.x, e.y);
+            if (tb >= te) continue;   // an empty row
+            s.qrow = row;
+            s.b = e.z;
+            s.start = tb * kBN;
+            s.end = min(te * kBN, e.w);
+            s.ntiles = te - tb;
+            s.direct = tb == 0 && te == e.y;
+            s.ws = static_cast<int>(blockIdx.x >> 1) + row;
+            return true;
+        }
+        r = p.num_q_rows;
+        return false;
+    }
+};
+
+template <bool kSparse>
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Layout<kSparse>::kThreads, 1)
+mla_decode_kernel(const __grid_constant__ MlaParams p) {
+    using Roles = Layout<kSparse>;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t *smem = reinterpret_cast<uint8_t *>(
+        (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    uint64_t *bar = reinterpret_cast<uint64_t *>(smem + Smem::bars);
+    uint32_t *tmem_slot = reinterpret_cast<uint32_t *>(smem + Smem::bars + kNumBars * 8);
+
+    const uint32_t rank = cluster_ctarank();
+    const uint32_t peer = rank ^ 1u;
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
     const int nbox = rank == 0 ? 4 : 5;
     const int col0 = rank == 0 ? 0 : 256;
 
-    uint32_t cap = uint32_t(p.num_partitions) * uint32_t(p.chunk);
-    if (kSparse) cap = min(cap, uint32_t(p.indices_stride));   // keys a sequence can name
-    const uint32_t len_in = p.kv_len[b];
-    if (len_in > cap && part == 0 && threadIdx.x == 0 && rank == 0)
-        atomicOr(p.err, kErrBadLength);
-    const int L = static_cast<int>(min(len_in, cap));
-    const int start = part * p.chunk;
-    const int nslices = (L + p.chunk - 1) / p.chunk;
-    const bool direct = nslices <= 1;
-    if (start >= L && !(direct && part == 0)) return;  // uniform over the cluster
-    // keys j <= L - n + i for row i of n when causal
-    const int L_vis = p.causal ? max(0, min(L, L - n_rows + i_row + 1)) : L;
-    const int end = min(min(start + p.chunk, L), L_vis);
-    const int ntiles = start < end ? (end - start + kBN - 1) / kBN : 0;
+    SegWalk<kSparse> walk;
+    walk.r = 1;
+    walk.x0 = walk.x1 = 0;
+    walk.nxt = make_int4(0, 0, 0, 0);
+    if (!p.balanced) {
+        MlaSeg s0;
+        if (!fixed_slice<kSparse>(p, s0, threadIdx.x == 0 && rank == 0))
+            return;   // uniform over the cluster
+    }
 
     if (threadIdx.x == 0) {
         for (int i = 0; i < kStages; ++i) {
@@ -206,54 +270,72 @@ mla_decode_kernel(const __grid_constant__ MlaParams p) {
     cluster_sync();  // both CTAs' barriers exist before any remote arrive
     tc::fence_after_sync();
     const uint32_t tmem = *tmem_slot;
+    if (p.balanced) {
+        // The plan kernel that precedes this grid wrote the tables.
+        pdl_wait_primary();
+        const int4 cl = __ldcg(p.plan_cluster + (blockIdx.x >> 1));   // {x0, x1, first row, 0}
+        walk.x0 = cl.x;
+        walk.x1 = cl.y;
+        walk.r = cl.z;
+        if (walk.r < p.num_q_rows) walk.nxt = __ldcg(p.plan_rows + walk.r);
+    }
 
     const int pidx = Roles::producer(warp);
     if (warp >= 8) {
-        if constexpr (kSparse) setmaxnreg_dec<80>();   // same instruction for both warpgroups
+        if constexpr (kSparse) setmaxnreg_dec<104>();   // same instruction for both warpgroups
         if (pidx >= 0) {
             // ------------------------------------------------------------ producer
+            // Tile i of the CTA's whole run list goes to stage i % kStages, so
+            // the ring runs on across the runs' boundaries.
+            SegWalk<kSparse> w = walk;
+            MlaSeg sg;
+            int issued = 0;   // tiles of every run so far
+            if (lane == 0) prefetch_tensormap(&p.kv_map);
             if constexpr (kSparse) {
-                if (ntiles > 0) {
-                    // Sparse top-k: key j of the sequence is cache row indices[b][j]
-                    // (rows at a uniform stride).  Rows are scattered, so a tile
-                    // arrives as gather4 copies (four rows x one 64-channel box,
-                    // 512 bytes, swizzled like a tiled load): 16 row groups x
-                    // nbox boxes per tile, spread over the six producer warps, one
-                    // copy per lane (warp w, lane l takes copy w + 6 l).  Each warp
-                    // posts the bytes of its own copies on the stage barrier, so
-                    // the stage is full when all six warps' copies have landed and
-                    // the producers run up to kStages tiles ahead, as for a dense
-                    // cache.  A key past the slice end, or an index outside the
-                    // cache (reported), reads row 0 in its place; the softmax
-                    // masks the former and the error word reports the latter.
-                    // The indices of tile i + 1 are loaded while tile i waits for
-                    // its stage.
-                    const int nq = 16 * nbox;
-                    const int q = pidx + Roles::kProducers * lane;
-                    const bool mine = q < nq;
-                    const int g = mine ? q / nbox : 0;        // rows 4g .. 4g + 3 of the tile
-                    const int cb = mine ? q - g * nbox : 0;   // 64-channel box
-                    const int32_t *idx = p.indices + size_t(b) * size_t(p.indices_stride);
+                // Sparse top-k: key j of the sequence is cache row indices[b][j]
+                // (rows at a uniform stride).  Rows are scattered, so a tile
+                // arrives as gather4 copies (four rows x one 64-channel box,
+                // 512 bytes, swizzled like a tiled load): 16 row groups x
+                // nbox boxes per tile, spread over the six producer warps, one
+                // copy per lane (warp w, lane l takes copy w + 6 l).  Each warp
+                // posts the bytes of its own copies on the stage barrier, so
+                // the stage is full when all six warps' copies have landed and
+                // the producers run up to kStages tiles ahead, as for a dense
+                // cache.  A key past the run end, or an index outside the
+                // cache (reported), reads row 0 in its place; the softmax
+                // masks the former and the error word reports the latter.
+                // The indices of tile i + 1 are loaded while tile i waits for
+                // its stage.
+                const int nq = 16 * nbox;
+                const int q = pidx + Roles::kProducers * lane;
+                const bool mine = q < nq;
+                const int g = mine ? q / nbox : 0;        // rows 4g .. 4g + 3 of the tile
+                const int cb = mine ? q - g * nbox : 0;   // 64-channel box
+                bool run = true;
+                while (run && w.next(p, sg)) {
+                    const int32_t *idx = p.indices + size_t(sg.b) * size_t(p.indices_stride);
                     auto load4 = [&](int tile, int (&r)[4]) {
 #pragma unroll
                         for (int u = 0; u < 4; ++u) {
-                            const int t = start + tile * kBN + 4 * g + u;
-                            r[u] = (mine && tile < ntiles && t < end) ? __ldg(idx + t) : 0;
+                            const int t = sg.start + tile * kBN + 4 * g + u;
+                            r[u] = (mine && tile < sg.ntiles && t < sg.end) ? __ldg(idx + t) : 0;
                         }
                     };
-                    if (lane == 0) prefetch_tensormap(&p.kv_map);
                     int cur[4], nxt[4];
                     load4(0, cur);
-                    int issued = 0;
-                    for (int i = 0; i < ntiles; ++i) {
+                    for (int i = 0; i < sg.ntiles; ++i) {
                         load4(i + 1, nxt);
-                        const int s = i % kStages;
+                        const int gi = issued;
+                        const int s = gi % kStages;
                         bool ok = true;
-                        if (lane == 0 && i >= kStages)
-                            ok = mbar_wait(&bar[kKvEmpty + s], ((i / kStages) - 1) & 1, p.err);
-                        if (!__shfl_sync(0xffffffffu, ok, 0)) break;
-                        const int t_g = start + i * kBN + 4 * g;
-                        const bool live = mine && t_g < end;
+                        if (lane == 0 && gi >= kStages)
+                            ok = mbar_wait(&bar[kKvEmpty + s], ((gi / kStages) - 1) & 1, p.err);
+                        if (!__shfl_sync(0xffffffffu, ok, 0)) {
+                            run = false;
+                            break;
+                        }
+                        const int t_g = sg.start + i * kBN + 4 * g;
+                        const bool live = mine && t_g < sg.end;
                         bool bad = false;
 #pragma unroll
                         for (int u = 0; u < 4; ++u) {
@@ -271,114 +353,112 @@ mla_decode_kernel(const __grid_constant__ MlaParams p) {
                                             g * 512,
                                         &p.kv_map, &bar[kKvFull + s], col0 + cb * 64, cur[0],
                                         cur[1], cur[2], cur[3]);
-                        issued = i + 1;
+                        issued = gi + 1;
 #pragma unroll
                         for (int u = 0; u < 4; ++u) cur[u] = nxt[u];
                     }
-                    // every copy this warp issued must land before the CTA may leave
-                    if (lane == 0) {
-                        for (int i = max(0, issued - kStages); i < issued; ++i)
-                            mbar_wait(&bar[kKvFull + i % kStages], (i / kStages) & 1, p.err);
-                    }
                 }
-            } else if (ntiles > 0) {
-                if (lane == 0) prefetch_tensormap(&p.kv_map);
+            } else {
                 const int box_rows = p.box_rows;
                 const int boxes_per_tile = kBN / box_rows;   // 1..8
                 bool aborted = false;
-                int issued = 0;
-                for (int base = 0; base < ntiles && !aborted; base += 32) {
-                    // lane i resolves the pages of tile base + i (up to 8 row boxes)
-                    int pg[8], sl[8];
-    #pragma unroll
-                    for (int r = 0; r < 8; ++r) { pg[r] = -1; sl[r] = 0; }
-                    const int my_tile = base + lane;
-                    if (my_tile < ntiles) {
-                        const int t0 = start + my_tile * kBN;
-    #pragma unroll
-                        for (int r = 0; r < 8; ++r) {
-                            const int t = t0 + r * box_rows;
-                            if (r >= boxes_per_tile || t >= L) continue;
-                            if (p.page_table) {
-                                const int pidx = t / p.page_size;
-                                int e = pidx < p.max_pages
-                                            ? p.page_table[size_t(b) * p.max_pages + pidx] : -1;
-                                if (e < 0 || e >= p.num_pages) {
-                                    atomicOr(p.err, kErrBadPage);
-                                    e = -1;
-                                }
-                                pg[r] = e;
-                                sl[r] = t % p.page_size;
-                            } else {
-                                pg[r] = b;
-                                sl[r] = t;
-                            }
-                        }
-                    }
-                    const int lim = min(base + 32, ntiles);
-                    for (int i = base; i < lim; ++i) {
-                        int pages[8], slots[8];
-    #pragma unroll
-                        for (int r = 0; r < 8; ++r) {
-                            pages[r] = __shfl_sync(0xffffffffu, pg[r], i - base);
-                            slots[r] = __shfl_sync(0xffffffffu, sl[r], i - base);
-                        }
-                        if (lane == 0) {
-                            const int s = i % kStages;
-                            if (i >= kStages &&
-                                !mbar_wait(&bar[kKvEmpty + s], ((i / kStages) - 1) & 1, p.err)) {
-                                aborted = true;
-                            } else {
-                                uint32_t nrow = 0;
-    #pragma unroll
-                                for (int r = 0; r < 8; ++r) nrow += pages[r] >= 0 ? 1u : 0u;
-                                mbar_arrive_expect_tx(&bar[kKvFull + s],
-                                                      nrow * uint32_t(nbox) * uint32_t(box_rows) * 128u);
-                                uint8_t *st = smem + Smem::kv + s * kStageBytes;
-    #pragma unroll
-                                for (int r = 0; r < 8; ++r) {
-                                    if (pages[r] < 0) continue;
-                                    for (int cb = 0; cb < nbox; ++cb)
-                                        tma_load_4d(st + cb * kKBoxBytes + r * box_rows * 128,
-                                                    &p.kv_map, &bar[kKvFull + s], col0 + cb * 64,
-                                                    slots[r], 0, pages[r]);
+                while (!aborted && w.next(p, sg)) {
+                    const int G = issued;
+                    for (int base = 0; base < sg.ntiles && !aborted; base += 32) {
+                        // lane i resolves the pages of tile base + i (up to 8 row boxes)
+                        int pg[8], sl[8];
+#pragma unroll
+                        for (int r = 0; r < 8; ++r) { pg[r] = -1; sl[r] = 0; }
+                        const int my_tile = base + lane;
+                        if (my_tile < sg.ntiles) {
+                            const int t0 = sg.start + my_tile * kBN;
+#pragma unroll
+                            for (int r = 0; r < 8; ++r) {
+                                const int t = t0 + r * box_rows;
+                                if (r >= boxes_per_tile || t >= sg.end) continue;
+                                if (p.page_table) {
+                                    const int pi = t / p.page_size;
+                                    int e = pi < p.max_pages
+                                                ? p.page_table[size_t(sg.b) * p.max_pages + pi] : -1;
+                                    if (e < 0 || e >= p.num_pages) {
+                                        atomicOr(p.err, kErrBadPage);
+                                        e = -1;
+                                    }
+                                    pg[r] = e;
+                                    sl[r] = t % p.page_size;
+                                } else {
+                                    pg[r] = sg.b;
+                                    sl[r] = t;
                                 }
                             }
                         }
-                        aborted = __shfl_sync(0xffffffffu, aborted, 0);
-                        if (aborted) break;
-                        issued = i + 1;
+                        const int lim = min(base + 32, sg.ntiles);
+                        for (int i = base; i < lim; ++i) {
+                            int pages[8], slots[8];
+#pragma unroll
+                            for (int r = 0; r < 8; ++r) {
+                                pages[r] = __shfl_sync(0xffffffffu, pg[r], i - base);
+                                slots[r] = __shfl_sync(0xffffffffu, sl[r], i - base);
+                            }
+                            const int gi = G + i;
+                            if (lane == 0) {
+                                const int s = gi % kStages;
+                                if (gi >= kStages &&
+                                    !mbar_wait(&bar[kKvEmpty + s], ((gi / kStages) - 1) & 1, p.err)) {
+                                    aborted = true;
+                                } else {
+                                    uint32_t nrow = 0;
+#pragma unroll
+                                    for (int r = 0; r < 8; ++r) nrow += pages[r] >= 0 ? 1u : 0u;
+                                    mbar_arrive_expect_tx(&bar[kKvFull + s],
+                                                          nrow * uint32_t(nbox) * uint32_t(box_rows) * 128u);
+                                    uint8_t *st = smem + Smem::kv + s * kStageBytes;
+#pragma unroll
+                                    for (int r = 0; r < 8; ++r) {
+                                        if (pages[r] < 0) continue;
+                                        for (int cb = 0; cb < nbox; ++cb)
+                                            tma_load_4d(st + cb * kKBoxBytes + r * box_rows * 128,
+                                                        &p.kv_map, &bar[kKvFull + s], col0 + cb * 64,
+                                                        slots[r], 0, pages[r]);
+                                    }
+                                }
+                            }
+                            aborted = __shfl_sync(0xffffffffu, aborted, 0);
+                            if (aborted) break;
+                            issued = gi + 1;
+                        }
                     }
                 }
-                // every copy this warp issued must land before the CTA may leave
-                if (lane == 0) {
-                    for (int i = max(0, issued - kStages); i < issued; ++i)
-                        mbar_wait(&bar[kKvFull + i % kStages], (i / kStages) & 1, p.err);
-                }
+            }
+            // every copy this warp issued must land before the CTA may leave
+            if (lane == 0) {
+                for (int i = max(0, issued - kStages); i < issued; ++i)
+                    mbar_wait(&bar[kKvFull + i % kStages], (i / kStages) & 1, p.err);
             }
         } else if (warp == Roles::kMmaWarp) {
             // ------------------------------------------------------------ MMA issue
-            if (ntiles > 0 && lane == 0) {
+            if (lane == 0) {
                 constexpr uint32_t idesc_s = tc::idesc_bf16_f32(128, kBN, 0, 0);
                 constexpr uint32_t idesc_o = tc::idesc_bf16_f32(128, 256, 0, 1);
                 const uint32_t kv_base = smem_addr(smem + Smem::kv);
-                // S(t) = Q K^T over this CTA's channels.  Descriptors advance by
-                // byte offset / 16 in their start field; the loops are unrolled so
-                // issue is not bound by descriptor arithmetic.
-                auto issue_s = [&](int t) -> bool {
-                    const int s = t % kStages;
-                    if (!mbar_wait(&bar[kKvFull + s], (t / kStages) & 1, p.err)) return false;
-                    if (t >= 1 && !mbar_wait(&bar[kSFree], (t - 1) & 1, p.err)) return false;
+                // S(g) = Q K^T over this CTA's channels for tile g of the run
+                // list.  Descriptors advance by byte offset / 16 in their start
+                // field; the loops are unrolled so issue is not bound by
+                // descriptor arithmetic.
+                auto issue_s = [&](int g) -> bool {
+                    const int s = g % kStages;
+                    if (!mbar_wait(&bar[kKvFull + s], (g / kStages) & 1, p.err)) return false;
+                    if (g >= 1 && !mbar_wait(&bar[kSFree], (g - 1) & 1, p.err)) return false;
                     tc::fence_after_sync();
                     const uint64_t b0 = tc::smem_desc_sw128(kv_base + s * kStageBytes, 16, 1024);
-    #pragma unroll
+#pragma unroll
                     for (int ks = 0; ks < 16; ++ks)
                         // A = Q from TMEM: 16 channels = 8 columns of bf16 pairs per step
                         tc::mma_bf16_tmem_a(tmem + kTmemS, tmem + kTmemQ + ks * 8,
                                             b0 + uint64_t(((ks >> 2) * kKBoxBytes + (ks & 3) * 32) >> 4),
                                             idesc_s, ks > 0);
                     if (nbox == 5) {
-    #pragma unroll
+#pragma unroll
                         for (int ks = 16; ks < 20; ++ks)
                             tc::mma_bf16_tmem_a(tmem + kTmemS, tmem + kTmemQ + ks * 8,
                                                 b0 + uint64_t((4 * kKBoxBytes + (ks & 3) * 32) >> 4),
@@ -387,53 +467,72 @@ mla_decode_kernel(const __grid_constant__ MlaParams p) {
                     tc::mma_commit(&bar[kSFull]);
                     return true;
                 };
-                bool ok = mbar_wait(&bar[kQFull], 0, p.err);
-                if (ok) ok = issue_s(0);
-                if (ok && ntiles > 1) ok = issue_s(1);
-                for (int t = 0; ok && t < ntiles; ++t) {
-                    if (t + 2 < ntiles && !(ok = issue_s(t + 2))) break;
-                    ok = mbar_wait(&bar[kPFull], t & 1, p.err);
-                    if (!ok) break;
-                    tc::fence_after_sync();
-                    const uint64_t v0 = tc::smem_desc_sw128(kv_base + (t % kStages) * kStageBytes,
-                                                            kVLbo, kVSbo);
-    #pragma unroll
-                    for (int kk = 0; kk < kBN / 16; ++kk)
-                        // A = P from TMEM: 16 keys = 8 columns of bf16 pairs per step
-                        tc::mma_bf16_tmem_a(tmem + kTmemO, tmem + kTmemP + kk * 8,
-                                            v0 + uint64_t((kk * 16 * 128) >> 4), idesc_o,
-                                            t > 0 || kk > 0);
-                    tc::mma_commit(&bar[kODone]);
-                    tc::mma_commit(&bar[kKvEmpty + (t % kStages)]);
+                SegWalk<kSparse> w = walk;
+                MlaSeg sg;
+                int G = 0, runs = 0;
+                bool ok = true;
+                while (ok && w.next(p, sg)) {
+                    const int n = sg.ntiles;
+                    if (n == 0) continue;
+                    // Q of this run is in TMEM (the softmax warps finished the last run)
+                    ok = mbar_wait(&bar[kQFull], runs & 1, p.err);
+                    ++runs;
+                    if (ok) ok = issue_s(G);
+                    if (ok && n > 1) ok = issue_s(G + 1);
+                    for (int t = 0; ok && t < n; ++t) {
+                        const int g = G + t;
+                        if (t + 2 < n && !(ok = issue_s(g + 2))) break;
+                        ok = mbar_wait(&bar[kPFull], g & 1, p.err);
+                        if (!ok) break;
+                        tc::fence_after_sync();
+                        const uint64_t v0 = tc::smem_desc_sw128(
+                            kv_base + (g % kStages) * kStageBytes, kVLbo, kVSbo);
+#pragma unroll
+                        for (int kk = 0; kk < kBN / 16; ++kk)
+                            // A = P from TMEM: 16 keys = 8 columns of bf16 pairs per step
+                            tc::mma_bf16_tmem_a(tmem + kTmemO, tmem + kTmemP + kk * 8,
+                                                v0 + uint64_t((kk * 16 * 128) >> 4), idesc_o,
+                                                t > 0 || kk > 0);
+                        tc::mma_commit(&bar[kODone]);
+                        tc::mma_commit(&bar[kKvEmpty + (g % kStages)]);
+                    }
+                    G += n;
                 }
             }
         } else if (warp == Roles::kXchgWarp) {
             // ------------------------------------------------------------ exchange
-            if (ntiles > 0 && lane == 0) {
+            if (lane == 0) {
                 const uint32_t dst = mapa_shared(smem_addr(smem + Smem::x_in), peer);
                 const uint32_t dst_bar = mapa_shared(smem_addr(&bar[kXFull]), peer);
                 const uint32_t src = smem_addr(smem + Smem::x_out);
                 // The two key halves go one after the other, so one half is
                 // staged while the other is on the wire.
+                SegWalk<kSparse> w = walk;
+                MlaSeg sg;
+                int G = 0;
                 bool run = true;
-                for (int t = 0; run && t < ntiles; ++t) {
-                    for (int hf = 0; hf < 2; ++hf) {
-                        if (!mbar_wait(&bar[kXoReady + hf], t & 1, p.err) ||
-                            (t >= 1 &&
-                             !mbar_wait_cluster(&bar[kXPeerFree + hf], (t - 1) & 1, p.err))) {
-                            run = false;
-                            break;
+                while (run && w.next(p, sg)) {
+                    for (int t = 0; run && t < sg.ntiles; ++t) {
+                        const int g = G + t;
+                        for (int hf = 0; hf < 2; ++hf) {
+                            if (!mbar_wait(&bar[kXoReady + hf], g & 1, p.err) ||
+                                (g >= 1 &&
+                                 !mbar_wait_cluster(&bar[kXPeerFree + hf], (g - 1) & 1, p.err))) {
+                                run = false;
+                                break;
+                            }
+                            bulk_copy_to_peer(dst + hf * kXHalfBytes, src + hf * kXHalfBytes,
+                                              kXHalfBytes, dst_bar + 8u * hf);
+                            bulk_wait_read();
+                            mbar_arrive(&bar[kXoFree + hf]);
                         }
-                        bulk_copy_to_peer(dst + hf * kXHalfBytes, src + hf * kXHalfBytes,
-                                          kXHalfBytes, dst_bar + 8u * hf);
-                        bulk_wait_read();
-                        mbar_arrive(&bar[kXoFree + hf]);
                     }
+                    G += sg.ntiles;
                 }
             }
         }
     } else {
-        if constexpr (kSparse) setmaxnreg_inc<168>();
+        if constexpr (kSparse) setmaxnreg_inc<152>();
         // ------------------------------------------------------------ softmax
         const int h = (warp & 3) * 32 + lane;    // head row == TMEM lane
         const int half = warp >> 2;              // keys [32 half, 32 half + 32)
@@ -443,269 +542,301 @@ mla_decode_kernel(const __grid_constant__ MlaParams p) {
         float *red = reinterpret_cast<float *>(smem + Smem::red);
         const uint32_t peer_xfree = mapa_shared(smem_addr(&bar[kXPeerFree + half]), peer);
         const uint32_t s_col = kTmemS + 32u * half;
-        float m_ref = -INFINITY;
-        float l = 0.f, l_r = 0.f;   // this half's share of the row sums
-        bool ok = ntiles > 0;
-        float s_own[32];
-        if (ok) {
-            // This CTA's Q channels of head row h into TMEM lane h: 64 channels
-            // (32 columns of bf16 pairs) per store, boxes split over the halves.
-            const uint4 *src = reinterpret_cast<const uint4 *>(
-                p.q + (size_t(qrow) * kMlaHeads + h) * kMlaDimQK + col0);
-            for (int cb = half; cb < nbox; cb += 2) {
-                float v[32];
-#pragma unroll
-                for (int i = 0; i < 8; ++i) {
-                    const uint4 w = src[cb * 8 + i];
-                    v[4 * i] = __uint_as_float(w.x);
-                    v[4 * i + 1] = __uint_as_float(w.y);
-                    v[4 * i + 2] = __uint_as_float(w.z);
-                    v[4 * i + 3] = __uint_as_float(w.w);
-                }
-                tc::tmem_st32(tmem + lane_base + kTmemQ + cb * 32, v);
+        SegWalk<kSparse> w = walk;
+        MlaSeg sg;
+        bool ok = true;   // no wait of this warp has failed
+        int G = 0;        // tiles of the runs before this one
+        while (w.next(p, sg)) {
+            const int ntiles = sg.ntiles;
+            const int start = sg.start, end = sg.end;
+            if (p.balanced && w.r < p.num_q_rows && w.nxt.x < w.x1) {
+                // The next run is row w.r: bring its Q lines of this CTA into
+                // L2 now, so the refill after this run reads them from there.
+                const uint8_t *qn = reinterpret_cast<const uint8_t *>(
+                    p.q + (size_t(w.r) * kMlaHeads + h) * kMlaDimQK + col0);
+                for (int cb = half; cb < nbox; cb += 2)
+                    asm volatile("prefetch.global.L2 [%0];" ::"l"(qn + cb * 128));
             }
-            tc::tmem_wait_st();
-            tc::fence_before_sync();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(&bar[kQFull]);
-
-            // Tile 0's partial: read this half and stage it for the copy.
-            ok = __all_sync(0xffffffffu, mbar_wait(&bar[kSFull], 0, p.err));
-            if (ok) {
-                tc::fence_after_sync();
-                tc::tmem_ld32(tmem + lane_base + s_col, s_own);
+            float m_ref = -INFINITY;
+            float l = 0.f, l_r = 0.f;   // this half's share of the row sums
+            bool live = ok && ntiles > 0;
+            float s_own[32];
+            if (live) {
+                // This CTA's Q channels of head row h into TMEM lane h: 64
+                // channels (32 columns of bf16 pairs) per store, boxes split
+                // over the halves.  The last run's MMAs have all finished.
+                const uint4 *src = reinterpret_cast<const uint4 *>(
+                    p.q + (size_t(sg.qrow) * kMlaHeads + h) * kMlaDimQK + col0);
+                for (int cb = half; cb < nbox; cb += 2) {
+                    float v[32];
+#pragma unroll
+                    for (int i = 0; i < 8; ++i) {
+                        const uint4 wq = src[cb * 8 + i];
+                        v[4 * i] = __uint_as_float(wq.x);
+                        v[4 * i + 1] = __uint_as_float(wq.y);
+                        v[4 * i + 2] = __uint_as_float(wq.z);
+                        v[4 * i + 3] = __uint_as_float(wq.w);
+                    }
+                    tc::tmem_st32(tmem + lane_base + kTmemQ + cb * 32, v);
+                }
+                tc::tmem_wait_st();
                 tc::fence_before_sync();
                 __syncwarp();
-                if (lane == 0) mbar_arrive(&bar[kSFree]);
-#pragma unroll
-                for (int c = 0; c < 8; ++c)
-                    *reinterpret_cast<float4 *>(x_out + x_half_off(half, h, c)) =
-                        make_float4(s_own[4 * c], s_own[4 * c + 1], s_own[4 * c + 2],
-                                    s_own[4 * c + 3]);
-                tc::fence_async_smem();   // generic writes -> the bulk copy engine
-                __syncwarp();
-                if (lane == 0) mbar_arrive(&bar[kXoReady + half]);
-            }
-        }
-        // The loop never breaks: every softmax warp reaches the named barriers
-        // of every tile; after a failed wait the remaining work is skipped.
-        for (int t = 0; t < ntiles; ++t) {
-            const int t0 = start + t * kBN;
-            const int nvalid = min(kBN, end - t0) - 32 * half;   // this half's valid keys
-            if (ok && h == 0) mbar_arrive_expect_tx(&bar[kXFull + half], kXHalfBytes);
+                if (lane == 0) mbar_arrive(&bar[kQFull]);
 
-            // ---- one tile ahead: partial S(t+1) out of TMEM, staged for the copy
-            float s_next[32];
-            const bool more = t + 1 < ntiles;
-            if (ok && more) {
-                ok = __all_sync(0xffffffffu, mbar_wait(&bar[kSFull], (t + 1) & 1, p.err));
-                if (ok) {
+                // The run's first partial: read this half and stage it for the
+                // copy once the copy of the last run's final tile has read x_out.
+                live = __all_sync(0xffffffffu, mbar_wait(&bar[kSFull], G & 1, p.err));
+                if (live) {
                     tc::fence_after_sync();
-                    tc::tmem_ld32(tmem + lane_base + s_col, s_next);
+                    tc::tmem_ld32(tmem + lane_base + s_col, s_own);
                     tc::fence_before_sync();
                     __syncwarp();
                     if (lane == 0) mbar_arrive(&bar[kSFree]);
-                    // copy(t) has read x_out
-                    ok = __all_sync(0xffffffffu, mbar_wait(&bar[kXoFree + half], t & 1, p.err));
+                    if (G >= 1)
+                        live = __all_sync(0xffffffffu,
+                                          mbar_wait(&bar[kXoFree + half], (G - 1) & 1, p.err));
                 }
-                if (ok) {
+                if (live) {
 #pragma unroll
                     for (int c = 0; c < 8; ++c)
                         *reinterpret_cast<float4 *>(x_out + x_half_off(half, h, c)) =
-                            make_float4(s_next[4 * c], s_next[4 * c + 1], s_next[4 * c + 2],
-                                        s_next[4 * c + 3]);
-                    tc::fence_async_smem();
+                            make_float4(s_own[4 * c], s_own[4 * c + 1], s_own[4 * c + 2],
+                                        s_own[4 * c + 3]);
+                    tc::fence_async_smem();   // generic writes -> the bulk copy engine
                     __syncwarp();
                     if (lane == 0) mbar_arrive(&bar[kXoReady + half]);
                 }
             }
+            // The loop never breaks: every softmax warp reaches the named
+            // barriers of every tile; after a failed wait the rest is skipped.
+            for (int t = 0; t < ntiles; ++t) {
+                const int g = G + t;   // tile of the CTA's run list
+                const int t0 = start + t * kBN;
+                const int nvalid = min(kBN, end - t0) - 32 * half;   // this half's valid keys
+                if (live && h == 0) mbar_arrive_expect_tx(&bar[kXFull + half], kXHalfBytes);
 
-            // ---- full S(t) = own partial + the peer's --------------------------
-            if (ok) ok = __all_sync(0xffffffffu, mbar_wait_cluster(&bar[kXFull + half], t & 1, p.err));
-            float mloc = -INFINITY;
-            if (ok) {
-#pragma unroll
-                for (int c = 0; c < 8; ++c) {
-                    const float4 o =
-                        *reinterpret_cast<const float4 *>(x_in + x_half_off(half, h, c));
-                    s_own[4 * c] += o.x;
-                    s_own[4 * c + 1] += o.y;
-                    s_own[4 * c + 2] += o.z;
-                    s_own[4 * c + 3] += o.w;
-                }
-                __syncwarp();   // the warp's reads of x_in happen before the release
-                // The values read from x_in are already consumed (added into
-                // s_own) when the arrive issues, so a relaxed arrive suffices.
-                if (lane == 0)
-                    asm volatile("mbarrier.arrive.relaxed.cluster.shared::cluster.b64 _, [%0];"
-                                 ::"r"(peer_xfree) : "memory");
-                if (nvalid >= 32) {
-#pragma unroll
-                    for (int j = 0; j < 32; ++j) {
-                        s_own[j] *= p.qk_scale_log2;
-                        mloc = fmaxf(mloc, s_own[j]);
+                // ---- one tile ahead: partial S(g+1) out of TMEM, staged for the copy
+                float s_next[32];
+                const bool more = t + 1 < ntiles;
+                if (live && more) {
+                    live = __all_sync(0xffffffffu, mbar_wait(&bar[kSFull], (g + 1) & 1, p.err));
+                    if (live) {
+                        tc::fence_after_sync();
+                        tc::tmem_ld32(tmem + lane_base + s_col, s_next);
+                        tc::fence_before_sync();
+                        __syncwarp();
+                        if (lane == 0) mbar_arrive(&bar[kSFree]);
+                        // copy(g) has read x_out
+                        live = __all_sync(0xffffffffu,
+                                          mbar_wait(&bar[kXoFree + half], g & 1, p.err));
                     }
+                    if (live) {
+#pragma unroll
+                        for (int c = 0; c < 8; ++c)
+                            *reinterpret_cast<float4 *>(x_out + x_half_off(half, h, c)) =
+                                make_float4(s_next[4 * c], s_next[4 * c + 1], s_next[4 * c + 2],
+                                            s_next[4 * c + 3]);
+                        tc::fence_async_smem();
+                        __syncwarp();
+                        if (lane == 0) mbar_arrive(&bar[kXoReady + half]);
+                    }
+                }
+
+                // ---- full S(g) = own partial + the peer's ------------------------
+                if (live)
+                    live = __all_sync(0xffffffffu,
+                                      mbar_wait_cluster(&bar[kXFull + half], g & 1, p.err));
+                float mloc = -INFINITY;
+                if (live) {
+#pragma unroll
+                    for (int c = 0; c < 8; ++c) {
+                        const float4 o =
+                            *reinterpret_cast<const float4 *>(x_in + x_half_off(half, h, c));
+                        s_own[4 * c] += o.x;
+                        s_own[4 * c + 1] += o.y;
+                        s_own[4 * c + 2] += o.z;
+                        s_own[4 * c + 3] += o.w;
+                    }
+                    __syncwarp();   // the warp's reads of x_in happen before the release
+                    // The values read from x_in are already consumed (added into
+                    // s_own) when the arrive issues, so a relaxed arrive suffices.
+                    if (lane == 0)
+                        asm volatile("mbarrier.arrive.relaxed.cluster.shared::cluster.b64 _, [%0];"
+                                     ::"r"(peer_xfree) : "memory");
+                    if (nvalid >= 32) {
+#pragma unroll
+                        for (int j = 0; j < 32; ++j) {
+                            s_own[j] *= p.qk_scale_log2;
+                            mloc = fmaxf(mloc, s_own[j]);
+                        }
+                    } else {
+#pragma unroll
+                        for (int j = 0; j < 32; ++j) {
+                            s_own[j] = j < nvalid ? s_own[j] * p.qk_scale_log2 : -INFINITY;
+                            mloc = fmaxf(mloc, s_own[j]);
+                        }
+                    }
+                }
+                // ---- row max over both halves --------------------------------
+                named_sync(kBarSoftmax, kSoftmaxThreads);   // the last reads of red are done
+                red[half * 128 + h] = mloc;
+                named_sync(kBarSoftmax, kSoftmaxThreads);
+                const float mt = fmaxf(mloc, red[(half ^ 1) * 128 + h]);
+
+                if (live) {
+                    // ---- online softmax in base 2, lazy max ----------------------
+                    const bool raise = mt > m_ref + kRescaleThreshold;   // always on the first tile
+                    float alpha = 1.f;
+                    if (raise) {
+                        alpha = fast_exp2(m_ref - mt);                  // 0 when m_ref = -inf
+                        m_ref = mt;
+                    }
+                    // Two row sums: of the fp32 weights (for lse) and of the bf16-
+                    // rounded weights the MMA multiplies V by (to normalise O).
+                    float rowsum = 0.f, rowsum_r = 0.f;
+                    float pk[16];
+#pragma unroll
+                    for (int j = 0; j < 16; ++j) {
+                        const float p0 = fast_exp2(s_own[2 * j] - m_ref);
+                        const float p1 = fast_exp2(s_own[2 * j + 1] - m_ref);
+                        const uint32_t wp = pack_bf16x2(p0, p1);
+                        pk[j] = __uint_as_float(wp);
+                        rowsum += p0 + p1;
+                        rowsum_r += bf16_lo(wp) + bf16_hi(wp);
+                    }
+                    l = l * alpha + rowsum;
+                    l_r = l_r * alpha + rowsum_r;
+
+                    // O(g-1) has read P(g-1) and must be finished before O is rescaled.
+                    if (t >= 1) {
+                        live = __all_sync(0xffffffffu,
+                                          mbar_wait(&bar[kODone], (g - 1) & 1, p.err));
+                        tc::fence_after_sync();
+                        if (live && __any_sync(0xffffffffu, raise)) {
+#pragma unroll 1
+                            for (int c = 0; c < 128; c += 32) {
+                                float v[32];
+                                const uint32_t oc = kTmemO + 128u * half + c;
+                                tc::tmem_ld32(tmem + lane_base + oc, v);
+#pragma unroll
+                                for (int j = 0; j < 32; ++j) v[j] *= alpha;
+                                tc::tmem_st32(tmem + lane_base + oc, v);
+                            }
+                        }
+                    }
+                    if (live) {
+                        float p8[8];
+#pragma unroll
+                        for (int j = 0; j < 8; ++j) p8[j] = pk[j];
+                        tc::tmem_st_n<8>(tmem + lane_base + kTmemP + 16u * half, p8);
+#pragma unroll
+                        for (int j = 0; j < 8; ++j) p8[j] = pk[8 + j];
+                        tc::tmem_st_n<8>(tmem + lane_base + kTmemP + 16u * half + 8, p8);
+                        const int nv = min(kBN, end - t0);
+                        if (nv < kBN) {
+                            // Rows past the run end may hold anything (even NaN):
+                            // zero them in the V part of the stage so 0 * V stays 0.
+                            uint8_t *st = smem + Smem::kv + (g % kStages) * kStageBytes;
+                            const int nz = (kBN - nv) * 4 * 8;   // 16-B chunks in 4 boxes
+                            for (int i = threadIdx.x; i < nz; i += kSoftmaxThreads) {
+                                const int box = i / ((kBN - nv) * 8);
+                                const int rem = i - box * ((kBN - nv) * 8);
+                                const int row = nv + rem / 8;
+                                const int ch = rem & 7;
+                                *reinterpret_cast<uint4 *>(st + box * kKBoxBytes + row * 128 +
+                                                           ch * 16) = make_uint4(0u, 0u, 0u, 0u);
+                            }
+                            tc::fence_async_smem();
+                        }
+                        tc::tmem_wait_st();
+                        tc::fence_before_sync();
+                        __syncwarp();
+                        if (lane == 0) mbar_arrive(&bar[kPFull]);   // one arrival per softmax warp
+                    }
+                }
+                if (more) {
+#pragma unroll
+                    for (int j = 0; j < 32; ++j) s_own[j] = s_next[j];
+                }
+            }
+
+            // ---- run epilogue ---------------------------------------------------
+            if (live) {
+                live = __all_sync(0xffffffffu,
+                                  mbar_wait(&bar[kODone], (G + ntiles - 1) & 1, p.err));
+                tc::fence_after_sync();
+            }
+            // Row sums of the two halves (same m_ref), one after the other
+            // through the row-max buffer.
+            named_sync(kBarSoftmax, kSoftmaxThreads);
+            red[half * 128 + h] = l;
+            named_sync(kBarSoftmax, kSoftmaxThreads);
+            const float l_other = red[(half ^ 1) * 128 + h];
+            named_sync(kBarSoftmax, kSoftmaxThreads);
+            red[half * 128 + h] = l_r;
+            named_sync(kBarSoftmax, kSoftmaxThreads);
+            l_r += red[(half ^ 1) * 128 + h];
+            l += l_other;
+            // O was accumulated with the rounded weights: normalise it by their
+            // sum (direct), or rescale it to the fp32 sum l kept for the merge.
+            float scale_o = 0.f, Mf = -INFINITY, Z = 0.f;
+            if (sg.direct) {
+                const float t2 = p.sink ? p.sink[h] * kLog2e : -INFINITY;
+                Mf = fmaxf(m_ref, t2);
+                float so = 0.f, Zr = 0.f;
+                if (Mf != -INFINITY) {
+                    so = fast_exp2(m_ref - Mf);
+                    const float st = fast_exp2(t2 - Mf);
+                    Z = l * so + st;
+                    Zr = l_r * so + st;
+                }
+                scale_o = Zr > 0.f ? so / Zr : 0.f;
+            } else {
+                scale_o = l_r > 0.f ? l / l_r : 0.f;
+            }
+            const size_t row = size_t(sg.qrow) * kMlaHeads + h;
+            const size_t wrow = size_t(sg.ws) * kMlaHeads + h;
+            const int ch0 = rank * 256 + half * 128;   // this warp's output channels
+#pragma unroll 1
+            for (int c = 0; c < 128; c += 32) {
+                float v[32];
+                if (live) {
+                    tc::tmem_ld32(tmem + lane_base + kTmemO + 128u * half + c, v);
                 } else {
 #pragma unroll
-                    for (int j = 0; j < 32; ++j) {
-                        s_own[j] = j < nvalid ? s_own[j] * p.qk_scale_log2 : -INFINITY;
-                        mloc = fmaxf(mloc, s_own[j]);
+                    for (int j = 0; j < 32; ++j) v[j] = 0.f;
+                }
+                if (sg.direct) {
+                    uint16_t *dst = p.out + row * kMlaDimV + ch0 + c;
+#pragma unroll
+                    for (int j = 0; j < 32; j += 8) {
+                        uint4 wv;
+                        wv.x = pack_bf16x2(v[j] * scale_o, v[j + 1] * scale_o);
+                        wv.y = pack_bf16x2(v[j + 2] * scale_o, v[j + 3] * scale_o);
+                        wv.z = pack_bf16x2(v[j + 4] * scale_o, v[j + 5] * scale_o);
+                        wv.w = pack_bf16x2(v[j + 6] * scale_o, v[j + 7] * scale_o);
+                        *reinterpret_cast<uint4 *>(dst + j) = wv;
                     }
+                } else {
+                    float *dst = p.ws_o + wrow * kMlaDimV + ch0 + c;
+#pragma unroll
+                    for (int j = 0; j < 32; j += 4)
+                        *reinterpret_cast<float4 *>(dst + j) =
+                            make_float4(v[j] * scale_o, v[j + 1] * scale_o, v[j + 2] * scale_o,
+                                        v[j + 3] * scale_o);
                 }
             }
-            // ---- row max over both halves ------------------------------------
-            named_sync(kBarSoftmax, kSoftmaxThreads);   // the last tile's reads are done
-            red[half * 128 + h] = mloc;
-            named_sync(kBarSoftmax, kSoftmaxThreads);
-            const float mt = fmaxf(mloc, red[(half ^ 1) * 128 + h]);
-
-            if (ok) {
-                // ---- online softmax in base 2, lazy max --------------------------
-                const bool raise = mt > m_ref + kRescaleThreshold;   // always on the first tile
-                float alpha = 1.f;
-                if (raise) {
-                    alpha = fast_exp2(m_ref - mt);                  // 0 when m_ref = -inf
-                    m_ref = mt;
-                }
-                // Two row sums: of the fp32 weights (for lse) and of the bf16-
-                // rounded weights the MMA multiplies V by (to normalise O).
-                float rowsum = 0.f, rowsum_r = 0.f;
-                float pk[16];
-#pragma unroll
-                for (int j = 0; j < 16; ++j) {
-                    const float p0 = fast_exp2(s_own[2 * j] - m_ref);
-                    const float p1 = fast_exp2(s_own[2 * j + 1] - m_ref);
-                    const uint32_t w = pack_bf16x2(p0, p1);
-                    pk[j] = __uint_as_float(w);
-                    rowsum += p0 + p1;
-                    rowsum_r += bf16_lo(w) + bf16_hi(w);
-                }
-                l = l * alpha + rowsum;
-                l_r = l_r * alpha + rowsum_r;
-
-                // O(t-1) has read P(t-1) and must be finished before O is rescaled.
-                if (t >= 1) {
-                    ok = __all_sync(0xffffffffu, mbar_wait(&bar[kODone], (t - 1) & 1, p.err));
-                    tc::fence_after_sync();
-                    if (ok && __any_sync(0xffffffffu, raise)) {
-#pragma unroll 1
-                        for (int c = 0; c < 128; c += 32) {
-                            float v[32];
-                            const uint32_t oc = kTmemO + 128u * half + c;
-                            tc::tmem_ld32(tmem + lane_base + oc, v);
-#pragma unroll
-                            for (int j = 0; j < 32; ++j) v[j] *= alpha;
-                            tc::tmem_st32(tmem + lane_base + oc, v);
-                        }
-                    }
-                }
-                if (ok) {
-                    float p8[8];
-#pragma unroll
-                    for (int j = 0; j < 8; ++j) p8[j] = pk[j];
-                    tc::tmem_st_n<8>(tmem + lane_base + kTmemP + 16u * half, p8);
-#pragma unroll
-                    for (int j = 0; j < 8; ++j) p8[j] = pk[8 + j];
-                    tc::tmem_st_n<8>(tmem + lane_base + kTmemP + 16u * half + 8, p8);
-                    const int nv = min(kBN, end - t0);
-                    if (nv < kBN) {
-                        // Rows past the sequence end may hold anything (even NaN):
-                        // zero them in the V part of the stage so 0 * V stays 0.
-                        uint8_t *st = smem + Smem::kv + (t % kStages) * kStageBytes;
-                        const int nz = (kBN - nv) * 4 * 8;   // 16-B chunks in 4 boxes
-                        for (int i = threadIdx.x; i < nz; i += kSoftmaxThreads) {
-                            const int box = i / ((kBN - nv) * 8);
-                            const int rem = i - box * ((kBN - nv) * 8);
-                            const int row = nv + rem / 8;
-                            const int ch = rem & 7;
-                            *reinterpret_cast<uint4 *>(st + box * kKBoxBytes + row * 128 +
-                                                       ch * 16) = make_uint4(0u, 0u, 0u, 0u);
-                        }
-                        tc::fence_async_smem();
-                    }
-                    tc::tmem_wait_st();
-                    tc::fence_before_sync();
-                    __syncwarp();
-                    if (lane == 0) mbar_arrive(&bar[kPFull]);   // one arrival per softmax warp
+            if (rank == 0 && half == 0) {
+                if (sg.direct) {
+                    if (p.lse) p.lse[row] = Z > 0.f ? (Mf + fast_log2(Z)) * kLn2 : -INFINITY;
+                } else {
+                    p.ws_m[wrow] = m_ref * kLn2;
+                    p.ws_l[wrow] = l;
                 }
             }
-            if (more) {
-#pragma unroll
-                for (int j = 0; j < 32; ++j) s_own[j] = s_next[j];
-            }
-        }
-
-        // ---- epilogue ---------------------------------------------------------
-        if (ok && ntiles > 0) {
-            ok = __all_sync(0xffffffffu, mbar_wait(&bar[kODone], (ntiles - 1) & 1, p.err));
-            tc::fence_after_sync();
-        }
-        // Row sums of the two halves (same m_ref): through shared memory in the
-        // K ring, which no MMA or copy touches any more.
-        float *sums = reinterpret_cast<float *>(smem + Smem::kv);
-        named_sync(kBarSoftmax, kSoftmaxThreads);
-        sums[half * 256 + h] = l;
-        sums[half * 256 + 128 + h] = l_r;
-        named_sync(kBarSoftmax, kSoftmaxThreads);
-        l += sums[(half ^ 1) * 256 + h];
-        l_r += sums[(half ^ 1) * 256 + 128 + h];
-        // O was accumulated with the rounded weights: normalise it by their
-        // sum (direct), or rescale it to the fp32 sum l kept for the merge.
-        float scale_o = 0.f, Mf = -INFINITY, Z = 0.f;
-        if (direct) {
-            const float t2 = p.sink ? p.sink[h] * kLog2e : -INFINITY;
-            Mf = fmaxf(m_ref, t2);
-            float so = 0.f, Zr = 0.f;
-            if (Mf != -INFINITY) {
-                so = fast_exp2(m_ref - Mf);
-                const float st = fast_exp2(t2 - Mf);
-                Z = l * so + st;
-                Zr = l_r * so + st;
-            }
-            scale_o = Zr > 0.f ? so / Zr : 0.f;
-        } else {
-            scale_o = l_r > 0.f ? l / l_r : 0.f;
-        }
-        const size_t row = size_t(qrow) * kMlaHeads + h;
-        const int ch0 = rank * 256 + half * 128;   // this warp's output channels
-#pragma unroll 1
-        for (int c = 0; c < 128; c += 32) {
-            float v[32];
-            if (ntiles > 0 && ok) {
-                tc::tmem_ld32(tmem + lane_base + kTmemO + 128u * half + c, v);
-            } else {
-#pragma unroll
-                for (int j = 0; j < 32; ++j) v[j] = 0.f;
-            }
-            if (direct) {
-                uint16_t *dst = p.out + row * kMlaDimV + ch0 + c;
-#pragma unroll
-                for (int j = 0; j < 32; j += 8) {
-                    uint4 w;
-                    w.x = pack_bf16x2(v[j] * scale_o, v[j + 1] * scale_o);
-                    w.y = pack_bf16x2(v[j + 2] * scale_o, v[j + 3] * scale_o);
-                    w.z = pack_bf16x2(v[j + 4] * scale_o, v[j + 5] * scale_o);
-                    w.w = pack_bf16x2(v[j + 6] * scale_o, v[j + 7] * scale_o);
-                    *reinterpret_cast<uint4 *>(dst + j) = w;
-                }
-            } else {
-                float *dst = p.ws_o + (size_t(part) * p.num_q_rows * kMlaHeads + row) * kMlaDimV +
-                             ch0 + c;
-#pragma unroll
-                for (int j = 0; j < 32; j += 4)
-                    *reinterpret_cast<float4 *>(dst + j) =
-                        make_float4(v[j] * scale_o, v[j + 1] * scale_o, v[j + 2] * scale_o,
-                                    v[j + 3] * scale_o);
-            }
-        }
-        if (rank == 0 && half == 0) {
-            if (direct) {
-                if (p.lse) p.lse[row] = Z > 0.f ? (Mf + fast_log2(Z)) * kLn2 : -INFINITY;
-            } else {
-                const size_t idx = size_t(part) * p.num_q_rows * kMlaHeads + row;
-                p.ws_m[idx] = m_ref * kLn2;
-                p.ws_l[idx] = l;
-            }
+            if (ntiles > 0) ok = live;
+            G += ntiles;
         }
         pdl_launch_dependents();
     }
@@ -719,21 +850,150 @@ mla_decode_kernel(const __grid_constant__ MlaParams p) {
     }
 }
 
+// Balanced split plan (one CTA, ahead of the decode grid).  Row r of the
+// concatenation has n_r = ceil(visible keys / 64) tiles starting at tile
+// cum_r; cluster c of C = min(clusters, T) takes tiles [c T / C, (c+1) T / C)
+// of the T in all, at least one each.
+// Pass 1 counts the tiles sequence by sequence (1024 at a time with a running
+// total) and writes each row's entry; pass 2 finds, for each row, the
+// clusters whose range starts in it and the slots of its partials: the
+// cluster holding tile x is ((x + 1) C - 1) / T, and cluster c writes row r's
+// partial to slot c + r, so a row's partials are consecutive.
+constexpr int kPlanThreads = 1024;
+
+__global__ void __launch_bounds__(kPlanThreads) mla_plan_kernel(const __grid_constant__ MlaParams p) {
+    pdl_launch_dependents();   // the decode CTAs may set up while this runs
+    __shared__ int warp_tot[kPlanThreads / 32];
+    const int tid = threadIdx.x, lane = tid & 31, wid = tid >> 5;
+    const int rows = p.num_q_rows;
+    for (int c = tid; c < p.num_clusters; c += kPlanThreads)
+        p.plan_cluster[c] = make_int4(0, 0, rows, 0);   // no rows unless found below
+    for (int r = tid; r < rows; r += kPlanThreads) p.plan_rows[r] = make_int4(0, 0, 0, 0);
+    __syncthreads();
+    const uint32_t cap = uint32_t(p.len_cap);
+    int carry = 0;
+    for (int b0 = 0; b0 < p.batch; b0 += kPlanThreads) {
+        const int b = b0 + tid;
+        int n_seq = 0, r0 = 0, nr = 0, L = 0;
+        if (b < p.batch) {
+            const uint32_t len_in = p.kv_len[b];
+            if (len_in > cap) atomicOr(p.err, kErrBadLength);
+            L = static_cast<int>(min(len_in, cap));
+            r0 = p.q_row_offsets ? static_cast<int>(p.q_row_offsets[b]) : b;
+            nr = p.q_row_offsets ? static_cast<int>(p.q_row_offsets[b + 1]) - r0 : 1;
+            nr = max(0, min(nr, rows - r0));   // rows outside [0, rows) are not written
+            if (r0 < 0) nr = 0;
+            for (int i = 0; i < nr; ++i) {
+                const int vis = p.causal ? max(0, min(L, L - nr + i + 1)) : L;
+                n_seq += (vis + kBN - 1) / kBN;
+            }
+        }
+        int incl = n_seq;   // inclusive scan over the block
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const int v = __shfl_up_sync(0xffffffffu, incl, o);
+            if (lane >= o) incl += v;
+        }
+        if (lane == 31) warp_tot[wid] = incl;
+        __syncthreads();
+        if (wid == 0) {
+            int v = warp_tot[lane];
+#pragma unroll
+            for (int o = 1; o < 32; o <<= 1) {
+                const int u = __shfl_up_sync(0xffffffffu, v, o);
+                if (lane >= o) v += u;
+            }
+            warp_tot[lane] = v;
+        }
+        __syncthreads();
+        int cum = carry + (wid > 0 ? warp_tot[wid - 1] : 0) + incl - n_seq;
+        carry += warp_tot[kPlanThreads / 32 - 1];
+        __syncthreads();   // warp_tot is rewritten by the next round
+        for (int i = 0; i < nr; ++i) {
+            const int vis = p.causal ? max(0, min(L, L - nr + i + 1)) : L;
+            const int n = (vis + kBN - 1) / kBN;
+            p.plan_rows[r0 + i] = make_int4(cum, n, b, vis);
+            cum += n;
+        }
+    }
+    __syncthreads();
+    // With fewer tiles than clusters only T clusters take part, so that every
+    // cluster between a row's first and last holds a piece of it (no gaps in
+    // the row's run of slots).
+    const long long T = carry;
+    const long long C = min(static_cast<long long>(p.num_clusters), T);
+    for (int r = tid; r < rows; r += kPlanThreads) {
+        const int4 e = __ldcg(p.plan_rows + r);
+        int2 slot = make_int2(0, 0);
+        if (e.y > 0) {
+            const long long first = e.x, last = static_cast<long long>(e.x) + e.y - 1;
+            const int cf = static_cast<int>(((first + 1) * C - 1) / T);
+            const int cl = static_cast<int>(((last + 1) * C - 1) / T);
+            slot = make_int2(cf + r, cl - cf + 1);
+            for (long long c = (first * C + T - 1) / T; c < C && c * T / C <= last; ++c)
+                p.plan_cluster[c] = make_int4(static_cast<int>(c * T / C),
+                                              static_cast<int>((c + 1) * T / C), r, 0);
+        }
+        p.plan_slots[r] = slot;
+    }
+}
+
 template <bool kSparse>
 cudaError_t launch_layout(const MlaParams &p, cudaStream_t stream) {
     cudaError_t e = cudaFuncSetAttribute(mla_decode_kernel<kSparse>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          int(kSmemBytes));
     if (e != cudaSuccess) return e;
-    dim3 grid(2 * p.num_partitions, p.num_q_rows);
-    mla_decode_kernel<kSparse><<<grid, Layout<kSparse>::kThreads, kSmemBytes, stream>>>(p);
-    return cudaGetLastError();
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = p.balanced ? dim3(2 * p.num_clusters, 1) : dim3(2 * p.num_partitions, p.num_q_rows);
+    cfg.blockDim = dim3(Layout<kSparse>::kThreads);
+    cfg.dynamicSmemBytes = kSmemBytes;
+    cfg.stream = stream;
+    // Balanced split: launched as a dependent of the plan kernel, so the
+    // CTAs set up (barriers, TMEM) while the plan is written.
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = p.balanced ? 1 : 0;
+    return cudaLaunchKernelEx(&cfg, mla_decode_kernel<kSparse>, p);
+}
+
+template <bool kSparse>
+int cluster_slots(int num_sms) {
+    static int cached = 0;
+    if (cached > 0) return cached;
+    int n = 0;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(2 * (num_sms / 2 > 0 ? num_sms / 2 : 1));
+    cfg.blockDim = dim3(Layout<kSparse>::kThreads);
+    cfg.dynamicSmemBytes = kSmemBytes;
+    if (cudaFuncSetAttribute(mla_decode_kernel<kSparse>,
+                             cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             int(kSmemBytes)) != cudaSuccess ||
+        cudaOccupancyMaxActiveClusters(&n, mla_decode_kernel<kSparse>, &cfg) != cudaSuccess ||
+        n <= 0) {
+        (void)cudaGetLastError();
+        n = num_sms / 2;
+    }
+    cached = n < num_sms / 2 ? n : num_sms / 2;
+    if (cached < 1) cached = 1;
+    return cached;
 }
 
 }  // namespace
 
 cudaError_t launch_mla_decode(const MlaParams &p, cudaStream_t stream) {
     return p.sparse ? launch_layout<true>(p, stream) : launch_layout<false>(p, stream);
+}
+
+cudaError_t launch_mla_plan(const MlaParams &p, cudaStream_t stream) {
+    mla_plan_kernel<<<1, kPlanThreads, 0, stream>>>(p);
+    return cudaGetLastError();
+}
+
+int mla_cluster_slots(int num_sms, bool sparse) {
+    return sparse ? cluster_slots<true>(num_sms) : cluster_slots<false>(num_sms);
 }
 
 }  // namespace attn

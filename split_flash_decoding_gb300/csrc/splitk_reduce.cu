@@ -51,7 +51,17 @@ splitk_reduce_kernel(const __grid_constant__ ReduceParams p) {
     const int h = static_cast<int>(item - static_cast<long long>(row) * p.num_q_heads);
 
     int P = p.num_partitions;
-    if (p.kv_len) {
+    size_t stride_p = static_cast<size_t>(p.rows) * p.num_q_heads;  // per partition
+    const size_t idx0 = static_cast<size_t>(row) * p.num_q_heads + h;  // out / lse
+    size_t widx0 = idx0;                                               // workspace
+    if (p.slots) {
+        // Balanced split: the row's partials sit in consecutive slots.
+        const int2 e = p.slots[row];
+        if (e.y == 1) return;   // finished by the decode kernel (uniform over the warp)
+        P = e.y;                // 0: an empty row, written below from the sink alone
+        stride_p = p.num_q_heads;
+        widx0 = static_cast<size_t>(e.x) * p.num_q_heads + h;
+    } else if (p.kv_len) {
         // Rows that fit in one slice were finished by the partition kernel.
         uint32_t cap = uint32_t(p.num_partitions) * uint32_t(p.chunk);
         if (p.len_cap > 0) cap = min(cap, uint32_t(p.len_cap));
@@ -60,16 +70,14 @@ splitk_reduce_kernel(const __grid_constant__ ReduceParams p) {
         if (ns < 2) return;  // uniform over the warp
         P = ns;
     }
-    const size_t stride_p = static_cast<size_t>(p.rows) * p.num_q_heads;  // per partition
-    const size_t idx0 = static_cast<size_t>(row) * p.num_q_heads + h;
 
     if (P <= kFastP) {
         // Few partitions: the O partials of the first channel block, m and l
         // are all requested at once (one round trip), and lane q's weight
         // reaches the other lanes by shuffle.
-        const float m_lane = lane < P ? p.ws_m[lane * stride_p + idx0] : -INFINITY;
-        const float l_lane = lane < P ? p.ws_l[lane * stride_p + idx0] : 0.f;
-        const float *src0 = p.ws_o + idx0 * p.dim_v + lane * 4;
+        const float m_lane = lane < P ? p.ws_m[lane * stride_p + widx0] : -INFINITY;
+        const float l_lane = lane < P ? p.ws_l[lane * stride_p + widx0] : 0.f;
+        const float *src0 = p.ws_o + widx0 * p.dim_v + lane * 4;
         const size_t step = stride_p * p.dim_v;
         float4 o[kFastP];
 #pragma unroll
@@ -107,7 +115,7 @@ splitk_reduce_kernel(const __grid_constant__ ReduceParams p) {
     }
 
     float mloc = -INFINITY;
-    for (int q = lane; q < P; q += 32) mloc = fmaxf(mloc, p.ws_m[q * stride_p + idx0]);
+    for (int q = lane; q < P; q += 32) mloc = fmaxf(mloc, p.ws_m[q * stride_p + widx0]);
     const float M = warp_max(mloc);
     const float t = p.sink ? p.sink[h] : -INFINITY;
     const float Mf = fmaxf(M, t);
@@ -117,11 +125,11 @@ splitk_reduce_kernel(const __grid_constant__ ReduceParams p) {
     const bool cached = P <= kMaxP / 4;
     float zloc = 0.f;
     for (int q = lane; q < P; q += 32) {
-        const float m = p.ws_m[q * stride_p + idx0];
+        const float m = p.ws_m[q * stride_p + widx0];
         float w = 0.f;
         if (m != -INFINITY) {
             w = fast_exp2((m - Mf) * kLog2e);
-            zloc += w * p.ws_l[q * stride_p + idx0];
+            zloc += w * p.ws_l[q * stride_p + widx0];
         }
         if (cached) w_s[warp][q] = w;
     }
@@ -132,14 +140,14 @@ splitk_reduce_kernel(const __grid_constant__ ReduceParams p) {
 
     for (int c = lane * 4; c < p.dim_v; c += 128) {
         float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-        const float *src = p.ws_o + idx0 * p.dim_v + c;
+        const float *src = p.ws_o + widx0 * p.dim_v + c;
 #pragma unroll 8
         for (int q = 0; q < P; ++q) {
             float w;
             if (cached) {
                 w = w_s[warp][q];
             } else {
-                const float m = p.ws_m[q * stride_p + idx0];
+                const float m = p.ws_m[q * stride_p + widx0];
                 w = m == -INFINITY ? 0.f : fast_exp2((m - Mf) * kLog2e);
             }
             if (w == 0.f) continue;
@@ -169,7 +177,16 @@ splitk_reduce_wide_kernel(const __grid_constant__ ReduceParams p) {
     const int h = blockIdx.x - row * p.num_q_heads;
 
     int P = p.num_partitions;
-    if (p.kv_len) {
+    size_t stride_p = static_cast<size_t>(p.rows) * p.num_q_heads;
+    const size_t idx0 = static_cast<size_t>(row) * p.num_q_heads + h;
+    size_t widx0 = idx0;
+    if (p.slots) {
+        const int2 e = p.slots[row];
+        if (e.y == 1) return;   // uniform over the CTA
+        P = e.y;
+        stride_p = p.num_q_heads;
+        widx0 = static_cast<size_t>(e.x) * p.num_q_heads + h;
+    } else if (p.kv_len) {
         uint32_t cap = uint32_t(p.num_partitions) * uint32_t(p.chunk);
         if (p.len_cap > 0) cap = min(cap, uint32_t(p.len_cap));
         const uint32_t L = min(p.kv_len[row_sequence(p, row)], cap);
@@ -177,11 +194,9 @@ splitk_reduce_wide_kernel(const __grid_constant__ ReduceParams p) {
         if (ns < 2) return;  // uniform over the CTA
         P = ns;
     }
-    const size_t stride_p = static_cast<size_t>(p.rows) * p.num_q_heads;
-    const size_t idx0 = static_cast<size_t>(row) * p.num_q_heads + h;
 
     float mloc = -INFINITY;
-    for (int q = tid; q < P; q += kWarps * 32) mloc = fmaxf(mloc, p.ws_m[q * stride_p + idx0]);
+    for (int q = tid; q < P; q += kWarps * 32) mloc = fmaxf(mloc, p.ws_m[q * stride_p + widx0]);
     mloc = warp_max(mloc);
     if (lane == 0) red[warp] = mloc;
     __syncthreads();
@@ -194,11 +209,11 @@ splitk_reduce_wide_kernel(const __grid_constant__ ReduceParams p) {
 
     float zloc = 0.f;
     for (int q = tid; q < P; q += kWarps * 32) {
-        const float m = p.ws_m[q * stride_p + idx0];
+        const float m = p.ws_m[q * stride_p + widx0];
         float w = 0.f;
         if (m != -INFINITY) {
             w = fast_exp2((m - Mf) * kLog2e);
-            zloc += w * p.ws_l[q * stride_p + idx0];
+            zloc += w * p.ws_l[q * stride_p + widx0];
         }
         w_s[q] = w;
     }
@@ -215,7 +230,7 @@ splitk_reduce_wide_kernel(const __grid_constant__ ReduceParams p) {
         const int c = c0 + lane * 4;
         float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
         if (c < p.dim_v) {
-            const float *src = p.ws_o + idx0 * p.dim_v + c;
+            const float *src = p.ws_o + widx0 * p.dim_v + c;
 #pragma unroll 4
             for (int q = warp; q < P; q += kWarps) {
                 const float w = w_s[q];

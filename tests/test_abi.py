@@ -151,7 +151,10 @@ def test_sparse_mla_rejects_bad_arguments_before_launch(attn):
     assert call_sparse(attn, stride=-1) == E.ATTN_ERR_INVALID_ARG
     assert call_sparse(attn, hq=64) == E.ATTN_ERR_UNSUPPORTED
     assert call_sparse(attn, dqk=512) == E.ATTN_ERR_UNSUPPORTED
-    assert call_sparse(attn, P=0) == E.ATTN_ERR_INVALID_ARG
+    assert call_sparse(attn, P=-1) == E.ATTN_ERR_INVALID_ARG
+    assert call_sparse(attn, P=1025) == E.ATTN_ERR_INVALID_ARG
+    # P = 0 (the balanced split) needs a workspace
+    assert call_sparse(attn, P=0) == E.ATTN_ERR_WORKSPACE
     assert call_sparse(attn, scale=float("nan")) == E.ATTN_ERR_INVALID_ARG
     # the indices replace the page table; row strides keep the 16-byte rule
     assert call_sparse(attn, k=kv(attn, **dict(rows, page_table=0x20000))) \
@@ -225,23 +228,25 @@ def test_planner_formulas(attn):
     assert P == 19 and 8 * P == 152
     P, _ = attn.attn_plan_partitions(1, 1, 16, 8, 64, 131072, 0, num_sms=152)
     assert P == 38 and 8 * P == 2 * 152
-    # automatic MLA (one KV head, 512 output channels): one cluster per SM
-    # pair; slices of ~4096 keys, at least one cluster's worth when the
-    # batch is small
-    P, _ = attn.attn_plan_partitions(32, 32, 128, 1, 512, 32768, 0, num_sms=152)
-    assert P == 8
-    P, _ = attn.attn_plan_partitions(1, 1, 128, 1, 512, 131072, 0, num_sms=152)
-    assert P == 76
-    # short (sparse top-k) spans: as many slices as one wave of 76 clusters holds
-    P, _ = attn.attn_plan_partitions(32, 32, 128, 1, 512, 2048, 0, num_sms=152)
-    assert P == 2
-    P, _ = attn.attn_plan_partitions(128, 128, 128, 1, 512, 2048, 0, num_sms=152)
-    assert P == 1
-    # MLA with several query rows per sequence: one cluster per (slice, row)
-    P, _ = attn.attn_plan_partitions(4, 8, 128, 1, 512, 2048, 0, num_sms=152)
-    assert P == 9
-    P, _ = attn.attn_plan_partitions(32, 64, 128, 1, 512, 32768, 0, num_sms=152)
-    assert P == 4                                     # slices of 8192 keys for 2 rows
+    # automatic MLA (one KV head, 512 output channels): keys that need a
+    # split at all take the balanced split (P = 0) over one wave of
+    # num_sms / 2 two-CTA clusters; fp32 partials for clusters + rows slots,
+    # then the plan tables
+    align = lambda x: (x + 255) // 256 * 256
+    for sms, batch, rows, max_len in ((152, 32, 32, 32768), (152, 1, 1, 131072),
+                                      (152, 4, 8, 2048), (16, 8, 8, 9000)):
+        P, ws = attn.attn_plan_partitions(batch, rows, 128, 1, 512, max_len, 0, num_sms=sms)
+        slots = sms // 2 + rows
+        assert P == 0
+        assert ws == (align(slots * 128 * 512 * 4) + 2 * align(slots * 128 * 4) +
+                      align(sms // 2 * 16) + align(rows * 16) + align(rows * 8))
+    # a wave of clusters or more with rows of <= ~4096 keys (a sparse top-k
+    # span of 2048), or a single tile per row: no split at all
+    assert attn.attn_plan_partitions(128, 128, 128, 1, 512, 2048, 0, num_sms=152) == (1, 0)
+    assert attn.attn_plan_partitions(32, 64, 128, 1, 512, 64, 0, num_sms=16) == (1, 0)
+    # an explicit MLA request is a fixed split into P slices per row
+    P, ws = attn.attn_plan_partitions(32, 64, 128, 1, 512, 32768, 4, num_sms=152)
+    assert P == 4 and ws == align(4 * 64 * 128 * 512 * 4) + 2 * align(4 * 64 * 128 * 4)
     P, _ = attn.attn_plan_partitions(1, 1, 32, 8, 128, 20, 0, num_sms=152)
     assert P == 1                                     # one tile of keys cannot split
     # a few query rows per sequence (the 16-column fold): long items

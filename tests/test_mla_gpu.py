@@ -38,7 +38,7 @@ def run(attn, w, P=0, sink="workload"):
     return out, lse
 
 
-@pytest.mark.parametrize("P", [1, 2, 5])
+@pytest.mark.parametrize("P", [0, 1, 2, 5])
 def test_mla_small_matches_oracle(attn, P):
     w = mla_workload([1, 63, 64, 65, 700], seed=21)
     out, lse = run(attn, w, P)
@@ -61,7 +61,7 @@ def test_mla_paged_equals_contiguous_bitwise(attn, page_size):
 def test_mla_sinks_and_empty(attn):
     w = mla_workload([0, 300, 2000], seed=23, sink=True)
     no_sink = torch.full((128,), -math.inf, dtype=torch.float32, device=DEV)
-    for P in (1, 4):
+    for P in (0, 1, 4):
         out, lse = run(attn, w, P)
         ref_o, ref_l = oracle_result(w)
         assert_close(out, lse, ref_o, ref_l, f"mla sinks P={P}")

@@ -41,7 +41,7 @@ def run(attn, w, P=0, sink="workload"):
     return out, lse
 
 
-@pytest.mark.parametrize("P", [1, 2, 5])
+@pytest.mark.parametrize("P", [0, 1, 2, 5])
 def test_mla_rows_small_matches_oracle(attn, P):
     # rows per sequence 1..4; short sequences leave early rows with no key
     w = rows_workload([1, 2, 63, 64, 65, 700, 3], [4, 2, 3, 1, 2, 4, 4], seed=41)
@@ -60,7 +60,7 @@ def test_mla_rows_non_causal(attn):
 
 def test_one_row_per_sequence_equals_single_token_call_bitwise(attn):
     w = rows_workload([5, 130, 1000, 4096], [1, 1, 1, 1], seed=43)
-    for P in (1, 3):
+    for P in (0, 1, 3):
         o1, l1 = run(attn, w, P)
         o2, l2 = attn.attn_mla_decode(w.q, w.k_cache, w.kv_len, scale=w.scale,
                                       max_kv_len=w.max_kv_len, page_table=w.page_table,
@@ -82,7 +82,7 @@ def test_mla_rows_paged_equals_contiguous_bitwise(attn, page_size):
 def test_mla_rows_sinks_and_empty(attn):
     w = rows_workload([0, 300, 2], [2, 3, 4], seed=45, sink=True)
     no_sink = torch.full((128,), -math.inf, dtype=torch.float32, device=DEV)
-    for P in (1, 4):
+    for P in (0, 1, 4):
         out, lse = run(attn, w, P)
         ref_o, ref_l = oracle_result(w)
         assert_close(out, lse, ref_o, ref_l, f"mla rows sinks P={P}")

@@ -40,7 +40,7 @@ def run(attn, w, P=0, sink="workload", cache=None, indices=None, topk=None):
     return out, lse
 
 
-@pytest.mark.parametrize("P", [1, 2, 5])
+@pytest.mark.parametrize("P", [0, 1, 2, 5])
 def test_sparse_small_matches_oracle(attn, P):
     w = sparse_workload([1, 70, 700, 3000, 64, 301], topk=300, seed=31)
     out, lse = run(attn, w, P)
@@ -52,7 +52,7 @@ def test_sparse_repeated_rows(attn):
     """Rows drawn with repetition: a row named twice counts twice."""
     w = sparse_workload([50, 400, 2000], topk=513, seed=32, replace_rows=True)
     assert any(len(set(w.indices[b, :n].tolist())) < n for b, n in enumerate(w.kv_len_host))
-    for P in (1, 3):
+    for P in (0, 1, 3):
         out, lse = run(attn, w, P)
         ref_o, ref_l = oracle_result(w)
         assert_close(out, lse, ref_o, ref_l, f"sparse repeated P={P}")
@@ -63,7 +63,7 @@ def test_sparse_row_mapping_is_layout_independent_bitwise(attn):
     so the results agree bit for bit."""
     w = sparse_workload([900, 2500, 130], topk=640, seed=33)
     n, ps = w.k_cache.shape[:2]
-    for P in (1, 4):
+    for P in (0, 1, 4):
         o64, l64 = run(attn, w, P)
         for new_ps in (16, 1):
             view = w.k_cache.view(n * ps // new_ps, new_ps, 1, 576)
@@ -85,7 +85,7 @@ def test_sparse_identity_indices_equal_dense_paged_bitwise(attn):
         t = torch.arange(L)
         idx[b, :L] = pt[b, t // 64] * 64 + t % 64
     idx = idx.to(torch.int32).to(DEV)
-    for P in (1, 3):
+    for P in (0, 1, 3):
         od, ld = attn.attn_mla_decode(w.q, w.k_cache, w.kv_len, scale=w.scale,
                                       max_kv_len=max(lens), page_table=w.page_table,
                                       num_partitions=P)
@@ -99,7 +99,7 @@ def test_sparse_sinks_and_empty(attn):
     w = sparse_workload([0, 300, 2000, 7], topk=1024, seed=35, sink=True)
     assert w.kv_len_host[0] == 0
     no_sink = torch.full((128,), -math.inf, dtype=torch.float32, device=DEV)
-    for P in (1, 4):
+    for P in (0, 1, 4):
         out, lse = run(attn, w, P)
         ref_o, ref_l = oracle_result(w)
         assert_close(out, lse, ref_o, ref_l, f"sparse sinks P={P}")
