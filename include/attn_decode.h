@@ -116,8 +116,9 @@ typedef struct attn_kv {
  * automatic choice treats num_kv_heads == 1 with head_dim_v == 512 as the
  * MLA shape and everything else as GQA.  GQA with head_dim 128 and more
  * query rows than sequences (the few-row fold): P = 1 when there are at
- * least 2 (sequence, KV head) units per SM, P = 2 when there are at least
- * num_sms / 2.  MLA: with
+ * least 2 (sequence, KV head) units per SM, else the many-unit rule (at
+ * least four items per CTA at full length and slices of at most ~1024
+ * keys) whatever the unit count.  MLA: with
  * P' = max(floor(num_sms / 2 / num_q_rows), ceil(max_kv_len / (4096 n))),
  * n = ceil(num_q_rows / batch) query rows per sequence, capped at
  * ceil(max_kv_len / 64), the plan is P = 1 (no split) when P' <= 1 and

@@ -289,14 +289,15 @@ extern "C" int attn_plan_partitions(int num_sms, int batch, int num_q_rows, int 
             const long long p_fill = ctas / units > 0 ? ctas / units : 1;
             const long long p_len = (static_cast<long long>(max_kv_len) + target - 1) / target;
             p = p_fill > p_len ? p_fill : p_len;
-        } else if (tc && num_q_rows > batch && units >= ctas / 2) {
+        } else if (tc && num_q_rows > batch && units >= 2 * ctas) {
             // A few query rows per sequence fold onto 16 score columns.  With
-            // enough units the split buys little (the memory streams are
-            // already spread over every SM) and costs a workspace and a
-            // reduce: one slice per unit when there are two units per CTA
-            // or more, else two slices merged on chip by a CTA pair.
-            p = units >= 2 * ctas ? 1 : 2;
-        } else if (units < ctas) {
+            // two units per CTA or more the split buys little (the memory
+            // streams are already spread over every SM) and costs a
+            // workspace and a reduce: one slice per unit.  With fewer units
+            // the folded items are long, and the many-item rule below (not
+            // one wave of slices) keeps a ragged batch balanced.
+            p = 1;
+        } else if (units < ctas && !(tc && num_q_rows > batch)) {
             p = (ctas + units - 1) / units;
         } else {
             const long long p_fill = (4 * ctas + units - 1) / units;

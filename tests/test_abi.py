@@ -253,7 +253,9 @@ def test_planner_formulas(attn):
     P, _ = attn.attn_plan_partitions(64, 160, 32, 8, 128, 8192, 0, num_sms=152)
     assert P == 1                                     # 512 units, >= 2 per CTA
     P, ws = attn.attn_plan_partitions(16, 40, 32, 8, 128, 8192, 0, num_sms=152)
-    assert P == 2 and ws == 0                         # 128 units: a pair merged on chip
+    assert P == 8 and ws > 0                          # 128 units: slices of <= 1024 keys
+    P, _ = attn.attn_plan_partitions(2, 8, 32, 8, 128, 8192, 0, num_sms=152)
+    assert P == 38                                    # 16 units: >= 4 items per CTA
     P, _ = attn.attn_plan_partitions(4, 4, 32, 8, 128, 0, 0, num_sms=152)
     assert P == 1
     # every CTA gets at least one slice of a full-length batch
