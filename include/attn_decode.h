@@ -56,6 +56,8 @@ enum {
 
 /* Largest split-K partition count accepted by every entry point. */
 #define ATTN_MAX_PARTITIONS 1024
+/* attn_plan_partitions request: the balanced MLA split (num_partitions 0) */
+#define ATTN_PARTITIONS_BALANCED (-1)
 
 /*
  * One K or V cache operand (the KV operand type carries the element type and
@@ -102,8 +104,11 @@ typedef struct attn_kv {
  *   num_q_heads, num_kv_heads   heads (num_kv_heads = 1 for MLA).
  *   head_dim_v    output channels (128 for GQA d128, 512 for MLA).
  *   max_kv_len    host upper bound of every kv_len[b].
- *   requested     0 = automatic; > 0 = use exactly this many partitions.
- *   num_partitions  out: partitions P (1 <= P <= ATTN_MAX_PARTITIONS).
+ *   requested     0 = automatic; > 0 = use exactly this many partitions;
+ *                 ATTN_PARTITIONS_BALANCED = the balanced split (MLA shapes
+ *                 only: num_kv_heads 1, head_dim_v 512; num_partitions out 0).
+ *   num_partitions  out: partitions P (1 <= P <= ATTN_MAX_PARTITIONS), or 0
+ *                 for the balanced MLA split.
  *   workspace_bytes out: workspace size attn_decode / attn_mla_decode need
  *                 for this P (0 when P == 1).
  *

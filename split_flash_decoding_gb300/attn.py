@@ -25,6 +25,7 @@ ATTN_ERR_WORKSPACE = 3
 ATTN_ERR_CUDA = 4
 ATTN_ERR_DEVICE = 5
 ATTN_MAX_PARTITIONS = 1024
+ATTN_PARTITIONS_BALANCED = -1   # the balanced MLA split (planner request; num_partitions 0)
 
 _STATUS_NAMES = {
     ATTN_ERR_INVALID_ARG: "ATTN_ERR_INVALID_ARG",
@@ -232,7 +233,10 @@ def attn_mla_decode(q: torch.Tensor, kv_cache: torch.Tensor, kv_len: torch.Tenso
                     workspace: Optional[torch.Tensor] = None, out: Optional[torch.Tensor] = None,
                     lse: Optional[torch.Tensor] = None, return_lse: bool = True, stream=None):
     """MLA decode through attn_mla_decode: q bf16 [batch, num_q_heads, 576],
-    one-head cache [pages, page_size, 1, 576]; V = K[..., :dim_v]."""
+    one-head cache [pages, page_size, 1, 576]; V = K[..., :dim_v].
+    num_partitions: 0 = the planner's choice, > 0 = that many key slices per
+    row, ATTN_PARTITIONS_BALANCED = the balanced split (as for the _rows and
+    _sparse variants)."""
     batch, hq, dqk = q.shape
     if out is None:
         out = torch.empty((batch, hq, dim_v), dtype=torch.bfloat16, device=q.device)

@@ -245,19 +245,27 @@ extern "C" int attn_plan_partitions(int num_sms, int batch, int num_q_rows, int 
                                     size_t *workspace_bytes) {
     if (!num_partitions || !workspace_bytes) return ATTN_ERR_INVALID_ARG;
     if (batch < 0 || num_q_rows < 0 || num_q_heads <= 0 || num_kv_heads <= 0 ||
-        head_dim_v <= 0 || max_kv_len < 0 || requested < 0)
+        head_dim_v <= 0 || max_kv_len < 0 || requested < ATTN_PARTITIONS_BALANCED)
         return ATTN_ERR_INVALID_ARG;
     if (num_q_heads % num_kv_heads) return ATTN_ERR_INVALID_ARG;
     if (requested > ATTN_MAX_PARTITIONS) return ATTN_ERR_INVALID_ARG;
+    const bool mla_shape = num_kv_heads == 1 && head_dim_v == kMlaDimV;
+    if (requested == ATTN_PARTITIONS_BALANCED && !mla_shape) return ATTN_ERR_INVALID_ARG;
+    if (requested <= 0 && num_sms <= 0) {
+        int dev = 0;
+        if (cudaGetDevice(&dev) != cudaSuccess ||
+            cudaDeviceGetAttribute(&num_sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+            return ATTN_ERR_CUDA;
+    }
+    if (requested == ATTN_PARTITIONS_BALANCED) {
+        *num_partitions = 0;
+        *workspace_bytes = mla_balanced_layout(num_sms / 2 > 0 ? num_sms / 2 : 1,
+                                               num_q_rows > 0 ? num_q_rows : 1, nullptr, nullptr,
+                                               nullptr);
+        return ATTN_OK;
+    }
     int P = requested;
     if (P == 0) {
-        if (num_sms <= 0) {
-            int dev = 0;
-            if (cudaGetDevice(&dev) != cudaSuccess ||
-                cudaDeviceGetAttribute(&num_sms, cudaDevAttrMultiProcessorCount, dev) !=
-                    cudaSuccess)
-                return ATTN_ERR_CUDA;
-        }
         // GQA runs a persistent grid over (sequence, KV head, slice) items,
         // one CTA per SM for head_dim 128 (tensor cores) and two for
         // head_dim 64.  GQA with fewer (sequence, KV head) units than CTAs

@@ -244,6 +244,17 @@ def test_planner_formulas(attn):
     # span of 2048), or a single tile per row: no split at all
     assert attn.attn_plan_partitions(128, 128, 128, 1, 512, 2048, 0, num_sms=152) == (1, 0)
     assert attn.attn_plan_partitions(32, 64, 128, 1, 512, 64, 0, num_sms=16) == (1, 0)
+    # the balanced split on request, whatever the lengths; MLA shapes only
+    for max_len in (1, 64, 100000):
+        P, ws = attn.attn_plan_partitions(3, 5, 128, 1, 512, max_len, attn.ATTN_PARTITIONS_BALANCED,
+                                          num_sms=152)
+        assert P == 0 and ws == (align(81 * 128 * 512 * 4) + 2 * align(81 * 128 * 4) +
+                                 align(76 * 16) + align(5 * 16) + align(5 * 8))
+    with pytest.raises(attn.AttnError):
+        attn.attn_plan_partitions(64, 64, 32, 8, 128, 8192, attn.ATTN_PARTITIONS_BALANCED,
+                                  num_sms=152)
+    with pytest.raises(attn.AttnError):
+        attn.attn_plan_partitions(3, 5, 128, 1, 512, 100, -2, num_sms=152)
     # an explicit MLA request is a fixed split into P slices per row
     P, ws = attn.attn_plan_partitions(32, 64, 128, 1, 512, 32768, 4, num_sms=152)
     assert P == 4 and ws == align(4 * 64 * 128 * 512 * 4) + 2 * align(4 * 64 * 128 * 4)

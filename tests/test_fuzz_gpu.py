@@ -1,7 +1,8 @@
 """Seeded random sweep of the configuration space against the fp64 oracle:
 every entry point over random shapes, group sizes, page sizes (or the
-contiguous layout), partition counts (workspace and on-chip), sinks, query
-rows per sequence, causal or not, with ragged, empty and sub-tile lengths."""
+contiguous layout), partition counts (workspace, on-chip, and for MLA the
+balanced split), sinks, query rows per sequence, causal or not, with ragged,
+empty and sub-tile lengths."""
 import math
 import random
 
@@ -70,7 +71,7 @@ def test_mla_random_configs(attn, case):
     lens = random_lengths(rng, batch, 5000)
     page = rng.choice([None, 8, 16, 64, 128])
     sink = rng.random() < 0.4
-    P = rng.choice([0, 1, 2, 3, 7])
+    P = rng.choice([-1, 0, 1, 2, 3, 7])   # -1: the balanced split
     rows = rng.random() < 0.5
     q_lens = [rng.randint(1, 3) for _ in range(batch)] if rows else None
     causal = rows and rng.random() < 0.7
@@ -100,7 +101,7 @@ def test_sparse_mla_random_configs(attn, case):
     ctx = [rng.randint(0, 4000) for _ in range(batch)]
     topk = rng.choice([1, 17, 64, 300, 1024])
     page = rng.choice([1, 16, 64])
-    P = rng.choice([0, 1, 2, 5])
+    P = rng.choice([-1, 0, 1, 2, 5])   # -1: the balanced split
     w = W.make_sparse_mla_workload("fuzz_sparse", ctx_lens=ctx, topk=topk, page_size=page,
                                    seed=6000 + case, device=DEV, sink=rng.random() < 0.4,
                                    scale=1.0 / math.sqrt(192.0),

@@ -1,5 +1,5 @@
-"""GPU parity of the balanced MLA split (num_partitions 0) against the fp64
-oracle.  The key tiles of every query row, concatenated, are dealt out in
+"""GPU parity of the balanced MLA split (num_partitions 0, requested from the
+planner as ATTN_PARTITIONS_BALANCED) against the fp64 oracle.  The key tiles of every query row, concatenated, are dealt out in
 equal contiguous ranges to one wave of two-CTA clusters; a cluster walks the
 rows its range meets, and rows cut by a range boundary are merged by the
 reduce from consecutive workspace slots."""
@@ -35,7 +35,7 @@ def mla_workload(lens, page_size=64, seed=0, sink=False, q_lens=None, causal=Fal
                            causal=causal)
 
 
-def run(attn, w, P=0, kv_len=None, max_kv_len=None, sink="workload"):
+def run(attn, w, P, kv_len=None, max_kv_len=None, sink="workload"):
     s = w.sink if sink == "workload" else sink
     kvl = w.kv_len if kv_len is None else kv_len
     mkl = max(1, w.max_kv_len) if max_kv_len is None else max_kv_len
@@ -68,7 +68,7 @@ def test_balanced_many_rows_per_cluster(attn):
             for _ in range(300)]
     lens[17], lens[200] = 9000, 5000
     w = mla_workload(lens, seed=71, sink=True)
-    out, lse = run(attn, w, 0)
+    out, lse = run(attn, w, attn.ATTN_PARTITIONS_BALANCED)
     sampled_check(attn, w, out, lse, 4, 1, "balanced many rows")
     o1, l1 = run(attn, w, 1)
     assert_close(out, lse, o1.float().cpu().numpy(), l1.cpu().double().numpy(),
@@ -79,7 +79,7 @@ def test_balanced_one_long_row_spans_every_cluster(attn):
     """One row of 40000 keys: each cluster takes ~1/76 of it and the reduce
     merges one partial per cluster."""
     w = mla_workload([40000], seed=72)
-    out, lse = run(attn, w, 0)
+    out, lse = run(attn, w, attn.ATTN_PARTITIONS_BALANCED)
     sampled_check(attn, w, out, lse, 16, 2, "balanced one long row")
     o1, l1 = run(attn, w, 1)
     assert_close(out, lse, o1.float().cpu().numpy(), l1.cpu().double().numpy(),
@@ -91,7 +91,7 @@ def test_balanced_fewer_tiles_than_clusters(attn, sink):
     """Four tiles in all: most clusters have nothing to do, a two-tile row is
     split across two clusters, the empty row is written by the reduce."""
     w = mla_workload([100, 30, 0, 1], seed=73, sink=sink)
-    out, lse = run(attn, w, 0)
+    out, lse = run(attn, w, attn.ATTN_PARTITIONS_BALANCED)
     ref_o, ref_l = oracle_result(w)
     assert_close(out, lse, ref_o, ref_l, f"balanced few tiles sink={sink}")
     if not sink:
@@ -101,10 +101,10 @@ def test_balanced_fewer_tiles_than_clusters(attn, sink):
 
 def test_balanced_all_rows_empty(attn):
     w = mla_workload([0, 0, 0], seed=74, sink=True)
-    out, lse = run(attn, w, 0)
+    out, lse = run(attn, w, attn.ATTN_PARTITIONS_BALANCED)
     ref_o, ref_l = oracle_result(w)
     assert_close(out, lse, ref_o, ref_l, "balanced all empty, sinks")
-    out, lse = run(attn, w, 0, sink=None)
+    out, lse = run(attn, w, attn.ATTN_PARTITIONS_BALANCED, sink=None)
     assert torch.count_nonzero(out.float()) == 0
     assert bool(torch.isneginf(lse).all())
 
@@ -113,7 +113,7 @@ def test_balanced_all_rows_empty(attn):
 def test_balanced_paged_equals_contiguous_bitwise(attn, page_size):
     w = mla_workload([5, 130, 1000, 77, 4000, 64], page_size=page_size, seed=75)
     c = W.contiguous_copy(w)
-    o1, l1 = run(attn, w, 0)
+    o1, l1 = run(attn, w, attn.ATTN_PARTITIONS_BALANCED)
     o2, l2 = run(attn, c, 0)
     assert bits_equal(o1, o2) and bits_equal(l1, l2)
     ref_o, ref_l = oracle_result(w)
@@ -126,7 +126,7 @@ def test_balanced_rows_causal(attn):
     lens = [1, 2, 63, 64, 65, 700, 3, 3000, 129]
     q_lens = [4, 2, 3, 1, 2, 4, 4, 3, 2]
     w = mla_workload(lens, seed=76, q_lens=q_lens, causal=True, sink=True)
-    out, lse = run(attn, w, 0)
+    out, lse = run(attn, w, attn.ATTN_PARTITIONS_BALANCED)
     ref_o, ref_l = oracle_result(w)
     assert_close(out, lse, ref_o, ref_l, "balanced causal rows")
 
@@ -134,10 +134,10 @@ def test_balanced_rows_causal(attn):
 def test_balanced_length_over_max_is_clamped_and_reported(attn):
     """kv_len above max_kv_len reads max_kv_len keys and sets bit 2."""
     w = mla_workload([3000, 500, 2500], seed=77)
-    out, lse = run(attn, w, 0, max_kv_len=2048)
+    out, lse = run(attn, w, attn.ATTN_PARTITIONS_BALANCED, max_kv_len=2048)
     assert attn.attn_device_error_flags(clear=True) == 4
     clamped = torch.clamp(w.kv_len, max=2048)
-    o2, l2 = run(attn, w, 0, kv_len=clamped, max_kv_len=2048)
+    o2, l2 = run(attn, w, attn.ATTN_PARTITIONS_BALANCED, kv_len=clamped, max_kv_len=2048)
     assert attn.attn_device_error_flags(clear=True) == 0
     assert bits_equal(out, o2) and bits_equal(lse, l2)
 
@@ -147,17 +147,40 @@ def test_balanced_repeated_calls_reuse_workspace(attn):
     call's plan replaces the last one's (the balanced workspace depends on
     the row count only)."""
     rng = random.Random(78)
-    P, ws_bytes = attn.attn_plan_partitions(6, 6, 128, 1, 512, 6000, 0)
+    BAL = attn.ATTN_PARTITIONS_BALANCED
+    P, ws_bytes = attn.attn_plan_partitions(6, 6, 128, 1, 512, 6000, BAL)
     assert P == 0
     assert attn.attn_plan_partitions(6, 6, 128, 1, 512, 600, 0) == (P, ws_bytes)
+    assert attn.attn_plan_partitions(6, 6, 128, 1, 512, 60, BAL) == (P, ws_bytes)
     ws = torch.empty(ws_bytes, dtype=torch.uint8, device=DEV)
     for i in range(3):
         lens = [rng.randint(0, 6000) for _ in range(6)]
         w = mla_workload(lens, seed=80 + i)
         out, lse = attn.attn_mla_decode(w.q, w.k_cache, w.kv_len, scale=w.scale,
                                         max_kv_len=w.max_kv_len, page_table=w.page_table,
-                                        num_partitions=0, workspace=ws)
+                                        num_partitions=BAL, workspace=ws)
         torch.cuda.synchronize()
         o1, l1 = run(attn, w, 1)
         assert_close(out, lse, o1.float().cpu().numpy(), l1.cpu().double().numpy(),
                      f"call {i}")
+
+
+@pytest.mark.parametrize("rows_per_seq", [1, 2])
+def test_balanced_plan_over_many_sequences(attn, rows_per_seq):
+    """More sequences than the plan kernel's 1024 threads: the tile counts
+    are scanned in chunks with a running total.  Forced balanced split
+    (the planner would not split rows this short)."""
+    rng = random.Random(90 + rows_per_seq)
+    batch = 1500 if rows_per_seq == 1 else 1100
+    lens = [rng.choice([0, 1, 64, 65]) if rng.random() < 0.2 else rng.randint(1, 300)
+            for _ in range(batch)]
+    q_lens = None if rows_per_seq == 1 else [rng.randint(1, 3) for _ in range(batch)]
+    if q_lens is not None:
+        lens = [max(L, n) for L, n in zip(lens, q_lens)]
+    w = mla_workload(lens, seed=95 + rows_per_seq, q_lens=q_lens, causal=q_lens is not None,
+                     sink=True)
+    out, lse = run(attn, w, attn.ATTN_PARTITIONS_BALANCED)
+    o1, l1 = run(attn, w, 1)
+    assert_close(out, lse, o1.float().cpu().numpy(), l1.cpu().double().numpy(),
+                 f"balanced vs P=1, {batch} sequences")
+    sampled_check(attn, w, out, lse, 1, 3, f"balanced, {batch} sequences")
