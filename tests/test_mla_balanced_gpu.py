@@ -184,3 +184,19 @@ def test_balanced_plan_over_many_sequences(attn, rows_per_seq):
     assert_close(out, lse, o1.float().cpu().numpy(), l1.cpu().double().numpy(),
                  f"balanced vs P=1, {batch} sequences")
     sampled_check(attn, w, out, lse, 1, 3, f"balanced, {batch} sequences")
+
+
+def test_bad_page_sets_error_bit_and_context_survives(attn):
+    """A page-table entry outside the pool is not read and sets bit 1, under
+    the balanced split and unsplit; the next call is correct."""
+    w = mla_workload([700, 300, 1500], seed=79)
+    bad = w.page_table.clone()
+    bad[2, 3] = w.k_cache.shape[0]          # one past the last page
+    for P in (attn.ATTN_PARTITIONS_BALANCED, 1):
+        attn.attn_mla_decode(w.q, w.k_cache, w.kv_len, scale=w.scale, max_kv_len=w.max_kv_len,
+                             page_table=bad, num_partitions=P)
+        torch.cuda.synchronize()
+        assert attn.attn_device_error_flags(clear=True) == 2
+    out, lse = run(attn, w, attn.ATTN_PARTITIONS_BALANCED)
+    ref_o, ref_l = oracle_result(w)
+    assert_close(out, lse, ref_o, ref_l, "balanced after a bad page")

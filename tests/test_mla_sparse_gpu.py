@@ -152,23 +152,25 @@ def test_sparse_bad_index_and_length_set_error_bits(attn):
     indices_stride (or below 0) is clamped and sets bit 2."""
     w = sparse_workload([500, 600], topk=256, seed=38)
     rows = w.k_cache.shape[0] * w.k_cache.shape[1]
-    bad = w.indices.clone()
-    bad[1, 5] = rows
-    run(attn, w, 1, indices=bad)
-    assert attn.attn_device_error_flags(clear=True) == 2
-    bad[1, 5] = -3
-    run(attn, w, 2, indices=bad)
-    assert attn.attn_device_error_flags(clear=True) == 2
-    too_long = torch.tensor([256, 300], dtype=torch.int32, device=DEV)
-    run(attn, w, 2, topk=too_long)
-    assert attn.attn_device_error_flags(clear=True) == 4
-    negative = torch.tensor([-1, 10], dtype=torch.int32, device=DEV)
-    run(attn, w, 1, topk=negative)
-    assert attn.attn_device_error_flags(clear=True) == 4
-    # the context is still usable and correct afterwards
-    out, lse = run(attn, w, 2)
-    ref_o, ref_l = oracle_result(w)
-    assert_close(out, lse, ref_o, ref_l, "sparse after errors")
+    BAL = attn.ATTN_PARTITIONS_BALANCED   # the plan kernel checks the counts there
+    for P1, P2 in ((1, 2), (BAL, BAL)):
+        bad = w.indices.clone()
+        bad[1, 5] = rows
+        run(attn, w, P1, indices=bad)
+        assert attn.attn_device_error_flags(clear=True) == 2
+        bad[1, 5] = -3
+        run(attn, w, P2, indices=bad)
+        assert attn.attn_device_error_flags(clear=True) == 2
+        too_long = torch.tensor([256, 300], dtype=torch.int32, device=DEV)
+        run(attn, w, P2, topk=too_long)
+        assert attn.attn_device_error_flags(clear=True) == 4
+        negative = torch.tensor([-1, 10], dtype=torch.int32, device=DEV)
+        run(attn, w, P1, topk=negative)
+        assert attn.attn_device_error_flags(clear=True) == 4
+        # the context is still usable and correct afterwards
+        out, lse = run(attn, w, P2)
+        ref_o, ref_l = oracle_result(w)
+        assert_close(out, lse, ref_o, ref_l, f"sparse after errors, P={P2}")
 
 
 def test_deepseek_v32_sparse_full_size_sampled(attn):
