@@ -6,8 +6,14 @@
 // taken from K: flare_mla_decoding_dispatch, Parameters: kv_num_heads and
 // Args: k).
 //
-// Work unit: a cluster of two CTAs per (key slice p, sequence b).  The 128
-// heads are the MMA's M dimension.  The two CTAs split the 576 channels:
+// Work: clusters of two CTAs.  Fixed split (num_partitions P >= 1): one
+// cluster per (key slice p, query row).  Balanced split (P = 0): one wave of
+// clusters, cluster c taking an equal contiguous range of the concatenated
+// 64-key tiles of all query rows, walked as runs of consecutive tiles of one
+// row (written by a one-CTA plan kernel that runs first); a run that is a
+// whole row writes the output, a run cut by a range end writes a partial
+// that the split-K reduce merges.  The 128 heads are the MMA's M dimension.
+// The two CTAs of a cluster split the 576 channels:
 //
 //   rank 0 loads channels [0, 256)   = the first half of V (4 TMA boxes),
 //   rank 1 loads channels [256, 576) = the second half of V + rope (5 boxes),
