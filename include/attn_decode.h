@@ -106,7 +106,8 @@ typedef struct attn_kv {
  *   max_kv_len    host upper bound of every kv_len[b].
  *   requested     0 = automatic; > 0 = use exactly this many partitions;
  *                 ATTN_PARTITIONS_BALANCED = the balanced split (MLA shapes
- *                 only: num_kv_heads 1, head_dim_v 512; num_partitions out 0).
+ *                 only: num_kv_heads 1, head_dim_v 512; num_partitions out 0;
+ *                 any other shape or negative value: ATTN_ERR_INVALID_ARG).
  *   num_partitions  out: partitions P (1 <= P <= ATTN_MAX_PARTITIONS), or 0
  *                 for the balanced MLA split.
  *   workspace_bytes out: workspace size attn_decode / attn_mla_decode need
