@@ -274,11 +274,12 @@ extern "C" int attn_plan_partitions(int num_sms, int batch, int num_q_rows, int 
         // items at full length and at least max_kv_len / 1024, which keeps a
         // ragged batch balanced; when it does not cost more than doubling P,
         // P is rounded up so that units * P is a multiple of the CTA count.
-        // MLA runs one two-CTA cluster per SM pair per (slice, sequence) and
-        // writes 256 KB of fp32 partials per slice, which the reduce reads
-        // back: slices of ~4096 keys, and as many slices per sequence as fit
-        // in one wave of clusters when that is more (a wave that spills over
-        // by a few clusters costs a whole extra round of tiles).
+        // MLA: the fixed-slice count P' is the larger of ~4096 keys per slice
+        // and as many slices per row as one wave of two-CTA clusters holds.
+        // It only decides whether to split: P' = 1 keeps one unsplit slice
+        // per row (no partials, no reduce), and anything larger becomes the
+        // balanced split (P = 0), which deals all rows' tiles out evenly to
+        // one wave of clusters instead of P' slices per row.
         const bool mla = num_kv_heads == 1 && head_dim_v == kMlaDimV;
         const bool tc = !mla && head_dim_v == 128;   // tensor-core decode: one CTA per SM
         // MLA runs a cluster per query row; GQA folds a sequence's rows
