@@ -88,6 +88,11 @@ def _open(path: str):
     lib.oracle_partials.argtypes = [
         ctypes.POINTER(_Problem), ctypes.c_void_p, ctypes.c_int,
         ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int]
+    if hasattr(lib, "oracle_spread"):
+        lib.oracle_spread.restype = ctypes.c_int
+        lib.oracle_spread.argtypes = [
+            ctypes.POINTER(_Problem), ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int64,
+            ctypes.c_void_p, ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int]
     return lib
 
 
@@ -331,3 +336,42 @@ def partials(q, k: KV, v: KV, kv_len, bounds, *, group, scale, dim_v=None,
     if st != 0:
         raise RuntimeError(f"oracle_partials failed with status {st}")
     return ws_o, ws_m, ws_l
+
+
+def spread(q, k: KV, v: KV, kv_len, *, group, scale, dim_v=None, sink=None, causal=False,
+           q_row_offsets=None, sample=None, threads=None):
+    """Error-bound statistics of the exact result (not part of the attention
+    definition): with the exact weights w_j = exp(s_j - M) / Z over the visible
+    keys (Z includes the sink),
+
+        sd[c] = sqrt(sum_j w_j (V[j, c] - out[c])^2),  am[c] = sum_j w_j |V[j, c]|,
+
+    and per (row, head) the visible key count, max_j scale * sum_c |q[c] K[j, c]|
+    and max_j |s_j|.  sample as for attention (default: every (row, head)).
+    Returns (sd, am, stats): sd and am shaped like attention's out, stats
+    [..., 3] = (nvis, sabs, smax).
+    """
+    lib = _load()
+    if dim_v is None:
+        dim_v = int(np.asarray(_bits(q)).shape[-1])
+    pr, rows, hq, keep = _problem(q, k, v, kv_len, q_row_offsets, group, scale, sink,
+                                  causal, dim_v)
+    if sample is None:
+        srows = np.repeat(np.arange(rows, dtype=np.int64), hq)
+        sheads = np.tile(np.arange(hq, dtype=np.int32), rows)
+        shape = (rows, hq)
+    else:
+        srows = np.ascontiguousarray(np.asarray(sample[0], dtype=np.int64))
+        sheads = np.ascontiguousarray(np.asarray(sample[1], dtype=np.int32))
+        shape = (srows.shape[0],)
+    n = srows.shape[0]
+    sd = np.zeros((n, dim_v), dtype=np.float64)
+    am = np.zeros((n, dim_v), dtype=np.float64)
+    stats = np.zeros((n, 3), dtype=np.float64)
+    st = lib.oracle_spread(ctypes.byref(pr), srows.ctypes.data, sheads.ctypes.data, n,
+                           sd.ctypes.data, am.ctypes.data, stats.ctypes.data,
+                           threads or os.cpu_count() or 1)
+    del keep
+    if st != 0:
+        raise RuntimeError(f"oracle_spread failed with status {st}")
+    return sd.reshape(shape + (dim_v,)), am.reshape(shape + (dim_v,)), stats.reshape(shape + (3,))

@@ -48,6 +48,16 @@
  *   O_S[c] = sum exp(s_j - m_S) V[j, c]   (unnormalised),
  * and (-inf, 0, 0) for an empty slice.
  *
+ * oracle_spread gives, for the exact result above, the quantities that bound
+ * how far an implementation that rounds its weights may land from it (the
+ * tolerance of the parity tests is stated in terms of them; they are not part
+ * of the attention definition).  With the exact weights w_j = exp(s_j - M) / Z
+ * (Z includes the sink, so the w_j sum to at most 1):
+ *   sd[c]  = sqrt( sum_{j in J} w_j (V[j, k, c] - out[c])^2 ),
+ *   am[c]  = sum_{j in J} w_j |V[j, k, c]|,
+ * and per (row, head): the visible key count |J|, the largest magnitude sum
+ * scale * sum_c |q[c] K[j, k, c]| over J, and the largest |s_j|.
+ *
  * Inputs are bf16 bit patterns (uint16); each one is widened exactly to
  * double.  All arithmetic is double; exp/log are the C library's.
  */
@@ -149,6 +159,8 @@ typedef struct {
     const int32_t *heads;  /* sample heads or NULL */
     int64_t num_items;
     double *out, *lse;
+    /* error-bound statistics (oracle_spread) */
+    double *sd, *am, *stats;
     /* partials */
     const int64_t *bounds; /* [num_parts+1] key boundaries, or NULL */
     int32_t num_parts;
@@ -194,6 +206,63 @@ static void attention_item(worker_arg *a, int64_t item, double *s, double *qd) {
     a->lse[item] = M + log(Z);
 }
 
+static void spread_item(worker_arg *a, int64_t item, double *s, double *qd) {
+    const oracle_problem *pr = a->pr;
+    int64_t row = a->rows[item];
+    int h = a->heads[item];
+    int b, i, n;
+    row_of(pr, row, &b, &i, &n);
+    int64_t L = pr->kv_len[b];
+    int64_t nvis = visible_keys(pr, L, i, n);
+    scores(pr, b, row, h, nvis, s, qd);
+    int kh = h / pr->group;
+
+    /* magnitudes of the scores and of their products */
+    double sabs = 0.0, smax = 0.0;
+    for (int64_t j = 0; j < nvis; ++j) {
+        const uint16_t *kp = kv_row(pr->k, b, j, kh);
+        double acc = 0.0;
+        for (int c = 0; c < pr->dim_qk; ++c) acc += fabs(qd[c] * bf16_to_double(kp[c]));
+        acc *= fabs(pr->scale);
+        if (acc > sabs) sabs = acc;
+        if (fabs(s[j]) > smax) smax = fabs(s[j]);
+    }
+    double *st = a->stats + item * 3;
+    st[0] = (double)nvis;
+    st[1] = sabs;
+    st[2] = smax;
+
+    double *sd = a->sd + item * (int64_t)pr->dim_v;
+    double *am = a->am + item * (int64_t)pr->dim_v;
+    for (int c = 0; c < pr->dim_v; ++c) { sd[c] = 0.0; am[c] = 0.0; }
+    double t = pr->sink ? pr->sink[h] : -INFINITY;
+    double M = t;
+    for (int64_t j = 0; j < nvis; ++j) if (s[j] > M) M = s[j];
+    if (M == -INFINITY) return;     /* no weights at all */
+    double Z = exp(t - M);
+    for (int64_t j = 0; j < nvis; ++j) Z += exp(s[j] - M);
+    /* out[c] first (am holds it for now), then the spread around it */
+    for (int64_t j = 0; j < nvis; ++j) {
+        double w = exp(s[j] - M) / Z;
+        const uint16_t *vp = kv_row(pr->v, b, j, kh);
+        for (int c = 0; c < pr->dim_v; ++c) am[c] += w * bf16_to_double(vp[c]);
+    }
+    for (int64_t j = 0; j < nvis; ++j) {
+        double w = exp(s[j] - M) / Z;
+        const uint16_t *vp = kv_row(pr->v, b, j, kh);
+        for (int c = 0; c < pr->dim_v; ++c) {
+            double d = bf16_to_double(vp[c]) - am[c];
+            sd[c] += w * d * d;
+        }
+    }
+    for (int c = 0; c < pr->dim_v; ++c) { sd[c] = sqrt(sd[c]); am[c] = 0.0; }
+    for (int64_t j = 0; j < nvis; ++j) {
+        double w = exp(s[j] - M) / Z;
+        const uint16_t *vp = kv_row(pr->v, b, j, kh);
+        for (int c = 0; c < pr->dim_v; ++c) am[c] += w * fabs(bf16_to_double(vp[c]));
+    }
+}
+
 static void partials_item(worker_arg *a, int64_t item, double *s, double *qd) {
     const oracle_problem *pr = a->pr;
     int64_t row = item / pr->num_q_heads;
@@ -232,6 +301,7 @@ static void *worker(void *p) {
     if (!s || !qd) { a->status = 1; free(s); free(qd); return NULL; }
     for (int64_t it = a->tid; it < a->num_items; it += a->nthreads) {
         if (a->bounds) partials_item(a, it, s, qd);
+        else if (a->sd) spread_item(a, it, s, qd);
         else attention_item(a, it, s, qd);
     }
     free(s);
@@ -322,5 +392,25 @@ int oracle_partials(const oracle_problem *pr, const int64_t *bounds, int num_par
     a.num_parts = num_parts;
     a.num_rows = total_rows;
     a.ws_o = ws_o; a.ws_m = ws_m; a.ws_l = ws_l;
+    return run(&a, nthreads);
+}
+
+/*
+ * Error-bound statistics of the exact result for the listed (rows[i],
+ * heads[i]) pairs: sd and am are [num_items][dim_v], stats [num_items][3] =
+ * (visible keys, max_j scale * sum_c |q[c] K[j, c]|, max_j |s_j|).
+ */
+int oracle_spread(const oracle_problem *pr, const int64_t *rows, const int32_t *heads,
+                  int64_t num_items, double *sd, double *am, double *stats, int nthreads) {
+    int st = check_problem(pr);
+    if (st) return st;
+    if (num_items < 0 || (num_items > 0 && (!rows || !heads || !sd || !am || !stats)))
+        return 2;
+    if (num_items == 0) return 0;
+    worker_arg a;
+    memset(&a, 0, sizeof a);
+    a.pr = pr;
+    a.rows = rows; a.heads = heads; a.num_items = num_items;
+    a.sd = sd; a.am = am; a.stats = stats;
     return run(&a, nthreads);
 }

@@ -24,3 +24,22 @@ def pytest_collection_modifyitems(config, items):
     for item in items:
         if "gpu" in item.keywords:
             item.add_marker(skip)
+
+
+def pytest_terminal_summary(terminalreporter, exitstatus, config):
+    """How many compared output elements needed more than the 1e-2 figure
+    (each within its derived bound, or the test failed) and the largest
+    excess."""
+    try:
+        from tests.helpers import STATS
+    except Exception:  # pragma: no cover
+        return
+    if not STATS["comparisons"]:
+        return
+    w = STATS["worst"]
+    line = (f"parity: {STATS['comparisons']} comparisons, {STATS['elements']} elements, "
+            f"{STATS['above_1e2']} above 1e-2")
+    if w:
+        line += (f"; largest excess {w['excess']:.3g} (error {w['err']:.4g} at exact "
+                 f"{w['ref']:.4g}, bound {w['bound']:.4g}) in {w['what']}")
+    terminalreporter.write_line(line)

@@ -8,7 +8,7 @@ import torch
 
 import oracle
 from split_flash_decoding_gb300 import workloads as W
-from tests.helpers import assert_close, bits_equal, oracle_result
+from tests.helpers import assert_close, assert_pair, bits_equal, oracle_result
 
 pytestmark = pytest.mark.gpu
 
@@ -78,9 +78,7 @@ def test_split_k_matches_single_partition(attn):
     assert_close(o1, l1, ref_o, ref_l, "P=1")
     for P in (2, 7, 16, 64, 256):
         oP, lP = run(attn, w, P)
-        assert_close(oP, lP, ref_o, ref_l, f"P={P}")
-        assert_close(oP, lP, o1.float().cpu().numpy(), l1.cpu().double().numpy(),
-                     f"P={P} vs P=1")
+        assert_pair(oP, lP, o1, l1, ref_o, ref_l, f"P={P} vs P=1")
 
 
 def test_empty_and_tiny_sequences(attn):
@@ -169,8 +167,7 @@ def test_small_split_merged_on_chip(attn, P):
         ref_o, ref_l = oracle_result(w)
         assert_close(out, lse, ref_o, ref_l, f"on-chip merge P={P} hq={hq} hkv={hkv}")
         o1, l1 = run(attn, w, 1)
-        assert_close(out, lse, o1.float().cpu().numpy(), l1.cpu().double().numpy(),
-                     f"on-chip merge P={P} vs P=1")
+        assert_pair(out, lse, o1, l1, ref_o, ref_l, f"on-chip merge P={P} vs P=1")
 
 
 def test_llama3_8b_full_size_merged_on_chip(attn):

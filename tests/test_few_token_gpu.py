@@ -7,7 +7,7 @@ import pytest
 import torch
 
 from split_flash_decoding_gb300 import workloads as W
-from tests.helpers import assert_close, bits_equal, oracle_result
+from tests.helpers import assert_close, assert_pair, bits_equal, oracle_result
 
 pytestmark = pytest.mark.gpu
 DEV = "cuda:0"
@@ -39,14 +39,6 @@ def run(attn, w, P, k=None, v=None, page_table="workload"):
                                 max_q_len=w.max_q_len, causal=w.causal, num_partitions=P)
     torch.cuda.synchronize()
     return out, lse
-
-
-def test_routes_to_split_path(attn):
-    assert attn.few_token_split(4, 4, 128, 64)
-    assert attn.few_token_split(2, 8, 128, 64)
-    assert not attn.few_token_split(5, 4, 128, 64)
-    assert not attn.few_token_split(2, 4, 64, 64)
-    assert not attn.few_token_split(1, 4, 128, 64)
 
 
 @pytest.mark.parametrize("causal", [True, False])
@@ -86,10 +78,10 @@ def test_sinks(attn):
 def test_split_matches_unsplit(attn):
     w = few_workload([4, 3, 2, 1, 4], [3000, 1500, 7000, 200, 5000], seed=65)
     o1, l1 = run(attn, w, 1)
+    ref_o, ref_l = oracle_result(w)
     for P in (2, 4, 7, 16):
         o, l = run(attn, w, P)
-        assert_close(o, l, o1.float().cpu().numpy().astype("float64"),
-                     l1.cpu().numpy().astype("float64"), f"few P={P} vs P=1")
+        assert_pair(o, l, o1, l1, ref_o, ref_l, f"few P={P} vs P=1")
 
 
 @pytest.mark.parametrize("page_size", [16, 64, 128])

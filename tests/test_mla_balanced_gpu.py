@@ -11,7 +11,7 @@ import pytest
 import torch
 
 from split_flash_decoding_gb300 import workloads as W
-from tests.helpers import assert_close, bits_equal, oracle_result
+from tests.helpers import assert_close, assert_consistent, bits_equal, oracle_result
 
 pytestmark = pytest.mark.gpu
 DEV = "cuda:0"
@@ -58,6 +58,7 @@ def sampled_check(attn, w, out, lse, heads_per_row, seed, what):
     ref_o, ref_l = oracle_result(w, sample=(rows, heads))
     ri, hi = torch.as_tensor(rows, device=DEV), torch.as_tensor(heads, device=DEV)
     assert_close(out[ri, hi], lse[ri, hi], ref_o, ref_l, what)
+    return float(ref_o.eps.max())
 
 
 def test_balanced_many_rows_per_cluster(attn):
@@ -69,10 +70,9 @@ def test_balanced_many_rows_per_cluster(attn):
     lens[17], lens[200] = 9000, 5000
     w = mla_workload(lens, seed=71, sink=True)
     out, lse = run(attn, w, attn.ATTN_PARTITIONS_BALANCED)
-    sampled_check(attn, w, out, lse, 4, 1, "balanced many rows")
+    eps = sampled_check(attn, w, out, lse, 4, 1, "balanced many rows")
     o1, l1 = run(attn, w, 1)
-    assert_close(out, lse, o1.float().cpu().numpy(), l1.cpu().double().numpy(),
-                 "balanced vs P=1, many rows")
+    assert_consistent(out, lse, o1, l1, eps, "balanced vs P=1, many rows")
 
 
 def test_balanced_one_long_row_spans_every_cluster(attn):
@@ -80,10 +80,9 @@ def test_balanced_one_long_row_spans_every_cluster(attn):
     merges one partial per cluster."""
     w = mla_workload([40000], seed=72)
     out, lse = run(attn, w, attn.ATTN_PARTITIONS_BALANCED)
-    sampled_check(attn, w, out, lse, 16, 2, "balanced one long row")
+    eps = sampled_check(attn, w, out, lse, 16, 2, "balanced one long row")
     o1, l1 = run(attn, w, 1)
-    assert_close(out, lse, o1.float().cpu().numpy(), l1.cpu().double().numpy(),
-                 "balanced vs P=1, one row")
+    assert_consistent(out, lse, o1, l1, eps, "balanced vs P=1, one row")
 
 
 @pytest.mark.parametrize("sink", [False, True])
@@ -160,9 +159,9 @@ def test_balanced_repeated_calls_reuse_workspace(attn):
                                         max_kv_len=w.max_kv_len, page_table=w.page_table,
                                         num_partitions=BAL, workspace=ws)
         torch.cuda.synchronize()
+        eps = sampled_check(attn, w, out, lse, 8, 20 + i, f"call {i}")
         o1, l1 = run(attn, w, 1)
-        assert_close(out, lse, o1.float().cpu().numpy(), l1.cpu().double().numpy(),
-                     f"call {i}")
+        assert_consistent(out, lse, o1, l1, eps, f"call {i} vs P=1")
 
 
 @pytest.mark.parametrize("rows_per_seq", [1, 2])
@@ -180,10 +179,9 @@ def test_balanced_plan_over_many_sequences(attn, rows_per_seq):
     w = mla_workload(lens, seed=95 + rows_per_seq, q_lens=q_lens, causal=q_lens is not None,
                      sink=True)
     out, lse = run(attn, w, attn.ATTN_PARTITIONS_BALANCED)
+    eps = sampled_check(attn, w, out, lse, 1, 3, f"balanced, {batch} sequences")
     o1, l1 = run(attn, w, 1)
-    assert_close(out, lse, o1.float().cpu().numpy(), l1.cpu().double().numpy(),
-                 f"balanced vs P=1, {batch} sequences")
-    sampled_check(attn, w, out, lse, 1, 3, f"balanced, {batch} sequences")
+    assert_consistent(out, lse, o1, l1, eps, f"balanced vs P=1, {batch} sequences")
 
 
 def test_bad_page_sets_error_bit_and_context_survives(attn):

@@ -497,3 +497,118 @@ def test_sparse_workload_names_rows_of_the_pool():
     again = W.make_sparse_mla_workload("s", ctx_lens=[0, 5, 300, 1000], topk=256, page_size=16,
                                        seed=3, dim_qk=32, dim_v=16, num_q_heads=4)
     assert torch.equal(w.indices, again.indices)
+
+
+# ---------------------------------------------------------------------------
+# oracle.spread: the error-bound statistics of the exact result
+# ---------------------------------------------------------------------------
+
+def _onehot_problem(a, v_rows, scale, hq=1, d=8, dv=4):
+    """One sequence whose key j is a_j e_0 and q = e_0, so s_j = scale * a_j
+    exactly; V rows given.  Returns (q, K, V) as bf16 tensors."""
+    L = len(a)
+    q = torch.zeros(1, hq, d)
+    q[0, :, 0] = 1.0
+    k = torch.zeros(1, L, 1, d)
+    k[0, :, 0, 0] = torch.tensor(a, dtype=torch.float32)
+    v = torch.tensor(v_rows, dtype=torch.float32).reshape(1, L, 1, dv)
+    return bf16(q), bf16(k), bf16(v)
+
+
+def _spread(q, k, v, lens, group, scale, **kw):
+    return oracle.spread(q, oracle.KV.contiguous(k), oracle.KV.contiguous(v),
+                         torch.tensor(lens, dtype=torch.int32), group=group, scale=scale,
+                         dim_v=v.shape[-1], **kw)
+
+
+def test_spread_single_key_is_zero():
+    q, k, v = _onehot_problem([3.0], [[1.5, -2.0, 0.25, 4.0]], 0.5)
+    sd, am, st = _spread(q, k, v, [1], 1, 0.5)
+    assert np.all(sd[0, 0] == 0.0)
+    assert np.allclose(am[0, 0], [1.5, 2.0, 0.25, 4.0], rtol=0, atol=1e-15)
+    assert st[0, 0, 0] == 1 and st[0, 0, 1] == 1.5 and st[0, 0, 2] == 1.5
+
+
+def test_spread_two_keys_closed_form():
+    """Two weights w and 1 - w: the spread of a two-point distribution is
+    sqrt(w (1 - w)) |v0 - v1|."""
+    v_rows = [[1.0, -2.0, 0.5, 3.0], [-1.0, 2.0, 0.5, -0.75]]
+    q, k, v = _onehot_problem([2.0, 0.0], v_rows, 0.5)
+    sd, am, st = _spread(q, k, v, [2], 1, 0.5)
+    w0 = 1.0 / (1.0 + math.exp(-1.0))           # scores 1 and 0
+    v0, v1 = np.array(v_rows[0]), np.array(v_rows[1])
+    assert np.allclose(sd[0, 0], math.sqrt(w0 * (1 - w0)) * np.abs(v0 - v1), rtol=1e-13, atol=0)
+    assert np.allclose(am[0, 0], w0 * np.abs(v0) + (1 - w0) * np.abs(v1), rtol=1e-13)
+    assert st[0, 0, 0] == 2 and st[0, 0, 2] == 1.0
+
+
+def test_spread_one_key_and_a_sink_closed_form():
+    """One key of weight w beside a sink (a zero value): out = w v, and the
+    spread of the key around it is sqrt(w) (1 - w) |v|."""
+    q, k, v = _onehot_problem([1.0], [[2.0, -1.0, 0.5, 3.0]], 1.0)
+    sink = torch.tensor([0.25])
+    sd, am, st = _spread(q, k, v, [1], 1, 1.0, sink=sink)
+    w = 1.0 / (1.0 + math.exp(0.25 - 1.0))
+    vv = np.array([2.0, 1.0, 0.5, 3.0])
+    assert np.allclose(sd[0, 0], math.sqrt(w) * (1 - w) * vv, rtol=1e-13)
+    assert np.allclose(am[0, 0], w * vv, rtol=1e-13)
+
+
+def test_spread_identical_keys_is_population_std():
+    """Equal scores: the weights are uniform, so sd is numpy's population
+    standard deviation of V over the keys and am the mean of |V|."""
+    g = torch.Generator().manual_seed(5)
+    L, d = 37, 16
+    q = bf16(torch.randn(1, 2, d, generator=g))
+    k = bf16(torch.randn(1, 1, 1, d, generator=g)).expand(1, L, 1, d).contiguous()
+    v = bf16(torch.randn(1, L, 1, 8, generator=g))
+    sd, am, _ = _spread(q, k, v, [L], 2, 0.3)
+    vv = v[0, :, 0].double().numpy()
+    for h in range(2):
+        assert np.allclose(sd[0, h], vv.std(axis=0), rtol=1e-12)
+        assert np.allclose(am[0, h], np.abs(vv).mean(axis=0), rtol=1e-12)
+
+
+@pytest.mark.parametrize("with_sink", [False, True])
+def test_spread_equals_the_second_moment_through_attention(with_sink):
+    """sd^2 = E_w[v^2] - out^2 (2 - sum w): the second moment taken by the
+    (separately pinned) attention function with V squared, on a paged GQA
+    cache with causal multi-row sequences.  V holds multiples of 1/8 below 2
+    in magnitude, so V^2 and |V| are exact in bf16."""
+    g = torch.Generator().manual_seed(9)
+    lens, q_lens, hq, hkv, d = [40, 3, 130], [2, 3, 1], 8, 2, 16
+    q, k, _ = logical_problem(9, 3, hq, hkv, d, lens, q_lens=q_lens)
+    v = bf16(torch.randint(-15, 16, (3, max(lens), hkv, 8), generator=g).float() / 8)
+    offs = torch.tensor(np.concatenate([[0], np.cumsum(q_lens)]), dtype=torch.int32)
+    kvl = torch.tensor(lens, dtype=torch.int32)
+    pk, table = to_paged(k, lens, 16, 3)
+    pv, _ = to_paged(v, lens, 16, 3)
+    K = oracle.KV.paged(pk, torch.tensor(table))
+    sink = torch.randn(hq, generator=g) if with_sink else None
+    kw = dict(group=hq // hkv, scale=0.25, dim_v=8, sink=sink, causal=True, q_row_offsets=offs)
+    out, lse = oracle.attention(q, K, oracle.KV.paged(pv, torch.tensor(table)), kvl, **kw)
+    m2, _ = oracle.attention(q, K, oracle.KV.paged(bf16(pv.float() ** 2), torch.tensor(table)),
+                             kvl, **kw)
+    ab, _ = oracle.attention(q, K, oracle.KV.paged(bf16(pv.float().abs()), torch.tensor(table)),
+                             kvl, **kw)
+    sd, am, st = oracle.spread(q, K, oracle.KV.paged(pv, torch.tensor(table)), kvl, **kw)
+    wsum = (np.ones_like(lse) if sink is None
+            else 1.0 - np.exp(sink.double().numpy()[None, :] - lse))
+    var = m2 - out ** 2 * (2.0 - wsum)[..., None]
+    assert np.allclose(sd ** 2, np.maximum(var, 0.0), rtol=1e-10, atol=1e-13)
+    assert np.allclose(am, ab, rtol=1e-12, atol=1e-15)
+    # visible keys: rows 0-1 of sequence 0 see 39 and 40; sequence 1's three
+    # rows see 1, 2, 3; sequence 2's row sees 130
+    assert st[:, 0, 0].tolist() == [39, 40, 1, 2, 3, 130]
+
+
+def test_spread_translation_invariant():
+    """Shifting every value by a constant shifts out by it and leaves the
+    spread unchanged (no sink)."""
+    g = torch.Generator().manual_seed(13)
+    q, k, _ = logical_problem(13, 2, 4, 1, 16, [50, 9])
+    v = bf16(torch.randint(-12, 13, (2, 50, 1, 8), generator=g).float() / 8)
+    a = _spread(q, k, v, [50, 9], 4, 0.25)[0]
+    b = _spread(q, k, bf16(v.float() + 1.0), [50, 9], 4, 0.25)[0]
+    assert np.allclose(a, b, rtol=1e-12, atol=1e-14)
+    assert np.any(a > 0.1)

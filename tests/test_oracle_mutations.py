@@ -35,6 +35,13 @@ MUTATIONS = {
                                  "slot = r / kv->page_size;\n    } else if"),
     "last_key_dropped": ("for (int64_t j = 0; j < nvis; ++j) {\n        double w",
                          "for (int64_t j = 0; j + 1 < nvis; ++j) {\n        double w"),
+    # the error-bound statistics (oracle_spread)
+    "spread_weights_unnormalised": ("double w = exp(s[j] - M) / Z;", "double w = exp(s[j] - M);"),
+    "spread_sqrt_dropped": ("sd[c] = sqrt(sd[c]);", "sd[c] = sd[c];"),
+    "spread_centre_dropped": ("double d = bf16_to_double(vp[c]) - am[c];",
+                              "double d = bf16_to_double(vp[c]);"),
+    "spread_abs_dropped": ("am[c] += w * fabs(bf16_to_double(vp[c]));",
+                           "am[c] += w * bf16_to_double(vp[c]);"),
 }
 # v_read_from_k: replace only in the full-attention item
 MUTATIONS["v_read_from_k"] = ("        Z += w;\n        const uint16_t *vp = kv_row(pr->v, b, j, kh);",
