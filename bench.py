@@ -50,18 +50,32 @@ KERNEL_SOURCES = {
 }
 
 
-def few_token(w) -> bool:
-    """A few rows per sequence run split-K on the decode kernel."""
-    return (w.max_q_len > 1 and w.dim_qk == 128 and w.max_q_len * w.group <= 16
-            and w.batch <= 2048)
+# The kernel that dominates each workload's call (the library decides the
+# route; this only names the kernel whose counters the profiles hold).
+DOMINANT_KERNEL = {
+    "llama3": "gqa_decode_tc", "long_context": "gqa_decode_tc", "few_token": "gqa_decode_tc",
+    "tiny": "gqa_decode", "mla": "mla_decode", "mla_mtp": "mla_decode",
+    "sparse_mla": "mla_decode", "mixed": "tile_attention",
+}
 
 
-def dominant_kernel(w) -> str:
-    if w.is_mla:
-        return "mla_decode"
-    if w.max_q_len > 1 and not few_token(w):
-        return "tile_attention"
-    return "gqa_decode_tc" if w.dim_qk == 128 else "gqa_decode"
+def dominant_kernel(workload: str) -> str:
+    return DOMINANT_KERNEL[workload]
+
+
+def workload_config(w, world: int) -> dict:
+    """The workload description both arms print under "config"."""
+    return {
+        "workload": w.name,
+        "batch": w.batch, "num_q_rows": w.rows, "num_q_heads": w.num_q_heads,
+        "num_kv_heads": w.num_kv_heads, "head_dim": w.dim_qk, "dim_v": w.dim_v,
+        "page_size": w.page_size, "total_kv_tokens": sum(w.kv_len_host),
+        "max_kv_len": w.max_kv_len, "max_q_len": w.max_q_len, "causal": bool(w.causal),
+        "algorithmic_bytes_per_call": algorithmic_bytes(w),
+        "flops_per_call": algorithmic_flops(w),
+        "l2": "inputs larger than L2: the KV cache read every step exceeds 129 MB; no flush",
+        "parallelism": f"replicas x{world}",
+    }
 
 
 def parse():
@@ -353,7 +367,7 @@ def run_reference(args, rank, world):
         "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": round(secs / max(1, args.steps) * 1e3, 3), "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-        "config": {"workload": w.name},
+        "config": workload_config(w, world),
         "cpu_baseline": {"value": round(value, 4), "unit": "GB/s", "cores": threads,
                          "kind": "oracle", "sample": sample},
         "e2e": {"value": round(value, 4), "unit": "GB/s", "h2d_bytes_per_step": 0,
@@ -376,16 +390,10 @@ def run_ours(args, rank, world, dist):
     stream = torch.cuda.Stream(device=dev)
 
     sparse = w.indices is not None
-    if w.is_mla:
-        span = w.indices.shape[1] if sparse else w.max_kv_len
-        P, ws_bytes = attn.attn_plan_partitions(w.batch, w.rows, w.num_q_heads, 1, w.dim_v,
-                                                span, args.partitions)
-    elif w.max_q_len > 1 and not few_token(w):
-        P, ws_bytes = 1, 0
-    else:
-        P, ws_bytes = attn.attn_plan_partitions(w.batch, w.rows, w.num_q_heads,
-                                                w.num_kv_heads, w.dim_v, w.max_kv_len,
-                                                args.partitions)
+    span = w.indices.shape[1] if sparse else w.max_kv_len
+    P, ws_bytes = attn.attn_plan_partitions(w.batch, w.rows, w.num_q_heads, w.num_kv_heads,
+                                            w.dim_v, span, args.partitions,
+                                            max_q_len=w.max_q_len)
     ws = torch.empty(max(ws_bytes, 1), dtype=torch.uint8, device=dev)
     out = torch.empty((w.rows, w.num_q_heads, w.dim_v), dtype=torch.bfloat16, device=dev)
     lse = torch.empty((w.rows, w.num_q_heads), dtype=torch.float32, device=dev)
@@ -510,7 +518,7 @@ def run_ours(args, rank, world, dist):
     achieved = nbytes / (mean_call_ms * 1e-3) / 1e9
     tflops = flops / (mean_call_ms * 1e-3) / 1e12
     tensor_peak = float(peaks.get("bf16_tflops", 1900.0))
-    kernel_key = dominant_kernel(w)
+    kernel_key = dominant_kernel(args.workload)
     traffic = profiled_traffic(kernel_key, w.name)
     cpu = None
     if not args.no_cpu_baseline:
@@ -566,16 +574,9 @@ def run_ours(args, rank, world, dist):
         "vs_baseline": None,
         "dtype": "bf16",
         "data": "synthetic",
-        "config": {
-            "workload": w.name,
-            "batch": w.batch, "num_q_heads": w.num_q_heads, "num_kv_heads": w.num_kv_heads,
-            "head_dim": w.dim_qk, "dim_v": w.dim_v, "page_size": w.page_size,
-            "total_kv_tokens": sum(w.kv_len_host), "max_kv_len": w.max_kv_len,
-            "num_partitions": P, "algorithmic_bytes_per_call": nbytes,
-            "flops_per_call": flops,
-            "l2": "inputs larger than L2: the KV cache read every step exceeds 129 MB; no flush",
-            "parallelism": f"replicas x{world}",
-        },
+        "config": workload_config(w, world),
+        "plan": {"num_partitions": P, "workspace_bytes": ws_bytes,
+                 "note": "num_partitions 0 = the balanced MLA split"},
         "clocks": clocks.summary(),
         "e2e": {"value": round(world * nbytes / e2e_s / 1e9, 2), "unit": "GB/s",
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,

@@ -101,6 +101,14 @@ typedef struct attn_kv {
  *   num_sms       SMs to plan for; <= 0 queries the current device.
  *   batch         sequences; num_q_rows total query rows (= batch for
  *                 single-token decode).
+ *   max_q_len     host upper bound of the query rows of any sequence (1 for
+ *                 single-token decode), as attn_decode takes it.  It picks
+ *                 the GQA kernel exactly as attn_decode does: a few rows
+ *                 (head_dim_v 128, max_q_len * group <= 16, batch <= 2048)
+ *                 fold onto the split-K decode kernel; longer row runs take
+ *                 the tile kernel, which does not split, so the plan is P = 1
+ *                 with workspace 0 (a request above 1 returns
+ *                 ATTN_ERR_UNSUPPORTED).  MLA ignores it.
  *   num_q_heads, num_kv_heads   heads (num_kv_heads = 1 for MLA).
  *   head_dim_v    output channels (128 for GQA d128, 512 for MLA).
  *   max_kv_len    host upper bound of every kv_len[b].
@@ -120,8 +128,8 @@ typedef struct attn_kv {
  * (workspace_bytes 0): a cluster of P CTAs splits each (sequence, KV head)
  * into P equal key slices of that sequence and merges them on chip.  The
  * automatic choice treats num_kv_heads == 1 with head_dim_v == 512 as the
- * MLA shape and everything else as GQA.  GQA with head_dim 128 and more
- * query rows than sequences (the few-row fold): P = 1 when there are at
+ * MLA shape and everything else as GQA.  GQA with head_dim 128 and
+ * max_q_len > 1 on the few-row fold: P = 1 when there are at
  * least 2 (sequence, KV head) units per SM, else the many-unit rule (at
  * least four items per CTA at full length and slices of at most ~1024
  * keys) whatever the unit count.  MLA: with
@@ -138,9 +146,9 @@ typedef struct attn_kv {
  * Returns ATTN_OK, ATTN_ERR_INVALID_ARG, or ATTN_ERR_CUDA if the SM count
  * query fails.  Launches nothing.
  */
-int attn_plan_partitions(int num_sms, int batch, int num_q_rows, int num_q_heads,
-                         int num_kv_heads, int head_dim_v, int max_kv_len, int requested,
-                         int *num_partitions, size_t *workspace_bytes);
+int attn_plan_partitions(int num_sms, int batch, int num_q_rows, int max_q_len,
+                         int num_q_heads, int num_kv_heads, int head_dim_v, int max_kv_len,
+                         int requested, int *num_partitions, size_t *workspace_bytes);
 
 /*
  * attn_decode -- GQA/MHA attention of few query rows per sequence against a
@@ -182,8 +190,11 @@ int attn_plan_partitions(int num_sms, int batch, int num_q_rows, int num_q_heads
  *   causal     non-zero: row i of a sequence with n rows and L keys sees
  *              keys j <= L - n + i (bottom-right aligned).  A no-op for
  *              single-row sequences.
- *   num_partitions  P from attn_plan_partitions (or any 1..MAX); must be 1
- *              on the tile kernel (max_q_len > 1 beyond the few-row fold).
+ *   num_partitions  P from attn_plan_partitions (or any 1..MAX), or 0 for
+ *              the planner's automatic choice on the current device (the
+ *              same call as attn_plan_partitions with num_sms 0 and
+ *              requested 0: size the workspace with that call); must be 0 or
+ *              1 on the tile kernel (max_q_len > 1 beyond the few-row fold).
  *   workspace  device, 256-byte aligned, >= the planner's workspace_bytes
  *              for this P; may be NULL when P == 1, and with head_dim 128
  *              when P is 2 or 4 (those merge on chip).  Contents on entry
@@ -340,20 +351,25 @@ int attn_splitk_reduce(const float *ws_o, const float *ws_m, const float *ws_l,
  * plain C program with no allocator at hand.  The source pages have no
  * counterpart; it exists only because split-K needs scratch space.
  *
- * Arguments are those of attn_decode without workspace / workspace_bytes;
- * num_partitions 0 plans automatically (attn_plan_partitions).  The split-K
- * scratch is a fixed 32 MiB array inside the library (a file-scope device
- * array that every GPU loading the library keeps until the process exits);
- * a partition count whose workspace would exceed it returns
- * ATTN_ERR_WORKSPACE and launches nothing.  The call itself allocates
- * nothing (no cudaMalloc/cudaFree, no allocating library routine).
+ * Arguments are those of attn_decode without workspace / workspace_bytes.
+ * The call is routed and planned by attn_plan_partitions, exactly as
+ * attn_decode routes it: num_partitions 0 plans automatically, a non-zero
+ * count is used as given (single rows and the few-row fold split K with it;
+ * the tile kernel for longer row runs does not split and rejects a count
+ * above 1 with ATTN_ERR_UNSUPPORTED).  The split-K scratch is a fixed 32 MiB
+ * array inside the library (a file-scope device array that every GPU loading
+ * the library keeps until the process exits); a partition count whose
+ * workspace would exceed it returns ATTN_ERR_WORKSPACE and launches nothing.
+ * The call itself allocates nothing (no cudaMalloc/cudaFree, no allocating
+ * library routine).
  *
- * The first call on a device looks up the array's device address
- * (cudaGetSymbolAddress, with that device current); make that first call
- * before any stream capture.  Every call shares the one array and leaves its
- * partials there: calls that can overlap on the GPU (other streams, other
- * host threads) race on it and must be serialised by the caller.  Nothing in
- * it needs to start at zero.
+ * Every call looks up the array's device address (cudaGetSymbolAddress,
+ * with the call's device current), so the address stays right after a
+ * device reset; the first call on a device may load the library's device
+ * code, so make it before any stream capture.  Every call shares the one
+ * array and leaves its partials there: calls that can overlap on the GPU
+ * (other streams, other host threads) race on it and must be serialised by
+ * the caller.  Nothing in it needs to start at zero.
  */
 int attn_decode_noalloc(const void *q, const attn_kv_t *k, const attn_kv_t *v,
                         const uint32_t *kv_len, const uint32_t *q_row_offsets, int batch,

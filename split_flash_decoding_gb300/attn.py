@@ -59,7 +59,7 @@ class attn_kv_t(ctypes.Structure):
 _c = ctypes
 _SIGNATURES = {
     "attn_plan_partitions": [_c.c_int, _c.c_int, _c.c_int, _c.c_int, _c.c_int, _c.c_int,
-                             _c.c_int, _c.c_int, _c.POINTER(_c.c_int),
+                             _c.c_int, _c.c_int, _c.c_int, _c.POINTER(_c.c_int),
                              _c.POINTER(_c.c_size_t)],
     "attn_decode": [_c.c_void_p, _c.POINTER(attn_kv_t), _c.POINTER(attn_kv_t), _c.c_void_p,
                     _c.c_void_p, _c.c_int, _c.c_int, _c.c_int, _c.c_int, _c.c_int, _c.c_int,
@@ -161,14 +161,16 @@ def kv_descriptor(cache: torch.Tensor, page_table: Optional[torch.Tensor] = None
 
 def attn_plan_partitions(batch: int, num_q_rows: int, num_q_heads: int, num_kv_heads: int,
                          head_dim_v: int, max_kv_len: int, requested: int = 0,
-                         num_sms: int = 0):
-    """Returns (num_partitions, workspace_bytes)."""
+                         num_sms: int = 0, max_q_len: int = 1):
+    """Returns (num_partitions, workspace_bytes).  max_q_len (rows of the
+    longest sequence) lets the library route a multi-row GQA call: the
+    few-row fold keeps split-K, longer row runs get (1, 0)."""
     P = ctypes.c_int(0)
     ws = ctypes.c_size_t(0)
     _check("attn_plan_partitions",
-           lib().attn_plan_partitions(num_sms, batch, num_q_rows, num_q_heads, num_kv_heads,
-                                      head_dim_v, max_kv_len, requested, ctypes.byref(P),
-                                      ctypes.byref(ws)))
+           lib().attn_plan_partitions(num_sms, batch, num_q_rows, max_q_len, num_q_heads,
+                                      num_kv_heads, head_dim_v, max_kv_len, requested,
+                                      ctypes.byref(P), ctypes.byref(ws)))
     return P.value, ws.value
 
 
@@ -178,13 +180,6 @@ def _workspace(nbytes: int, device, workspace: Optional[torch.Tensor]):
     if workspace is None:
         workspace = torch.empty(nbytes, dtype=torch.uint8, device=device)
     return workspace, workspace.numel() * workspace.element_size()
-
-
-def few_token_split(max_q_len: int, group: int, head_dim: int, batch: int) -> bool:
-    """True when attn_decode folds the rows of each sequence onto the decode
-    kernel (and may split K): head_dim 128, max_q_len * group <= 16, batch
-    within the decode kernel's limit.  Mirrors the library's routing."""
-    return max_q_len > 1 and head_dim == 128 and max_q_len * group <= 16 and batch <= 2048
 
 
 def attn_decode(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tensor,
@@ -200,9 +195,10 @@ def attn_decode(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tensor,
     decode, else q_row_offsets[-1]); caches as for kv_descriptor; kv_len
     int32/uint32 [batch] on the device; q_row_offsets int32 [batch + 1] on
     the device or None; sink fp32 [num_q_heads] or None.  num_partitions 0
-    plans automatically.  A few rows per sequence (max_q_len * group <= 16,
-    head_dim 128) run split-K on the decode kernel; longer row runs take the
-    tile kernel, which is not split (P = 1).  Returns (out, lse).
+    plans automatically.  The library's planner routes the call (a few rows
+    per sequence keep split-K on the decode kernel; longer row runs take the
+    tile kernel, which is not split) and sizes the workspace.  Returns
+    (out, lse).
     """
     rows, hq, d = q.shape
     batch = kv_len.shape[0]
@@ -210,11 +206,8 @@ def attn_decode(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tensor,
         out = torch.empty((rows, hq, d), dtype=torch.bfloat16, device=q.device)
     if lse is None and return_lse:
         lse = torch.empty((rows, hq), dtype=torch.float32, device=q.device)
-    if max_q_len > 1 and not few_token_split(max_q_len, group, d, batch):
-        P, ws_bytes = 1, 0
-    else:
-        P, ws_bytes = attn_plan_partitions(batch, rows, hq, hq // group, d, max_kv_len,
-                                           num_partitions)
+    P, ws_bytes = attn_plan_partitions(batch, rows, hq, hq // group, d, max_kv_len,
+                                       num_partitions, max_q_len=max_q_len)
     ws, ws_size = _workspace(ws_bytes, q.device, workspace)
     kd = kv_descriptor(k_cache, page_table)
     vd = kv_descriptor(v_cache, page_table)

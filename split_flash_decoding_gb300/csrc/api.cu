@@ -18,22 +18,14 @@ namespace {
 // Device error word written by kernels instead of trapping or hanging.
 __device__ unsigned g_error_word;
 
-constexpr int kMaxDevices = 64;
-std::mutex g_mu;
-unsigned *g_err_ptr[kMaxDevices];
-
-// Address of g_error_word on the current device (looked up once per device).
+// Address of g_error_word in the current device's context.  Looked up on
+// every call (a host-side table lookup, far cheaper than a launch), so a
+// device reset or a new primary context never leaves a stale address behind.
 int error_word(unsigned **out) {
-    int dev = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices)
+    void *ptr = nullptr;
+    if (cudaGetSymbolAddress(&ptr, g_error_word) != cudaSuccess || ptr == nullptr)
         return ATTN_ERR_CUDA;
-    std::lock_guard<std::mutex> lk(g_mu);
-    if (!g_err_ptr[dev]) {
-        void *ptr = nullptr;
-        if (cudaGetSymbolAddress(&ptr, g_error_word) != cudaSuccess) return ATTN_ERR_CUDA;
-        g_err_ptr[dev] = static_cast<unsigned *>(ptr);
-    }
-    *out = g_err_ptr[dev];
+    *out = static_cast<unsigned *>(ptr);
     return ATTN_OK;
 }
 
@@ -83,6 +75,13 @@ size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
 // GQA decode on the tensor cores (head_dim 128) with 2 or 4 partitions
 // merges them on chip (a cluster of P CTAs) and needs no workspace.
 bool merges_on_chip(int P, int head_dim) { return head_dim == 128 && (P == 2 || P == 4); }
+
+// A few query rows per sequence (head_dim 128, max_q_len * group <= 16)
+// fold onto the N side of the tensor-core decode kernel, next to the group's
+// heads, and keep its split-K; longer row runs take the tile kernel.
+bool folds_rows(int max_q_len, int head_dim, int group, int batch) {
+    return max_q_len > 1 && head_dim == 128 && max_q_len * group <= 16 && batch <= kGqaMaxBatch;
+}
 
 // Workspace layout for P partitions: ws_o | ws_m | ws_l, each 256-B aligned.
 size_t workspace_layout(int P, long long rows, int hq, int dv, size_t *off_m, size_t *off_l) {
@@ -239,18 +238,33 @@ int prefill_path(const void *q, const attn_kv_t *k, const attn_kv_t *v, const ui
 
 using namespace attn;
 
-extern "C" int attn_plan_partitions(int num_sms, int batch, int num_q_rows, int num_q_heads,
-                                    int num_kv_heads, int head_dim_v, int max_kv_len,
-                                    int requested, int *num_partitions,
-                                    size_t *workspace_bytes) {
+namespace attn {
+namespace {
+
+// The partition plan behind attn_plan_partitions and the automatic choice of
+// attn_decode (num_partitions 0).  The one place that decides which GQA
+// kernel a call with max_q_len rows per sequence takes: single rows and the
+// few-row fold run split-K on the decode kernel, longer row runs take the
+// tile kernel, which does not split (P = 1, no workspace).
+int plan_impl(int num_sms, int batch, int num_q_rows, int max_q_len, int num_q_heads,
+              int num_kv_heads, int head_dim_v, int max_kv_len, int requested,
+              int *num_partitions, size_t *workspace_bytes) {
     if (!num_partitions || !workspace_bytes) return ATTN_ERR_INVALID_ARG;
-    if (batch < 0 || num_q_rows < 0 || num_q_heads <= 0 || num_kv_heads <= 0 ||
+    if (batch < 0 || num_q_rows < 0 || max_q_len < 1 || num_q_heads <= 0 || num_kv_heads <= 0 ||
         head_dim_v <= 0 || max_kv_len < 0 || requested < ATTN_PARTITIONS_BALANCED)
         return ATTN_ERR_INVALID_ARG;
     if (num_q_heads % num_kv_heads) return ATTN_ERR_INVALID_ARG;
     if (requested > ATTN_MAX_PARTITIONS) return ATTN_ERR_INVALID_ARG;
     const bool mla_shape = num_kv_heads == 1 && head_dim_v == kMlaDimV;
     if (requested == ATTN_PARTITIONS_BALANCED && !mla_shape) return ATTN_ERR_INVALID_ARG;
+    if (!mla_shape && max_q_len > 1 &&
+        !folds_rows(max_q_len, head_dim_v, num_q_heads / num_kv_heads, batch)) {
+        // the tile kernel: every row run in one pass, no split-K
+        if (requested > 1) return ATTN_ERR_UNSUPPORTED;
+        *num_partitions = 1;
+        *workspace_bytes = 0;
+        return ATTN_OK;
+    }
     if (requested <= 0 && num_sms <= 0) {
         int dev = 0;
         if (cudaGetDevice(&dev) != cudaSuccess ||
@@ -298,7 +312,7 @@ extern "C" int attn_plan_partitions(int num_sms, int batch, int num_q_rows, int 
             const long long p_fill = ctas / units > 0 ? ctas / units : 1;
             const long long p_len = (static_cast<long long>(max_kv_len) + target - 1) / target;
             p = p_fill > p_len ? p_fill : p_len;
-        } else if (tc && num_q_rows > batch && units >= 2 * ctas) {
+        } else if (tc && max_q_len > 1 && units >= 2 * ctas) {
             // A few query rows per sequence fold onto 16 score columns.  With
             // two units per CTA or more the split buys little (the memory
             // streams are already spread over every SM) and costs a
@@ -306,7 +320,7 @@ extern "C" int attn_plan_partitions(int num_sms, int batch, int num_q_rows, int 
             // the folded items are long, and the many-item rule below (not
             // one wave of slices) keeps a ragged batch balanced.
             p = 1;
-        } else if (units < ctas && !(tc && num_q_rows > batch)) {
+        } else if (units < ctas && !(tc && max_q_len > 1)) {
             p = (ctas + units - 1) / units;
         } else {
             const long long p_fill = (4 * ctas + units - 1) / units;
@@ -343,6 +357,17 @@ extern "C" int attn_plan_partitions(int num_sms, int batch, int num_q_rows, int 
     return ATTN_OK;
 }
 
+}  // namespace
+}  // namespace attn
+
+extern "C" int attn_plan_partitions(int num_sms, int batch, int num_q_rows, int max_q_len,
+                                    int num_q_heads, int num_kv_heads, int head_dim_v,
+                                    int max_kv_len, int requested, int *num_partitions,
+                                    size_t *workspace_bytes) {
+    return plan_impl(num_sms, batch, num_q_rows, max_q_len, num_q_heads, num_kv_heads,
+                     head_dim_v, max_kv_len, requested, num_partitions, workspace_bytes);
+}
+
 extern "C" int attn_decode(const void *q, const attn_kv_t *k, const attn_kv_t *v,
                            const uint32_t *kv_len, const uint32_t *q_row_offsets, int batch,
                            int num_q_rows, int num_q_heads, int group, int head_dim,
@@ -353,16 +378,22 @@ extern "C" int attn_decode(const void *q, const attn_kv_t *k, const attn_kv_t *v
         max_q_len < 1)
         return ATTN_ERR_INVALID_ARG;
     if (num_q_heads % group) return ATTN_ERR_INVALID_ARG;
-    if (num_partitions < 1 || num_partitions > ATTN_MAX_PARTITIONS) return ATTN_ERR_INVALID_ARG;
+    if (num_partitions < 0 || num_partitions > ATTN_MAX_PARTITIONS) return ATTN_ERR_INVALID_ARG;
     if (!(scale == scale)) return ATTN_ERR_INVALID_ARG;
     if (!q_row_offsets && (num_q_rows != batch || max_q_len != 1)) return ATTN_ERR_INVALID_ARG;
     if (batch == 0 || num_q_rows == 0) return ATTN_OK;
     if (!q || !kv_len || !out) return ATTN_ERR_INVALID_ARG;
-    // A few rows per sequence (max_q_len * group <= 16, head_dim 128) fold
-    // onto the N side of the tensor-core decode kernel, split-K included;
-    // longer row runs take the tensor-core tile path (not split).
-    const bool fold = max_q_len > 1 && head_dim == 128 && max_q_len * group <= 16 &&
-                      batch <= kGqaMaxBatch;
+    if (num_partitions == 0) {
+        // automatic: the planner's choice for this shape on the current device
+        size_t planned = 0;
+        const int st = plan_impl(0, batch, num_q_rows, max_q_len, num_q_heads,
+                                 num_q_heads / group, head_dim, max_kv_len, 0, &num_partitions,
+                                 &planned);
+        if (st) return st;
+    }
+    // A few rows per sequence fold onto the N side of the tensor-core decode
+    // kernel, split-K included; longer row runs take the tile path (not split).
+    const bool fold = folds_rows(max_q_len, head_dim, group, batch);
     if (max_q_len > 1 && !fold) {
         if (num_partitions != 1) return ATTN_ERR_UNSUPPORTED;
         return prefill_path(q, k, v, kv_len, q_row_offsets, batch, num_q_rows, num_q_heads,

@@ -9,8 +9,6 @@
 // in a file-scope __device__ array, so the call itself allocates nothing.
 #include <cuda_runtime.h>
 
-#include <mutex>
-
 #include "attn_decode.h"
 
 namespace {
@@ -21,25 +19,16 @@ namespace {
 constexpr size_t kScratchBytes = size_t(32) << 20;
 static __device__ __align__(256) unsigned char g_scratch[kScratchBytes];
 
-constexpr int kMaxDevices = 64;
-std::mutex g_mu;
-void *g_scratch_ptr[kMaxDevices];
-
-// Device address of g_scratch on the current device.  In host code the name
-// g_scratch is only a host-side stand-in, so the address is looked up with
-// cudaGetSymbolAddress, once per device, with that device current.
+// Device address of g_scratch in the current device's context.  In host
+// code the name g_scratch is only a host-side stand-in, so the address is
+// looked up with cudaGetSymbolAddress, with that device current.  It is
+// looked up on every call (a host-side table lookup), so a device reset or
+// a new primary context never leaves a stale address behind.
 int scratch_address(void **out) {
-    int dev = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices)
+    void *ptr = nullptr;
+    if (cudaGetSymbolAddress(&ptr, g_scratch) != cudaSuccess || ptr == nullptr)
         return ATTN_ERR_CUDA;
-    std::lock_guard<std::mutex> lk(g_mu);
-    if (!g_scratch_ptr[dev]) {
-        void *ptr = nullptr;
-        if (cudaGetSymbolAddress(&ptr, g_scratch) != cudaSuccess || ptr == nullptr)
-            return ATTN_ERR_CUDA;
-        g_scratch_ptr[dev] = ptr;
-    }
-    *out = g_scratch_ptr[dev];
+    *out = ptr;
     return ATTN_OK;
 }
 
@@ -53,23 +42,22 @@ extern "C" int attn_decode_noalloc(const void *q, const attn_kv_t *k, const attn
                                    float *lse, attn_stream_t stream) {
     if (num_partitions < 0 || group <= 0 || num_q_heads <= 0 || num_q_heads % group)
         return ATTN_ERR_INVALID_ARG;
-    int P = num_partitions;
+    // The planner routes the call exactly as attn_decode does: single rows and
+    // the few-row fold keep split-K (a non-zero P is taken as given, 0 plans
+    // it), and longer row runs take the tile kernel, which does not split
+    // (there a P above 1 is rejected).  It only does arithmetic (and, for
+    // P = 0, reads the SM count); it allocates nothing.
+    int P = 0;
     size_t need = 0;
-    if (max_q_len > 1) {
-        P = 1;  // the multi-row tile path does not split
-    } else {
-        // The planner only does arithmetic (and, for P = 0, reads the SM
-        // count); it allocates nothing.
-        const int st = attn_plan_partitions(0, batch, num_q_rows, num_q_heads,
-                                            num_q_heads / group, head_dim, max_kv_len, P, &P,
-                                            &need);
-        if (st != ATTN_OK) return st;
-    }
+    const int st = attn_plan_partitions(0, batch, num_q_rows, max_q_len, num_q_heads,
+                                        num_q_heads / group, head_dim, max_kv_len,
+                                        num_partitions, &P, &need);
+    if (st != ATTN_OK) return st;
     if (need > kScratchBytes) return ATTN_ERR_WORKSPACE;  // beyond the fixed scratch
     void *scratch = nullptr;
     if (need > 0) {
-        const int st = scratch_address(&scratch);
-        if (st != ATTN_OK) return st;
+        const int sa = scratch_address(&scratch);
+        if (sa != ATTN_OK) return sa;
     }
     return attn_decode(q, k, v, kv_len, q_row_offsets, batch, num_q_rows, num_q_heads, group,
                        head_dim, max_q_len, max_kv_len, scale, sink, causal, P, scratch, need,

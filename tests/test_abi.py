@@ -91,7 +91,7 @@ def test_decode_rejects_bad_arguments_before_launch(attn):
     assert call_decode(attn, group=0) == E.ATTN_ERR_INVALID_ARG
     assert call_decode(attn, hq=48, group=16) == E.ATTN_ERR_UNSUPPORTED
     assert call_decode(attn, d=96) == E.ATTN_ERR_UNSUPPORTED
-    assert call_decode(attn, P=0) == E.ATTN_ERR_INVALID_ARG
+    assert call_decode(attn, P=-1) == E.ATTN_ERR_INVALID_ARG
     assert call_decode(attn, P=E.ATTN_MAX_PARTITIONS + 1) == E.ATTN_ERR_INVALID_ARG
     assert call_decode(attn, scale=float("nan")) == E.ATTN_ERR_INVALID_ARG
     assert call_decode(attn, max_kv_len=-1) == E.ATTN_ERR_INVALID_ARG
@@ -261,11 +261,11 @@ def test_planner_formulas(attn):
     P, _ = attn.attn_plan_partitions(1, 1, 32, 8, 128, 20, 0, num_sms=152)
     assert P == 1                                     # one tile of keys cannot split
     # a few query rows per sequence (the 16-column fold): long items
-    P, _ = attn.attn_plan_partitions(64, 160, 32, 8, 128, 8192, 0, num_sms=152)
+    P, _ = attn.attn_plan_partitions(64, 160, 32, 8, 128, 8192, 0, num_sms=152, max_q_len=4)
     assert P == 1                                     # 512 units, >= 2 per CTA
-    P, ws = attn.attn_plan_partitions(16, 40, 32, 8, 128, 8192, 0, num_sms=152)
+    P, ws = attn.attn_plan_partitions(16, 40, 32, 8, 128, 8192, 0, num_sms=152, max_q_len=4)
     assert P == 8 and ws > 0                          # 128 units: slices of <= 1024 keys
-    P, _ = attn.attn_plan_partitions(2, 8, 32, 8, 128, 8192, 0, num_sms=152)
+    P, _ = attn.attn_plan_partitions(2, 8, 32, 8, 128, 8192, 0, num_sms=152, max_q_len=4)
     assert P == 38                                    # 16 units: >= 4 items per CTA
     P, _ = attn.attn_plan_partitions(4, 4, 32, 8, 128, 0, 0, num_sms=152)
     assert P == 1
@@ -278,6 +278,69 @@ def test_planner_formulas(attn):
     with pytest.raises(attn.AttnError):
         attn.attn_plan_partitions(2, 2, 32, 8, 128, 100, attn.ATTN_MAX_PARTITIONS + 1,
                                   num_sms=152)
+
+
+def test_planner_routes_multi_row_calls(attn):
+    """The planner is the one place that routes a multi-row GQA call: the
+    few-row fold (head_dim 128, max_q_len * group <= 16, batch <= 2048) keeps
+    split-K on the decode kernel; longer row runs take the tile kernel, which
+    does not split (P = 1, no workspace, a larger request rejected)."""
+    plan = attn.attn_plan_partitions
+    # folded: a request is honoured verbatim, as for single rows
+    for q_len, hq, hkv in ((4, 32, 8), (2, 64, 8), (16, 8, 8)):
+        assert plan(4, 4 * q_len, hq, hkv, 128, 4096, 3, num_sms=152, max_q_len=q_len)[0] == 3
+        assert plan(4, 4 * q_len, hq, hkv, 128, 4096, 2, num_sms=152,
+                    max_q_len=q_len) == (2, 0)             # merged on chip
+    # not folded: rows x group above 16, head_dim 64, or more than 2048 sequences
+    for batch, q_len, hq, hkv, d in ((16, 4096, 32, 8, 128), (4, 5, 32, 8, 128),
+                                     (4, 3, 64, 8, 128), (4, 2, 16, 8, 64),
+                                     (2049, 2, 32, 8, 128)):
+        for req in (0, 1):
+            assert plan(batch, batch * q_len, hq, hkv, d, 8192, req, num_sms=152,
+                        max_q_len=q_len) == (1, 0)
+        with pytest.raises(attn.AttnError) as e:
+            plan(batch, batch * q_len, hq, hkv, d, 8192, 2, num_sms=152, max_q_len=q_len)
+        assert e.value.status == attn.ATTN_ERR_UNSUPPORTED
+    # MLA shapes ignore max_q_len (draft rows plan per query row)
+    assert plan(32, 64, 128, 1, 512, 32768, 4, num_sms=152, max_q_len=2) == \
+        plan(32, 64, 128, 1, 512, 32768, 4, num_sms=152, max_q_len=1)
+    with pytest.raises(attn.AttnError) as e:
+        plan(4, 4, 32, 8, 128, 100, 0, num_sms=152, max_q_len=0)
+    assert e.value.status == attn.ATTN_ERR_INVALID_ARG
+
+
+def call_noalloc(attn, k=None, v=None, **over):
+    args = dict(q=0x30000, kv_len=0x40000, offs=None, batch=2, rows=None, hq=32, group=4,
+                d=128, max_q_len=1, max_kv_len=500, scale=0.088, sink=None, causal=0, P=1,
+                out=0x50000, lse=None)
+    args.update(over)
+    if args["rows"] is None:
+        args["rows"] = args["batch"]
+    k = k or kv(attn)
+    v = v or kv(attn)
+    return attn.lib().attn_decode_noalloc(args["q"], ctypes.byref(k), ctypes.byref(v),
+                                          args["kv_len"], args["offs"], args["batch"],
+                                          args["rows"], args["hq"], args["group"], args["d"],
+                                          args["max_q_len"], args["max_kv_len"], args["scale"],
+                                          args["sink"], args["causal"], args["P"], args["out"],
+                                          args["lse"], None)
+
+
+def test_noalloc_routes_and_rejects_as_attn_decode(attn):
+    """attn_decode_noalloc plans through the same planner: a count attn_decode
+    rejects is rejected here too, before anything is launched."""
+    E = attn
+    assert call_noalloc(attn, P=-1) == E.ATTN_ERR_INVALID_ARG
+    assert call_noalloc(attn, P=E.ATTN_MAX_PARTITIONS + 1) == E.ATTN_ERR_INVALID_ARG
+    assert call_decode(attn, P=E.ATTN_MAX_PARTITIONS + 1) == E.ATTN_ERR_INVALID_ARG
+    # the tile kernel (rows x group above 16) does not split
+    assert call_noalloc(attn, offs=0x70000, rows=40, max_q_len=30, P=2) == E.ATTN_ERR_UNSUPPORTED
+    assert call_decode(attn, offs=0x70000, rows=40, max_q_len=30, P=2) == E.ATTN_ERR_UNSUPPORTED
+    # 64 partitions x 64 rows x 32 heads x 128 channels x 4 B = 64 MiB > 32 MiB of scratch
+    assert call_noalloc(attn, batch=64, P=64) == E.ATTN_ERR_WORKSPACE
+    # argument checks of attn_decode still apply
+    assert call_noalloc(attn, q=None) == E.ATTN_ERR_INVALID_ARG
+    assert call_noalloc(attn, hq=30) == E.ATTN_ERR_INVALID_ARG
 
 
 def test_product_package_does_not_import_the_oracle():
