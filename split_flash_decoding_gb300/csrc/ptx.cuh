@@ -141,6 +141,16 @@ __device__ __forceinline__ float fast_log2(float x) {
 __device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }
 __device__ __forceinline__ float bf16_hi(uint32_t w) { return __uint_as_float(w & 0xffff0000u); }
 
+// acc.x += low bf16 of w, acc.y += high bf16 of w, each widened exactly and
+// added in fp32 with one rounding (the mixed-precision add: one instruction
+// per half, no separate unpacking).
+__device__ __forceinline__ void add_bf16x2_f32(float2 &acc, uint32_t w) {
+    asm("{\n\t.reg .b16 lo, hi;\n\tmov.b32 {lo, hi}, %2;\n\t"
+        "add.rn.f32.bf16 %0, lo, %0;\n\tadd.rn.f32.bf16 %1, hi, %1;\n\t}"
+        : "+f"(acc.x), "+f"(acc.y)
+        : "r"(w));
+}
+
 __device__ __forceinline__ float2 bf16x2_to_float2(uint32_t w) {
     return make_float2(bf16_lo(w), bf16_hi(w));
 }

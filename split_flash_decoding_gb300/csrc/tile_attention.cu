@@ -14,7 +14,8 @@
 // TMEM accumulator, online softmax by eight warps (two per row: warps w and
 // w+4 share TMEM lanes 32(w%4).. and split the 128 keys; causal and length
 // masks applied per element; the two halves' row maxima combined through
-// shared memory), P (bf16 pairs) into TMEM, then O += P V (M=128, N=128,
+// shared memory, synchronising only the two warps of a row quarter, which
+// share an SM sub-partition), P (bf16 pairs) into TMEM, then O += P V (M=128, N=128,
 // K=128) with P as the A operand from TMEM.  The running max is lazy: it is
 // raised, and O rescaled, only when a tile's max exceeds it by more than 8
 // (base 2).  No split-K: each CTA covers all keys its rows can see.
@@ -40,7 +41,7 @@ constexpr int kBoxBytes = 128 * 128;         // 128 rows x 128 B (64 channels)
 constexpr int kTileBytes = 2 * kBoxBytes;    // 128 rows x 128 channels
 constexpr int kThreads = 352;
 constexpr int kSoftmaxThreads = 256;         // warps 0-7
-constexpr int kBarSoftmax = 1;               // named barrier of the softmax warps
+constexpr int kBarPair = 2;                  // named barriers 2..5: the two warps of a row quarter
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kTmemS = 0;               // S buffers at 0 and 128
 constexpr uint32_t kTmemO = 256;
@@ -313,10 +314,10 @@ tile_attention_kernel(const __grid_constant__ TileParams p) {
                     }
                 }
             }
-            // ---- row max over both halves ------------------------------------
-            named_sync(kBarSoftmax, kSoftmaxThreads);   // the last tile's reads are done
+            // ---- row max over both halves (warps w and w + 4 only) --------------
+            named_sync(kBarPair + (warp & 3), 64);   // the partner read the last tile's
             red[half * 128 + r] = mloc;
-            named_sync(kBarSoftmax, kSoftmaxThreads);
+            named_sync(kBarPair + (warp & 3), 64);
             const float mt = fmaxf(mloc, red[(half ^ 1) * 128 + r]);
             if (!ok) continue;
 
@@ -349,7 +350,7 @@ tile_attention_kernel(const __grid_constant__ TileParams p) {
                 const uint32_t w = pack_bf16x2(p0, p1);
                 pk[j] = __uint_as_float(w);
                 rs[j & 1] = __fadd2_rn(rs[j & 1], make_float2(p0, p1));
-                rr[j & 1] = __fadd2_rn(rr[j & 1], make_float2(bf16_lo(w), bf16_hi(w)));
+                add_bf16x2_f32(rr[j & 1], w);
             }
             const float rowsum = (rs[0].x + rs[1].x) + (rs[0].y + rs[1].y);
             const float rowsum_r = (rr[0].x + rr[1].x) + (rr[0].y + rr[1].y);
@@ -407,10 +408,10 @@ tile_attention_kernel(const __grid_constant__ TileParams p) {
         // Row sums of the two halves (same m_ref), through the Q buffer, which
         // no MMA reads any more.
         float *sums = reinterpret_cast<float *>(smem + Smem::q);
-        named_sync(kBarSoftmax, kSoftmaxThreads);
+        named_sync(kBarPair + (warp & 3), 64);
         sums[half * 256 + r] = l;
         sums[half * 256 + 128 + r] = l_r;
-        named_sync(kBarSoftmax, kSoftmaxThreads);
+        named_sync(kBarPair + (warp & 3), 64);
         l += sums[(half ^ 1) * 256 + r];
         l_r += sums[(half ^ 1) * 256 + 128 + r];
         const int h = kvh * G + (r % G);

@@ -15,8 +15,9 @@ element (error_bound below) from the arithmetic every tensor-core kernel
 here shares:
 
 * Each weight p_j = 2^(s_j - m) enters the P.V product rounded to bf16
-  (relative error at most u = 2^-8), after an approximate exp2 (at most
-  2^-22 relative) of a score carrying its own fp32 error.  Output and
+  (relative error at most u = 2^-8), after the approximate exp2 of the
+  special-function unit (at most 2^-22 relative) of a score carrying its own
+  fp32 error.  Output and
   partials are normalised by the sum of the weights actually multiplied, so
   the output is a convex combination with perturbed weights and its error is
   sum_j d_j (v_j - out) / Z (d_j the weight errors): at most

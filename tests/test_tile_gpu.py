@@ -24,11 +24,25 @@ def attn():
     assert a.attn_device_error_flags(clear=True) == 0
 
 
-def tile_workload(q_lens, prefix, hq=8, hkv=2, page_size=16, seed=0, causal=True, sink=False):
+def tile_workload(q_lens, prefix, hq=8, hkv=2, page_size=16, seed=0, causal=True, sink=False,
+                  scale=None):
     kv_lens = [p + n for p, n in zip(prefix, q_lens)]
     return W.make_workload("tile", batch=len(q_lens), num_q_heads=hq, num_kv_heads=hkv,
                            dim_qk=128, kv_lens=kv_lens, page_size=page_size, seed=seed,
-                           device=DEV, q_lens=q_lens, causal=causal, sink=sink)
+                           device=DEV, q_lens=q_lens, causal=causal, sink=sink, scale=scale)
+
+
+def grow_keys(w, per_token):
+    """Scale the K row of logical token t of every sequence by 1 + t * per_token
+    (through the page table), so scores grow along the sequence."""
+    ps = w.k_cache.shape[1]
+    flat = w.k_cache.view(-1, w.k_cache.shape[2], w.k_cache.shape[3])
+    pt = w.page_table.cpu()
+    for b, L in enumerate(w.kv_len_host):
+        t = torch.arange(L)
+        rows = (pt[b, t // ps].long() * ps + t % ps).to(DEV)
+        f = (1.0 + t.float() * per_token).to(DEV)[:, None, None]
+        flat[rows] = (flat[rows].float() * f).to(torch.bfloat16)
 
 
 def run(attn, w, sink="workload"):
@@ -48,6 +62,20 @@ def test_mixed_rows_match_oracle(attn, causal):
     out, lse = run(attn, w)
     ref_o, ref_l = oracle_result(w)
     assert_close(out, lse, ref_o, ref_l, f"tile causal={causal}")
+
+
+@pytest.mark.parametrize("scale", [4.0, 0.7, -0.3])
+def test_scores_far_above_the_reference(attn, scale):
+    """Keys whose scores grow along the sequence and large (or negative)
+    scales: later tiles hold keys tens to hundreds of base-2 units above the
+    reference set by earlier ones, so rows leave the weight range, take the
+    exact tile max and are redone, many times per row; the first tile of a
+    row always sets its reference that way."""
+    w = tile_workload([1, 37, 300, 129], [0, 500, 60, 900], seed=35, scale=scale, sink=True)
+    grow_keys(w, 1.0 / 64)
+    out, lse = run(attn, w)
+    ref_o, ref_l = oracle_result(w)
+    assert_close(out, lse, ref_o, ref_l, f"tile growing keys scale={scale}")
 
 
 @pytest.mark.parametrize("hq,hkv", [(8, 8), (8, 4), (16, 4), (32, 4)])
