@@ -68,9 +68,8 @@ def test_mixed_rows_match_oracle(attn, causal):
 def test_scores_far_above_the_reference(attn, scale):
     """Keys whose scores grow along the sequence and large (or negative)
     scales: later tiles hold keys tens to hundreds of base-2 units above the
-    reference set by earlier ones, so rows leave the weight range, take the
-    exact tile max and are redone, many times per row; the first tile of a
-    row always sets its reference that way."""
+    running maximum of earlier ones, so the maximum is raised and O rescaled
+    many times per row."""
     w = tile_workload([1, 37, 300, 129], [0, 500, 60, 900], seed=35, scale=scale, sink=True)
     grow_keys(w, 1.0 / 64)
     out, lse = run(attn, w)
