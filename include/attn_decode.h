@@ -58,6 +58,9 @@ enum {
 #define ATTN_MAX_PARTITIONS 1024
 /* attn_plan_partitions request: the balanced MLA split (num_partitions 0) */
 #define ATTN_PARTITIONS_BALANCED (-1)
+/* attn_plan_partitions request and attn_decode num_partitions on the tile
+ * path: two Q tiles per CTA pair sharing each K/V tile */
+#define ATTN_PARTITIONS_TILE_PAIR (-2)
 
 /*
  * One K or V cache operand (the KV operand type carries the element type and
@@ -106,18 +109,22 @@ typedef struct attn_kv {
  *                 the GQA kernel exactly as attn_decode does: a few rows
  *                 (head_dim_v 128, max_q_len * group <= 16, batch <= 2048)
  *                 fold onto the split-K decode kernel; longer row runs take
- *                 the tile kernel, which does not split, so the plan is P = 1
- *                 with workspace 0 (a request above 1 returns
- *                 ATTN_ERR_UNSUPPORTED).  MLA ignores it.
+ *                 the tile kernels, which do not split: the plan is P = 1
+ *                 (one Q tile per CTA, for requests 0 and 1) or, for the
+ *                 request ATTN_PARTITIONS_TILE_PAIR, that value (two Q tiles
+ *                 per CTA pair), with workspace 0; a request above 1 returns
+ *                 ATTN_ERR_UNSUPPORTED.  MLA ignores it.
  *   num_q_heads, num_kv_heads   heads (num_kv_heads = 1 for MLA).
  *   head_dim_v    output channels (128 for GQA d128, 512 for MLA).
  *   max_kv_len    host upper bound of every kv_len[b].
  *   requested     0 = automatic; > 0 = use exactly this many partitions;
  *                 ATTN_PARTITIONS_BALANCED = the balanced split (MLA shapes
- *                 only: num_kv_heads 1, head_dim_v 512; num_partitions out 0;
- *                 any other shape or negative value: ATTN_ERR_INVALID_ARG).
- *   num_partitions  out: partitions P (1 <= P <= ATTN_MAX_PARTITIONS), or 0
- *                 for the balanced MLA split.
+ *                 only: num_kv_heads 1, head_dim_v 512; num_partitions out 0);
+ *                 ATTN_PARTITIONS_TILE_PAIR = two Q tiles per CTA pair (the
+ *                 tile path only); any other shape or negative value:
+ *                 ATTN_ERR_INVALID_ARG.
+ *   num_partitions  out: partitions P (1 <= P <= ATTN_MAX_PARTITIONS), 0 for
+ *                 the balanced MLA split, or ATTN_PARTITIONS_TILE_PAIR.
  *   workspace_bytes out: workspace size attn_decode / attn_mla_decode need
  *                 for this P (0 when P == 1).
  *
@@ -177,11 +184,13 @@ int attn_plan_partitions(int num_sms, int batch, int num_q_rows, int max_q_len,
  *              tokens being verified) stay on that kernel: the rows of a
  *              sequence fold onto the tensor-core N side next to the group's
  *              heads and share every K/V tile, split-K included.  More rows
- *              select the tensor-core tile kernel, which takes every sequence
+ *              select the tensor-core tile path, which takes every sequence
  *              of the batch, single-token ones included (that page handles
  *              one-token decode as the degenerate case of prefill rather
  *              than a route of its own, mha_sm100_dispatch, summary), and does
- *              not split.
+ *              not split: one 128-row Q tile per CTA, or two adjacent Q tiles
+ *              per CTA pair sharing each K/V tile through the pair's MMA (the
+ *              1Q and 2Q configurations that page chooses between).
  *   max_kv_len host upper bound of kv_len ("max_cache_valid_length_arg").
  *   scale      multiplies Q.K' before the softmax.
  *   sink       device fp32 [num_q_heads] attention-sink logits, or NULL.
@@ -194,7 +203,14 @@ int attn_plan_partitions(int num_sms, int batch, int num_q_rows, int max_q_len,
  *              the planner's automatic choice on the current device (the
  *              same call as attn_plan_partitions with num_sms 0 and
  *              requested 0: size the workspace with that call); must be 0 or
- *              1 on the tile kernel (max_q_len > 1 beyond the few-row fold).
+ *              1 on the tile path (max_q_len > 1 beyond the few-row fold),
+ *              both one Q tile per CTA, or ATTN_PARTITIONS_TILE_PAIR there:
+ *              two adjacent Q tiles per CTA pair.  The automatic choice (0)
+ *              is one tile per CTA, measured faster than the pair on every
+ *              shape tried; the pages choose between the two by occupancy
+ *              and prompt length and make a non-zero override force the
+ *              smaller tile (mha_sm100_dispatch, summary and Args:
+ *              num_partitions_override).
  *   workspace  device, 256-byte aligned, >= the planner's workspace_bytes
  *              for this P; may be NULL when P == 1, and with head_dim 128
  *              when P is 2 or 4 (those merge on chip).  Contents on entry

@@ -26,6 +26,7 @@ ATTN_ERR_CUDA = 4
 ATTN_ERR_DEVICE = 5
 ATTN_MAX_PARTITIONS = 1024
 ATTN_PARTITIONS_BALANCED = -1   # the balanced MLA split (planner request; num_partitions 0)
+ATTN_PARTITIONS_TILE_PAIR = -2  # the tile path with two Q tiles per CTA pair
 
 _STATUS_NAMES = {
     ATTN_ERR_INVALID_ARG: "ATTN_ERR_INVALID_ARG",

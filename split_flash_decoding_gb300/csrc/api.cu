@@ -163,7 +163,8 @@ __global__ void selftest_wait_kernel(unsigned *err) {
 int prefill_path(const void *q, const attn_kv_t *k, const attn_kv_t *v, const uint32_t *kv_len,
                  const uint32_t *q_row_offsets, int batch, int num_q_rows, int num_q_heads,
                  int group, int head_dim, int max_q_len, int max_kv_len, float scale,
-                 const float *sink, int causal, void *out, float *lse, attn_stream_t stream);
+                 const float *sink, int causal, int num_partitions, void *out, float *lse,
+                 attn_stream_t stream);
 
 }  // namespace
 }  // namespace attn
@@ -175,7 +176,8 @@ namespace {
 int prefill_path(const void *q, const attn_kv_t *k, const attn_kv_t *v, const uint32_t *kv_len,
                  const uint32_t *q_row_offsets, int batch, int num_q_rows, int num_q_heads,
                  int group, int head_dim, int max_q_len, int max_kv_len, float scale,
-                 const float *sink, int causal, void *out, float *lse, attn_stream_t stream) {
+                 const float *sink, int causal, int num_partitions, void *out, float *lse,
+                 attn_stream_t stream) {
     if (head_dim != 128) return ATTN_ERR_UNSUPPORTED;
     if (group != 1 && group != 2 && group != 4 && group != 8) return ATTN_ERR_UNSUPPORTED;
     if (reinterpret_cast<uintptr_t>(out) % 16 || reinterpret_cast<uintptr_t>(q) % 16)
@@ -189,13 +191,20 @@ int prefill_path(const void *q, const attn_kv_t *k, const attn_kv_t *v, const ui
         k->max_pages != v->max_pages || k->num_pages != v->num_pages)
         return ATTN_ERR_UNSUPPORTED;
 
+    // num_partitions 0 (automatic) and 1 take one Q tile per CTA, measured
+    // faster than two Q tiles per CTA pair on every shape tried (1.43-1.51x:
+    // the pair runs each tile in lockstep across two SMs);
+    // ATTN_PARTITIONS_TILE_PAIR asks for the pair.
+    const bool pair = num_partitions == ATTN_PARTITIONS_TILE_PAIR;
     TileParams p;
     std::memset(&p, 0, sizeof(p));
-    p.box_rows = k->page_table ? (k->page_size < kTileKeys ? k->page_size : kTileKeys)
-                               : kTileKeys;
+    const int ps = k->page_table ? k->page_size : kTileKeys;
+    p.box_rows = ps < kTileKeys ? ps : kTileKeys;
+    p.box_rows_v = p.box_rows;
+    if (pair) p.box_rows = ps < 64 ? ps : 64;   // the K half of a pair: 64 keys
     st = encode_kv_map(&p.k_map, *k, head_dim, hkv, p.box_rows);
     if (st) return st;
-    st = encode_kv_map(&p.v_map, *v, head_dim, hkv, p.box_rows);
+    st = encode_kv_map(&p.v_map, *v, head_dim, hkv, p.box_rows_v);
     if (st) return st;
     const int tokens = kTileRows / group;
     {
@@ -230,7 +239,8 @@ int prefill_path(const void *q, const attn_kv_t *k, const attn_kv_t *v, const ui
     p.causal = causal ? 1 : 0;
     p.tiles_per_seq = (max_q_len + tokens - 1) / tokens;
     p.qk_scale_log2 = scale * 1.4426950408889634f;
-    return map_cuda(launch_tile_attention(p, reinterpret_cast<cudaStream_t>(stream)));
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    return map_cuda(pair ? launch_tile_attention_pair(p, s) : launch_tile_attention(p, s));
 }
 
 }  // namespace
@@ -251,17 +261,20 @@ int plan_impl(int num_sms, int batch, int num_q_rows, int max_q_len, int num_q_h
               int *num_partitions, size_t *workspace_bytes) {
     if (!num_partitions || !workspace_bytes) return ATTN_ERR_INVALID_ARG;
     if (batch < 0 || num_q_rows < 0 || max_q_len < 1 || num_q_heads <= 0 || num_kv_heads <= 0 ||
-        head_dim_v <= 0 || max_kv_len < 0 || requested < ATTN_PARTITIONS_BALANCED)
+        head_dim_v <= 0 || max_kv_len < 0 || requested < ATTN_PARTITIONS_TILE_PAIR)
         return ATTN_ERR_INVALID_ARG;
     if (num_q_heads % num_kv_heads) return ATTN_ERR_INVALID_ARG;
     if (requested > ATTN_MAX_PARTITIONS) return ATTN_ERR_INVALID_ARG;
     const bool mla_shape = num_kv_heads == 1 && head_dim_v == kMlaDimV;
     if (requested == ATTN_PARTITIONS_BALANCED && !mla_shape) return ATTN_ERR_INVALID_ARG;
-    if (!mla_shape && max_q_len > 1 &&
-        !folds_rows(max_q_len, head_dim_v, num_q_heads / num_kv_heads, batch)) {
-        // the tile kernel: every row run in one pass, no split-K
+    const bool tile_path = !mla_shape && max_q_len > 1 &&
+                           !folds_rows(max_q_len, head_dim_v, num_q_heads / num_kv_heads, batch);
+    if (requested == ATTN_PARTITIONS_TILE_PAIR && !tile_path) return ATTN_ERR_INVALID_ARG;
+    if (tile_path) {
+        // the tile kernels: every row run in one pass, no split-K; one Q tile
+        // per CTA unless two per CTA pair are asked for
         if (requested > 1) return ATTN_ERR_UNSUPPORTED;
-        *num_partitions = 1;
+        *num_partitions = requested == ATTN_PARTITIONS_TILE_PAIR ? requested : 1;
         *workspace_bytes = 0;
         return ATTN_OK;
     }
@@ -378,11 +391,24 @@ extern "C" int attn_decode(const void *q, const attn_kv_t *k, const attn_kv_t *v
         max_q_len < 1)
         return ATTN_ERR_INVALID_ARG;
     if (num_q_heads % group) return ATTN_ERR_INVALID_ARG;
-    if (num_partitions < 0 || num_partitions > ATTN_MAX_PARTITIONS) return ATTN_ERR_INVALID_ARG;
+    if ((num_partitions < 0 && num_partitions != ATTN_PARTITIONS_TILE_PAIR) ||
+        num_partitions > ATTN_MAX_PARTITIONS)
+        return ATTN_ERR_INVALID_ARG;
     if (!(scale == scale)) return ATTN_ERR_INVALID_ARG;
     if (!q_row_offsets && (num_q_rows != batch || max_q_len != 1)) return ATTN_ERR_INVALID_ARG;
     if (batch == 0 || num_q_rows == 0) return ATTN_OK;
     if (!q || !kv_len || !out) return ATTN_ERR_INVALID_ARG;
+    // A few rows per sequence fold onto the N side of the tensor-core decode
+    // kernel, split-K included; longer row runs take the tile path (not split).
+    const bool fold = folds_rows(max_q_len, head_dim, group, batch);
+    if (num_partitions == ATTN_PARTITIONS_TILE_PAIR && !(max_q_len > 1 && !fold))
+        return ATTN_ERR_INVALID_ARG;   // the pair of Q tiles is a tile-path request
+    if (max_q_len > 1 && !fold) {
+        if (num_partitions > 1) return ATTN_ERR_UNSUPPORTED;
+        return prefill_path(q, k, v, kv_len, q_row_offsets, batch, num_q_rows, num_q_heads,
+                            group, head_dim, max_q_len, max_kv_len, scale, sink, causal,
+                            num_partitions, out, lse, stream);
+    }
     if (num_partitions == 0) {
         // automatic: the planner's choice for this shape on the current device
         size_t planned = 0;
@@ -390,15 +416,6 @@ extern "C" int attn_decode(const void *q, const attn_kv_t *k, const attn_kv_t *v
                                  num_q_heads / group, head_dim, max_kv_len, 0, &num_partitions,
                                  &planned);
         if (st) return st;
-    }
-    // A few rows per sequence fold onto the N side of the tensor-core decode
-    // kernel, split-K included; longer row runs take the tile path (not split).
-    const bool fold = folds_rows(max_q_len, head_dim, group, batch);
-    if (max_q_len > 1 && !fold) {
-        if (num_partitions != 1) return ATTN_ERR_UNSUPPORTED;
-        return prefill_path(q, k, v, kv_len, q_row_offsets, batch, num_q_rows, num_q_heads,
-                            group, head_dim, max_q_len, max_kv_len, scale, sink, causal, out,
-                            lse, stream);
     }
     if (!fold && q_row_offsets && num_q_rows != batch) return ATTN_ERR_INVALID_ARG;
     if (batch > kGqaMaxBatch) return ATTN_ERR_UNSUPPORTED;

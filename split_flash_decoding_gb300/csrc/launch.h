@@ -105,8 +105,9 @@ struct TileParams {
     unsigned *err;
     int batch, num_q_rows, num_q_heads, group;
     int max_pages, page_size, num_pages, box_rows;
+    int box_rows_v;               // two-Q-tile kernel: tokens per V box (K boxes: box_rows)
     int causal;
-    int tiles_per_seq;            // grid.x = ceil(max_q_len / (128 / group))
+    int tiles_per_seq;            // Q tiles of the longest sequence: ceil(max_q_len / (128 / group))
     float qk_scale_log2;
 };
 
@@ -135,6 +136,9 @@ cudaError_t launch_mla_plan(const MlaParams &p, cudaStream_t stream);
 // Two-CTA MLA clusters that run at once on num_sms SMs (at most num_sms / 2).
 int mla_cluster_slots(int num_sms, bool sparse);
 cudaError_t launch_tile_attention(const TileParams &p, cudaStream_t stream);
+// Two adjacent Q tiles per CTA pair sharing each K/V tile (K boxes of
+// min(64, page size) tokens, V boxes of min(128, page size)).
+cudaError_t launch_tile_attention_pair(const TileParams &p, cudaStream_t stream);
 cudaError_t launch_splitk_reduce(const ReduceParams &p, cudaStream_t stream, bool pdl);
 
 }  // namespace attn

@@ -76,13 +76,6 @@ enum Bar {
     kNumBars = kODone + 1
 };
 
-// max of three (one instruction on this architecture)
-__device__ __forceinline__ float fmax3(float a, float b, float c) {
-    float r;
-    asm("max.f32 %0, %1, %2, %3;" : "=f"(r) : "f"(a), "f"(b), "f"(c));
-    return r;
-}
-
 __global__ void __launch_bounds__(kThreads, 1)
 tile_attention_kernel(const __grid_constant__ TileParams p) {
     extern __shared__ uint8_t smem_raw[];

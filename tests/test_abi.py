@@ -283,8 +283,9 @@ def test_planner_formulas(attn):
 def test_planner_routes_multi_row_calls(attn):
     """The planner is the one place that routes a multi-row GQA call: the
     few-row fold (head_dim 128, max_q_len * group <= 16, batch <= 2048) keeps
-    split-K on the decode kernel; longer row runs take the tile kernel, which
-    does not split (P = 1, no workspace, a larger request rejected)."""
+    split-K on the decode kernel; longer row runs take the tile path, which
+    does not split (P = 1, or the two-Q-tile request; no workspace; a larger
+    request rejected)."""
     plan = attn.attn_plan_partitions
     # folded: a request is honoured verbatim, as for single rows
     for q_len, hq, hkv in ((4, 32, 8), (2, 64, 8), (16, 8, 8)):
@@ -295,12 +296,21 @@ def test_planner_routes_multi_row_calls(attn):
     for batch, q_len, hq, hkv, d in ((16, 4096, 32, 8, 128), (4, 5, 32, 8, 128),
                                      (4, 3, 64, 8, 128), (4, 2, 16, 8, 64),
                                      (2049, 2, 32, 8, 128)):
-        for req in (0, 1):
+        for req in (0, 1):     # one Q tile per CTA
             assert plan(batch, batch * q_len, hq, hkv, d, 8192, req, num_sms=152,
                         max_q_len=q_len) == (1, 0)
+        pair = attn.ATTN_PARTITIONS_TILE_PAIR
+        assert plan(batch, batch * q_len, hq, hkv, d, 8192, pair, num_sms=152,
+                    max_q_len=q_len) == (pair, 0)
         with pytest.raises(attn.AttnError) as e:
             plan(batch, batch * q_len, hq, hkv, d, 8192, 2, num_sms=152, max_q_len=q_len)
         assert e.value.status == attn.ATTN_ERR_UNSUPPORTED
+    # the pair of Q tiles is a tile-path request only
+    for batch, q_len, hq, hkv in ((4, 1, 32, 8), (4, 4, 32, 8), (4, 2, 128, 1)):
+        with pytest.raises(attn.AttnError) as e:
+            plan(batch, batch * q_len, hq, hkv, 512 if hkv == 1 else 128, 8192,
+                 attn.ATTN_PARTITIONS_TILE_PAIR, num_sms=152, max_q_len=q_len)
+        assert e.value.status == attn.ATTN_ERR_INVALID_ARG
     # MLA shapes ignore max_q_len (draft rows plan per query row)
     assert plan(32, 64, 128, 1, 512, 32768, 4, num_sms=152, max_q_len=2) == \
         plan(32, 64, 128, 1, 512, 32768, 4, num_sms=152, max_q_len=1)
@@ -333,6 +343,10 @@ def test_noalloc_routes_and_rejects_as_attn_decode(attn):
     assert call_noalloc(attn, P=-1) == E.ATTN_ERR_INVALID_ARG
     assert call_noalloc(attn, P=E.ATTN_MAX_PARTITIONS + 1) == E.ATTN_ERR_INVALID_ARG
     assert call_decode(attn, P=E.ATTN_MAX_PARTITIONS + 1) == E.ATTN_ERR_INVALID_ARG
+    # the pair of Q tiles only on the tile path
+    pair = E.ATTN_PARTITIONS_TILE_PAIR
+    assert call_decode(attn, P=pair) == E.ATTN_ERR_INVALID_ARG
+    assert call_decode(attn, P=-3) == E.ATTN_ERR_INVALID_ARG
     # the tile kernel (rows x group above 16) does not split
     assert call_noalloc(attn, offs=0x70000, rows=40, max_q_len=30, P=2) == E.ATTN_ERR_UNSUPPORTED
     assert call_decode(attn, offs=0x70000, rows=40, max_q_len=30, P=2) == E.ATTN_ERR_UNSUPPORTED
