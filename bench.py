@@ -420,9 +420,12 @@ def run_ours(args, rank, world, dist):
                              causal=w.causal, num_partitions=P, workspace=ws, out=o, lse=l,
                              stream=stream)
 
-    # plan + decode + reduce for the balanced MLA split (P = 0); decode +
-    # reduce for P slices per row; the decode kernel alone when P = 1
-    launches_per_call = 1 if P == 1 else (3 if P == 0 else 2)
+    # plan + decode + reduce for the balanced MLA split (P = 0); the tile
+    # kernels alone (P = 1 or the pair); decode + reduce otherwise (P slices
+    # or the balanced GQA split)
+    tile_path = args.workload == "mixed"
+    launches_per_call = (1 if P == 1 or tile_path else
+                         (3 if P == 0 and w.is_mla else 2))
     nbytes = algorithmic_bytes(w)
     flops = algorithmic_flops(w)
 

@@ -56,7 +56,8 @@ enum {
 
 /* Largest split-K partition count accepted by every entry point. */
 #define ATTN_MAX_PARTITIONS 1024
-/* attn_plan_partitions request: the balanced MLA split (num_partitions 0) */
+/* attn_plan_partitions request: the balanced split (MLA: num_partitions 0;
+ * attn_decode on the tensor cores: num_partitions ATTN_PARTITIONS_BALANCED) */
 #define ATTN_PARTITIONS_BALANCED (-1)
 /* attn_plan_partitions request and attn_decode num_partitions on the tile
  * path: two Q tiles per CTA pair sharing each K/V tile */
@@ -118,13 +119,17 @@ typedef struct attn_kv {
  *   head_dim_v    output channels (128 for GQA d128, 512 for MLA).
  *   max_kv_len    host upper bound of every kv_len[b].
  *   requested     0 = automatic; > 0 = use exactly this many partitions;
- *                 ATTN_PARTITIONS_BALANCED = the balanced split (MLA shapes
- *                 only: num_kv_heads 1, head_dim_v 512; num_partitions out 0);
+ *                 ATTN_PARTITIONS_BALANCED = the balanced split (MLA shapes:
+ *                 num_kv_heads 1, head_dim_v 512, num_partitions out 0; or
+ *                 attn_decode with head_dim 128 on its split-K route, single
+ *                 rows or the few-row fold, num_partitions out
+ *                 ATTN_PARTITIONS_BALANCED);
  *                 ATTN_PARTITIONS_TILE_PAIR = two Q tiles per CTA pair (the
  *                 tile path only); any other shape or negative value:
  *                 ATTN_ERR_INVALID_ARG.
  *   num_partitions  out: partitions P (1 <= P <= ATTN_MAX_PARTITIONS), 0 for
- *                 the balanced MLA split, or ATTN_PARTITIONS_TILE_PAIR.
+ *                 the balanced MLA split, ATTN_PARTITIONS_BALANCED for the
+ *                 balanced GQA split, or ATTN_PARTITIONS_TILE_PAIR.
  *   workspace_bytes out: workspace size attn_decode / attn_mla_decode need
  *                 for this P (0 when P == 1).
  *
@@ -135,7 +140,14 @@ typedef struct attn_kv {
  * (workspace_bytes 0): a cluster of P CTAs splits each (sequence, KV head)
  * into P equal key slices of that sequence and merges them on chip.  The
  * automatic choice treats num_kv_heads == 1 with head_dim_v == 512 as the
- * MLA shape and everything else as GQA.  GQA with head_dim 128 and
+ * MLA shape and everything else as GQA.  GQA with head_dim 128 on the
+ * split-K route and fewer (sequence, KV head) units than 2 num_sms
+ * (max_kv_len above one 128-key tile) takes the balanced split: the 128-key
+ * tiles of every unit (an empty unit counts one), concatenated, are dealt
+ * out in equal contiguous ranges to num_sms CTAs; a unit a range end cuts
+ * leaves one partial per piece, merged by the reduce.  Its workspace_bytes
+ * = (num_sms + units) slots of 16 x 128 fp32 plus 16 m and 16 l each (each
+ * array 256-byte aligned) plus 8 bytes per unit (256-byte aligned).  GQA with head_dim 128 and
  * max_q_len > 1 on the few-row fold: P = 1 when there are at
  * least 2 (sequence, KV head) units per SM, else the many-unit rule (at
  * least four items per CTA at full length and slices of at most ~1024
@@ -202,7 +214,10 @@ int attn_plan_partitions(int num_sms, int batch, int num_q_rows, int max_q_len,
  *   num_partitions  P from attn_plan_partitions (or any 1..MAX), or 0 for
  *              the planner's automatic choice on the current device (the
  *              same call as attn_plan_partitions with num_sms 0 and
- *              requested 0: size the workspace with that call); must be 0 or
+ *              requested 0: size the workspace with that call), or
+ *              ATTN_PARTITIONS_BALANCED (head_dim 128, not the tile path):
+ *              the balanced split over one CTA per SM of the current device,
+ *              the workspace sized for it; must be 0 or
  *              1 on the tile path (max_q_len > 1 beyond the few-row fold),
  *              both one Q tile per CTA, or ATTN_PARTITIONS_TILE_PAIR there:
  *              two adjacent Q tiles per CTA pair.  The automatic choice (0)

@@ -112,6 +112,19 @@ size_t mla_balanced_layout(int clusters, long long rows, size_t *off_m, size_t *
            align256(size_t(rows) * 8);
 }
 
+// Balanced GQA split: partial slots (CTAs + units) of 16 columns x 128
+// channels, m and l per column, then the unit table {first slot, pieces}.
+size_t gqa_balanced_layout(int ctas, long long units, size_t *off_m, size_t *off_l,
+                           size_t *off_table) {
+    const size_t n = (size_t(ctas) + size_t(units)) * size_t(kGqaSlotCols);
+    const size_t o_bytes = align256(n * 128 * sizeof(float));
+    const size_t m_bytes = align256(n * sizeof(float));
+    if (off_m) *off_m = o_bytes;
+    if (off_l) *off_l = o_bytes + m_bytes;
+    if (off_table) *off_table = o_bytes + 2 * m_bytes;
+    return o_bytes + 2 * m_bytes + align256(size_t(units) * 8);
+}
+
 int chunk_for(int max_kv_len, int P, int tile) {
     long long per = (static_cast<long long>(max_kv_len) + P - 1) / P;
     if (per < 1) per = 1;
@@ -266,9 +279,13 @@ int plan_impl(int num_sms, int batch, int num_q_rows, int max_q_len, int num_q_h
     if (num_q_heads % num_kv_heads) return ATTN_ERR_INVALID_ARG;
     if (requested > ATTN_MAX_PARTITIONS) return ATTN_ERR_INVALID_ARG;
     const bool mla_shape = num_kv_heads == 1 && head_dim_v == kMlaDimV;
-    if (requested == ATTN_PARTITIONS_BALANCED && !mla_shape) return ATTN_ERR_INVALID_ARG;
     const bool tile_path = !mla_shape && max_q_len > 1 &&
                            !folds_rows(max_q_len, head_dim_v, num_q_heads / num_kv_heads, batch);
+    // the split-K route on the tensor cores (head_dim 128): single rows and
+    // the few-row fold
+    const bool gqa_tc = !mla_shape && !tile_path && head_dim_v == 128;
+    if (requested == ATTN_PARTITIONS_BALANCED && !mla_shape && !gqa_tc)
+        return ATTN_ERR_INVALID_ARG;
     if (requested == ATTN_PARTITIONS_TILE_PAIR && !tile_path) return ATTN_ERR_INVALID_ARG;
     if (tile_path) {
         // the tile kernels: every row run in one pass, no split-K; one Q tile
@@ -284,11 +301,27 @@ int plan_impl(int num_sms, int batch, int num_q_rows, int max_q_len, int num_q_h
             cudaDeviceGetAttribute(&num_sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
             return ATTN_ERR_CUDA;
     }
+    const long long gqa_units = static_cast<long long>(batch > 0 ? batch : 1) * num_kv_heads;
+    if (requested == ATTN_PARTITIONS_BALANCED && gqa_tc) {
+        *num_partitions = ATTN_PARTITIONS_BALANCED;
+        *workspace_bytes = gqa_balanced_layout(num_sms, gqa_units, nullptr, nullptr, nullptr);
+        return ATTN_OK;
+    }
     if (requested == ATTN_PARTITIONS_BALANCED) {
         *num_partitions = 0;
         *workspace_bytes = mla_balanced_layout(num_sms / 2 > 0 ? num_sms / 2 : 1,
                                                num_q_rows > 0 ? num_q_rows : 1, nullptr, nullptr,
                                                nullptr);
+        return ATTN_OK;
+    }
+    if (requested == 0 && gqa_tc && gqa_units < 2LL * num_sms &&
+        max_kv_len > kGqaTcTileKeys) {
+        // Fewer (sequence, KV head) units than two per SM: slices of one size
+        // cannot balance ragged lengths over the SMs, so every unit's 128-key
+        // tiles, concatenated, are dealt out in equal contiguous ranges, one
+        // per SM (the units a range end cuts are merged by the reduce).
+        *num_partitions = ATTN_PARTITIONS_BALANCED;
+        *workspace_bytes = gqa_balanced_layout(num_sms, gqa_units, nullptr, nullptr, nullptr);
         return ATTN_OK;
     }
     int P = requested;
@@ -391,7 +424,8 @@ extern "C" int attn_decode(const void *q, const attn_kv_t *k, const attn_kv_t *v
         max_q_len < 1)
         return ATTN_ERR_INVALID_ARG;
     if (num_q_heads % group) return ATTN_ERR_INVALID_ARG;
-    if ((num_partitions < 0 && num_partitions != ATTN_PARTITIONS_TILE_PAIR) ||
+    if ((num_partitions < 0 && num_partitions != ATTN_PARTITIONS_TILE_PAIR &&
+         num_partitions != ATTN_PARTITIONS_BALANCED) ||
         num_partitions > ATTN_MAX_PARTITIONS)
         return ATTN_ERR_INVALID_ARG;
     if (!(scale == scale)) return ATTN_ERR_INVALID_ARG;
@@ -403,6 +437,8 @@ extern "C" int attn_decode(const void *q, const attn_kv_t *k, const attn_kv_t *v
     const bool fold = folds_rows(max_q_len, head_dim, group, batch);
     if (num_partitions == ATTN_PARTITIONS_TILE_PAIR && !(max_q_len > 1 && !fold))
         return ATTN_ERR_INVALID_ARG;   // the pair of Q tiles is a tile-path request
+    if (num_partitions == ATTN_PARTITIONS_BALANCED && ((max_q_len > 1 && !fold) || head_dim != 128))
+        return ATTN_ERR_INVALID_ARG;   // the balanced split is a split-K route on the tensor cores
     if (max_q_len > 1 && !fold) {
         if (num_partitions > 1) return ATTN_ERR_UNSUPPORTED;
         return prefill_path(q, k, v, kv_len, q_row_offsets, batch, num_q_rows, num_q_heads,
@@ -436,11 +472,23 @@ extern "C" int attn_decode(const void *q, const attn_kv_t *k, const attn_kv_t *v
     // the CUDA cores (32-key tiles).  On the tensor cores a split into 2 or 4
     // partitions is merged on chip by a cluster of that many CTAs.
     const bool tc = head_dim == 128;
-    const bool on_chip = merges_on_chip(num_partitions, head_dim);
-    size_t off_m = 0, off_l = 0;
-    const size_t need = workspace_layout(num_partitions, num_q_rows, num_q_heads, head_dim,
-                                         &off_m, &off_l);
-    if (num_partitions > 1 && !on_chip) {
+    const bool balanced = num_partitions == ATTN_PARTITIONS_BALANCED;
+    const bool on_chip = !balanced && merges_on_chip(num_partitions, head_dim);
+    size_t off_m = 0, off_l = 0, off_table = 0;
+    int ctas = 0;
+    size_t need;
+    if (balanced) {
+        int dev = 0;
+        if (cudaGetDevice(&dev) != cudaSuccess ||
+            cudaDeviceGetAttribute(&ctas, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+            return ATTN_ERR_CUDA;
+        need = gqa_balanced_layout(ctas, static_cast<long long>(batch) * hkv, &off_m, &off_l,
+                                   &off_table);
+    } else {
+        need = workspace_layout(num_partitions, num_q_rows, num_q_heads, head_dim, &off_m,
+                                &off_l);
+    }
+    if (balanced || (num_partitions > 1 && !on_chip)) {
         if (!workspace || workspace_bytes < need) return ATTN_ERR_WORKSPACE;
         if (reinterpret_cast<uintptr_t>(workspace) % 256) return ATTN_ERR_WORKSPACE;
     }
@@ -475,11 +523,12 @@ extern "C" int attn_decode(const void *q, const attn_kv_t *k, const attn_kv_t *v
     p.q_row_offsets = fold ? q_row_offsets : nullptr;
     p.page_table = k->page_table;
     p.sink = sink;
-    if (num_partitions > 1 && !on_chip) {
+    if (balanced || (num_partitions > 1 && !on_chip)) {
         uint8_t *ws = static_cast<uint8_t *>(workspace);
         p.ws_o = reinterpret_cast<float *>(ws);
         p.ws_m = reinterpret_cast<float *>(ws + off_m);
         p.ws_l = reinterpret_cast<float *>(ws + off_l);
+        if (balanced) p.unit_slots = reinterpret_cast<int2 *>(ws + off_table);
     }
     p.cluster = on_chip ? num_partitions : 0;
     p.out = static_cast<uint16_t *>(out);
@@ -496,11 +545,37 @@ extern "C" int attn_decode(const void *q, const attn_kv_t *k, const attn_kv_t *v
     p.num_pages = k->num_pages;
     p.num_partitions = num_partitions;
     p.chunk = chunk_for(max_kv_len, num_partitions, tile);
+    if (balanced) {
+        // the item table counts 128-key tiles of every unit
+        p.balanced = 1;
+        p.chunk = kGqaTcTileKeys;
+        p.num_partitions = max_kv_len > 0 ? (max_kv_len + kGqaTcTileKeys - 1) / kGqaTcTileKeys : 1;
+    }
     p.qk_scale_log2 = scale * 1.4426950408889634f;
 
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
     st = map_cuda(tc ? launch_gqa_decode_tc(p, s) : launch_gqa_decode(p, s));
     if (st || num_partitions == 1 || on_chip) return st;
+    if (balanced) {
+        ReduceParams r;
+        std::memset(&r, 0, sizeof(r));
+        r.ws_o = p.ws_o;
+        r.ws_m = p.ws_m;
+        r.ws_l = p.ws_l;
+        r.sink = sink;
+        r.out = p.out;
+        r.lse = lse;
+        r.q_row_offsets = p.q_row_offsets;
+        r.batch = batch;
+        r.num_partitions = ctas;   // the most pieces a unit can have
+        r.rows = p.num_q_rows;
+        r.num_q_heads = num_q_heads;
+        r.dim_v = head_dim;
+        r.unit_slots = p.unit_slots;
+        r.group = group;
+        r.hkv = hkv;
+        return map_cuda(launch_splitk_reduce(r, s, /*pdl=*/true));
+    }
 
     ReduceParams r;
     std::memset(&r, 0, sizeof(r));

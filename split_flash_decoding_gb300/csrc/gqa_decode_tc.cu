@@ -26,6 +26,14 @@
 // TMEM and issues the MMAs.  Rings: 3 K stages and 3 V stages of 32 KB, each
 // consumed in order by the single MMA thread, so parity waits never alias.
 //
+// Balanced split (small batches): the 128-key tiles of every (sequence, KV
+// head) unit, concatenated, are dealt out in equal contiguous ranges, one per
+// CTA, so ragged lengths cannot leave SMs idle; a CTA walks the pieces of the
+// units its range meets, writes the units it holds whole and leaves a
+// 16-column partial in slot (CTA + unit) for each piece of a cut unit; the
+// CTA holding a unit's first tile publishes the unit's slot range for the
+// split-K reduce.
+//
 // Small P, merged on chip: with 2 or 4 partitions the kernel can run as
 // clusters of that many CTAs instead.  A cluster takes one (sequence, KV
 // head) unit at a time and CTA r of the cluster covers the r-th of equal key
@@ -161,18 +169,27 @@ size_t tc_smem_bytes(int batch) {
 }
 
 // Work walk of one CTA.  Without clusters: items (sequence, KV head, slice)
-// j = blockIdx.x, blockIdx.x + gridDim.x, ...  With clusters of C: units
-// (sequence, KV head) j = cluster, cluster + clusters, ..., this CTA taking
-// the slice of its rank.
+// j = blockIdx.x, blockIdx.x + gridDim.x, ...; under the balanced split the
+// pieces of the units that meet the CTA's tile range, in order.  With
+// clusters of C: units (sequence, KV head) j = cluster, cluster + clusters,
+// ..., this CTA taking the slice of its rank.
 template <int C>
-__device__ __forceinline__ int walk_first() { return C > 1 ? int(blockIdx.x) / C : int(blockIdx.x); }
-template <int C>
-__device__ __forceinline__ int walk_stride() { return C > 1 ? int(gridDim.x) / C : int(gridDim.x); }
+__device__ __forceinline__ GqaWalk make_walk(const GqaParams &p, const int *cum, int hkv) {
+    GqaWalk w;
+    if (C == 1 && p.balanced) return gqa_balanced_walk(p, cum, hkv);
+    w.first = C > 1 ? int(blockIdx.x) / C : int(blockIdx.x);
+    w.stride = C > 1 ? int(gridDim.x) / C : int(gridDim.x);
+    w.count = C > 1 ? p.batch * hkv : cum[p.batch];
+    w.x0 = w.x1 = w.tiles = w.ctas = 0;
+    w.u0 = 0;
+    return w;
+}
 
 template <int C>
-__device__ __forceinline__ GqaItem walk_item(const GqaParams &p, const int *cum, int j, int hkv) {
+__device__ __forceinline__ GqaItem walk_item(const GqaParams &p, const int *cum, int j, int hkv,
+                                             const GqaWalk &w) {
     if constexpr (C == 1) {
-        return gqa_item<kBK>(p, cum, j, hkv);
+        return p.balanced ? gqa_balanced_item(p, cum, hkv, w, j) : gqa_item<kBK>(p, cum, j, hkv);
     } else {
         GqaItem it;
         it.b = j / hkv;
@@ -189,6 +206,9 @@ __device__ __forceinline__ GqaItem walk_item(const GqaParams &p, const int *cum,
         it.end = min(it.start + cs, it.L);
         it.ntiles = it.start < it.end ? (it.end - it.start + kBK - 1) / kBK : 0;
         it.direct = false;
+        it.unit = j;
+        it.unit_x = it.unit_tiles = 0;
+        it.first = false;
         return it;
     }
 }
@@ -204,8 +224,8 @@ __device__ __forceinline__ uint32_t n_operand_offset(int r, int c) {
 // tiles, resolves pages lane-parallel (32 row boxes at a time) and lets lane
 // 0 issue the boxes of each tile into the ring.
 template <bool kIsK, int C>
-__device__ __forceinline__ void produce(const GqaParams &p, const int *cum, int num_items, int hkv,
-                                        uint8_t *smem, uint64_t *bar, int lane) {
+__device__ __forceinline__ void produce(const GqaParams &p, const int *cum, const GqaWalk &w,
+                                        int hkv, uint8_t *smem, uint64_t *bar, int lane) {
     const CUtensorMap *map = kIsK ? &p.k_map : &p.v_map;
     uint64_t *full = bar + (kIsK ? kKFull : kVFull);
     uint64_t *empty = bar + (kIsK ? kKEmpty : kVEmpty);
@@ -220,8 +240,8 @@ __device__ __forceinline__ void produce(const GqaParams &p, const int *cum, int 
     const uint32_t box_bytes = uint32_t(box_rows) * 128u;
     int g = 0, itq = 0;
     bool aborted = false;
-    for (int j = walk_first<C>(); j < num_items && !aborted; j += walk_stride<C>()) {
-        const GqaItem it = walk_item<C>(p, cum, j, hkv);
+    for (int j = w.first; j < w.count && !aborted; j += w.stride) {
+        const GqaItem it = walk_item<C>(p, cum, j, hkv, w);
         if (it.ntiles == 0) continue;
         if (kIsK && lane == 0) {
             const int qb = itq & 1;
@@ -349,12 +369,12 @@ gqa_decode_tc_kernel(const __grid_constant__ GqaParams p) {
     if constexpr (C > 1) cluster_sync();   // every CTA's barriers exist before a remote arrive
     tc::fence_after_sync();
     const uint32_t tmem = *tmem_slot;
-    const int num_items = C > 1 ? p.batch * hkv : cum[p.batch];
+    const GqaWalk walk = make_walk<C>(p, cum, hkv);
 
     if (warp == kWarpK) {
-        produce<true, C>(p, cum, num_items, hkv, smem, bar, lane);
+        produce<true, C>(p, cum, walk, hkv, smem, bar, lane);
     } else if (warp == kWarpV) {
-        produce<false, C>(p, cum, num_items, hkv, smem, bar, lane);
+        produce<false, C>(p, cum, walk, hkv, smem, bar, lane);
     } else if (warp == kWarpMma) {
         // ---------------------------------------------------------- MMA issue
         if (lane == 0) {
@@ -366,8 +386,8 @@ gqa_decode_tc_kernel(const __grid_constant__ GqaParams p) {
             const uint32_t p_base = smem_addr(smem + Smem::p);
             int g = 0, itq = 0;
             bool ok = true;
-            for (int j = walk_first<C>(); ok && j < num_items; j += walk_stride<C>()) {
-                const GqaItem it = walk_item<C>(p, cum, j, hkv);
+            for (int j = walk.first; ok && j < walk.count; j += walk.stride) {
+                const GqaItem it = walk_item<C>(p, cum, j, hkv, walk);
                 if (it.ntiles == 0) continue;
                 const int qb = itq & 1;
                 ok = mbar_wait(&bar[kQFull + qb], (itq >> 1) & 1, p.err);
@@ -433,8 +453,8 @@ gqa_decode_tc_kernel(const __grid_constant__ GqaParams p) {
         uint8_t *pbuf = smem + Smem::p;
         int g = 0, iter = 0;
         bool ok = true;
-        for (int j = walk_first<C>(); j < num_items; j += walk_stride<C>(), ++iter) {
-            const GqaItem it = walk_item<C>(p, cum, j, hkv);
+        for (int j = walk.first; j < walk.count; j += walk.stride, ++iter) {
+            const GqaItem it = walk_item<C>(p, cum, j, hkv, walk);
             int row0, nrows;
             seq_rows(p, it.b, row0, nrows);
             // Column cg = (row cg / G, head cg % G): keys j < lim visible.
@@ -596,8 +616,11 @@ gqa_decode_tc_kernel(const __grid_constant__ GqaParams p) {
                             p.lse[row * p.num_q_heads + hq] =
                                 Z > 0.f ? (Mf + fast_log2(Z)) * kLn2 : -INFINITY;
                     } else {
+                        // partition part: [P][rows][heads]; balanced-split slot:
+                        // [slots][16 columns]
                         const size_t base =
-                            (size_t(it.part) * p.num_q_rows + row) * p.num_q_heads + hq;
+                            p.balanced ? size_t(it.part) * kGqaSlotCols + (cg0 + c)
+                                       : (size_t(it.part) * p.num_q_rows + row) * p.num_q_heads + hq;
                         const float scale_o = lrsum[c] > 0.f ? lsum[c] / lrsum[c] : 0.f;
                         p.ws_o[base * kD + ch] = o[c] * scale_o;
                         if (ch == 0) {
@@ -605,6 +628,17 @@ gqa_decode_tc_kernel(const __grid_constant__ GqaParams p) {
                             p.ws_l[base] = lsum[c];
                         }
                     }
+                }
+                if (p.balanced && it.first && threadIdx.x == 0) {
+                    // The CTA holding the unit's first tile publishes where its
+                    // pieces are: slots c + unit for the CTAs c holding its
+                    // first through last tile (CTA ((x + 1) C' - 1) / T holds
+                    // tile x).
+                    const long long last = it.unit_x + it.unit_tiles - 1;
+                    const int c_last =
+                        static_cast<int>(((last + 1) * walk.ctas - 1) / walk.tiles);
+                    const int c_first = static_cast<int>(blockIdx.x);
+                    p.unit_slots[it.unit] = make_int2(c_first + it.unit, c_last - c_first + 1);
                 }
             } else {
                 // ---- on-chip merge of the cluster's partials -----------------
@@ -711,7 +745,7 @@ cudaError_t launch_g(const GqaParams &p, cudaStream_t stream) {
     if constexpr (C == 1) {
         long long grid = g_num_sms_tc[dev];   // one resident CTA per SM
         const long long max_items = units * p.num_partitions;
-        if (grid > max_items) grid = max_items;
+        if (grid > max_items && !p.balanced) grid = max_items;
         if (grid < 1) grid = 1;
         kern<<<dim3(static_cast<unsigned>(grid)), threads_for(NC), smem, stream>>>(p);
         return cudaGetLastError();

@@ -16,7 +16,77 @@ namespace attn {
 struct GqaItem {
     int b, kvh, part, L, start, end, ntiles;
     bool direct;  // the sequence needs at most one slice: write the final rows
+    // balanced split: the unit (sequence, KV head), whether this piece holds
+    // its first tile, and the global tile index of that first tile and its
+    // tile count
+    int unit, unit_x, unit_tiles;
+    bool first;
 };
+
+// This CTA's items: j = first, first + stride, ... < count.  The balanced
+// split also keeps the CTA's tile range [x0, x1) of the concatenation of
+// every unit's tiles (tiles in all, dealt over ctas CTAs) and the unit of
+// its first tile.
+struct GqaWalk {
+    int first, stride, count;
+    long long x0, x1, tiles, ctas;
+    int u0;
+};
+
+// Unit (sequence b, KV head) holding global tile x: cum[b] <= x < cum[b+1].
+__device__ __forceinline__ int gqa_unit_of(const int *cum, int batch, int hkv, long long x) {
+    int lo = 0, hi = batch;
+    while (hi - lo > 1) {
+        const int mid = (lo + hi) >> 1;
+        if (cum[mid] <= x) lo = mid; else hi = mid;
+    }
+    const int per_head = (cum[lo + 1] - cum[lo]) / hkv;
+    return lo * hkv + static_cast<int>((x - cum[lo]) / per_head);
+}
+
+// Balanced split: this CTA's tile range and units.  CTA c of C' = min(grid,
+// tiles) takes tiles [c T / C', (c + 1) T / C'), at least one; CTAs past C'
+// take none.
+__device__ __forceinline__ GqaWalk gqa_balanced_walk(const GqaParams &p, const int *cum, int hkv) {
+    GqaWalk w;
+    w.first = 0;
+    w.stride = 1;
+    w.tiles = cum[p.batch];
+    w.ctas = min(static_cast<long long>(gridDim.x), w.tiles);
+    const long long c = blockIdx.x;
+    w.count = 0;
+    w.u0 = 0;
+    w.x0 = w.x1 = 0;
+    if (c < w.ctas) {
+        w.x0 = c * w.tiles / w.ctas;
+        w.x1 = (c + 1) * w.tiles / w.ctas;
+        w.u0 = gqa_unit_of(cum, p.batch, hkv, w.x0);
+        w.count = gqa_unit_of(cum, p.batch, hkv, w.x1 - 1) - w.u0 + 1;
+    }
+    return w;
+}
+
+// Item j of a balanced walk: the piece of unit u0 + j inside [x0, x1).
+__device__ __forceinline__ GqaItem gqa_balanced_item(const GqaParams &p, const int *cum, int hkv,
+                                                     const GqaWalk &w, int j) {
+    GqaItem it;
+    it.unit = w.u0 + j;
+    it.b = it.unit / hkv;
+    it.kvh = it.unit - it.b * hkv;
+    it.unit_tiles = (cum[it.b + 1] - cum[it.b]) / hkv;
+    it.unit_x = cum[it.b] + it.kvh * it.unit_tiles;
+    const long long tb = max(w.x0 - it.unit_x, 0LL);
+    const long long te = min(w.x1 - it.unit_x, static_cast<long long>(it.unit_tiles));
+    const uint32_t cap = uint32_t(p.num_partitions) * uint32_t(p.chunk);
+    it.L = static_cast<int>(min(p.kv_len[it.b], cap));
+    it.start = static_cast<int>(tb) * kGqaTcTileKeys;
+    it.end = min(static_cast<int>(te) * kGqaTcTileKeys, it.L);
+    it.ntiles = it.start < it.end ? (it.end - it.start + kGqaTcTileKeys - 1) / kGqaTcTileKeys : 0;
+    it.first = tb == 0;
+    it.direct = tb == 0 && te == it.unit_tiles;
+    it.part = static_cast<int>(blockIdx.x) + it.unit;   // partial slot
+    return it;
+}
 
 // Build cum[0..batch] with warp `warp_id` (all 32 lanes must call).
 __device__ __forceinline__ void gqa_build_items(const GqaParams &p, int hkv, int *cum, int lane) {
@@ -72,6 +142,10 @@ __device__ __forceinline__ GqaItem gqa_item(const GqaParams &p, const int *cum, 
     it.end = min(it.start + p.chunk, it.L);
     it.ntiles = it.start < it.end ? (it.end - it.start + kTileKeys - 1) / kTileKeys : 0;
     it.direct = per_head <= 1;
+    it.unit = lo * hkv + it.kvh;
+    it.unit_x = 0;
+    it.unit_tiles = 0;
+    it.first = false;
     return it;
 }
 

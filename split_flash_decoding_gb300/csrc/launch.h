@@ -43,8 +43,19 @@ struct GqaParams {
     int chunk;                    // keys per partition slice, multiple of kGqaTileKeys
     int cluster;                  // tensor-core kernel: 2 or 4 = P CTAs of a cluster split a
                                   // unit and merge on chip (no workspace); 0 = off
+    // Balanced split (tensor-core kernel): the 128-key tiles of every
+    // (sequence, KV head) unit, concatenated, in equal contiguous ranges per
+    // CTA (num_partitions = ceil(max_kv_len / 128), chunk = 128, so the item
+    // table counts tiles).  A unit cut by a range end leaves one partial per
+    // piece in slot (CTA + unit): ws_o [slots][16 columns][128], ws_m / ws_l
+    // [slots][16]; unit_slots[unit] = {first slot, pieces} for the reduce.
+    int balanced;
+    int2 *unit_slots;             // [batch * num_kv_heads]
     float qk_scale_log2;          // scale * log2(e)
 };
+// Columns of one balanced-split partial slot (the N side of the tensor-core
+// decode kernel: query rows x heads of a group).
+constexpr int kGqaSlotCols = 16;
 
 // Keys per tile in the MLA kernel; its partition slices are multiples of it.
 constexpr int kMlaTileKeys = 64;
@@ -127,6 +138,13 @@ struct ReduceParams {
     // the workspace (e = slots[r]); e.y == 1 rows were finished by the
     // decode kernel, e.y == 0 rows are empty.
     const int2 *slots;
+    // Balanced GQA split: (row r, head h) of sequence b belongs to unit u =
+    // b * hkv + h / group, whose partials are slots e.x .. e.x + e.y - 1
+    // (e = unit_slots[u]) of [slots][kGqaSlotCols][dim_v], at column
+    // (r - first row of b) * group + h % group; e.y == 1: finished by the
+    // decode kernel.
+    const int2 *unit_slots;
+    int group, hkv;
 };
 
 cudaError_t launch_gqa_decode(const GqaParams &p, cudaStream_t stream);

@@ -36,6 +36,44 @@ __device__ __forceinline__ int row_sequence(const ReduceParams &p, int row) {
     return lo;
 }
 
+// Where the partials of (row, h) are: returns their count P (-1: the row was
+// finished by the partition kernel), the distance between consecutive
+// partials and the index of the first, in units of one (row, head) entry.
+__device__ __forceinline__ int locate_partials(const ReduceParams &p, int row, int h,
+                                               size_t &stride_p, size_t &widx0) {
+    int P = p.num_partitions;
+    stride_p = static_cast<size_t>(p.rows) * p.num_q_heads;   // per partition
+    widx0 = static_cast<size_t>(row) * p.num_q_heads + h;
+    if (p.slots) {
+        // Balanced MLA split: the row's partials sit in consecutive slots.
+        const int2 e = p.slots[row];
+        if (e.y == 1) return -1;   // finished by the decode kernel
+        stride_p = p.num_q_heads;
+        widx0 = static_cast<size_t>(e.x) * p.num_q_heads + h;
+        return e.y;                // 0: an empty row, written from the sink alone
+    }
+    if (p.unit_slots) {
+        // Balanced GQA split: the unit's partials sit in consecutive slots of
+        // 16 columns (query row within the sequence x head within the group).
+        const int b = row_sequence(p, row);
+        const int first_row = p.q_row_offsets ? int(p.q_row_offsets[b]) : b;
+        const int2 e = p.unit_slots[b * p.hkv + h / p.group];
+        if (e.y == 1) return -1;
+        stride_p = kGqaSlotCols;
+        widx0 = static_cast<size_t>(e.x) * kGqaSlotCols + (row - first_row) * p.group + h % p.group;
+        return e.y;
+    }
+    if (p.kv_len) {
+        // Rows that fit in one slice were finished by the partition kernel.
+        uint32_t cap = uint32_t(p.num_partitions) * uint32_t(p.chunk);
+        if (p.len_cap > 0) cap = min(cap, uint32_t(p.len_cap));
+        const uint32_t L = min(p.kv_len[row_sequence(p, row)], cap);
+        const int ns = static_cast<int>((L + p.chunk - 1) / p.chunk);
+        return ns < 2 ? -1 : ns;
+    }
+    return P;
+}
+
 __global__ void __launch_bounds__(kWarps * 32)
 splitk_reduce_kernel(const __grid_constant__ ReduceParams p) {
     // With programmatic dependent launch this grid may start while the
@@ -50,26 +88,10 @@ splitk_reduce_kernel(const __grid_constant__ ReduceParams p) {
     const int row = static_cast<int>(item / p.num_q_heads);
     const int h = static_cast<int>(item - static_cast<long long>(row) * p.num_q_heads);
 
-    int P = p.num_partitions;
-    size_t stride_p = static_cast<size_t>(p.rows) * p.num_q_heads;  // per partition
     const size_t idx0 = static_cast<size_t>(row) * p.num_q_heads + h;  // out / lse
-    size_t widx0 = idx0;                                               // workspace
-    if (p.slots) {
-        // Balanced split: the row's partials sit in consecutive slots.
-        const int2 e = p.slots[row];
-        if (e.y == 1) return;   // finished by the decode kernel (uniform over the warp)
-        P = e.y;                // 0: an empty row, written below from the sink alone
-        stride_p = p.num_q_heads;
-        widx0 = static_cast<size_t>(e.x) * p.num_q_heads + h;
-    } else if (p.kv_len) {
-        // Rows that fit in one slice were finished by the partition kernel.
-        uint32_t cap = uint32_t(p.num_partitions) * uint32_t(p.chunk);
-        if (p.len_cap > 0) cap = min(cap, uint32_t(p.len_cap));
-        const uint32_t L = min(p.kv_len[row_sequence(p, row)], cap);
-        const int ns = static_cast<int>((L + p.chunk - 1) / p.chunk);
-        if (ns < 2) return;  // uniform over the warp
-        P = ns;
-    }
+    size_t stride_p, widx0;                                            // workspace
+    const int P = locate_partials(p, row, h, stride_p, widx0);
+    if (P < 0) return;   // uniform over the warp
 
     if (P <= kFastP) {
         // Few partitions: the O partials of the first channel block, m and l
@@ -176,24 +198,10 @@ splitk_reduce_wide_kernel(const __grid_constant__ ReduceParams p) {
     const int row = blockIdx.x / p.num_q_heads;
     const int h = blockIdx.x - row * p.num_q_heads;
 
-    int P = p.num_partitions;
-    size_t stride_p = static_cast<size_t>(p.rows) * p.num_q_heads;
     const size_t idx0 = static_cast<size_t>(row) * p.num_q_heads + h;
-    size_t widx0 = idx0;
-    if (p.slots) {
-        const int2 e = p.slots[row];
-        if (e.y == 1) return;   // uniform over the CTA
-        P = e.y;
-        stride_p = p.num_q_heads;
-        widx0 = static_cast<size_t>(e.x) * p.num_q_heads + h;
-    } else if (p.kv_len) {
-        uint32_t cap = uint32_t(p.num_partitions) * uint32_t(p.chunk);
-        if (p.len_cap > 0) cap = min(cap, uint32_t(p.len_cap));
-        const uint32_t L = min(p.kv_len[row_sequence(p, row)], cap);
-        const int ns = static_cast<int>((L + p.chunk - 1) / p.chunk);
-        if (ns < 2) return;  // uniform over the CTA
-        P = ns;
-    }
+    size_t stride_p, widx0;
+    const int P = locate_partials(p, row, h, stride_p, widx0);
+    if (P < 0) return;   // uniform over the CTA
 
     float mloc = -INFINITY;
     for (int q = tid; q < P; q += kWarps * 32) mloc = fmaxf(mloc, p.ws_m[q * stride_p + widx0]);

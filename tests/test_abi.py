@@ -91,7 +91,9 @@ def test_decode_rejects_bad_arguments_before_launch(attn):
     assert call_decode(attn, group=0) == E.ATTN_ERR_INVALID_ARG
     assert call_decode(attn, hq=48, group=16) == E.ATTN_ERR_UNSUPPORTED
     assert call_decode(attn, d=96) == E.ATTN_ERR_UNSUPPORTED
-    assert call_decode(attn, P=-1) == E.ATTN_ERR_INVALID_ARG
+    assert call_decode(attn, P=-3) == E.ATTN_ERR_INVALID_ARG
+    # the balanced split (-1) runs on the tensor-core decode kernel only
+    assert call_decode(attn, d=64, P=E.ATTN_PARTITIONS_BALANCED) == E.ATTN_ERR_INVALID_ARG
     assert call_decode(attn, P=E.ATTN_MAX_PARTITIONS + 1) == E.ATTN_ERR_INVALID_ARG
     assert call_decode(attn, scale=float("nan")) == E.ATTN_ERR_INVALID_ARG
     assert call_decode(attn, max_kv_len=-1) == E.ATTN_ERR_INVALID_ARG
@@ -214,18 +216,28 @@ def test_planner_formulas(attn):
         align = lambda x: (x + 255) // 256 * 256
         expect = 0 if req == 1 else align(n * 128 * 4) + 2 * align(n * 4)
         assert ws == expect
+    align = lambda x: (x + 255) // 256 * 256
     # 2 or 4 partitions on the tensor-core path merge on chip: no workspace
     for req in (2, 4):
         assert attn.attn_plan_partitions(64, 64, 32, 8, 128, 8192, req, num_sms=152)[1] == 0
         P, ws = attn.attn_plan_partitions(64, 64, 32, 16, 64, 8192, req, num_sms=152)
         assert ws > 0                                 # head_dim 64 keeps the workspace
-    # automatic GQA (head_dim 128: one CTA per SM; head_dim 64: two): fewer
-    # units than CTAs -> one wave of slices; otherwise >= 4 items per CTA at
-    # full length and slices of <= ~1024 keys
+    # automatic GQA (head_dim 128: one CTA per SM; head_dim 64: two): with
+    # head_dim 128 and fewer (sequence, KV head) units than two per SM, the
+    # balanced split; otherwise (and for head_dim 64: fewer units than CTAs
+    # -> one wave of slices) >= 4 items per CTA at full length and slices of
+    # <= ~1024 keys
     P, _ = attn.attn_plan_partitions(64, 64, 32, 8, 128, 8192, 0, num_sms=152)
     assert P == 8
-    P, _ = attn.attn_plan_partitions(1, 1, 32, 8, 128, 131072, 0, num_sms=152)
-    assert P == 19 and 8 * P == 152
+    BAL = attn.ATTN_PARTITIONS_BALANCED
+    for batch, rows, hkv, max_len in ((1, 1, 8, 131072), (16, 16, 8, 8192), (37, 37, 8, 5000)):
+        P, ws = attn.attn_plan_partitions(batch, rows, 8 * hkv // 2, hkv, 128, max_len, 0,
+                                          num_sms=152)
+        slots = 152 + batch * hkv
+        assert P == BAL
+        assert ws == align(slots * 16 * 128 * 4) + 2 * align(slots * 16 * 4) + align(batch * hkv * 8)
+    # one tile per unit cannot be balanced further: one slice
+    assert attn.attn_plan_partitions(16, 16, 32, 8, 128, 128, 0, num_sms=152) == (1, 0)
     P, _ = attn.attn_plan_partitions(1, 1, 16, 8, 64, 131072, 0, num_sms=152)
     assert P == 38 and 8 * P == 2 * 152
     # automatic MLA (one KV head, 512 output channels): keys that need a
@@ -251,28 +263,39 @@ def test_planner_formulas(attn):
         assert P == 0 and ws == (align(81 * 128 * 512 * 4) + 2 * align(81 * 128 * 4) +
                                  align(76 * 16) + align(5 * 16) + align(5 * 8))
     with pytest.raises(attn.AttnError):
-        attn.attn_plan_partitions(64, 64, 32, 8, 128, 8192, attn.ATTN_PARTITIONS_BALANCED,
+        attn.attn_plan_partitions(64, 64, 16, 8, 64, 8192, attn.ATTN_PARTITIONS_BALANCED,
                                   num_sms=152)
     with pytest.raises(attn.AttnError):
-        attn.attn_plan_partitions(3, 5, 128, 1, 512, 100, -2, num_sms=152)
+        attn.attn_plan_partitions(3, 5, 128, 1, 512, 100, -3, num_sms=152)
     # an explicit MLA request is a fixed split into P slices per row
     P, ws = attn.attn_plan_partitions(32, 64, 128, 1, 512, 32768, 4, num_sms=152)
     assert P == 4 and ws == align(4 * 64 * 128 * 512 * 4) + 2 * align(4 * 64 * 128 * 4)
     P, _ = attn.attn_plan_partitions(1, 1, 32, 8, 128, 20, 0, num_sms=152)
     assert P == 1                                     # one tile of keys cannot split
-    # a few query rows per sequence (the 16-column fold): long items
+    # a few query rows per sequence (the 16-column fold): long items with two
+    # units per SM or more, else the balanced split
     P, _ = attn.attn_plan_partitions(64, 160, 32, 8, 128, 8192, 0, num_sms=152, max_q_len=4)
     assert P == 1                                     # 512 units, >= 2 per CTA
     P, ws = attn.attn_plan_partitions(16, 40, 32, 8, 128, 8192, 0, num_sms=152, max_q_len=4)
-    assert P == 8 and ws > 0                          # 128 units: slices of <= 1024 keys
+    assert P == BAL and ws > 0                        # 128 units
     P, _ = attn.attn_plan_partitions(2, 8, 32, 8, 128, 8192, 0, num_sms=152, max_q_len=4)
-    assert P == 38                                    # 16 units: >= 4 items per CTA
+    assert P == BAL                                   # 16 units
+    # the balanced split on request: any head_dim-128 decode or few-row shape
+    P, ws = attn.attn_plan_partitions(300, 300, 32, 8, 128, 4000, BAL, num_sms=152)
+    assert P == BAL and ws == (align((152 + 2400) * 16 * 128 * 4) +
+                               2 * align((152 + 2400) * 16 * 4) + align(2400 * 8))
+    for args in ((4, 4, 16, 8, 64, 4000), (4, 40, 32, 8, 128, 4000)):   # head_dim 64; tile path
+        with pytest.raises(attn.AttnError):
+            attn.attn_plan_partitions(*args, BAL, num_sms=152,
+                                      max_q_len=10 if args[1] > args[0] else 1)
     P, _ = attn.attn_plan_partitions(4, 4, 32, 8, 128, 0, 0, num_sms=152)
     assert P == 1
-    # every CTA gets at least one slice of a full-length batch
+    # every CTA gets at least one slice of a full-length batch (head_dim 64:
+    # two CTAs per SM); head_dim 128 deals the tiles out evenly instead
     for sms in (16, 64, 132, 152, 304):
-        P, _ = attn.attn_plan_partitions(2, 2, 32, 8, 128, 65536, 0, num_sms=sms)
-        assert 2 * 8 * P >= sms
+        P, _ = attn.attn_plan_partitions(2, 2, 16, 8, 64, 65536, 0, num_sms=sms)
+        assert 2 * 8 * P >= 2 * sms
+        assert attn.attn_plan_partitions(2, 2, 32, 8, 128, 65536, 0, num_sms=sms)[0] == BAL
     with pytest.raises(attn.AttnError):
         attn.attn_plan_partitions(2, 2, 30, 8, 128, 100, 0, num_sms=152)
     with pytest.raises(attn.AttnError):
