@@ -579,7 +579,7 @@ def run_ours(args, rank, world, dist):
         "data": "synthetic",
         "config": workload_config(w, world),
         "plan": {"num_partitions": P, "workspace_bytes": ws_bytes,
-                 "note": "num_partitions 0 = the balanced MLA split"},
+                 "note": "num_partitions 0: the balanced MLA split; -1: the balanced GQA split; -2: two Q tiles per CTA pair"},
         "clocks": clocks.summary(),
         "e2e": {"value": round(world * nbytes / e2e_s / 1e9, 2), "unit": "GB/s",
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,

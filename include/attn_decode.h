@@ -141,8 +141,8 @@ typedef struct attn_kv {
  * into P equal key slices of that sequence and merges them on chip.  The
  * automatic choice treats num_kv_heads == 1 with head_dim_v == 512 as the
  * MLA shape and everything else as GQA.  GQA with head_dim 128 on the
- * split-K route and fewer (sequence, KV head) units than 2 num_sms
- * (max_kv_len above one 128-key tile) takes the balanced split: the 128-key
+ * split-K route and at most 8 num_sms (sequence, KV head) units (max_kv_len
+ * above one 128-key tile) takes the balanced split: the 128-key
  * tiles of every unit (an empty unit counts one), concatenated, are dealt
  * out in equal contiguous ranges to num_sms CTAs; a unit a range end cuts
  * leaves one partial per piece, merged by the reduce.  Its workspace_bytes

@@ -314,12 +314,15 @@ int plan_impl(int num_sms, int batch, int num_q_rows, int max_q_len, int num_q_h
                                                nullptr);
         return ATTN_OK;
     }
-    if (requested == 0 && gqa_tc && gqa_units < 2LL * num_sms &&
+    if (requested == 0 && gqa_tc && gqa_units <= 8LL * num_sms &&
         max_kv_len > kGqaTcTileKeys) {
-        // Fewer (sequence, KV head) units than two per SM: slices of one size
-        // cannot balance ragged lengths over the SMs, so every unit's 128-key
+        // Up to eight (sequence, KV head) units per SM: every unit's 128-key
         // tiles, concatenated, are dealt out in equal contiguous ranges, one
-        // per SM (the units a range end cuts are merged by the reduce).
+        // per SM, so ragged lengths cannot leave SMs idle and only the units a
+        // range end cuts leave partials for the reduce (measured faster than
+        // the slice plans at 16 to 64 sequences of Llama-3-8B shapes, single
+        // or a few rows).  The workspace grows by ~8 KB per unit, so larger
+        // batches keep the slice plans below.
         *num_partitions = ATTN_PARTITIONS_BALANCED;
         *workspace_bytes = gqa_balanced_layout(num_sms, gqa_units, nullptr, nullptr, nullptr);
         return ATTN_OK;

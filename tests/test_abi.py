@@ -223,14 +223,15 @@ def test_planner_formulas(attn):
         P, ws = attn.attn_plan_partitions(64, 64, 32, 16, 64, 8192, req, num_sms=152)
         assert ws > 0                                 # head_dim 64 keeps the workspace
     # automatic GQA (head_dim 128: one CTA per SM; head_dim 64: two): with
-    # head_dim 128 and fewer (sequence, KV head) units than two per SM, the
+    # head_dim 128 and at most eight (sequence, KV head) units per SM, the
     # balanced split; otherwise (and for head_dim 64: fewer units than CTAs
     # -> one wave of slices) >= 4 items per CTA at full length and slices of
     # <= ~1024 keys
-    P, _ = attn.attn_plan_partitions(64, 64, 32, 8, 128, 8192, 0, num_sms=152)
-    assert P == 8
     BAL = attn.ATTN_PARTITIONS_BALANCED
-    for batch, rows, hkv, max_len in ((1, 1, 8, 131072), (16, 16, 8, 8192), (37, 37, 8, 5000)):
+    P, _ = attn.attn_plan_partitions(200, 200, 32, 8, 128, 8192, 0, num_sms=152)
+    assert P == 8                                     # 1600 units: slices of <= 1024 keys
+    for batch, rows, hkv, max_len in ((1, 1, 8, 131072), (16, 16, 8, 8192), (37, 37, 8, 5000),
+                                      (64, 64, 8, 8192), (152, 152, 8, 8192)):
         P, ws = attn.attn_plan_partitions(batch, rows, 8 * hkv // 2, hkv, 128, max_len, 0,
                                           num_sms=152)
         slots = 152 + batch * hkv
@@ -272,10 +273,12 @@ def test_planner_formulas(attn):
     assert P == 4 and ws == align(4 * 64 * 128 * 512 * 4) + 2 * align(4 * 64 * 128 * 4)
     P, _ = attn.attn_plan_partitions(1, 1, 32, 8, 128, 20, 0, num_sms=152)
     assert P == 1                                     # one tile of keys cannot split
-    # a few query rows per sequence (the 16-column fold): long items with two
-    # units per SM or more, else the balanced split
+    # a few query rows per sequence (the 16-column fold): the balanced split
+    # up to 8 units per SM, long items beyond
+    P, _ = attn.attn_plan_partitions(200, 500, 32, 8, 128, 8192, 0, num_sms=152, max_q_len=4)
+    assert P == 1                                     # 1600 units, >= 2 per CTA
     P, _ = attn.attn_plan_partitions(64, 160, 32, 8, 128, 8192, 0, num_sms=152, max_q_len=4)
-    assert P == 1                                     # 512 units, >= 2 per CTA
+    assert P == BAL                                   # 512 units
     P, ws = attn.attn_plan_partitions(16, 40, 32, 8, 128, 8192, 0, num_sms=152, max_q_len=4)
     assert P == BAL and ws > 0                        # 128 units
     P, _ = attn.attn_plan_partitions(2, 8, 32, 8, 128, 8192, 0, num_sms=152, max_q_len=4)

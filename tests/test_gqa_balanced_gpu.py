@@ -1,6 +1,6 @@
 """GPU parity of the balanced split of the tensor-core GQA decode kernel
 (attn_decode with num_partitions ATTN_PARTITIONS_BALANCED, the automatic
-choice for fewer (sequence, KV head) units than two per SM): the 128-key
+choice for at most eight (sequence, KV head) units per SM): the 128-key
 tiles of every unit, concatenated, are dealt out in equal contiguous ranges
 to one CTA per SM; units a range end cuts leave partials that the split-K
 reduce merges through a slot table.  Against the fp64 oracle, against one
