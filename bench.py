@@ -47,6 +47,8 @@ KERNEL_SOURCES = {
     "mla_decode": [_CSRC + f for f in ("mla_decode.cu", "tc.cuh", "ptx.cuh", "launch.h")],
     "tile_attention": [_CSRC + f for f in ("tile_attention.cu", "tc.cuh", "ptx.cuh",
                                            "launch.h")],
+    "tile_attention_pair": [_CSRC + f for f in ("tile_attention_pair.cu", "tc.cuh", "ptx.cuh",
+                                                "launch.h")],
 }
 
 
@@ -59,7 +61,9 @@ DOMINANT_KERNEL = {
 }
 
 
-def dominant_kernel(workload: str) -> str:
+def dominant_kernel(workload: str, partitions: int = 0) -> str:
+    if workload == "mixed" and partitions == -2:      # two Q tiles per CTA pair, on request
+        return "tile_attention_pair"
     return DOMINANT_KERNEL[workload]
 
 
@@ -521,7 +525,7 @@ def run_ours(args, rank, world, dist):
     achieved = nbytes / (mean_call_ms * 1e-3) / 1e9
     tflops = flops / (mean_call_ms * 1e-3) / 1e12
     tensor_peak = float(peaks.get("bf16_tflops", 1900.0))
-    kernel_key = dominant_kernel(args.workload)
+    kernel_key = dominant_kernel(args.workload, args.partitions)
     traffic = profiled_traffic(kernel_key, w.name)
     cpu = None
     if not args.no_cpu_baseline:

@@ -50,20 +50,22 @@ EncodeTiledFn encode_fn() {
 }
 
 // 4-D map over a cache operand: (channel, slot in page, kv head, page) with a
-// box of 64 channels (128 B, swizzled 128B) x box_rows slots x 1 x 1.
+// box of box_ch channels x box_rows slots x 1 x 1: 64 channels (128 B) with
+// the 128-byte swizzle, or 32 channels (64 B) with the 64-byte swizzle.
 int encode_kv_map(CUtensorMap *map, const attn_kv_t &kv, int dim, int num_kv_heads,
-                  int box_rows) {
+                  int box_rows, int box_ch = 64) {
     EncodeTiledFn fn = encode_fn();
     if (!fn) return ATTN_ERR_CUDA;
     cuuint64_t gdim[4] = {cuuint64_t(dim), cuuint64_t(kv.page_size), cuuint64_t(num_kv_heads),
                           cuuint64_t(kv.num_pages)};
     cuuint64_t gstride[3] = {cuuint64_t(kv.token_stride) * 2, cuuint64_t(kv.head_stride) * 2,
                              cuuint64_t(kv.page_stride) * 2};
-    cuuint32_t box[4] = {64, cuuint32_t(box_rows), 1, 1};
+    cuuint32_t box[4] = {cuuint32_t(box_ch), cuuint32_t(box_rows), 1, 1};
     cuuint32_t estride[4] = {1, 1, 1, 1};
     CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void *>(kv.base), gdim,
                     gstride, box, estride, CU_TENSOR_MAP_INTERLEAVE_NONE,
-                    CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                    box_ch == 64 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B,
+                    CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                     CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     return r == CUDA_SUCCESS ? ATTN_OK : ATTN_ERR_UNSUPPORTED;
 }
@@ -620,19 +622,20 @@ int check_kv_rows(const attn_kv_t *kv, int dim) {
     return ATTN_OK;
 }
 
-// The cache as a 2-D row array (channel, row) for gather4: box 64 channels x
-// one row, 128-byte swizzle.
-int encode_rows_map(CUtensorMap *map, const attn_kv_t &kv, int dim) {
+// The cache as a 2-D row array (channel, row) for gather4: box box_ch
+// channels x one row, 128-byte swizzle for 64 channels, 64-byte for 32.
+int encode_rows_map(CUtensorMap *map, const attn_kv_t &kv, int dim, int box_ch = 64) {
     EncodeTiledFn fn = encode_fn();
     if (!fn) return ATTN_ERR_CUDA;
     const long long rows = static_cast<long long>(kv.num_pages) * kv.page_size;
     cuuint64_t gdim[2] = {cuuint64_t(dim), cuuint64_t(rows)};
     cuuint64_t gstride[1] = {cuuint64_t(kv.token_stride) * 2};
-    cuuint32_t box[2] = {64, 1};
+    cuuint32_t box[2] = {cuuint32_t(box_ch), 1};
     cuuint32_t estride[2] = {1, 1};
     CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void *>(kv.base), gdim,
                     gstride, box, estride, CU_TENSOR_MAP_INTERLEAVE_NONE,
-                    CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                    box_ch == 64 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B,
+                    CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                     CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     return r == CUDA_SUCCESS ? ATTN_OK : ATTN_ERR_UNSUPPORTED;
 }
@@ -692,6 +695,9 @@ int mla_decode_impl(const void *q, const attn_kv_t *kv, const uint32_t *kv_len,
                                   : kMlaTileKeys;
     st = sparse ? encode_rows_map(&p.kv_map, *kv, dim_qk)
                 : encode_kv_map(&p.kv_map, *kv, dim_qk, 1, p.box_rows);
+    if (st) return st;
+    st = sparse ? encode_rows_map(&p.rope_map, *kv, dim_qk, kMlaRopeBoxCh)
+                : encode_kv_map(&p.rope_map, *kv, dim_qk, 1, p.box_rows, kMlaRopeBoxCh);
     if (st) return st;
     p.q = static_cast<const uint16_t *>(q);
     st = error_word(&p.err);

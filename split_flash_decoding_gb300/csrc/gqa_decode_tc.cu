@@ -26,7 +26,7 @@
 // TMEM and issues the MMAs.  Rings: 3 K stages and 3 V stages of 32 KB, each
 // consumed in order by the single MMA thread, so parity waits never alias.
 //
-// Balanced split (small batches): the 128-key tiles of every (sequence, KV
+// Balanced split (up to 8 units per SM): the 128-key tiles of every (sequence, KV
 // head) unit, concatenated, are dealt out in equal contiguous ranges, one per
 // CTA, so ragged lengths cannot leave SMs idle; a CTA walks the pieces of the
 // units its range meets, writes the units it holds whole and leaves a

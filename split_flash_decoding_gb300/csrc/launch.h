@@ -62,10 +62,12 @@ constexpr int kMlaTileKeys = 64;
 constexpr int kMlaHeads = 128;
 constexpr int kMlaDimQK = 576;
 constexpr int kMlaDimV = 512;
+constexpr int kMlaRopeBoxCh = 32;   // rope channels each CTA of an MLA pair loads
 
 struct MlaParams {
     CUtensorMap kv_map;           // 4-D: (channel 576, slot, head 1, page); sparse:
-                                  // 2-D (channel 576, row), box height 1
+                                  // 2-D (channel 576, row), box height 1; 64-channel boxes
+    CUtensorMap rope_map;         // the same cache with 32-channel boxes (64-byte swizzle)
     const uint16_t *q;            // bf16 [rows][128][576]
     const uint32_t *kv_len;       // [batch]
     const int32_t *page_table;    // [batch][max_pages] or nullptr

@@ -13,12 +13,14 @@
 // row (written by a one-CTA plan kernel that runs first); a run that is a
 // whole row writes the output, a run cut by a range end writes a partial
 // that the split-K reduce merges.  The 128 heads are the MMA's M dimension.
-// The two CTAs of a cluster split the 576 channels:
+// The two CTAs of a cluster split the 576 channels evenly:
 //
-//   rank 0 loads channels [0, 256)   = the first half of V (4 TMA boxes),
-//   rank 1 loads channels [256, 576) = the second half of V + rope (5 boxes),
+//   rank 0 loads channels [0, 256)   (its half of V) + rope [512, 544),
+//   rank 1 loads channels [256, 512) (its half of V) + rope [544, 576),
 //
-// so every byte of a K row is fetched from HBM exactly once per cluster.
+// as four 64-channel TMA boxes (128-byte swizzle) and one 32-channel box
+// (64-byte swizzle) per row group, so every byte of a K row is fetched from
+// HBM exactly once per cluster and both CTAs issue 18 score MMA steps.
 // Per 64-key tile each CTA computes a partial score S_r = Q[:, ch_r] K[:, ch_r]^T
 // with tcgen05.mma into TMEM, the two CTAs swap partials through distributed
 // shared memory and add them (fp32 addition is commutative, so both hold the
@@ -29,7 +31,8 @@
 // tile over the SM-to-SM network), so it is kept busy: the softmax warps
 // work one tile ahead, staging tile t+1's partial scores for the copy
 // before they run the softmax of tile t, which then overlaps the copy of
-// tile t+1.
+// tile t+1; and the receive side has three key-half slots, so the copy of
+// a half never waits for the peer to finish reading the previous tile.
 //
 // Warp roles (352 threads per CTA):
 //   warps 0-7  softmax: warps w and w+4 share head rows 32(w%4).. (their
@@ -46,12 +49,15 @@
 //              as soon as S(t+1) has been read, ahead of O(t)
 //   warp 10    exchange: two bulk copies per tile, one per key half
 //              (cp.async.bulk, shared::cta to the peer's shared::cluster,
-//              complete-tx on the peer's barrier of that half), 16 KB each;
-//              a half is staged while the other half is on the wire
+//              complete-tx on the peer's barrier of the receiving slot),
+//              16 KB each; a half is staged while the other half is on the
+//              wire.  Half i = 2 t + half of the CTA's tile sequence lands
+//              in receive slot i % 3.
 //
 // Q is the A operand of the score MMA straight from TMEM, so shared memory
-// holds only the K ring and the two exchange buffers.  TMEM columns: Q
-// [0, 160) (bf16 pairs), P [160, 192), S [192, 256), O half [256, 512).
+// holds only the K ring and the exchange buffers.  TMEM columns: Q [0, 144)
+// (bf16 pairs: 256 V channels, then 32 rope channels), P [160, 192), S
+// [192, 256), O half [256, 512).
 // The running max is kept lazily: P = exp2(s - m_ref) with m_ref raised (and
 // O rescaled) only when a tile's max exceeds m_ref by more than 8 (base 2),
 // so P <= 256 and O/l stay finite in fp32.
@@ -64,9 +70,11 @@ namespace {
 
 constexpr int kBN = kMlaTileKeys;          // 64 keys per tile
 constexpr int kStages = 4;
-constexpr int kMaxBoxes = 5;               // 64-channel boxes per rank (4 or 5)
+constexpr int kVBoxes = 4;                 // 64-channel boxes: this CTA's 256 V channels
 constexpr int kKBoxBytes = kBN * 128;      // 64 rows x 128 B
-constexpr int kStageBytes = kMaxBoxes * kKBoxBytes;
+constexpr int kRopeBoxBytes = kBN * 2 * kMlaRopeBoxCh;   // 64 rows x 64 B
+constexpr int kStageBytes = kVBoxes * kKBoxBytes + kRopeBoxBytes;   // 36 KB
+constexpr int kScoreSteps = (kVBoxes * 64 + kMlaRopeBoxCh) / 16;   // 18 MMAs of K = 16
 constexpr int kSoftmaxThreads = 256;   // warps 0-7
 
 // Warp roles.  Dense (paged or contiguous) caches: 352 threads, one TMA
@@ -87,11 +95,12 @@ struct Layout {
         return warp >= 14 ? warp - 10 : -1;
     }
 };
-constexpr int kBarSoftmax = 1;         // named barrier of the softmax warps
+constexpr int kBarPair = 2;            // + (warp & 3): the two softmax warps of a row quarter
 constexpr uint32_t kXBytes = 128u * kMlaTileKeys * 4u;   // one tile of fp32 partial scores
 constexpr uint32_t kXHalfBytes = kXBytes / 2;            // one key half (32 keys)
+constexpr int kXSlots = 3;                               // receive slots of key halves
 constexpr uint32_t kTmemCols = 512;
-constexpr uint32_t kTmemQ = 0;             // up to 160 columns of packed bf16 pairs
+constexpr uint32_t kTmemQ = 0;             // 144 columns of packed bf16 pairs
 constexpr uint32_t kTmemP = 160;           // 32 columns: P of one tile as bf16 pairs
 constexpr uint32_t kTmemS = 192;           // 64-column S buffer
 constexpr uint32_t kTmemO = 256;           // 256-column O half
@@ -103,8 +112,8 @@ constexpr uint32_t kVSbo = 1024;           // stride between 8-key groups
 
 struct Smem {
     static constexpr int kv = 0;
-    static constexpr int x_in = kv + kStages * kStageBytes;           // 160 KB
-    static constexpr int x_out = x_in + int(kXBytes);                 // +32 KB (peer's partial)
+    static constexpr int x_in = kv + kStages * kStageBytes;           // 144 KB
+    static constexpr int x_out = x_in + kXSlots * int(kXHalfBytes);   // +48 KB (peer's partials)
     static constexpr int red = x_out + int(kXBytes);                  // +32 KB (own partial)
     static constexpr int bars = red + 2 * 128 * 4;                    // +1 KB (row maxima)
     static constexpr int total = bars + 192;
@@ -119,20 +128,21 @@ enum Bar {
     kSFree,       // the softmax warps have read it (4 arrivals)
     kPFull,       // P of a tile in TMEM, V tail cleared (4 arrivals)
     kODone,       // O MMA of a tile finished (commit)
-    // [2] each: one per key half of the exchange buffers
-    kXFull,                     // peer's half landed in x_in (own expect_tx + peer's copy bytes)
-    kXPeerFree = kXFull + 2,    // the peer has read its half of x_in (its 4 warps of that half)
-    kXoReady = kXPeerFree + 2,  // own 4 softmax warps of the half staged x_out
-    kXoFree = kXoReady + 2,     // the bulk copy finished reading the half of x_out
+    // [kXSlots] each: one per receive slot
+    kXFull,                           // peer's half landed in the slot (own expect_tx + copy bytes)
+    kXPeerFree = kXFull + kXSlots,    // the peer has read the slot (its 4 warps of that half)
+    // [2] each: one per key half of x_out
+    kXoReady = kXPeerFree + kXSlots,  // own 4 softmax warps of the half staged x_out
+    kXoFree = kXoReady + 2,           // the bulk copy finished reading the half of x_out
     kXEnd = kXoFree + 2,
     kNumBars = kXEnd
 };
 
-// Partial score row h of one key half (32 keys, 128 B) in an exchange
-// buffer: 16-B chunk c at a row-dependent rotation, so the 8 rows of a
-// quarter-warp access hit all 32 banks.
-__device__ __forceinline__ uint32_t x_half_off(int hf, int h, int c) {
-    return uint32_t(hf) * kXHalfBytes + uint32_t(h * 128 + (((c + h) & 7) << 4));
+// Partial score row h of one key half (32 keys, 128 B) in slot k of an
+// exchange buffer: 16-B chunk c at a row-dependent rotation, so the 8 rows of
+// a quarter-warp access hit all 32 banks.
+__device__ __forceinline__ uint32_t x_half_off(int k, int h, int c) {
+    return uint32_t(k) * kXHalfBytes + uint32_t(h * 128 + (((c + h) & 7) << 4));
 }
 
 // One run of consecutive key tiles of one query row: keys [start, end) of
@@ -236,8 +246,8 @@ mla_decode_kernel(const __grid_constant__ MlaParams p) {
     const uint32_t peer = rank ^ 1u;
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
-    const int nbox = rank == 0 ? 4 : 5;
-    const int col0 = rank == 0 ? 0 : 256;
+    const int col0 = int(rank) * (kMlaDimV / 2);                 // this CTA's V channels
+    const int rope_col = kMlaDimV + int(rank) * kMlaRopeBoxCh;  // and rope channels
 
     SegWalk<kSparse> walk;
     walk.r = 1;
@@ -259,9 +269,11 @@ mla_decode_kernel(const __grid_constant__ MlaParams p) {
         mbar_init(&bar[kSFree], 8);
         mbar_init(&bar[kPFull], 8);
         mbar_init(&bar[kODone], 1);
-        for (int i = 0; i < 2; ++i) {
+        for (int i = 0; i < kXSlots; ++i) {
             mbar_init(&bar[kXFull + i], 1);
             mbar_init(&bar[kXPeerFree + i], 4);
+        }
+        for (int i = 0; i < 2; ++i) {
             mbar_init(&bar[kXoReady + i], 4);
             mbar_init(&bar[kXoFree + i], 1);
         }
@@ -296,14 +308,18 @@ mla_decode_kernel(const __grid_constant__ MlaParams p) {
             SegWalk<kSparse> w = walk;
             MlaSeg sg;
             int issued = 0;   // tiles of every run so far
-            if (lane == 0) prefetch_tensormap(&p.kv_map);
+            if (lane == 0) {
+                prefetch_tensormap(&p.kv_map);
+                prefetch_tensormap(&p.rope_map);
+            }
             if constexpr (kSparse) {
                 // Sparse top-k: key j of the sequence is cache row indices[b][j]
                 // (rows at a uniform stride).  Rows are scattered, so a tile
-                // arrives as gather4 copies (four rows x one 64-channel box,
-                // 512 bytes, swizzled like a tiled load): 16 row groups x
-                // nbox boxes per tile, spread over the six producer warps, one
-                // copy per lane (warp w, lane l takes copy w + 6 l).  Each warp
+                // arrives as gather4 copies (four rows x one box, swizzled like
+                // a tiled load: 512 bytes for a 64-channel box, 256 for the
+                // 32 rope channels): 16 row groups x 5 boxes per tile, spread
+                // over the six producer warps, one copy per lane (warp w,
+                // lane l takes copy w + 6 l).  Each warp
                 // posts the bytes of its own copies on the stage barrier, so
                 // the stage is full when all six warps' copies have landed and
                 // the producers run up to kStages tiles ahead, as for a dense
@@ -312,11 +328,12 @@ mla_decode_kernel(const __grid_constant__ MlaParams p) {
                 // masks the former and the error word reports the latter.
                 // The indices of tile i + 1 are loaded while tile i waits for
                 // its stage.
-                const int nq = 16 * nbox;
+                constexpr int kCopies = kVBoxes + 1;      // boxes per row group
+                const int nq = 16 * kCopies;
                 const int q = pidx + Roles::kProducers * lane;
                 const bool mine = q < nq;
-                const int g = mine ? q / nbox : 0;        // rows 4g .. 4g + 3 of the tile
-                const int cb = mine ? q - g * nbox : 0;   // 64-channel box
+                const int g = mine ? q / kCopies : 0;        // rows 4g .. 4g + 3 of the tile
+                const int cb = mine ? q - g * kCopies : 0;   // box; kVBoxes = the rope box
                 bool run = true;
                 while (run && w.next(p, sg)) {
                     const int32_t *idx = p.indices + size_t(sg.b) * size_t(p.indices_stride);
@@ -351,14 +368,19 @@ mla_decode_kernel(const __grid_constant__ MlaParams p) {
                             }
                         }
                         if (live && bad) atomicOr(p.err, kErrBadPage);
-                        const uint32_t n = __popc(__ballot_sync(0xffffffffu, live));
-                        if (lane == 0) mbar_arrive_expect_tx(&bar[kKvFull + s], n * 512u);
+                        const uint32_t bytes =
+                            __reduce_add_sync(0xffffffffu, live ? (cb < kVBoxes ? 512u : 256u) : 0u);
+                        if (lane == 0) mbar_arrive_expect_tx(&bar[kKvFull + s], bytes);
                         __syncwarp();   // the expected bytes are posted before any copy lands
-                        if (live)
-                            tma_gather4(smem + Smem::kv + s * kStageBytes + cb * kKBoxBytes +
-                                            g * 512,
-                                        &p.kv_map, &bar[kKvFull + s], col0 + cb * 64, cur[0],
-                                        cur[1], cur[2], cur[3]);
+                        uint8_t *st = smem + Smem::kv + s * kStageBytes;
+                        if (live && cb < kVBoxes)
+                            tma_gather4(st + cb * kKBoxBytes + g * 512, &p.kv_map,
+                                        &bar[kKvFull + s], col0 + cb * 64, cur[0], cur[1], cur[2],
+                                        cur[3]);
+                        else if (live)
+                            tma_gather4(st + kVBoxes * kKBoxBytes + g * 256, &p.rope_map,
+                                        &bar[kKvFull + s], rope_col, cur[0], cur[1], cur[2],
+                                        cur[3]);
                         issued = gi + 1;
 #pragma unroll
                         for (int u = 0; u < 4; ++u) cur[u] = nxt[u];
@@ -416,16 +438,21 @@ mla_decode_kernel(const __grid_constant__ MlaParams p) {
                                     uint32_t nrow = 0;
 #pragma unroll
                                     for (int r = 0; r < 8; ++r) nrow += pages[r] >= 0 ? 1u : 0u;
-                                    mbar_arrive_expect_tx(&bar[kKvFull + s],
-                                                          nrow * uint32_t(nbox) * uint32_t(box_rows) * 128u);
+                                    mbar_arrive_expect_tx(
+                                        &bar[kKvFull + s],
+                                        nrow * uint32_t(box_rows) * uint32_t(kVBoxes * 128 + 2 * kMlaRopeBoxCh));
                                     uint8_t *st = smem + Smem::kv + s * kStageBytes;
 #pragma unroll
                                     for (int r = 0; r < 8; ++r) {
                                         if (pages[r] < 0) continue;
-                                        for (int cb = 0; cb < nbox; ++cb)
+#pragma unroll
+                                        for (int cb = 0; cb < kVBoxes; ++cb)
                                             tma_load_4d(st + cb * kKBoxBytes + r * box_rows * 128,
                                                         &p.kv_map, &bar[kKvFull + s], col0 + cb * 64,
                                                         slots[r], 0, pages[r]);
+                                        tma_load_4d(st + kVBoxes * kKBoxBytes + r * box_rows * 2 * kMlaRopeBoxCh,
+                                                    &p.rope_map, &bar[kKvFull + s], rope_col, slots[r],
+                                                    0, pages[r]);
                                     }
                                 }
                             }
@@ -457,19 +484,20 @@ mla_decode_kernel(const __grid_constant__ MlaParams p) {
                     if (g >= 1 && !mbar_wait(&bar[kSFree], (g - 1) & 1, p.err)) return false;
                     tc::fence_after_sync();
                     const uint64_t b0 = tc::smem_desc_sw128(kv_base + s * kStageBytes, 16, 1024);
+                    const uint64_t br = tc::smem_desc_sw64(
+                        kv_base + s * kStageBytes + kVBoxes * kKBoxBytes, 16, 512);
 #pragma unroll
-                    for (int ks = 0; ks < 16; ++ks)
+                    for (int ks = 0; ks < 4 * kVBoxes; ++ks)
                         // A = Q from TMEM: 16 channels = 8 columns of bf16 pairs per step
                         tc::mma_bf16_tmem_a(tmem + kTmemS, tmem + kTmemQ + ks * 8,
                                             b0 + uint64_t(((ks >> 2) * kKBoxBytes + (ks & 3) * 32) >> 4),
                                             idesc_s, ks > 0);
-                    if (nbox == 5) {
 #pragma unroll
-                        for (int ks = 16; ks < 20; ++ks)
-                            tc::mma_bf16_tmem_a(tmem + kTmemS, tmem + kTmemQ + ks * 8,
-                                                b0 + uint64_t((4 * kKBoxBytes + (ks & 3) * 32) >> 4),
-                                                idesc_s, true);
-                    }
+                    for (int ks = 4 * kVBoxes; ks < kScoreSteps; ++ks)
+                        // the rope box: 64-byte rows, two steps of 32 bytes
+                        tc::mma_bf16_tmem_a(tmem + kTmemS, tmem + kTmemQ + ks * 8,
+                                            br + uint64_t(((ks - 4 * kVBoxes) * 32) >> 4), idesc_s,
+                                            true);
                     tc::mma_commit(&bar[kSFull]);
                     return true;
                 };
@@ -512,7 +540,9 @@ mla_decode_kernel(const __grid_constant__ MlaParams p) {
                 const uint32_t dst_bar = mapa_shared(smem_addr(&bar[kXFull]), peer);
                 const uint32_t src = smem_addr(smem + Smem::x_out);
                 // The two key halves go one after the other, so one half is
-                // staged while the other is on the wire.
+                // staged while the other is on the wire; half i = 2 g + hf
+                // goes to the peer's slot i % 3 once the peer has read that
+                // slot's previous half, i - 3.
                 SegWalk<kSparse> w = walk;
                 MlaSeg sg;
                 int G = 0;
@@ -521,14 +551,15 @@ mla_decode_kernel(const __grid_constant__ MlaParams p) {
                     for (int t = 0; run && t < sg.ntiles; ++t) {
                         const int g = G + t;
                         for (int hf = 0; hf < 2; ++hf) {
+                            const int i = 2 * g + hf, slot = i % kXSlots, use = i / kXSlots;
                             if (!mbar_wait(&bar[kXoReady + hf], g & 1, p.err) ||
-                                (g >= 1 &&
-                                 !mbar_wait_cluster(&bar[kXPeerFree + hf], (g - 1) & 1, p.err))) {
+                                (use >= 1 && !mbar_wait_cluster(&bar[kXPeerFree + slot],
+                                                                (use - 1) & 1, p.err))) {
                                 run = false;
                                 break;
                             }
-                            bulk_copy_to_peer(dst + hf * kXHalfBytes, src + hf * kXHalfBytes,
-                                              kXHalfBytes, dst_bar + 8u * hf);
+                            bulk_copy_to_peer(dst + slot * kXHalfBytes, src + hf * kXHalfBytes,
+                                              kXHalfBytes, dst_bar + 8u * slot);
                             bulk_wait_read();
                             mbar_arrive(&bar[kXoFree + hf]);
                         }
@@ -546,7 +577,7 @@ mla_decode_kernel(const __grid_constant__ MlaParams p) {
         uint8_t *x_in = smem + Smem::x_in;
         uint8_t *x_out = smem + Smem::x_out;
         float *red = reinterpret_cast<float *>(smem + Smem::red);
-        const uint32_t peer_xfree = mapa_shared(smem_addr(&bar[kXPeerFree + half]), peer);
+        const uint32_t peer_xfree = mapa_shared(smem_addr(&bar[kXPeerFree]), peer);
         const uint32_t s_col = kTmemS + 32u * half;
         SegWalk<kSparse> w = walk;
         MlaSeg sg;
@@ -558,10 +589,11 @@ mla_decode_kernel(const __grid_constant__ MlaParams p) {
             if (p.balanced && w.r < p.num_q_rows && w.nxt.x < w.x1) {
                 // The next run is row w.r: bring its Q lines of this CTA into
                 // L2 now, so the refill after this run reads them from there.
-                const uint8_t *qn = reinterpret_cast<const uint8_t *>(
-                    p.q + (size_t(w.r) * kMlaHeads + h) * kMlaDimQK + col0);
-                for (int cb = half; cb < nbox; cb += 2)
+                const uint16_t *qr = p.q + (size_t(w.r) * kMlaHeads + h) * kMlaDimQK;
+                const uint8_t *qn = reinterpret_cast<const uint8_t *>(qr + col0);
+                for (int cb = half; cb < kVBoxes; cb += 2)
                     asm volatile("prefetch.global.L2 [%0];" ::"l"(qn + cb * 128));
+                if (half == 1) asm volatile("prefetch.global.L2 [%0];" ::"l"(qr + rope_col));
             }
             float m_ref = -INFINITY;
             float l = 0.f, l_r = 0.f;   // this half's share of the row sums
@@ -570,10 +602,11 @@ mla_decode_kernel(const __grid_constant__ MlaParams p) {
             if (live) {
                 // This CTA's Q channels of head row h into TMEM lane h: 64
                 // channels (32 columns of bf16 pairs) per store, boxes split
-                // over the halves.  The last run's MMAs have all finished.
-                const uint4 *src = reinterpret_cast<const uint4 *>(
-                    p.q + (size_t(sg.qrow) * kMlaHeads + h) * kMlaDimQK + col0);
-                for (int cb = half; cb < nbox; cb += 2) {
+                // over the halves, then the 32 rope channels (16 columns).
+                // The last run's MMAs have all finished.
+                const uint16_t *qr = p.q + (size_t(sg.qrow) * kMlaHeads + h) * kMlaDimQK;
+                const uint4 *src = reinterpret_cast<const uint4 *>(qr + col0);
+                for (int cb = half; cb < kVBoxes; cb += 2) {
                     float v[32];
 #pragma unroll
                     for (int i = 0; i < 8; ++i) {
@@ -584,6 +617,18 @@ mla_decode_kernel(const __grid_constant__ MlaParams p) {
                         v[4 * i + 3] = __uint_as_float(wq.w);
                     }
                     tc::tmem_st32(tmem + lane_base + kTmemQ + cb * 32, v);
+                }
+                if (half == 1) {
+                    const uint4 *rp = reinterpret_cast<const uint4 *>(qr + rope_col);
+#pragma unroll
+                    for (int k = 0; k < 2; ++k) {
+                        const uint4 a = rp[2 * k], b = rp[2 * k + 1];
+                        const float v[8] = {__uint_as_float(a.x), __uint_as_float(a.y),
+                                            __uint_as_float(a.z), __uint_as_float(a.w),
+                                            __uint_as_float(b.x), __uint_as_float(b.y),
+                                            __uint_as_float(b.z), __uint_as_float(b.w)};
+                        tc::tmem_st_n<8>(tmem + lane_base + kTmemQ + 4 * kVBoxes * 8 + 8 * k, v);
+                    }
                 }
                 tc::tmem_wait_st();
                 tc::fence_before_sync();
@@ -620,7 +665,9 @@ mla_decode_kernel(const __grid_constant__ MlaParams p) {
                 const int g = G + t;   // tile of the CTA's run list
                 const int t0 = start + t * kBN;
                 const int nvalid = min(kBN, end - t0) - 32 * half;   // this half's valid keys
-                if (live && h == 0) mbar_arrive_expect_tx(&bar[kXFull + half], kXHalfBytes);
+                const int xi = 2 * g + half;             // this half's receive slot and use
+                const int xslot = xi % kXSlots;
+                if (live && h == 0) mbar_arrive_expect_tx(&bar[kXFull + xslot], kXHalfBytes);
 
                 // ---- one tile ahead: partial S(g+1) out of TMEM, staged for the copy
                 float s_next[32];
@@ -651,31 +698,42 @@ mla_decode_kernel(const __grid_constant__ MlaParams p) {
 
                 // ---- full S(g) = own partial + the peer's ------------------------
                 if (live)
-                    live = __all_sync(0xffffffffu,
-                                      mbar_wait_cluster(&bar[kXFull + half], g & 1, p.err));
+                    live = __all_sync(0xffffffffu, mbar_wait_cluster(&bar[kXFull + xslot],
+                                                                     (xi / kXSlots) & 1, p.err));
                 float mloc = -INFINITY;
                 if (live) {
 #pragma unroll
                     for (int c = 0; c < 8; ++c) {
                         const float4 o =
-                            *reinterpret_cast<const float4 *>(x_in + x_half_off(half, h, c));
-                        s_own[4 * c] += o.x;
-                        s_own[4 * c + 1] += o.y;
-                        s_own[4 * c + 2] += o.z;
-                        s_own[4 * c + 3] += o.w;
+                            *reinterpret_cast<const float4 *>(x_in + x_half_off(xslot, h, c));
+                        const float2 a = __fadd2_rn(make_float2(s_own[4 * c], s_own[4 * c + 1]),
+                                                    make_float2(o.x, o.y));
+                        const float2 b = __fadd2_rn(make_float2(s_own[4 * c + 2], s_own[4 * c + 3]),
+                                                    make_float2(o.z, o.w));
+                        s_own[4 * c] = a.x;
+                        s_own[4 * c + 1] = a.y;
+                        s_own[4 * c + 2] = b.x;
+                        s_own[4 * c + 3] = b.y;
                     }
                     __syncwarp();   // the warp's reads of x_in happen before the release
                     // The values read from x_in are already consumed (added into
                     // s_own) when the arrive issues, so a relaxed arrive suffices.
                     if (lane == 0)
                         asm volatile("mbarrier.arrive.relaxed.cluster.shared::cluster.b64 _, [%0];"
-                                     ::"r"(peer_xfree) : "memory");
-                    if (nvalid >= 32) {
+                                     ::"r"(peer_xfree + 8u * uint32_t(xslot)) : "memory");
+                    if (p.qk_scale_log2 > 0.f) {
+                        // Raw scores stay in s_own (keys past the run end -inf);
+                        // the scale goes into the exponent's FMA and, being
+                        // positive, commutes with the max (a tree of 3-input maxima).
+                        if (nvalid < 32) {
 #pragma unroll
-                        for (int j = 0; j < 32; ++j) {
-                            s_own[j] *= p.qk_scale_log2;
-                            mloc = fmaxf(mloc, s_own[j]);
+                            for (int j = 0; j < 32; ++j) s_own[j] = j < nvalid ? s_own[j] : -INFINITY;
                         }
+                        float m4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+#pragma unroll
+                        for (int j = 0; j < 32; j += 2)
+                            m4[(j >> 1) & 3] = fmax3(m4[(j >> 1) & 3], s_own[j], s_own[j + 1]);
+                        mloc = fmaxf(fmaxf(m4[0], m4[1]), fmaxf(m4[2], m4[3])) * p.qk_scale_log2;
                     } else {
 #pragma unroll
                         for (int j = 0; j < 32; ++j) {
@@ -685,9 +743,10 @@ mla_decode_kernel(const __grid_constant__ MlaParams p) {
                     }
                 }
                 // ---- row max over both halves --------------------------------
-                named_sync(kBarSoftmax, kSoftmaxThreads);   // the last reads of red are done
+                // the two warps of this row quarter (same SM sub-partition)
+                named_sync(kBarPair + (warp & 3), 64);   // the last reads of red are done
                 red[half * 128 + h] = mloc;
-                named_sync(kBarSoftmax, kSoftmaxThreads);
+                named_sync(kBarPair + (warp & 3), 64);
                 const float mt = fmaxf(mloc, red[(half ^ 1) * 128 + h]);
 
                 if (live) {
@@ -700,17 +759,28 @@ mla_decode_kernel(const __grid_constant__ MlaParams p) {
                     }
                     // Two row sums: of the fp32 weights (for lse) and of the bf16-
                     // rounded weights the MMA multiplies V by (to normalise O).
-                    float rowsum = 0.f, rowsum_r = 0.f;
+                    // Key pairs go through the packed fp32x2 FMA (score times the
+                    // folded scale minus m_ref: m_ref is finite here, every tile
+                    // having a visible key in its first half) and adds.
+                    const float sc_mul = p.qk_scale_log2 > 0.f ? p.qk_scale_log2 : 1.f;
+                    const float2 mul2 = make_float2(sc_mul, sc_mul);
+                    const float2 neg2 = make_float2(-m_ref, -m_ref);
+                    float2 rs[2] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
+                    float2 rr[2] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
                     float pk[16];
 #pragma unroll
                     for (int j = 0; j < 16; ++j) {
-                        const float p0 = fast_exp2(s_own[2 * j] - m_ref);
-                        const float p1 = fast_exp2(s_own[2 * j + 1] - m_ref);
+                        const float2 e =
+                            __ffma2_rn(make_float2(s_own[2 * j], s_own[2 * j + 1]), mul2, neg2);
+                        const float p0 = fast_exp2(e.x);
+                        const float p1 = fast_exp2(e.y);
                         const uint32_t wp = pack_bf16x2(p0, p1);
                         pk[j] = __uint_as_float(wp);
-                        rowsum += p0 + p1;
-                        rowsum_r += bf16_lo(wp) + bf16_hi(wp);
+                        rs[j & 1] = __fadd2_rn(rs[j & 1], make_float2(p0, p1));
+                        add_bf16x2_f32(rr[j & 1], wp);
                     }
+                    const float rowsum = (rs[0].x + rs[1].x) + (rs[0].y + rs[1].y);
+                    const float rowsum_r = (rr[0].x + rr[1].x) + (rr[0].y + rr[1].y);
                     l = l * alpha + rowsum;
                     l_r = l_r * alpha + rowsum_r;
 
@@ -720,14 +790,15 @@ mla_decode_kernel(const __grid_constant__ MlaParams p) {
                                           mbar_wait(&bar[kODone], (g - 1) & 1, p.err));
                         tc::fence_after_sync();
                         if (live && __any_sync(0xffffffffu, raise)) {
+                            // 8 columns at a time: both score arrays are live here
 #pragma unroll 1
-                            for (int c = 0; c < 128; c += 32) {
-                                float v[32];
+                            for (int c = 0; c < 128; c += 8) {
+                                float v[8];
                                 const uint32_t oc = kTmemO + 128u * half + c;
-                                tc::tmem_ld32(tmem + lane_base + oc, v);
+                                tc::tmem_ld_n<8>(tmem + lane_base + oc, v);
 #pragma unroll
-                                for (int j = 0; j < 32; ++j) v[j] *= alpha;
-                                tc::tmem_st32(tmem + lane_base + oc, v);
+                                for (int j = 0; j < 8; ++j) v[j] *= alpha;
+                                tc::tmem_st_n<8>(tmem + lane_base + oc, v);
                             }
                         }
                     }
@@ -775,13 +846,13 @@ mla_decode_kernel(const __grid_constant__ MlaParams p) {
             }
             // Row sums of the two halves (same m_ref), one after the other
             // through the row-max buffer.
-            named_sync(kBarSoftmax, kSoftmaxThreads);
+            named_sync(kBarPair + (warp & 3), 64);
             red[half * 128 + h] = l;
-            named_sync(kBarSoftmax, kSoftmaxThreads);
+            named_sync(kBarPair + (warp & 3), 64);
             const float l_other = red[(half ^ 1) * 128 + h];
-            named_sync(kBarSoftmax, kSoftmaxThreads);
+            named_sync(kBarPair + (warp & 3), 64);
             red[half * 128 + h] = l_r;
-            named_sync(kBarSoftmax, kSoftmaxThreads);
+            named_sync(kBarPair + (warp & 3), 64);
             l_r += red[(half ^ 1) * 128 + h];
             l += l_other;
             // O was accumulated with the rounded weights: normalise it by their
