@@ -110,3 +110,39 @@ def test_workload_full_size_sampled(attn):
     ri = torch.tensor(rows)
     hi = torch.tensor(heads)
     assert_close(out[ri, hi], lse[ri, hi], ref_o, ref_l, "few-token workload sampled")
+
+
+def test_graph_capture_replays_with_new_lengths(attn):
+    """Draft rows on the balanced split: one captured call replayed with other
+    cache lengths (the rows per sequence fixed by the captured offsets)."""
+    q_lens, lens = [1, 4, 2, 3], [700, 2500, 130, 64]
+    w = few_workload(q_lens, lens, seed=69, sink=True)
+    P, ws_bytes = attn.attn_plan_partitions(4, w.rows, 32, 8, 128, 2500, 0, max_q_len=4)
+    assert P == attn.ATTN_PARTITIONS_BALANCED
+    ws = torch.empty(ws_bytes, dtype=torch.uint8, device=DEV)
+    out = torch.empty(w.rows, 32, 128, dtype=torch.bfloat16, device=DEV)
+    lse = torch.empty(w.rows, 32, dtype=torch.float32, device=DEV)
+    kv_len = w.kv_len.clone()
+    s = torch.cuda.Stream()
+
+    def call():
+        attn.attn_decode(w.q, w.k_cache, w.v_cache, kv_len, group=4, scale=w.scale,
+                         max_kv_len=2500, page_table=w.page_table, sink=w.sink,
+                         q_row_offsets=w.q_row_offsets, max_q_len=4, causal=True,
+                         num_partitions=P, workspace=ws, out=out, lse=lse, stream=s)
+
+    with torch.cuda.stream(s):
+        call()
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=s):
+        call()
+    for new in ([700, 2500, 130, 64], [4, 1999, 128, 3]):
+        kv_len.copy_(torch.tensor(new, dtype=torch.int32))
+        g.replay()
+        torch.cuda.synchronize()
+        w2 = few_workload(q_lens, lens, seed=69, sink=True)
+        w2.kv_len_host = new
+        w2.kv_len = kv_len
+        ref_o, ref_l = oracle_result(w2)
+        assert_close(out, lse, ref_o, ref_l, f"few-token graph replay {new}")

@@ -198,3 +198,39 @@ def test_bad_page_sets_error_bit_and_context_survives(attn):
     out, lse = run(attn, w, attn.ATTN_PARTITIONS_BALANCED)
     ref_o, ref_l = oracle_result(w)
     assert_close(out, lse, ref_o, ref_l, "balanced after a bad page")
+
+
+def test_graph_capture_replays_with_new_lengths(attn):
+    """The balanced split is planned on the device from kv_len, so one
+    captured call (plan kernel, decode, reduce) serves any lengths up to the
+    planned maximum: replayed with other lengths, including an empty row."""
+    lens = [3000, 64, 1500, 700]
+    w = mla_workload(lens, seed=90)
+    P, ws_bytes = attn.attn_plan_partitions(4, 4, 128, 1, 512, 3000, 0)
+    assert P == 0
+    ws = torch.empty(ws_bytes, dtype=torch.uint8, device=DEV)
+    out = torch.empty(4, 128, 512, dtype=torch.bfloat16, device=DEV)
+    lse = torch.empty(4, 128, dtype=torch.float32, device=DEV)
+    kv_len = w.kv_len.clone()
+    s = torch.cuda.Stream()
+
+    def call():
+        attn.attn_mla_decode(w.q, w.k_cache, kv_len, scale=w.scale, max_kv_len=3000,
+                             page_table=w.page_table, num_partitions=P, workspace=ws, out=out,
+                             lse=lse, stream=s)
+
+    with torch.cuda.stream(s):
+        call()
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=s):
+        call()
+    for new in ([3000, 64, 1500, 700], [1, 2999, 65, 0]):
+        kv_len.copy_(torch.tensor(new, dtype=torch.int32))
+        g.replay()
+        torch.cuda.synchronize()
+        w2 = mla_workload(lens, seed=90)
+        w2.kv_len_host = new
+        w2.kv_len = kv_len
+        ref_o, ref_l = oracle_result(w2)
+        assert_close(out, lse, ref_o, ref_l, f"mla graph replay {new}")
