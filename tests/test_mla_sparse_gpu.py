@@ -186,3 +186,41 @@ def test_deepseek_v32_sparse_full_size_sampled(attn):
     o1, l1 = run(attn, w, 1)
     assert_consistent(out, lse, o1, l1, float(ref_o.eps.max()),
                       "deepseek-v3.2 sparse auto P vs P=1")
+
+
+def test_graph_capture_replays_with_new_index_lists(attn):
+    """One captured sparse call replayed with other index lists and counts
+    (lists swapped between sequences, shortened, one emptied)."""
+    w = sparse_workload([900, 2500, 130, 3000], topk=640, seed=36)
+    stride = w.indices.shape[1]
+    P, ws_bytes = attn.attn_plan_partitions(4, 4, 128, 1, 512, stride, 0)
+    ws = torch.empty(max(ws_bytes, 1), dtype=torch.uint8, device=DEV)
+    out = torch.empty(4, 128, 512, dtype=torch.bfloat16, device=DEV)
+    lse = torch.empty(4, 128, dtype=torch.float32, device=DEV)
+    idx = w.indices.clone()
+    cnt = w.kv_len.clone()
+    s = torch.cuda.Stream()
+
+    def call():
+        attn.attn_mla_decode_sparse(w.q, w.k_cache, idx, cnt, scale=w.scale, num_partitions=P,
+                                    workspace=ws, out=out, lse=lse, stream=s)
+
+    with torch.cuda.stream(s):
+        call()
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=s):
+        call()
+    swapped = w.indices.clone()
+    swapped[0], swapped[3] = w.indices[3].clone(), w.indices[0].clone()
+    for new_idx, new_cnt in ((w.indices, list(w.kv_len_host)), (swapped, [640, 1, 0, 300])):
+        idx.copy_(new_idx)
+        cnt.copy_(torch.tensor(new_cnt, dtype=torch.int32))
+        g.replay()
+        torch.cuda.synchronize()
+        w2 = sparse_workload([900, 2500, 130, 3000], topk=640, seed=36)
+        w2.indices = idx
+        w2.kv_len = cnt
+        w2.kv_len_host = new_cnt
+        ref_o, ref_l = oracle_result(w2)
+        assert_close(out, lse, ref_o, ref_l, f"sparse graph replay {new_cnt}")

@@ -156,3 +156,39 @@ def test_pair_and_one_tile_kernels_agree(attn, q_lens, prefix):
     assert bits_equal(o0, o1) and bits_equal(l0, l1)
     ref_o, ref_l = oracle_result(w)
     assert_pair(o2, l2, o1, l1, ref_o, ref_l, f"pair vs one tile {q_lens}")
+
+
+@KERNELS
+def test_graph_capture_replays_with_new_prefixes(attn, kern):
+    """One captured tile call replayed with other cached prefixes (the rows
+    per sequence fixed by the captured offsets, causal alignment following
+    the new lengths)."""
+    q_lens, prefix = [300, 1, 140, 7], [200, 900, 0, 260]
+    w = tile_workload(q_lens, prefix, seed=95, sink=True)
+    out = torch.empty(w.rows, w.num_q_heads, 128, dtype=torch.bfloat16, device=DEV)
+    lse = torch.empty(w.rows, w.num_q_heads, dtype=torch.float32, device=DEV)
+    kv_len = w.kv_len.clone()
+    s = torch.cuda.Stream()
+
+    def call():
+        attn.attn_decode(w.q, w.k_cache, w.v_cache, kv_len, group=w.group, scale=w.scale,
+                         max_kv_len=w.max_kv_len, page_table=w.page_table, sink=w.sink,
+                         q_row_offsets=w.q_row_offsets, max_q_len=w.max_q_len, causal=True,
+                         num_partitions=kern, out=out, lse=lse, stream=s)
+
+    with torch.cuda.stream(s):
+        call()
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=s):
+        call()
+    for new_prefix in (prefix, [17, 0, 500, 1]):
+        new = [p + n for p, n in zip(new_prefix, q_lens)]
+        kv_len.copy_(torch.tensor(new, dtype=torch.int32))
+        g.replay()
+        torch.cuda.synchronize()
+        w2 = tile_workload(q_lens, prefix, seed=95, sink=True)
+        w2.kv_len_host = new
+        w2.kv_len = kv_len
+        ref_o, ref_l = oracle_result(w2)
+        assert_close(out, lse, ref_o, ref_l, f"tile graph replay {new_prefix} kern={kern}")
