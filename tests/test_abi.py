@@ -237,6 +237,11 @@ def test_planner_formulas(attn):
         slots = 152 + batch * hkv
         assert P == BAL
         assert ws == align(slots * 16 * 128 * 4) + 2 * align(slots * 16 * 4) + align(batch * hkv * 8)
+    # the rule's edge: 8 units per SM exactly is balanced, one sequence more is not
+    assert attn.attn_plan_partitions(152, 152, 32, 8, 128, 8192, 0, num_sms=152)[0] == BAL
+    assert attn.attn_plan_partitions(153, 153, 32, 8, 128, 8192, 0, num_sms=152)[0] > 0
+    assert attn.attn_plan_partitions(16, 16, 32, 8, 128, 8192, 0, num_sms=16)[0] == BAL
+    assert attn.attn_plan_partitions(17, 17, 32, 8, 128, 8192, 0, num_sms=16)[0] > 0
     # one tile per unit cannot be balanced further: one slice
     assert attn.attn_plan_partitions(16, 16, 32, 8, 128, 128, 0, num_sms=152) == (1, 0)
     P, _ = attn.attn_plan_partitions(1, 1, 16, 8, 64, 131072, 0, num_sms=152)
