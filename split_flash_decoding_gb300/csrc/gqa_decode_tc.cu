@@ -27,8 +27,9 @@
 // consumed in order by the single MMA thread, so parity waits never alias.
 //
 // Balanced split (up to 8 units per SM): the 128-key tiles of every (sequence, KV
-// head) unit, concatenated, are dealt out in equal contiguous ranges, one per
-// CTA, so ragged lengths cannot leave SMs idle; a CTA walks the pieces of the
+// head) unit, concatenated, are dealt out in contiguous ranges of equal cost
+// (tiles plus a fixed cost per unit opened), one per CTA, so ragged lengths
+// cannot leave SMs idle; a CTA walks the pieces of the
 // units its range meets, writes the units it holds whole and leaves a
 // 16-column partial in slot (CTA + unit) for each piece of a cut unit; the
 // CTA holding a unit's first tile publishes the unit's slot range for the
@@ -180,7 +181,7 @@ __device__ __forceinline__ GqaWalk make_walk(const GqaParams &p, const int *cum,
     w.first = C > 1 ? int(blockIdx.x) / C : int(blockIdx.x);
     w.stride = C > 1 ? int(gridDim.x) / C : int(gridDim.x);
     w.count = C > 1 ? p.batch * hkv : cum[p.batch];
-    w.x0 = w.x1 = w.tiles = w.ctas = 0;
+    w.x0 = w.x1 = w.tiles = w.wtiles = w.ctas = 0;
     w.u0 = 0;
     return w;
 }
@@ -632,11 +633,13 @@ gqa_decode_tc_kernel(const __grid_constant__ GqaParams p) {
                 if (p.balanced && it.first && threadIdx.x == 0) {
                     // The CTA holding the unit's first tile publishes where its
                     // pieces are: slots c + unit for the CTAs c holding its
-                    // first through last tile (CTA ((x + 1) C' - 1) / T holds
-                    // tile x).
-                    const long long last = it.unit_x + it.unit_tiles - 1;
+                    // first through last tile (CTA ((y + 1) C' - 1) / T_w holds
+                    // weighted position y; tile x of unit u sits at y = x +
+                    // kGqaUnitCost (u + 1)).
+                    const long long last = it.unit_x + it.unit_tiles - 1 +
+                                           static_cast<long long>(kGqaUnitCost) * (it.unit + 1);
                     const int c_last =
-                        static_cast<int>(((last + 1) * walk.ctas - 1) / walk.tiles);
+                        static_cast<int>(((last + 1) * walk.ctas - 1) / walk.wtiles);
                     const int c_first = static_cast<int>(blockIdx.x);
                     p.unit_slots[it.unit] = make_int2(c_first + it.unit, c_last - c_first + 1);
                 }

@@ -25,13 +25,20 @@ struct GqaItem {
 
 // This CTA's items: j = first, first + stride, ... < count.  The balanced
 // split also keeps the CTA's tile range [x0, x1) of the concatenation of
-// every unit's tiles (tiles in all, dealt over ctas CTAs) and the unit of
-// its first tile.
+// every unit's tiles (tiles in all; wtiles weighted positions dealt over
+// ctas CTAs) and the unit of its first tile.
 struct GqaWalk {
     int first, stride, count;
-    long long x0, x1, tiles, ctas;
+    long long x0, x1, tiles, wtiles, ctas;
     int u0;
 };
+
+// Balanced split: a CTA's time is its tiles plus a fixed cost for every unit
+// it opens (the unit's Q, the pipeline refill, the epilogue and partial),
+// about this many tiles' worth.  The split deals out a weighted
+// concatenation in which every unit is preceded by that many virtual tiles,
+// so a CTA whose range meets more units gets fewer tiles.
+constexpr int kGqaUnitCost = 2;
 
 // Unit (sequence b, KV head) holding global tile x: cum[b] <= x < cum[b+1].
 __device__ __forceinline__ int gqa_unit_of(const int *cum, int batch, int hkv, long long x) {
@@ -44,24 +51,51 @@ __device__ __forceinline__ int gqa_unit_of(const int *cum, int batch, int hkv, l
     return lo * hkv + static_cast<int>((x - cum[lo]) / per_head);
 }
 
+// Weighted concatenation of the balanced split: unit u (n_u tiles, starting
+// at tile x_u) occupies positions [x_u + kGqaUnitCost u, x_u + kGqaUnitCost
+// (u + 1) + n_u), its virtual tiles first, so real tile x of unit u sits at
+// x + kGqaUnitCost (u + 1).  The real tile a position y < T_w maps to (a
+// position in a virtual block: the unit's first tile).
+__device__ __forceinline__ long long gqa_tile_of_position(const int *cum, int batch, int hkv,
+                                                          long long y) {
+    const long long per_seq = static_cast<long long>(kGqaUnitCost) * hkv;
+    int lo = 0, hi = batch;   // sequence b: cum[b] + per_seq b <= y
+    while (hi - lo > 1) {
+        const int mid = (lo + hi) >> 1;
+        if (cum[mid] + per_seq * mid <= y) lo = mid; else hi = mid;
+    }
+    const long long n = (cum[lo + 1] - cum[lo]) / hkv;   // tiles per unit of sequence lo
+    const long long off = y - (cum[lo] + per_seq * lo);
+    const long long h = off / (n + kGqaUnitCost);
+    const long long o = off - h * (n + kGqaUnitCost) - kGqaUnitCost;
+    return cum[lo] + h * n + min(max(o, 0LL), n);
+}
+
 // Balanced split: this CTA's tile range and units.  CTA c of C' = min(grid,
-// tiles) takes tiles [c T / C', (c + 1) T / C'), at least one; CTAs past C'
-// take none.
+// tiles) takes the weighted positions [c T_w / C', (c + 1) T_w / C'), i.e.
+// the real tiles from the image of its first position up to the next
+// CTA's; CTAs past C' take none, and a range inside one virtual block is
+// empty.
 __device__ __forceinline__ GqaWalk gqa_balanced_walk(const GqaParams &p, const int *cum, int hkv) {
     GqaWalk w;
     w.first = 0;
     w.stride = 1;
     w.tiles = cum[p.batch];
+    w.wtiles = w.tiles + static_cast<long long>(kGqaUnitCost) * hkv * p.batch;
     w.ctas = min(static_cast<long long>(gridDim.x), w.tiles);
     const long long c = blockIdx.x;
     w.count = 0;
     w.u0 = 0;
     w.x0 = w.x1 = 0;
     if (c < w.ctas) {
-        w.x0 = c * w.tiles / w.ctas;
-        w.x1 = (c + 1) * w.tiles / w.ctas;
-        w.u0 = gqa_unit_of(cum, p.batch, hkv, w.x0);
-        w.count = gqa_unit_of(cum, p.batch, hkv, w.x1 - 1) - w.u0 + 1;
+        w.x0 = gqa_tile_of_position(cum, p.batch, hkv, c * w.wtiles / w.ctas);
+        w.x1 = c + 1 == w.ctas
+                   ? w.tiles
+                   : gqa_tile_of_position(cum, p.batch, hkv, (c + 1) * w.wtiles / w.ctas);
+        if (w.x1 > w.x0) {
+            w.u0 = gqa_unit_of(cum, p.batch, hkv, w.x0);
+            w.count = gqa_unit_of(cum, p.batch, hkv, w.x1 - 1) - w.u0 + 1;
+        }
     }
     return w;
 }

@@ -929,14 +929,52 @@ mla_decode_kernel(const __grid_constant__ MlaParams p) {
 
 // Balanced split plan (one CTA, ahead of the decode grid).  Row r of the
 // concatenation has n_r = ceil(visible keys / 64) tiles starting at tile
-// cum_r; cluster c of C = min(clusters, T) takes tiles [c T / C, (c+1) T / C)
-// of the T in all, at least one each.
-// Pass 1 counts the tiles sequence by sequence (1024 at a time with a running
-// total) and writes each row's entry; pass 2 finds, for each row, the
-// clusters whose range starts in it and the slots of its partials: the
-// cluster holding tile x is ((x + 1) C - 1) / T, and cluster c writes row r's
-// partial to slot c + r, so a row's partials are consecutive.
+// cum_r.  A cluster's time is its tiles plus a fixed cost for every run it
+// opens (the row's Q into TMEM and the pipeline refill, then the epilogue:
+// about kRunCost tiles' worth), so the split deals out a weighted
+// concatenation in which every row with tiles is preceded by kRunCost
+// virtual tiles: row r occupies weighted positions [W_r, W_r + kRunCost +
+// n_r), its real tile x at y(x) = x - cum_r + W_r + kRunCost.  Cluster c of
+// C = min(clusters, T) takes weighted positions [c T' / C, (c+1) T' / C) of
+// the T' in all, i.e. the real tiles from the image of its first position
+// (a position inside a virtual block maps to the row's first tile) up to
+// the next cluster's; a range inside one virtual block is empty.  A cluster
+// whose range meets more rows so gets fewer tiles.
+// Pass 1 counts the tiles (and weighted tiles) sequence by sequence (1024
+// at a time with running totals) and writes each row's entry; pass 2 finds,
+// for each row, the clusters whose range starts in it and the slots of its
+// partials: the cluster holding weighted position y is ((y + 1) C - 1) / T',
+// and cluster c writes row r's partial to slot c + r, so a row's partials
+// are consecutive.
 constexpr int kPlanThreads = 1024;
+constexpr int kRunCost = 8;
+
+// Exclusive scan of v over the block (1024 threads), continuing from carry;
+// carry advances by the block total.
+__device__ __forceinline__ int plan_block_scan(int v, int &carry, int *warp_tot, int lane, int wid) {
+    int incl = v;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const int u = __shfl_up_sync(0xffffffffu, incl, o);
+        if (lane >= o) incl += u;
+    }
+    if (lane == 31) warp_tot[wid] = incl;
+    __syncthreads();
+    if (wid == 0) {
+        int t = warp_tot[lane];
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const int u = __shfl_up_sync(0xffffffffu, t, o);
+            if (lane >= o) t += u;
+        }
+        warp_tot[lane] = t;
+    }
+    __syncthreads();
+    const int excl = carry + (wid > 0 ? warp_tot[wid - 1] : 0) + incl - v;
+    carry += warp_tot[kPlanThreads / 32 - 1];
+    __syncthreads();   // warp_tot is rewritten by the next scan
+    return excl;
+}
 
 __global__ void __launch_bounds__(kPlanThreads) mla_plan_kernel(const __grid_constant__ MlaParams p) {
     pdl_launch_dependents();   // the decode CTAs may set up while this runs
@@ -945,13 +983,16 @@ __global__ void __launch_bounds__(kPlanThreads) mla_plan_kernel(const __grid_con
     const int rows = p.num_q_rows;
     for (int c = tid; c < p.num_clusters; c += kPlanThreads)
         p.plan_cluster[c] = make_int4(0, 0, rows, 0);   // no rows unless found below
-    for (int r = tid; r < rows; r += kPlanThreads) p.plan_rows[r] = make_int4(0, 0, 0, 0);
+    for (int r = tid; r < rows; r += kPlanThreads) {
+        p.plan_rows[r] = make_int4(0, 0, 0, 0);
+        p.plan_slots[r] = make_int2(0, 0);
+    }
     __syncthreads();
     const uint32_t cap = uint32_t(p.len_cap);
-    int carry = 0;
+    int carry = 0, carry_w = 0;
     for (int b0 = 0; b0 < p.batch; b0 += kPlanThreads) {
         const int b = b0 + tid;
-        int n_seq = 0, r0 = 0, nr = 0, L = 0;
+        int n_seq = 0, w_seq = 0, r0 = 0, nr = 0, L = 0;
         if (b < p.batch) {
             const uint32_t len_in = p.kv_len[b];
             if (len_in > cap) atomicOr(p.err, kErrBadLength);
@@ -962,54 +1003,49 @@ __global__ void __launch_bounds__(kPlanThreads) mla_plan_kernel(const __grid_con
             if (r0 < 0) nr = 0;
             for (int i = 0; i < nr; ++i) {
                 const int vis = p.causal ? max(0, min(L, L - nr + i + 1)) : L;
-                n_seq += (vis + kBN - 1) / kBN;
+                const int n = (vis + kBN - 1) / kBN;
+                n_seq += n;
+                w_seq += n > 0 ? n + kRunCost : 0;
             }
         }
-        int incl = n_seq;   // inclusive scan over the block
-#pragma unroll
-        for (int o = 1; o < 32; o <<= 1) {
-            const int v = __shfl_up_sync(0xffffffffu, incl, o);
-            if (lane >= o) incl += v;
-        }
-        if (lane == 31) warp_tot[wid] = incl;
-        __syncthreads();
-        if (wid == 0) {
-            int v = warp_tot[lane];
-#pragma unroll
-            for (int o = 1; o < 32; o <<= 1) {
-                const int u = __shfl_up_sync(0xffffffffu, v, o);
-                if (lane >= o) v += u;
-            }
-            warp_tot[lane] = v;
-        }
-        __syncthreads();
-        int cum = carry + (wid > 0 ? warp_tot[wid - 1] : 0) + incl - n_seq;
-        carry += warp_tot[kPlanThreads / 32 - 1];
-        __syncthreads();   // warp_tot is rewritten by the next round
+        int cum = plan_block_scan(n_seq, carry, warp_tot, lane, wid);
+        int cum_w = plan_block_scan(w_seq, carry_w, warp_tot, lane, wid);
         for (int i = 0; i < nr; ++i) {
             const int vis = p.causal ? max(0, min(L, L - nr + i + 1)) : L;
             const int n = (vis + kBN - 1) / kBN;
             p.plan_rows[r0 + i] = make_int4(cum, n, b, vis);
+            p.plan_slots[r0 + i] = make_int2(cum_w, 0);   // W_r until pass 2
             cum += n;
+            cum_w += n > 0 ? n + kRunCost : 0;
         }
     }
     __syncthreads();
     // With fewer tiles than clusters only T clusters take part, so that every
     // cluster between a row's first and last holds a piece of it (no gaps in
-    // the row's run of slots).
-    const long long T = carry;
+    // the row's run of slots: a range inside a virtual block lies before the
+    // first of those).  Each field of plan_cluster is written by one thread:
+    // x0, row of cluster c by the row its range starts in, x1 of cluster c - 1
+    // (its successor's x0) by the same thread.
+    const long long T = carry, Tw = carry_w;
     const long long C = min(static_cast<long long>(p.num_clusters), T);
     for (int r = tid; r < rows; r += kPlanThreads) {
         const int4 e = __ldcg(p.plan_rows + r);
+        const long long W = __ldcg(p.plan_slots + r).x;
         int2 slot = make_int2(0, 0);
         if (e.y > 0) {
-            const long long first = e.x, last = static_cast<long long>(e.x) + e.y - 1;
-            const int cf = static_cast<int>(((first + 1) * C - 1) / T);
-            const int cl = static_cast<int>(((last + 1) * C - 1) / T);
+            const long long wf = W + kRunCost, wl = wf + e.y - 1;   // weighted first / last tile
+            const int cf = static_cast<int>(((wf + 1) * C - 1) / Tw);
+            const int cl = static_cast<int>(((wl + 1) * C - 1) / Tw);
             slot = make_int2(cf + r, cl - cf + 1);
-            for (long long c = (first * C + T - 1) / T; c < C && c * T / C <= last; ++c)
-                p.plan_cluster[c] = make_int4(static_cast<int>(c * T / C),
-                                              static_cast<int>((c + 1) * T / C), r, 0);
+            for (long long c = (W * C + Tw - 1) / Tw; c < C && c * Tw / C <= wl; ++c) {
+                const long long y = c * Tw / C;
+                const int x0 = e.x + static_cast<int>(min(max(y - wf, 0LL), static_cast<long long>(e.y)));
+                int *f = reinterpret_cast<int *>(p.plan_cluster + c);
+                f[0] = x0;
+                f[2] = r;
+                if (c > 0) reinterpret_cast<int *>(p.plan_cluster + (c - 1))[1] = x0;
+                if (c == C - 1) f[1] = static_cast<int>(T);
+            }
         }
         p.plan_slots[r] = slot;
     }

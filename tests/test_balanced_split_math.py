@@ -1,38 +1,60 @@
-"""Host-side check of the balanced MLA split's arithmetic, restated from the
-plan kernel and the decode kernel's run walk: row r has n_r tiles starting
-at cum_r in the concatenation (T tiles in all); with C' = min(C, T) clusters,
-cluster c takes [floor(c T / C'), floor((c+1) T / C')), tile x belongs to
-cluster ((x + 1) C' - 1) // T, cluster c writes the partial of a cut row r to
-slot c + r, and the reduce reads row r's partials from slots
+"""Host-side check of the balanced splits' arithmetic.  MLA (first part),
+restated from the plan kernel and the decode kernel's run walk.  Row r has n_r tiles starting
+at cum_r in the concatenation (T tiles in all).  Every row with tiles is
+preceded by RUN_COST virtual tiles in a weighted concatenation (T_w
+positions): row r occupies [W_r, W_r + RUN_COST + n_r), its real tile x sits
+at W_r + RUN_COST + (x - cum_r).  With C' = min(C, T) clusters, cluster c
+takes weighted positions [floor(c T_w / C'), floor((c+1) T_w / C')), i.e. the
+real tiles from the image of its first position (a position in a virtual
+block maps to the row's first tile) to the next cluster's; weighted position
+y belongs to cluster ((y + 1) C' - 1) // T_w, cluster c writes the partial of
+a cut row r to slot c + r, and the reduce reads row r's partials from slots
 c_first + r .. c_last + r.  Over random length mixes and cluster counts:
 every tile is covered exactly once, every row's pieces are exactly its slot
 range (so the reduce never reads an unwritten slot), a row with one piece is
-written directly, slots stay below C + rows, and ranges differ by at most
-one tile."""
+written directly, slots stay below C + rows, the weighted ranges differ by at
+most one position, and a cluster's cost (its tiles plus RUN_COST per run it
+opens) stays within RUN_COST of its weighted length.  GQA (second part):
+the same weighting over (sequence, KV head) units, each CTA finding its range
+from the lengths, the CTA holding a unit's first tile publishing the unit's
+slot range."""
 import random
 
+RUN_COST = 8
 
-def plan(tiles, clusters):
+
+def plan(tiles, clusters, run_cost=RUN_COST):
     rows = len(tiles)
-    cum, total = [], 0
+    cum, wcum, total, wtotal = [], [], 0, 0
     for n in tiles:
         cum.append(total)
+        wcum.append(wtotal)
         total += n
+        wtotal += n + run_cost if n > 0 else 0
     C = min(clusters, total)
-    ranges = [(0, 0, rows)] * clusters          # {x0, x1, first row}; no rows by default
+    ranges = [[0, 0, rows] for _ in range(clusters)]   # {x0, x1, first row}; no rows by default
     slots = [(0, 0)] * rows
     for r in range(rows):
-        if tiles[r] == 0:
+        n = tiles[r]
+        if n == 0:
             continue
-        first, last = cum[r], cum[r] + tiles[r] - 1
-        cf = ((first + 1) * C - 1) // total
-        cl = ((last + 1) * C - 1) // total
+        W = wcum[r]
+        wf, wl = W + run_cost, W + run_cost + n - 1      # weighted first / last real tile
+        cf = ((wf + 1) * C - 1) // wtotal
+        cl = ((wl + 1) * C - 1) // wtotal
         slots[r] = (cf + r, cl - cf + 1)
-        c = (first * C + total - 1) // total      # clusters whose range starts in row r
-        while c < C and c * total // C <= last:
-            ranges[c] = (c * total // C, (c + 1) * total // C, r)
+        c = (W * C + wtotal - 1) // wtotal               # clusters whose range starts in row r
+        while c < C and c * wtotal // C <= wl:
+            y = c * wtotal // C
+            x0 = cum[r] + min(max(y - wf, 0), n)
+            ranges[c][0] = x0
+            ranges[c][2] = r
+            if c > 0:
+                ranges[c - 1][1] = x0
+            if c == C - 1:
+                ranges[c][1] = total
             c += 1
-    return cum, total, C, ranges, slots
+    return cum, total, wtotal, C, [tuple(x) for x in ranges], slots
 
 
 def walk(cum, tiles, ranges, c):
@@ -53,18 +75,24 @@ def walk(cum, tiles, ranges, c):
 
 def test_balanced_split_covers_every_tile_once_and_slots_match():
     rng = random.Random(2024)
-    for _ in range(4000):
+    for it in range(4000):
         rows = rng.randint(1, 40)
         clusters = rng.randint(1, 80)
+        run_cost = RUN_COST if it % 4 else rng.choice([0, 1, 3, 8, 20])
         tiles = [rng.choice([0, 0, 1, 2, 3, rng.randint(0, 200)]) for _ in range(rows)]
-        cum, total, C, ranges, slots = plan(tiles, clusters)
+        cum, total, wtotal, C, ranges, slots = plan(tiles, clusters, run_cost)
         owner, pieces = {}, {}
         for c in range(clusters):
-            for row, tb, te, direct, slot in walk(cum, tiles, ranges, c):
+            runs = walk(cum, tiles, ranges, c)
+            for row, tb, te, direct, slot in runs:
                 for t in range(tb, te):
                     assert (row, t) not in owner
                     owner[(row, t)] = c
                 pieces.setdefault(row, []).append((slot, direct))
+            if total and c < C:
+                wlen = (c + 1) * wtotal // C - c * wtotal // C
+                cost = sum(te - tb for _, tb, te, _, _ in runs) + run_cost * len(runs)
+                assert wlen - run_cost <= cost <= wlen + run_cost
         assert len(owner) == total
         for r in range(rows):
             got = pieces.get(r, [])
@@ -75,5 +103,112 @@ def test_balanced_split_covers_every_tile_once_and_slots_match():
             assert all(d == (count == 1) for _, d in got)
             assert all(0 <= s < clusters + rows for s, _ in got)
         if total:
-            sizes = [ranges[c][1] - ranges[c][0] for c in range(C)]
-            assert min(sizes) >= 1 and max(sizes) - min(sizes) <= 1
+            wsizes = [(c + 1) * wtotal // C - c * wtotal // C for c in range(C)]
+            assert min(wsizes) >= 1 and max(wsizes) - min(wsizes) <= 1
+            assert all(ranges[c][0] <= ranges[c][1] for c in range(C))
+
+
+def test_run_cost_zero_is_the_equal_tile_split():
+    # with no cost per run the weighted split is the plain one: equal tile ranges
+    rng = random.Random(7)
+    for _ in range(500):
+        tiles = [rng.randint(0, 50) for _ in range(rng.randint(1, 30))]
+        clusters = rng.randint(1, 60)
+        cum, total, wtotal, C, ranges, _ = plan(tiles, clusters, 0)
+        assert wtotal == total
+        for c in range(C):
+            assert ranges[c][:2] == (c * total // C, (c + 1) * total // C)
+
+
+def test_more_runs_get_fewer_tiles():
+    # a cluster whose range meets many short rows holds fewer tiles than one
+    # inside a long row
+    tiles = [400] + [4] * 40
+    cum, total, wtotal, C, ranges, _ = plan(tiles, 4)
+    counts = [sum(te - tb for _, tb, te, _, _ in walk(cum, tiles, ranges, c)) for c in range(C)]
+    runs = [len(walk(cum, tiles, ranges, c)) for c in range(C)]
+    assert runs[0] == 1 and runs[-1] > 5
+    assert counts[0] > counts[-1] + 5 * RUN_COST
+
+
+# ---- the balanced GQA split (computed by every CTA from the lengths) --------
+
+GQA_UNIT_COST = 2
+
+
+def gqa_tile_of_position(cum, hkv, y, cost):
+    """Real tile of weighted position y: sequence b by the last b with
+    cum[b] + cost hkv b <= y, then the unit and the offset inside it (a
+    position in a unit's virtual block maps to its first tile)."""
+    batch = len(cum) - 1
+    b = max(i for i in range(batch) if cum[i] + cost * hkv * i <= y)
+    n = (cum[b + 1] - cum[b]) // hkv
+    off = y - (cum[b] + cost * hkv * b)
+    h = off // (n + cost)
+    o = off - h * (n + cost) - cost
+    return cum[b] + h * n + min(max(o, 0), n)
+
+
+def gqa_plan(n_seq, hkv, grid, cost=GQA_UNIT_COST):
+    cum = [0]
+    for n in n_seq:
+        cum.append(cum[-1] + n * hkv)
+    T = cum[-1]
+    Tw = T + cost * hkv * len(n_seq)
+    C = min(grid, T)
+    ranges = []
+    for c in range(grid):
+        if c >= C:
+            ranges.append((0, 0))
+            continue
+        x0 = gqa_tile_of_position(cum, hkv, c * Tw // C, cost)
+        x1 = T if c + 1 == C else gqa_tile_of_position(cum, hkv, (c + 1) * Tw // C, cost)
+        ranges.append((x0, x1))
+    return cum, T, Tw, C, ranges
+
+
+def test_gqa_balanced_split_covers_every_tile_once_and_slots_match():
+    rng = random.Random(99)
+    for it in range(3000):
+        batch = rng.randint(1, 24)
+        hkv = rng.choice([1, 2, 4, 8])
+        grid = rng.randint(1, 160)
+        cost = GQA_UNIT_COST if it % 3 else rng.choice([0, 1, 5])
+        n_seq = [max(1, rng.choice([1, 2, 3, rng.randint(1, 90)])) for _ in range(batch)]
+        cum, T, Tw, C, ranges = gqa_plan(n_seq, hkv, grid, cost)
+        units = [(b, h) for b in range(batch) for h in range(hkv)]
+        ux = [cum[b] + h * n_seq[b] for b, h in units]         # first tile of each unit
+        owner, pieces, published = {}, {}, {}
+        for c in range(grid):
+            x0, x1 = ranges[c]
+            assert x0 <= x1
+            for u, (b, h) in enumerate(units):
+                tb, te = max(x0 - ux[u], 0), min(x1 - ux[u], n_seq[b])
+                if tb >= te:
+                    continue
+                for t in range(tb, te):
+                    assert (u, t) not in owner
+                    owner[(u, t)] = c
+                pieces.setdefault(u, []).append(c + u)           # the piece's slot
+                if tb == 0:
+                    # the CTA holding the first tile publishes the slot range
+                    last = ux[u] + n_seq[b] - 1 + cost * (u + 1)
+                    c_last = ((last + 1) * C - 1) // Tw
+                    published[u] = (c + u, c_last - c + 1)
+        assert len(owner) == T
+        for u in range(len(units)):
+            first, count = published[u]
+            assert sorted(pieces[u]) == list(range(first, first + count))
+        if T:
+            wsizes = [(c + 1) * Tw // C - c * Tw // C for c in range(C)]
+            assert max(wsizes) - min(wsizes) <= 1
+
+
+def test_gqa_unit_cost_zero_is_the_equal_tile_split():
+    rng = random.Random(5)
+    for _ in range(300):
+        n_seq = [rng.randint(1, 40) for _ in range(rng.randint(1, 16))]
+        hkv, grid = rng.choice([1, 8]), rng.randint(1, 152)
+        cum, T, Tw, C, ranges = gqa_plan(n_seq, hkv, grid, 0)
+        for c in range(C):
+            assert ranges[c] == (c * T // C, (c + 1) * T // C)
