@@ -145,6 +145,13 @@ __device__ __forceinline__ uint32_t x_half_off(int k, int h, int c) {
     return uint32_t(k) * kXHalfBytes + uint32_t(h * 128 + (((c + h) & 7) << 4));
 }
 
+// Row r (0..31), 16-byte chunk k of a warp's 4 KB slice of x_out, with the
+// same rotation: both a lane per row and eight lanes per row are free of
+// bank conflicts.
+__device__ __forceinline__ uint32_t xw_off(int r, int k) {
+    return uint32_t(r * 128 + (((k + r) & 7) << 4));
+}
+
 // One run of consecutive key tiles of one query row: keys [start, end) of
 // row qrow (sequence b).  direct: the run is the whole row, so the final
 // output is written; otherwise the partial goes to workspace slot ws.
@@ -576,6 +583,10 @@ mla_decode_kernel(const __grid_constant__ MlaParams p) {
         const uint32_t lane_base = uint32_t((warp & 3) * 32) << 16;
         uint8_t *x_in = smem + Smem::x_in;
         uint8_t *x_out = smem + Smem::x_out;
+        // This warp's 4 KB of x_out: rows h of its key half, the rows it
+        // stages for the exchange; also its transpose buffer for the Q load
+        // and the epilogue stores (row r, 16-byte chunk k at xw_off(r, k)).
+        uint8_t *xw = x_out + x_half_off(half, (warp & 3) * 32, 0);
         float *red = reinterpret_cast<float *>(smem + Smem::red);
         const uint32_t peer_xfree = mapa_shared(smem_addr(&bar[kXPeerFree]), peer);
         const uint32_t s_col = kTmemS + 32u * half;
@@ -603,32 +614,70 @@ mla_decode_kernel(const __grid_constant__ MlaParams p) {
                 // This CTA's Q channels of head row h into TMEM lane h: 64
                 // channels (32 columns of bf16 pairs) per store, boxes split
                 // over the halves, then the 32 rope channels (16 columns).
-                // The last run's MMAs have all finished.
-                const uint16_t *qr = p.q + (size_t(sg.qrow) * kMlaHeads + h) * kMlaDimQK;
-                const uint4 *src = reinterpret_cast<const uint4 *>(qr + col0);
+                // The last run's MMAs have all finished.  The warp reads its
+                // 32 rows a 128-byte line per 8 lanes into its slice of x_out
+                // (free: the last copy has read it, waited for in the last
+                // run's epilogue) and each lane takes its row back out.
+                const uint8_t *qw = reinterpret_cast<const uint8_t *>(
+                    p.q + (size_t(sg.qrow) * kMlaHeads + (warp & 3) * 32) * kMlaDimQK);
+                // Every line the warp needs requested up front (lane = row:
+                // its two boxes and, for half 1, the rope channels), so the
+                // boxes' loads below overlap their latencies.
+                {
+                    const uint8_t *mine = qw + size_t(lane) * kMlaDimQK * 2;
+                    asm volatile("prefetch.global.L1 [%0];" ::"l"(mine + col0 * 2 + half * 128));
+                    asm volatile("prefetch.global.L1 [%0];" ::"l"(mine + col0 * 2 + (half + 2) * 128));
+                    if (half == 1) asm volatile("prefetch.global.L1 [%0];" ::"l"(mine + rope_col * 2));
+                }
                 for (int cb = half; cb < kVBoxes; cb += 2) {
-                    float v[32];
+                    uint4 ld[8];
 #pragma unroll
                     for (int i = 0; i < 8; ++i) {
-                        const uint4 wq = src[cb * 8 + i];
-                        v[4 * i] = __uint_as_float(wq.x);
-                        v[4 * i + 1] = __uint_as_float(wq.y);
-                        v[4 * i + 2] = __uint_as_float(wq.z);
-                        v[4 * i + 3] = __uint_as_float(wq.w);
+                        const int r = 4 * i + (lane >> 3);
+                        ld[i] = *reinterpret_cast<const uint4 *>(
+                            qw + size_t(r) * kMlaDimQK * 2 + (col0 + cb * 64) * 2 + (lane & 7) * 16);
                     }
+#pragma unroll
+                    for (int i = 0; i < 8; ++i)
+                        *reinterpret_cast<uint4 *>(xw + xw_off(4 * i + (lane >> 3), lane & 7)) = ld[i];
+                    __syncwarp();
+                    float v[32];
+#pragma unroll
+                    for (int k = 0; k < 8; ++k) {
+                        const uint4 wq = *reinterpret_cast<const uint4 *>(xw + xw_off(lane, k));
+                        v[4 * k] = __uint_as_float(wq.x);
+                        v[4 * k + 1] = __uint_as_float(wq.y);
+                        v[4 * k + 2] = __uint_as_float(wq.z);
+                        v[4 * k + 3] = __uint_as_float(wq.w);
+                    }
+                    __syncwarp();
                     tc::tmem_st32(tmem + lane_base + kTmemQ + cb * 32, v);
                 }
                 if (half == 1) {
-                    const uint4 *rp = reinterpret_cast<const uint4 *>(qr + rope_col);
+                    uint4 lr[4];
+#pragma unroll
+                    for (int i = 0; i < 4; ++i) {
+                        const int r = 8 * i + (lane >> 2);
+                        lr[i] = *reinterpret_cast<const uint4 *>(
+                            qw + size_t(r) * kMlaDimQK * 2 + rope_col * 2 + (lane & 3) * 16);
+                    }
+#pragma unroll
+                    for (int i = 0; i < 4; ++i) {
+                        const int r = 8 * i + (lane >> 2);
+                        *reinterpret_cast<uint4 *>(xw + xw_off(r, lane & 3)) = lr[i];
+                    }
+                    __syncwarp();
 #pragma unroll
                     for (int k = 0; k < 2; ++k) {
-                        const uint4 a = rp[2 * k], b = rp[2 * k + 1];
+                        const uint4 a = *reinterpret_cast<const uint4 *>(xw + xw_off(lane, 2 * k));
+                        const uint4 b = *reinterpret_cast<const uint4 *>(xw + xw_off(lane, 2 * k + 1));
                         const float v[8] = {__uint_as_float(a.x), __uint_as_float(a.y),
                                             __uint_as_float(a.z), __uint_as_float(a.w),
                                             __uint_as_float(b.x), __uint_as_float(b.y),
                                             __uint_as_float(b.z), __uint_as_float(b.w)};
                         tc::tmem_st_n<8>(tmem + lane_base + kTmemQ + 4 * kVBoxes * 8 + 8 * k, v);
                     }
+                    __syncwarp();
                 }
                 tc::tmem_wait_st();
                 tc::fence_before_sync();
@@ -875,6 +924,16 @@ mla_decode_kernel(const __grid_constant__ MlaParams p) {
             const size_t row = size_t(sg.qrow) * kMlaHeads + h;
             const size_t wrow = size_t(sg.ws) * kMlaHeads + h;
             const int ch0 = rank * 256 + half * 128;   // this warp's output channels
+            // The rows go out through the warp's slice of x_out, eight lanes
+            // a row (whole 128-byte lines), once the copy of the CTA's last
+            // staged partial has read it.
+            const int g_last = G + ntiles - 1;
+            if (ok && g_last >= 0 &&
+                !__all_sync(0xffffffffu, mbar_wait(&bar[kXoFree + half], g_last & 1, p.err))) {
+                ok = false;   // sticks: the end of the run keeps a failed wait
+                live = false;
+            }
+            const size_t row0 = size_t(sg.direct ? sg.qrow : sg.ws) * kMlaHeads + (warp & 3) * 32;
 #pragma unroll 1
             for (int c = 0; c < 128; c += 32) {
                 float v[32];
@@ -884,25 +943,24 @@ mla_decode_kernel(const __grid_constant__ MlaParams p) {
 #pragma unroll
                     for (int j = 0; j < 32; ++j) v[j] = 0.f;
                 }
-                if (sg.direct) {
-                    uint16_t *dst = p.out + row * kMlaDimV + ch0 + c;
 #pragma unroll
-                    for (int j = 0; j < 32; j += 8) {
-                        uint4 wv;
-                        wv.x = pack_bf16x2(v[j] * scale_o, v[j + 1] * scale_o);
-                        wv.y = pack_bf16x2(v[j + 2] * scale_o, v[j + 3] * scale_o);
-                        wv.z = pack_bf16x2(v[j + 4] * scale_o, v[j + 5] * scale_o);
-                        wv.w = pack_bf16x2(v[j + 6] * scale_o, v[j + 7] * scale_o);
-                        *reinterpret_cast<uint4 *>(dst + j) = wv;
-                    }
-                } else {
-                    float *dst = p.ws_o + wrow * kMlaDimV + ch0 + c;
+                for (int k = 0; k < 8; ++k)
+                    *reinterpret_cast<float4 *>(xw + xw_off(lane, k)) =
+                        make_float4(v[4 * k] * scale_o, v[4 * k + 1] * scale_o,
+                                    v[4 * k + 2] * scale_o, v[4 * k + 3] * scale_o);
+                __syncwarp();
 #pragma unroll
-                    for (int j = 0; j < 32; j += 4)
-                        *reinterpret_cast<float4 *>(dst + j) =
-                            make_float4(v[j] * scale_o, v[j + 1] * scale_o, v[j + 2] * scale_o,
-                                        v[j + 3] * scale_o);
+                for (int i = 0; i < 8; ++i) {
+                    const int r = 4 * i + (lane >> 3), k = lane & 7;
+                    const float4 f = *reinterpret_cast<const float4 *>(xw + xw_off(r, k));
+                    const size_t at = (row0 + r) * kMlaDimV + ch0 + c + 4 * k;
+                    if (sg.direct)
+                        *reinterpret_cast<uint2 *>(p.out + at) =
+                            make_uint2(pack_bf16x2(f.x, f.y), pack_bf16x2(f.z, f.w));
+                    else
+                        *reinterpret_cast<float4 *>(p.ws_o + at) = f;
                 }
+                __syncwarp();
             }
             if (rank == 0 && half == 0) {
                 if (sg.direct) {

@@ -419,7 +419,10 @@ tile_attention_kernel(const __grid_constant__ TileParams p) {
         }
         const float scale_o = Zr > 0.f ? so / Zr : 0.f;
         const size_t row = size_t(q_off) + tok;
-        uint16_t *dst = p.out + (row * p.num_q_heads + h) * kD + 64 * half;
+        // The warp's 32 rows x 64 channels (bf16) go out through 4 KB of the K
+        // ring, which no MMA reads any more: a lane writes its row, then eight
+        // lanes a row store whole 128-byte lines.
+        uint8_t *tw = smem + Smem::k + warp * 4096;
 #pragma unroll 1
         for (int c = 0; c < 64; c += 32) {
             float v[32];
@@ -429,16 +432,27 @@ tile_attention_kernel(const __grid_constant__ TileParams p) {
 #pragma unroll
                 for (int j = 0; j < 32; ++j) v[j] = 0.f;
             }
-            if (row_valid) {
 #pragma unroll
-                for (int j = 0; j < 32; j += 8) {
-                    uint4 w;
-                    w.x = pack_bf16x2(v[j] * scale_o, v[j + 1] * scale_o);
-                    w.y = pack_bf16x2(v[j + 2] * scale_o, v[j + 3] * scale_o);
-                    w.z = pack_bf16x2(v[j + 4] * scale_o, v[j + 5] * scale_o);
-                    w.w = pack_bf16x2(v[j + 6] * scale_o, v[j + 7] * scale_o);
-                    *reinterpret_cast<uint4 *>(dst + c + j) = w;
-                }
+            for (int j = 0; j < 32; j += 8) {
+                uint4 w;
+                w.x = pack_bf16x2(v[j] * scale_o, v[j + 1] * scale_o);
+                w.y = pack_bf16x2(v[j + 2] * scale_o, v[j + 3] * scale_o);
+                w.z = pack_bf16x2(v[j + 4] * scale_o, v[j + 5] * scale_o);
+                w.w = pack_bf16x2(v[j + 6] * scale_o, v[j + 7] * scale_o);
+                const int k = (c + j) >> 3;          // 16-byte chunk of the row
+                *reinterpret_cast<uint4 *>(tw + lane * 128 + (((k + lane) & 7) << 4)) = w;
+            }
+        }
+        __syncwarp();
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+            const int rr = 4 * i + (lane >> 3), k = lane & 7;
+            const int r2 = (warp & 3) * 32 + rr;     // MMA row of that line
+            const int tok2 = t0 + r2 / G;
+            if (tok2 < n) {
+                const uint4 w = *reinterpret_cast<const uint4 *>(tw + rr * 128 + (((k + rr) & 7) << 4));
+                const size_t orow = (size_t(q_off) + tok2) * p.num_q_heads + kvh * G + (r2 % G);
+                *reinterpret_cast<uint4 *>(p.out + orow * kD + 64 * half + 8 * k) = w;
             }
         }
         if (row_valid && p.lse && half == 0)
