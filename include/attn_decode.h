@@ -144,7 +144,8 @@ typedef struct attn_kv {
  * split-K route and at most 8 num_sms (sequence, KV head) units (max_kv_len
  * above one 128-key tile) takes the balanced split: the 128-key
  * tiles of every unit (an empty unit counts one), concatenated, are dealt
- * out in equal contiguous ranges to num_sms CTAs; a unit a range end cuts
+ * out in contiguous ranges of equal cost (tiles plus 2 tiles' worth for
+ * every unit a range opens) to num_sms CTAs; a unit a range end cuts
  * leaves one partial per piece, merged by the reduce.  Its workspace_bytes
  * = (num_sms + units) slots of 16 x 128 fp32 plus 16 m and 16 l each (each
  * array 256-byte aligned) plus 8 bytes per unit (256-byte aligned).  GQA with head_dim 128 and
@@ -156,11 +157,12 @@ typedef struct attn_kv {
  * n = ceil(num_q_rows / batch) query rows per sequence, capped at
  * ceil(max_kv_len / 64), the plan is P = 1 (no split) when P' <= 1 and
  * otherwise P = 0, the balanced split: the 64-key tiles of every query row,
- * concatenated, are dealt out in equal contiguous ranges to
- * min(num_sms / 2, tiles) two-CTA clusters (one wave), with workspace_bytes
- * = (num_sms / 2 + num_q_rows) slots of fp32 partials (128 x 512 O, m, l,
- * each array 256-byte aligned) plus 16 (num_sms / 2) + 24 num_q_rows bytes
- * of plan tables (each 256-byte aligned); it does not depend on max_kv_len.
+ * concatenated, are dealt out in contiguous ranges of equal cost (tiles
+ * plus 8 tiles' worth for every row a range opens) to min(num_sms / 2,
+ * tiles) two-CTA clusters (one wave), with workspace_bytes = (num_sms / 2 +
+ * num_q_rows) slots of fp32 partials (128 x 512 O, m, l, each array
+ * 256-byte aligned) plus 8 num_q_rows bytes (256-byte aligned) for the
+ * table of where each row's partials are; it does not depend on max_kv_len.
  * For attn_mla_decode_sparse pass max_kv_len = indices_stride.
  * Returns ATTN_OK, ATTN_ERR_INVALID_ARG, or ATTN_ERR_CUDA if the SM count
  * query fails.  Launches nothing.
@@ -263,13 +265,13 @@ int attn_decode(const void *q, const attn_kv_t *k, const attn_kv_t *v, const uin
  *
  * P >= 1: one two-CTA cluster per (key slice, row); slice p of a row is
  * [p C, (p+1) C) as attn_plan_partitions states, then the split-K reduce.
- * P == 0: a plan kernel (one CTA) writes the tile ranges of the clusters
- * into the workspace, the decode grid (one wave of clusters, a dependent
- * launch of the plan) walks them, a cluster writing the final rows of the
+ * P == 0: the decode grid (one wave of clusters) finds each cluster's tile
+ * range from kv_len and walks it, a cluster writing the final rows of the
  * rows its range holds whole and fp32 partials of the rows a range end
- * cuts, and the reduce merges the latter (three launches).  kv_len above
- * max_kv_len is then clamped to it and sets error bit 2, as a length above
- * P C does for P >= 1.
+ * cuts, and the entry of the workspace table saying where the partials of
+ * each row whose first tile it holds are; the reduce merges them (two
+ * launches).  kv_len above max_kv_len is then clamped to it and sets error
+ * bit 2, as a length above P C does for P >= 1.
  */
 int attn_mla_decode(const void *q, const attn_kv_t *kv, const uint32_t *kv_len, int batch,
                     int num_q_heads, int dim_qk, int dim_v, int max_kv_len, float scale,

@@ -101,7 +101,7 @@ size_t workspace_layout(int P, long long rows, int hq, int dv, size_t *off_m, si
 }
 
 // Balanced MLA split: fp32 partials for clusters + rows slots, then the
-// plan tables (per cluster, per row, per row for the reduce).
+// reduce's table (per row: its first slot and partials).
 size_t mla_balanced_layout(int clusters, long long rows, size_t *off_m, size_t *off_l,
                            size_t *off_plan) {
     const size_t n = (size_t(clusters) + size_t(rows)) * size_t(kMlaHeads);
@@ -110,8 +110,7 @@ size_t mla_balanced_layout(int clusters, long long rows, size_t *off_m, size_t *
     if (off_m) *off_m = o_bytes;
     if (off_l) *off_l = o_bytes + m_bytes;
     if (off_plan) *off_plan = o_bytes + 2 * m_bytes;
-    return o_bytes + 2 * m_bytes + align256(size_t(clusters) * 16) + align256(size_t(rows) * 16) +
-           align256(size_t(rows) * 8);
+    return o_bytes + 2 * m_bytes + align256(size_t(rows) * 8);
 }
 
 // Balanced GQA split: partial slots (CTAs + units) of 16 columns x 128
@@ -719,12 +718,7 @@ int mla_decode_impl(const void *q, const attn_kv_t *kv, const uint32_t *kv_len,
         p.ws_l = reinterpret_cast<float *>(ws + off_l);
     }
     if (balanced) {
-        uint8_t *plan = static_cast<uint8_t *>(workspace) + off_plan;
-        p.plan_cluster = reinterpret_cast<int4 *>(plan);
-        plan += align256(size_t(clusters) * 16);
-        p.plan_rows = reinterpret_cast<int4 *>(plan);
-        plan += align256(size_t(num_q_rows) * 16);
-        p.plan_slots = reinterpret_cast<int2 *>(plan);
+        p.plan_slots = reinterpret_cast<int2 *>(static_cast<uint8_t *>(workspace) + off_plan);
         p.balanced = 1;
         p.num_clusters = clusters;
         p.len_cap = max_kv_len;
@@ -740,10 +734,6 @@ int mla_decode_impl(const void *q, const attn_kv_t *kv, const uint32_t *kv_len,
     p.qk_scale_log2 = scale * 1.4426950408889634f;
 
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-    if (balanced) {
-        st = map_cuda(launch_mla_plan(p, s));
-        if (st) return st;
-    }
     st = map_cuda(launch_mla_decode(p, s));
     if (st || num_partitions == 1) return st;
 
@@ -766,6 +756,7 @@ int mla_decode_impl(const void *q, const attn_kv_t *kv, const uint32_t *kv_len,
     r.len_cap = sparse ? indices_stride : 0;
     if (balanced) {
         r.slots = p.plan_slots;
+        r.num_slots = clusters + num_q_rows;
         r.kv_len = nullptr;
         r.q_row_offsets = nullptr;
         r.num_partitions = clusters;   // the most partials a row can have

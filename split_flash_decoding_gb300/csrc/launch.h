@@ -90,13 +90,13 @@ struct MlaParams {
     int num_partitions, chunk;    // chunk: multiple of kMlaTileKeys
     float qk_scale_log2;
     // Balanced split (num_partitions 0): cluster c takes tiles [x0, x1) of the
-    // concatenation of every query row's key tiles; the plan kernel writes
-    // the tables below into the workspace.  Partials go to slot c + row.
+    // concatenation of every query row's key tiles, found by the cluster from
+    // the lengths.  Partials go to slot c + row; the cluster holding a row's
+    // first tile writes its entry of the table below (cluster 0 those of the
+    // rows without tiles) for the reduce.
     int balanced;
     int num_clusters;
     int len_cap;                  // kv_len above it is clamped (error bit 2)
-    int4 *plan_cluster;           // [num_clusters] {x0, x1, first row, 0}
-    int4 *plan_rows;              // [num_q_rows] {first tile, tiles, sequence, visible keys}
     int2 *plan_slots;             // [num_q_rows] {first slot, partials} for the reduce
 };
 
@@ -138,8 +138,10 @@ struct ReduceParams {
     int len_cap;                  // > 0: kv_len is clamped to it as well as to P * chunk
     // Balanced MLA split: row r's partials are slots e.x .. e.x + e.y - 1 of
     // the workspace (e = slots[r]); e.y == 1 rows were finished by the
-    // decode kernel, e.y == 0 rows are empty.
+    // decode kernel, e.y == 0 rows are empty.  An entry outside the
+    // num_slots slots (a row no sequence owns) is read as an empty row.
     const int2 *slots;
+    int num_slots;
     // Balanced GQA split: (row r, head h) of sequence b belongs to unit u =
     // b * hkv + h / group, whose partials are slots e.x .. e.x + e.y - 1
     // (e = unit_slots[u]) of [slots][kGqaSlotCols][dim_v], at column
@@ -152,7 +154,6 @@ struct ReduceParams {
 cudaError_t launch_gqa_decode(const GqaParams &p, cudaStream_t stream);
 cudaError_t launch_gqa_decode_tc(const GqaParams &p, cudaStream_t stream);
 cudaError_t launch_mla_decode(const MlaParams &p, cudaStream_t stream);
-cudaError_t launch_mla_plan(const MlaParams &p, cudaStream_t stream);
 // Two-CTA MLA clusters that run at once on num_sms SMs (at most num_sms / 2).
 int mla_cluster_slots(int num_sms, bool sparse);
 cudaError_t launch_tile_attention(const TileParams &p, cudaStream_t stream);

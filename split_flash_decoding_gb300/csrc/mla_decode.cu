@@ -116,7 +116,8 @@ struct Smem {
     static constexpr int x_out = x_in + kXSlots * int(kXHalfBytes);   // +48 KB (peer's partials)
     static constexpr int red = x_out + int(kXBytes);                  // +32 KB (own partial)
     static constexpr int bars = red + 2 * 128 * 4;                    // +1 KB (row maxima)
-    static constexpr int total = bars + 192;
+    static constexpr int range = bars + 192;                          // balanced: MlaRange
+    static constexpr int total = range + 64;
 };
 constexpr size_t kSmemBytes = Smem::total + 1024;
 
@@ -202,42 +203,228 @@ __device__ __forceinline__ bool fixed_slice(const MlaParams &p, MlaSeg &s, bool 
     return true;
 }
 
+// Balanced split (plan kernel and decode grid alike): a cluster's time is
+// its tiles plus a fixed cost for every run it opens (the row's Q into TMEM
+// and the pipeline refill, then the epilogue: about kRunCost tiles' worth),
+// so the split deals out a weighted concatenation in which every row with
+// tiles is preceded by kRunCost virtual tiles: row r (n_r tiles from tile
+// cum_r) occupies weighted positions [W_r, W_r + kRunCost + n_r), its real
+// tile x at y(x) = x - cum_r + W_r + kRunCost.  Cluster c of C = min(clusters,
+// T) takes the weighted positions [c T_w / C, (c+1) T_w / C) of the T_w in
+// all, i.e. the real tiles from the image of its first position (a position
+// inside a virtual block maps to the row's first tile) up to the next
+// cluster's; a range inside one virtual block is empty.  A cluster whose
+// range meets more rows so gets fewer tiles.
+constexpr int kRunCost = 8;
+
+// The rows of sequence b: first row r0, count nr (clipped to [0, rows)), and
+// its visible length L (at most cap).
+struct MlaSeqRows {
+    int r0, nr, L;
+};
+__device__ __forceinline__ MlaSeqRows mla_seq_rows(const MlaParams &p, int b, uint32_t cap) {
+    MlaSeqRows q;
+    q.L = static_cast<int>(min(p.kv_len[b], cap));
+    q.r0 = p.q_row_offsets ? static_cast<int>(p.q_row_offsets[b]) : b;
+    q.nr = p.q_row_offsets ? static_cast<int>(p.q_row_offsets[b + 1]) - q.r0 : 1;
+    q.nr = max(0, min(q.nr, p.num_q_rows - q.r0));   // rows outside [0, rows) are skipped
+    if (q.r0 < 0) q.nr = 0;
+    return q;
+}
+// Row i of n of a sequence of length L sees keys j <= L - n + i when causal.
+__device__ __forceinline__ int mla_row_vis(const MlaParams &p, int L, int nr, int i) {
+    return p.causal ? max(0, min(L, L - nr + i + 1)) : L;
+}
+
 // The runs a cluster processes, in order.  Fixed split: the one key slice of
 // the cluster's grid position.  Balanced split: the rows that meet the
-// cluster's tile range [x0, x1) of the concatenated row tiles, read from the
-// plan one row ahead.  Every role walks the same list on its own.
+// cluster's tile range [x0, x1) of the concatenated row tiles, computed from
+// the lengths as the walk goes (row i of sequence b, whose first tile is
+// cum).  Every role walks the same list on its own.
 template <bool kSparse>
 struct SegWalk {
-    int r, x0, x1;   // fixed split: r = 1 while the slice is still to come
-    int4 nxt;        // plan entry of row r: {first tile, tiles, sequence, visible keys}
+    int x0, x1;   // balanced: the cluster's tiles
+    int b, i;     // balanced: the next row is row i of sequence b; fixed split: b = 0
+                  // while the slice is still to come
+    int cum;      // balanced: the next row's first tile
 
     __device__ __forceinline__ bool next(const MlaParams &p, MlaSeg &s) {
         if (!p.balanced) {
-            if (r == 0) return false;
-            r = 0;
+            if (b != 0) return false;
+            b = 1;
             return fixed_slice<kSparse>(p, s, false);
         }
-        while (r < p.num_q_rows) {
-            const int4 e = nxt;
-            const int row = r++;
-            if (e.x >= x1) break;
-            if (r < p.num_q_rows) nxt = __ldcg(p.plan_rows + r);
-            const int tb = max(x0 - e.x, 0);
-            const int te = min(x1 - e.x, e.y);
+        const uint32_t cap = uint32_t(p.len_cap);
+        while (b < p.batch) {
+            int vis, row, seq;
+            if constexpr (kSparse) {
+                // one query row per sequence, every listed key visible
+                seq = row = b++;
+                vis = static_cast<int>(min(p.kv_len[seq], cap));
+            } else {
+                const MlaSeqRows sq = mla_seq_rows(p, b, cap);
+                if (i >= sq.nr) {
+                    ++b;
+                    i = 0;
+                    continue;
+                }
+                seq = b;
+                vis = mla_row_vis(p, sq.L, sq.nr, i);
+                row = sq.r0 + i;
+                ++i;
+            }
+            const int n = (vis + kBN - 1) / kBN;
+            const int first = cum;
+            cum += n;
+            if (first >= x1) {
+                b = p.batch;   // past the range: the walk is over
+                break;
+            }
+            const int tb = max(x0 - first, 0);
+            const int te = min(x1 - first, n);
             if (tb >= te) continue;   // an empty row
             s.qrow = row;
-            s.b = e.z;
+            s.b = seq;
             s.start = tb * kBN;
-            s.end = min(te * kBN, e.w);
+            s.end = min(te * kBN, vis);
             s.ntiles = te - tb;
-            s.direct = tb == 0 && te == e.y;
+            s.direct = tb == 0 && te == n;
             s.ws = static_cast<int>(blockIdx.x >> 1) + row;
             return true;
         }
-        r = p.num_q_rows;
         return false;
     }
+    // Row of the run after the one next() returned last, if there may be one
+    // in the same sequence (balanced split).
+    __device__ __forceinline__ int peek_row(const MlaParams &p) const {
+        if (b >= p.batch || cum >= x1) return -1;
+        if constexpr (kSparse) return b;
+        const MlaSeqRows sq = mla_seq_rows(p, b, uint32_t(p.len_cap));
+        return i < sq.nr ? sq.r0 + i : -1;
+    }
 };
+
+// Balanced split: this cluster's range and the walk's first row, from the
+// lengths, by one warp (all 32 lanes call; every lane gets the result).
+// Lane l sums the tiles and weighted tiles of sequences [l m, (l+1) m); a
+// warp scan gives every lane its first position; the lane whose weighted
+// positions hold the cluster's first (the next cluster's first) position
+// finds the row and the real tile.  With mark_empty, the reduce's entry of
+// every row without tiles is written ({0, 0}: an empty row).
+struct MlaRange {
+    int x0, x1;      // the cluster's real tiles
+    int b, i, cum;   // its first row (row i of sequence b) and that row's first tile
+    int w;           // that row's first weighted position
+    int tw, c;       // weighted positions in all, clusters taking part
+};
+__device__ __forceinline__ int4 mla_locate(const MlaParams &p, uint32_t cap, int b_lo, int b_hi,
+                                           long long cum, long long W, long long y) {
+    // {first tile, sequence b, row i in it, first weighted position} of the
+    // row holding weighted position y, searched in sequences [b_lo, b_hi)
+    // whose first row starts at tile cum and weighted position W.
+    for (int b = b_lo; b < b_hi; ++b) {
+        const MlaSeqRows q = mla_seq_rows(p, b, cap);
+        for (int i = 0; i < q.nr; ++i) {
+            const int n = (mla_row_vis(p, q.L, q.nr, i) + kBN - 1) / kBN;
+            if (n > 0 && y < W + kRunCost + n)
+                return make_int4(static_cast<int>(cum), b, i,
+                                 static_cast<int>(W));
+            cum += n;
+            W += n > 0 ? n + kRunCost : 0;
+        }
+    }
+    return make_int4(0, b_hi, 0, 0);
+}
+__device__ __forceinline__ MlaRange mla_balanced_range(const MlaParams &p, int lane, bool mark_empty) {
+    const uint32_t cap = uint32_t(p.len_cap);
+    const int per_lane = (p.batch + 31) / 32;
+    const int b_lo = min(lane * per_lane, p.batch), b_hi = min(b_lo + per_lane, p.batch);
+    long long tl = 0, wl = 0;
+    for (int b = b_lo; b < b_hi; ++b) {
+        if (mark_empty && p.kv_len[b] > cap) atomicOr(p.err, kErrBadLength);
+        const MlaSeqRows q = mla_seq_rows(p, b, cap);
+        for (int i = 0; i < q.nr; ++i) {
+            const int n = (mla_row_vis(p, q.L, q.nr, i) + kBN - 1) / kBN;
+            tl += n;
+            wl += n > 0 ? n + kRunCost : 0;
+            if (mark_empty && n == 0) p.plan_slots[q.r0 + i] = make_int2(0, 0);
+        }
+    }
+    long long ti = tl, wi = wl;   // inclusive scans
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const long long u = __shfl_up_sync(0xffffffffu, ti, o);
+        const long long v = __shfl_up_sync(0xffffffffu, wi, o);
+        if (lane >= o) {
+            ti += u;
+            wi += v;
+        }
+    }
+    const long long T = __shfl_sync(0xffffffffu, ti, 31), Tw = __shfl_sync(0xffffffffu, wi, 31);
+    const long long C = min(static_cast<long long>(p.num_clusters), T);
+    const long long c = blockIdx.x >> 1;
+    MlaRange r;
+    r.x0 = r.x1 = r.cum = r.i = r.w = 0;
+    r.b = p.batch;   // no rows
+    r.tw = static_cast<int>(Tw);
+    r.c = static_cast<int>(C);
+    if (c < C) {
+        for (int k = 0; k < 2; ++k) {
+            if (k == 1 && c + 1 == C) {
+                r.x1 = static_cast<int>(T);
+                break;
+            }
+            const long long y = (c + k) * Tw / C;
+            const bool mine = wi - wl <= y && y < wi;
+            const int src = __ffs(__ballot_sync(0xffffffffu, mine)) - 1;
+            int4 e = make_int4(0, 0, 0, 0);
+            int x = 0;
+            if (lane == src) {
+                e = mla_locate(p, cap, b_lo, b_hi, ti - tl, wi - wl, y);
+                const MlaSeqRows q = mla_seq_rows(p, e.y, cap);
+                const int n = (mla_row_vis(p, q.L, q.nr, e.z) + kBN - 1) / kBN;
+                x = e.x + static_cast<int>(min(max(y - e.w - kRunCost, 0LL),
+                                               static_cast<long long>(n)));
+            }
+            x = __shfl_sync(0xffffffffu, x, src);
+            if (k == 0) {
+                r.x0 = x;
+                r.cum = __shfl_sync(0xffffffffu, e.x, src);
+                r.b = __shfl_sync(0xffffffffu, e.y, src);
+                r.i = __shfl_sync(0xffffffffu, e.z, src);
+                r.w = __shfl_sync(0xffffffffu, e.w, src);
+            } else {
+                r.x1 = x;
+            }
+        }
+    }
+    return r;
+}
+
+// Balanced split, the reduce's table: for every row whose first tile this
+// cluster holds, {first slot, partials}.  Cluster c writes row r's partial
+// to slot c + r, and the cluster holding weighted position y is
+// ((y + 1) C - 1) / T_w, so a row's partials are consecutive slots.
+__device__ __forceinline__ void mla_write_slots(const MlaParams &p, const MlaRange &g) {
+    const uint32_t cap = uint32_t(p.len_cap);
+    const int c = static_cast<int>(blockIdx.x >> 1);
+    long long cum = g.cum, W = g.w;
+    int i = g.i;
+    for (int b = g.b; b < p.batch; ++b, i = 0) {
+        const MlaSeqRows q = mla_seq_rows(p, b, cap);
+        for (; i < q.nr; ++i) {
+            if (cum >= g.x1) return;
+            const int n = (mla_row_vis(p, q.L, q.nr, i) + kBN - 1) / kBN;
+            if (n > 0 && cum >= g.x0) {
+                const long long wl = W + kRunCost + n - 1;   // weighted last tile
+                const int cl = static_cast<int>(((wl + 1) * g.c - 1) / g.tw);
+                p.plan_slots[q.r0 + i] = make_int2(c + q.r0 + i, cl - c + 1);
+            }
+            cum += n;
+            W += n > 0 ? n + kRunCost : 0;
+        }
+    }
+}
 
 template <bool kSparse>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(Layout<kSparse>::kThreads, 1)
@@ -257,9 +444,7 @@ mla_decode_kernel(const __grid_constant__ MlaParams p) {
     const int rope_col = kMlaDimV + int(rank) * kMlaRopeBoxCh;  // and rope channels
 
     SegWalk<kSparse> walk;
-    walk.r = 1;
-    walk.x0 = walk.x1 = 0;
-    walk.nxt = make_int4(0, 0, 0, 0);
+    walk.x0 = walk.x1 = walk.cum = walk.i = walk.b = 0;
     if (!p.balanced) {
         MlaSeg s0;
         if (!fixed_slice<kSparse>(p, s0, threadIdx.x == 0 && rank == 0))
@@ -290,19 +475,24 @@ mla_decode_kernel(const __grid_constant__ MlaParams p) {
         tc::tmem_alloc(tmem_slot, kTmemCols);
         tc::tmem_relinquish();
     }
+    MlaRange *range = reinterpret_cast<MlaRange *>(smem + Smem::range);
+    if (p.balanced && warp == 0) {
+        // The cluster's range, from the lengths (both CTAs find the same);
+        // the first CTA also marks the rows without tiles for the reduce.
+        const MlaRange r = mla_balanced_range(p, lane, blockIdx.x == 0);
+        if (lane == 0) *range = r;
+    }
     tc::fence_before_sync();
     __syncthreads();
     cluster_sync();  // both CTAs' barriers exist before any remote arrive
     tc::fence_after_sync();
     const uint32_t tmem = *tmem_slot;
     if (p.balanced) {
-        // The plan kernel that precedes this grid wrote the tables.
-        pdl_wait_primary();
-        const int4 cl = __ldcg(p.plan_cluster + (blockIdx.x >> 1));   // {x0, x1, first row, 0}
-        walk.x0 = cl.x;
-        walk.x1 = cl.y;
-        walk.r = cl.z;
-        if (walk.r < p.num_q_rows) walk.nxt = __ldcg(p.plan_rows + walk.r);
+        walk.x0 = range->x0;
+        walk.x1 = range->x1;
+        walk.cum = range->cum;
+        walk.b = range->b;
+        walk.i = range->i;
     }
 
     const int pidx = Roles::producer(warp);
@@ -597,10 +787,12 @@ mla_decode_kernel(const __grid_constant__ MlaParams p) {
         while (w.next(p, sg)) {
             const int ntiles = sg.ntiles;
             const int start = sg.start, end = sg.end;
-            if (p.balanced && w.r < p.num_q_rows && w.nxt.x < w.x1) {
-                // The next run is row w.r: bring its Q lines of this CTA into
-                // L2 now, so the refill after this run reads them from there.
-                const uint16_t *qr = p.q + (size_t(w.r) * kMlaHeads + h) * kMlaDimQK;
+            const int next_row = p.balanced ? w.peek_row(p) : -1;
+            if (next_row >= 0) {
+                // The next run is likely that row: bring its Q lines of this
+                // CTA into L2 now, so the refill after this run reads them
+                // from there.
+                const uint16_t *qr = p.q + (size_t(next_row) * kMlaHeads + h) * kMlaDimQK;
                 const uint8_t *qn = reinterpret_cast<const uint8_t *>(qr + col0);
                 for (int cb = half; cb < kVBoxes; cb += 2)
                     asm volatile("prefetch.global.L2 [%0];" ::"l"(qn + cb * 128));
@@ -973,6 +1165,8 @@ mla_decode_kernel(const __grid_constant__ MlaParams p) {
             if (ntiles > 0) ok = live;
             G += ntiles;
         }
+        // The reduce's entries of the rows whose first tile this cluster holds.
+        if (p.balanced && rank == 0 && warp == 0 && lane == 0) mla_write_slots(p, *range);
         pdl_launch_dependents();
     }
 
@@ -982,130 +1176,6 @@ mla_decode_kernel(const __grid_constant__ MlaParams p) {
     if (warp == Roles::kMmaWarp) {
         tc::fence_after_sync();
         tc::tmem_dealloc(tmem, kTmemCols);
-    }
-}
-
-// Balanced split plan (one CTA, ahead of the decode grid).  Row r of the
-// concatenation has n_r = ceil(visible keys / 64) tiles starting at tile
-// cum_r.  A cluster's time is its tiles plus a fixed cost for every run it
-// opens (the row's Q into TMEM and the pipeline refill, then the epilogue:
-// about kRunCost tiles' worth), so the split deals out a weighted
-// concatenation in which every row with tiles is preceded by kRunCost
-// virtual tiles: row r occupies weighted positions [W_r, W_r + kRunCost +
-// n_r), its real tile x at y(x) = x - cum_r + W_r + kRunCost.  Cluster c of
-// C = min(clusters, T) takes weighted positions [c T' / C, (c+1) T' / C) of
-// the T' in all, i.e. the real tiles from the image of its first position
-// (a position inside a virtual block maps to the row's first tile) up to
-// the next cluster's; a range inside one virtual block is empty.  A cluster
-// whose range meets more rows so gets fewer tiles.
-// Pass 1 counts the tiles (and weighted tiles) sequence by sequence (1024
-// at a time with running totals) and writes each row's entry; pass 2 finds,
-// for each row, the clusters whose range starts in it and the slots of its
-// partials: the cluster holding weighted position y is ((y + 1) C - 1) / T',
-// and cluster c writes row r's partial to slot c + r, so a row's partials
-// are consecutive.
-constexpr int kPlanThreads = 1024;
-constexpr int kRunCost = 8;
-
-// Exclusive scan of v over the block (1024 threads), continuing from carry;
-// carry advances by the block total.
-__device__ __forceinline__ int plan_block_scan(int v, int &carry, int *warp_tot, int lane, int wid) {
-    int incl = v;
-#pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-        const int u = __shfl_up_sync(0xffffffffu, incl, o);
-        if (lane >= o) incl += u;
-    }
-    if (lane == 31) warp_tot[wid] = incl;
-    __syncthreads();
-    if (wid == 0) {
-        int t = warp_tot[lane];
-#pragma unroll
-        for (int o = 1; o < 32; o <<= 1) {
-            const int u = __shfl_up_sync(0xffffffffu, t, o);
-            if (lane >= o) t += u;
-        }
-        warp_tot[lane] = t;
-    }
-    __syncthreads();
-    const int excl = carry + (wid > 0 ? warp_tot[wid - 1] : 0) + incl - v;
-    carry += warp_tot[kPlanThreads / 32 - 1];
-    __syncthreads();   // warp_tot is rewritten by the next scan
-    return excl;
-}
-
-__global__ void __launch_bounds__(kPlanThreads) mla_plan_kernel(const __grid_constant__ MlaParams p) {
-    pdl_launch_dependents();   // the decode CTAs may set up while this runs
-    __shared__ int warp_tot[kPlanThreads / 32];
-    const int tid = threadIdx.x, lane = tid & 31, wid = tid >> 5;
-    const int rows = p.num_q_rows;
-    for (int c = tid; c < p.num_clusters; c += kPlanThreads)
-        p.plan_cluster[c] = make_int4(0, 0, rows, 0);   // no rows unless found below
-    for (int r = tid; r < rows; r += kPlanThreads) {
-        p.plan_rows[r] = make_int4(0, 0, 0, 0);
-        p.plan_slots[r] = make_int2(0, 0);
-    }
-    __syncthreads();
-    const uint32_t cap = uint32_t(p.len_cap);
-    int carry = 0, carry_w = 0;
-    for (int b0 = 0; b0 < p.batch; b0 += kPlanThreads) {
-        const int b = b0 + tid;
-        int n_seq = 0, w_seq = 0, r0 = 0, nr = 0, L = 0;
-        if (b < p.batch) {
-            const uint32_t len_in = p.kv_len[b];
-            if (len_in > cap) atomicOr(p.err, kErrBadLength);
-            L = static_cast<int>(min(len_in, cap));
-            r0 = p.q_row_offsets ? static_cast<int>(p.q_row_offsets[b]) : b;
-            nr = p.q_row_offsets ? static_cast<int>(p.q_row_offsets[b + 1]) - r0 : 1;
-            nr = max(0, min(nr, rows - r0));   // rows outside [0, rows) are not written
-            if (r0 < 0) nr = 0;
-            for (int i = 0; i < nr; ++i) {
-                const int vis = p.causal ? max(0, min(L, L - nr + i + 1)) : L;
-                const int n = (vis + kBN - 1) / kBN;
-                n_seq += n;
-                w_seq += n > 0 ? n + kRunCost : 0;
-            }
-        }
-        int cum = plan_block_scan(n_seq, carry, warp_tot, lane, wid);
-        int cum_w = plan_block_scan(w_seq, carry_w, warp_tot, lane, wid);
-        for (int i = 0; i < nr; ++i) {
-            const int vis = p.causal ? max(0, min(L, L - nr + i + 1)) : L;
-            const int n = (vis + kBN - 1) / kBN;
-            p.plan_rows[r0 + i] = make_int4(cum, n, b, vis);
-            p.plan_slots[r0 + i] = make_int2(cum_w, 0);   // W_r until pass 2
-            cum += n;
-            cum_w += n > 0 ? n + kRunCost : 0;
-        }
-    }
-    __syncthreads();
-    // With fewer tiles than clusters only T clusters take part, so that every
-    // cluster between a row's first and last holds a piece of it (no gaps in
-    // the row's run of slots: a range inside a virtual block lies before the
-    // first of those).  Each field of plan_cluster is written by one thread:
-    // x0, row of cluster c by the row its range starts in, x1 of cluster c - 1
-    // (its successor's x0) by the same thread.
-    const long long T = carry, Tw = carry_w;
-    const long long C = min(static_cast<long long>(p.num_clusters), T);
-    for (int r = tid; r < rows; r += kPlanThreads) {
-        const int4 e = __ldcg(p.plan_rows + r);
-        const long long W = __ldcg(p.plan_slots + r).x;
-        int2 slot = make_int2(0, 0);
-        if (e.y > 0) {
-            const long long wf = W + kRunCost, wl = wf + e.y - 1;   // weighted first / last tile
-            const int cf = static_cast<int>(((wf + 1) * C - 1) / Tw);
-            const int cl = static_cast<int>(((wl + 1) * C - 1) / Tw);
-            slot = make_int2(cf + r, cl - cf + 1);
-            for (long long c = (W * C + Tw - 1) / Tw; c < C && c * Tw / C <= wl; ++c) {
-                const long long y = c * Tw / C;
-                const int x0 = e.x + static_cast<int>(min(max(y - wf, 0LL), static_cast<long long>(e.y)));
-                int *f = reinterpret_cast<int *>(p.plan_cluster + c);
-                f[0] = x0;
-                f[2] = r;
-                if (c > 0) reinterpret_cast<int *>(p.plan_cluster + (c - 1))[1] = x0;
-                if (c == C - 1) f[1] = static_cast<int>(T);
-            }
-        }
-        p.plan_slots[r] = slot;
     }
 }
 
@@ -1120,13 +1190,6 @@ cudaError_t launch_layout(const MlaParams &p, cudaStream_t stream) {
     cfg.blockDim = dim3(Layout<kSparse>::kThreads);
     cfg.dynamicSmemBytes = kSmemBytes;
     cfg.stream = stream;
-    // Balanced split: launched as a dependent of the plan kernel, so the
-    // CTAs set up (barriers, TMEM) while the plan is written.
-    cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-    attr[0].val.programmaticStreamSerializationAllowed = 1;
-    cfg.attrs = attr;
-    cfg.numAttrs = p.balanced ? 1 : 0;
     return cudaLaunchKernelEx(&cfg, mla_decode_kernel<kSparse>, p);
 }
 
@@ -1158,10 +1221,6 @@ cudaError_t launch_mla_decode(const MlaParams &p, cudaStream_t stream) {
     return p.sparse ? launch_layout<true>(p, stream) : launch_layout<false>(p, stream);
 }
 
-cudaError_t launch_mla_plan(const MlaParams &p, cudaStream_t stream) {
-    mla_plan_kernel<<<1, kPlanThreads, 0, stream>>>(p);
-    return cudaGetLastError();
-}
 
 int mla_cluster_slots(int num_sms, bool sparse) {
     return sparse ? cluster_slots<true>(num_sms) : cluster_slots<false>(num_sms);

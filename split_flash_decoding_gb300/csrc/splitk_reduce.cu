@@ -49,6 +49,7 @@ __device__ __forceinline__ int locate_partials(const ReduceParams &p, int row, i
         const int2 e = p.slots[row];
         if (e.y == 1) return -1;   // finished by the decode kernel
         stride_p = p.num_q_heads;
+        if (e.x < 0 || e.y < 0 || e.y > p.num_slots - e.x) return 0;
         widx0 = static_cast<size_t>(e.x) * p.num_q_heads + h;
         return e.y;                // 0: an empty row, written from the sink alone
     }

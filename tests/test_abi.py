@@ -249,7 +249,7 @@ def test_planner_formulas(attn):
     # automatic MLA (one KV head, 512 output channels): keys that need a
     # split at all take the balanced split (P = 0) over one wave of
     # num_sms / 2 two-CTA clusters; fp32 partials for clusters + rows slots,
-    # then the plan tables
+    # then the reduce's per-row table of slots
     align = lambda x: (x + 255) // 256 * 256
     for sms, batch, rows, max_len in ((152, 32, 32, 32768), (152, 1, 1, 131072),
                                       (152, 4, 8, 2048), (16, 8, 8, 9000)):
@@ -257,7 +257,7 @@ def test_planner_formulas(attn):
         slots = sms // 2 + rows
         assert P == 0
         assert ws == (align(slots * 128 * 512 * 4) + 2 * align(slots * 128 * 4) +
-                      align(sms // 2 * 16) + align(rows * 16) + align(rows * 8))
+                      align(rows * 8))
     # a wave of clusters or more with rows of <= ~4096 keys (a sparse top-k
     # span of 2048), or a single tile per row: no split at all
     assert attn.attn_plan_partitions(128, 128, 128, 1, 512, 2048, 0, num_sms=152) == (1, 0)
@@ -267,7 +267,7 @@ def test_planner_formulas(attn):
         P, ws = attn.attn_plan_partitions(3, 5, 128, 1, 512, max_len, attn.ATTN_PARTITIONS_BALANCED,
                                           num_sms=152)
         assert P == 0 and ws == (align(81 * 128 * 512 * 4) + 2 * align(81 * 128 * 4) +
-                                 align(76 * 16) + align(5 * 16) + align(5 * 8))
+                                 align(5 * 8))
     with pytest.raises(attn.AttnError):
         attn.attn_plan_partitions(64, 64, 16, 8, 64, 8192, attn.ATTN_PARTITIONS_BALANCED,
                                   num_sms=152)

@@ -1,5 +1,5 @@
 """Host-side check of the balanced splits' arithmetic.  MLA (first part),
-restated from the plan kernel and the decode kernel's run walk.  Row r has n_r tiles starting
+restated from the decode kernel's range search, run walk and slot table.  Row r has n_r tiles starting
 at cum_r in the concatenation (T tiles in all).  Every row with tiles is
 preceded by RUN_COST virtual tiles in a weighted concatenation (T_w
 positions): row r occupies [W_r, W_r + RUN_COST + n_r), its real tile x sits
@@ -212,3 +212,59 @@ def test_gqa_unit_cost_zero_is_the_equal_tile_split():
         cum, T, Tw, C, ranges = gqa_plan(n_seq, hkv, grid, 0)
         for c in range(C):
             assert ranges[c] == (c * T // C, (c + 1) * T // C)
+
+
+def decode_range(tiles, clusters, c, run_cost=RUN_COST, lanes=32):
+    """The decode grid's own search for cluster c's range, restated: lane l
+    sums the tiles and weighted tiles of its chunk of rows, a scan gives the
+    chunk starts, and the lane whose weighted chunk holds the cluster's
+    first (next cluster's first) position walks its rows to the real tile."""
+    rows = len(tiles)
+    per = (rows + lanes - 1) // lanes
+    chunks = [range(min(l * per, rows), min(l * per + per, rows)) for l in range(lanes)]
+    tl = [sum(tiles[r] for r in ch) for ch in chunks]
+    wl = [sum(tiles[r] + run_cost for r in ch if tiles[r] > 0) for ch in chunks]
+    T, Tw = sum(tl), sum(wl)
+    C = min(clusters, T)
+    if c >= C:
+        return None
+
+    def locate(y):
+        cum0, w0 = 0, 0
+        for l in range(lanes):
+            if w0 <= y < w0 + wl[l]:
+                cum, W = cum0, w0
+                for r in chunks[l]:
+                    n = tiles[r]
+                    if n > 0 and y < W + run_cost + n:
+                        return r, cum + min(max(y - W - run_cost, 0), n)
+                    cum += n
+                    W += n + run_cost if n > 0 else 0
+            cum0 += tl[l]
+            w0 += wl[l]
+        raise AssertionError("position outside every chunk")
+
+    r0, x0 = locate(c * Tw // C)
+    x1 = T if c + 1 == C else locate((c + 1) * Tw // C)[1]
+    return x0, x1, r0
+
+
+def test_decode_grid_finds_the_plans_ranges():
+    rng = random.Random(31)
+    for it in range(1500):
+        rows = rng.randint(1, 90)
+        clusters = rng.randint(1, 80)
+        run_cost = RUN_COST if it % 3 else rng.choice([0, 2, 11])
+        tiles = [rng.choice([0, 1, 2, 5, rng.randint(0, 300)]) for _ in range(rows)]
+        cum, total, wtotal, C, ranges, _ = plan(tiles, clusters, run_cost)
+        for c in range(clusters):
+            got = decode_range(tiles, clusters, c, run_cost)
+            if c >= C:
+                assert got is None
+                continue
+            x0, x1, r0 = got
+            assert (x0, x1) == ranges[c][:2]
+            # the walk from row r0 finds the same runs as from the plan's row
+            mine = list(ranges)
+            mine[c] = (x0, x1, r0)
+            assert walk(cum, tiles, mine, c) == walk(cum, tiles, ranges, c)

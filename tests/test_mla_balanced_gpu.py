@@ -166,9 +166,10 @@ def test_balanced_repeated_calls_reuse_workspace(attn):
 
 @pytest.mark.parametrize("rows_per_seq", [1, 2])
 def test_balanced_plan_over_many_sequences(attn, rows_per_seq):
-    """More sequences than the plan kernel's 1024 threads: the tile counts
-    are scanned in chunks with a running total.  Forced balanced split
-    (the planner would not split rows this short)."""
+    """More sequences than the 32 lanes of the warp that finds a cluster's
+    range: each lane sums a chunk of sequences before the warp scan, and
+    the lane holding a range end walks its chunk's rows.  Forced balanced
+    split (the planner would not split rows this short)."""
     rng = random.Random(90 + rows_per_seq)
     batch = 1500 if rows_per_seq == 1 else 1100
     lens = [rng.choice([0, 1, 64, 65]) if rng.random() < 0.2 else rng.randint(1, 300)
@@ -202,8 +203,8 @@ def test_bad_page_sets_error_bit_and_context_survives(attn):
 
 def test_graph_capture_replays_with_new_lengths(attn):
     """The balanced split is planned on the device from kv_len, so one
-    captured call (plan kernel, decode, reduce) serves any lengths up to the
-    planned maximum: replayed with other lengths, including an empty row."""
+    captured call (decode, reduce) serves any lengths up to the planned
+    maximum: replayed with other lengths, including an empty row."""
     lens = [3000, 64, 1500, 700]
     w = mla_workload(lens, seed=90)
     P, ws_bytes = attn.attn_plan_partitions(4, 4, 128, 1, 512, 3000, 0)

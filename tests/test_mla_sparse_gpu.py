@@ -152,7 +152,7 @@ def test_sparse_bad_index_and_length_set_error_bits(attn):
     indices_stride (or below 0) is clamped and sets bit 2."""
     w = sparse_workload([500, 600], topk=256, seed=38)
     rows = w.k_cache.shape[0] * w.k_cache.shape[1]
-    BAL = attn.ATTN_PARTITIONS_BALANCED   # the plan kernel checks the counts there
+    BAL = attn.ATTN_PARTITIONS_BALANCED   # the first cluster checks the counts there
     for P1, P2 in ((1, 2), (BAL, BAL)):
         bad = w.indices.clone()
         bad[1, 5] = rows
