@@ -153,6 +153,9 @@ struct Tail {
     static constexpr int items = bars + 256;
 };
 
+// The balanced split's GqaRange sits after the barriers and the TMEM slot.
+constexpr int kRangeOffset = 208;
+
 enum Bar {
     kKFull = 0, kKEmpty = 3, kVFull = 6, kVEmpty = 9,   // [3] each
     kQFull = 12, kQEmpty = 14,                          // [2] each
@@ -161,6 +164,8 @@ enum Bar {
     kMrgFull = 22,                                      // [2] clusters: partials in place
     kNumBars = 24
 };
+static_assert(kNumBars * 8 + 4 <= kRangeOffset && kRangeOffset + int(sizeof(GqaRange)) <= 256,
+              "barriers, TMEM slot and range fit the 256-byte tail");
 
 // Dynamic shared memory: the item table (one int per sequence) only without
 // clusters.
@@ -175,9 +180,10 @@ size_t tc_smem_bytes(int batch) {
 // clusters of C: units (sequence, KV head) j = cluster, cluster + clusters,
 // ..., this CTA taking the slice of its rank.
 template <int C>
-__device__ __forceinline__ GqaWalk make_walk(const GqaParams &p, const int *cum, int hkv) {
+__device__ __forceinline__ GqaWalk make_walk(const GqaParams &p, const int *cum, int hkv,
+                                             const GqaRange &rg) {
     GqaWalk w;
-    if (C == 1 && p.balanced) return gqa_balanced_walk(p, cum, hkv);
+    if (C == 1 && p.balanced) return gqa_balanced_walk(rg);
     w.first = C > 1 ? int(blockIdx.x) / C : int(blockIdx.x);
     w.stride = C > 1 ? int(gridDim.x) / C : int(gridDim.x);
     w.count = C > 1 ? p.batch * hkv : cum[p.batch];
@@ -347,7 +353,8 @@ gqa_decode_tc_kernel(const __grid_constant__ GqaParams p) {
     const int lane = threadIdx.x & 31;
     const int hkv = p.num_q_heads / G;
 
-    if (C == 1 && warp == 0) gqa_build_items(p, hkv, cum, lane);
+    GqaRange *range = reinterpret_cast<GqaRange *>(smem + Tail<C>::bars + kRangeOffset);
+    if (C == 1 && warp == 0) gqa_build_items(p, hkv, cum, lane, range);
     if (threadIdx.x == 32) {
         for (int i = 0; i < kNumBars; ++i) {
             const bool per_warp = (i == kSFree || i == kSFree + 1 || i == kPFull);
@@ -370,7 +377,7 @@ gqa_decode_tc_kernel(const __grid_constant__ GqaParams p) {
     if constexpr (C > 1) cluster_sync();   // every CTA's barriers exist before a remote arrive
     tc::fence_after_sync();
     const uint32_t tmem = *tmem_slot;
-    const GqaWalk walk = make_walk<C>(p, cum, hkv);
+    const GqaWalk walk = make_walk<C>(p, cum, hkv, *range);
 
     if (warp == kWarpK) {
         produce<true, C>(p, cum, walk, hkv, smem, bar, lane);

@@ -51,52 +51,25 @@ __device__ __forceinline__ int gqa_unit_of(const int *cum, int batch, int hkv, l
     return lo * hkv + static_cast<int>((x - cum[lo]) / per_head);
 }
 
-// Weighted concatenation of the balanced split: unit u (n_u tiles, starting
-// at tile x_u) occupies positions [x_u + kGqaUnitCost u, x_u + kGqaUnitCost
-// (u + 1) + n_u), its virtual tiles first, so real tile x of unit u sits at
-// x + kGqaUnitCost (u + 1).  The real tile a position y < T_w maps to (a
-// position in a virtual block: the unit's first tile).
-__device__ __forceinline__ long long gqa_tile_of_position(const int *cum, int batch, int hkv,
-                                                          long long y) {
-    const long long per_seq = static_cast<long long>(kGqaUnitCost) * hkv;
-    int lo = 0, hi = batch;   // sequence b: cum[b] + per_seq b <= y
-    while (hi - lo > 1) {
-        const int mid = (lo + hi) >> 1;
-        if (cum[mid] + per_seq * mid <= y) lo = mid; else hi = mid;
-    }
-    const long long n = (cum[lo + 1] - cum[lo]) / hkv;   // tiles per unit of sequence lo
-    const long long off = y - (cum[lo] + per_seq * lo);
-    const long long h = off / (n + kGqaUnitCost);
-    const long long o = off - h * (n + kGqaUnitCost) - kGqaUnitCost;
-    return cum[lo] + h * n + min(max(o, 0LL), n);
-}
+// Balanced split: this CTA's tile range [x0, x1), the first of its units
+// and their count, and the totals the slot table needs; found by the warp
+// that builds the item table (gqa_build_items) and read by every role.
+struct GqaRange {
+    int x0, x1, u0, count, tiles, wtiles, ctas;
+};
 
-// Balanced split: this CTA's tile range and units.  CTA c of C' = min(grid,
-// tiles) takes the weighted positions [c T_w / C', (c + 1) T_w / C'), i.e.
-// the real tiles from the image of its first position up to the next
-// CTA's; CTAs past C' take none, and a range inside one virtual block is
-// empty.
-__device__ __forceinline__ GqaWalk gqa_balanced_walk(const GqaParams &p, const int *cum, int hkv) {
+// Balanced split: this CTA's walk from its range.
+__device__ __forceinline__ GqaWalk gqa_balanced_walk(const GqaRange &rg) {
     GqaWalk w;
     w.first = 0;
     w.stride = 1;
-    w.tiles = cum[p.batch];
-    w.wtiles = w.tiles + static_cast<long long>(kGqaUnitCost) * hkv * p.batch;
-    w.ctas = min(static_cast<long long>(gridDim.x), w.tiles);
-    const long long c = blockIdx.x;
-    w.count = 0;
-    w.u0 = 0;
-    w.x0 = w.x1 = 0;
-    if (c < w.ctas) {
-        w.x0 = gqa_tile_of_position(cum, p.batch, hkv, c * w.wtiles / w.ctas);
-        w.x1 = c + 1 == w.ctas
-                   ? w.tiles
-                   : gqa_tile_of_position(cum, p.batch, hkv, (c + 1) * w.wtiles / w.ctas);
-        if (w.x1 > w.x0) {
-            w.u0 = gqa_unit_of(cum, p.batch, hkv, w.x0);
-            w.count = gqa_unit_of(cum, p.batch, hkv, w.x1 - 1) - w.u0 + 1;
-        }
-    }
+    w.count = rg.count;
+    w.x0 = rg.x0;
+    w.x1 = rg.x1;
+    w.u0 = rg.u0;
+    w.tiles = rg.tiles;
+    w.wtiles = rg.wtiles;
+    w.ctas = rg.ctas;
     return w;
 }
 
@@ -122,21 +95,29 @@ __device__ __forceinline__ GqaItem gqa_balanced_item(const GqaParams &p, const i
     return it;
 }
 
-// Build cum[0..batch] with warp `warp_id` (all 32 lanes must call).
-__device__ __forceinline__ void gqa_build_items(const GqaParams &p, int hkv, int *cum, int lane) {
+// Build cum[0..batch] with one warp (all 32 lanes must call): lane l sums
+// the tiles of sequences [l m, (l+1) m), a warp scan gives the chunk starts.
+// Under the balanced split the same warp also finds this CTA's range (into
+// *rg): in the weighted concatenation unit u (n_u tiles from tile x_u)
+// occupies positions [x_u + kGqaUnitCost u, x_u + kGqaUnitCost (u + 1) +
+// n_u), its virtual tiles first; CTA c of C' = min(grid, tiles) takes the
+// positions [c T_w / C', (c + 1) T_w / C'), i.e. the real tiles from the image
+// of its first position (a position in a virtual block maps to the unit's
+// first tile) up to the next CTA's; CTAs past C' take none, and a range
+// inside one virtual block is empty.  The lane whose chunk holds a range end
+// finds its sequence, unit and tile.
+__device__ __forceinline__ void gqa_build_items(const GqaParams &p, int hkv, int *cum, int lane,
+                                                GqaRange *rg) {
     const uint32_t cap = uint32_t(p.num_partitions) * uint32_t(p.chunk);
     const int per_lane = (p.batch + 31) / 32;
-    const int b0 = lane * per_lane;
+    const int b0 = min(lane * per_lane, p.batch), b1 = min(b0 + per_lane, p.batch);
     int local = 0;
-    for (int i = 0; i < per_lane; ++i) {
-        const int b = b0 + i;
-        if (b < p.batch) {
-            const uint32_t len_in = p.kv_len[b];
-            if (len_in > cap && blockIdx.x == 0) atomicOr(p.err, kErrBadLength);
-            const uint32_t L = min(len_in, cap);
-            const int ns = static_cast<int>((L + p.chunk - 1) / p.chunk);
-            local += max(ns, 1) * hkv;
-        }
+    for (int b = b0; b < b1; ++b) {
+        const uint32_t len_in = p.kv_len[b];
+        if (len_in > cap && blockIdx.x == 0) atomicOr(p.err, kErrBadLength);
+        const uint32_t L = min(len_in, cap);
+        const int ns = static_cast<int>((L + p.chunk - 1) / p.chunk);
+        local += max(ns, 1) * hkv;
     }
     int incl = local;  // inclusive warp scan of the per-lane sums
 #pragma unroll
@@ -145,16 +126,71 @@ __device__ __forceinline__ void gqa_build_items(const GqaParams &p, int hkv, int
         if (lane >= o) incl += v;
     }
     int run = incl - local;
-    for (int i = 0; i < per_lane; ++i) {
-        const int b = b0 + i;
-        if (b < p.batch) {
-            cum[b] = run;
-            const uint32_t L = min(p.kv_len[b], cap);
-            const int ns = static_cast<int>((L + p.chunk - 1) / p.chunk);
-            run += max(ns, 1) * hkv;
-        }
+    for (int b = b0; b < b1; ++b) {
+        cum[b] = run;
+        const uint32_t L = min(p.kv_len[b], cap);
+        const int ns = static_cast<int>((L + p.chunk - 1) / p.chunk);
+        run += max(ns, 1) * hkv;
     }
     if (lane == 31) cum[p.batch] = incl;
+    if (!p.balanced) return;
+
+    const long long per_seq = static_cast<long long>(kGqaUnitCost) * hkv;
+    const long long T = __shfl_sync(0xffffffffu, incl, 31);
+    const long long Tw = T + per_seq * p.batch;
+    const long long C = min(static_cast<long long>(gridDim.x), T);
+    const long long c = blockIdx.x;
+    const long long w_lo = (incl - local) + per_seq * b0, w_hi = incl + per_seq * b1;
+    // Real tile of weighted position y: {x, unit, x is the unit's first tile}.
+    auto locate = [&](long long y, int &unit, bool &at_first) -> long long {
+        const bool mine = w_lo <= y && y < w_hi;
+        const int src = __ffs(__ballot_sync(0xffffffffu, mine)) - 1;
+        long long x = 0;
+        int u = 0, f = 0;
+        if (lane == src) {
+            long long xs = incl - local, ws = w_lo;   // the chunk's first tile / position
+            for (int b = b0; b < b1; ++b) {
+                const uint32_t L = min(p.kv_len[b], cap);
+                const long long n = max(static_cast<int>((L + p.chunk - 1) / p.chunk), 1);
+                const long long span = hkv * (n + kGqaUnitCost);
+                if (y < ws + span) {
+                    const long long off = y - ws;
+                    const long long h = off / (n + kGqaUnitCost);
+                    const long long o = off - h * (n + kGqaUnitCost) - kGqaUnitCost;
+                    x = xs + h * n + min(max(o, 0LL), n);
+                    u = b * hkv + static_cast<int>(h);
+                    f = o <= 0;
+                    break;
+                }
+                xs += hkv * n;
+                ws += span;
+            }
+        }
+        unit = __shfl_sync(0xffffffffu, u, src);
+        at_first = __shfl_sync(0xffffffffu, f, src) != 0;
+        return __shfl_sync(0xffffffffu, x, src);
+    };
+    GqaRange r;
+    r.x0 = r.x1 = r.u0 = r.count = 0;
+    r.tiles = static_cast<int>(T);
+    r.wtiles = static_cast<int>(Tw);
+    r.ctas = static_cast<int>(C);
+    if (c < C) {
+        int u0, u1;
+        bool f0, f1;
+        r.x0 = static_cast<int>(locate(c * Tw / C, u0, f0));
+        int u_last;
+        if (c + 1 == C) {
+            r.x1 = static_cast<int>(T);
+            u_last = p.batch * hkv - 1;
+        } else {
+            r.x1 = static_cast<int>(locate((c + 1) * Tw / C, u1, f1));
+            u_last = f1 ? u1 - 1 : u1;   // x1 - 1 lies in the unit before when x1 opens one
+        }
+        r.u0 = u0;
+        r.count = r.x1 > r.x0 ? u_last - u0 + 1 : 0;
+    }
+    if (lane == 0) *rg = r;
 }
 
 template <int kTileKeys>

@@ -268,3 +268,67 @@ def test_decode_grid_finds_the_plans_ranges():
             mine = list(ranges)
             mine[c] = (x0, x1, r0)
             assert walk(cum, tiles, mine, c) == walk(cum, tiles, ranges, c)
+
+
+def gqa_device_range(n_seq, hkv, grid, c, cost=GQA_UNIT_COST, lanes=32):
+    """The GQA kernel's own search for CTA c's range, restated: lane l holds
+    sequences [l m, (l+1) m) and their weighted positions (every sequence
+    has hkv units of n + cost positions); the lane holding a range end walks
+    its sequences to the unit and tile.  Returns (x0, x1, first unit, units)."""
+    batch = len(n_seq)
+    per = (batch + lanes - 1) // lanes
+    T = sum(n * hkv for n in n_seq)
+    Tw = T + cost * hkv * batch
+    C = min(grid, T)
+    if c >= C:
+        return 0, 0, 0, 0
+
+    def locate(y):
+        xs, ws = 0, 0
+        for l in range(lanes):
+            seqs = range(min(l * per, batch), min(l * per + per, batch))
+            w_lo = ws
+            w_hi = ws + sum(hkv * (n_seq[b] + cost) for b in seqs)
+            if w_lo <= y < w_hi:
+                for b in seqs:
+                    n = n_seq[b]
+                    span = hkv * (n + cost)
+                    if y < ws + span:
+                        off = y - ws
+                        h = off // (n + cost)
+                        o = off - h * (n + cost) - cost
+                        return xs + h * n + min(max(o, 0), n), b * hkv + h, o <= 0
+                    xs += hkv * n
+                    ws += span
+                raise AssertionError("position not in the lane's sequences")
+            xs += sum(hkv * n_seq[b] for b in seqs)
+            ws = w_hi
+        raise AssertionError("position outside every chunk")
+
+    x0, u0, _ = locate(c * Tw // C)
+    if c + 1 == C:
+        x1, u_last = T, batch * hkv - 1
+    else:
+        x1, u1, f1 = locate((c + 1) * Tw // C)
+        u_last = u1 - 1 if f1 else u1
+    return x0, x1, u0, (u_last - u0 + 1 if x1 > x0 else 0)
+
+
+def test_gqa_kernel_search_matches_the_split():
+    rng = random.Random(77)
+    for it in range(1500):
+        batch = rng.randint(1, 80)
+        hkv = rng.choice([1, 2, 8])
+        grid = rng.randint(1, 160)
+        cost = GQA_UNIT_COST if it % 3 else rng.choice([0, 1, 4])
+        n_seq = [max(1, rng.choice([1, 2, rng.randint(1, 60)])) for _ in range(batch)]
+        cum, T, Tw, C, ranges = gqa_plan(n_seq, hkv, grid, cost)
+        ux = [cum[b] + h * n_seq[b] for b in range(batch) for h in range(hkv)]
+        for c in range(grid):
+            x0, x1, u0, count = gqa_device_range(n_seq, hkv, grid, c, cost)
+            assert (x0, x1) == ranges[c]
+            met = [u for u in range(batch * hkv)
+                   if max(x0, ux[u]) < min(x1, ux[u] + n_seq[u // hkv])]
+            assert count == len(met)
+            if met:
+                assert u0 == met[0] and met == list(range(u0, u0 + count))
