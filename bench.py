@@ -402,26 +402,30 @@ def run_ours(args, rank, world, dist):
     out = torch.empty((w.rows, w.num_q_heads, w.dim_v), dtype=torch.bfloat16, device=dev)
     lse = torch.empty((w.rows, w.num_q_heads), dtype=torch.float32, device=dev)
 
+    # The binding plans again from its num_partitions; 0 there is its own
+    # automatic choice, so the balanced MLA split goes in as its request.
+    Pc = attn.ATTN_PARTITIONS_BALANCED if (w.is_mla and P == 0) else P
+
     def call(q=w.q, kv_len=w.kv_len, page_table=w.page_table, o=out, l=lse, indices=w.indices,
              offs=w.q_row_offsets):
         if sparse:
             attn.attn_mla_decode_sparse(q, w.k_cache, indices, kv_len, scale=w.scale,
-                                        dim_v=w.dim_v, sink=w.sink, num_partitions=P,
+                                        dim_v=w.dim_v, sink=w.sink, num_partitions=Pc,
                                         workspace=ws, out=o, lse=l, stream=stream)
         elif w.is_mla and offs is not None:
             attn.attn_mla_decode_rows(q, w.k_cache, kv_len, offs, scale=w.scale,
                                       max_kv_len=w.max_kv_len, causal=w.causal, dim_v=w.dim_v,
-                                      page_table=page_table, sink=w.sink, num_partitions=P,
+                                      page_table=page_table, sink=w.sink, num_partitions=Pc,
                                       workspace=ws, out=o, lse=l, stream=stream)
         elif w.is_mla:
             attn.attn_mla_decode(q, w.k_cache, kv_len, scale=w.scale, max_kv_len=w.max_kv_len,
                                  dim_v=w.dim_v, page_table=page_table, sink=w.sink,
-                                 num_partitions=P, workspace=ws, out=o, lse=l, stream=stream)
+                                 num_partitions=Pc, workspace=ws, out=o, lse=l, stream=stream)
         else:
             attn.attn_decode(q, w.k_cache, w.v_cache, kv_len, group=w.group, scale=w.scale,
                              max_kv_len=w.max_kv_len, page_table=page_table, sink=w.sink,
                              q_row_offsets=offs, max_q_len=w.max_q_len,
-                             causal=w.causal, num_partitions=P, workspace=ws, out=o, lse=l,
+                             causal=w.causal, num_partitions=Pc, workspace=ws, out=o, lse=l,
                              stream=stream)
 
     # one kernel for P = 1, the tile kernels (one Q tile or the pair) and
