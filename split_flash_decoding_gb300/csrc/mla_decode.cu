@@ -8,11 +8,11 @@
 //
 // Work: clusters of two CTAs.  Fixed split (num_partitions P >= 1): one
 // cluster per (key slice p, query row).  Balanced split (P = 0): one wave of
-// clusters, cluster c taking an equal contiguous range of the concatenated
-// 64-key tiles of all query rows, walked as runs of consecutive tiles of one
-// row (written by a one-CTA plan kernel that runs first); a run that is a
-// whole row writes the output, a run cut by a range end writes a partial
-// that the split-K reduce merges.  The 128 heads are the MMA's M dimension.
+// clusters, cluster c taking a contiguous range of equal cost (tiles plus a
+// fixed cost per row it opens) of the concatenated 64-key tiles of all query
+// rows, found by the cluster from the lengths and walked as runs of
+// consecutive tiles of one row; a run that is a whole row writes the output,
+// a run cut by a range end writes a partial that the split-K reduce merges.  The 128 heads are the MMA's M dimension.
 // The two CTAs of a cluster split the 576 channels evenly:
 //
 //   rank 0 loads channels [0, 256)   (its half of V) + rope [512, 544),
@@ -203,7 +203,7 @@ __device__ __forceinline__ bool fixed_slice(const MlaParams &p, MlaSeg &s, bool 
     return true;
 }
 
-// Balanced split (plan kernel and decode grid alike): a cluster's time is
+// Balanced split: a cluster's time is
 // its tiles plus a fixed cost for every run it opens (the row's Q into TMEM
 // and the pipeline refill, then the epilogue: about kRunCost tiles' worth),
 // so the split deals out a weighted concatenation in which every row with
