@@ -566,10 +566,8 @@ gqa_decode_tc_kernel(const __grid_constant__ GqaParams p) {
             }
 
             // ---- item epilogue ----------------------------------------------------
-            if (ok && it.ntiles > 0) {
-                ok = mbar_wait(&bar[kODone], (g + it.ntiles - 1) & 1, p.err);
-                tc::fence_after_sync();
-            }
+            // The row sums first: they do not need O, so their exchange runs
+            // while the last P.V is still in flight.
             float lsum[NW], lrsum[NW];
             {
                 float *lb = lred + (iter & 1) * 128;   // [4 key warps][2][16 columns]
@@ -589,6 +587,10 @@ gqa_decode_tc_kernel(const __grid_constant__ GqaParams p) {
                     lsum[c] = (lb[cg] + lb[32 + cg]) + (lb[64 + cg] + lb[96 + cg]);
                     lrsum[c] = (lb[16 + cg] + lb[48 + cg]) + (lb[80 + cg] + lb[112 + cg]);
                 }
+            }
+            if (ok && it.ntiles > 0) {
+                ok = mbar_wait(&bar[kODone], (g + it.ntiles - 1) & 1, p.err);
+                tc::fence_after_sync();
             }
             float o[NW];
             if (ok && it.ntiles > 0) {

@@ -1080,13 +1080,8 @@ mla_decode_kernel(const __grid_constant__ MlaParams p) {
             }
 
             // ---- run epilogue ---------------------------------------------------
-            if (live) {
-                live = __all_sync(0xffffffffu,
-                                  mbar_wait(&bar[kODone], (G + ntiles - 1) & 1, p.err));
-                tc::fence_after_sync();
-            }
             // Row sums of the two halves (same m_ref), one after the other
-            // through the row-max buffer.
+            // through the row-max buffer, while the last P.V is in flight.
             named_sync(kBarPair + (warp & 3), 64);
             red[half * 128 + h] = l;
             named_sync(kBarPair + (warp & 3), 64);
@@ -1096,6 +1091,11 @@ mla_decode_kernel(const __grid_constant__ MlaParams p) {
             named_sync(kBarPair + (warp & 3), 64);
             l_r += red[(half ^ 1) * 128 + h];
             l += l_other;
+            if (live) {
+                live = __all_sync(0xffffffffu,
+                                  mbar_wait(&bar[kODone], (G + ntiles - 1) & 1, p.err));
+                tc::fence_after_sync();
+            }
             // O was accumulated with the rounded weights: normalise it by their
             // sum (direct), or rescale it to the fp32 sum l kept for the merge.
             float scale_o = 0.f, Mf = -INFINITY, Z = 0.f;

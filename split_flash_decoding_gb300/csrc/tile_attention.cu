@@ -394,12 +394,9 @@ tile_attention_kernel(const __grid_constant__ TileParams p) {
         }
 
         // ---- epilogue ---------------------------------------------------------
-        if (ok && ntiles > 0) {
-            ok = __all_sync(0xffffffffu, mbar_wait(&bar[kODone], (ntiles - 1) & 1, p.err));
-            tc::fence_after_sync();
-        }
         // Row sums of the two halves (same m_ref), through the Q buffer, which
-        // no MMA reads any more.
+        // no MMA reads any more (the last score MMA was done when its S was
+        // read), while the last P.V is still in flight.
         float *sums = reinterpret_cast<float *>(smem + Smem::q);
         named_sync(kBarPair + (warp & 3), 64);
         sums[half * 256 + r] = l;
@@ -407,6 +404,10 @@ tile_attention_kernel(const __grid_constant__ TileParams p) {
         named_sync(kBarPair + (warp & 3), 64);
         l += sums[(half ^ 1) * 256 + r];
         l_r += sums[(half ^ 1) * 256 + 128 + r];
+        if (ok && ntiles > 0) {
+            ok = __all_sync(0xffffffffu, mbar_wait(&bar[kODone], (ntiles - 1) & 1, p.err));
+            tc::fence_after_sync();
+        }
         const int h = kvh * G + (r % G);
         const float t2 = p.sink ? p.sink[h] * kLog2e : -INFINITY;
         const float Mf = fmaxf(m_ref, t2);
