@@ -318,8 +318,8 @@ int plan_impl(int num_sms, int batch, int num_q_rows, int max_q_len, int num_q_h
     if (requested == 0 && gqa_tc && gqa_units <= 8LL * num_sms &&
         max_kv_len > kGqaTcTileKeys) {
         // Up to eight (sequence, KV head) units per SM: every unit's 128-key
-        // tiles, concatenated, are dealt out in equal contiguous ranges, one
-        // per SM, so ragged lengths cannot leave SMs idle and only the units a
+        // tiles, concatenated, are dealt out in contiguous ranges of equal
+        // cost, one per SM, so ragged lengths cannot leave SMs idle and only the units a
         // range end cuts leave partials for the reduce (measured faster than
         // the slice plans at 16 to 64 sequences of Llama-3-8B shapes, single
         // or a few rows).  The workspace grows by ~8 KB per unit, so larger
